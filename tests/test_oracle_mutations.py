@@ -1,0 +1,104 @@
+"""Plant plausible mistakes in the oracle (on the CPU, one at a time) and check
+that the pins catch each one: evidence that the pins constrain every step."""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import draft, philox, sampling, schedule, tv, verify
+import tests.test_oracle_draft as T_draft
+import tests.test_oracle_schedule as T_sched
+import tests.test_oracle_tv as T_tv
+import tests.test_oracle_verify as T_verify
+
+
+def _fails(fn):
+    try:
+        fn()
+    except AssertionError:
+        return True
+    return False
+
+
+def test_gumbel_sign_slip_is_caught(monkeypatch):
+    monkeypatch.setattr(philox, "gumbel", lambda u: np.log(-np.log(np.asarray(u, np.float64))))
+    assert _fails(T_draft.test_two_level_gumbel_matches_softmax)
+
+
+def test_block_level_dropped_is_caught(monkeypatch):
+    # choosing the block by its max logit instead of its logsumexp
+    orig = sampling.logsumexp
+    monkeypatch.setattr(sampling, "logsumexp", lambda x, axis=-1: np.max(x, axis=axis))
+    assert _fails(T_draft.test_two_level_gumbel_matches_softmax)
+    monkeypatch.setattr(sampling, "logsumexp", orig)
+
+
+def test_transposed_bias_is_caught(monkeypatch):
+    def bad(W1, W2, prev):
+        E = np.asarray(W2, np.float64)[np.asarray(prev)]
+        return E @ np.asarray(W1, np.float64).T
+    monkeypatch.setattr(draft, "markov_bias", bad)
+    assert _fails(T_draft.test_markov_bias_orientation)
+    assert _fails(T_draft.test_chain_uses_previous_token)
+
+
+def test_anchor_instead_of_previous_token_is_caught(monkeypatch):
+    orig = draft.draft_block
+
+    def bad(U, h, W1, W2, w, bias, x0, temperature, seed, forced_tokens=None):
+        B, G, _ = np.shape(U)
+        return orig(U, h, W1, W2, w, bias, x0, temperature, seed,
+                    forced_tokens=np.repeat(np.asarray(x0)[:, None], G, axis=1))
+    monkeypatch.setattr(draft, "draft_block", bad)
+    assert _fails(T_draft.test_chain_uses_previous_token)
+    assert _fails(T_draft.test_confidence_markov_part_reads_previous_token)
+
+
+def test_theta_without_per_row_normalisation_is_caught(monkeypatch):
+    from fractions import Fraction
+
+    def bad(a, sps):
+        a = np.asarray(a, np.float32)
+        B, G = a.shape
+        pairs = sorted(((b, j) for b in range(B) for j in range(1, G + 1)),
+                       key=lambda p: (-float(a[p[0], p[1] - 1]), p[0], p[1]))
+        ell, E, N = np.zeros(B, np.int64), Fraction(B), B
+        best = float(E) * sps[N]
+        for b, j in pairs:
+            th = float(E + Fraction(float(a[b, j - 1]))) * sps[N + 1]
+            if th > best:
+                ell[b] += 1
+                E += Fraction(float(a[b, j - 1]))
+                N += 1
+                best = th
+            else:
+                break
+        return ell, N, best
+    monkeypatch.setattr(schedule, "schedule_prefix", bad)
+    assert _fails(T_sched.test_greedy_stop_is_global_optimum_for_rational_sps)
+
+
+def test_non_strict_comparison_is_caught(monkeypatch):
+    src = schedule.schedule_prefix
+
+    def bad(a, sps):
+        a = np.asarray(a, np.float32)
+        eps_sps = np.asarray(sps, np.float64) * (1 + 1e-15)
+        eps_sps[:a.shape[0] + 1] = np.asarray(sps)[:a.shape[0] + 1]
+        return src(a, eps_sps)
+    monkeypatch.setattr(schedule, "schedule_prefix", bad)
+    assert _fails(T_sched.test_equal_theta_stops_the_scan)
+
+
+def test_resampling_from_target_on_reject_is_caught(monkeypatch):
+    # a classic slip: on a rejection draw from p_t instead of max(0, p_t - p_d)
+    import oracle.verify as V
+    monkeypatch.setattr(V, "draft_logits",
+                        lambda U, W1, W2, x0, tokens, b, k: np.full((len(b), np.shape(U)[-1]), -np.inf))
+    assert _fails(T_verify.test_first_emitted_token_follows_target)
+
+
+def test_tv_missing_half_is_caught(monkeypatch):
+    monkeypatch.setattr(tv, "accept_rate_tv",
+                        lambda d, t: 1.0 - np.sum(np.abs(tv.softmax(d) - tv.softmax(t)), axis=-1))
+    assert _fails(T_tv.test_disjoint_supports_give_zero)
+    assert _fails(T_tv.test_two_point_closed_form)
