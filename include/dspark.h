@@ -1,0 +1,186 @@
+/*
+ * dspark.h -- C ABI of the DSpark draft / schedule / verify / accept-rate path
+ * for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * Four operations, each a hand-written CUDA kernel sequence:
+ *   dspark_draft_block      semi-autoregressive draft block, confidence, survival
+ *   dspark_schedule_prefix  hardware-aware prefix scheduler (Algorithm 1)
+ *   dspark_verify           rejection-sampling verification + residual/bonus token
+ *   dspark_accept_rate_tv   c* = 1 - 1/2 ||softmax(d) - softmax(t)||_1 per row
+ *
+ * Sources (cited per call): the DeepSpec / DSpark walkthrough at
+ * wangjunjian.com ("DSpark" post, sections 2.1, 3.2, 3.3, 8.2) and the
+ * Qwen3.8-27B-DSpark model-card explainer at dpshk.com (AcceptRatePredictor,
+ * config.json fields).
+ *
+ * Conventions shared by every call
+ *   - Every pointer is a DEVICE pointer owned by the caller, except where a
+ *     comment says "host".  The library allocates nothing and frees nothing on
+ *     these calls; it caches only device properties and kernel attributes.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  The return value reports host-side argument checks
+ *     and launch errors only.
+ *   - Device-side status: the first 16 bytes of `workspace` hold a status
+ *     block {uint32 code, uint32 detail, ...}; the call clears it, and a
+ *     kernel that meets a device-side error (an out-of-range token id, a
+ *     bounded wait that ran out) writes a nonzero dspark_status_t there and
+ *     skips the affected work.  Read it after the stream completes, e.g. with
+ *     dspark_workspace_status().
+ *   - Layouts are row-major with the vocabulary dimension contiguous.  Float
+ *     tensors of one call share one dtype (dspark_dtype_t).  bf16 rows need
+ *     V % 8 == 0 and f32 rows V % 4 == 0 (16-byte aligned rows); every tensor
+ *     base pointer must be 16-byte aligned and workspace 256-byte aligned.
+ *   - Positions k are 1-based as on the pages: U[b][k-1] is the base logit
+ *     row of draft position k; t_logits[b][k-1] is the target row that
+ *     verifies position k, and t_logits[b][gamma] the bonus row.
+ *   - Random draws use Philox4x32-10 (Salmon et al., SC'11) keyed by
+ *     (seed_lo, seed_hi) with counter (index >> 2, k, b, stream), output word
+ *     index & 3.  Streams: 0 draft token, 1 accept uniform, 2 residual token,
+ *     3 draft block, 4 residual block, 5 target token, 6 target block.
+ *   - Sampling from a softmax uses an exact two-level Gumbel-max over blocks
+ *     of DSPARK_SAMPLE_BLOCK consecutive vocabulary indices: pick the block by
+ *     argmax(logsumexp(block) + Gumbel), then the token inside it by
+ *     argmax(logit + Gumbel); ties go to the lowest index.  This draws token v
+ *     with probability exactly softmax(.)_v.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSPARK_SAMPLE_BLOCK 64
+#define DSPARK_MAX_GAMMA 32
+
+typedef enum {
+    DSPARK_OK = 0,
+    DSPARK_ERR_INVALID_ARGUMENT = 1,   /* a host-side check failed; nothing was launched */
+    DSPARK_ERR_UNSUPPORTED = 2,        /* valid but outside what the kernels handle */
+    DSPARK_ERR_WORKSPACE_TOO_SMALL = 3,
+    DSPARK_ERR_CUDA = 4,               /* a CUDA runtime call or launch failed */
+    DSPARK_ERR_TIMEOUT = 5,            /* device status only: a bounded wait ran out */
+    DSPARK_ERR_DEVICE_CHECK = 6        /* device status only: a device-side input check failed */
+} dspark_status_t;
+
+typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype_t;
+
+typedef struct CUstream_st* dspark_stream_t;   /* same type as cudaStream_t */
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* dspark_status_string(dspark_status_t s);
+
+/* Synchronises `stream`, then returns the device status code stored at the
+ * head of `workspace` by the last call that used it (DSPARK_OK if none).
+ * Returns DSPARK_ERR_CUDA if the synchronisation or the copy fails. */
+dspark_status_t dspark_workspace_status(const void* workspace, dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Draft block.  DeepSpec walkthrough section 3.2 (stage two): for k = 1..gamma
+ *   z_k = U_k + B(x_{k-1}),  B(x_{k-1}, v) = sum_j W2[v][j] * W1[x_{k-1}][j]
+ * (VanillaMarkovHead, paper eq. 5, rank r), x_k ~ softmax(z_k / T) -- the
+ * `sample_block_tokens` loop, x_0 = anchor.  Section 3.3 confidence head:
+ *   c_k = sigmoid(sum_i w[i] h[b][k-1][i] + sum_j w[H+j] W1[x_{k-1}][j] + bias)
+ * (model card: one nn.Linear(H + r, 1) returning a logit), and the Algorithm 1
+ * survival a_k = a_{k-1} * c_k in float32, a_0 = 1.
+ *
+ *   U [B][gamma][V], h [B][gamma][H], W1 [V][r], W2 [V][r], w [H + r] in `dt`;
+ *   x0 [B] int32 anchors in [0, V).
+ *   temperature > 0 samples; temperature == 0 takes argmax z_k (lowest index
+ *   on ties) and writes lse_d = logp_d = 0.
+ *   Outputs [B][gamma]: x (int32 tokens), lse_d = logsumexp(z_k / T),
+ *   logp_d = z_k[x_k] / T - lse_d, c, a (float32).
+ * Requires 1 <= B <= 65535, 1 <= gamma <= DSPARK_MAX_GAMMA, r % 8 == 0 and
+ * r <= 256.  bf16 inputs with r % 64 == 0 run the bias on tensor cores.
+ * An anchor or token id outside [0, V) sets DSPARK_ERR_DEVICE_CHECK in the
+ * workspace status and is read as 0.
+ * ------------------------------------------------------------------------ */
+size_t dspark_draft_block_workspace_size(int B, int gamma, int V, int r);
+
+dspark_status_t dspark_draft_block(int B, int gamma, int V, int H, int r, dspark_dtype_t dt,
+                                   const void* U, const void* h, const void* W1, const void* W2,
+                                   const void* w, float bias, const int32_t* x0,
+                                   float temperature, uint64_t seed,
+                                   int32_t* x, float* lse_d, float* logp_d, float* c, float* a,
+                                   void* workspace, size_t workspace_bytes, dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Prefix scheduler, Algorithm 1 (DeepSpec walkthrough section 3.3 flowchart):
+ * sort all (b, j) pairs by a[b][j-1] descending (ties: lower b, then lower
+ * j), scan them starting from l_b = 0 for all b, and accept a pair while
+ *   Theta = (E / N) * sps[N] > Theta_best
+ * with N = sum_b (l_b + 1) verified rows (the bonus row included) and
+ * E = sum_b (1 + sum_{j <= l_b} a[b][j-1]) expected emitted tokens; stop at the
+ * first pair that does not raise Theta.  E is the exact sum of the float32
+ * survivals rounded once to double; Theta is one IEEE double division and one
+ * multiplication, so the result is bit-reproducible.
+ *
+ *   a [B][gamma] float32 survivals, each in [0, 1] and non-increasing in j
+ *     (as dspark_draft_block writes them);
+ *   sps [B*(gamma+1) + 1] double, sps[N] the verification throughput at N rows;
+ *   outputs: ell [B] int32 (l*_b in 0..gamma), n_sched [1] int32 (N),
+ *   theta [1] double (Theta_best).
+ * Requires B * gamma <= 16384.  A value of a outside [0, 1] sets
+ * DSPARK_ERR_DEVICE_CHECK in the workspace status.
+ * ------------------------------------------------------------------------ */
+size_t dspark_schedule_prefix_workspace_size(int B, int gamma);
+
+dspark_status_t dspark_schedule_prefix(int B, int gamma, const float* a, const double* sps,
+                                       int32_t* ell, int32_t* n_sched, double* theta,
+                                       void* workspace, size_t workspace_bytes,
+                                       dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Verification (DeepSpec walkthrough section 8.2, verify_draft_tokens): for
+ * k = 1..ell[b], accept x_k iff u < min(1, p_t(x_k) / p_d(x_k)) with
+ *   p_t = softmax(t_logits[b][k-1] / T),  log p_d(x_k) = logp_d[b][k-1],
+ *   u = (Philox word >> 8) * 2^-24, stream 1, counter (0, k, b, 1);
+ * stop at the first rejection and draw next_token from norm(max(0, p_t - p_d))
+ * at that position, where p_d(v) = exp(z_k(v) / T - lse_d[b][k-1]) and z_k is
+ * rebuilt from U, W1, W2 and x_{k-1} exactly as the draft built it; if that
+ * residual has no mass, draw from p_t.  If all ell[b] are accepted, draw the
+ * bonus token from p_t of row ell[b] + 1 (section 2.1: one extra token per
+ * round).  temperature == 0: accept iff x_k == argmax t_k, next_token =
+ * argmax t at the stop row.
+ *
+ *   t_logits [B][gamma+1][V], U [B][gamma][V], W1/W2 [V][r] in `dt`;
+ *   x0 [B], x [B][gamma] int32; lse_d, logp_d [B][gamma] float32 (from the
+ *   draft); ell [B] int32 in 0..gamma.
+ *   Outputs: n_accept [B] int32 in 0..ell[b]; next_token [B] int32.  The
+ *   request emits x[b][0 .. n_accept-1] followed by next_token[b].
+ * Only target rows 1..ell[b]+1 of each request are read.
+ * ------------------------------------------------------------------------ */
+size_t dspark_verify_workspace_size(int B, int gamma, int V, int r);
+
+dspark_status_t dspark_verify(int B, int gamma, int V, int r, dspark_dtype_t dt,
+                              const void* t_logits, const void* U, const void* W1, const void* W2,
+                              const int32_t* x0, const int32_t* x, const float* lse_d,
+                              const float* logp_d, const int32_t* ell, float temperature,
+                              uint64_t seed, int32_t* n_accept, int32_t* next_token,
+                              void* workspace, size_t workspace_bytes, dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Analytic accept rate, paper eq. 8 (DeepSpec walkthrough section 3.3 and the
+ * `_compute_accept_rate_3d` snippet): for each row
+ *   c_star[row] = 1 - 1/2 sum_v |softmax(d[row])_v - softmax(t[row])_v|
+ * over the full vocabulary, no temperature.  Computed as
+ * sum_v min(p_d(v), p_t(v)), which is the same quantity.
+ *
+ *   d, t [rows][V] in `dt`; c_star [rows] float32.  Each row needs at least
+ *   one finite logit.  rows == 0 launches nothing.  Requires V <= 163840.
+ * ------------------------------------------------------------------------ */
+size_t dspark_accept_rate_tv_workspace_size(int64_t rows, int V);
+
+dspark_status_t dspark_accept_rate_tv(int64_t rows, int V, dspark_dtype_t dt,
+                                      const void* d, const void* t, float* c_star,
+                                      void* workspace, size_t workspace_bytes,
+                                      dspark_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */

@@ -37,12 +37,14 @@ def confidence(w, bias, h_k, W1_prev):
     return 1.0 / (1.0 + np.exp(-logit))
 
 
-def draft_block(U, h, W1, W2, w, bias, x0, temperature, seed, forced_tokens=None):
+def draft_block(U, h, W1, W2, w, bias, x0, temperature, seed, forced_tokens=None, requests=None):
     """One draft block for B requests.
 
     U[B, gamma, V], h[B, gamma, H], W1/W2[V, r], w[H + r], x0[B].
     forced_tokens[B, gamma] (optional): use these as x_k when building step k+1
     (teacher forcing), so each position can be checked on its own.
+    requests[B] (optional): the request index b that keys each row's random
+    draws (default 0..B-1), so a sample of rows can be checked on its own.
     Returns a dict of x, lse_d, logp_d, c, a [B, gamma] and margin [B, gamma].
     """
     U = np.asarray(U, dtype=np.float64)
@@ -56,13 +58,14 @@ def draft_block(U, h, W1, W2, w, bias, x0, temperature, seed, forced_tokens=None
     prev = np.asarray(x0, dtype=np.int64).copy()
     surv = np.ones(B)
     req = np.arange(B)
+    keys = req if requests is None else np.asarray(requests, dtype=np.int64)
     T = float(temperature)
     for k in range(1, gamma + 1):
         z = U[:, k - 1, :] + markov_bias(W1, W2, prev)
         if T > 0.0:
             l = z / T
             L = logsumexp(l, axis=-1)
-            tok, mar = two_level_gumbel(l, seed, req, k, philox.STREAM_DRAFT_BLOCK,
+            tok, mar = two_level_gumbel(l, seed, keys, k, philox.STREAM_DRAFT_BLOCK,
                                         philox.STREAM_DRAFT_TOKEN)
             lse_d[:, k - 1] = L
             logp_d[:, k - 1] = l[req, tok] - L

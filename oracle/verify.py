@@ -23,13 +23,15 @@ from .sampling import two_level_gumbel, greedy, logsumexp
 from .draft import draft_logits
 
 
-def verify(t_logits, U, W1, W2, x0, x, lse_d, logp_d, ell, temperature, seed):
+def verify(t_logits, U, W1, W2, x0, x, lse_d, logp_d, ell, temperature, seed, requests=None):
     """Return dict(n_accept[B], next_token[B], margin[B]).
 
     t_logits[B, gamma+1, V], U[B, gamma, V], W1/W2[V, r], x0[B], x[B, gamma],
     lse_d/logp_d[B, gamma], ell[B] in 0..gamma.  margin[b] is the smallest
     decision margin of request b: |u - ratio| of each acceptance test taken
     and the margin of the final draw (greedy: top-2 logit gaps).
+    requests[B] (optional): the request index b that keys each row's random
+    draws (default 0..B-1).
     """
     t_logits = np.asarray(t_logits, dtype=np.float64)
     B, gp1, V = t_logits.shape
@@ -39,6 +41,7 @@ def verify(t_logits, U, W1, W2, x0, x, lse_d, logp_d, ell, temperature, seed):
     lse_d = np.asarray(lse_d, dtype=np.float64)
     logp_d = np.asarray(logp_d, dtype=np.float64)
     req = np.arange(B)
+    keys = req if requests is None else np.asarray(requests, dtype=np.int64)
     T = float(temperature)
     n_accept = np.zeros(B, np.int64)
     next_token = np.full(B, -1, np.int64)
@@ -55,7 +58,7 @@ def verify(t_logits, U, W1, W2, x0, x, lse_d, logp_d, ell, temperature, seed):
             Lt = logsumexp(trow / T, axis=-1)
             log_pt = trow[np.arange(len(rows)), x[rows, k - 1]] / T - Lt
             ratio = np.exp(log_pt - logp_d[rows, k - 1])
-            u = philox.uniform_accept(philox.draw_words(seed, rows, k, philox.STREAM_ACCEPT, 0))
+            u = philox.uniform_accept(philox.draw_words(seed, keys[rows], k, philox.STREAM_ACCEPT, 0))
             ok = u < ratio
             margin[rows] = np.minimum(margin[rows], np.abs(u - ratio))
         else:
@@ -91,7 +94,7 @@ def verify(t_logits, U, W1, W2, x0, x, lse_d, logp_d, ell, temperature, seed):
                 logq = np.where(q > 0.0, np.log(q), -np.inf)
             if np.any(has_mass):
                 r = res_rows[has_mass]
-                tok, mar = two_level_gumbel(logq[has_mass], seed, r, k,
+                tok, mar = two_level_gumbel(logq[has_mass], seed, keys[r], k,
                                             philox.STREAM_RESIDUAL_BLOCK,
                                             philox.STREAM_RESIDUAL_TOKEN)
                 next_token[r] = tok
@@ -99,7 +102,7 @@ def verify(t_logits, U, W1, W2, x0, x, lse_d, logp_d, ell, temperature, seed):
             fallback = res_rows[~has_mass]
         from_target = np.concatenate([bonus_rows, fallback])
         if len(from_target):
-            tok, mar = two_level_gumbel(t_logits[from_target, k - 1, :] / T, seed, from_target, k,
+            tok, mar = two_level_gumbel(t_logits[from_target, k - 1, :] / T, seed, keys[from_target], k,
                                         philox.STREAM_TARGET_BLOCK, philox.STREAM_TARGET_TOKEN)
             next_token[from_target] = tok
             margin[from_target] = np.minimum(margin[from_target], mar)

@@ -1,0 +1,236 @@
+"""ctypes binding of libdspark.so: argument marshalling only.
+
+Every function here has the name of the C entry point it calls and takes torch
+tensors on the GPU; it checks shapes and dtypes, passes data pointers and the
+current CUDA stream, and raises DSparkError on a non-OK status.  All compute
+runs in the library's CUDA kernels -- there is no fallback of any kind: if the
+library is missing, every call raises.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libdspark.so")
+
+DSPARK_OK = 0
+DSPARK_F32 = 0
+DSPARK_BF16 = 1
+SAMPLE_BLOCK = 64
+MAX_GAMMA = 32
+
+_c_int, _c_i64, _c_u64, _c_size, _c_float = (ctypes.c_int, ctypes.c_int64, ctypes.c_uint64,
+                                            ctypes.c_size_t, ctypes.c_float)
+_p = ctypes.c_void_p
+
+_SIGNATURES = {
+    "dspark_status_string": (ctypes.c_char_p, [_c_int]),
+    "dspark_workspace_status": (_c_int, [_p, _p]),
+    "dspark_draft_block_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "dspark_draft_block": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _p, _p, _p, _p, _p,
+                                    _c_float, _p, _c_float, _c_u64, _p, _p, _p, _p, _p, _p, _c_size, _p]),
+    "dspark_schedule_prefix_workspace_size": (_c_size, [_c_int, _c_int]),
+    "dspark_schedule_prefix": (_c_int, [_c_int, _c_int, _p, _p, _p, _p, _p, _p, _c_size, _p]),
+    "dspark_verify_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "dspark_verify": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _p, _p, _p, _p, _p, _p, _p, _p, _p,
+                               _c_float, _c_u64, _p, _p, _p, _c_size, _p]),
+    "dspark_accept_rate_tv_workspace_size": (_c_size, [_c_i64, _c_int]),
+    "dspark_accept_rate_tv": (_c_int, [_c_i64, _c_int, _c_int, _p, _p, _p, _p, _c_size, _p]),
+    "dspark_debug_draft_logits": (_c_int, [_c_int, _c_int, _c_int, _p, _p, _p, _p, _p, _p, _c_size, _p]),
+}
+
+_lib = None
+
+
+class DSparkError(RuntimeError):
+    def __init__(self, name, status):
+        self.status = status
+        super().__init__(f"{name} failed: {status_string(status) if _lib else status}")
+
+
+def load():
+    """Load libdspark.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def exported_symbols():
+    return sorted(_SIGNATURES)
+
+
+def status_string(status):
+    return load().dspark_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(*ts):
+    dts = {t.dtype for t in ts}
+    if len(dts) != 1:
+        raise TypeError(f"float inputs must share one dtype, got {dts}")
+    dt = dts.pop()
+    if dt == torch.bfloat16:
+        return DSPARK_BF16
+    if dt == torch.float32:
+        return DSPARK_F32
+    raise TypeError(f"unsupported dtype {dt}")
+
+
+def _check(name, status):
+    if status != DSPARK_OK:
+        raise DSparkError(name, status)
+
+
+def _need(t, shape, dtype=None, name="tensor"):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _workspace(nbytes, device, workspace):
+    if workspace is None:
+        return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError("workspace too small")
+    return workspace
+
+
+def _nbytes(t):
+    return t.numel() * t.element_size()
+
+
+def workspace_status(workspace, stream=None):
+    """Device status code left at the head of `workspace` (synchronises)."""
+    return load().dspark_workspace_status(_ptr(workspace), _stream(stream))
+
+
+# ----------------------------------------------------------------- calls ---
+def dspark_accept_rate_tv(d, t, c_star=None, workspace=None, stream=None):
+    """c*[row] = 1 - 1/2 ||softmax(d[row]) - softmax(t[row])||_1 (float32 [rows])."""
+    lib = load()
+    rows, V = d.shape
+    _need(d, (rows, V), name="d")
+    _need(t, (rows, V), d.dtype, name="t")
+    dt = _dtype_code(d, t)
+    if c_star is None:
+        c_star = torch.empty(rows, dtype=torch.float32, device=d.device)
+    _need(c_star, (rows,), torch.float32, name="c_star")
+    ws = _workspace(lib.dspark_accept_rate_tv_workspace_size(rows, V), d.device, workspace)
+    _check("dspark_accept_rate_tv",
+           lib.dspark_accept_rate_tv(rows, V, dt, _ptr(d), _ptr(t), _ptr(c_star), _ptr(ws), _nbytes(ws),
+                                     _stream(stream)))
+    return c_star
+
+
+def dspark_draft_block(U, h, W1, W2, w, bias, x0, temperature, seed, out=None, workspace=None,
+                       stream=None):
+    """Draft block; returns dict x, lse_d, logp_d, c, a (each [B, gamma])."""
+    lib = load()
+    B, G, V = U.shape
+    H = h.shape[-1]
+    r = W1.shape[-1]
+    _need(U, (B, G, V), name="U")
+    _need(h, (B, G, H), U.dtype, name="h")
+    _need(W1, (V, r), U.dtype, name="W1")
+    _need(W2, (V, r), U.dtype, name="W2")
+    _need(w, (H + r,), U.dtype, name="w")
+    _need(x0, (B,), torch.int32, name="x0")
+    dt = _dtype_code(U, h, W1, W2, w)
+    dev = U.device
+    if out is None:
+        out = dict(x=torch.empty((B, G), dtype=torch.int32, device=dev),
+                   **{k: torch.empty((B, G), dtype=torch.float32, device=dev)
+                      for k in ("lse_d", "logp_d", "c", "a")})
+    ws = _workspace(lib.dspark_draft_block_workspace_size(B, G, V, r), dev, workspace)
+    _check("dspark_draft_block",
+           lib.dspark_draft_block(B, G, V, H, r, dt, _ptr(U), _ptr(h), _ptr(W1), _ptr(W2), _ptr(w),
+                                  float(bias), _ptr(x0), float(temperature), int(seed) & (2**64 - 1),
+                                  _ptr(out["x"]), _ptr(out["lse_d"]), _ptr(out["logp_d"]),
+                                  _ptr(out["c"]), _ptr(out["a"]), _ptr(ws), _nbytes(ws), _stream(stream)))
+    return out
+
+
+def dspark_schedule_prefix(a, sps, out=None, workspace=None, stream=None):
+    """Algorithm 1; returns dict ell [B] int32, n_sched [1] int32, theta [1] float64."""
+    lib = load()
+    B, G = a.shape
+    _need(a, (B, G), torch.float32, name="a")
+    _need(sps, (B * (G + 1) + 1,), torch.float64, name="sps")
+    dev = a.device
+    if out is None:
+        out = dict(ell=torch.empty(B, dtype=torch.int32, device=dev),
+                   n_sched=torch.empty(1, dtype=torch.int32, device=dev),
+                   theta=torch.empty(1, dtype=torch.float64, device=dev))
+    ws = _workspace(lib.dspark_schedule_prefix_workspace_size(B, G), dev, workspace)
+    _check("dspark_schedule_prefix",
+           lib.dspark_schedule_prefix(B, G, _ptr(a), _ptr(sps), _ptr(out["ell"]), _ptr(out["n_sched"]),
+                                      _ptr(out["theta"]), _ptr(ws), _nbytes(ws), _stream(stream)))
+    return out
+
+
+def dspark_verify(t_logits, U, W1, W2, x0, x, lse_d, logp_d, ell, temperature, seed, out=None,
+                  workspace=None, stream=None):
+    """Verification; returns dict n_accept [B], next_token [B] (int32)."""
+    lib = load()
+    B, G, V = U.shape
+    r = W1.shape[-1]
+    _need(t_logits, (B, G + 1, V), U.dtype, name="t_logits")
+    _need(U, (B, G, V), name="U")
+    _need(W1, (V, r), U.dtype, name="W1")
+    _need(W2, (V, r), U.dtype, name="W2")
+    _need(x0, (B,), torch.int32, name="x0")
+    _need(x, (B, G), torch.int32, name="x")
+    _need(lse_d, (B, G), torch.float32, name="lse_d")
+    _need(logp_d, (B, G), torch.float32, name="logp_d")
+    _need(ell, (B,), torch.int32, name="ell")
+    dt = _dtype_code(t_logits, U, W1, W2)
+    dev = U.device
+    if out is None:
+        out = dict(n_accept=torch.empty(B, dtype=torch.int32, device=dev),
+                   next_token=torch.empty(B, dtype=torch.int32, device=dev))
+    ws = _workspace(lib.dspark_verify_workspace_size(B, G, V, r), dev, workspace)
+    _check("dspark_verify",
+           lib.dspark_verify(B, G, V, r, dt, _ptr(t_logits), _ptr(U), _ptr(W1), _ptr(W2), _ptr(x0),
+                             _ptr(x), _ptr(lse_d), _ptr(logp_d), _ptr(ell), float(temperature),
+                             int(seed) & (2**64 - 1), _ptr(out["n_accept"]), _ptr(out["next_token"]),
+                             _ptr(ws), _nbytes(ws), _stream(stream)))
+    return out
+
+
+def dspark_debug_draft_logits(U_k, W1, W2, prev, z=None, workspace=None, stream=None):
+    """Test hook: z = U_k + W2 . W1[prev] through the tensor-core draft path."""
+    lib = load()
+    B, V = U_k.shape
+    r = W1.shape[-1]
+    _need(W1, (V, r), U_k.dtype, name="W1")
+    _need(W2, (V, r), U_k.dtype, name="W2")
+    _need(prev, (B,), torch.int32, name="prev")
+    if z is None:
+        z = torch.empty((B, V), dtype=torch.float32, device=U_k.device)
+    ws = _workspace(lib.dspark_draft_block_workspace_size(B, 1, V, r), U_k.device, workspace)
+    _check("dspark_debug_draft_logits",
+           lib.dspark_debug_draft_logits(B, V, r, _ptr(U_k), _ptr(W1), _ptr(W2), _ptr(prev), _ptr(z), _ptr(ws),
+                                         _nbytes(ws), _stream(stream)))
+    return z, ws

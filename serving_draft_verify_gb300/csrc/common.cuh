@@ -1,0 +1,172 @@
+// Shared device helpers for the DSpark kernels (sm_103a): status block,
+// bounded mbarrier waits, bulk copies, Philox4x32-10 and the uniform /
+// Gumbel draws, and small reductions.  Inline PTX is used where CUDA C++ has
+// no spelling for the instruction.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/dspark.h"
+
+namespace dspark {
+
+// ---------------------------------------------------------------- status ---
+// Workspace head: {code, detail, pad, pad}.  Written only on error.
+struct StatusBlock {
+    uint32_t code;
+    uint32_t detail;
+    uint32_t pad[2];
+};
+constexpr size_t kStatusBytes = 256;   // keeps what follows 256-byte aligned
+
+__device__ __forceinline__ void set_status(StatusBlock* st, uint32_t code, uint32_t detail) {
+    if (st != nullptr && atomicCAS(&st->code, 0u, code) == 0u) st->detail = detail;
+}
+
+// A bounded wait gives up after this many nanoseconds of %globaltimer.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// -------------------------------------------------------------- mbarrier ---
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Waits for phase `parity` of `bar`; returns false if kWaitLimitNs passed first.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// ------------------------------------------------------------ bulk copy ---
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// ---------------------------------------------------------------- Philox ---
+// Philox4x32-10 (Salmon et al., SC'11): per round, 32x32->64 products of
+// c0 and c2 with the two round multipliers, the high halves xored into the
+// other words with the round key, key bumped by the Weyl constants.
+struct U4 {
+    uint32_t x, y, z, w;
+};
+__device__ __forceinline__ U4 philox4x32_10(U4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int i = 0; i < 10; ++i) {
+        const uint32_t lo0 = 0xD2511F53u * c.x;
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo1 = 0xCD9E8D57u * c.z;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = U4{hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0};
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+enum Stream : uint32_t {
+    kStreamDraftToken = 0,
+    kStreamAccept = 1,
+    kStreamResidualToken = 2,
+    kStreamDraftBlock = 3,
+    kStreamResidualBlock = 4,
+    kStreamTargetToken = 5,
+    kStreamTargetBlock = 6,
+};
+// The 32-bit word keyed by (seed, request b, position k, stream, index).
+__device__ __forceinline__ uint32_t draw_word(uint64_t seed, uint32_t b, uint32_t k, uint32_t stream,
+                                              uint32_t index) {
+    const U4 r = philox4x32_10(U4{index >> 2, k, b, stream}, static_cast<uint32_t>(seed),
+                               static_cast<uint32_t>(seed >> 32));
+    const uint32_t sel = index & 3u;
+    return sel == 0 ? r.x : sel == 1 ? r.y : sel == 2 ? r.z : r.w;
+}
+// u in (0, 1): ((w >> 9) + 1/2) * 2^-23 (exact in float32).
+__device__ __forceinline__ float uniform_open(uint32_t w) {
+    return (static_cast<float>(w >> 9) + 0.5f) * 1.1920928955078125e-07f;
+}
+// u in [0, 1): (w >> 8) * 2^-24 (exact in float32).
+__device__ __forceinline__ float uniform_accept(uint32_t w) {
+    return static_cast<float>(w >> 8) * 5.9604644775390625e-08f;
+}
+// Standard Gumbel variate -ln(-ln u).  For u near 1, -ln u is formed as
+// -log1p(u - 1) (u - 1 is exact there) to keep its relative accuracy.
+__device__ __forceinline__ float gumbel_of(float u) {
+    const float e = (u > 0.5f) ? -log1pf(u - 1.0f) : -logf(u);
+    return -logf(e);
+}
+
+// ------------------------------------------------------------ reductions ---
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// bf16 pair (packed in a 32-bit word) -> two floats, exactly.
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994531f;
+
+}  // namespace dspark

@@ -1,0 +1,62 @@
+// Host-side helpers shared by the C-ABI entry points: argument checks,
+// per-device caches, launch error mapping.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/dspark.h"
+
+namespace dspark {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Current device and its SM count (cached per device).
+inline int current_device() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    return dev;
+}
+inline int sm_count(int dev) {
+    static int cache[64] = {0};
+    if (dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// Launch-error check mapped to a status.
+inline dspark_status_t launch_status() {
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+// Clears the status block at the head of a workspace (async on `stream`).
+inline dspark_status_t clear_status(void* workspace, cudaStream_t stream) {
+    return cudaMemsetAsync(workspace, 0, 16, stream) == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+// Once-per-device flag for one-time kernel attribute setup.
+struct OncePerDevice {
+    std::mutex mu;
+    bool done[64] = {false};
+    template <class F>
+    cudaError_t run(int dev, F&& f) {
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        std::lock_guard<std::mutex> lock(mu);
+        if (done[dev]) return cudaSuccess;
+        const cudaError_t e = f();
+        if (e == cudaSuccess) done[dev] = true;
+        return e;
+    }
+};
+
+}  // namespace dspark

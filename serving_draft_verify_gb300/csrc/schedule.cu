@@ -1,0 +1,283 @@
+// dspark_schedule_prefix: the hardware-aware prefix scheduler, Algorithm 1
+// (DeepSpec walkthrough, section 3.3 flowchart): sort all (b, j) pairs by the
+// survival a_{b,j} descending, scan them greedily while
+// Theta = (E / N) * SPS(N) rises, stop at the first pair that does not raise it.
+//
+// One CTA of 1024 threads, everything in shared memory (B * gamma <= 16384):
+//   1. keys k = ~bits(a) (ascending k = descending a), values = pair index
+//      b * gamma + j - 1, padded with k = ~0 to a multiple of 1024;
+//   2. stable LSD radix sort, four 8-bit passes; within a warp, equal digits
+//      are ranked with __match_any_sync, so ties keep (b, j) order;
+//   3. exact prefix sums of a * 2^149 (each float32 a in [0, 1] is an integer
+//      below 2^150 at that scale) in 192-bit integers, plus B * 2^149;
+//   4. E_n = the prefix rounded once to double (round-to-nearest-even),
+//      Theta_n = (E_n / (B + n)) * sps[B + n] with IEEE double ops;
+//   5. n* = (first n with !(Theta_n > Theta_{n-1})) - 1, block-wide min;
+//   6. l*_b = number of pairs of request b among the first n* sorted pairs.
+#include "common.cuh"
+#include "host_common.h"
+
+namespace dspark {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxPairs = 16384;
+constexpr int kPerThread = kMaxPairs / kThreads;   // 16
+
+struct U192 {
+    unsigned long long w0, w1, w2;   // little-endian limbs
+};
+__device__ __forceinline__ U192 add192(U192 a, U192 b) {
+    U192 r;
+    r.w0 = a.w0 + b.w0;
+    unsigned long long c = r.w0 < a.w0;
+    const unsigned long long t1 = a.w1 + b.w1;
+    const unsigned long long c1 = t1 < a.w1;
+    r.w1 = t1 + c;
+    c = c1 | (r.w1 < t1);
+    r.w2 = a.w2 + b.w2 + c;
+    return r;
+}
+__device__ __forceinline__ U192 shfl_up192(U192 v, int d) {
+    return U192{__shfl_up_sync(0xffffffffu, v.w0, d), __shfl_up_sync(0xffffffffu, v.w1, d),
+                __shfl_up_sync(0xffffffffu, v.w2, d)};
+}
+// a * 2^149 for a float32 a in [0, 1] (bits already validated).
+__device__ __forceinline__ U192 scaled_survival(uint32_t bits) {
+    const uint32_t e = (bits >> 23) & 0xFFu, m = bits & 0x7FFFFFu;
+    const unsigned long long mant = (e == 0) ? m : (m | 0x800000u);
+    const int sh = (e == 0) ? 0 : static_cast<int>(e) - 1;     // 0..126
+    U192 r{0, 0, 0};
+    if (sh < 64) {
+        r.w0 = mant << sh;
+        r.w1 = sh ? (mant >> (64 - sh)) : 0;
+    } else if (sh < 128) {
+        r.w1 = mant << (sh - 64);
+        r.w2 = (sh > 64) ? (mant >> (128 - sh)) : 0;
+    } else {
+        r.w2 = mant << (sh - 128);
+    }
+    return r;
+}
+// round(v) to double (nearest, ties to even), times 2^-149.  v > 0 here.
+__device__ __forceinline__ double u192_to_double_scaled(U192 v) {
+    int hb;   // index of the highest set bit
+    if (v.w2) hb = 191 - __clzll(v.w2);
+    else if (v.w1) hb = 127 - __clzll(v.w1);
+    else if (v.w0) hb = 63 - __clzll(v.w0);
+    else return 0.0;
+    // left-justify so that bit hb lands on bit 191
+    const int sh = 191 - hb, q = sh >> 6, r = sh & 63;
+    unsigned long long a0 = v.w0, a1 = v.w1, a2 = v.w2;
+    if (q == 1) { a2 = a1; a1 = a0; a0 = 0; }
+    else if (q == 2) { a2 = a0; a1 = 0; a0 = 0; }
+    if (r) {
+        a2 = (a2 << r) | (a1 >> (64 - r));
+        a1 = (a1 << r) | (a0 >> (64 - r));
+        a0 <<= r;
+    }
+    unsigned long long mant = a2 >> 11;                 // 53 bits, top bit set
+    const bool round = (a2 >> 10) & 1ull;
+    const bool sticky = (a2 & 0x3FFull) != 0 || a1 != 0 || a0 != 0;
+    if (round && (sticky || (mant & 1ull))) mant += 1;   // 2^53 is still exact
+    return scalbn(static_cast<double>(mant), hb - 52 - 149);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+schedule_kernel(const float* __restrict__ a, const double* __restrict__ sps, int B, int gamma,
+                int32_t* __restrict__ ell, int32_t* __restrict__ n_sched, double* __restrict__ theta,
+                StatusBlock* status) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint32_t* key[2] = {reinterpret_cast<uint32_t*>(smem), reinterpret_cast<uint32_t*>(smem) + kMaxPairs};
+    uint16_t* val[2] = {reinterpret_cast<uint16_t*>(smem + 2 * kMaxPairs * 4),
+                        reinterpret_cast<uint16_t*>(smem + 2 * kMaxPairs * 4) + kMaxPairs};
+    uint16_t* hist = reinterpret_cast<uint16_t*>(smem + 2 * kMaxPairs * 6);   // [256][kWarps]
+    __shared__ unsigned long long wsum[3 * kWarps];
+    __shared__ int red_min[kWarps];
+    __shared__ uint32_t bad_seen;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n = B * gamma;
+    const int R = (n + kThreads - 1) / kThreads;      // rounds per warp chunk
+    const int npad = R * kThreads;
+    if (tid == 0) bad_seen = 0;
+    __syncthreads();
+
+    // 1. keys in pair order; validate a in [0, 1]
+    for (int i = tid; i < npad; i += kThreads) {
+        uint32_t k = 0xFFFFFFFFu;
+        if (i < n) {
+            const float v = a[i];
+            uint32_t bits = __float_as_uint(v);
+            if (!(v >= 0.f && v <= 1.f)) {
+                bits = 0;
+                atomicOr(&bad_seen, 1u);
+            }
+            if (bits == 0x80000000u) bits = 0;      // -0 counts as +0
+            k = ~bits;
+        }
+        key[0][i] = k;
+        val[0][i] = static_cast<uint16_t>(i < n ? i : 0xFFFF);
+    }
+    __syncthreads();
+    if (tid == 0 && bad_seen) set_status(status, DSPARK_ERR_DEVICE_CHECK, 1);
+
+    // 2. stable LSD radix sort: warp w owns elements [w R 32, (w+1) R 32) in order
+    int src = 0;
+    for (int shift = 0; shift < 32; shift += 8) {
+        for (int i = tid; i < 256 * kWarps; i += kThreads) hist[i] = 0;
+        __syncthreads();
+        const int base = warp * R * 32;
+        for (int rd = 0; rd < R; ++rd) {
+            const int e = base + rd * 32 + lane;
+            const uint32_t dg = (key[src][e] >> shift) & 0xFFu;
+            const uint32_t peers = __match_any_sync(0xffffffffu, dg);
+            if (lane == __ffs(peers) - 1) hist[dg * kWarps + warp] += __popc(peers);
+            __syncwarp();
+        }
+        __syncthreads();
+        // exclusive scan of hist in digit-major order (8192 entries, 8 per thread)
+        {
+            unsigned s = 0;
+            uint16_t loc[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) { loc[q] = hist[tid * 8 + q]; s += loc[q]; }
+            unsigned inc = s;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned y = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += y;
+            }
+            if (lane == 31) red_min[warp] = static_cast<int>(inc);
+            __syncthreads();
+            unsigned wpre = 0;
+            for (int q = 0; q < warp; ++q) wpre += static_cast<unsigned>(red_min[q]);
+            unsigned run = wpre + inc - s;
+            __syncthreads();
+#pragma unroll
+            for (int q = 0; q < 8; ++q) { hist[tid * 8 + q] = static_cast<uint16_t>(run); run += loc[q]; }
+        }
+        __syncthreads();
+        for (int rd = 0; rd < R; ++rd) {
+            const int e = base + rd * 32 + lane;
+            const uint32_t k = key[src][e];
+            const uint16_t v = val[src][e];
+            const uint32_t dg = (k >> shift) & 0xFFu;
+            const uint32_t peers = __match_any_sync(0xffffffffu, dg);
+            const int rank = __popc(peers & ((1u << lane) - 1u));
+            const int pos = hist[dg * kWarps + warp] + rank;
+            key[src ^ 1][pos] = k;
+            val[src ^ 1][pos] = v;
+            __syncwarp();
+            if (lane == __ffs(peers) - 1) hist[dg * kWarps + warp] += __popc(peers);
+            __syncwarp();
+        }
+        __syncthreads();
+        src ^= 1;
+    }
+    const uint32_t* skey = key[src];
+    const uint16_t* sval = val[src];
+
+    // 3. exact prefix sums: thread t owns sorted positions [16 t, 16 t + 16)
+    U192 tot{0, 0, 0};
+#pragma unroll
+    for (int q = 0; q < kPerThread; ++q) {
+        const int p = tid * kPerThread + q;
+        if (p < n) tot = add192(tot, scaled_survival(~skey[p]));
+    }
+    U192 inc = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const U192 y = shfl_up192(inc, o);
+        if (lane >= o) inc = add192(inc, y);
+    }
+    if (lane == 31) { wsum[3 * warp] = inc.w0; wsum[3 * warp + 1] = inc.w1; wsum[3 * warp + 2] = inc.w2; }
+    __syncthreads();
+    U192 excl{0, 0, static_cast<unsigned long long>(B) << 21};   // B * 2^149
+    for (int q = 0; q < warp; ++q) excl = add192(excl, U192{wsum[3 * q], wsum[3 * q + 1], wsum[3 * q + 2]});
+    {
+        const U192 y = shfl_up192(inc, 1);
+        if (lane >= 1) excl = add192(excl, y);
+    }
+
+    // 4-5. Theta along the scan and the first position that does not raise it
+    auto theta_at = [&](int m, U192 E) -> double {    // m pairs taken; E = their scaled sum + B
+        const double Ed = u192_to_double_scaled(E);
+        const int N = B + m;
+        return __dmul_rn(__ddiv_rn(Ed, static_cast<double>(N)), sps[N]);
+    };
+    int first_fail = 0x7FFFFFFF;
+    if (tid * kPerThread < n) {
+        double prev = theta_at(tid * kPerThread, excl);
+        U192 run = excl;
+        for (int q = 0; q < kPerThread; ++q) {
+            const int m = tid * kPerThread + q + 1;
+            if (m > n) break;
+            run = add192(run, scaled_survival(~skey[m - 1]));
+            const double th = theta_at(m, run);
+            if (!(th > prev)) { first_fail = m; break; }
+            prev = th;
+        }
+    }
+    int fmin = first_fail;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) fmin = min(fmin, __shfl_xor_sync(0xffffffffu, fmin, o));
+    __syncthreads();
+    if (lane == 0) red_min[warp] = fmin;
+    __syncthreads();
+    int nfail = 0x7FFFFFFF;
+    for (int q = 0; q < kWarps; ++q) nfail = min(nfail, red_min[q]);
+    const int nstar = (nfail == 0x7FFFFFFF) ? n : nfail - 1;
+
+    // 6. per-request counts among the first n* sorted pairs (reuse key[src ^ 1])
+    int* cnt = reinterpret_cast<int*>(key[src ^ 1]);
+    for (int b = tid; b < B; b += kThreads) cnt[b] = 0;
+    __syncthreads();
+    for (int p = tid; p < nstar; p += kThreads) atomicAdd(&cnt[sval[p] / gamma], 1);
+    __syncthreads();
+    for (int b = tid; b < B; b += kThreads) ell[b] = cnt[b];
+    // the thread owning position n* reports Theta_{n*} (thread 0 for n* = 0)
+    const int owner = (nstar == 0) ? 0 : (nstar - 1) / kPerThread;
+    if (tid == owner) {
+        U192 E = excl;
+        for (int p = tid * kPerThread; p < nstar; ++p) E = add192(E, scaled_survival(~skey[p]));
+        *theta = theta_at(nstar, E);
+        *n_sched = B + nstar;
+    }
+}
+
+constexpr size_t kSmem = 2 * kMaxPairs * 4 + 2 * kMaxPairs * 2 + 256 * kWarps * 2;
+
+}  // namespace
+}  // namespace dspark
+
+using namespace dspark;
+
+extern "C" size_t dspark_schedule_prefix_workspace_size(int B, int gamma) {
+    (void)B;
+    (void)gamma;
+    return kStatusBytes;
+}
+
+extern "C" dspark_status_t dspark_schedule_prefix(int B, int gamma, const float* a, const double* sps,
+                                                  int32_t* ell, int32_t* n_sched, double* theta,
+                                                  void* workspace, size_t workspace_bytes,
+                                                  dspark_stream_t stream) {
+    if (B <= 0 || gamma <= 0 || gamma > DSPARK_MAX_GAMMA) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (static_cast<long long>(B) * gamma > kMaxPairs) return DSPARK_ERR_UNSUPPORTED;
+    if (!a || !sps || !ell || !n_sched || !theta) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (workspace == nullptr || !aligned256(workspace)) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (workspace_bytes < dspark_schedule_prefix_workspace_size(B, gamma)) return DSPARK_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    static OncePerDevice once;
+    if (once.run(current_device(), [] {
+            return cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(kSmem));
+        }) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+    if (clear_status(workspace, s) != DSPARK_OK) return DSPARK_ERR_CUDA;
+    schedule_kernel<<<1, kThreads, kSmem, s>>>(a, sps, B, gamma, ell, n_sched, theta,
+                                                 static_cast<StatusBlock*>(workspace));
+    return launch_status();
+}

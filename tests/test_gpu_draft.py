@@ -1,0 +1,152 @@
+"""GPU parity of dspark_draft_block against the oracle.
+
+Integer outputs (tokens) must match exactly except decisions whose oracle
+margin (top-2 gap of block keys or of perturbed logits; greedy: of logits)
+is below 1e-4; those are counted and reported.  The oracle is run teacher-
+forced on the GPU's tokens so every position is checked on its own.
+Float outputs: |err| <= 2e-3 for bf16 inputs and 1e-5 for fp32 (c, a); the
+same bars hold for lse_d / logp_d.  The tensor-core bias itself is checked
+against a float64 matmul at 1e-5 relative.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from serving_draft_verify_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+MARGIN = 1e-4
+FTOL = {"bf16": 2e-3, "f32": 1e-5}
+
+
+@pytest.fixture(scope="module")
+def dsv():
+    import serving_draft_verify_gb300 as m
+    m.load()
+    return m
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+def gpu_draft(dsv, inp, temperature=None, seed=None):
+    dev = torch.device("cuda")
+    T = inp["temperature"] if temperature is None else temperature
+    s = inp["seed"] if seed is None else seed
+    B, G, V = inp["U"].shape
+    ws = torch.empty(dsv.load().dspark_draft_block_workspace_size(B, G, V, inp["W1"].shape[1]),
+                     dtype=torch.uint8, device=dev)
+    out = dsv.dspark_draft_block(inp["U"].to(dev), inp["h"].to(dev), inp["W1"].to(dev), inp["W2"].to(dev),
+                                 inp["w"].to(dev), inp["bias"], inp["x0"].to(dev), T, s, workspace=ws)
+    assert dsv.workspace_status(ws) == 0
+    return {k: _np(v) for k, v in out.items()}
+
+
+def oracle_draft(inp, gpu_x, temperature=None, seed=None, rows=None):
+    """Teacher-forced oracle for the listed requests (all by default), each keyed
+    by its own request index."""
+    rows = np.arange(inp["U"].shape[0]) if rows is None else np.asarray(rows)
+    T = inp["temperature"] if temperature is None else temperature
+    s = inp["seed"] if seed is None else seed
+    idx = torch.from_numpy(rows).to(inp["U"].device)
+    return oracle.draft_block(wl.to_f64(inp["U"][idx]), wl.to_f64(inp["h"][idx]), wl.to_f64(inp["W1"]),
+                              wl.to_f64(inp["W2"]), wl.to_f64(inp["w"]), inp["bias"], _np(inp["x0"])[rows], T, s,
+                              forced_tokens=gpu_x[rows], requests=rows)
+
+
+def compare(gpu, ref, dtype, rows=None):
+    rows = np.arange(gpu["x"].shape[0]) if rows is None else np.asarray(rows)
+    gx = gpu["x"][rows]
+    exempt = ref["margin"] < MARGIN
+    mismatch = (gx != ref["x"]) & ~exempt
+    assert not mismatch.any(), f"{mismatch.sum()} token mismatches at {np.argwhere(mismatch)[:5]}"
+    same = gx == ref["x"]
+    for k in ("c", "a"):
+        err = np.abs(gpu[k][rows] - ref[k]).max()
+        assert err <= FTOL[dtype], (k, err)
+    for k in ("lse_d", "logp_d"):
+        err = np.abs(gpu[k][rows] - ref[k])[same].max(initial=0.0)
+        assert err <= FTOL["bf16"], (k, err)
+    return int(exempt.sum())
+
+
+@pytest.mark.parametrize("B,V,r", [(1, 1024, 64), (20, 5000, 256), (130, 2048, 128), (300, 1000, 192)])
+def test_tensor_core_logits(dsv, B, V, r):
+    """z = U_k + W2 . W1[prev] from the tcgen05 path vs a float64 matmul."""
+    g = torch.Generator().manual_seed(B + V + r)
+    U = (torch.randn((B, V), generator=g) * 2).bfloat16()
+    W1 = (torch.randn((V, r), generator=g) * 0.5).bfloat16()
+    W2 = (torch.randn((V, r), generator=g) * 0.5).bfloat16()
+    prev = torch.randint(0, V, (B,), generator=g).int()
+    z, ws = dsv._binding.dspark_debug_draft_logits(U.cuda(), W1.cuda(), W2.cuda(), prev.cuda())
+    assert dsv.workspace_status(ws) == 0
+    ref = U.double() + W1.double()[prev.long()] @ W2.double().T
+    err = (z.cpu().double() - ref).abs() / (1.0 + ref.abs())
+    assert err.max().item() < 1e-5, err.max().item()
+
+
+SMALL = [
+    ("tiny", wl.TINY, {}),                                                        # fp32, CUDA-core path
+    ("qwen_small", wl.QWEN3_8B, dict(B=20, V=5000, H=64)),                        # bf16, tensor cores
+    ("two_mtiles", wl.DRAFT_27B, dict(B=130, gamma=3, V=2048, H=96)),            # ragged second M-tile
+    ("r64_bf16", wl.QWEN3_8B, dict(B=9, gamma=5, V=1000, H=32, r=64)),
+    ("r16_bf16", wl.QWEN3_8B, dict(B=5, gamma=4, V=1000, H=32, r=16)),            # CUDA-core, bf16
+]
+
+
+@pytest.mark.parametrize("name,cfg,changes", SMALL, ids=[c[0] for c in SMALL])
+@pytest.mark.parametrize("temperature", [None, 0.0, 1.7])
+def test_draft_parity_small(dsv, name, cfg, changes, temperature):
+    cfg = wl.scaled(cfg, **changes)
+    inp = wl.make_draft_inputs(cfg)
+    gpu = gpu_draft(dsv, inp, temperature=temperature)
+    ref = oracle_draft(inp, gpu["x"], temperature=temperature)
+    exempt = compare(gpu, ref, cfg.dtype)
+    assert exempt <= max(2, gpu["x"].size // 50)
+    T = cfg.temperature if temperature is None else temperature
+    if T == 0.0:
+        assert np.all(gpu["lse_d"] == 0) and np.all(gpu["logp_d"] == 0)
+
+
+def test_draft_strong_bias_chain(dsv):
+    """Markov weights N(0, 0.5^2) make the bias O(1): tokens then depend on x_{k-1}."""
+    cfg = wl.scaled(wl.QWEN3_8B, B=16, gamma=6, V=3000, H=32)
+    inp = wl.make_draft_inputs(cfg)
+    g = torch.Generator().manual_seed(5)
+    inp["W1"] = (torch.randn(inp["W1"].shape, generator=g) * 0.5).bfloat16()
+    inp["W2"] = (torch.randn(inp["W2"].shape, generator=g) * 0.5).bfloat16()
+    for T in (0.7, 0.0):
+        gpu = gpu_draft(dsv, inp, temperature=T)
+        compare(gpu, oracle_draft(inp, gpu["x"], temperature=T), "bf16")
+
+
+def test_draft_rejects_bad_anchor(dsv):
+    cfg = wl.scaled(wl.QWEN3_8B, B=4, gamma=2, V=1024, H=16)
+    inp = wl.make_draft_inputs(cfg)
+    inp["x0"][2] = cfg.V + 5
+    dev = torch.device("cuda")
+    ws = torch.empty(dsv.load().dspark_draft_block_workspace_size(4, 2, 1024, 256), dtype=torch.uint8, device=dev)
+    dsv.dspark_draft_block(inp["U"].to(dev), inp["h"].to(dev), inp["W1"].to(dev), inp["W2"].to(dev),
+                           inp["w"].to(dev), 0.0, inp["x0"].to(dev), 1.0, 3, workspace=ws)
+    assert dsv.workspace_status(ws) == 6
+
+
+@pytest.mark.parametrize("key,temperature,nrows", [("qwen3_8b", 0.7, 12), ("qwen3_8b", 0.0, 12),
+                                                   ("draft_27b", None, 8), ("high_conc", None, 6)])
+def test_draft_full_size_sampled(dsv, key, temperature, nrows):
+    """Full-size configs on the GPU; a sample of requests checked one by one."""
+    cfg = wl.DRAFT_CONFIGS[key]
+    inp = wl.make_draft_inputs(cfg, device="cuda")
+    gpu = gpu_draft(dsv, inp, temperature=temperature)
+    rows = np.random.default_rng(0).choice(cfg.B, nrows, replace=False)
+    rows[0] = cfg.B - 1
+    ref = oracle_draft(inp, gpu["x"], temperature=temperature, rows=rows)
+    exempt = compare(gpu, ref, cfg.dtype, rows=rows)
+    assert exempt <= max(2, rows.size * cfg.gamma // 20)
+    a = gpu["a"]
+    assert np.all(np.diff(a, axis=1) <= 0) and np.all((a >= 0) & (a <= 1))
+    del inp
+    torch.cuda.empty_cache()
