@@ -80,6 +80,12 @@ __device__ __forceinline__ int prev_token(const int32_t* x0, const int32_t* x, i
     return t;
 }
 
+__device__ __forceinline__ void ld_u32x4(const void* p, uint32_t* o, uint64_t pol) {
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+                 : "l"(p), "l"(pol));
+}
+
 // Combine (m1, s1) += (m2, s2) for sums of 2^(y - m).
 __device__ __forceinline__ void lse_merge(float& m1, float& s1, float m2, float s2) {
     if (s2 <= 0.f) return;
@@ -199,11 +205,6 @@ struct RowRes {
     float m, s;
 };
 
-__device__ __forceinline__ void ld_u32x4(const void* p, uint32_t* o, uint64_t pol) {
-    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-                 : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
-                 : "l"(p), "l"(pol));
-}
 
 __global__ void __launch_bounds__(kTcThreads, 1)
 draft_phase_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
@@ -431,69 +432,121 @@ constexpr size_t kTcSmem = 1024 + 4 * kASlabBytes + kStages * kSlabBytes + (4 * 
                            kEpiWG * kBM * sizeof(RowRes);
 
 // ============================================================ winner ====
-// One warp per request: the token inside the winning block (greedy: the
-// argmax token itself), and y at that token.
-template <bool kBF16>
-__global__ void __launch_bounds__(256)
+// After v[i] (i < 32) is given in every lane, lane l ends with sum over lanes of
+// v[l] in v[0] (a butterfly that halves the live values at every stage).
+__device__ __forceinline__ void transpose_reduce32(float* v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool up = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            const float send = up ? v[i] : v[i + s];
+            const float keep = up ? v[i + s] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
+    }
+}
+
+// Two warps per request: the token inside the winning 64-token block (greedy:
+// the argmax token itself) and y at that token.  Warp w rebuilds z for tokens
+// blk*64 + 32w + (0..31): every lane loads one 16-byte chunk of each W2 row
+// (coalesced rows), forms its partial dot products, and a transpose-reduce
+// leaves token (32w + lane)'s dot product in lane `lane`.
+template <bool kBF16, int kCPL>
+__global__ void __launch_bounds__(64)
 draft_winner(int B, int gamma, int V, int r, int k, const void* __restrict__ U, const void* __restrict__ W1,
              const void* __restrict__ W2, const int32_t* __restrict__ x0, int32_t* __restrict__ x,
              float cscale, int greedy, uint64_t seed, DraftWs ws) {
+    constexpr int EPC = kBF16 ? 8 : 4;                    // elements per 16-byte chunk
+    __shared__ float sbest[2], sy[2];
+    __shared__ int sidx[2];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b = blockIdx.x * 8 + warp;
-    if (b >= B) return;
+    const int b = blockIdx.x;
     const size_t slot = static_cast<size_t>(k - 1) * B + b;
     const unsigned long long word = ws.words[slot];
     if (word == 0ull) {
-        if (lane == 0) { set_status(ws.status, DSPARK_ERR_DEVICE_CHECK, 3); x[b * gamma + k - 1] = 0; }
+        if (threadIdx.x == 0) { set_status(ws.status, DSPARK_ERR_DEVICE_CHECK, 3); x[b * gamma + k - 1] = 0; }
         return;
     }
     const uint32_t idx = unpack_idx(word);
     if (greedy) {
-        if (lane == 0) { x[b * gamma + k - 1] = static_cast<int>(idx); ws.ytok[slot] = 0.f; }
+        if (threadIdx.x == 0) { x[b * gamma + k - 1] = static_cast<int>(idx); ws.ytok[slot] = 0.f; }
         return;
     }
     const int prev = prev_token(x0, x, b, gamma, k, V, ws.status);
-    float ep[8];
+    const int nch = r / EPC;                              // 16-byte chunks per row
+    float e[kCPL][EPC];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const int j = lane + 32 * q;
-        ep[q] = (j < r) ? ld_elem<kBF16>(W1, static_cast<size_t>(prev) * r + j) : 0.f;
+    for (int cc = 0; cc < kCPL; ++cc) {
+        const int c = lane + 32 * cc;
+#pragma unroll
+        for (int q = 0; q < EPC; ++q)
+            e[cc][q] = (c < nch) ? ld_elem<kBF16>(W1, static_cast<size_t>(prev) * r + c * EPC + q) : 0.f;
     }
-    const size_t urow = (static_cast<size_t>(b) * gamma + (k - 1)) * V;
-    float yv[2] = {-INFINITY, -INFINITY};
-    for (int i = 0; i < 64; ++i) {
-        const int v = static_cast<int>(idx) * 64 + i;
-        if (v >= V) break;                                 // warp-uniform
-        float part = 0.f;
+    const int vbase = static_cast<int>(idx) * 64 + warp * 32;
+    const uint64_t pol = policy_evict_last();
+    float part[32];
+    constexpr int kBatch = 32 / kCPL;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int j = lane + 32 * q;
-            if (j < r) part = fmaf(ld_elem<kBF16>(W2, static_cast<size_t>(v) * r + j), ep[q], part);
+    for (int i0 = 0; i0 < 32; i0 += kBatch) {
+        uint4 raw[kBatch][kCPL];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int v = vbase + i0 + i;
+#pragma unroll
+            for (int cc = 0; cc < kCPL; ++cc) {
+                const int c = lane + 32 * cc;
+                raw[i][cc] = make_uint4(0, 0, 0, 0);
+                if (v < V && c < nch)   // volatile loads: all issue before the first use
+                    ld_u32x4(static_cast<const uint8_t*>(W2) + (static_cast<size_t>(v) * r + c * EPC) * (kBF16 ? 2 : 4),
+                             &raw[i][cc].x, pol);
+            }
         }
-        const float z = warp_sum(part) + ld_elem<kBF16>(U, urow + v);
-        if (lane == (i & 31)) yv[i >> 5] = z * cscale;
-    }
-    float best = -INFINITY, by = 0.f;
-    int bi = 0x7FFFFFFF;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int v = static_cast<int>(idx) * 64 + h * 32 + lane;
-        if (v < V && yv[h] > -INFINITY) {
-            const float g = gumbel_of(uniform_open(draw_word(seed, b, k, kStreamDraftToken, static_cast<uint32_t>(v))));
-            const float sc = yv[h] + g * kLog2e;
-            if (sc > best || (sc == best && v < bi)) { best = sc; bi = v; by = yv[h]; }
+        for (int i = 0; i < kBatch; ++i) {
+            float acc = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < kCPL; ++cc) {
+                const uint32_t wv[4] = {raw[i][cc].x, raw[i][cc].y, raw[i][cc].z, raw[i][cc].w};
+                if constexpr (kBF16) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc = fmaf(bf16lo(wv[q]), e[cc][2 * q], acc);
+                        acc = fmaf(bf16hi(wv[q]), e[cc][2 * q + 1], acc);
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc = fmaf(__uint_as_float(wv[q]), e[cc][q], acc);
+                }
+            }
+            part[i0 + i] = acc;
         }
     }
+    transpose_reduce32(part);
+    const int v = vbase + lane;
+    float score = -INFINITY, yv = 0.f;
+    if (v < V) {
+        const size_t urow = (static_cast<size_t>(b) * gamma + (k - 1)) * V;
+        yv = (part[0] + ld_elem<kBF16>(U, urow + v)) * cscale;
+        const float g = gumbel_of(uniform_open(draw_word(seed, b, k, kStreamDraftToken, static_cast<uint32_t>(v))));
+        score = yv + g * kLog2e;
+    }
+    int bi = (v < V) ? v : 0x7FFFFFFF;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-        const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+        const float os = __shfl_xor_sync(0xffffffffu, score, o);
         const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        const float oy = __shfl_xor_sync(0xffffffffu, by, o);
-        if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; by = oy; }
+        const float oy = __shfl_xor_sync(0xffffffffu, yv, o);
+        if (os > score || (os == score && oi < bi)) { score = os; bi = oi; yv = oy; }
     }
-    if (lane == 0) {
-        x[b * gamma + k - 1] = (bi == 0x7FFFFFFF) ? 0 : bi;
-        ws.ytok[slot] = by;
+    if (lane == 0) { sbest[warp] = score; sidx[warp] = bi; sy[warp] = yv; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int w = 0;
+        if (sbest[1] > sbest[0] || (sbest[1] == sbest[0] && sidx[1] < sidx[0])) w = 1;
+        x[b * gamma + k - 1] = (sidx[w] == 0x7FFFFFFF) ? 0 : sidx[w];
+        ws.ytok[slot] = sy[w];
     }
 }
 
@@ -650,11 +703,13 @@ dspark_status_t draft_block_impl(int B, int gamma, int V, int H, int r, dspark_d
             stt = launch_status();
         }
         if (stt != DSPARK_OK) return stt;
-        const int wgrid = (B + 7) / 8;
+        // chunks of 16 bytes per W2 row: up to 32 (bf16, r <= 256) or 64 (f32) -> 1 or 2 per lane
         if (bf)
-            draft_winner<true><<<wgrid, 256, 0, s>>>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale, greedy, seed, ws);
+            draft_winner<true, 1><<<B, 64, 0, s>>>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale, greedy, seed, ws);
+        else if (r <= 128)
+            draft_winner<false, 1><<<B, 64, 0, s>>>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale, greedy, seed, ws);
         else
-            draft_winner<false><<<wgrid, 256, 0, s>>>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale, greedy, seed, ws);
+            draft_winner<false, 2><<<B, 64, 0, s>>>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale, greedy, seed, ws);
         if ((stt = launch_status()) != DSPARK_OK) return stt;
     }
     const int fgrid = (B + 7) / 8;

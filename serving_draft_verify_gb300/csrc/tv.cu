@@ -158,7 +158,9 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
         m = block_max2(m, red);
         // y = x log2e is rounded before the max is subtracted: rounding is monotone,
         // so max(y) is exactly md2 and y - md2 <= 0 even for |x| near the float range
-        const float md2 = __fmul_rn(m.x, kLog2e), mt2 = __fmul_rn(m.y, kLog2e);
+        // a slice with no finite logit keeps reference 0 so that its terms are 2^-inf = 0
+        const float md2 = (m.x > -INFINITY) ? __fmul_rn(m.x, kLog2e) : 0.f;
+        const float mt2 = (m.y > -INFINITY) ? __fmul_rn(m.y, kLog2e) : 0.f;
 
         // B: exponentials in registers, slice sums
         float ed[GMAX * EPG], et[GMAX * EPG];
@@ -203,7 +205,9 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
         float rmd = -INFINITY, rsd = 0.f, rmt = -INFINITY, rst = 0.f;
         if (lane < kCS) {
             const Slot* rs = cluster.map_shared_rank(slot, lane);
-            rmd = rs->md; rsd = rs->sd; rmt = rs->mt; rst = rs->st;
+            rsd = rs->sd; rst = rs->st;
+            rmd = rsd > 0.f ? rs->md : -INFINITY;          // empty slices do not set the reference
+            rmt = rst > 0.f ? rs->mt : -INFINITY;
         }
         const float Md = warp_max(rmd), Mt = warp_max(rmt);
         const float Sd = warp_sum(rsd > 0.f ? rsd * exp2f(rmd - Md) : 0.f);
