@@ -1,0 +1,367 @@
+"""Benchmark of the DSpark serving round on GB300: draft block -> prefix
+scheduler -> verification, on the Qwen3-8B-shaped serving workload
+(B = 64 requests, gamma = 7, V = 151936, H = 4096, r = 256, bf16, T = 0.7),
+synthetic seeded inputs.
+
+One step = one round through the library's C ABI (all kernels on one stream).
+The timed region holds exactly K steps; the L2 is flushed (a 512 MiB write)
+between steps, outside each step's CUDA-event pair.  The JSON line also
+reports the dominant kernel's roofline (the draft phase kernel: its launches
+are timed with CUDA events recorded by the library around each launch), an
+end-to-end number through the same C-ABI calls with inputs copied from pinned
+host memory each step, the oracle timed on the host cores on a bounded sample,
+and extra lines for greedy decoding and the accept-rate TV kernel.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With --gpus N > 1 (under torchrun) every rank runs an independent replica of
+the round (the path has no cross-request exchange); value = rows of all ranks
+over the slowest rank's time.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft+verify rows/s over B·γ×V logits; achieved HBM GB/s vs GB300 peak"
+WORKLOAD = ("Qwen3-8B-shaped serving round: B=64, gamma=7 (verify width 8), V=151936, H=4096, r=256, "
+            "bf16, T=0.7, seed 1")
+FALLBACK_HBM_GBS = 6800.0
+CPU_SAMPLE_REQUESTS = 12
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def engine_source_hash():
+    """Hash of the draft phase kernel's sources: a recorded ncu traffic figure is
+    only reported while the kernel it was measured on is unchanged."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("engine.cuh", "draft.cu", "tc.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "serving_draft_verify_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_phase_traffic():
+    p = os.path.join(ROOT, "profiles", "draft_phase_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    return d.get("dram_bytes_per_launch") if d.get("source_hash") == engine_source_hash() else None
+
+
+def smi_index(local):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").strip()
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if local < len(ids) and ids[local].isdigit():
+            return int(ids[local])
+    return local
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------ clocks ---
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------- GPU arm ---
+def run_gpu(args):
+    import torch
+    import serving_draft_verify_gb300 as dsv
+    from serving_draft_verify_gb300 import workloads as wl
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dsv.load()
+    lib = dsv._binding.load()
+    cfg = wl.QWEN3_8B
+    inp = wl.make_draft_inputs(cfg, device=dev)
+    B, G, V, H, r = cfg.B, cfg.gamma, cfg.V, cfg.H, cfg.r
+    T, seed = cfg.temperature, cfg.seed
+    stream = torch.cuda.current_stream()
+
+    ws_d = torch.empty(lib.dspark_draft_block_workspace_size(B, G, V, r), dtype=torch.uint8, device=dev)
+    ws_s = torch.empty(lib.dspark_schedule_prefix_workspace_size(B, G), dtype=torch.uint8, device=dev)
+    ws_v = torch.empty(lib.dspark_verify_workspace_size(B, G, V, r), dtype=torch.uint8, device=dev)
+    outd = dict(x=torch.empty((B, G), dtype=torch.int32, device=dev),
+                **{k: torch.empty((B, G), dtype=torch.float32, device=dev) for k in ("lse_d", "logp_d", "c", "a")})
+    outs = dict(ell=torch.empty(B, dtype=torch.int32, device=dev), n_sched=torch.empty(1, dtype=torch.int32, device=dev),
+                theta=torch.empty(1, dtype=torch.float64, device=dev))
+    outv = dict(n_accept=torch.empty(B, dtype=torch.int32, device=dev),
+                next_token=torch.empty(B, dtype=torch.int32, device=dev))
+
+    def round_(g, temperature):
+        dsv.dspark_draft_block(g["U"], g["h"], g["W1"], g["W2"], g["w"], 0.0, g["x0"], temperature, seed,
+                               out=outd, workspace=ws_d)
+        dsv.dspark_schedule_prefix(outd["a"], g["sps"], out=outs, workspace=ws_s)
+        dsv.dspark_verify(g["t"], g["U"], g["W1"], g["W2"], g["x0"], outd["x"], outd["lse_d"], outd["logp_d"],
+                          outs["ell"], temperature, seed, out=outv, workspace=ws_v)
+
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            torch.cuda.synchronize()
+
+    def timed(fn, steps, warmup, phase_times=False):
+        for _ in range(warmup):
+            fn()
+        barrier()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        phases = []
+        for s, e in evs:
+            flush.zero_()
+            s.record(stream)
+            fn()
+            e.record(stream)
+            if phase_times:
+                phases.extend(dsv._binding.phase_times())
+        barrier()
+        return [s.elapsed_time(e) for s, e in evs], phases
+
+    # main arm, T = 0.7, with per-phase-launch timing of the draft phase kernel
+    clocks = ClockSampler(smi_index(local))
+    dsv._binding.phase_timing(True)
+    clocks.start()
+    times, phase_ms = timed(lambda: round_(inp, T), args.steps, args.warmup, phase_times=True)
+    clk = clocks.stop()
+    dsv._binding.phase_timing(False)
+    assert dsv.workspace_status(ws_d) == 0 and dsv.workspace_status(ws_v) == 0
+    total_ms = sum(times)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    rows = B * G * args.steps * world
+    value = rows / (total_ms * 1e-3)
+    ms_per_step = total_ms / args.steps
+
+    # algorithmic bytes of one round: U and h once, W2 once per draft call, W1 rows,
+    # the scheduled target rows, and the residual rows (U and t) of rejected requests
+    ell = outs["ell"].cpu().numpy()
+    nacc = outv["n_accept"].cpu().numpy()
+    n_rej = int((nacc < ell).sum())
+    round_bytes = (B * G * V * 2 + V * r * 2 + B * G * H * 2 + B * G * r * 2 + int((ell + 1).sum()) * V * 2
+                   + n_rej * 2 * V * 2)
+    hbm_gbs = round_bytes * args.steps / (total_ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+
+    # dominant kernel: the draft phase kernel (one per position k)
+    phase_bytes = B * V * 2 + V * r * 2 / G + B * r * 2
+    ph = sorted(phase_ms)
+    phase_avg = sum(ph) / len(ph) if ph else float("nan")
+    achieved = phase_bytes / (phase_avg * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "bias_engine_tc<kDraft> (draft phase)", "achieved": round(achieved, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": args.phase_traffic if args.phase_traffic is not None else recorded_phase_traffic(),
+                "peak_kind": f"{peak_kind} (copy bandwidth)", "bytes_per_launch": int(phase_bytes),
+                "avg_launch_us": round(phase_avg * 1e3, 2), "launches_timed": len(ph)}
+
+    # greedy round (same workload, T = 0)
+    g_times, _ = timed(lambda: round_(inp, 0.0), max(3, args.steps // 2), args.warmup)
+    greedy = {"value": B * G * len(g_times) / (sum(g_times) * 1e-3), "unit": "rows/s",
+              "ms_per_step": sum(g_times) / len(g_times)}
+
+    # end to end: per-round inputs from pinned host memory, results back to the host
+    host = {k: inp[k].cpu().pin_memory() for k in ("U", "t", "h", "x0", "sps")}
+    dev_in = {k: torch.empty_like(inp[k]) for k in host}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    res_host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                for k, v in (("x", outd["x"]), ("n_accept", outv["n_accept"]), ("next_token", outv["next_token"]))}
+    d2h = sum(v.numel() * v.element_size() for v in res_host.values())
+    gfull = dict(inp)
+
+    def e2e_round():
+        for k in host:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        gfull.update(dev_in)
+        round_(gfull, T)
+        res_host["x"].copy_(outd["x"], non_blocking=True)
+        res_host["n_accept"].copy_(outv["n_accept"], non_blocking=True)
+        res_host["next_token"].copy_(outv["next_token"], non_blocking=True)
+
+    e_times, _ = timed(e2e_round, args.steps, args.warmup)
+    e2e = {"value": B * G * args.steps * world / (sum(e_times) * 1e-3), "unit": "rows/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    # accept-rate TV on the training workload (16384 x 151936 bf16 rows)
+    tv = None
+    if not args.skip_tv:
+        d_, t_ = wl.make_tv_inputs(wl.TV_TRAIN, device=dev)
+        cst = torch.empty(d_.shape[0], dtype=torch.float32, device=dev)
+        ws_t = torch.empty(256, dtype=torch.uint8, device=dev)
+        tv_times, _ = timed(lambda: dsv.dspark_accept_rate_tv(d_, t_, c_star=cst, workspace=ws_t), 5, 3)
+        tvb = 2 * d_.numel() * 2
+        tv_ms = sum(tv_times) / len(tv_times)
+        tv = {"rows": d_.shape[0], "ms": tv_ms, "rows_per_s": d_.shape[0] / (tv_ms * 1e-3),
+              "achieved_gbs": tvb / (tv_ms * 1e-3) / 1e9, "frac_of_peak": tvb / (tv_ms * 1e-3) / 1e9 / peak}
+        del d_, t_
+    launches_per_step = (2 * G + 1) + 1 + 4          # draft: phase + winner per k, finalize; schedule; verify
+
+    line = {"metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; shapes of the Qwen3-8B draft setting)",
+            "config": {"workload": WORKLOAD, "B": B, "gamma": G, "V": V, "H": H, "r": r, "temperature": T,
+                       "l2": "flushed between steps (512 MiB write outside the timed step)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / peak, "roofline": roofline, "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps, "clocks": clk,
+            "extra": {"greedy_round": greedy, "accept_rate_tv": tv,
+                      "accepted_per_request": float(nacc.mean()), "scheduled_rows": int((ell + 1).sum())}}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, T, seed)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+# ------------------------------------------------------------ oracle ---
+def cpu_baseline(inp, T, seed, nreq=CPU_SAMPLE_REQUESTS):
+    """The oracle (float64, numpy) on a bounded sample of the same round: the
+    first `nreq` requests through draft, schedule (over the sample) and verify."""
+    import numpy as np
+    import torch
+    import oracle
+    from serving_draft_verify_gb300 import workloads as wl
+
+    rows = np.arange(nreq)
+    idx = torch.from_numpy(rows).to(inp["U"].device)
+    U, h, t = (wl.to_f64(inp[k][idx]) for k in ("U", "h", "t"))
+    W1, W2, w = (wl.to_f64(inp[k]) for k in ("W1", "W2", "w"))
+    x0 = inp["x0"][idx].cpu().numpy()
+    G = U.shape[1]
+    t0 = time.perf_counter()
+    d = oracle.draft_block(U, h, W1, W2, w, 0.0, x0, T, seed, requests=rows)
+    N = np.arange(nreq * (G + 1) + 1, dtype=np.float64)
+    ell, _, _ = oracle.schedule_prefix(d["a"].astype(np.float32), N / (20.0 + 0.05 * N))
+    oracle.verify_round(t, U, W1, W2, x0, d["x"], d["lse_d"], d["logp_d"], ell, T, seed, requests=rows)
+    dt = time.perf_counter() - t0
+    return {"value": nreq * G / dt, "unit": "rows/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{nreq} of 64 requests x {G} positions, one full round (draft, schedule, verify), "
+                      f"float64 numpy; {dt:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, local = dist_setup()
+    if rank != 0:
+        return
+    import torch
+    from serving_draft_verify_gb300 import workloads as wl
+    cfg = wl.QWEN3_8B
+    inp = wl.make_draft_inputs(cfg, device="cpu")
+    for _ in range(args.warmup):
+        pass                                              # the oracle has nothing to warm
+    times = []
+    nreq = 4
+    for _ in range(args.steps):
+        r = cpu_baseline(inp, cfg.temperature, cfg.seed, nreq=nreq)
+        times.append(nreq * cfg.gamma / r["value"])
+    total = sum(times)
+    value = nreq * cfg.gamma * args.steps / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)", "config": {"workload": WORKLOAD + f"; {nreq} requests per step"},
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"{nreq} of 64 requests x {cfg.gamma} positions per step"},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--skip-tv", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--phase-traffic", type=float, default=None,
+                    help="dram bytes per draft phase launch from an ncu capture (reported as roofline.traffic)")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "native":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

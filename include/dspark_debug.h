@@ -25,6 +25,17 @@ dspark_status_t dspark_debug_draft_logits(int B, int V, int r, const void* U_k, 
                                           void* workspace, size_t workspace_bytes,
                                           dspark_stream_t stream);
 
+/* Measurement hook: while enabled, dspark_draft_block records a pair of CUDA
+ * events (created by the library on the current device at the first enable)
+ * around every phase-kernel launch, i.e. the vocabulary-wide pass that forms
+ * z_k and its block keys for one position k.  dspark_debug_phase_times()
+ * waits for the last recorded event and writes the duration in ms of each
+ * phase launch of the most recent dspark_draft_block call into ms[0..n-1];
+ * it returns the number of phases recorded (0 if timing is off).  Not
+ * thread-safe; meant for benchmarks, one device at a time. */
+dspark_status_t dspark_debug_enable_phase_timing(int enable);
+int dspark_debug_phase_times(float* ms, int n);
+
 #ifdef __cplusplus
 }
 #endif

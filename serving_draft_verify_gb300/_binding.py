@@ -38,6 +38,8 @@ _SIGNATURES = {
     "dspark_accept_rate_tv_workspace_size": (_c_size, [_c_i64, _c_int]),
     "dspark_accept_rate_tv": (_c_int, [_c_i64, _c_int, _c_int, _p, _p, _p, _p, _c_size, _p]),
     "dspark_debug_draft_logits": (_c_int, [_c_int, _c_int, _c_int, _p, _p, _p, _p, _p, _p, _c_size, _p]),
+    "dspark_debug_enable_phase_timing": (_c_int, [_c_int]),
+    "dspark_debug_phase_times": (_c_int, [_p, _c_int]),
 }
 
 _lib = None
@@ -234,3 +236,15 @@ def dspark_debug_draft_logits(U_k, W1, W2, prev, z=None, workspace=None, stream=
            lib.dspark_debug_draft_logits(B, V, r, _ptr(U_k), _ptr(W1), _ptr(W2), _ptr(prev), _ptr(z), _ptr(ws),
                                          _nbytes(ws), _stream(stream)))
     return z, ws
+
+
+def phase_timing(enable):
+    """Measurement hook: record CUDA events around every draft phase launch."""
+    _check("dspark_debug_enable_phase_timing", load().dspark_debug_enable_phase_timing(1 if enable else 0))
+
+
+def phase_times():
+    """Durations (ms) of the phase launches of the most recent draft call."""
+    buf = (ctypes.c_float * 64)()
+    n = load().dspark_debug_phase_times(ctypes.cast(buf, ctypes.c_void_p), 64)
+    return [buf[i] for i in range(n)]

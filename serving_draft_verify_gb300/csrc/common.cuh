@@ -162,6 +162,13 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// 2^x on the special-function unit (ex2.approx.ftz: ~2 ulp; -inf -> 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // bf16 pair (packed in a 32-bit word) -> two floats, exactly.
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

@@ -1,0 +1,536 @@
+// The bias engine shared by dspark_draft_block and dspark_verify: for a set of
+// request rows, each with a position k_b, it forms the draft logits
+//   z_b = U[b][k_b-1] + W2 . W1[x_{k_b-1}]       (VanillaMarkovHead, eq. 5;
+//                                                 DeepSpec walkthrough 3.2)
+// tile by tile on the tensor cores and reduces them in its epilogue:
+//   kDraft     per 64-token block: logsumexp of z / T and a Gumbel block key
+//              (draft sampling), or the running argmax of z (greedy);
+//   kResidual  per 64-token block: the mass of max(0, p_t - p_d) and a Gumbel
+//              block key (the residual draw of verification, section 8.2).
+// Each CTA publishes its best block per row with a 64-bit atomicMax of
+// (key, ~block) and, for kDraft, its (max, sum) partial.
+//
+// Layout of one CTA (384 threads, one CTA per SM):
+//   warp 0      TMA producer: W2 tiles [128 tokens x 64 K] into a slab ring
+//               (128-byte swizzle, L2 evict-last so W2 stays resident);
+//   warp 1      TMEM allocator and MMA issuer: tcgen05.mma kind::f16,
+//               M = 128 request rows, N = 128 tokens, K = r, fp32 in TMEM;
+//   warps 4-11  two epilogue warpgroups, each with two TMEM accumulators, so
+//               the MMA of the next tile overlaps the epilogue of this one.
+// The A operand (rows W1[x_{k_b-1}], gathered into shared memory with the
+// same swizzle) is built once per launch.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "host_common.h"
+#include "tc.cuh"
+
+namespace dspark {
+namespace eng {
+
+constexpr int kMaxChunks = 256;   // partial slots per (position, request)
+
+struct Ws {
+    StatusBlock* status;
+    unsigned long long* words;   // [positions][B] best (key, ~block) or (value, ~token)
+    float2* part;                // [positions][B][kMaxChunks] (max, sum) of y = z log2e / T
+    float* ytok;                 // [positions][B] y of the drawn token
+};
+
+// ------------------------------------------------------------ helpers ---
+__device__ __forceinline__ uint32_t f2ord(float f) {
+    const uint32_t b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ unsigned long long pack_key(float key, uint32_t idx) {
+    return (static_cast<unsigned long long>(f2ord(key)) << 32) | static_cast<uint32_t>(~idx);
+}
+__device__ __forceinline__ uint32_t unpack_idx(unsigned long long w) { return ~static_cast<uint32_t>(w); }
+
+template <bool kBF16>
+__device__ __forceinline__ float ld_elem(const void* p, size_t i) {
+    if constexpr (kBF16) {
+        return __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(p)[i]) << 16);
+    } else {
+        return static_cast<const float*>(p)[i];
+    }
+}
+
+__device__ __forceinline__ void ld_u32x4(const void* p, uint32_t* o, uint64_t pol) {
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+                 : "l"(p), "l"(pol));
+}
+
+// Token x_{k-1} of request b (the anchor for k = 1), checked against [0, V).
+__device__ __forceinline__ int prev_token(const int32_t* x0, const int32_t* x, int b, int gamma, int k, int V,
+                                          StatusBlock* st) {
+    const int t = (k == 1) ? x0[b] : x[b * gamma + k - 2];
+    if (t < 0 || t >= V) {
+        set_status(st, DSPARK_ERR_DEVICE_CHECK, 2);
+        return 0;
+    }
+    return t;
+}
+
+// Combine (m1, s1) += (m2, s2) for sums of 2^(y - m).
+__device__ __forceinline__ void lse_merge(float& m1, float& s1, float m2, float s2) {
+    if (s2 <= 0.f) return;
+    if (s1 <= 0.f) { m1 = m2; s1 = s2; return; }
+    const float M = fmaxf(m1, m2);
+    s1 = s1 * exp2f(m1 - M) + s2 * exp2f(m2 - M);
+    m1 = M;
+}
+
+// After v[i] (i < 32) is given in every lane, lane l ends with sum over lanes of
+// v[l] in v[0] (a butterfly that halves the live values at every stage).
+__device__ __forceinline__ void transpose_reduce32(float* v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool up = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            const float send = up ? v[i] : v[i + s];
+            const float keep = up ? v[i + s] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
+    }
+}
+
+// Two warps per request: z for the 64 tokens of block `blk` of row (b, k):
+// warp w rebuilds tokens blk*64 + 32w + (0..31); each lane loads one or two
+// 16-byte chunks of every W2 row (coalesced rows) and a transpose-reduce
+// leaves token (32w + lane)'s dot product in that lane.  Returns z for the
+// lane's token (-inf past V).
+template <bool kBF16, int kCPL>
+__device__ __forceinline__ float block_logit(int b, int gamma, int k, int V, int r, int blk, const void* U,
+                                             const void* W1, const void* W2, const int32_t* x0, const int32_t* x,
+                                             StatusBlock* st) {
+    constexpr int EPC = kBF16 ? 8 : 4;                    // elements per 16-byte chunk
+    const int warp = (threadIdx.x >> 5) & 1, lane = threadIdx.x & 31;
+    const int prev = prev_token(x0, x, b, gamma, k, V, st);
+    const int nch = r / EPC;
+    float e[kCPL][EPC];
+#pragma unroll
+    for (int cc = 0; cc < kCPL; ++cc) {
+        const int c = lane + 32 * cc;
+#pragma unroll
+        for (int q = 0; q < EPC; ++q)
+            e[cc][q] = (c < nch) ? ld_elem<kBF16>(W1, static_cast<size_t>(prev) * r + c * EPC + q) : 0.f;
+    }
+    const int vbase = blk * 64 + warp * 32;
+    const uint64_t pol = policy_evict_last();
+    float part[32];
+    constexpr int kBatch = 32 / kCPL;
+#pragma unroll
+    for (int i0 = 0; i0 < 32; i0 += kBatch) {
+        uint4 raw[kBatch][kCPL];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int v = vbase + i0 + i;
+#pragma unroll
+            for (int cc = 0; cc < kCPL; ++cc) {
+                const int c = lane + 32 * cc;
+                raw[i][cc] = make_uint4(0, 0, 0, 0);
+                if (v < V && c < nch)
+                    ld_u32x4(static_cast<const uint8_t*>(W2) + (static_cast<size_t>(v) * r + c * EPC) * (kBF16 ? 2 : 4),
+                             &raw[i][cc].x, pol);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            float acc = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < kCPL; ++cc) {
+                const uint32_t wv[4] = {raw[i][cc].x, raw[i][cc].y, raw[i][cc].z, raw[i][cc].w};
+                if constexpr (kBF16) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc = fmaf(bf16lo(wv[q]), e[cc][2 * q], acc);
+                        acc = fmaf(bf16hi(wv[q]), e[cc][2 * q + 1], acc);
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc = fmaf(__uint_as_float(wv[q]), e[cc][q], acc);
+                }
+            }
+            part[i0 + i] = acc;
+        }
+    }
+    transpose_reduce32(part);
+    const int v = vbase + lane;
+    if (v >= V) return -INFINITY;
+    const size_t urow = (static_cast<size_t>(b) * gamma + (k - 1)) * V;
+    return part[0] + ld_elem<kBF16>(U, urow + v);
+}
+
+// ===================================================== tcgen05 engine ====
+constexpr int kBM = 128;              // request rows per M-tile (TMEM lanes)
+constexpr int kBN = 128;              // vocabulary columns per tile
+constexpr int kBK = 64;               // K per smem slab (128 bytes of bf16)
+constexpr int kStages = 6;            // W2 slab ring
+constexpr int kEpiWG = 2;             // epilogue warpgroups, two TMEM buffers each
+constexpr int kTcThreads = 128 * (1 + kEpiWG);
+constexpr int kSlabBytes = kBN * kBK * 2;     // 16 KB
+constexpr int kASlabBytes = kBM * kBK * 2;    // 16 KB
+
+enum Mode : int { kDraft = 0, kResidual = 1 };
+
+struct TcParams {
+    int B, gamma, V, r, k;           // k: the position of every row (kDraft)
+    const uint16_t* U;               // [B][gamma][V]
+    const uint16_t* W1;              // [V][r]
+    const int32_t* x0;               // [B]
+    const int32_t* x;                // [B][gamma]
+    float cscale;                    // log2e / T (1 for greedy)
+    int greedy;
+    uint64_t seed;
+    int P;                           // CTAs per M-tile
+    Ws ws;
+    float* debug_z;                  // kDraft: write y to [B][V] instead of reducing
+    // kResidual
+    const int32_t* krow;             // [B] rejected position k_b (0: row inactive)
+    const uint16_t* T;               // t_logits [B][gamma+1][V]
+    const float* lt2;                // [B] log2-sum-exp2 of t / T at row k_b (log2 units)
+    const float* ld2;                // [B] lse_d[b][k_b-1] * log2e
+};
+
+struct RowRes {
+    float key;
+    int idx;
+    float m, s;
+};
+
+template <int kMode>
+__global__ void __launch_bounds__(kTcThreads, 1)
+bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const int nslab = p.r / kBK;
+    uint8_t* sA = smem;                                   // nslab x 16 KB
+    uint8_t* sB = smem + 4 * kASlabBytes;                 // kStages x 16 KB
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kSlabBytes);
+    uint64_t* empty = full + kStages;
+    uint64_t* tfull = empty + kStages;                    // [2 * kEpiWG]
+    uint64_t* tempty = tfull + 2 * kEpiWG;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2 * kEpiWG);
+    RowRes* rowres = reinterpret_cast<RowRes*>(tmem_slot + 4);   // [kEpiWG][128]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = blockIdx.x / p.P, pc = blockIdx.x % p.P;
+    const int m0 = g * kBM;
+    const int NT = (p.V + kBN - 1) / kBN;
+    const int t_lo = static_cast<int>(static_cast<long long>(pc) * NT / p.P);
+    const int t_hi = static_cast<int>(static_cast<long long>(pc + 1) * NT / p.P);
+    const int ntiles = t_hi - t_lo;
+    StatusBlock* st = p.ws.status;
+    auto row_k = [&](int b) -> int { return (kMode == kResidual) ? p.krow[b] : p.k; };
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int e = 0; e < 2 * kEpiWG; ++e) { mbar_init(&tfull[e], 1); mbar_init(&tempty[e], 4); }
+        fence_mbar_init();
+        tc::prefetch_tmap(&tmW2);
+    }
+    if (warp == 1) tc::tmem_alloc(tmem_slot, 512);
+
+    // A operand: rows W1[x_{k_b-1}] of this M-tile, K-major, 128-byte swizzle
+    {
+        const int cpr = p.r / 8;                          // 16-byte chunks per row
+        for (int idx = tid; idx < kBM * cpr; idx += kTcThreads) {
+            const int row = idx / cpr, c16 = idx % cpr;
+            const int slab = c16 >> 3, c = c16 & 7;
+            const int b = m0 + row;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (b < p.B) {
+                const int kb = row_k(b);
+                if (kb > 0) {
+                    const int prev = prev_token(p.x0, p.x, b, p.gamma, kb, p.V, st);
+                    v = *reinterpret_cast<const uint4*>(p.W1 + static_cast<size_t>(prev) * p.r + c16 * 8);
+                }
+            }
+            uint8_t* dst = sA + slab * kASlabBytes + (row >> 3) * 1024 + (row & 7) * 128 + ((c ^ (row & 7)) << 4);
+            *reinterpret_cast<uint4*>(dst) = v;
+        }
+    }
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    bool failed = false;
+
+    if (warp == 0) {
+        // ---------------------------------------------------- TMA producer
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_last();
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int t = t_lo; t < t_hi && !failed; ++t) {
+                for (int s = 0; s < nslab; ++s) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u)) { failed = true; break; }
+                    mbar_arrive_expect_tx(&full[stage], kSlabBytes);
+                    tc::tma_load_2d(sB + stage * kSlabBytes, &tmW2, s * kBK, t * kBN, &full[stage], pol);
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (failed) set_status(st, DSPARK_ERR_TIMEOUT, 10);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN);
+            const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int i = 0; i < ntiles && !failed; ++i) {
+                const int eg = i % kEpiWG, use = i / kEpiWG;
+                const int buf = eg * 2 + (use & 1);
+                const uint32_t par = static_cast<uint32_t>(use >> 1) & 1u;
+                if (!mbar_wait(&tempty[buf], par ^ 1u)) { failed = true; break; }
+                tc::fence_after_sync();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(buf * kBN);
+                for (int s = 0; s < nslab; ++s) {
+                    if (!mbar_wait(&full[stage], phase)) { failed = true; break; }
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint64_t ad = tc::smem_desc_sw128(a0 + s * kASlabBytes + kk * 32);
+                        const uint64_t bd = tc::smem_desc_sw128(b0 + stage * kSlabBytes + kk * 32);
+                        tc::mma_bf16(d, ad, bd, idesc, (s | kk) != 0);
+                    }
+                    tc::commit(&empty[stage]);
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+                tc::commit(&tfull[buf]);
+            }
+            if (failed) set_status(st, DSPARK_ERR_TIMEOUT, 11);
+        }
+    } else if (warp >= 4) {
+        // -------------------------------------------------------- epilogue
+        const int eg = (warp - 4) >> 2;                   // warpgroup 0..kEpiWG-1
+        const int q = warp & 3;                           // TMEM lane quarter
+        const int row = q * 32 + lane;
+        const int b = m0 + row;
+        const int kb = (b < p.B) ? row_k(b) : 0;
+        const bool valid = b < p.B && kb > 0;
+        const bool warp_live = (m0 + q * 32) < p.B;
+        const uint64_t pol = policy_evict_first();
+        const size_t urow_off = (static_cast<size_t>(valid ? b : 0) * p.gamma + (valid ? kb - 1 : 0)) * p.V;
+        const uint16_t* urow = p.U + urow_off;
+        float ld2 = 0.f, lt2 = 0.f;
+        const uint16_t* trow = nullptr;
+        if constexpr (kMode == kResidual) {
+            if (valid) {
+                ld2 = p.ld2[b];
+                lt2 = p.lt2[b];
+                trow = p.T + (static_cast<size_t>(b) * (p.gamma + 1) + (kb - 1)) * p.V;
+            }
+        }
+        float best = -INFINITY, M = -INFINITY, S = 0.f;
+        int best_i = 0x7FFFFFFF;
+        const int nmine = (ntiles > eg) ? (ntiles - eg + kEpiWG - 1) / kEpiWG : 0;
+
+        uint32_t u[2][32];                                // U of the two 64-token blocks of one tile
+        auto load_blk = [&](const uint16_t* base, int t, int hb, uint32_t* dst) {
+            const int v0 = t * kBN + hb * 64;
+#pragma unroll
+            for (int g8 = 0; g8 < 8; ++g8) {
+                if (valid && v0 + g8 * 8 < p.V) ld_u32x4(base + v0 + g8 * 8, dst + g8 * 4, pol);
+                else { dst[g8 * 4] = dst[g8 * 4 + 1] = dst[g8 * 4 + 2] = dst[g8 * 4 + 3] = 0u; }
+            }
+        };
+        if (kMode == kDraft && nmine > 0 && warp_live) {
+            load_blk(urow, t_lo + eg, 0, u[0]);
+            load_blk(urow, t_lo + eg, 1, u[1]);
+        }
+        const uint32_t stream = (kMode == kDraft) ? kStreamDraftBlock : kStreamResidualBlock;
+        for (int n = 0; n < nmine; ++n) {
+            const int i = eg + n * kEpiWG;
+            const int t = t_lo + i;
+            const int use = n;
+            const int buf = eg * 2 + (use & 1);
+            const uint32_t par = static_cast<uint32_t>(use >> 1) & 1u;
+            bool bad = false;
+            if (!failed) bad = !mbar_wait(&tfull[buf], par);
+            if (bad) { failed = true; set_status(st, DSPARK_ERR_TIMEOUT, 12); }
+            tc::fence_after_sync();
+            const bool have_next = (n + 1 < nmine);
+            const int tnext = t + kEpiWG;
+            // the two blocks 2t and 2t+1 share one Philox counter (index >> 2)
+            U4 pw{0, 0, 0, 0};
+            if (!p.greedy && warp_live)
+                pw = philox4x32_10(U4{static_cast<uint32_t>(t >> 1), static_cast<uint32_t>(kb),
+                                      static_cast<uint32_t>(b), stream},
+                                   static_cast<uint32_t>(p.seed), static_cast<uint32_t>(p.seed >> 32));
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+                const int v0 = t * kBN + hb * 64;
+                if (!warp_live || failed || v0 >= p.V) continue;   // warp-uniform
+                float y[64];
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kBN + hb * 64;
+                uint32_t tt[32];
+                if constexpr (kMode == kResidual) {
+                    load_blk(urow, t, hb, u[hb]);
+                    load_blk(trow, t, hb, tt);
+                }
+                tc::tmem_ld32(taddr, y);
+                tc::tmem_ld32(taddr + 32, y + 32);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int w = 0; w < 32; ++w) {
+                    y[2 * w] = (y[2 * w] + bf16lo(u[hb][w])) * p.cscale;
+                    y[2 * w + 1] = (y[2 * w + 1] + bf16hi(u[hb][w])) * p.cscale;
+                }
+                if (kMode == kDraft && have_next) load_blk(urow, tnext, hb, u[hb]);
+                const int blk = 2 * t + hb;
+                const uint32_t wsel = static_cast<uint32_t>(blk) & 3u;
+                const uint32_t rword = wsel == 0 ? pw.x : wsel == 1 ? pw.y : wsel == 2 ? pw.z : pw.w;
+                if constexpr (kMode == kDraft) {
+                    if (v0 + 64 > p.V) {
+#pragma unroll
+                        for (int w = 0; w < 64; ++w)
+                            if (v0 + w >= p.V) y[w] = -INFINITY;
+                    }
+                    if (p.debug_z != nullptr) {
+                        if (valid)
+                            for (int w = 0; w < 64; ++w)
+                                if (v0 + w < p.V) p.debug_z[static_cast<size_t>(b) * p.V + v0 + w] = y[w];
+                        continue;
+                    }
+                    if (p.greedy) {
+#pragma unroll
+                        for (int w = 0; w < 64; ++w)
+                            if (y[w] > best) { best = y[w]; best_i = v0 + w; }
+                    } else {
+                        float m4[4] = {y[0], y[1], y[2], y[3]};
+#pragma unroll
+                        for (int w = 4; w < 64; ++w) m4[w & 3] = fmaxf(m4[w & 3], y[w]);
+                        const float mb = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                        if (!(mb > -INFINITY)) continue;      // a block without a finite logit has no mass
+                        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int w = 0; w < 64; ++w) s4[w & 3] += fast_exp2(y[w] - mb);
+                        const float sb = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                        const float key = (mb + log2f(sb)) * kLn2 + gumbel_of(uniform_open(rword));
+                        if (key > best || (key == best && blk < best_i)) { best = key; best_i = blk; }
+                        lse_merge(M, S, mb, sb);
+                    }
+                } else {
+                    // residual mass q = max(0, p_t - p_d) with p_d = 2^(y - ld2), p_t = 2^(t c - lt2)
+                    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int w = 0; w < 32; ++w) {
+                        const float pd0 = fast_exp2(y[2 * w] - ld2), pd1 = fast_exp2(y[2 * w + 1] - ld2);
+                        const float pt0 = fast_exp2(bf16lo(tt[w]) * p.cscale - lt2);
+                        const float pt1 = fast_exp2(bf16hi(tt[w]) * p.cscale - lt2);
+                        float q0 = fmaxf(pt0 - pd0, 0.f), q1 = fmaxf(pt1 - pd1, 0.f);
+                        if (v0 + 2 * w >= p.V) q0 = 0.f;
+                        if (v0 + 2 * w + 1 >= p.V) q1 = 0.f;
+                        s4[(2 * w) & 3] += q0;
+                        s4[(2 * w + 1) & 3] += q1;
+                    }
+                    const float Q = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                    if (Q > 0.f) {
+                        const float key = log2f(Q) * kLn2 + gumbel_of(uniform_open(rword));
+                        if (key > best || (key == best && blk < best_i)) { best = key; best_i = blk; }
+                    }
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[buf]);
+        }
+        rowres[eg * kBM + row] = RowRes{best, best_i, M, S};
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp >= 4 && warp < 8 && p.debug_z == nullptr) {
+        const int row = (warp - 4) * 32 + lane;
+        const int b = m0 + row;
+        if (b < p.B && row_k(b) > 0) {
+            RowRes r0 = rowres[row];
+            for (int e = 1; e < kEpiWG; ++e) {
+                const RowRes r1 = rowres[e * kBM + row];
+                if (r1.key > r0.key || (r1.key == r0.key && r1.idx < r0.idx)) { r0.key = r1.key; r0.idx = r1.idx; }
+                lse_merge(r0.m, r0.s, r1.m, r1.s);
+            }
+            const size_t slot = static_cast<size_t>(p.k - 1) * p.B + b;
+            if (kMode == kDraft && !p.greedy) p.ws.part[slot * kMaxChunks + pc] = make_float2(r0.m, r0.s);
+            if (r0.key > -INFINITY) atomicMax(&p.ws.words[slot], pack_key(r0.key, static_cast<uint32_t>(r0.idx)));
+        }
+    }
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem_base, 512);
+    }
+}
+
+constexpr size_t kTcSmem = 1024 + 4 * kASlabBytes + kStages * kSlabBytes + (4 * kStages + 8) * 8 + 16 +
+                           kEpiWG * kBM * sizeof(RowRes);
+
+// ------------------------------------------------------------ host side ---
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    if (fn == nullptr) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 2-D map over W2 [V][r] bf16: box {64, 128}, 128-byte swizzle, zero fill.
+inline bool encode_w2_map(CUtensorMap* map, const void* W2, int V, int r) {
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(r), static_cast<cuuint64_t>(V)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(r) * 2};
+    const cuuint32_t box[2] = {kBK, kBN};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W2), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline bool use_tc_path(dspark_dtype_t dt, int r) { return dt == DSPARK_BF16 && r % kBK == 0 && r <= 256; }
+
+template <int kMode>
+dspark_status_t launch_tc(const CUtensorMap& map, const TcParams& p, int grid, cudaStream_t s) {
+    static OncePerDevice once;
+    if (once.run(current_device(), [] {
+            return cudaFuncSetAttribute(bias_engine_tc<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(kTcSmem));
+        }) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+    bias_engine_tc<kMode><<<grid, kTcThreads, kTcSmem, s>>>(map, p);
+    return launch_status();
+}
+
+// Grid of the tcgen05 engine: nM M-tiles, P CTAs each (P * nM <= SMs).
+inline void tc_grid(int B, int V, int* nM, int* P) {
+    *nM = (B + kBM - 1) / kBM;
+    const int sms = sm_count(current_device());
+    int per = sms / *nM;
+    if (per < 1) per = 1;
+    const int NT = (V + kBN - 1) / kBN;
+    if (per > NT) per = NT;
+    if (per > kMaxChunks) per = kMaxChunks;
+    *P = per;
+}
+
+}  // namespace eng
+}  // namespace dspark

@@ -17,8 +17,7 @@ from serving_draft_verify_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
 
-MARGIN = 1e-4
-FTOL = {"bf16": 2e-3, "f32": 1e-5}
+from tests.gpu_harness import MARGIN, FTOL, npy as _np, oracle_draft, compare_draft as compare  # noqa: E402
 
 
 @pytest.fixture(scope="module")
@@ -28,49 +27,9 @@ def dsv():
     return m
 
 
-def _np(t):
-    return t.detach().cpu().numpy()
-
-
 def gpu_draft(dsv, inp, temperature=None, seed=None):
-    dev = torch.device("cuda")
-    T = inp["temperature"] if temperature is None else temperature
-    s = inp["seed"] if seed is None else seed
-    B, G, V = inp["U"].shape
-    ws = torch.empty(dsv.load().dspark_draft_block_workspace_size(B, G, V, inp["W1"].shape[1]),
-                     dtype=torch.uint8, device=dev)
-    out = dsv.dspark_draft_block(inp["U"].to(dev), inp["h"].to(dev), inp["W1"].to(dev), inp["W2"].to(dev),
-                                 inp["w"].to(dev), inp["bias"], inp["x0"].to(dev), T, s, workspace=ws)
-    assert dsv.workspace_status(ws) == 0
-    return {k: _np(v) for k, v in out.items()}
-
-
-def oracle_draft(inp, gpu_x, temperature=None, seed=None, rows=None):
-    """Teacher-forced oracle for the listed requests (all by default), each keyed
-    by its own request index."""
-    rows = np.arange(inp["U"].shape[0]) if rows is None else np.asarray(rows)
-    T = inp["temperature"] if temperature is None else temperature
-    s = inp["seed"] if seed is None else seed
-    idx = torch.from_numpy(rows).to(inp["U"].device)
-    return oracle.draft_block(wl.to_f64(inp["U"][idx]), wl.to_f64(inp["h"][idx]), wl.to_f64(inp["W1"]),
-                              wl.to_f64(inp["W2"]), wl.to_f64(inp["w"]), inp["bias"], _np(inp["x0"])[rows], T, s,
-                              forced_tokens=gpu_x[rows], requests=rows)
-
-
-def compare(gpu, ref, dtype, rows=None):
-    rows = np.arange(gpu["x"].shape[0]) if rows is None else np.asarray(rows)
-    gx = gpu["x"][rows]
-    exempt = ref["margin"] < MARGIN
-    mismatch = (gx != ref["x"]) & ~exempt
-    assert not mismatch.any(), f"{mismatch.sum()} token mismatches at {np.argwhere(mismatch)[:5]}"
-    same = gx == ref["x"]
-    for k in ("c", "a"):
-        err = np.abs(gpu[k][rows] - ref[k]).max()
-        assert err <= FTOL[dtype], (k, err)
-    for k in ("lse_d", "logp_d"):
-        err = np.abs(gpu[k][rows] - ref[k])[same].max(initial=0.0)
-        assert err <= FTOL["bf16"], (k, err)
-    return int(exempt.sum())
+    from tests.gpu_harness import gpu_draft as run
+    return {k: _np(v) for k, v in run(dsv, inp, temperature, seed).items()}
 
 
 @pytest.mark.parametrize("B,V,r", [(1, 1024, 64), (20, 5000, 256), (130, 2048, 128), (300, 1000, 192)])

@@ -61,7 +61,9 @@ def test_tv_special_cases(dsv):
     t[4, 100] = -4.0
     for dt in (torch.float32, torch.bfloat16):
         got = dsv.dspark_accept_rate_tv(d.to(dt).cuda(), t.to(dt).cuda()).cpu().numpy()
-        assert abs(got[0] - 1.0) < 1e-5 and abs(got[1] - 1.0) < 1e-5
+        assert abs(got[0] - 1.0) < 1e-5
+        if dt == torch.float32:      # d + 3 rounded to bf16 is not an exact shift of d in bf16
+            assert abs(got[1] - 1.0) < 1e-5
         assert got[2] == 0.0
         assert abs(got[4] - 1.0) < 1e-6
         want = oracle.accept_rate_tv(wl.to_f64(d.to(dt)), wl.to_f64(t.to(dt)))
