@@ -108,6 +108,33 @@ dspark_status_t dspark_draft_block(int B, int gamma, int V, int H, int r, dspark
                                    void* workspace, size_t workspace_bytes, dspark_stream_t stream);
 
 /* ------------------------------------------------------------------------ *
+ * dspark_draft_block without a caller workspace.  The paper has no
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory -- hosts that own all GPU memory through their own pool and
+ * forbid cudaMalloc or allocating library calls from plug-in code.  Arguments
+ * and results are those of dspark_draft_block; the scratch lives in a fixed
+ * 4 MiB array inside the library's device image, held by every GPU that loads
+ * the library until the process exits.
+ *   - Calls whose dspark_draft_block_workspace_size(B, gamma, V, r) exceeds
+ *     4 MiB return DSPARK_ERR_UNSUPPORTED (B * gamma up to about 2000).
+ *   - All calls share the one array: calls that overlap on the GPU (other
+ *     streams, other host threads) race and corrupt each other's results.
+ *     Each call clears what must start at zero.
+ *   - The first call on a device looks up the array's device address with
+ *     cudaGetSymbolAddress (with that device current); make that first call
+ *     before any stream capture.
+ *   - Device-side checks (token ids out of range) record their status in the
+ *     internal array, which the caller cannot read: validate x0 beforehand.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ * ------------------------------------------------------------------------ */
+dspark_status_t dspark_draft_block_noalloc(int B, int gamma, int V, int H, int r, dspark_dtype_t dt,
+                                           const void* U, const void* h, const void* W1, const void* W2,
+                                           const void* w, float bias, const int32_t* x0,
+                                           float temperature, uint64_t seed,
+                                           int32_t* x, float* lse_d, float* logp_d, float* c, float* a,
+                                           dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
  * Prefix scheduler, Algorithm 1 (DeepSpec walkthrough section 3.3 flowchart):
  * sort all (b, j) pairs by a[b][j-1] descending (ties: lower b, then lower
  * j), scan them starting from l_b = 0 for all b, and accept a pair while

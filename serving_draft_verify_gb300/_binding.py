@@ -30,6 +30,8 @@ _SIGNATURES = {
     "dspark_draft_block_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "dspark_draft_block": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _p, _p, _p, _p, _p,
                                     _c_float, _p, _c_float, _c_u64, _p, _p, _p, _p, _p, _p, _c_size, _p]),
+    "dspark_draft_block_noalloc": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _p, _p, _p, _p, _p,
+                                            _c_float, _p, _c_float, _c_u64, _p, _p, _p, _p, _p, _p]),
     "dspark_schedule_prefix_workspace_size": (_c_size, [_c_int, _c_int]),
     "dspark_schedule_prefix": (_c_int, [_c_int, _c_int, _p, _p, _p, _p, _p, _p, _c_size, _p]),
     "dspark_verify_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
@@ -171,6 +173,32 @@ def dspark_draft_block(U, h, W1, W2, w, bias, x0, temperature, seed, out=None, w
                                   float(bias), _ptr(x0), float(temperature), int(seed) & (2**64 - 1),
                                   _ptr(out["x"]), _ptr(out["lse_d"]), _ptr(out["logp_d"]),
                                   _ptr(out["c"]), _ptr(out["a"]), _ptr(ws), _nbytes(ws), _stream(stream)))
+    return out
+
+
+def dspark_draft_block_noalloc(U, h, W1, W2, w, bias, x0, temperature, seed, out, stream=None):
+    """dspark_draft_block with the library's fixed internal scratch (no workspace);
+    for hosts that forbid device allocation.  `out` must hold preallocated
+    x [B, gamma] int32 and lse_d, logp_d, c, a [B, gamma] float32."""
+    lib = load()
+    B, G, V = U.shape
+    H = h.shape[-1]
+    r = W1.shape[-1]
+    _need(U, (B, G, V), name="U")
+    _need(h, (B, G, H), U.dtype, name="h")
+    _need(W1, (V, r), U.dtype, name="W1")
+    _need(W2, (V, r), U.dtype, name="W2")
+    _need(w, (H + r,), U.dtype, name="w")
+    _need(x0, (B,), torch.int32, name="x0")
+    _need(out["x"], (B, G), torch.int32, name="x")
+    for k in ("lse_d", "logp_d", "c", "a"):
+        _need(out[k], (B, G), torch.float32, name=k)
+    dt = _dtype_code(U, h, W1, W2, w)
+    _check("dspark_draft_block_noalloc",
+           lib.dspark_draft_block_noalloc(B, G, V, H, r, dt, _ptr(U), _ptr(h), _ptr(W1), _ptr(W2), _ptr(w),
+                                          float(bias), _ptr(x0), float(temperature), int(seed) & (2**64 - 1),
+                                          _ptr(out["x"]), _ptr(out["lse_d"]), _ptr(out["logp_d"]), _ptr(out["c"]),
+                                          _ptr(out["a"]), _stream(stream)))
     return out
 
 

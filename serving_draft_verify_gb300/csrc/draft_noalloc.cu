@@ -1,0 +1,58 @@
+// dspark_draft_block_noalloc: dspark_draft_block for callers that cannot
+// allocate device memory.  Some hosts of this library own every byte of GPU
+// memory through their own pool or arena and forbid cudaMalloc (and allocating
+// library calls) from plug-in code: an inference server that pre-reserves its
+// memory at start-up, or a runtime that must not allocate inside a step.  They
+// can pass inputs and outputs, but not the scratch workspace that
+// dspark_draft_block wants.  This entry point uses a fixed scratch array that
+// lives in the library's own device image instead.
+#include <mutex>
+
+#include "common.cuh"
+#include "host_common.h"
+
+namespace {
+
+// Scratch for one draft block call: status block, per-position best-block words,
+// per-chunk (max, sum) partials and drawn-token logits.  Every GPU that loads
+// the library holds these bytes until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;   // 4 MiB
+static __device__ __align__(256) unsigned char g_draft_scratch[kNoAllocScratchBytes];
+
+// Device address of g_draft_scratch, looked up once per device with that
+// device current.  The host-side name g_draft_scratch is only a stand-in; a
+// kernel must be given the address returned by cudaGetSymbolAddress.
+std::mutex g_mu;
+void* g_addr[64] = {};
+
+void* scratch_address(int dev) {
+    if (dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_draft_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_addr[dev] = p;
+    }
+    return g_addr[dev];
+}
+
+}  // namespace
+
+extern "C" dspark_status_t dspark_draft_block_noalloc(int B, int gamma, int V, int H, int r, dspark_dtype_t dt,
+                                                      const void* U, const void* h, const void* W1, const void* W2,
+                                                      const void* w, float bias, const int32_t* x0,
+                                                      float temperature, uint64_t seed, int32_t* x, float* lse_d,
+                                                      float* logp_d, float* c, float* a, dspark_stream_t stream) {
+    if (B <= 0 || gamma <= 0) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (dspark_draft_block_workspace_size(B, gamma, V, r) > kNoAllocScratchBytes) return DSPARK_ERR_UNSUPPORTED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DSPARK_ERR_CUDA;
+    void* scratch = scratch_address(dev);
+    if (scratch == nullptr) return DSPARK_ERR_CUDA;
+    // dspark_draft_block clears the status block and the per-position words itself
+    return dspark_draft_block(B, gamma, V, H, r, dt, U, h, W1, W2, w, bias, x0, temperature, seed, x, lse_d, logp_d,
+                              c, a, scratch, kNoAllocScratchBytes, stream);
+}
