@@ -27,14 +27,22 @@ dspark_status_t dspark_debug_draft_logits(int B, int V, int r, const void* U_k, 
 
 /* Measurement hook: while enabled, dspark_draft_block records a pair of CUDA
  * events (created by the library on the current device at the first enable)
- * around every phase-kernel launch, i.e. the vocabulary-wide pass that forms
- * z_k and its block keys for one position k.  dspark_debug_phase_times()
- * waits for the last recorded event and writes the duration in ms of each
- * phase launch of the most recent dspark_draft_block call into ms[0..n-1];
- * it returns the number of phases recorded (0 if timing is off).  Not
- * thread-safe; meant for benchmarks, one device at a time. */
+ * around every launch of its vocabulary-wide pass: the one cooperative
+ * tensor-core launch that covers all gamma positions, or, on the per-position
+ * path, each position's phase kernel.  dspark_debug_phase_times() waits for
+ * the last recorded event and writes the duration in ms of each such launch
+ * of the most recent dspark_draft_block call into ms[0..n-1]; it returns the
+ * number of launches recorded (1 for the cooperative launch, gamma on the
+ * per-position path, 0 if timing is off).  Not thread-safe; meant for
+ * benchmarks, one device at a time. */
 dspark_status_t dspark_debug_enable_phase_timing(int enable);
 int dspark_debug_phase_times(float* ms, int n);
+
+/* Test hook: while enabled, the tensor-core draft path launches one engine
+ * kernel and one winner kernel per position instead of the single
+ * cooperative launch (the path it takes anyway when its grid cannot be
+ * co-resident).  Results are identical either way.  Process-wide flag. */
+dspark_status_t dspark_debug_force_phase_launches(int enable);
 
 #ifdef __cplusplus
 }

@@ -42,6 +42,7 @@ _SIGNATURES = {
     "dspark_debug_draft_logits": (_c_int, [_c_int, _c_int, _c_int, _p, _p, _p, _p, _p, _p, _c_size, _p]),
     "dspark_debug_enable_phase_timing": (_c_int, [_c_int]),
     "dspark_debug_phase_times": (_c_int, [_p, _c_int]),
+    "dspark_debug_force_phase_launches": (_c_int, [_c_int]),
 }
 
 _lib = None
@@ -269,6 +270,12 @@ def dspark_debug_draft_logits(U_k, W1, W2, prev, z=None, workspace=None, stream=
 def phase_timing(enable):
     """Measurement hook: record CUDA events around every draft phase launch."""
     _check("dspark_debug_enable_phase_timing", load().dspark_debug_enable_phase_timing(1 if enable else 0))
+
+
+def force_phase_launches(enable):
+    """Test hook: the tensor-core draft path launches per position instead of
+    its single cooperative launch."""
+    _check("dspark_debug_force_phase_launches", load().dspark_debug_force_phase_launches(1 if enable else 0))
 
 
 def phase_times():

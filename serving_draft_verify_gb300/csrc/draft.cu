@@ -4,13 +4,15 @@
 //                      x_k ~ softmax(z_k / T)          (two-level Gumbel-max)
 // plus the confidence head and survival product (section 3.3).
 //
-// Per position k (x_k needs a vocabulary-wide reduction before k+1 starts):
-//   phase kernel   the bias engine (engine.cuh; tcgen05 for bf16 with
-//                  r % 64 == 0) or a CUDA-core kernel: per request, every
-//                  64-token block's logsumexp and Gumbel key, the CTA's best
-//                  block (atomicMax) and (max, sum) partial;
-//   winner kernel  two warps per request: z on the winning block only, and the
-//                  token inside it (second Gumbel level).
+// Tensor-core path (bf16, r % 64 == 0): one cooperative launch of the bias
+// engine (engine.cuh) runs every position; between positions its CTAs meet at
+// a grid barrier, draw x_{k-1} (second Gumbel level) for the requests each
+// owns, and meet again.  A winner kernel draws x_gamma.
+// CUDA-core path (and the tensor-core path when the grid cannot be
+// co-resident): per position a phase kernel (every 64-token block's
+// logsumexp and Gumbel key, the CTA's best block by atomicMax, its (max, sum)
+// partial) and a winner kernel (two warps per request: z on the winning block
+// and the token inside it).
 // After the last position a finalize kernel forms lse_d / logp_d and the
 // confidence c_k and survival a_k.
 #include "engine.cuh"
@@ -26,8 +28,13 @@ using eng::prev_token;
 using eng::unpack_idx;
 using DraftWs = eng::Ws;
 
-inline size_t draft_ws_layout(int B, int gamma, size_t* o_words, size_t* o_part, size_t* o_ytok) {
+// Workspace: status | grid-barrier counter | words [gamma][B] |
+// partials [gamma][B][kMaxChunks] | ytok [gamma][B].  The first three are
+// cleared by every call.
+inline size_t draft_ws_layout(int B, int gamma, size_t* o_bar, size_t* o_words, size_t* o_part, size_t* o_ytok) {
     size_t o = kStatusBytes;
+    *o_bar = o;
+    o += 256;
     *o_words = o;
     o += round_up(static_cast<size_t>(gamma) * B * 8, 256);
     *o_part = o;
@@ -35,6 +42,16 @@ inline size_t draft_ws_layout(int B, int gamma, size_t* o_words, size_t* o_part,
     *o_ytok = o;
     o += round_up(static_cast<size_t>(gamma) * B * 4, 256);
     return o;
+}
+
+inline DraftWs draft_ws(void* workspace, int B, int gamma, size_t* clear_bytes) {
+    size_t ob, ow, op, oy;
+    draft_ws_layout(B, gamma, &ob, &ow, &op, &oy);
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    *clear_bytes = op;
+    return DraftWs{reinterpret_cast<StatusBlock*>(wsb), reinterpret_cast<unsigned long long*>(wsb + ow),
+                   reinterpret_cast<float2*>(wsb + op), reinterpret_cast<float*>(wsb + oy),
+                   reinterpret_cast<unsigned int*>(wsb + ob)};
 }
 
 namespace {
@@ -138,6 +155,10 @@ draft_winner(int B, int gamma, int V, int r, int k, const void* __restrict__ U, 
         return;
     }
     const uint32_t idx = unpack_idx(word);
+    if (idx >= static_cast<uint32_t>(greedy ? V : (V + 63) / 64)) {   // never produced by the phase kernels
+        if (threadIdx.x == 0) { set_status(ws.status, DSPARK_ERR_DEVICE_CHECK, 8); x[b * gamma + k - 1] = 0; }
+        return;
+    }
     if (greedy) {
         if (threadIdx.x == 0) { x[b * gamma + k - 1] = static_cast<int>(idx); ws.ytok[slot] = 0.f; }
         return;
@@ -270,6 +291,19 @@ int simt_chunks(int V) {
     return n < 1 ? 1 : n;
 }
 
+bool g_force_phase_launches = false;
+
+template <bool kBF16>
+dspark_status_t launch_winner(int B, int gamma, int V, int r, int k, const void* U, const void* W1, const void* W2,
+                              const int32_t* x0, int32_t* x, float cscale, int greedy, uint64_t seed, DraftWs ws,
+                              cudaStream_t s) {
+    if (kBF16 || r <= 128)
+        draft_winner<kBF16, 1><<<B, 64, 0, s>>>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale, greedy, seed, ws);
+    else
+        draft_winner<kBF16, 2><<<B, 64, 0, s>>>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale, greedy, seed, ws);
+    return launch_status();
+}
+
 }  // namespace
 
 // Full draft block on `s`.
@@ -277,57 +311,68 @@ dspark_status_t draft_block_impl(int B, int gamma, int V, int H, int r, dspark_d
                                  const void* h, const void* W1, const void* W2, const void* w, float bias,
                                  const int32_t* x0, float temperature, uint64_t seed, int32_t* x, float* lse_d,
                                  float* logp_d, float* c, float* a, void* workspace, cudaStream_t s) {
-    size_t ow, op, oy;
-    draft_ws_layout(B, gamma, &ow, &op, &oy);
-    uint8_t* wsb = static_cast<uint8_t*>(workspace);
-    DraftWs ws{reinterpret_cast<StatusBlock*>(wsb), reinterpret_cast<unsigned long long*>(wsb + ow),
-               reinterpret_cast<float2*>(wsb + op), reinterpret_cast<float*>(wsb + oy)};
-    if (cudaMemsetAsync(wsb, 0, op, s) != cudaSuccess) return DSPARK_ERR_CUDA;   // status + words
+    size_t clear = 0;
+    const DraftWs ws = draft_ws(workspace, B, gamma, &clear);
+    if (cudaMemsetAsync(workspace, 0, clear, s) != cudaSuccess) return DSPARK_ERR_CUDA;   // status, barrier, words
     const int greedy = (temperature == 0.f);
     const float cscale = greedy ? 1.f : kLog2e / temperature;
     const bool tcp = eng::use_tc_path(dt, r);
+    const bool bf = (dt == DSPARK_BF16);
     CUtensorMap map;
     int nM = 1, P = 1, nchunk = 1;
+    eng::TcParams p{};
     if (tcp) {
         if (!eng::encode_w2_map(&map, W2, V, r)) return DSPARK_ERR_CUDA;
         eng::tc_grid(B, V, &nM, &P);
         nchunk = P;
+        p.B = B; p.gamma = gamma; p.V = V; p.r = r;
+        p.U = static_cast<const uint16_t*>(U); p.W1 = static_cast<const uint16_t*>(W1);
+        p.W2 = static_cast<const uint16_t*>(W2);
+        p.x0 = x0; p.x = x; p.cscale = cscale; p.greedy = greedy; p.seed = seed; p.P = P; p.ws = ws;
     } else {
         nchunk = simt_chunks(V);
     }
-    const bool bf = (dt == DSPARK_BF16);
-    for (int k = 1; k <= gamma; ++k) {
-        dspark_status_t stt;
-        if (g_timing.on) cudaEventRecord(g_timing.ev[2 * (k - 1)], s);
-        if (tcp) {
-            eng::TcParams p{};
-            p.B = B; p.gamma = gamma; p.V = V; p.r = r; p.k = k;
-            p.U = static_cast<const uint16_t*>(U); p.W1 = static_cast<const uint16_t*>(W1);
-            p.x0 = x0; p.x = x; p.cscale = cscale; p.greedy = greedy; p.seed = seed; p.P = P; p.ws = ws;
-            stt = eng::launch_tc<eng::kDraft>(map, p, nM * P, s);
-        } else {
-            dim3 grid(nchunk, B);
-            if (bf)
-                draft_phase_simt<true><<<grid, kSimtThreads, 0, s>>>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale,
-                                                                     greedy, seed, nchunk, ws);
-            else
-                draft_phase_simt<false><<<grid, kSimtThreads, 0, s>>>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale,
-                                                                      greedy, seed, nchunk, ws);
-            stt = launch_status();
-        }
+    const bool one_launch = tcp && !g_force_phase_launches && nM * P <= sm_count(current_device());
+    dspark_status_t stt = DSPARK_OK;
+    if (one_launch) {
+        // every position in one cooperative launch; x_1..x_{gamma-1} are drawn inside it
+        if (g_timing.on) cudaEventRecord(g_timing.ev[0], s);
+        p.k = 1;
+        p.k_last = gamma;
+        stt = eng::launch_tc<eng::kDraft>(map, p, nM * P, s, /*cooperative=*/gamma > 1);
         if (g_timing.on) {
-            cudaEventRecord(g_timing.ev[2 * (k - 1) + 1], s);
-            g_timing.recorded = k;
+            cudaEventRecord(g_timing.ev[1], s);
+            g_timing.recorded = 1;
         }
         if (stt != DSPARK_OK) return stt;
-        // chunks of 16 bytes per W2 row: up to 32 (bf16, r <= 256) or 64 (f32) -> 1 or 2 per lane
-        if (bf)
-            draft_winner<true, 1><<<B, 64, 0, s>>>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale, greedy, seed, ws);
-        else if (r <= 128)
-            draft_winner<false, 1><<<B, 64, 0, s>>>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale, greedy, seed, ws);
-        else
-            draft_winner<false, 2><<<B, 64, 0, s>>>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale, greedy, seed, ws);
-        if ((stt = launch_status()) != DSPARK_OK) return stt;
+        if ((stt = launch_winner<true>(B, gamma, V, r, gamma, U, W1, W2, x0, x, cscale, greedy, seed, ws, s)) !=
+            DSPARK_OK)
+            return stt;
+    } else {
+        for (int k = 1; k <= gamma; ++k) {
+            if (g_timing.on) cudaEventRecord(g_timing.ev[2 * (k - 1)], s);
+            if (tcp) {
+                p.k = p.k_last = k;
+                stt = eng::launch_tc<eng::kDraft>(map, p, nM * P, s, false);
+            } else {
+                dim3 grid(nchunk, B);
+                if (bf)
+                    draft_phase_simt<true><<<grid, kSimtThreads, 0, s>>>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale,
+                                                                         greedy, seed, nchunk, ws);
+                else
+                    draft_phase_simt<false><<<grid, kSimtThreads, 0, s>>>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale,
+                                                                          greedy, seed, nchunk, ws);
+                stt = launch_status();
+            }
+            if (g_timing.on) {
+                cudaEventRecord(g_timing.ev[2 * (k - 1) + 1], s);
+                g_timing.recorded = k;
+            }
+            if (stt != DSPARK_OK) return stt;
+            stt = bf ? launch_winner<true>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale, greedy, seed, ws, s)
+                     : launch_winner<false>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale, greedy, seed, ws, s);
+            if (stt != DSPARK_OK) return stt;
+        }
     }
     const int fthreads = 32 * gamma;
     if (bf)
@@ -348,17 +393,15 @@ dspark_status_t debug_tc_logits(int B, int V, int r, const void* U, const void* 
     if (!eng::encode_w2_map(&map, W2, V, r)) return DSPARK_ERR_CUDA;
     int nM, P;
     eng::tc_grid(B, V, &nM, &P);
-    size_t ow, op, oy;
-    draft_ws_layout(B, 1, &ow, &op, &oy);
-    uint8_t* wsb = static_cast<uint8_t*>(workspace);
-    DraftWs ws{reinterpret_cast<StatusBlock*>(wsb), reinterpret_cast<unsigned long long*>(wsb + ow),
-               reinterpret_cast<float2*>(wsb + op), reinterpret_cast<float*>(wsb + oy)};
-    if (cudaMemsetAsync(wsb, 0, 16, s) != cudaSuccess) return DSPARK_ERR_CUDA;
+    size_t clear = 0;
+    const DraftWs ws = draft_ws(workspace, B, 1, &clear);
+    if (cudaMemsetAsync(workspace, 0, clear, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     eng::TcParams p{};
-    p.B = B; p.gamma = 1; p.V = V; p.r = r; p.k = 1;
+    p.B = B; p.gamma = 1; p.V = V; p.r = r; p.k = 1; p.k_last = 1;
     p.U = static_cast<const uint16_t*>(U); p.W1 = static_cast<const uint16_t*>(W1);
+    p.W2 = static_cast<const uint16_t*>(W2);
     p.x0 = prev; p.x = nullptr; p.cscale = 1.f; p.greedy = 1; p.seed = 0; p.P = P; p.ws = ws; p.debug_z = z;
-    return eng::launch_tc<eng::kDraft>(map, p, nM * P, s);
+    return eng::launch_tc<eng::kDraft>(map, p, nM * P, s, false);
 }
 
 }  // namespace dspark
@@ -366,11 +409,11 @@ dspark_status_t debug_tc_logits(int B, int V, int r, const void* U, const void* 
 using namespace dspark;
 
 extern "C" size_t dspark_draft_block_workspace_size(int B, int gamma, int V, int r) {
-    (void)V;
     (void)r;
-    if (B <= 0 || gamma <= 0) return kStatusBytes;
-    size_t ow, op, oy;
-    return draft_ws_layout(B, gamma, &ow, &op, &oy);
+    (void)V;
+    if (B <= 0 || gamma <= 0 || V <= 0) return kStatusBytes;
+    size_t ob, ow, op, oy;
+    return draft_ws_layout(B, gamma, &ob, &ow, &op, &oy);
 }
 
 extern "C" dspark_status_t dspark_draft_block(int B, int gamma, int V, int H, int r, dspark_dtype_t dt,
@@ -410,6 +453,11 @@ extern "C" dspark_status_t dspark_debug_enable_phase_timing(int enable) {
     }
     g_timing.on = enable != 0;
     g_timing.recorded = 0;
+    return DSPARK_OK;
+}
+
+extern "C" dspark_status_t dspark_debug_force_phase_launches(int enable) {
+    g_force_phase_launches = enable != 0;
     return DSPARK_OK;
 }
 

@@ -18,7 +18,14 @@
 //   warps 4-11  two epilogue warpgroups, each with two TMEM accumulators, so
 //               the MMA of the next tile overlaps the epilogue of this one.
 // The A operand (rows W1[x_{k_b-1}], gathered into shared memory with the
-// same swizzle) is built once per launch.
+// same swizzle) is built by warps 1-11 at the start of every position.
+//
+// Draft launches may cover positions k .. k_last (a cooperative launch, all
+// CTAs resident, TMEM and barriers set up once, the producer streaming W2
+// straight through all positions).  Between positions the grid meets at a
+// bounded counter barrier; then CTA c draws x_{k} for requests b = c (mod
+// grid) from the published block winners (pairs of warps rebuild z on the
+// winning block from W2 rows), and the grid meets again before x_{k} is read.
 #pragma once
 
 #include <cuda.h>
@@ -40,6 +47,7 @@ struct Ws {
     unsigned long long* words;   // [positions][B] best (key, ~block) or (value, ~token)
     float2* part;                // [positions][B][kMaxChunks] (max, sum) of y = z log2e / T
     float* ytok;                 // [positions][B] y of the drawn token
+    unsigned int* gbar;          // grid-barrier counter of the multi-position draft launch (starts at 0)
 };
 
 // ------------------------------------------------------------ helpers ---
@@ -68,9 +76,10 @@ __device__ __forceinline__ void ld_u32x4(const void* p, uint32_t* o, uint64_t po
 }
 
 // Token x_{k-1} of request b (the anchor for k = 1), checked against [0, V).
+// x may have been written by other CTAs of a running grid: read it from L2.
 __device__ __forceinline__ int prev_token(const int32_t* x0, const int32_t* x, int b, int gamma, int k, int V,
                                           StatusBlock* st) {
-    const int t = (k == 1) ? x0[b] : x[b * gamma + k - 2];
+    const int t = (k == 1) ? x0[b] : __ldcg(x + b * gamma + k - 2);
     if (t < 0 || t >= V) {
         set_status(st, DSPARK_ERR_DEVICE_CHECK, 2);
         return 0;
@@ -174,7 +183,7 @@ __device__ __forceinline__ float block_logit(int b, int gamma, int k, int V, int
 constexpr int kBM = 128;              // request rows per M-tile (TMEM lanes)
 constexpr int kBN = 128;              // vocabulary columns per tile
 constexpr int kBK = 64;               // K per smem slab (128 bytes of bf16)
-constexpr int kStages = 6;            // W2 slab ring
+constexpr int kStages = 8;            // W2 slab ring
 constexpr int kEpiWG = 2;             // epilogue warpgroups, two TMEM buffers each
 constexpr int kTcThreads = 128 * (1 + kEpiWG);
 constexpr int kSlabBytes = kBN * kBK * 2;     // 16 KB
@@ -186,14 +195,16 @@ struct TcParams {
     int B, gamma, V, r, k;           // k: the position of every row (kDraft)
     const uint16_t* U;               // [B][gamma][V]
     const uint16_t* W1;              // [V][r]
+    const uint16_t* W2;              // [V][r] (the redraw of the winning block reads rows directly)
     const int32_t* x0;               // [B]
-    const int32_t* x;                // [B][gamma]
+    int32_t* x;                      // [B][gamma]; kDraft writes x_{k-1} here (CTA 0 of each M-tile)
     float cscale;                    // log2e / T (1 for greedy)
     int greedy;
     uint64_t seed;
     int P;                           // CTAs per M-tile
     Ws ws;
     float* debug_z;                  // kDraft: write y to [B][V] instead of reducing
+    int k_last;                      // kDraft: positions k .. k_last in one (cooperative) launch
     // kResidual
     const int32_t* krow;             // [B] rejected position k_b (0: row inactive)
     const uint16_t* T;               // t_logits [B][gamma+1][V]
@@ -206,6 +217,70 @@ struct RowRes {
     int idx;
     float m, s;
 };
+// Grid barrier of the multi-position draft launch (cooperative launch: every CTA
+// is resident).  Epoch e is complete once the counter reaches e * gridDim.x;
+// every CTA arrives once per epoch.  Waits are bounded (kWaitLimitNs).
+__device__ __forceinline__ void grid_arrive(unsigned int* ctr) {
+    __threadfence();
+    atomicAdd(ctr, 1u);
+}
+__device__ __forceinline__ bool grid_wait(const unsigned int* ctr, unsigned int target) {
+    auto load = [&]() {
+        unsigned int v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        return v;
+    };
+    if (load() >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (load() < target) {
+        __nanosleep(64);
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+// Draw x_k for request b inside a running multi-position launch: a pair of
+// warps (named barrier `bar`, 64 threads) rebuilds z on the winning block from
+// W2 rows and takes the second Gumbel level (stream 0); the even warp's lane 0
+// writes x and ytok.  xch/xchi: this pair's 2-entry exchange slots.
+__device__ __forceinline__ void pair_draw(const TcParams& p, int b, int k, int bar, float2* xch, int* xchi) {
+    const int lane = threadIdx.x & 31, wp = (threadIdx.x >> 5) & 1;
+    const size_t slot = static_cast<size_t>(k - 1) * p.B + b;
+    const unsigned long long word = __ldcg(p.ws.words + slot);
+    const uint32_t idx = unpack_idx(word);
+    const bool ok = word != 0ull && idx < static_cast<uint32_t>((p.V + 63) / 64);
+    float score = -INFINITY, yv = 0.f;
+    int bi = 0x7FFFFFFF;
+    if (ok) {
+        const int blk = static_cast<int>(idx);
+        const float z = block_logit<true, 1>(b, p.gamma, k, p.V, p.r, blk, p.U, p.W1, p.W2, p.x0, p.x, p.ws.status);
+        const int v = blk * 64 + wp * 32 + lane;
+        if (z > -INFINITY) {
+            yv = z * p.cscale;
+            const float g = gumbel_of(uniform_open(draw_word(p.seed, b, k, kStreamDraftToken, static_cast<uint32_t>(v))));
+            score = yv + g * kLog2e;
+            bi = v;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float os = __shfl_xor_sync(0xffffffffu, score, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        const float oy = __shfl_xor_sync(0xffffffffu, yv, o);
+        if (os > score || (os == score && oi < bi)) { score = os; bi = oi; yv = oy; }
+    }
+    if (lane == 0) { xch[wp] = make_float2(score, yv); xchi[wp] = bi; }
+    asm volatile("bar.sync %0, 64;" ::"r"(bar) : "memory");
+    if (wp == 0 && lane == 0) {
+        int w = 0;
+        if (xch[1].x > xch[0].x || (xch[1].x == xch[0].x && xchi[1] < xchi[0])) w = 1;
+        int tok = xchi[w];
+        if (tok == 0x7FFFFFFF) { set_status(p.ws.status, DSPARK_ERR_DEVICE_CHECK, 3); tok = 0; }
+        p.x[b * p.gamma + k - 1] = tok;
+        p.ws.ytok[slot] = xch[w].y;
+    }
+    asm volatile("bar.sync %0, 64;" ::"r"(bar) : "memory");
+}
 
 template <int kMode>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -222,6 +297,10 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
     uint64_t* tempty = tfull + 2 * kEpiWG;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2 * kEpiWG);
     RowRes* rowres = reinterpret_cast<RowRes*>(tmem_slot + 4);   // [kEpiWG][128]
+    int* s_prev = reinterpret_cast<int*>(rowres + kEpiWG * kBM);   // [128] x_{k-1} per request row
+    float2* xch = reinterpret_cast<float2*>(s_prev + kBM);        // [10] pair exchange
+    int* xchi = reinterpret_cast<int*>(xch + 10);                 // [10]
+    int* s_fail = xchi + 10;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = blockIdx.x / p.P, pc = blockIdx.x % p.P;
@@ -231,251 +310,336 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
     const int t_hi = static_cast<int>(static_cast<long long>(pc + 1) * NT / p.P);
     const int ntiles = t_hi - t_lo;
     StatusBlock* st = p.ws.status;
-    auto row_k = [&](int b) -> int { return (kMode == kResidual) ? p.krow[b] : p.k; };
+    // Row replication: with at most 64 requests the A tile holds every request
+    // twice (TMEM lanes 0-63 and 64-127) and the two copies reduce different
+    // 64-token blocks of each tile, so all epilogue warps have work.
+    const int R = (kMode == kDraft && p.B <= 64) ? 2 : 1;
+    const int rpc = kBM / R;                              // request rows per copy
+    const int nrows = min(rpc, p.B - m0);                 // requests of this M-tile
+    const int k0 = p.k;
+    const int k1 = (kMode == kDraft && p.k_last > p.k) ? p.k_last : p.k;
+    const bool multi = k1 > k0;                           // positions k0..k1, grid barriers between
+    auto row_k = [&](int b, int k) -> int { return (kMode == kResidual) ? p.krow[b] : k; };
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
         for (int e = 0; e < 2 * kEpiWG; ++e) { mbar_init(&tfull[e], 1); mbar_init(&tempty[e], 4); }
+        *s_fail = 0;
         fence_mbar_init();
         tc::prefetch_tmap(&tmW2);
     }
     if (warp == 1) tc::tmem_alloc(tmem_slot, 512);
-
-    // A operand: rows W1[x_{k_b-1}] of this M-tile, K-major, 128-byte swizzle
-    {
-        const int cpr = p.r / 8;                          // 16-byte chunks per row
-        for (int idx = tid; idx < kBM * cpr; idx += kTcThreads) {
-            const int row = idx / cpr, c16 = idx % cpr;
-            const int slab = c16 >> 3, c = c16 & 7;
-            const int b = m0 + row;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (b < p.B) {
-                const int kb = row_k(b);
-                if (kb > 0) {
-                    const int prev = prev_token(p.x0, p.x, b, p.gamma, kb, p.V, st);
-                    v = *reinterpret_cast<const uint4*>(p.W1 + static_cast<size_t>(prev) * p.r + c16 * 8);
-                }
-            }
-            uint8_t* dst = sA + slab * kASlabBytes + (row >> 3) * 1024 + (row & 7) * 128 + ((c ^ (row & 7)) << 4);
-            *reinterpret_cast<uint4*>(dst) = v;
-        }
-    }
-    fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
-    bool failed = false;
 
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer
+        // streams W2 for every position without waiting for the prologues
         if (lane == 0) {
             const uint64_t pol = policy_evict_last();
             int stage = 0;
             uint32_t phase = 0;
-            for (int t = t_lo; t < t_hi && !failed; ++t) {
-                for (int s = 0; s < nslab; ++s) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u)) { failed = true; break; }
-                    mbar_arrive_expect_tx(&full[stage], kSlabBytes);
-                    tc::tma_load_2d(sB + stage * kSlabBytes, &tmW2, s * kBK, t * kBN, &full[stage], pol);
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
-                }
-            }
+            bool failed = false;
+            for (int k = k0; k <= k1 && !failed; ++k)
+                for (int t = t_lo; t < t_hi && !failed; ++t)
+                    for (int s = 0; s < nslab; ++s) {
+                        if (!mbar_wait(&empty[stage], phase ^ 1u)) { failed = true; break; }
+                        mbar_arrive_expect_tx(&full[stage], kSlabBytes);
+                        tc::tma_load_2d(sB + stage * kSlabBytes, &tmW2, s * kBK, t * kBN, &full[stage], pol);
+                        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    }
             if (failed) set_status(st, DSPARK_ERR_TIMEOUT, 10);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN);
-            const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
-            int stage = 0;
-            uint32_t phase = 0;
-            for (int i = 0; i < ntiles && !failed; ++i) {
-                const int eg = i % kEpiWG, use = i / kEpiWG;
-                const int buf = eg * 2 + (use & 1);
-                const uint32_t par = static_cast<uint32_t>(use >> 1) & 1u;
-                if (!mbar_wait(&tempty[buf], par ^ 1u)) { failed = true; break; }
-                tc::fence_after_sync();
-                const uint32_t d = tmem_base + static_cast<uint32_t>(buf * kBN);
-                for (int s = 0; s < nslab; ++s) {
-                    if (!mbar_wait(&full[stage], phase)) { failed = true; break; }
-                    tc::fence_after_sync();
-#pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t ad = tc::smem_desc_sw128(a0 + s * kASlabBytes + kk * 32);
-                        const uint64_t bd = tc::smem_desc_sw128(b0 + stage * kSlabBytes + kk * 32);
-                        tc::mma_bf16(d, ad, bd, idesc, (s | kk) != 0);
-                    }
-                    tc::commit(&empty[stage]);
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
-                }
-                tc::commit(&tfull[buf]);
-            }
-            if (failed) set_status(st, DSPARK_ERR_TIMEOUT, 11);
-        }
-    } else if (warp >= 4) {
-        // -------------------------------------------------------- epilogue
-        const int eg = (warp - 4) >> 2;                   // warpgroup 0..kEpiWG-1
-        const int q = warp & 3;                           // TMEM lane quarter
-        const int row = q * 32 + lane;
-        const int b = m0 + row;
-        const int kb = (b < p.B) ? row_k(b) : 0;
-        const bool valid = b < p.B && kb > 0;
-        const bool warp_live = (m0 + q * 32) < p.B;
-        const uint64_t pol = policy_evict_first();
-        const size_t urow_off = (static_cast<size_t>(valid ? b : 0) * p.gamma + (valid ? kb - 1 : 0)) * p.V;
-        const uint16_t* urow = p.U + urow_off;
-        float ld2 = 0.f, lt2 = 0.f;
-        const uint16_t* trow = nullptr;
-        if constexpr (kMode == kResidual) {
-            if (valid) {
-                ld2 = p.ld2[b];
-                lt2 = p.lt2[b];
-                trow = p.T + (static_cast<size_t>(b) * (p.gamma + 1) + (kb - 1)) * p.V;
-            }
-        }
-        float best = -INFINITY, M = -INFINITY, S = 0.f;
-        int best_i = 0x7FFFFFFF;
-        const int nmine = (ntiles > eg) ? (ntiles - eg + kEpiWG - 1) / kEpiWG : 0;
-
-        uint32_t u[2][32];                                // U of the two 64-token blocks of one tile
-        auto load_blk = [&](const uint16_t* base, int t, int hb, uint32_t* dst) {
-            const int v0 = t * kBN + hb * 64;
-#pragma unroll
-            for (int g8 = 0; g8 < 8; ++g8) {
-                if (valid && v0 + g8 * 8 < p.V) ld_u32x4(base + v0 + g8 * 8, dst + g8 * 4, pol);
-                else { dst[g8 * 4] = dst[g8 * 4 + 1] = dst[g8 * 4 + 2] = dst[g8 * 4 + 3] = 0u; }
-            }
+        __syncwarp();
+    } else {
+        constexpr int kPro = kTcThreads - 32;             // warps 1.. : prologue, MMA, epilogue
+        const int ptid = tid - 32;
+        auto pro_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(kPro) : "memory"); };
+        unsigned int epoch = 0;                           // grid-barrier epochs this CTA has arrived at
+        auto arrive = [&] {
+            pro_sync();                                   // this CTA's writes of the step are done
+            if (ptid == 0) grid_arrive(p.ws.gbar);
+            ++epoch;
         };
-        if (kMode == kDraft && nmine > 0 && warp_live) {
-            load_blk(urow, t_lo + eg, 0, u[0]);
-            load_blk(urow, t_lo + eg, 1, u[1]);
-        }
-        const uint32_t stream = (kMode == kDraft) ? kStreamDraftBlock : kStreamResidualBlock;
-        for (int n = 0; n < nmine; ++n) {
-            const int i = eg + n * kEpiWG;
-            const int t = t_lo + i;
-            const int use = n;
-            const int buf = eg * 2 + (use & 1);
-            const uint32_t par = static_cast<uint32_t>(use >> 1) & 1u;
-            bool bad = false;
-            if (!failed) bad = !mbar_wait(&tfull[buf], par);
-            if (bad) { failed = true; set_status(st, DSPARK_ERR_TIMEOUT, 12); }
-            tc::fence_after_sync();
-            const bool have_next = (n + 1 < nmine);
-            const int tnext = t + kEpiWG;
-            // the two blocks 2t and 2t+1 share one Philox counter (index >> 2)
-            U4 pw{0, 0, 0, 0};
-            if (!p.greedy && warp_live)
-                pw = philox4x32_10(U4{static_cast<uint32_t>(t >> 1), static_cast<uint32_t>(kb),
-                                      static_cast<uint32_t>(b), stream},
-                                   static_cast<uint32_t>(p.seed), static_cast<uint32_t>(p.seed >> 32));
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {
-                const int v0 = t * kBN + hb * 64;
-                if (!warp_live || failed || v0 >= p.V) continue;   // warp-uniform
-                float y[64];
-                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kBN + hb * 64;
-                uint32_t tt[32];
-                if constexpr (kMode == kResidual) {
-                    load_blk(urow, t, hb, u[hb]);
-                    load_blk(trow, t, hb, tt);
-                }
-                tc::tmem_ld32(taddr, y);
-                tc::tmem_ld32(taddr + 32, y + 32);
-                tc::tmem_ld_wait();
-#pragma unroll
-                for (int w = 0; w < 32; ++w) {
-                    y[2 * w] = (y[2 * w] + bf16lo(u[hb][w])) * p.cscale;
-                    y[2 * w + 1] = (y[2 * w + 1] + bf16hi(u[hb][w])) * p.cscale;
-                }
-                if (kMode == kDraft && have_next) load_blk(urow, tnext, hb, u[hb]);
-                const int blk = 2 * t + hb;
-                const uint32_t wsel = static_cast<uint32_t>(blk) & 3u;
-                const uint32_t rword = wsel == 0 ? pw.x : wsel == 1 ? pw.y : wsel == 2 ? pw.z : pw.w;
-                if constexpr (kMode == kDraft) {
-                    if (v0 + 64 > p.V) {
-#pragma unroll
-                        for (int w = 0; w < 64; ++w)
-                            if (v0 + w >= p.V) y[w] = -INFINITY;
+        auto wait_all = [&] {
+            if (ptid == 0 && *s_fail == 0 && !grid_wait(p.ws.gbar, epoch * gridDim.x)) {
+                set_status(st, DSPARK_ERR_TIMEOUT, 13);
+                *s_fail = 1;
+            }
+            pro_sync();
+        };
+        // per-thread pipeline state that continues across positions
+        int mma_stage = 0;
+        uint32_t mma_phase = 0;
+        bool failed = false;
+
+        for (int k = k0; k <= k1; ++k) {
+            const int base = (k - k0) * ntiles;           // running index of this position's first tile
+            // ---------------------------------------------- prologue: x_{k-1}
+            if (kMode == kDraft && multi && k > k0) {
+                wait_all();                               // every CTA published position k-1
+                if (!p.greedy) {
+                    // second Gumbel level for x_{k-1}, spread over the grid: requests
+                    // b = blockIdx + j * gridDim, one pair of warps per request
+                    if (warp >= 2 && *s_fail == 0) {
+                        const int pair = (warp - 2) >> 1;
+                        for (int b = blockIdx.x + pair * gridDim.x; b < p.B; b += 5 * gridDim.x)
+                            pair_draw(p, b, k - 1, 2 + pair, xch + 2 * pair, xchi + 2 * pair);
                     }
-                    if (p.debug_z != nullptr) {
-                        if (valid)
-                            for (int w = 0; w < 64; ++w)
-                                if (v0 + w < p.V) p.debug_z[static_cast<size_t>(b) * p.V + v0 + w] = y[w];
-                        continue;
-                    }
-                    if (p.greedy) {
-#pragma unroll
-                        for (int w = 0; w < 64; ++w)
-                            if (y[w] > best) { best = y[w]; best_i = v0 + w; }
-                    } else {
-                        float m4[4] = {y[0], y[1], y[2], y[3]};
-#pragma unroll
-                        for (int w = 4; w < 64; ++w) m4[w & 3] = fmaxf(m4[w & 3], y[w]);
-                        const float mb = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-                        if (!(mb > -INFINITY)) continue;      // a block without a finite logit has no mass
-                        float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                        for (int w = 0; w < 64; ++w) s4[w & 3] += fast_exp2(y[w] - mb);
-                        const float sb = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-                        const float key = (mb + log2f(sb)) * kLn2 + gumbel_of(uniform_open(rword));
-                        if (key > best || (key == best && blk < best_i)) { best = key; best_i = blk; }
-                        lse_merge(M, S, mb, sb);
-                    }
+                    arrive();
+                    wait_all();                           // every x_{k-1} is written
+                    for (int rr = ptid; rr < nrows; rr += kPro)
+                        s_prev[rr] = prev_token(p.x0, p.x, m0 + rr, p.gamma, k, p.V, st);
                 } else {
-                    // residual mass q = max(0, p_t - p_d) with p_d = 2^(y - ld2), p_t = 2^(t c - lt2)
-                    float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int w = 0; w < 32; ++w) {
-                        const float pd0 = fast_exp2(y[2 * w] - ld2), pd1 = fast_exp2(y[2 * w + 1] - ld2);
-                        const float pt0 = fast_exp2(bf16lo(tt[w]) * p.cscale - lt2);
-                        const float pt1 = fast_exp2(bf16hi(tt[w]) * p.cscale - lt2);
-                        float q0 = fmaxf(pt0 - pd0, 0.f), q1 = fmaxf(pt1 - pd1, 0.f);
-                        if (v0 + 2 * w >= p.V) q0 = 0.f;
-                        if (v0 + 2 * w + 1 >= p.V) q1 = 0.f;
-                        s4[(2 * w) & 3] += q0;
-                        s4[(2 * w + 1) & 3] += q1;
+                    for (int rr = ptid; rr < nrows; rr += kPro) {
+                        const int b = m0 + rr;
+                        const unsigned long long w = __ldcg(p.ws.words + static_cast<size_t>(k - 2) * p.B + b);
+                        const uint32_t idx = unpack_idx(w);
+                        int tok = static_cast<int>(idx);
+                        if (w == 0ull || idx >= static_cast<uint32_t>(p.V)) {
+                            set_status(st, DSPARK_ERR_DEVICE_CHECK, 3);
+                            tok = 0;
+                        }
+                        s_prev[rr] = tok;
+                        if (pc == 0) p.x[b * p.gamma + k - 2] = tok;
                     }
-                    const float Q = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-                    if (Q > 0.f) {
-                        const float key = log2f(Q) * kLn2 + gumbel_of(uniform_open(rword));
-                        if (key > best || (key == best && blk < best_i)) { best = key; best_i = blk; }
-                    }
+                }
+            } else {
+                for (int rr = ptid; rr < nrows; rr += kPro) {
+                    const int b = m0 + rr;
+                    const int kb = row_k(b, k);
+                    s_prev[rr] = (kb > 0) ? prev_token(p.x0, p.x, b, p.gamma, kb, p.V, st) : -1;
                 }
             }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[buf]);
+            pro_sync();
+            failed = failed || (*s_fail != 0);
+
+            // A operand: rows W1[x_{k_b-1}] of this M-tile, K-major, 128-byte swizzle
+            {
+                const int cpr = p.r / 8;                  // 16-byte chunks per row
+                for (int idx = ptid; idx < kBM * cpr; idx += kPro) {
+                    const int row = idx / cpr, c16 = idx % cpr;
+                    const int slab = c16 >> 3, c = c16 & 7;
+                    const int rr = row % rpc;
+                    uint4 v = make_uint4(0, 0, 0, 0);
+                    if (rr < nrows) {
+                        const int prev = s_prev[rr];
+                        if (prev >= 0)
+                            v = *reinterpret_cast<const uint4*>(p.W1 + static_cast<size_t>(prev) * p.r + c16 * 8);
+                    }
+                    uint8_t* dst = sA + slab * kASlabBytes + (row >> 3) * 1024 + (row & 7) * 128 + ((c ^ (row & 7)) << 4);
+                    *reinterpret_cast<uint4*>(dst) = v;
+                }
+                fence_proxy_async_smem();
+                tc::fence_before_sync();
+                pro_sync();
+                tc::fence_after_sync();
+            }
+
+            if (warp == 1) {
+                // -------------------------------------------------- MMA issuer
+                if (lane == 0) {
+                    constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN);
+                    const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+                    for (int i = 0; i < ntiles && !failed; ++i) {
+                        const int gi = base + i;
+                        const int eg = gi % kEpiWG, use = gi / kEpiWG;
+                        const int buf = eg * 2 + (use & 1);
+                        const uint32_t par = static_cast<uint32_t>(use >> 1) & 1u;
+                        if (!mbar_wait(&tempty[buf], par ^ 1u)) { failed = true; break; }
+                        tc::fence_after_sync();
+                        const uint32_t d = tmem_base + static_cast<uint32_t>(buf * kBN);
+                        for (int s = 0; s < nslab; ++s) {
+                            if (!mbar_wait(&full[mma_stage], mma_phase)) { failed = true; break; }
+                            tc::fence_after_sync();
+#pragma unroll
+                            for (int kk = 0; kk < kBK / 16; ++kk) {
+                                const uint64_t ad = tc::smem_desc_sw128(a0 + s * kASlabBytes + kk * 32);
+                                const uint64_t bd = tc::smem_desc_sw128(b0 + mma_stage * kSlabBytes + kk * 32);
+                                tc::mma_bf16(d, ad, bd, idesc, (s | kk) != 0);
+                            }
+                            tc::commit(&empty[mma_stage]);
+                            if (++mma_stage == kStages) { mma_stage = 0; mma_phase ^= 1u; }
+                        }
+                        tc::commit(&tfull[buf]);
+                    }
+                    if (failed) set_status(st, DSPARK_ERR_TIMEOUT, 11);
+                }
+                __syncwarp();
+            } else if (warp >= 4) {
+                // ---------------------------------------------------- epilogue
+                const int eg = (warp - 4) >> 2;           // warpgroup 0..kEpiWG-1
+                const int q = warp & 3;                   // TMEM lane quarter
+                const int lrow = q * 32 + lane;           // TMEM lane = A row
+                const int copy = lrow / rpc;              // which copy of the request rows
+                const int rr = lrow % rpc;                // request row within the M-tile
+                const int b = m0 + rr;
+                const int kb = (rr < nrows) ? row_k(b, k) : 0;
+                const bool valid = rr < nrows && kb > 0;
+                const bool warp_live = ((q * 32) % rpc) < nrows;
+                const uint64_t pol = policy_evict_first();
+                const uint16_t* urow = p.U + (static_cast<size_t>(valid ? b : 0) * p.gamma + (valid ? kb - 1 : 0)) * p.V;
+                float ld2 = 0.f, lt2 = 0.f;
+                const uint16_t* trow = nullptr;
+                if constexpr (kMode == kResidual) {
+                    if (valid) {
+                        ld2 = p.ld2[b];
+                        lt2 = p.lt2[b];
+                        trow = p.T + (static_cast<size_t>(b) * (p.gamma + 1) + (kb - 1)) * p.V;
+                    }
+                }
+                float best = -INFINITY, M = -INFINITY, S = 0.f;
+                int best_i = 0x7FFFFFFF;
+                const int i0 = ((eg - base) % kEpiWG + kEpiWG) % kEpiWG;   // this WG's first local tile
+
+                uint32_t u[2][32];                        // U of the two 64-token blocks of one tile
+                auto load_blk = [&](const uint16_t* src, int t, int hb, uint32_t* dst) {
+                    const int v0 = t * kBN + hb * 64;
+#pragma unroll
+                    for (int g8 = 0; g8 < 8; ++g8) {
+                        if (valid && v0 + g8 * 8 < p.V) ld_u32x4(src + v0 + g8 * 8, dst + g8 * 4, pol);
+                        else { dst[g8 * 4] = dst[g8 * 4 + 1] = dst[g8 * 4 + 2] = dst[g8 * 4 + 3] = 0u; }
+                    }
+                };
+                auto mine = [&](int hb) -> bool { return R == 1 || hb == copy; };
+                if (kMode == kDraft && i0 < ntiles && warp_live) {
+                    if (mine(0)) load_blk(urow, t_lo + i0, 0, u[0]);
+                    if (mine(1)) load_blk(urow, t_lo + i0, 1, u[1]);
+                }
+                const uint32_t stream = (kMode == kDraft) ? kStreamDraftBlock : kStreamResidualBlock;
+                for (int i = i0; i < ntiles; i += kEpiWG) {
+                    const int t = t_lo + i;
+                    const int use = (base + i) / kEpiWG;
+                    const int buf = eg * 2 + (use & 1);
+                    const uint32_t par = static_cast<uint32_t>(use >> 1) & 1u;
+                    bool bad = false;
+                    if (!failed) bad = !mbar_wait(&tfull[buf], par);
+                    if (bad) { failed = true; set_status(st, DSPARK_ERR_TIMEOUT, 12); }
+                    tc::fence_after_sync();
+                    const bool have_next = (i + kEpiWG < ntiles);
+                    const int tnext = t + kEpiWG;
+                    // the two blocks 2t and 2t+1 share one Philox counter (index >> 2)
+                    U4 pw{0, 0, 0, 0};
+                    if (!p.greedy && warp_live)
+                        pw = philox4x32_10(U4{static_cast<uint32_t>(t >> 1), static_cast<uint32_t>(kb),
+                                              static_cast<uint32_t>(b), stream},
+                                           static_cast<uint32_t>(p.seed), static_cast<uint32_t>(p.seed >> 32));
+#pragma unroll
+                    for (int hb = 0; hb < 2; ++hb) {
+                        const int v0 = t * kBN + hb * 64;
+                        if (!mine(hb) || !warp_live || failed || v0 >= p.V) continue;   // warp-uniform
+                        float y[64];
+                        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kBN + hb * 64;
+                        uint32_t tt[32];
+                        if constexpr (kMode == kResidual) {
+                            load_blk(urow, t, hb, u[hb]);
+                            load_blk(trow, t, hb, tt);
+                        }
+                        tc::tmem_ld32(taddr, y);
+                        tc::tmem_ld32(taddr + 32, y + 32);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int w = 0; w < 32; ++w) {
+                            y[2 * w] = (y[2 * w] + bf16lo(u[hb][w])) * p.cscale;
+                            y[2 * w + 1] = (y[2 * w + 1] + bf16hi(u[hb][w])) * p.cscale;
+                        }
+                        if (kMode == kDraft && have_next) load_blk(urow, tnext, hb, u[hb]);
+                        const int blk = 2 * t + hb;
+                        const uint32_t wsel = static_cast<uint32_t>(blk) & 3u;
+                        const uint32_t rword = wsel == 0 ? pw.x : wsel == 1 ? pw.y : wsel == 2 ? pw.z : pw.w;
+                        if constexpr (kMode == kDraft) {
+                            if (v0 + 64 > p.V) {
+#pragma unroll
+                                for (int w = 0; w < 64; ++w)
+                                    if (v0 + w >= p.V) y[w] = -INFINITY;
+                            }
+                            if (p.debug_z != nullptr) {
+                                if (valid)                // copies own disjoint blocks
+                                    for (int w = 0; w < 64; ++w)
+                                        if (v0 + w < p.V) p.debug_z[static_cast<size_t>(b) * p.V + v0 + w] = y[w];
+                                continue;
+                            }
+                            if (p.greedy) {
+#pragma unroll
+                                for (int w = 0; w < 64; ++w)
+                                    if (y[w] > best) { best = y[w]; best_i = v0 + w; }
+                            } else {
+                                float m4[4] = {y[0], y[1], y[2], y[3]};
+#pragma unroll
+                                for (int w = 4; w < 64; ++w) m4[w & 3] = fmaxf(m4[w & 3], y[w]);
+                                const float mb = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                                if (!(mb > -INFINITY)) continue;   // a block without a finite logit has no mass
+                                float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                                for (int w = 0; w < 64; ++w) s4[w & 3] += fast_exp2(y[w] - mb);
+                                const float sb = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                                const float key = (mb + log2f(sb)) * kLn2 + gumbel_of(uniform_open(rword));
+                                if (key > best || (key == best && blk < best_i)) { best = key; best_i = blk; }
+                                lse_merge(M, S, mb, sb);
+                            }
+                        } else {
+                            // residual mass q = max(0, p_t - p_d), p_d = 2^(y - ld2), p_t = 2^(t c - lt2)
+                            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                            for (int w = 0; w < 32; ++w) {
+                                const float pd0 = fast_exp2(y[2 * w] - ld2), pd1 = fast_exp2(y[2 * w + 1] - ld2);
+                                const float pt0 = fast_exp2(bf16lo(tt[w]) * p.cscale - lt2);
+                                const float pt1 = fast_exp2(bf16hi(tt[w]) * p.cscale - lt2);
+                                float q0 = fmaxf(pt0 - pd0, 0.f), q1 = fmaxf(pt1 - pd1, 0.f);
+                                if (v0 + 2 * w >= p.V) q0 = 0.f;
+                                if (v0 + 2 * w + 1 >= p.V) q1 = 0.f;
+                                s4[(2 * w) & 3] += q0;
+                                s4[(2 * w + 1) & 3] += q1;
+                            }
+                            const float Q = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                            if (Q > 0.f) {
+                                const float key = log2f(Q) * kLn2 + gumbel_of(uniform_open(rword));
+                                if (key > best || (key == best && blk < best_i)) { best = key; best_i = blk; }
+                            }
+                        }
+                    }
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[buf]);
+                }
+                rowres[eg * kBM + lrow] = RowRes{best, best_i, M, S};
+            }
+            pro_sync();
+
+            // --------------------------------------- publish this position
+            if (warp >= 4 && warp < 8 && p.debug_z == nullptr) {
+                const int rr = (warp - 4) * 32 + lane;
+                const int b = m0 + rr;
+                if (rr < nrows && row_k(b, k) > 0) {
+                    RowRes r0{-INFINITY, 0x7FFFFFFF, -INFINITY, 0.f};
+                    for (int e = 0; e < kEpiWG; ++e)
+                        for (int c = 0; c < R; ++c) {
+                            const RowRes r1 = rowres[e * kBM + c * rpc + rr];
+                            if (r1.key > r0.key || (r1.key == r0.key && r1.idx < r0.idx)) { r0.key = r1.key; r0.idx = r1.idx; }
+                            lse_merge(r0.m, r0.s, r1.m, r1.s);
+                        }
+                    const size_t slot = static_cast<size_t>(k - 1) * p.B + b;
+                    if (kMode == kDraft && !p.greedy) p.ws.part[slot * kMaxChunks + pc] = make_float2(r0.m, r0.s);
+                    if (r0.key > -INFINITY) atomicMax(&p.ws.words[slot], pack_key(r0.key, static_cast<uint32_t>(r0.idx)));
+                }
+            }
+            if (kMode == kDraft && multi && k < k1) arrive();
+            else pro_sync();                              // rowres is rewritten by the next position
         }
-        rowres[eg * kBM + row] = RowRes{best, best_i, M, S};
     }
 
     tc::fence_before_sync();
     __syncthreads();
-    if (warp >= 4 && warp < 8 && p.debug_z == nullptr) {
-        const int row = (warp - 4) * 32 + lane;
-        const int b = m0 + row;
-        if (b < p.B && row_k(b) > 0) {
-            RowRes r0 = rowres[row];
-            for (int e = 1; e < kEpiWG; ++e) {
-                const RowRes r1 = rowres[e * kBM + row];
-                if (r1.key > r0.key || (r1.key == r0.key && r1.idx < r0.idx)) { r0.key = r1.key; r0.idx = r1.idx; }
-                lse_merge(r0.m, r0.s, r1.m, r1.s);
-            }
-            const size_t slot = static_cast<size_t>(p.k - 1) * p.B + b;
-            if (kMode == kDraft && !p.greedy) p.ws.part[slot * kMaxChunks + pc] = make_float2(r0.m, r0.s);
-            if (r0.key > -INFINITY) atomicMax(&p.ws.words[slot], pack_key(r0.key, static_cast<uint32_t>(r0.idx)));
-        }
-    }
     if (warp == 1) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem_base, 512);
     }
 }
 
-constexpr size_t kTcSmem = 1024 + 4 * kASlabBytes + kStages * kSlabBytes + (4 * kStages + 8) * 8 + 16 +
-                           kEpiWG * kBM * sizeof(RowRes);
+constexpr size_t kTcSmem = 1024 + 4 * kASlabBytes + kStages * kSlabBytes + (2 * kStages + 4 * kEpiWG) * 8 + 16 +
+                           kEpiWG * kBM * sizeof(RowRes) + kBM * 4 + 10 * 8 + 10 * 4 + 16;
 
 // ------------------------------------------------------------ host side ---
 inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -509,15 +673,28 @@ inline bool encode_w2_map(CUtensorMap* map, const void* W2, int V, int r) {
 inline bool use_tc_path(dspark_dtype_t dt, int r) { return dt == DSPARK_BF16 && r % kBK == 0 && r <= 256; }
 
 template <int kMode>
-dspark_status_t launch_tc(const CUtensorMap& map, const TcParams& p, int grid, cudaStream_t s) {
+dspark_status_t launch_tc(const CUtensorMap& map, const TcParams& p, int grid, cudaStream_t s, bool cooperative) {
     static OncePerDevice once;
     if (once.run(current_device(), [] {
             return cudaFuncSetAttribute(bias_engine_tc<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(kTcSmem));
         }) != cudaSuccess)
         return DSPARK_ERR_CUDA;
-    bias_engine_tc<kMode><<<grid, kTcThreads, kTcSmem, s>>>(map, p);
-    return launch_status();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = kTcSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = cooperative ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, bias_engine_tc<kMode>, map, p) != cudaSuccess) {
+        cudaGetLastError();
+        return DSPARK_ERR_CUDA;
+    }
+    return DSPARK_OK;
 }
 
 // Grid of the tcgen05 engine: nM M-tiles, P CTAs each (P * nM <= SMs).

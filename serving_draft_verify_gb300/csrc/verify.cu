@@ -223,7 +223,7 @@ verify_chain(int B, int gamma, int V, const void* __restrict__ t, const int32_t*
         if (greedy) {
             const unsigned long long w = ws.wt[b * (gamma + 1) + srow - 1];
             if (w == 0ull) set_status(ws.status, DSPARK_ERR_DEVICE_CHECK, 6);
-            next_token[b] = (w == 0ull) ? 0 : static_cast<int>(unpack_idx(w));
+            next_token[b] = (w == 0ull || unpack_idx(w) >= static_cast<uint32_t>(V)) ? 0 : static_cast<int>(unpack_idx(w));
             ws.krow[b] = 0;
         } else {
             ws.krow[b] = rej;
@@ -303,7 +303,8 @@ verify_finish(int B, int gamma, int V, int r, const void* __restrict__ t, const 
     const int b = blockIdx.x;
     const int kr = ws.krow[b];
     const unsigned long long rw = (kr > 0) ? ws.res_word[b] : 0ull;
-    bool residual = rw != 0ull;
+    const uint32_t nblk = static_cast<uint32_t>((V + 63) / 64);
+    bool residual = rw != 0ull && unpack_idx(rw) < nblk;
     float score = -INFINITY;
     int v = 0x7FFFFFFF;
     if (residual) {
@@ -326,6 +327,10 @@ verify_finish(int B, int gamma, int V, int r, const void* __restrict__ t, const 
         const unsigned long long w = ws.wt[b * (gamma + 1) + srow - 1];
         if (w == 0ull) {
             if (threadIdx.x == 0) { set_status(ws.status, DSPARK_ERR_DEVICE_CHECK, 7); next_token[b] = 0; }
+            return;
+        }
+        if (unpack_idx(w) >= nblk) {
+            if (threadIdx.x == 0) { set_status(ws.status, DSPARK_ERR_DEVICE_CHECK, 9); next_token[b] = 0; }
             return;
         }
         const int blk = static_cast<int>(unpack_idx(w));
@@ -422,10 +427,12 @@ extern "C" dspark_status_t dspark_verify(int B, int gamma, int V, int r, dspark_
         eng::TcParams p{};
         p.B = B; p.gamma = gamma; p.V = V; p.r = r; p.k = 1;
         p.U = static_cast<const uint16_t*>(U); p.W1 = static_cast<const uint16_t*>(W1);
-        p.x0 = x0; p.x = x; p.cscale = cscale; p.greedy = 0; p.seed = seed; p.P = P;
-        p.ws = eng::Ws{ws.status, ws.res_word, nullptr, nullptr};
+        p.W2 = static_cast<const uint16_t*>(W2); p.k_last = 1;
+        p.x0 = x0; p.x = const_cast<int32_t*>(x); p.cscale = cscale; p.greedy = 0;   // read only here
+        p.seed = seed; p.P = P;
+        p.ws = eng::Ws{ws.status, ws.res_word, nullptr, nullptr, nullptr};
         p.krow = ws.krow; p.T = static_cast<const uint16_t*>(t_logits); p.lt2 = ws.lt2; p.ld2 = ws.ld2;
-        if ((stt = eng::launch_tc<eng::kResidual>(map, p, nM * P, s)) != DSPARK_OK) return stt;
+        if ((stt = eng::launch_tc<eng::kResidual>(map, p, nM * P, s, false)) != DSPARK_OK) return stt;
     } else {
         int nchunk = (nblk + 7) / 8;
         if (nchunk > 256) nchunk = 256;

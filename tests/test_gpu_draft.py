@@ -109,3 +109,28 @@ def test_draft_full_size_sampled(dsv, key, temperature, nrows):
     assert np.all(np.diff(a, axis=1) <= 0) and np.all((a >= 0) & (a <= 1))
     del inp
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("key,changes,temperature", [
+    ("qwen3_8b", dict(B=20, V=5000, H=64), 0.7),
+    ("qwen3_8b", dict(B=20, V=5000, H=64), 0.0),
+    ("draft_27b", dict(B=130, gamma=3, V=2048, H=96), 1.0),
+    ("qwen3_8b", {}, 0.7),
+])
+def test_draft_one_launch_equals_per_position(dsv, key, changes, temperature):
+    """The single cooperative launch (grid barriers between positions, the
+    token draw spread over the grid) and the per-position launches (engine
+    kernel + winner kernel each) compute the same values in the same order:
+    every output must agree bit for bit."""
+    cfg = wl.scaled(wl.DRAFT_CONFIGS[key], **changes)
+    inp = wl.make_draft_inputs(cfg, device="cuda")
+    one = gpu_draft(dsv, inp, temperature=temperature)
+    dsv._binding.force_phase_launches(True)
+    try:
+        per = gpu_draft(dsv, inp, temperature=temperature)
+    finally:
+        dsv._binding.force_phase_launches(False)
+    for name in one:
+        assert np.array_equal(one[name], per[name]), name
+    del inp
+    torch.cuda.empty_cache()
