@@ -6,8 +6,8 @@ synthetic seeded inputs.
 One step = one round through the library's C ABI (all kernels on one stream).
 The timed region holds exactly K steps; the L2 is flushed (a 512 MiB write)
 between steps, outside each step's CUDA-event pair.  The JSON line also
-reports the dominant kernel's roofline (the draft phase kernel: its launches
-are timed with CUDA events recorded by the library around each launch), an
+reports the dominant kernel's roofline (the draft engine, one cooperative
+launch per draft call: timed with CUDA events the library records around it), an
 end-to-end number through the same C-ABI calls with inputs copied from pinned
 host memory each step, the oracle timed on the host cores on a bounded sample,
 and extra lines for greedy decoding and the accept-rate TV kernel.
@@ -34,7 +34,6 @@ METRIC = "draft+verify rows/s over B·γ×V logits; achieved HBM GB/s vs GB300 p
 WORKLOAD = ("Qwen3-8B-shaped serving round: B=64, gamma=7 (verify width 8), V=151936, H=4096, r=256, "
             "bf16, T=0.7, seed 1")
 FALLBACK_HBM_GBS = 6800.0
-CPU_SAMPLE_REQUESTS = 12
 
 
 def peaks():
@@ -98,7 +97,7 @@ class ClockSampler:
         os.close(fd)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "25"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -220,15 +219,19 @@ def run_gpu(args):
     hbm_gbs = round_bytes * args.steps / (total_ms * 1e-3) / 1e9
     peak, peak_kind = peaks()
 
-    # dominant kernel: the draft phase kernel (one per position k)
-    phase_bytes = B * V * 2 + V * r * 2 / G + B * r * 2
+    # dominant kernel: the draft engine, one cooperative launch per draft call that
+    # covers all gamma positions (the library records CUDA events around it on the
+    # launching stream).  Algorithmic bytes of one launch: U, W2 once, W1 rows.
+    launch_bytes = B * G * V * 2 + V * r * 2 + B * G * r * 2
+    per_call = len(phase_ms) // args.steps if args.steps else 0
+    launch_bytes /= max(per_call, 1)
     ph = sorted(phase_ms)
     phase_avg = sum(ph) / len(ph) if ph else float("nan")
-    achieved = phase_bytes / (phase_avg * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": "bias_engine_tc<kDraft> (draft phase)", "achieved": round(achieved, 1),
-                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+    achieved = launch_bytes / (phase_avg * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "bias_engine_tc<kDraft> (draft block, all positions)",
+                "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "traffic": args.phase_traffic if args.phase_traffic is not None else recorded_phase_traffic(),
-                "peak_kind": f"{peak_kind} (copy bandwidth)", "bytes_per_launch": int(phase_bytes),
+                "peak_kind": f"{peak_kind} (copy bandwidth)", "bytes_per_launch": int(launch_bytes),
                 "avg_launch_us": round(phase_avg * 1e3, 2), "launches_timed": len(ph)}
 
     # greedy round (same workload, T = 0)
@@ -270,19 +273,18 @@ def run_gpu(args):
         tv = {"rows": d_.shape[0], "ms": tv_ms, "rows_per_s": d_.shape[0] / (tv_ms * 1e-3),
               "achieved_gbs": tvb / (tv_ms * 1e-3) / 1e9, "frac_of_peak": tvb / (tv_ms * 1e-3) / 1e9 / peak}
         del d_, t_
-    launches_per_step = (2 * G + 1) + 1 + 4          # draft: phase + winner per k, finalize; schedule; verify
+    # draft: engine, winner (x_gamma), finalize; schedule: 1; verify: rows, chain, residual, finish
+    launches_per_step = 3 + 1 + 4
 
     line = {"metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; shapes of the Qwen3-8B draft setting)",
-            "config": {"workload": WORKLOAD, "B": B, "gamma": G, "V": V, "H": H, "r": r, "temperature": T,
-                       "l2": "flushed between steps (512 MiB write outside the timed step)",
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "config": workload_config(world),
             "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / peak, "roofline": roofline, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps, "clocks": clk,
             "extra": {"greedy_round": greedy, "accept_rate_tv": tv,
                       "accepted_per_request": float(nacc.mean()), "scheduled_rows": int((ell + 1).sum())}}
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, T, seed)
     if world > 1:
         import torch.distributed as dist
@@ -292,29 +294,59 @@ def run_gpu(args):
 
 
 # ------------------------------------------------------------ oracle ---
-def cpu_baseline(inp, T, seed, nreq=CPU_SAMPLE_REQUESTS):
-    """The oracle (float64, numpy) on a bounded sample of the same round: the
-    first `nreq` requests through draft, schedule (over the sample) and verify."""
-    import numpy as np
-    import torch
-    import oracle
+def workload_config(world):
     from serving_draft_verify_gb300 import workloads as wl
+    c = wl.QWEN3_8B
+    return {"workload": WORKLOAD, "B": c.B, "gamma": c.gamma, "V": c.V, "H": c.H, "r": c.r,
+            "temperature": c.temperature, "l2": "flushed between steps (512 MiB write outside the timed step)",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
+def host_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def oracle_inputs(inp):
+    """The round's inputs as float64 numpy arrays (converted once)."""
+    from serving_draft_verify_gb300 import workloads as wl
+    out = {k: wl.to_f64(inp[k]) for k in ("U", "h", "t", "W1", "W2", "w")}
+    out["x0"] = inp["x0"].cpu().numpy()
+    return out
+
+
+def oracle_round(f64, T, seed, nreq):
+    """One round of the oracle (float64 numpy) over the first `nreq` requests:
+    draft, schedule over the sample, verify.  Returns its wall time in s."""
+    import numpy as np
+    import oracle
 
     rows = np.arange(nreq)
-    idx = torch.from_numpy(rows).to(inp["U"].device)
-    U, h, t = (wl.to_f64(inp[k][idx]) for k in ("U", "h", "t"))
-    W1, W2, w = (wl.to_f64(inp[k]) for k in ("W1", "W2", "w"))
-    x0 = inp["x0"][idx].cpu().numpy()
+    U, h, t, x0 = f64["U"][:nreq], f64["h"][:nreq], f64["t"][:nreq], f64["x0"][:nreq]
+    W1, W2, w = f64["W1"], f64["W2"], f64["w"]
     G = U.shape[1]
     t0 = time.perf_counter()
     d = oracle.draft_block(U, h, W1, W2, w, 0.0, x0, T, seed, requests=rows)
     N = np.arange(nreq * (G + 1) + 1, dtype=np.float64)
     ell, _, _ = oracle.schedule_prefix(d["a"].astype(np.float32), N / (20.0 + 0.05 * N))
     oracle.verify_round(t, U, W1, W2, x0, d["x"], d["lse_d"], d["logp_d"], ell, T, seed, requests=rows)
-    dt = time.perf_counter() - t0
-    return {"value": nreq * G / dt, "unit": "rows/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{nreq} of 64 requests x {G} positions, one full round (draft, schedule, verify), "
-                      f"float64 numpy; {dt:.1f} s"}
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(inp, T, seed, min_seconds=10.0, max_rounds=24):
+    """The oracle on the host cores: whole 64-request rounds of the same workload,
+    repeated until at least `min_seconds` of work (at most `max_rounds`)."""
+    f64 = oracle_inputs(inp)
+    B, G = f64["U"].shape[0], f64["U"].shape[1]
+    spent, n = 0.0, 0
+    while n < max_rounds and (n == 0 or spent < min_seconds):
+        spent += oracle_round(f64, T, seed, B)
+        n += 1
+    return {"value": n * B * G / spent, "unit": "rows/s", "cores": host_threads(), "kind": "oracle",
+            "sample": f"{n} full rounds (draft, schedule, verify) of all {B} requests x {G} positions, "
+                      f"float64 numpy (BLAS threads up to the core count); {spent:.1f} s"}
 
 
 def run_reference(args):
@@ -328,18 +360,19 @@ def run_reference(args):
     for _ in range(args.warmup):
         pass                                              # the oracle has nothing to warm
     times = []
-    nreq = 4
+    nreq = 4                                              # requests per step (a fraction of a second of oracle work)
+    f64 = oracle_inputs(inp)
     for _ in range(args.steps):
-        r = cpu_baseline(inp, cfg.temperature, cfg.seed, nreq=nreq)
-        times.append(nreq * cfg.gamma / r["value"])
+        times.append(oracle_round(f64, cfg.temperature, cfg.seed, nreq))
     total = sum(times)
     value = nreq * cfg.gamma * args.steps / total
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded)", "config": {"workload": WORKLOAD + f"; {nreq} requests per step"},
-            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": f"{nreq} of 64 requests x {cfg.gamma} positions per step"},
+            "data": "synthetic (seeded)", "config": workload_config(1),
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": host_threads(), "kind": "oracle",
+                             "sample": f"{nreq} of {cfg.B} requests x {cfg.gamma} positions per step, one "
+                                       f"round each (draft, schedule over the sample, verify)"},
             "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
@@ -347,7 +380,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--skip-tv", action="store_true")

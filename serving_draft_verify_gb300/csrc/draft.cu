@@ -6,15 +6,16 @@
 //
 // Tensor-core path (bf16, r % 64 == 0): one cooperative launch of the bias
 // engine (engine.cuh) runs every position; between positions its CTAs meet at
-// a grid barrier, draw x_{k-1} (second Gumbel level) for the requests each
-// owns, and meet again.  A winner kernel draws x_gamma.
+// a grid barrier and draw x_{k-1} (second Gumbel level) for the requests each
+// owns, publishing each token as it is drawn.  After the last position the
+// same launch draws x_gamma and finalizes the requests each CTA owns.
 // CUDA-core path (and the tensor-core path when the grid cannot be
 // co-resident): per position a phase kernel (every 64-token block's
 // logsumexp and Gumbel key, the CTA's best block by atomicMax, its (max, sum)
 // partial) and a winner kernel (two warps per request: z on the winning block
 // and the token inside it).
-// After the last position a finalize kernel forms lse_d / logp_d and the
-// confidence c_k and survival a_k.
+// There, after the last position a finalize kernel forms lse_d / logp_d and
+// the confidence c_k and survival a_k.
 #include "engine.cuh"
 #include "../../include/dspark_debug.h"
 
@@ -28,13 +29,16 @@ using eng::prev_token;
 using eng::unpack_idx;
 using DraftWs = eng::Ws;
 
-// Workspace: status | grid-barrier counter | words [gamma][B] |
-// partials [gamma][B][kMaxChunks] | ytok [gamma][B].  The first three are
+// Workspace: status | grid-barrier counter | tagged tokens [B] | words [gamma][B] |
+// partials [gamma][B][kMaxChunks] | ytok [gamma][B].  The first four are
 // cleared by every call.
-inline size_t draft_ws_layout(int B, int gamma, size_t* o_bar, size_t* o_words, size_t* o_part, size_t* o_ytok) {
+inline size_t draft_ws_layout(int B, int gamma, size_t* o_bar, size_t* o_xw, size_t* o_words, size_t* o_part,
+                              size_t* o_ytok) {
     size_t o = kStatusBytes;
     *o_bar = o;
     o += 256;
+    *o_xw = o;
+    o += round_up(static_cast<size_t>(B) * 8, 256);
     *o_words = o;
     o += round_up(static_cast<size_t>(gamma) * B * 8, 256);
     *o_part = o;
@@ -45,13 +49,13 @@ inline size_t draft_ws_layout(int B, int gamma, size_t* o_bar, size_t* o_words, 
 }
 
 inline DraftWs draft_ws(void* workspace, int B, int gamma, size_t* clear_bytes) {
-    size_t ob, ow, op, oy;
-    draft_ws_layout(B, gamma, &ob, &ow, &op, &oy);
+    size_t ob, ox, ow, op, oy;
+    draft_ws_layout(B, gamma, &ob, &ox, &ow, &op, &oy);
     uint8_t* wsb = static_cast<uint8_t*>(workspace);
     *clear_bytes = op;
     return DraftWs{reinterpret_cast<StatusBlock*>(wsb), reinterpret_cast<unsigned long long*>(wsb + ow),
                    reinterpret_cast<float2*>(wsb + op), reinterpret_cast<float*>(wsb + oy),
-                   reinterpret_cast<unsigned int*>(wsb + ob)};
+                   reinterpret_cast<unsigned int*>(wsb + ob), reinterpret_cast<unsigned long long*>(wsb + ox)};
 }
 
 namespace {
@@ -191,85 +195,28 @@ draft_winner(int B, int gamma, int V, int r, int k, const void* __restrict__ U, 
 }
 
 // ========================================================== finalize ====
-// One CTA per request, one warp per position k: lse_d / logp_d from the phase
-// partials and the confidence logit w . [h_k ; W1[x_{k-1}]] + bias (16-byte
-// loads); thread 0 then forms c_k and the float32 survival product in k order.
-template <bool kBF16>
-__device__ __forceinline__ float dot_row(const void* a, size_t a_off, const void* b, size_t b_off, int n, int lane) {
-    // n elements from a[a_off..] and b[b_off..]; 16-byte chunks when both are aligned
-    constexpr int EPC = kBF16 ? 8 : 4;
-    constexpr size_t ESZ = kBF16 ? 2 : 4;
-    float acc = 0.f;
-    const bool vec = ((a_off * ESZ) % 16 == 0) && ((b_off * ESZ) % 16 == 0) && (n % EPC == 0);
-    if (vec) {
-        const uint4* pa = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a) + a_off * ESZ);
-        const uint4* pb = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(b) + b_off * ESZ);
-        for (int c = lane; c < n / EPC; c += 32) {
-            const uint4 x = pa[c], y = pb[c];
-            const uint32_t xv[4] = {x.x, x.y, x.z, x.w}, yv[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if constexpr (kBF16) {
-                    acc = fmaf(bf16lo(xv[q]), bf16lo(yv[q]), acc);
-                    acc = fmaf(bf16hi(xv[q]), bf16hi(yv[q]), acc);
-                } else {
-                    acc = fmaf(__uint_as_float(xv[q]), __uint_as_float(yv[q]), acc);
-                }
-            }
-        }
-    } else {
-        for (int i = lane; i < n; i += 32) acc = fmaf(ld_elem<kBF16>(a, a_off + i), ld_elem<kBF16>(b, b_off + i), acc);
-    }
-    return acc;
-}
-
+// One CTA per request, one warp per position k (eng::finalize_position: lse_d,
+// logp_d and the confidence c_k); thread 0 then forms the float32 survival
+// product in k order.  Used by the per-position path; the cooperative launch
+// does the same work in its tail.
 template <bool kBF16>
 __global__ void __launch_bounds__(1024, 1)
 draft_finalize(int B, int gamma, int V, int H, int r, const void* __restrict__ h, const void* __restrict__ W1,
                const void* __restrict__ w, float bias, const int32_t* __restrict__ x0,
                const int32_t* __restrict__ x, int greedy, int nchunk, float* __restrict__ lse_d,
                float* __restrict__ logp_d, float* __restrict__ c, float* __restrict__ a, DraftWs ws) {
-    __shared__ float sc[DSPARK_MAX_GAMMA];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
     const int b = blockIdx.x;
     const int k = warp + 1;
-    if (k <= gamma) {
-        const size_t slot = static_cast<size_t>(k - 1) * B + b;
-        const size_t o = static_cast<size_t>(b) * gamma + (k - 1);
-        float L = 0.f, lp = 0.f;
-        if (!greedy) {
-            float m = -INFINITY, s = 0.f;
-            for (int ch = lane; ch < nchunk; ch += 32) {
-                const float2 pr = ws.part[slot * kMaxChunks + ch];
-                lse_merge(m, s, pr.x, pr.y);
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float om = __shfl_xor_sync(0xffffffffu, m, off);
-                const float os = __shfl_xor_sync(0xffffffffu, s, off);
-                lse_merge(m, s, om, os);
-            }
-            const float L2 = m + log2f(s);
-            L = L2 * kLn2;
-            lp = (ws.ytok[slot] - L2) * kLn2;
-        }
-        const int prev = prev_token(x0, x, b, gamma, k, V, ws.status);
-        float acc = dot_row<kBF16>(w, 0, h, o * H, H, lane);
-        acc += dot_row<kBF16>(w, H, W1, static_cast<size_t>(prev) * r, r, lane);
-        const float logit = warp_sum(acc) + bias;
-        if (lane == 0) {
-            sc[k - 1] = 1.f / (1.f + expf(-logit));
-            lse_d[o] = L;
-            logp_d[o] = lp;
-        }
-    }
+    if (k <= gamma)
+        eng::finalize_position<kBF16>(b, k, B, gamma, V, H, r, h, W1, w, bias, x0, x, greedy, nchunk, ws.part,
+                                      ws.ytok, lse_d, logp_d, c, ws.status);
     __syncthreads();
     if (threadIdx.x == 0) {
         float surv = 1.f;
         for (int kk = 0; kk < gamma; ++kk) {
-            surv = surv * sc[kk];
             const size_t o = static_cast<size_t>(b) * gamma + kk;
-            c[o] = sc[kk];
+            surv = surv * c[o];
             a[o] = surv;
         }
     }
@@ -313,7 +260,7 @@ dspark_status_t draft_block_impl(int B, int gamma, int V, int H, int r, dspark_d
                                  float* logp_d, float* c, float* a, void* workspace, cudaStream_t s) {
     size_t clear = 0;
     const DraftWs ws = draft_ws(workspace, B, gamma, &clear);
-    if (cudaMemsetAsync(workspace, 0, clear, s) != cudaSuccess) return DSPARK_ERR_CUDA;   // status, barrier, words
+    if (cudaMemsetAsync(workspace, 0, clear, s) != cudaSuccess) return DSPARK_ERR_CUDA;   // status .. words
     const int greedy = (temperature == 0.f);
     const float cscale = greedy ? 1.f : kLog2e / temperature;
     const bool tcp = eng::use_tc_path(dt, r);
@@ -335,19 +282,19 @@ dspark_status_t draft_block_impl(int B, int gamma, int V, int H, int r, dspark_d
     const bool one_launch = tcp && !g_force_phase_launches && nM * P <= sm_count(current_device());
     dspark_status_t stt = DSPARK_OK;
     if (one_launch) {
-        // every position in one cooperative launch; x_1..x_{gamma-1} are drawn inside it
+        // every position, x_gamma and the finalize in one cooperative launch
         if (g_timing.on) cudaEventRecord(g_timing.ev[0], s);
         p.k = 1;
         p.k_last = gamma;
-        stt = eng::launch_tc<eng::kDraft>(map, p, nM * P, s, /*cooperative=*/gamma > 1);
+        p.fuse_tail = 1;
+        p.H = H; p.h = static_cast<const uint16_t*>(h); p.w = static_cast<const uint16_t*>(w); p.bias = bias;
+        p.lse_d = lse_d; p.logp_d = logp_d; p.c = c; p.a = a;
+        stt = eng::launch_tc<eng::kDraft>(map, p, nM * P, s, /*cooperative=*/true);
         if (g_timing.on) {
             cudaEventRecord(g_timing.ev[1], s);
             g_timing.recorded = 1;
         }
-        if (stt != DSPARK_OK) return stt;
-        if ((stt = launch_winner<true>(B, gamma, V, r, gamma, U, W1, W2, x0, x, cscale, greedy, seed, ws, s)) !=
-            DSPARK_OK)
-            return stt;
+        return stt;
     } else {
         for (int k = 1; k <= gamma; ++k) {
             if (g_timing.on) cudaEventRecord(g_timing.ev[2 * (k - 1)], s);
@@ -412,8 +359,8 @@ extern "C" size_t dspark_draft_block_workspace_size(int B, int gamma, int V, int
     (void)r;
     (void)V;
     if (B <= 0 || gamma <= 0 || V <= 0) return kStatusBytes;
-    size_t ob, ow, op, oy;
-    return draft_ws_layout(B, gamma, &ob, &ow, &op, &oy);
+    size_t ob, ox, ow, op, oy;
+    return draft_ws_layout(B, gamma, &ob, &ox, &ow, &op, &oy);
 }
 
 extern "C" dspark_status_t dspark_draft_block(int B, int gamma, int V, int H, int r, dspark_dtype_t dt,

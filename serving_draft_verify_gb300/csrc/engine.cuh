@@ -48,6 +48,7 @@ struct Ws {
     float2* part;                // [positions][B][kMaxChunks] (max, sum) of y = z log2e / T
     float* ytok;                 // [positions][B] y of the drawn token
     unsigned int* gbar;          // grid-barrier counter of the multi-position draft launch (starts at 0)
+    unsigned long long* xw;      // [B] (k << 32) | x_k, the last token drawn in the running launch (starts at 0)
 };
 
 // ------------------------------------------------------------ helpers ---
@@ -116,15 +117,17 @@ __device__ __forceinline__ void transpose_reduce32(float* v) {
 // warp w rebuilds tokens blk*64 + 32w + (0..31); each lane loads one or two
 // 16-byte chunks of every W2 row (coalesced rows) and a transpose-reduce
 // leaves token (32w + lane)'s dot product in that lane.  Returns z for the
-// lane's token (-inf past V).
+// lane's token (-inf past V).  prev: x_{k-1}, already checked against V.
 template <bool kBF16, int kCPL>
-__device__ __forceinline__ float block_logit(int b, int gamma, int k, int V, int r, int blk, const void* U,
-                                             const void* W1, const void* W2, const int32_t* x0, const int32_t* x,
-                                             StatusBlock* st) {
+__device__ __forceinline__ float block_logit_prev(int b, int gamma, int k, int V, int r, int blk, int prev,
+                                                  const void* U, const void* W1, const void* W2) {
     constexpr int EPC = kBF16 ? 8 : 4;                    // elements per 16-byte chunk
     const int warp = (threadIdx.x >> 5) & 1, lane = threadIdx.x & 31;
-    const int prev = prev_token(x0, x, b, gamma, k, V, st);
     const int nch = r / EPC;
+    const int vbase = blk * 64 + warp * 32;
+    const int vl = vbase + lane;
+    const size_t urow = (static_cast<size_t>(b) * gamma + (k - 1)) * V;
+    const float u = (vl < V) ? ld_elem<kBF16>(U, urow + vl) : 0.f;
     float e[kCPL][EPC];
 #pragma unroll
     for (int cc = 0; cc < kCPL; ++cc) {
@@ -133,7 +136,6 @@ __device__ __forceinline__ float block_logit(int b, int gamma, int k, int V, int
         for (int q = 0; q < EPC; ++q)
             e[cc][q] = (c < nch) ? ld_elem<kBF16>(W1, static_cast<size_t>(prev) * r + c * EPC + q) : 0.f;
     }
-    const int vbase = blk * 64 + warp * 32;
     const uint64_t pol = policy_evict_last();
     float part[32];
     constexpr int kBatch = 32 / kCPL;
@@ -173,10 +175,16 @@ __device__ __forceinline__ float block_logit(int b, int gamma, int k, int V, int
         }
     }
     transpose_reduce32(part);
-    const int v = vbase + lane;
-    if (v >= V) return -INFINITY;
-    const size_t urow = (static_cast<size_t>(b) * gamma + (k - 1)) * V;
-    return part[0] + ld_elem<kBF16>(U, urow + v);
+    if (vl >= V) return -INFINITY;
+    return part[0] + u;
+}
+
+template <bool kBF16, int kCPL>
+__device__ __forceinline__ float block_logit(int b, int gamma, int k, int V, int r, int blk, const void* U,
+                                             const void* W1, const void* W2, const int32_t* x0, const int32_t* x,
+                                             StatusBlock* st) {
+    const int prev = prev_token(x0, x, b, gamma, k, V, st);
+    return block_logit_prev<kBF16, kCPL>(b, gamma, k, V, r, blk, prev, U, W1, W2);
 }
 
 // ===================================================== tcgen05 engine ====
@@ -205,6 +213,17 @@ struct TcParams {
     Ws ws;
     float* debug_z;                  // kDraft: write y to [B][V] instead of reducing
     int k_last;                      // kDraft: positions k .. k_last in one (cooperative) launch
+    // kDraft with fuse_tail: the launch also draws x_gamma and finalizes
+    // (lse_d, logp_d, confidence c and survival a), as draft_finalize does
+    int fuse_tail;
+    int H;
+    const uint16_t* h;               // [B][gamma][H]
+    const uint16_t* w;               // [H + r]
+    float bias;
+    float* lse_d;
+    float* logp_d;
+    float* c;
+    float* a;
     // kResidual
     const int32_t* krow;             // [B] rejected position k_b (0: row inactive)
     const uint16_t* T;               // t_logits [B][gamma+1][V]
@@ -239,6 +258,96 @@ __device__ __forceinline__ bool grid_wait(const unsigned int* ctr, unsigned int 
     return true;
 }
 
+// Waits (bounded) until the tagged token word of a request carries position k.
+__device__ __forceinline__ bool wait_token(const unsigned long long* xw, int k, int* tok) {
+    auto load = [&]() {
+        unsigned long long v;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(xw) : "memory");
+        return v;
+    };
+    unsigned long long v = load();
+    if (static_cast<uint32_t>(v >> 32) != static_cast<uint32_t>(k)) {
+        const uint64_t t0 = globaltimer_ns();
+        while (static_cast<uint32_t>((v = load()) >> 32) != static_cast<uint32_t>(k)) {
+            __nanosleep(32);
+            if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        }
+    }
+    *tok = static_cast<int>(static_cast<uint32_t>(v));
+    return true;
+}
+
+// Warp dot product of n elements of a[a_off..] and b[b_off..] (16-byte chunks
+// when both are aligned); lane partial sums, reduced by the caller.
+template <bool kBF16>
+__device__ __forceinline__ float dot_row(const void* a, size_t a_off, const void* b, size_t b_off, int n, int lane) {
+    constexpr int EPC = kBF16 ? 8 : 4;
+    constexpr size_t ESZ = kBF16 ? 2 : 4;
+    float acc = 0.f;
+    const bool vec = ((a_off * ESZ) % 16 == 0) && ((b_off * ESZ) % 16 == 0) && (n % EPC == 0);
+    if (vec) {
+        const uint4* pa = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a) + a_off * ESZ);
+        const uint4* pb = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(b) + b_off * ESZ);
+        for (int c = lane; c < n / EPC; c += 32) {
+            const uint4 x = pa[c], y = pb[c];
+            const uint32_t xv[4] = {x.x, x.y, x.z, x.w}, yv[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if constexpr (kBF16) {
+                    acc = fmaf(bf16lo(xv[q]), bf16lo(yv[q]), acc);
+                    acc = fmaf(bf16hi(xv[q]), bf16hi(yv[q]), acc);
+                } else {
+                    acc = fmaf(__uint_as_float(xv[q]), __uint_as_float(yv[q]), acc);
+                }
+            }
+        }
+    } else {
+        for (int i = lane; i < n; i += 32) acc = fmaf(ld_elem<kBF16>(a, a_off + i), ld_elem<kBF16>(b, b_off + i), acc);
+    }
+    return acc;
+}
+
+// One warp finalizes position k of request b (DeepSpec walkthrough 3.3,
+// AcceptRatePredictor): lse_d = logsumexp(z / T) from the nchunk (max, sum)
+// partials, logp_d = y(x_k) - lse_d, and the confidence
+// c = sigmoid(w . [h_k ; W1[x_{k-1}]] + bias), written by lane 0.
+template <bool kBF16>
+__device__ __forceinline__ void finalize_position(int b, int k, int B, int gamma, int V, int H, int r, const void* h,
+                                                  const void* W1, const void* w, float bias, const int32_t* x0,
+                                                  const int32_t* x, int greedy, int nchunk, const float2* part,
+                                                  const float* ytok, float* lse_d, float* logp_d, float* c,
+                                                  StatusBlock* st) {
+    const int lane = threadIdx.x & 31;
+    const size_t slot = static_cast<size_t>(k - 1) * B + b;
+    const size_t o = static_cast<size_t>(b) * gamma + (k - 1);
+    float L = 0.f, lp = 0.f;
+    if (!greedy) {
+        float m = -INFINITY, s = 0.f;
+        for (int ch = lane; ch < nchunk; ch += 32) {
+            const float2 pr = __ldcg(part + slot * kMaxChunks + ch);
+            lse_merge(m, s, pr.x, pr.y);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float om = __shfl_xor_sync(0xffffffffu, m, off);
+            const float os = __shfl_xor_sync(0xffffffffu, s, off);
+            lse_merge(m, s, om, os);
+        }
+        const float L2 = m + log2f(s);
+        L = L2 * kLn2;
+        lp = (__ldcg(ytok + slot) - L2) * kLn2;
+    }
+    const int prev = prev_token(x0, x, b, gamma, k, V, st);
+    float acc = dot_row<kBF16>(w, 0, h, o * H, H, lane);
+    acc += dot_row<kBF16>(w, H, W1, static_cast<size_t>(prev) * r, r, lane);
+    const float logit = warp_sum(acc) + bias;
+    if (lane == 0) {
+        c[o] = 1.f / (1.f + expf(-logit));
+        lse_d[o] = L;
+        logp_d[o] = lp;
+    }
+}
+
 // Draw x_k for request b inside a running multi-position launch: a pair of
 // warps (named barrier `bar`, 64 threads) rebuilds z on the winning block from
 // W2 rows and takes the second Gumbel level (stream 0); the even warp's lane 0
@@ -246,14 +355,16 @@ __device__ __forceinline__ bool grid_wait(const unsigned int* ctr, unsigned int 
 __device__ __forceinline__ void pair_draw(const TcParams& p, int b, int k, int bar, float2* xch, int* xchi) {
     const int lane = threadIdx.x & 31, wp = (threadIdx.x >> 5) & 1;
     const size_t slot = static_cast<size_t>(k - 1) * p.B + b;
+    // independent L2 reads first: the winning block, and x_{k-1} for W1
     const unsigned long long word = __ldcg(p.ws.words + slot);
+    const int prev = prev_token(p.x0, p.x, b, p.gamma, k, p.V, p.ws.status);
     const uint32_t idx = unpack_idx(word);
     const bool ok = word != 0ull && idx < static_cast<uint32_t>((p.V + 63) / 64);
     float score = -INFINITY, yv = 0.f;
     int bi = 0x7FFFFFFF;
     if (ok) {
         const int blk = static_cast<int>(idx);
-        const float z = block_logit<true, 1>(b, p.gamma, k, p.V, p.r, blk, p.U, p.W1, p.W2, p.x0, p.x, p.ws.status);
+        const float z = block_logit_prev<true, 1>(b, p.gamma, k, p.V, p.r, blk, prev, p.U, p.W1, p.W2);
         const int v = blk * 64 + wp * 32 + lane;
         if (z > -INFINITY) {
             yv = z * p.cscale;
@@ -278,7 +389,14 @@ __device__ __forceinline__ void pair_draw(const TcParams& p, int b, int k, int b
         if (tok == 0x7FFFFFFF) { set_status(p.ws.status, DSPARK_ERR_DEVICE_CHECK, 3); tok = 0; }
         p.x[b * p.gamma + k - 1] = tok;
         p.ws.ytok[slot] = xch[w].y;
+        const unsigned long long tagged = (static_cast<unsigned long long>(k) << 32) | static_cast<uint32_t>(tok);
+        asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p.ws.xw + b), "l"(tagged) : "memory");
+        xchi[0] = tok;
     }
+    asm volatile("bar.sync %0, 64;" ::"r"(bar) : "memory");
+    // W1[x_k] is the next position's A row and the next draw's e: bring it into L2
+    if (wp == 0 && lane * 128 < p.r * 2)
+        prefetch_l2(reinterpret_cast<const uint8_t*>(p.W1) + static_cast<size_t>(xchi[0]) * p.r * 2 + lane * 128);
     asm volatile("bar.sync %0, 64;" ::"r"(bar) : "memory");
 }
 
@@ -388,10 +506,16 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                         for (int b = blockIdx.x + pair * gridDim.x; b < p.B; b += 5 * gridDim.x)
                             pair_draw(p, b, k - 1, 2 + pair, xch + 2 * pair, xchi + 2 * pair);
                     }
-                    arrive();
-                    wait_all();                           // every x_{k-1} is written
-                    for (int rr = ptid; rr < nrows; rr += kPro)
-                        s_prev[rr] = prev_token(p.x0, p.x, m0 + rr, p.gamma, k, p.V, st);
+                    // x_{k-1} of this M-tile's requests, as their drawers publish them
+                    for (int rr = ptid; rr < nrows; rr += kPro) {
+                        int tok = 0;
+                        if (*s_fail == 0 && !wait_token(p.ws.xw + m0 + rr, k - 1, &tok)) {
+                            set_status(st, DSPARK_ERR_TIMEOUT, 14);
+                            *s_fail = 1;
+                        }
+                        if (tok < 0 || tok >= p.V) { set_status(st, DSPARK_ERR_DEVICE_CHECK, 2); tok = 0; }
+                        s_prev[rr] = tok;
+                    }
                 } else {
                     for (int rr = ptid; rr < nrows; rr += kPro) {
                         const int b = m0 + rr;
@@ -418,20 +542,19 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
 
             // A operand: rows W1[x_{k_b-1}] of this M-tile, K-major, 128-byte swizzle
             {
-                const int cpr = p.r / 8;                  // 16-byte chunks per row
-                for (int idx = ptid; idx < kBM * cpr; idx += kPro) {
-                    const int row = idx / cpr, c16 = idx % cpr;
-                    const int slab = c16 >> 3, c = c16 & 7;
-                    const int rr = row % rpc;
-                    uint4 v = make_uint4(0, 0, 0, 0);
-                    if (rr < nrows) {
-                        const int prev = s_prev[rr];
-                        if (prev >= 0)
-                            v = *reinterpret_cast<const uint4*>(p.W1 + static_cast<size_t>(prev) * p.r + c16 * 8);
+                // one warp per A row, one lane per 16-byte chunk (r / 8 <= 32 chunks)
+                const int cpr = p.r / 8;
+                for (int row = ptid >> 5; row < kBM; row += kPro / 32) {
+                    const int rr = row & (rpc - 1);       // rpc is 64 or 128
+                    const int prev = (rr < nrows) ? s_prev[rr] : -1;
+                    if (lane < cpr) {
+                        const int slab = lane >> 3, c = lane & 7;
+                        uint8_t* dst = sA + slab * kASlabBytes + (row >> 3) * 1024 + (row & 7) * 128 + ((c ^ (row & 7)) << 4);
+                        if (prev >= 0) cp_async16(dst, p.W1 + static_cast<size_t>(prev) * p.r + lane * 8);
+                        else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
                     }
-                    uint8_t* dst = sA + slab * kASlabBytes + (row >> 3) * 1024 + (row & 7) * 128 + ((c ^ (row & 7)) << 4);
-                    *reinterpret_cast<uint4*>(dst) = v;
                 }
+                cp_async_wait_all();
                 fence_proxy_async_smem();
                 tc::fence_before_sync();
                 pro_sync();
@@ -479,7 +602,9 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                 const int kb = (rr < nrows) ? row_k(b, k) : 0;
                 const bool valid = rr < nrows && kb > 0;
                 const bool warp_live = ((q * 32) % rpc) < nrows;
-                const uint64_t pol = policy_evict_first();
+                // U rows stay in L2 (normal policy): the token draw after this position
+                // re-reads the 64 values of each winning block
+                const uint64_t pol = (kMode == kDraft) ? policy_evict_normal() : policy_evict_first();
                 const uint16_t* urow = p.U + (static_cast<size_t>(valid ? b : 0) * p.gamma + (valid ? kb - 1 : 0)) * p.V;
                 float ld2 = 0.f, lt2 = 0.f;
                 const uint16_t* trow = nullptr;
@@ -623,10 +748,59 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                     const size_t slot = static_cast<size_t>(k - 1) * p.B + b;
                     if (kMode == kDraft && !p.greedy) p.ws.part[slot * kMaxChunks + pc] = make_float2(r0.m, r0.s);
                     if (r0.key > -INFINITY) atomicMax(&p.ws.words[slot], pack_key(r0.key, static_cast<uint32_t>(r0.idx)));
+                    // greedy: the next A row is one of the CTAs' best tokens; bring ours into L2
+                    if (kMode == kDraft && p.greedy && k < k1 && r0.idx >= 0 && r0.idx < p.V)
+                        for (int off = 0; off < p.r * 2; off += 128)
+                            prefetch_l2(reinterpret_cast<const uint8_t*>(p.W1) + static_cast<size_t>(r0.idx) * p.r * 2 + off);
                 }
             }
             if (kMode == kDraft && multi && k < k1) arrive();
             else pro_sync();                              // rowres is rewritten by the next position
+        }
+
+        if (kMode == kDraft && p.fuse_tail && p.debug_z == nullptr) {
+            // ------------------------------------------ x_gamma and finalize
+            arrive();
+            wait_all();                                   // every CTA published the last position
+            // requests b = blockIdx.x + j * gridDim.x < B, j < nown, belong to this CTA
+            const int cta = static_cast<int>(blockIdx.x), ncta = static_cast<int>(gridDim.x);
+            const int nown = (cta < p.B) ? (p.B - 1 - cta) / ncta + 1 : 0;
+            if (!p.greedy) {
+                if (warp >= 2 && *s_fail == 0) {
+                    const int pair = (warp - 2) >> 1;
+                    for (int b = blockIdx.x + pair * gridDim.x; b < p.B; b += 5 * gridDim.x)
+                        pair_draw(p, b, k1, 2 + pair, xch + 2 * pair, xchi + 2 * pair);
+                }
+            } else {
+                for (int j = ptid; j < nown; j += kPro) {
+                    const int b = blockIdx.x + j * gridDim.x;
+                    const unsigned long long w = __ldcg(p.ws.words + static_cast<size_t>(k1 - 1) * p.B + b);
+                    const uint32_t idx = unpack_idx(w);
+                    int tok = static_cast<int>(idx);
+                    if (w == 0ull || idx >= static_cast<uint32_t>(p.V)) {
+                        set_status(st, DSPARK_ERR_DEVICE_CHECK, 3);
+                        tok = 0;
+                    }
+                    p.x[b * p.gamma + k1 - 1] = tok;
+                }
+            }
+            pro_sync();
+            // one warp per (owned request, position)
+            for (int item = warp - 1; item < nown * p.gamma; item += kPro / 32) {
+                const int b = blockIdx.x + (item / p.gamma) * gridDim.x, k = item % p.gamma + 1;
+                finalize_position<true>(b, k, p.B, p.gamma, p.V, p.H, p.r, p.h, p.W1, p.w, p.bias, p.x0, p.x,
+                                        p.greedy, p.P, p.ws.part, p.ws.ytok, p.lse_d, p.logp_d, p.c, st);
+            }
+            pro_sync();
+            for (int j = ptid; j < nown; j += kPro) {     // survival a_k = prod c_1..c_k, in k order
+                const int b = blockIdx.x + j * gridDim.x;
+                float surv = 1.f;
+                for (int kk = 0; kk < p.gamma; ++kk) {
+                    const size_t o = static_cast<size_t>(b) * p.gamma + kk;
+                    surv = surv * p.c[o];
+                    p.a[o] = surv;
+                }
+            }
         }
     }
 

@@ -9,9 +9,11 @@
 //   2. stable LSD radix sort, four 8-bit passes; within a warp, equal digits
 //      are ranked with __match_any_sync, so ties keep (b, j) order;
 //   3. exact prefix sums of a * 2^149 (each float32 a in [0, 1] is an integer
-//      below 2^150 at that scale) in 192-bit integers, plus B * 2^149;
+//      below 2^150 at that scale) in 192-bit integers, plus B * 2^149; each
+//      thread owns ceil(n / 1024) consecutive sorted positions;
 //   4. E_n = the prefix rounded once to double (round-to-nearest-even),
-//      Theta_n = (E_n / (B + n)) * sps[B + n] with IEEE double ops;
+//      Theta_n = (E_n / (B + n)) * sps[B + n] with IEEE double ops, every n
+//      in parallel (the SPS entries are loaded up front);
 //   5. n* = (first n with !(Theta_n > Theta_{n-1})) - 1, block-wide min;
 //   6. l*_b = number of pairs of request b among the first n* sorted pairs.
 #include "common.cuh"
@@ -23,7 +25,6 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxPairs = 16384;
-constexpr int kPerThread = kMaxPairs / kThreads;   // 16
 
 struct U192 {
     unsigned long long w0, w1, w2;   // little-endian limbs
@@ -101,7 +102,11 @@ schedule_kernel(const float* __restrict__ a, const double* __restrict__ sps, int
     const int n = B * gamma;
     const int R = (n + kThreads - 1) / kThreads;      // rounds per warp chunk
     const int npad = R * kThreads;
-    if (tid == 0) bad_seen = 0;
+    if (tid == 0) {
+        bad_seen = 0;
+        status->code = 0u;                            // this call's status starts clear
+        status->detail = 0u;
+    }
     __syncthreads();
 
     // 1. keys in pair order; validate a in [0, 1]
@@ -123,9 +128,36 @@ schedule_kernel(const float* __restrict__ a, const double* __restrict__ sps, int
     __syncthreads();
     if (tid == 0 && bad_seen) set_status(status, DSPARK_ERR_DEVICE_CHECK, 1);
 
-    // 2. stable LSD radix sort: warp w owns elements [w R 32, (w+1) R 32) in order
     int src = 0;
-    for (int shift = 0; shift < 32; shift += 8) {
+    if (n <= kThreads) {
+        // 2a. up to 1024 pairs: rank by counting.  rank(i) = #{j : k_j < k_i} +
+        //     #{j < i : k_j == k_i}, a stable order; one pair per thread.
+        if (tid < n) {
+            const uint32_t ki = key[0][tid];
+            const int wbase = warp * 32;
+            const int n4 = (n + 3) / 4;                   // keys past n are ~0: never counted
+            const uint4* k4 = reinterpret_cast<const uint4*>(key[0]);
+            int rank = 0;
+            for (int j4 = 0; j4 < wbase / 4; ++j4) {      // j < tid: count k_j <= k_i
+                const uint4 q = k4[j4];
+                rank += (q.x <= ki) + (q.y <= ki) + (q.z <= ki) + (q.w <= ki);
+            }
+            for (int j = wbase; j < wbase + 32 && j < n; ++j) {
+                const uint32_t kj = key[0][j];
+                rank += (kj < ki) || (kj == ki && j < tid);
+            }
+            for (int j4 = (wbase + 32) / 4; j4 < n4; ++j4) {   // j > tid: count k_j < k_i
+                const uint4 q = k4[j4];
+                rank += (q.x < ki) + (q.y < ki) + (q.z < ki) + (q.w < ki);
+            }
+            key[1][rank] = ki;
+            val[1][rank] = static_cast<uint16_t>(tid);
+        }
+        src = 1;
+        __syncthreads();
+    }
+    // 2b. stable LSD radix sort: warp w owns elements [w R 32, (w+1) R 32) in order
+    for (int shift = 0; shift < 32 && n > kThreads; shift += 8) {
         for (int i = tid; i < 256 * kWarps; i += kThreads) hist[i] = 0;
         __syncthreads();
         const int base = warp * R * 32;
@@ -179,13 +211,11 @@ schedule_kernel(const float* __restrict__ a, const double* __restrict__ sps, int
     const uint32_t* skey = key[src];
     const uint16_t* sval = val[src];
 
-    // 3. exact prefix sums: thread t owns sorted positions [16 t, 16 t + 16)
+    // 3. exact prefix sums: thread t owns sorted positions [PT t, PT t + PT)
+    const int PT = R;                                 // ceil(n / 1024), at most 16
+    const int p0 = tid * PT;
     U192 tot{0, 0, 0};
-#pragma unroll
-    for (int q = 0; q < kPerThread; ++q) {
-        const int p = tid * kPerThread + q;
-        if (p < n) tot = add192(tot, scaled_survival(~skey[p]));
-    }
+    for (int q = 0; q < PT && p0 + q < n; ++q) tot = add192(tot, scaled_survival(~skey[p0 + q]));
     U192 inc = tot;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -194,41 +224,87 @@ schedule_kernel(const float* __restrict__ a, const double* __restrict__ sps, int
     }
     if (lane == 31) { wsum[3 * warp] = inc.w0; wsum[3 * warp + 1] = inc.w1; wsum[3 * warp + 2] = inc.w2; }
     __syncthreads();
-    U192 excl{0, 0, static_cast<unsigned long long>(B) << 21};   // B * 2^149
-    for (int q = 0; q < warp; ++q) excl = add192(excl, U192{wsum[3 * q], wsum[3 * q + 1], wsum[3 * q + 2]});
+    if (warp == 0) {                                  // exclusive scan of the warp totals, plus B * 2^149
+        const U192 wt{wsum[3 * lane], wsum[3 * lane + 1], wsum[3 * lane + 2]};
+        U192 wi = wt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const U192 y = shfl_up192(wi, o);
+            if (lane >= o) wi = add192(wi, y);
+        }
+        U192 we = add192(wi, U192{~wt.w0, ~wt.w1, ~wt.w2});
+        we = add192(we, U192{1, 0, 0});               // wi - wt (two's complement)
+        we = add192(we, U192{0, 0, static_cast<unsigned long long>(B) << 21});
+        __syncwarp();
+        wsum[3 * lane] = we.w0;
+        wsum[3 * lane + 1] = we.w1;
+        wsum[3 * lane + 2] = we.w2;
+    }
+    __syncthreads();
+    U192 excl{wsum[3 * warp], wsum[3 * warp + 1], wsum[3 * warp + 2]};
     {
         const U192 y = shfl_up192(inc, 1);
         if (lane >= 1) excl = add192(excl, y);
     }
 
-    // 4-5. Theta along the scan and the first position that does not raise it
-    auto theta_at = [&](int m, U192 E) -> double {    // m pairs taken; E = their scaled sum + B
+    // 4-5. Theta_m for every m, each thread for its own positions, and the
+    //      first m with !(Theta_m > Theta_{m-1}); Theta_{p0} (the comparison
+    //      of a thread's first position) comes from the thread before it.
+    auto theta_at = [&](int m, U192 E, double sps_n) -> double {   // m pairs taken; E = scaled sum + B
         const double Ed = u192_to_double_scaled(E);
-        const int N = B + m;
-        return __dmul_rn(__ddiv_rn(Ed, static_cast<double>(N)), sps[N]);
+        return __dmul_rn(__ddiv_rn(Ed, static_cast<double>(B + m)), sps_n);
     };
+    const bool active = p0 < n;
     int first_fail = 0x7FFFFFFF;
-    if (tid * kPerThread < n) {
-        double prev = theta_at(tid * kPerThread, excl);
+    double th_first = 0.0, th_last = 0.0, fail_prev = 0.0;
+    if (active) {
         U192 run = excl;
-        for (int q = 0; q < kPerThread; ++q) {
-            const int m = tid * kPerThread + q + 1;
-            if (m > n) break;
-            run = add192(run, scaled_survival(~skey[m - 1]));
-            const double th = theta_at(m, run);
-            if (!(th > prev)) { first_fail = m; break; }
-            prev = th;
+        double prev = 0.0;
+        for (int q0 = 0; q0 < PT; q0 += 4) {
+            double sp[4];                             // four SPS loads in flight at once
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int m = p0 + q0 + u + 1;
+                sp[u] = (q0 + u < PT && m <= n) ? sps[B + m] : 0.0;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int q = q0 + u, m = p0 + q + 1;
+                if (q < PT && m <= n) {
+                    run = add192(run, scaled_survival(~skey[m - 1]));
+                    const double th = theta_at(m, run, sp[u]);
+                    if (q == 0) th_first = th;
+                    else if (first_fail == 0x7FFFFFFF && !(th > prev)) { first_fail = m; fail_prev = prev; }
+                    prev = th;
+                    th_last = th;
+                }
+            }
         }
     }
+    __shared__ double wlast[kWarps];
+    double before = __shfl_up_sync(0xffffffffu, th_last, 1);   // Theta_{p0} from the thread before
+    if (lane == 31) wlast[warp] = th_last;
+    __syncthreads();
+    if (lane == 0 && warp > 0) before = wlast[warp - 1];
+    if (tid == 0) before = theta_at(0, excl, sps[B]);           // Theta_0: every request at its bonus row
+    if (active && !(th_first > before)) { first_fail = p0 + 1; fail_prev = before; }
     int fmin = first_fail;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) fmin = min(fmin, __shfl_xor_sync(0xffffffffu, fmin, o));
-    __syncthreads();
     if (lane == 0) red_min[warp] = fmin;
     __syncthreads();
     int nfail = 0x7FFFFFFF;
     for (int q = 0; q < kWarps; ++q) nfail = min(nfail, red_min[q]);
     const int nstar = (nfail == 0x7FFFFFFF) ? n : nfail - 1;
+    // Theta_{n*}: the failing comparison's left side, or the last Theta
+    if (nfail != 0x7FFFFFFF && first_fail == nfail) {
+        *theta = fail_prev;
+        *n_sched = B + nstar;
+    }
+    if (nfail == 0x7FFFFFFF && active && p0 + PT >= n) {
+        *theta = th_last;
+        *n_sched = B + nstar;
+    }
 
     // 6. per-request counts among the first n* sorted pairs (reuse key[src ^ 1])
     int* cnt = reinterpret_cast<int*>(key[src ^ 1]);
@@ -237,14 +313,6 @@ schedule_kernel(const float* __restrict__ a, const double* __restrict__ sps, int
     for (int p = tid; p < nstar; p += kThreads) atomicAdd(&cnt[sval[p] / gamma], 1);
     __syncthreads();
     for (int b = tid; b < B; b += kThreads) ell[b] = cnt[b];
-    // the thread owning position n* reports Theta_{n*} (thread 0 for n* = 0)
-    const int owner = (nstar == 0) ? 0 : (nstar - 1) / kPerThread;
-    if (tid == owner) {
-        U192 E = excl;
-        for (int p = tid * kPerThread; p < nstar; ++p) E = add192(E, scaled_survival(~skey[p]));
-        *theta = theta_at(nstar, E);
-        *n_sched = B + nstar;
-    }
 }
 
 constexpr size_t kSmem = 2 * kMaxPairs * 4 + 2 * kMaxPairs * 2 + 256 * kWarps * 2;
@@ -276,7 +344,6 @@ extern "C" dspark_status_t dspark_schedule_prefix(int B, int gamma, const float*
                                         static_cast<int>(kSmem));
         }) != cudaSuccess)
         return DSPARK_ERR_CUDA;
-    if (clear_status(workspace, s) != DSPARK_OK) return DSPARK_ERR_CUDA;
     schedule_kernel<<<1, kThreads, kSmem, s>>>(a, sps, B, gamma, ell, n_sched, theta,
                                                  static_cast<StatusBlock*>(workspace));
     return launch_status();
