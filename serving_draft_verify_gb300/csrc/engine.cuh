@@ -199,6 +199,19 @@ constexpr int kASlabBytes = kBM * kBK * 2;    // 16 KB
 
 enum Mode : int { kDraft = 0, kResidual = 1 };
 
+// What the final token draw of verification reads and writes (section 8.2:
+// the residual draw after a rejection, or a draw from p_t at the stop row).
+struct FinishArgs {
+    const uint16_t* T;               // t_logits [B][gamma+1][V]
+    const int32_t* krow;             // [B] rejected position (0: none)
+    const int32_t* stop;             // [B] row of the final draw
+    const float* lt2;                // [B]
+    const float* ld2;                // [B]
+    const unsigned long long* res_word;   // [B] residual block winner
+    const unsigned long long* wt;    // [B][gamma+1] target-row block winner
+    int32_t* next_token;             // [B]
+};
+
 struct TcParams {
     int B, gamma, V, r, k;           // k: the position of every row (kDraft)
     const uint16_t* U;               // [B][gamma][V]
@@ -224,6 +237,8 @@ struct TcParams {
     float* logp_d;
     float* c;
     float* a;
+    // kResidual with fuse_tail: the launch also draws the final token
+    FinishArgs fin;
     // kResidual
     const int32_t* krow;             // [B] rejected position k_b (0: row inactive)
     const uint16_t* T;               // t_logits [B][gamma+1][V]
@@ -348,6 +363,89 @@ __device__ __forceinline__ void finalize_position(int b, int k, int B, int gamma
     }
 }
 
+// OR of `v` over the 64 threads of named barrier `bar`.
+__device__ __forceinline__ bool pair_any(bool v, int bar) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, 64, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(bar)
+        : "memory");
+    return r != 0;
+}
+
+// The final token of request b (two warps, named barrier `bar`; xch/xchi: a
+// 2-entry exchange): if a draft token was rejected at k and the residual
+// max(0, p_t - p_d) has mass, the token inside the residual's winning block
+// (second Gumbel level, stream 2); otherwise a draw from p_t at the stop row
+// (bonus row, stream 5) inside that row's winning block.
+template <bool kBF16, int kCPL>
+__device__ __forceinline__ void finish_pair(const FinishArgs& f, int b, int gamma, int V, int r, const void* U,
+                                            const void* W1, const void* W2, const int32_t* x0, const int32_t* x,
+                                            float cscale, uint64_t seed, StatusBlock* st, int bar, float* xch,
+                                            int* xchi) {
+    const int lane = threadIdx.x & 31, wp = (threadIdx.x >> 5) & 1;
+    const int kr = f.krow[b];
+    const unsigned long long rw = (kr > 0) ? __ldcg(f.res_word + b) : 0ull;
+    const uint32_t nblk = static_cast<uint32_t>((V + 63) / 64);
+    bool residual = rw != 0ull && unpack_idx(rw) < nblk;
+    float score = -INFINITY;
+    int v = 0x7FFFFFFF;
+    if (residual) {
+        const int blk = static_cast<int>(unpack_idx(rw));
+        const float z = block_logit<kBF16, kCPL>(b, gamma, kr, V, r, blk, U, W1, W2, x0, x, st);
+        v = blk * 64 + wp * 32 + lane;
+        if (z > -INFINITY) {
+            const float yd = z * cscale;
+            const float yt = ld_elem<kBF16>(f.T, (static_cast<size_t>(b) * (gamma + 1) + (kr - 1)) * V + v) * cscale;
+            const float qv = fast_exp2(yt - f.lt2[b]) - fast_exp2(yd - f.ld2[b]);
+            if (qv > 0.f) {
+                const float g =
+                    gumbel_of(uniform_open(draw_word(seed, b, kr, kStreamResidualToken, static_cast<uint32_t>(v))));
+                score = log2f(qv) * kLn2 + g;
+            }
+        }
+        if (!pair_any(score > -INFINITY, bar)) residual = false;   // no mass left after rounding
+    }
+    bool bad = false;
+    if (!residual) {
+        const int srow = (kr > 0) ? kr : f.stop[b];
+        const unsigned long long w = __ldcg(f.wt + static_cast<size_t>(b) * (gamma + 1) + srow - 1);
+        if (w == 0ull || unpack_idx(w) >= nblk) {
+            if (threadIdx.x % 64 == 0) set_status(st, DSPARK_ERR_DEVICE_CHECK, w == 0ull ? 7 : 9);
+            bad = true;
+        } else {
+            const int blk = static_cast<int>(unpack_idx(w));
+            v = blk * 64 + wp * 32 + lane;
+            score = -INFINITY;
+            if (v < V) {
+                const float yt = ld_elem<kBF16>(f.T, (static_cast<size_t>(b) * (gamma + 1) + (srow - 1)) * V + v) * cscale;
+                const float g =
+                    gumbel_of(uniform_open(draw_word(seed, b, srow, kStreamTargetToken, static_cast<uint32_t>(v))));
+                score = yt + g * kLog2e;
+            }
+        }
+    }
+    int bi = (score > -INFINITY) ? v : 0x7FFFFFFF;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float os = __shfl_xor_sync(0xffffffffu, score, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (os > score || (os == score && oi < bi)) { score = os; bi = oi; }
+    }
+    if (lane == 0) { xch[wp] = score; xchi[wp] = bi; }
+    asm volatile("bar.sync %0, 64;" ::"r"(bar) : "memory");
+    if (wp == 0 && lane == 0) {
+        int w = 0;
+        if (xch[1] > xch[0] || (xch[1] == xch[0] && xchi[1] < xchi[0])) w = 1;
+        f.next_token[b] = (bad || xchi[w] == 0x7FFFFFFF) ? 0 : xchi[w];
+    }
+    asm volatile("bar.sync %0, 64;" ::"r"(bar) : "memory");
+}
+
 // Draw x_k for request b inside a running multi-position launch: a pair of
 // warps (named barrier `bar`, 64 threads) rebuilds z on the winning block from
 // W2 rows and takes the second Gumbel level (stream 0); the even warp's lane 0
@@ -431,7 +529,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
     // Row replication: with at most 64 requests the A tile holds every request
     // twice (TMEM lanes 0-63 and 64-127) and the two copies reduce different
     // 64-token blocks of each tile, so all epilogue warps have work.
-    const int R = (kMode == kDraft && p.B <= 64) ? 2 : 1;
+    const int R = (p.B <= 64) ? 2 : 1;
     const int rpc = kBM / R;                              // request rows per copy
     const int nrows = min(rpc, p.B - m0);                 // requests of this M-tile
     const int k0 = p.k;
@@ -758,6 +856,17 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
             else pro_sync();                              // rowres is rewritten by the next position
         }
 
+        if (kMode == kResidual && p.fuse_tail) {
+            // ------------------------------------------------ final tokens
+            arrive();
+            wait_all();                                   // every CTA published its residual blocks
+            if (warp >= 2 && *s_fail == 0) {
+                const int pair = (warp - 2) >> 1;
+                for (int b = blockIdx.x + pair * gridDim.x; b < p.B; b += 5 * gridDim.x)
+                    finish_pair<true, 1>(p.fin, b, p.gamma, p.V, p.r, p.U, p.W1, p.W2, p.x0, p.x, p.cscale, p.seed,
+                                         st, 2 + pair, reinterpret_cast<float*>(xch + 2 * pair), xchi + 2 * pair);
+            }
+        }
         if (kMode == kDraft && p.fuse_tail && p.debug_z == nullptr) {
             // ------------------------------------------ x_gamma and finalize
             arrive();

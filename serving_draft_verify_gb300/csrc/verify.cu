@@ -42,22 +42,67 @@ struct VerifyWs {
     float* lt2;                    // [B] log2-sum-exp2 of t / T at the rejected row
     float* ld2;                    // [B] lse_d at the rejected row, log2 units
     int32_t* stop;                 // [B] row of the final draw
+    int32_t* row_cnt;              // [N] rows-pass CTAs done with compacted row n
+    int32_t* req_cnt;              // [B] rows of request b whose decision is made
+    int32_t* dec;                  // [B][gamma+1] acceptance of x_k at row k (k <= l*_b)
+    float* lt2row;                 // [B][gamma+1] log2-sum-exp2 of t / T per decided row
+    float* tx;                     // [B][gamma+1] t[b][k][x_k] for k <= l*_b, picked up by the rows pass
+    unsigned int* gbar;            // grid barrier of the residual launch
 };
 
-size_t verify_ws_layout(int B, int gamma, size_t* off) {
+// Workspace: status | plan | gbar | wt | res_word | row_cnt | req_cnt (cleared by
+// the plan kernel) | part | krow | lt2 | ld2 | stop | rows | first | dec | lt2row | tx.
+struct VerifyLayout {
+    size_t plan, gbar, wt, res_word, row_cnt, req_cnt, part, krow, lt2, ld2, stop, rows, first, dec, lt2row, tx, total;
+};
+
+VerifyLayout verify_ws_layout(int B, int gamma) {
+    VerifyLayout L{};
+    const size_t rows = static_cast<size_t>(B) * (gamma + 1), nb = static_cast<size_t>(B);
     size_t o = kStatusBytes;
-    const size_t rows = static_cast<size_t>(B) * (gamma + 1);
-    off[0] = o; o += round_up(rows * 8, 256);                 // wt
-    off[1] = o; o += round_up(static_cast<size_t>(B) * 8, 256);   // res_word
-    off[2] = o; o += round_up(rows * kNchMax * 8, 256);       // part
-    off[3] = o; o += round_up(static_cast<size_t>(B) * 4, 256);   // krow
-    off[4] = o; o += round_up(static_cast<size_t>(B) * 4, 256);   // lt2
-    off[5] = o; o += round_up(static_cast<size_t>(B) * 4, 256);   // ld2
-    off[6] = o; o += round_up(static_cast<size_t>(B) * 4, 256);   // stop
-    off[7] = o; o += round_up(rows * 4, 256);                 // compacted rows
-    off[8] = o; o += 256;                                     // plan
-    off[9] = o; o += round_up(static_cast<size_t>(B) * 4, 256);   // first
-    return o;
+    auto take = [&](size_t& off, size_t bytes) { off = o; o += round_up(bytes, 256); };
+    take(L.plan, 16);
+    take(L.gbar, 16);
+    take(L.wt, rows * 8);
+    take(L.res_word, nb * 8);
+    take(L.row_cnt, rows * 4);
+    take(L.req_cnt, nb * 4);
+    take(L.part, rows * kNchMax * 8);
+    take(L.krow, nb * 4);
+    take(L.lt2, nb * 4);
+    take(L.ld2, nb * 4);
+    take(L.stop, nb * 4);
+    take(L.rows, rows * 4);
+    take(L.first, nb * 4);
+    take(L.dec, rows * 4);
+    take(L.lt2row, rows * 4);
+    take(L.tx, rows * 4);
+    L.total = o;
+    return L;
+}
+
+VerifyWs verify_ws(void* workspace, int B, int gamma) {
+    const VerifyLayout L = verify_ws_layout(B, gamma);
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    VerifyWs ws;
+    ws.status = reinterpret_cast<StatusBlock*>(w);
+    ws.rows = reinterpret_cast<int32_t*>(w + L.rows);
+    ws.first = reinterpret_cast<int32_t*>(w + L.first);
+    ws.plan = reinterpret_cast<int32_t*>(w + L.plan);
+    ws.wt = reinterpret_cast<unsigned long long*>(w + L.wt);
+    ws.part = reinterpret_cast<float2*>(w + L.part);
+    ws.res_word = reinterpret_cast<unsigned long long*>(w + L.res_word);
+    ws.krow = reinterpret_cast<int32_t*>(w + L.krow);
+    ws.lt2 = reinterpret_cast<float*>(w + L.lt2);
+    ws.ld2 = reinterpret_cast<float*>(w + L.ld2);
+    ws.stop = reinterpret_cast<int32_t*>(w + L.stop);
+    ws.row_cnt = reinterpret_cast<int32_t*>(w + L.row_cnt);
+    ws.req_cnt = reinterpret_cast<int32_t*>(w + L.req_cnt);
+    ws.dec = reinterpret_cast<int32_t*>(w + L.dec);
+    ws.lt2row = reinterpret_cast<float*>(w + L.lt2row);
+    ws.tx = reinterpret_cast<float*>(w + L.tx);
+    ws.gbar = reinterpret_cast<unsigned int*>(w + L.gbar);
+    return ws;
 }
 
 __device__ __forceinline__ int clamp_ell(const int32_t* ell, int b, int gamma, StatusBlock* st) {
@@ -89,9 +134,16 @@ verify_plan(int B, int gamma, int V, int rows_ctas, const int32_t* __restrict__ 
     __shared__ int carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const size_t nrows = static_cast<size_t>(B) * (gamma + 1);
-    for (size_t i = tid; i < nrows; i += kPlanThreads) ws.wt[i] = 0ull;
-    for (int i = tid; i < B; i += kPlanThreads) ws.res_word[i] = 0ull;
+    for (size_t i = tid; i < nrows; i += kPlanThreads) {
+        ws.wt[i] = 0ull;
+        ws.row_cnt[i] = 0;
+    }
+    for (int i = tid; i < B; i += kPlanThreads) {
+        ws.res_word[i] = 0ull;
+        ws.req_cnt[i] = 0;
+    }
     if (tid < static_cast<int>(kStatusBytes / 4)) reinterpret_cast<uint32_t*>(ws.status)[tid] = 0u;
+    if (tid == 0) *ws.gbar = 0u;
     if (tid == 0) carry = 0;
     __syncthreads();
     for (int base = 0; base < B; base += kPlanThreads) {
@@ -135,6 +187,88 @@ verify_plan(int B, int gamma, int V, int rows_ctas, const int32_t* __restrict__ 
     }
 }
 
+// --------------------------------------------------------- row decisions ---
+// One warp, run by the rows-pass CTA that finished row (b, k) last: for
+// k <= l*_b the acceptance test of x_k (u < p_t(x_k) / p_d(x_k), u from
+// stream 1; greedy: x_k == argmax t_k), and, if this was the last of request
+// b's l*_b + 1 rows, the request's outcome: n_accept, the stop row, and what
+// the final draw needs (greedy: the token itself).
+template <bool kBF16>
+__device__ __noinline__ void decide_row(int n, int row, int b, int k, int gamma, int V, int per, int npad,
+                                        const void* __restrict__ t, const int32_t* __restrict__ x,
+                                        const float* __restrict__ lse_d, const float* __restrict__ logp_d,
+                                        const int32_t* __restrict__ ell, float cscale, int greedy, uint64_t seed,
+                                        int32_t* __restrict__ n_accept, int32_t* __restrict__ next_token,
+                                        const VerifyWs& ws) {
+    const int lane = threadIdx.x & 31;
+    const int e = clamp_ell(ell, b, gamma, ws.status);
+    if (k <= e) {
+        int xk = x[b * gamma + k - 1];
+        if (xk < 0 || xk >= V) {
+            if (lane == 0) set_status(ws.status, DSPARK_ERR_DEVICE_CHECK, 5);
+            xk = 0;
+        }
+        bool ok;
+        float Lt2 = 0.f;
+        if (greedy) {
+            const unsigned long long w = __ldcg(ws.wt + row);
+            ok = (w != 0ull) && static_cast<int>(unpack_idx(w)) == xk;
+        } else {
+            // the rows-pass CTAs that covered this row wrote slots 0 .. c_last - c_first
+            const long long g0 = static_cast<long long>(n) * npad;
+            const int nch = static_cast<int>((g0 + npad - 1) / per - g0 / per) + 1;
+            float m = -INFINITY, s = 0.f;
+            for (int c = lane; c < nch; c += 32) {
+                const float2 pr = __ldcg(ws.part + static_cast<size_t>(row) * kNchMax + c);
+                lse_merge(m, s, pr.x, pr.y);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float om = __shfl_xor_sync(0xffffffffu, m, o);
+                const float os = __shfl_xor_sync(0xffffffffu, s, o);
+                lse_merge(m, s, om, os);
+            }
+            Lt2 = m + log2f(s);
+            const float yk = __ldcg(ws.tx + row) * cscale;
+            const float ratio = expf((yk - Lt2) * kLn2 - logp_d[b * gamma + k - 1]);
+            const float u = uniform_accept(draw_word(seed, b, k, kStreamAccept, 0));
+            ok = u < ratio;
+        }
+        if (lane == 0) {
+            ws.dec[row] = ok ? 1 : 0;
+            ws.lt2row[row] = Lt2;
+        }
+    }
+    int last = 0;
+    if (lane == 0) {
+        __threadfence();                                  // this row's decision before the count
+        last = atomicAdd(ws.req_cnt + b, 1) == e;         // rows k = 1 .. e + 1
+        __threadfence();
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    // the request's first rejection (gamma <= 32: one lane per position)
+    const int kk = lane + 1;
+    const bool rejected = kk <= e && __ldcg(ws.dec + b * (gamma + 1) + kk - 1) == 0;
+    const unsigned mask = __ballot_sync(0xffffffffu, rejected);
+    const int rej = mask ? __ffs(mask) : 0;
+    if (lane == 0) {
+        const int nacc = rej ? rej - 1 : e;
+        n_accept[b] = nacc;
+        const int srow = nacc + 1;                        // row of the final draw
+        ws.stop[b] = srow;
+        if (greedy) {
+            const unsigned long long w = __ldcg(ws.wt + static_cast<size_t>(b) * (gamma + 1) + srow - 1);
+            if (w == 0ull) set_status(ws.status, DSPARK_ERR_DEVICE_CHECK, 6);
+            next_token[b] = (w == 0ull || unpack_idx(w) >= static_cast<uint32_t>(V)) ? 0 : static_cast<int>(unpack_idx(w));
+            ws.krow[b] = 0;
+        } else {
+            ws.krow[b] = rej;
+            ws.lt2[b] = rej ? __ldcg(ws.lt2row + b * (gamma + 1) + rej - 1) : 0.f;
+            ws.ld2[b] = rej ? lse_d[b * gamma + rej - 1] * kLog2e : 0.f;
+        }
+    }
+}
+
 // ------------------------------------------------------------- rows pass ---
 // CTA c takes blocks [c per, (c+1) per) of the padded scheduled rows laid end
 // to end, one piece per row it touches; per piece a warp covers 4 quads of 4
@@ -142,13 +276,17 @@ verify_plan(int B, int gamma, int V, int rows_ctas, const int32_t* __restrict__ 
 // 64-token block: the logsumexp of t / T and a Gumbel key for a draw from p_t
 // (greedy: the argmax of t); per piece the CTA's best and its (max, sum).
 // Sixteen lanes finish the 16 blocks of a step, one block each.
-constexpr int kRowsCtasPerSm = 4;
+constexpr int kRowsCtasPerSm = 3;
 
 template <bool kBF16>
 __global__ void __launch_bounds__(256, kRowsCtasPerSm)
-verify_rows(int gamma, int V, const void* __restrict__ t, float cscale, int greedy, uint64_t seed, VerifyWs ws) {
+verify_rows(int gamma, int V, const void* __restrict__ t, const int32_t* __restrict__ x,
+            const float* __restrict__ lse_d, const float* __restrict__ logp_d, const int32_t* __restrict__ ell,
+            float cscale, int greedy, uint64_t seed, int32_t* __restrict__ n_accept, int32_t* __restrict__ next_token,
+            VerifyWs ws) {
     __shared__ float rk[8], rm[8], rs[8];
     __shared__ int ri[8];
+    __shared__ int s_last;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sub = lane >> 3, part = lane & 7;
     const int nblk = (V + 63) / 64, npad = padded_blocks(V);
@@ -167,6 +305,12 @@ verify_rows(int gamma, int V, const void* __restrict__ t, float cscale, int gree
             const int row = ws.rows[n];
             const int b = row / (gamma + 1), k = row % (gamma + 1) + 1;
             const size_t rowoff = static_cast<size_t>(row) * V;
+            // x_k of a decided row: the lane that loads it keeps t[x_k] for the decision
+            int e = ell[b];
+            e = e < 0 ? 0 : (e > gamma ? gamma : e);
+            const int xk = (k <= e) ? x[b * gamma + k - 1] : -1;
+            float txk = 0.f;
+            bool have_tx = false;
             float best = -INFINITY, M = -INFINITY, S = 0.f;
             int best_i = 0x7FFFFFFF;
             // each warp takes 4 consecutive quads per step; all loads of a step are issued first
@@ -198,6 +342,16 @@ verify_rows(int gamma, int V, const void* __restrict__ t, float cscale, int gree
                                 }
                             }
                         }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int d = xk - (((q0 + u) * 4 + sub) * 64 + part * 8);
+                    if (static_cast<unsigned>(d) < 8u && (q0 + u) * 4 + sub < hi) {   // rare: one lane, one step
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            if (i == d) txk = y[u][i];
+                        have_tx = true;
                     }
                 }
                 if (greedy) {
@@ -257,6 +411,7 @@ verify_rows(int gamma, int V, const void* __restrict__ t, float cscale, int gree
                 if (ob > best || (ob == best && oi < best_i)) { best = ob; best_i = oi; }
                 lse_merge(M, S, om, os);
             }
+            if (have_tx) ws.tx[row] = txk;
             if (lane == 0) { rk[warp] = best; ri[warp] = best_i; rm[warp] = M; rs[warp] = S; }
             __syncthreads();
             if (threadIdx.x == 0) {
@@ -268,81 +423,18 @@ verify_rows(int gamma, int V, const void* __restrict__ t, float cscale, int gree
                 }
                 if (!greedy) ws.part[static_cast<size_t>(row) * kNchMax + slot] = make_float2(m, s);
                 if (bk > -INFINITY) atomicMax(&ws.wt[row], pack_key(bk, static_cast<uint32_t>(bi)));
+                // the CTA that completes the row makes its decision
+                const long long g0 = static_cast<long long>(n) * npad;
+                const int ncta = static_cast<int>((g0 + npad - 1) / per - g0 / per) + 1;
+                __threadfence();
+                s_last = atomicAdd(ws.row_cnt + n, 1) == ncta - 1;
+                __threadfence();
             }
             __syncthreads();                              // rk..ri are rewritten by the next piece
+            if (s_last && warp == 0)
+                decide_row<kBF16>(n, row, b, k, gamma, V, per, npad, t, x, lse_d, logp_d, ell, cscale, greedy, seed,
+                                  n_accept, next_token, ws);
             g += hi_pad - lo;
-        }
-    }
-}
-
-// ------------------------------------------------------------ chain pass ---
-template <bool kBF16>
-__global__ void __launch_bounds__(256)
-verify_chain(int B, int gamma, int V, const void* __restrict__ t, const int32_t* __restrict__ x,
-             const float* __restrict__ lse_d, const float* __restrict__ logp_d, const int32_t* __restrict__ ell,
-             float cscale, int greedy, uint64_t seed, int32_t* __restrict__ n_accept,
-             int32_t* __restrict__ next_token, VerifyWs ws) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b = blockIdx.x * 8 + warp;
-    if (b >= B) return;
-    const int e = clamp_ell(ell, b, gamma, ws.status);
-    const int per = ws.plan[1], npad = padded_blocks(V), n0 = ws.first[b];
-    int nacc = 0, rej = 0;
-    float rej_lt2 = 0.f;
-    for (int k = 1; k <= e; ++k) {
-        const int row = b * (gamma + 1) + (k - 1);
-        int xk = x[b * gamma + k - 1];
-        if (xk < 0 || xk >= V) {
-            if (lane == 0) set_status(ws.status, DSPARK_ERR_DEVICE_CHECK, 5);
-            xk = 0;
-        }
-        bool ok;
-        float Lt2 = 0.f;
-        if (greedy) {
-            const unsigned long long w = ws.wt[row];
-            ok = (w != 0ull) && static_cast<int>(unpack_idx(w)) == xk;
-        } else {
-            // the rows-pass CTAs that covered this row wrote slots 0 .. c_last - c_first
-            const long long g0 = static_cast<long long>(n0 + k - 1) * npad;
-            const int nch = static_cast<int>((g0 + npad - 1) / per - g0 / per) + 1;
-            float m = -INFINITY, s = 0.f;
-            for (int c = lane; c < nch; c += 32) {
-                const float2 pr = ws.part[static_cast<size_t>(row) * kNchMax + c];
-                lse_merge(m, s, pr.x, pr.y);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float om = __shfl_xor_sync(0xffffffffu, m, o);
-                const float os = __shfl_xor_sync(0xffffffffu, s, o);
-                lse_merge(m, s, om, os);
-            }
-            Lt2 = m + log2f(s);
-            const float yk = ld_elem<kBF16>(t, static_cast<size_t>(row) * V + xk) * cscale;
-            const float ratio = expf((yk - Lt2) * kLn2 - logp_d[b * gamma + k - 1]);
-            const float u = uniform_accept(draw_word(seed, b, k, kStreamAccept, 0));
-            ok = u < ratio;
-        }
-        if (ok) {
-            ++nacc;
-        } else {
-            rej = k;
-            rej_lt2 = Lt2;
-            break;
-        }
-    }
-    if (lane == 0) {
-        n_accept[b] = nacc;
-        const int srow = nacc + 1;                        // row of the final draw
-        ws.stop[b] = srow;
-        if (greedy) {
-            const unsigned long long w = ws.wt[b * (gamma + 1) + srow - 1];
-            if (w == 0ull) set_status(ws.status, DSPARK_ERR_DEVICE_CHECK, 6);
-            next_token[b] = (w == 0ull || unpack_idx(w) >= static_cast<uint32_t>(V)) ? 0 : static_cast<int>(unpack_idx(w));
-            ws.krow[b] = 0;
-        } else {
-            ws.krow[b] = rej;
-            ws.lt2[b] = rej_lt2;
-            ws.ld2[b] = rej ? lse_d[b * gamma + rej - 1] * kLog2e : 0.f;
         }
     }
 }
@@ -403,73 +495,16 @@ residual_simt(int B, int gamma, int V, int r, const void* __restrict__ t, const 
 }
 
 // ----------------------------------------------------------- finish pass ---
-// Two warps per request (T > 0): the token inside the winning block of the
-// residual, or of the draw from p_t at the stop row.
+// Two warps per request (T > 0): eng::finish_pair, for the paths whose
+// residual launch does not draw the final token itself.
 template <bool kBF16, int kCPL>
 __global__ void __launch_bounds__(64)
-verify_finish(int B, int gamma, int V, int r, const void* __restrict__ t, const void* __restrict__ U,
-              const void* __restrict__ W1, const void* __restrict__ W2, const int32_t* __restrict__ x0,
-              const int32_t* __restrict__ x, float cscale, uint64_t seed, int32_t* __restrict__ next_token,
-              VerifyWs ws) {
-    __shared__ float sbest[2];
-    __shared__ int sidx[2];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b = blockIdx.x;
-    const int kr = ws.krow[b];
-    const unsigned long long rw = (kr > 0) ? ws.res_word[b] : 0ull;
-    const uint32_t nblk = static_cast<uint32_t>((V + 63) / 64);
-    bool residual = rw != 0ull && unpack_idx(rw) < nblk;
-    float score = -INFINITY;
-    int v = 0x7FFFFFFF;
-    if (residual) {
-        const int blk = static_cast<int>(unpack_idx(rw));
-        const float z = eng::block_logit<kBF16, kCPL>(b, gamma, kr, V, r, blk, U, W1, W2, x0, x, ws.status);
-        v = blk * 64 + warp * 32 + lane;
-        if (z > -INFINITY) {
-            const float yd = z * cscale;
-            const float yt = ld_elem<kBF16>(t, (static_cast<size_t>(b) * (gamma + 1) + (kr - 1)) * V + v) * cscale;
-            const float qv = fast_exp2(yt - ws.lt2[b]) - fast_exp2(yd - ws.ld2[b]);
-            if (qv > 0.f) {
-                const float g = gumbel_of(uniform_open(draw_word(seed, b, kr, kStreamResidualToken, static_cast<uint32_t>(v))));
-                score = log2f(qv) * kLn2 + g;
-            }
-        }
-        if (!__syncthreads_or(score > -INFINITY)) residual = false;   // no mass left after rounding
-    }
-    if (!residual) {
-        const int srow = (kr > 0) ? kr : ws.stop[b];
-        const unsigned long long w = ws.wt[b * (gamma + 1) + srow - 1];
-        if (w == 0ull) {
-            if (threadIdx.x == 0) { set_status(ws.status, DSPARK_ERR_DEVICE_CHECK, 7); next_token[b] = 0; }
-            return;
-        }
-        if (unpack_idx(w) >= nblk) {
-            if (threadIdx.x == 0) { set_status(ws.status, DSPARK_ERR_DEVICE_CHECK, 9); next_token[b] = 0; }
-            return;
-        }
-        const int blk = static_cast<int>(unpack_idx(w));
-        v = blk * 64 + warp * 32 + lane;
-        score = -INFINITY;
-        if (v < V) {
-            const float yt = ld_elem<kBF16>(t, (static_cast<size_t>(b) * (gamma + 1) + (srow - 1)) * V + v) * cscale;
-            const float g = gumbel_of(uniform_open(draw_word(seed, b, srow, kStreamTargetToken, static_cast<uint32_t>(v))));
-            score = yt + g * kLog2e;
-        }
-    }
-    int bi = (score > -INFINITY) ? v : 0x7FFFFFFF;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float os = __shfl_xor_sync(0xffffffffu, score, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (os > score || (os == score && oi < bi)) { score = os; bi = oi; }
-    }
-    if (lane == 0) { sbest[warp] = score; sidx[warp] = bi; }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int w = 0;
-        if (sbest[1] > sbest[0] || (sbest[1] == sbest[0] && sidx[1] < sidx[0])) w = 1;
-        next_token[b] = (sidx[w] == 0x7FFFFFFF) ? 0 : sidx[w];
-    }
+verify_finish(int gamma, int V, int r, eng::FinishArgs f, const void* __restrict__ U, const void* __restrict__ W1,
+              const void* __restrict__ W2, const int32_t* __restrict__ x0, const int32_t* __restrict__ x, float cscale,
+              uint64_t seed, StatusBlock* st) {
+    __shared__ float xch[2];
+    __shared__ int xchi[2];
+    eng::finish_pair<kBF16, kCPL>(f, blockIdx.x, gamma, V, r, U, W1, W2, x0, x, cscale, seed, st, 1, xch, xchi);
 }
 
 }  // namespace
@@ -481,8 +516,7 @@ extern "C" size_t dspark_verify_workspace_size(int B, int gamma, int V, int r) {
     (void)V;
     (void)r;
     if (B <= 0 || gamma <= 0) return kStatusBytes;
-    size_t off[10];
-    return verify_ws_layout(B, gamma, off);
+    return verify_ws_layout(B, gamma).total;
 }
 
 extern "C" dspark_status_t dspark_verify(int B, int gamma, int V, int r, dspark_dtype_t dt, const void* t_logits,
@@ -503,35 +537,30 @@ extern "C" dspark_status_t dspark_verify(int B, int gamma, int V, int r, dspark_
     if (workspace == nullptr || !aligned256(workspace)) return DSPARK_ERR_INVALID_ARGUMENT;
     if (workspace_bytes < dspark_verify_workspace_size(B, gamma, V, r)) return DSPARK_ERR_WORKSPACE_TOO_SMALL;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    size_t off[10];
-    verify_ws_layout(B, gamma, off);
-    uint8_t* wsb = static_cast<uint8_t*>(workspace);
-    VerifyWs ws{reinterpret_cast<StatusBlock*>(wsb), reinterpret_cast<int32_t*>(wsb + off[7]),
-                reinterpret_cast<int32_t*>(wsb + off[9]), reinterpret_cast<int32_t*>(wsb + off[8]), reinterpret_cast<unsigned long long*>(wsb + off[0]),
-                reinterpret_cast<float2*>(wsb + off[2]), reinterpret_cast<unsigned long long*>(wsb + off[1]),
-                reinterpret_cast<int32_t*>(wsb + off[3]), reinterpret_cast<float*>(wsb + off[4]),
-                reinterpret_cast<float*>(wsb + off[5]), reinterpret_cast<int32_t*>(wsb + off[6])};
+    const VerifyWs ws = verify_ws(workspace, B, gamma);
     const int greedy = (temperature == 0.f);
     const float cscale = greedy ? 1.f : kLog2e / temperature;
     const bool bf = (dt == DSPARK_BF16);
     const int nblk = (V + 63) / 64;
-    // persistent rows pass: all resident CTAs
+    // plan, then the persistent rows pass (all resident CTAs) with the per-row
+    // decisions and per-request outcomes made by the CTAs that finish them
     const int rgrid = kRowsCtasPerSm * sm_count(current_device());
     verify_plan<<<1, kPlanThreads, 0, s>>>(B, gamma, V, rgrid, ell, ws);
     dspark_status_t stt = launch_status();
     if (stt != DSPARK_OK) return stt;
-    if (bf) verify_rows<true><<<rgrid, 256, 0, s>>>(gamma, V, t_logits, cscale, greedy, seed, ws);
-    else verify_rows<false><<<rgrid, 256, 0, s>>>(gamma, V, t_logits, cscale, greedy, seed, ws);
-    if ((stt = launch_status()) != DSPARK_OK) return stt;
-    const int cgrid = (B + 7) / 8;
     if (bf)
-        verify_chain<true><<<cgrid, 256, 0, s>>>(B, gamma, V, t_logits, x, lse_d, logp_d, ell, cscale, greedy, seed,
-                                                 n_accept, next_token, ws);
+        verify_rows<true><<<rgrid, 256, 0, s>>>(gamma, V, t_logits, x, lse_d, logp_d, ell, cscale, greedy, seed,
+                                                n_accept, next_token, ws);
     else
-        verify_chain<false><<<cgrid, 256, 0, s>>>(B, gamma, V, t_logits, x, lse_d, logp_d, ell, cscale, greedy,
-                                                  seed, n_accept, next_token, ws);
+        verify_rows<false><<<rgrid, 256, 0, s>>>(gamma, V, t_logits, x, lse_d, logp_d, ell, cscale, greedy, seed,
+                                                 n_accept, next_token, ws);
     if ((stt = launch_status()) != DSPARK_OK || greedy) return stt;
 
+    eng::FinishArgs f{};
+    f.T = static_cast<const uint16_t*>(t_logits);
+    f.krow = ws.krow; f.stop = ws.stop; f.lt2 = ws.lt2; f.ld2 = ws.ld2;
+    f.res_word = ws.res_word; f.wt = ws.wt; f.next_token = next_token;
+    bool drawn = false;                                   // final tokens drawn by the residual launch
     if (eng::use_tc_path(dt, r)) {
         CUtensorMap map;
         if (!eng::encode_w2_map(&map, W2, V, r)) return DSPARK_ERR_CUDA;
@@ -543,9 +572,13 @@ extern "C" dspark_status_t dspark_verify(int B, int gamma, int V, int r, dspark_
         p.W2 = static_cast<const uint16_t*>(W2); p.k_last = 1;
         p.x0 = x0; p.x = const_cast<int32_t*>(x); p.cscale = cscale; p.greedy = 0;   // read only here
         p.seed = seed; p.P = P;
-        p.ws = eng::Ws{ws.status, ws.res_word, nullptr, nullptr, nullptr, nullptr};
+        p.ws = eng::Ws{ws.status, ws.res_word, nullptr, nullptr, ws.gbar, nullptr};
         p.krow = ws.krow; p.T = static_cast<const uint16_t*>(t_logits); p.lt2 = ws.lt2; p.ld2 = ws.ld2;
-        if ((stt = eng::launch_tc<eng::kResidual>(map, p, nM * P, s, false)) != DSPARK_OK) return stt;
+        // with a co-resident grid the same launch draws the final tokens
+        drawn = nM * P <= sm_count(current_device());
+        p.fuse_tail = drawn ? 1 : 0;
+        p.fin = f;
+        if ((stt = eng::launch_tc<eng::kResidual>(map, p, nM * P, s, drawn)) != DSPARK_OK) return stt;
     } else {
         int nchunk = (nblk + 7) / 8;
         if (nchunk > 256) nchunk = 256;
@@ -554,11 +587,12 @@ extern "C" dspark_status_t dspark_verify(int B, int gamma, int V, int r, dspark_
         else residual_simt<false><<<g, 256, 0, s>>>(B, gamma, V, r, t_logits, U, W1, W2, x0, x, cscale, seed, nchunk, ws);
         if ((stt = launch_status()) != DSPARK_OK) return stt;
     }
+    if (drawn) return DSPARK_OK;
     if (bf)
-        verify_finish<true, 1><<<B, 64, 0, s>>>(B, gamma, V, r, t_logits, U, W1, W2, x0, x, cscale, seed, next_token, ws);
+        verify_finish<true, 1><<<B, 64, 0, s>>>(gamma, V, r, f, U, W1, W2, x0, x, cscale, seed, ws.status);
     else if (r <= 128)
-        verify_finish<false, 1><<<B, 64, 0, s>>>(B, gamma, V, r, t_logits, U, W1, W2, x0, x, cscale, seed, next_token, ws);
+        verify_finish<false, 1><<<B, 64, 0, s>>>(gamma, V, r, f, U, W1, W2, x0, x, cscale, seed, ws.status);
     else
-        verify_finish<false, 2><<<B, 64, 0, s>>>(B, gamma, V, r, t_logits, U, W1, W2, x0, x, cscale, seed, next_token, ws);
+        verify_finish<false, 2><<<B, 64, 0, s>>>(gamma, V, r, f, U, W1, W2, x0, x, cscale, seed, ws.status);
     return launch_status();
 }
