@@ -46,8 +46,8 @@ def peaks():
 
 
 def engine_source_hash():
-    """Hash of the draft phase kernel's sources: a recorded ncu traffic figure is
-    only reported while the kernel it was measured on is unchanged."""
+    """Hash of the draft engine's sources: a recorded ncu traffic figure is only
+    reported while the kernel it was measured on is unchanged."""
     import hashlib
     h = hashlib.sha256()
     for f in ("engine.cuh", "draft.cu", "tc.cuh", "common.cuh"):
@@ -56,8 +56,8 @@ def engine_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_phase_traffic():
-    p = os.path.join(ROOT, "profiles", "draft_phase_traffic.json")
+def recorded_engine_traffic():
+    p = os.path.join(ROOT, "profiles", "draft_engine_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
@@ -79,6 +79,20 @@ def dist_setup():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def aggregate(local_ms, local_rows, world, device):
+    """Whole-job figures over `world` ranks: the slowest rank's time and the
+    rows of all ranks (every rank calls this, after its own timed region)."""
+    if world == 1:
+        return float(local_ms), int(local_rows)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    n = torch.tensor([int(local_rows)], dtype=torch.int64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(n.item())
 
 
 # ------------------------------------------------------------ clocks ---
@@ -199,13 +213,7 @@ def run_gpu(args):
     clk = clocks.stop()
     dsv._binding.phase_timing(False)
     assert dsv.workspace_status(ws_d) == 0 and dsv.workspace_status(ws_v) == 0
-    total_ms = sum(times)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    rows = B * G * args.steps * world
+    total_ms, rows = aggregate(sum(times), B * G * args.steps, world, dev)
     value = rows / (total_ms * 1e-3)
     ms_per_step = total_ms / args.steps
 
@@ -230,7 +238,7 @@ def run_gpu(args):
     achieved = launch_bytes / (phase_avg * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": "bias_engine_tc<kDraft> (draft block, all positions)",
                 "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "traffic": args.phase_traffic if args.phase_traffic is not None else recorded_phase_traffic(),
+                "traffic": args.phase_traffic if args.phase_traffic is not None else recorded_engine_traffic(),
                 "peak_kind": f"{peak_kind} (copy bandwidth)", "bytes_per_launch": int(launch_bytes),
                 "avg_launch_us": round(phase_avg * 1e3, 2), "launches_timed": len(ph)}
 
@@ -273,8 +281,8 @@ def run_gpu(args):
         tv = {"rows": d_.shape[0], "ms": tv_ms, "rows_per_s": d_.shape[0] / (tv_ms * 1e-3),
               "achieved_gbs": tvb / (tv_ms * 1e-3) / 1e9, "frac_of_peak": tvb / (tv_ms * 1e-3) / 1e9 / peak}
         del d_, t_
-    # draft: engine, winner (x_gamma), finalize; schedule: 1; verify: rows, chain, residual, finish
-    launches_per_step = 3 + 1 + 4
+    # draft: the cooperative engine launch; schedule: 1; verify: plan, rows, residual (+ final token)
+    launches_per_step = 1 + 1 + 3
 
     line = {"metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",

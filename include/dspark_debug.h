@@ -44,6 +44,16 @@ int dspark_debug_phase_times(float* ms, int n);
  * co-resident).  Results are identical either way.  Process-wide flag. */
 dspark_status_t dspark_debug_force_phase_launches(int enable);
 
+/* Test hook for the bounded waits: one thread waits at the grid barrier kept
+ * in a draft workspace (dspark_draft_block_workspace_size(1, 1, 1, 8) bytes,
+ * 256-byte aligned) for an arrival that never comes, giving up after
+ * limit_ns nanoseconds (1 .. 100 ms) with DSPARK_ERR_TIMEOUT in the
+ * workspace's status block -- the same wait routine and status path the
+ * cooperative draft and verify launches use.  The device context stays
+ * usable.  Asynchronous on `stream`. */
+dspark_status_t dspark_debug_bounded_wait(void* workspace, size_t workspace_bytes, uint64_t limit_ns,
+                                          dspark_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

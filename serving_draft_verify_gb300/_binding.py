@@ -43,6 +43,7 @@ _SIGNATURES = {
     "dspark_debug_enable_phase_timing": (_c_int, [_c_int]),
     "dspark_debug_phase_times": (_c_int, [_p, _c_int]),
     "dspark_debug_force_phase_launches": (_c_int, [_c_int]),
+    "dspark_debug_bounded_wait": (_c_int, [_p, _c_size, ctypes.c_uint64, _p]),
 }
 
 _lib = None
@@ -276,6 +277,15 @@ def force_phase_launches(enable):
     """Test hook: the tensor-core draft path launches per position instead of
     its single cooperative launch."""
     _check("dspark_debug_force_phase_launches", load().dspark_debug_force_phase_launches(1 if enable else 0))
+
+
+def bounded_wait(limit_ns, workspace=None, stream=None):
+    """Test hook: a wait that nothing ends, bounded by limit_ns; returns the workspace."""
+    lib = load()
+    ws = _workspace(lib.dspark_draft_block_workspace_size(1, 1, 1, 8), torch.device("cuda"), workspace)
+    _check("dspark_debug_bounded_wait", lib.dspark_debug_bounded_wait(_ptr(ws), _nbytes(ws), int(limit_ns),
+                                                                      _stream(stream)))
+    return ws
 
 
 def phase_times():

@@ -419,3 +419,27 @@ extern "C" int dspark_debug_phase_times(float* ms, int n) {
     }
     return m;
 }
+
+// ---------------------------------------------------------------- debug ---
+namespace dspark {
+namespace {
+// One thread waits at the grid barrier of the draft workspace for an epoch
+// that no CTA arrives at; the bounded wait must give up and report.
+__global__ void debug_bounded_wait(const unsigned int* ctr, uint64_t limit_ns, StatusBlock* st) {
+    if (threadIdx.x == 0 && !eng::grid_wait(ctr, 1u, limit_ns)) set_status(st, DSPARK_ERR_TIMEOUT, 99);
+}
+}  // namespace
+}  // namespace dspark
+
+extern "C" dspark_status_t dspark_debug_bounded_wait(void* workspace, size_t workspace_bytes, uint64_t limit_ns,
+                                                     dspark_stream_t stream) {
+    if (workspace == nullptr || !aligned256(workspace)) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (workspace_bytes < dspark_draft_block_workspace_size(1, 1, 1, 8)) return DSPARK_ERR_WORKSPACE_TOO_SMALL;
+    if (limit_ns == 0 || limit_ns > 100000000ull) return DSPARK_ERR_INVALID_ARGUMENT;   // at most 100 ms
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    size_t clear = 0;
+    const DraftWs ws = draft_ws(workspace, 1, 1, &clear);
+    if (cudaMemsetAsync(workspace, 0, clear, s) != cudaSuccess) return DSPARK_ERR_CUDA;
+    debug_bounded_wait<<<1, 32, 0, s>>>(ws.gbar, limit_ns, ws.status);
+    return launch_status();
+}

@@ -258,7 +258,8 @@ __device__ __forceinline__ void grid_arrive(unsigned int* ctr) {
     __threadfence();
     atomicAdd(ctr, 1u);
 }
-__device__ __forceinline__ bool grid_wait(const unsigned int* ctr, unsigned int target) {
+__device__ __forceinline__ bool grid_wait(const unsigned int* ctr, unsigned int target,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     auto load = [&]() {
         unsigned int v;
         asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
@@ -268,7 +269,7 @@ __device__ __forceinline__ bool grid_wait(const unsigned int* ctr, unsigned int 
     const uint64_t t0 = globaltimer_ns();
     while (load() < target) {
         __nanosleep(64);
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
     return true;
 }
