@@ -113,6 +113,30 @@ __device__ __forceinline__ void transpose_reduce32(float* v) {
     }
 }
 
+// N (8, 16 or 32) partial sums v[0..N) per lane, summed over the 32 lanes: lane
+// l ends with the total of v[l % N] in v[0].  Lanes pair by the same bits, in
+// the same order (16, 8, 4, 2, 1), as in transpose_reduce32, so the totals are
+// bit-identical to it; levels above N/2 add without halving.
+template <int N>
+__device__ __forceinline__ void tree_reduce(float* v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int s = 16; s >= N; s >>= 1) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], s);
+    }
+#pragma unroll
+    for (int s = N / 2; s >= 1; s >>= 1) {
+        const bool up = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            const float send = up ? v[i] : v[i + s];
+            const float keep = up ? v[i + s] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
+    }
+}
+
 // Two warps per request: z for the 64 tokens of block `blk` of row (b, k):
 // warp w rebuilds tokens blk*64 + 32w + (0..31); each lane loads one or two
 // 16-byte chunks of every W2 row (coalesced rows) and a transpose-reduce
@@ -278,7 +302,7 @@ __device__ __forceinline__ bool grid_wait(const unsigned int* ctr, unsigned int 
 __device__ __forceinline__ bool wait_token(const unsigned long long* xw, int k, int* tok) {
     auto load = [&]() {
         unsigned long long v;
-        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(xw) : "memory");
+        asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(xw) : "memory");
         return v;
     };
     unsigned long long v = load();
@@ -447,6 +471,98 @@ __device__ __forceinline__ void finish_pair(const FinishArgs& f, int b, int gamm
     asm volatile("bar.sync %0, 64;" ::"r"(bar) : "memory");
 }
 
+// Draw x_k for request b with a group of G = 4 or 8 warps (group warp gw,
+// named barrier `bar` over 32 G threads).  Each warp rebuilds z on 64 / G
+// tokens of the winning block: lane c multiplies the c-th 16-byte chunk of
+// each W2 row by the same chunk of e = W1[x_{k-1}], kept in shared memory
+// (e_s, float[r]) since this CTA drew x_{k-1}; a butterfly over the lanes sums
+// the chunks (the same order as the two-warp draw, so z is bit-identical).
+// The second Gumbel level (stream 0) picks the token; the group leader
+// publishes it ((k << 32) | x_k word, x, ytok) and the group refills e_s with
+// W1[x_k] for the next draw.  g: [3 G] words of exchange space.
+template <int G>
+__device__ __forceinline__ void group_draw(const TcParams& p, int b, int k, int gw, int bar, float* e_s, float* g) {
+    constexpr int NT = 64 / G;                            // tokens per warp
+    const int lane = threadIdx.x & 31;
+    float* gsc = g;
+    float* gy = g + G;
+    int* gix = reinterpret_cast<int*>(g + 2 * G);
+    const size_t slot = static_cast<size_t>(k - 1) * p.B + b;
+    const unsigned long long word = __ldcg(p.ws.words + slot);
+    const uint32_t idx = unpack_idx(word);
+    const bool ok = word != 0ull && idx < static_cast<uint32_t>((p.V + 63) / 64);
+    float score = -INFINITY, yv = 0.f;
+    int bi = 0x7FFFFFFF;
+    if (ok) {
+        const int vbase = static_cast<int>(idx) * 64 + gw * NT;
+        const int vl = vbase + (lane & (NT - 1));
+        const int nch = p.r / 8;
+        const float u = (lane < NT && vl < p.V)
+                            ? bf16lo(p.U[(static_cast<size_t>(b) * p.gamma + (k - 1)) * p.V + vl])
+                            : 0.f;
+        const uint64_t pol = policy_evict_last();
+        uint4 raw[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            raw[t] = make_uint4(0, 0, 0, 0);
+            if (vbase + t < p.V && lane < nch)
+                ld_u32x4(p.W2 + static_cast<size_t>(vbase + t) * p.r + lane * 8, &raw[t].x, pol);
+        }
+        float e[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) e[q] = (lane < nch) ? e_s[lane * 8 + q] : 0.f;
+        float part[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const uint32_t wv[4] = {raw[t].x, raw[t].y, raw[t].z, raw[t].w};
+            float acc = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                acc = fmaf(bf16lo(wv[q]), e[2 * q], acc);
+                acc = fmaf(bf16hi(wv[q]), e[2 * q + 1], acc);
+            }
+            part[t] = acc;
+        }
+        tree_reduce<NT>(part);
+        if (lane < NT && vl < p.V) {
+            yv = (part[0] + u) * p.cscale;
+            const float gum = gumbel_of(uniform_open(draw_word(p.seed, b, k, kStreamDraftToken, static_cast<uint32_t>(vl))));
+            score = yv + gum * kLog2e;
+            bi = vl;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float os = __shfl_xor_sync(0xffffffffu, score, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        const float oy = __shfl_xor_sync(0xffffffffu, yv, o);
+        if (os > score || (os == score && oi < bi)) { score = os; bi = oi; yv = oy; }
+    }
+    if (lane == 0) { gsc[gw] = score; gix[gw] = bi; gy[gw] = yv; }
+    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(32 * G) : "memory");
+    if (gw == 0 && lane == 0) {
+        int w = 0;
+        for (int q = 1; q < G; ++q)
+            if (gsc[q] > gsc[w] || (gsc[q] == gsc[w] && gix[q] < gix[w])) w = q;
+        int tok = gix[w];
+        if (tok == 0x7FFFFFFF) { set_status(p.ws.status, DSPARK_ERR_DEVICE_CHECK, 3); tok = 0; }
+        const unsigned long long tagged = (static_cast<unsigned long long>(k) << 32) | static_cast<uint32_t>(tok);
+        asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p.ws.xw + b), "l"(tagged) : "memory");
+        p.x[b * p.gamma + k - 1] = tok;
+        p.ws.ytok[slot] = gy[w];
+        gix[0] = tok;
+    }
+    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(32 * G) : "memory");
+    // e for the next draw: W1[x_k] (also the next position's A row, so bring it into L2 too)
+    const int tok = gix[0];
+    for (int j = gw * 32 + lane; j < p.r / 2; j += 32 * G) {
+        const uint32_t w2 = reinterpret_cast<const uint32_t*>(p.W1 + static_cast<size_t>(tok) * p.r)[j];
+        e_s[2 * j] = bf16lo(w2);
+        e_s[2 * j + 1] = bf16hi(w2);
+    }
+    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(32 * G) : "memory");
+}
+
 // Draw x_k for request b inside a running multi-position launch: a pair of
 // warps (named barrier `bar`, 64 threads) rebuilds z on the winning block from
 // W2 rows and takes the second Gumbel level (stream 0); the even warp's lane 0
@@ -486,10 +602,11 @@ __device__ __forceinline__ void pair_draw(const TcParams& p, int b, int k, int b
         if (xch[1].x > xch[0].x || (xch[1].x == xch[0].x && xchi[1] < xchi[0])) w = 1;
         int tok = xchi[w];
         if (tok == 0x7FFFFFFF) { set_status(p.ws.status, DSPARK_ERR_DEVICE_CHECK, 3); tok = 0; }
+        // the tagged word carries the token itself: no ordering with other stores is needed
+        const unsigned long long tagged = (static_cast<unsigned long long>(k) << 32) | static_cast<uint32_t>(tok);
+        asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p.ws.xw + b), "l"(tagged) : "memory");
         p.x[b * p.gamma + k - 1] = tok;
         p.ws.ytok[slot] = xch[w].y;
-        const unsigned long long tagged = (static_cast<unsigned long long>(k) << 32) | static_cast<uint32_t>(tok);
-        asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p.ws.xw + b), "l"(tagged) : "memory");
         xchi[0] = tok;
     }
     asm volatile("bar.sync %0, 64;" ::"r"(bar) : "memory");
@@ -518,6 +635,8 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
     float2* xch = reinterpret_cast<float2*>(s_prev + kBM);        // [10] pair exchange
     int* xchi = reinterpret_cast<int*>(xch + 10);                 // [10]
     int* s_fail = xchi + 10;
+    float* e_s = reinterpret_cast<float*>(s_fail + 4);           // [2][256] W1 row of the last token drawn
+    float* gx = e_s + 2 * 256;                                     // [2][3 * 8] group-draw exchange
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = blockIdx.x / p.P, pc = blockIdx.x % p.P;
@@ -591,6 +710,28 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
         int mma_stage = 0;
         uint32_t mma_phase = 0;
         bool failed = false;
+        // requests b = blockIdx.x + j * gridDim.x < B, j < nown, belong to this CTA: it draws their
+        // tokens (with one group of 8 or two of 4 warps when it owns at most two, keeping e = W1[x]
+        // in shared memory; with pairs of warps otherwise) and finalizes them
+        const int cta = static_cast<int>(blockIdx.x), ncta = static_cast<int>(gridDim.x);
+        const int nown = (cta < p.B) ? (p.B - 1 - cta) / ncta + 1 : 0;
+        const bool grouped = kMode == kDraft && !p.greedy && nown <= 2 && (multi || p.fuse_tail);
+        auto draw_owned = [&](int kd) {
+            if (*s_fail != 0) return;
+            if (grouped) {
+                if (warp >= 4) {
+                    if (nown == 1)
+                        group_draw<8>(p, cta, kd, warp - 4, 2, e_s, gx);
+                    else if (nown == 2)
+                        group_draw<4>(p, cta + ((warp - 4) >> 2) * ncta, kd, (warp - 4) & 3, 2 + ((warp - 4) >> 2),
+                                      e_s + ((warp - 4) >> 2) * 256, gx + ((warp - 4) >> 2) * 24);
+                }
+            } else if (warp >= 2) {
+                const int pair = (warp - 2) >> 1;
+                for (int b = cta + pair * ncta; b < p.B; b += 5 * ncta)
+                    pair_draw(p, b, kd, 2 + pair, xch + 2 * pair, xchi + 2 * pair);
+            }
+        };
 
         for (int k = k0; k <= k1; ++k) {
             const int base = (k - k0) * ntiles;           // running index of this position's first tile
@@ -598,13 +739,8 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
             if (kMode == kDraft && multi && k > k0) {
                 wait_all();                               // every CTA published position k-1
                 if (!p.greedy) {
-                    // second Gumbel level for x_{k-1}, spread over the grid: requests
-                    // b = blockIdx + j * gridDim, one pair of warps per request
-                    if (warp >= 2 && *s_fail == 0) {
-                        const int pair = (warp - 2) >> 1;
-                        for (int b = blockIdx.x + pair * gridDim.x; b < p.B; b += 5 * gridDim.x)
-                            pair_draw(p, b, k - 1, 2 + pair, xch + 2 * pair, xchi + 2 * pair);
-                    }
+                    // second Gumbel level for x_{k-1}, spread over the grid (owned requests)
+                    draw_owned(k - 1);
                     // x_{k-1} of this M-tile's requests, as their drawers publish them
                     for (int rr = ptid; rr < nrows; rr += kPro) {
                         int tok = 0;
@@ -634,6 +770,16 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                     const int b = m0 + rr;
                     const int kb = row_k(b, k);
                     s_prev[rr] = (kb > 0) ? prev_token(p.x0, p.x, b, p.gamma, kb, p.V, st) : -1;
+                }
+                if (grouped && warp >= 4) {                // e of the first draw: W1[x_{k0-1}]
+                    for (int j = 0; j < nown; ++j) {
+                        const int prev = prev_token(p.x0, p.x, cta + j * ncta, p.gamma, k, p.V, st);
+                        for (int i = tid - 128; i < p.r / 2; i += kTcThreads - 128) {
+                            const uint32_t w2 = reinterpret_cast<const uint32_t*>(p.W1 + static_cast<size_t>(prev) * p.r)[i];
+                            e_s[j * 256 + 2 * i] = bf16lo(w2);
+                            e_s[j * 256 + 2 * i + 1] = bf16hi(w2);
+                        }
+                    }
                 }
             }
             pro_sync();
@@ -828,6 +974,19 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&tempty[buf]);
                 }
+                // the next position's first U tile of this lane does not depend on x_k:
+                // bring it into L2 while the grid hands over
+                if (kMode == kDraft && k < k1 && valid && warp_live) {
+                    const int inext = ((eg - (base + ntiles)) % kEpiWG + kEpiWG) % kEpiWG;
+                    if (inext < ntiles) {
+                        const uint16_t* un = p.U + (static_cast<size_t>(b) * p.gamma + k) * p.V;
+#pragma unroll
+                        for (int hb = 0; hb < 2; ++hb) {
+                            const int v0 = (t_lo + inext) * kBN + hb * 64;
+                            if (mine(hb) && v0 < p.V) prefetch_l2(un + v0);
+                        }
+                    }
+                }
                 rowres[eg * kBM + lrow] = RowRes{best, best_i, M, S};
             }
             pro_sync();
@@ -872,15 +1031,8 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
             // ------------------------------------------ x_gamma and finalize
             arrive();
             wait_all();                                   // every CTA published the last position
-            // requests b = blockIdx.x + j * gridDim.x < B, j < nown, belong to this CTA
-            const int cta = static_cast<int>(blockIdx.x), ncta = static_cast<int>(gridDim.x);
-            const int nown = (cta < p.B) ? (p.B - 1 - cta) / ncta + 1 : 0;
             if (!p.greedy) {
-                if (warp >= 2 && *s_fail == 0) {
-                    const int pair = (warp - 2) >> 1;
-                    for (int b = blockIdx.x + pair * gridDim.x; b < p.B; b += 5 * gridDim.x)
-                        pair_draw(p, b, k1, 2 + pair, xch + 2 * pair, xchi + 2 * pair);
-                }
+                draw_owned(k1);
             } else {
                 for (int j = ptid; j < nown; j += kPro) {
                     const int b = blockIdx.x + j * gridDim.x;
@@ -923,7 +1075,8 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
 }
 
 constexpr size_t kTcSmem = 1024 + 4 * kASlabBytes + kStages * kSlabBytes + (2 * kStages + 4 * kEpiWG) * 8 + 16 +
-                           kEpiWG * kBM * sizeof(RowRes) + kBM * 4 + 10 * 8 + 10 * 4 + 16;
+                           kEpiWG * kBM * sizeof(RowRes) + kBM * 4 + 10 * 8 + 10 * 4 + 16 + 2 * 256 * 4 +
+                           2 * 24 * 4 + 16;
 
 // ------------------------------------------------------------ host side ---
 inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
