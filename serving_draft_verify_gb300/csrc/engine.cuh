@@ -328,16 +328,29 @@ __device__ __forceinline__ float dot_row(const void* a, size_t a_off, const void
     if (vec) {
         const uint4* pa = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a) + a_off * ESZ);
         const uint4* pb = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(b) + b_off * ESZ);
-        for (int c = lane; c < n / EPC; c += 32) {
-            const uint4 x = pa[c], y = pb[c];
-            const uint32_t xv[4] = {x.x, x.y, x.z, x.w}, yv[4] = {y.x, y.y, y.z, y.w};
+        // four chunks of each operand in flight per lane, accumulated in chunk order
+        const int nc = n / EPC;
+        for (int c0 = lane; c0 < nc; c0 += 4 * 32) {
+            uint4 xs[4], ys[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if constexpr (kBF16) {
-                    acc = fmaf(bf16lo(xv[q]), bf16lo(yv[q]), acc);
-                    acc = fmaf(bf16hi(xv[q]), bf16hi(yv[q]), acc);
-                } else {
-                    acc = fmaf(__uint_as_float(xv[q]), __uint_as_float(yv[q]), acc);
+            for (int u = 0; u < 4; ++u) {
+                const int c = c0 + u * 32;
+                xs[u] = (c < nc) ? pa[c] : make_uint4(0, 0, 0, 0);
+                ys[u] = (c < nc) ? pb[c] : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (c0 + u * 32 >= nc) break;
+                const uint32_t xv[4] = {xs[u].x, xs[u].y, xs[u].z, xs[u].w};
+                const uint32_t yv[4] = {ys[u].x, ys[u].y, ys[u].z, ys[u].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if constexpr (kBF16) {
+                        acc = fmaf(bf16lo(xv[q]), bf16lo(yv[q]), acc);
+                        acc = fmaf(bf16hi(xv[q]), bf16hi(yv[q]), acc);
+                    } else {
+                        acc = fmaf(__uint_as_float(xv[q]), __uint_as_float(yv[q]), acc);
+                    }
                 }
             }
         }
@@ -363,10 +376,15 @@ __device__ __forceinline__ void finalize_position(int b, int k, int B, int gamma
     float L = 0.f, lp = 0.f;
     if (!greedy) {
         float m = -INFINITY, s = 0.f;
-        for (int ch = lane; ch < nchunk; ch += 32) {
-            const float2 pr = __ldcg(part + slot * kMaxChunks + ch);
-            lse_merge(m, s, pr.x, pr.y);
+        float2 pr[kMaxChunks / 32];                       // every partial of this lane in flight at once
+#pragma unroll
+        for (int u = 0; u < kMaxChunks / 32; ++u) {
+            const int ch = lane + 32 * u;
+            pr[u] = (ch < nchunk) ? __ldcg(part + slot * kMaxChunks + ch) : make_float2(0.f, 0.f);
         }
+#pragma unroll
+        for (int u = 0; u < kMaxChunks / 32; ++u)
+            if (lane + 32 * u < nchunk) lse_merge(m, s, pr[u].x, pr[u].y);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             const float om = __shfl_xor_sync(0xffffffffu, m, off);
