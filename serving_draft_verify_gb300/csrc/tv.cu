@@ -5,11 +5,12 @@
 // One HBM pass per row.  A thread-block cluster of kCS CTAs owns one row at a
 // time; each CTA bulk-copies its 1/kCS slice of d and t into shared memory
 // (double-buffered, so the next row streams in while this one is reduced):
-//   A. slice max of d and t;
-//   B. e_d = 2^(d log2e - m_d), e_t likewise, kept in registers; slice sums;
-//   -- cluster exchange of (m, s) through distributed shared memory --
-//   C. sum min(e_d 2^(m_d - L_d), e_t 2^(m_t - L_t)) from registers (no exp);
-//   -- cluster exchange of the partial sums; rank 0 writes c*.
+//   A. each thread's max of its d and t elements (packed bf16 max);
+//   B. e_d = 2^(d log2e - m_d), e_t likewise, kept in registers as packed
+//      float pairs; the thread's sums, merged per warp and per CTA;
+//   -- one cluster barrier per row: the CTAs' (m, s) through distributed shared
+//      memory (and the previous row's partials, which rank 0 sums into c*) --
+//   C. sum min(e_d 2^(m_d - L_d), e_t 2^(m_t - L_t)) from registers (no exp).
 // Two exponentials per logit pair; every byte of d and t is read once from HBM.
 #include <cooperative_groups.h>
 
@@ -29,7 +30,7 @@ template <bool kBF16>
 struct TVTraits {
     static constexpr int kEPG = kBF16 ? 8 : 4;   // elements per 16-byte group
     static constexpr int kESZ = kBF16 ? 2 : 4;
-    static constexpr int kStages = kBF16 ? 2 : 1;
+    static constexpr int kStages = kBF16 ? 2 : 1;     // at most 2: their mbarriers fit in 16 bytes
     static constexpr int kGMax = kBF16 ? 5 : 10;  // groups per thread held in registers
 };
 
@@ -46,37 +47,59 @@ __device__ __forceinline__ void unpack(const uint4 v, float* out) {
     }
 }
 
-// Block-wide reductions over kThreads threads; `red` holds 2 * kWarps floats.
-__device__ __forceinline__ float2 block_max2(float2 v, float* red) {
-    v.x = warp_max(v.x);
-    v.y = warp_max(v.y);
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
-    if (l == 0) { red[w] = v.x; red[kWarps + w] = v.y; }
-    __syncthreads();
-    float a = -INFINITY, b = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kWarps; ++i) { a = fmaxf(a, red[i]); b = fmaxf(b, red[kWarps + i]); }
-    return make_float2(a, b);
+// Packed pairs of float32 (Blackwell f32x2 arithmetic): two lanes of work per
+// instruction for the element-wise part of the sums.
+__device__ __forceinline__ unsigned long long pk(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
 }
-__device__ __forceinline__ float2 block_sum2(float2 v, float* red) {
-    v.x = warp_sum(v.x);
-    v.y = warp_sum(v.y);
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
-    if (l == 0) { red[w] = v.x; red[kWarps + w] = v.y; }
-    __syncthreads();
-    float a = 0.f, b = 0.f;
-#pragma unroll
-    for (int i = 0; i < kWarps; ++i) { a += red[i]; b += red[kWarps + i]; }
-    return make_float2(a, b);
+__device__ __forceinline__ float2 upk(unsigned long long v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
+// One CTA's exchange slot, double-buffered by row parity: a CTA writes row it+1's
+// values only after the cluster barrier of row it+1, which every CTA reaches
+// only after its reads of row it-1's values, so parity it+1 is free.
 struct Slot {
-    float md, sd, mt, st;   // slice max (log2 units) and sum of 2^(y - m)
-    float p;                // slice partial of sum min(p_d, p_t)
-    float pad[3];
+    float4 ms[2];           // slice max (log2 units) and sum of 2^(y - m) of d and t: (md, sd, mt, st)
+    float p[2];             // CTA partial of sum min(p_d, p_t)
+    float pad[2];
 };
+
+// (m, s) with s a sum of 2^((x - m) log2e): merge across a warp.
+__device__ __forceinline__ void warp_lse(float& m, float& s) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float om = __shfl_xor_sync(0xffffffffu, m, o);
+        const float os = __shfl_xor_sync(0xffffffffu, s, o);
+        if (os > 0.f) {
+            if (s <= 0.f) { m = om; s = os; }
+            else {
+                const float M = fmaxf(m, om);
+                s = s * fast_exp2((m - M) * kLog2e) + os * fast_exp2((om - M) * kLog2e);
+                m = M;
+            }
+        }
+    }
+}
 
 template <bool kBF16>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -86,7 +109,7 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
     constexpr int EPG = Tr::kEPG, ESZ = Tr::kESZ, STAGES = Tr::kStages, GMAX = Tr::kGMax;
     extern __shared__ __align__(128) uint8_t smem[];
     cg::cluster_group cluster = cg::this_cluster();
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t rank = cluster.block_rank();
     const int64_t cid = blockIdx.x / kCS;
     const int64_t ncl = gridDim.x / kCS;
@@ -96,10 +119,13 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
     const int ngroups = len / EPG;
     const size_t stage_bytes = static_cast<size_t>(slice) * ESZ;
 
+    // shared memory: data stages (each a multiple of 16 bytes) | mbarriers (16 B) | pad |
+    // red (16-byte aligned float4 per warp) | slot
     uint8_t* buf = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * 2 * stage_bytes);
-    float* red = reinterpret_cast<float*>(bars + STAGES);
-    Slot* slot = reinterpret_cast<Slot*>(red + 2 * kWarps);
+    const size_t data_bytes = static_cast<size_t>(STAGES) * 2 * stage_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + data_bytes);
+    float4* red = reinterpret_cast<float4*>(smem + data_bytes + 32);   // (md, sd, mt, st) / partials
+    Slot* slot = reinterpret_cast<Slot*>(red + kWarps);
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
@@ -129,6 +155,7 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
 
     bool failed = false;
     int it = 0;
+    int64_t prev_row = -1;                                // row whose partials wait in the slots
     for (int64_t row = cid; row < rows; row += ncl, ++it) {
         const int s = it % STAGES;
         const uint32_t par = static_cast<uint32_t>(it / STAGES) & 1u;
@@ -144,27 +171,46 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
         const uint4* dg = reinterpret_cast<const uint4*>(buf + (2 * s) * stage_bytes);
         const uint4* tg = reinterpret_cast<const uint4*>(buf + (2 * s + 1) * stage_bytes);
 
-        // A: slice maxima
-        float2 m = make_float2(-INFINITY, -INFINITY);
-        if (!failed) {
-            for (int g = tid; g < ngroups; g += kThreads) {
-                float a[EPG], b[EPG];
-                unpack<kBF16>(dg[g], a);
-                unpack<kBF16>(tg[g], b);
+        // A: this thread's maxima (bf16: packed, exact)
+        float mxd = -INFINITY, mxt = -INFINITY;
+        if constexpr (kBF16) {
+            uint32_t ad = 0xFF80FF80u, at = 0xFF80FF80u;  // (-inf, -inf)
 #pragma unroll
-                for (int e = 0; e < EPG; ++e) { m.x = fmaxf(m.x, a[e]); m.y = fmaxf(m.y, b[e]); }
+            for (int gi = 0; gi < GMAX; ++gi) {
+                const int g = tid + gi * kThreads;
+                if (!failed && g < ngroups) {
+                    const uint4 a = dg[g], b = tg[g];
+                    ad = bmax2(bmax2(ad, a.x), bmax2(a.y, bmax2(a.z, a.w)));
+                    at = bmax2(bmax2(at, b.x), bmax2(b.y, bmax2(b.z, b.w)));
+                }
+            }
+            mxd = fmaxf(bf16lo(ad), bf16hi(ad));
+            mxt = fmaxf(bf16lo(at), bf16hi(at));
+        } else {
+#pragma unroll
+            for (int gi = 0; gi < GMAX; ++gi) {
+                const int g = tid + gi * kThreads;
+                if (!failed && g < ngroups) {
+                    float a[EPG], b[EPG];
+                    unpack<kBF16>(dg[g], a);
+                    unpack<kBF16>(tg[g], b);
+#pragma unroll
+                    for (int e = 0; e < EPG; ++e) { mxd = fmaxf(mxd, a[e]); mxt = fmaxf(mxt, b[e]); }
+                }
             }
         }
-        m = block_max2(m, red);
-        // y = x log2e is rounded before the max is subtracted: rounding is monotone,
-        // so max(y) is exactly md2 and y - md2 <= 0 even for |x| near the float range
-        // a slice with no finite logit keeps reference 0 so that its terms are 2^-inf = 0
-        const float md2 = (m.x > -INFINITY) ? __fmul_rn(m.x, kLog2e) : 0.f;
-        const float mt2 = (m.y > -INFINITY) ? __fmul_rn(m.y, kLog2e) : 0.f;
+        // e = 2^((x - m) log2e): the difference is formed first, so it is exactly 0 at
+        // the max and <= 0 elsewhere, whatever the magnitude of x (a multiply-add of
+        // x log2e - m log2e would leave the product's rounding error in the exponent);
+        // a thread without a finite logit keeps reference 0 so that its terms are 0
+        const float md = (mxd > -INFINITY) ? mxd : 0.f;
+        const float mt = (mxt > -INFINITY) ? mxt : 0.f;
 
-        // B: exponentials in registers, slice sums
-        float ed[GMAX * EPG], et[GMAX * EPG];
-        float2 sum = make_float2(0.f, 0.f);
+        // B: e in registers (packed pairs), the thread's sums
+        unsigned long long ed[GMAX * EPG / 2], et[GMAX * EPG / 2];
+        const unsigned long long L2E = pk(kLog2e, kLog2e);
+        const unsigned long long nmd = pk(-md, -md), nmt = pk(-mt, -mt);
+        unsigned long long sdp = pk(0.f, 0.f), stp = pk(0.f, 0.f);
 #pragma unroll
         for (int gi = 0; gi < GMAX; ++gi) {
             const int g = tid + gi * kThreads;
@@ -173,18 +219,28 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
                 unpack<kBF16>(dg[g], a);
                 unpack<kBF16>(tg[g], b);
 #pragma unroll
-                for (int e = 0; e < EPG; ++e) {
-                    ed[gi * EPG + e] = exp2f(__fmul_rn(a[e], kLog2e) - md2);
-                    et[gi * EPG + e] = exp2f(__fmul_rn(b[e], kLog2e) - mt2);
-                    sum.x += ed[gi * EPG + e];
-                    sum.y += et[gi * EPG + e];
+                for (int e = 0; e < EPG; e += 2) {
+                    const float2 ya = upk(mul2(add2(pk(a[e], a[e + 1]), nmd), L2E));
+                    const float2 yb = upk(mul2(add2(pk(b[e], b[e + 1]), nmt), L2E));
+                    const unsigned long long va = pk(fast_exp2(ya.x), fast_exp2(ya.y));
+                    const unsigned long long vb = pk(fast_exp2(yb.x), fast_exp2(yb.y));
+                    ed[(gi * EPG + e) / 2] = va;
+                    et[(gi * EPG + e) / 2] = vb;
+                    sdp = add2(sdp, va);
+                    stp = add2(stp, vb);
                 }
             } else {
 #pragma unroll
-                for (int e = 0; e < EPG; ++e) { ed[gi * EPG + e] = 0.f; et[gi * EPG + e] = 0.f; }
+                for (int e = 0; e < EPG; e += 2) { ed[(gi * EPG + e) / 2] = 0ull; et[(gi * EPG + e) / 2] = 0ull; }
             }
         }
-        sum = block_sum2(sum, red);   // ends with every thread past its smem reads of this stage
+        float tmd = md, tsd = upk(sdp).x + upk(sdp).y;
+        float tmt = mt, tst = upk(stp).x + upk(stp).y;
+        float wmd = tmd, wsd = tsd, wmt = tmt, wst = tst;
+        warp_lse(wmd, wsd);
+        warp_lse(wmt, wst);
+        if (lane == 0) red[warp] = make_float4(wmd, wsd, wmt, wst);
+        __syncthreads();                                  // every thread is past its reads of this stage
 
         // refill this stage with the row STAGES iterations ahead
         {
@@ -197,39 +253,62 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
                 pend_it[s] = it + STAGES;
             }
         }
-        if (tid == 0) { slot->md = md2; slot->sd = sum.x; slot->mt = mt2; slot->st = sum.y; }
-        cluster.sync();
+        if (warp == 0) {
+            float4 r = (lane < kWarps) ? red[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+            float a = r.x, b = r.y, c = r.z, e = r.w;
+            warp_lse(a, b);
+            warp_lse(c, e);
+            if (lane == 0) slot->ms[it & 1] = make_float4(a, b, c, e);
+        }
+        cluster.sync();                                   // slices' (m, s) and the previous row's partials
 
+        // the previous row's c*: rank 0 sums its CTAs' partials in rank order
+        if (rank == 0 && warp == 1 && prev_row >= 0) {
+            const float pr = (lane < kCS) ? cluster.map_shared_rank(slot, lane)->p[(it - 1) & 1] : 0.f;
+            const float c = warp_sum(pr);
+            if (lane == 0 && !failed) c_star[prev_row] = c;
+        }
         // every warp combines the kCS slots itself: lane r reads CTA r's slot
-        const int lane = tid & 31;
         float rmd = -INFINITY, rsd = 0.f, rmt = -INFINITY, rst = 0.f;
         if (lane < kCS) {
-            const Slot* rs = cluster.map_shared_rank(slot, lane);
-            rsd = rs->sd; rst = rs->st;
-            rmd = rsd > 0.f ? rs->md : -INFINITY;          // empty slices do not set the reference
-            rmt = rst > 0.f ? rs->mt : -INFINITY;
+            const float4 rs = cluster.map_shared_rank(slot, lane)->ms[it & 1];
+            rsd = rs.y; rst = rs.w;
+            rmd = rsd > 0.f ? rs.x : -INFINITY;            // empty slices do not set the reference
+            rmt = rst > 0.f ? rs.z : -INFINITY;
         }
         const float Md = warp_max(rmd), Mt = warp_max(rmt);
-        const float Sd = warp_sum(rsd > 0.f ? rsd * exp2f(rmd - Md) : 0.f);
-        const float St = warp_sum(rst > 0.f ? rst * exp2f(rmt - Mt) : 0.f);
-        const float Ld2 = Md + log2f(Sd), Lt2 = Mt + log2f(St);
-        const float alpha = (sum.x > 0.f) ? exp2f(md2 - Ld2) : 0.f;
-        const float beta = (sum.y > 0.f) ? exp2f(mt2 - Lt2) : 0.f;
+        const float Sd = warp_sum(rsd > 0.f ? rsd * exp2f((rmd - Md) * kLog2e) : 0.f);
+        const float St = warp_sum(rst > 0.f ? rst * exp2f((rmt - Mt) * kLog2e) : 0.f);
+        // p = e 2^((m_thread - M) log2e) / S
+        const float alpha = (tsd > 0.f) ? exp2f((tmd - Md) * kLog2e - log2f(Sd)) : 0.f;
+        const float beta = (tst > 0.f) ? exp2f((tmt - Mt) * kLog2e - log2f(St)) : 0.f;
 
-        // C: sum of min(p_d, p_t) over this slice, from registers
-        float p = 0.f;
+        // C: sum of min(p_d, p_t) over this thread's elements, from registers
+        const unsigned long long al = pk(alpha, alpha), be = pk(beta, beta);
+        unsigned long long pp = pk(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < GMAX * EPG; ++i) p += fminf(ed[i] * alpha, et[i] * beta);
-        p = block_sum2(make_float2(p, 0.f), red).x;
-        if (tid == 0) slot->p = p;
-        cluster.sync();
-        if (rank == 0 && tid < 32) {
-            const float pr = (tid < kCS) ? cluster.map_shared_rank(slot, tid)->p : 0.f;
-            const float c = warp_sum(pr);
-            if (tid == 0 && !failed) c_star[row] = c;
+        for (int i = 0; i < GMAX * EPG / 2; ++i) {
+            const float2 x = upk(mul2(ed[i], al)), y = upk(mul2(et[i], be));
+            pp = add2(pp, pk(fminf(x.x, y.x), fminf(x.y, y.y)));
         }
+        float p = warp_sum(upk(pp).x + upk(pp).y);
+        __syncthreads();                                  // red is free again
+        if (lane == 0) red[warp].x = p;
+        __syncthreads();
+        if (warp == 0) {
+            float q = (lane < kWarps) ? red[lane].x : 0.f;
+            q = warp_sum(q);
+            if (lane == 0) slot->p[it & 1] = q;
+        }
+        prev_row = row;
     }
-    // no CTA leaves while a peer may still read its shared memory
+    // the last row's c*, and no CTA leaves while a peer may still read its shared memory
+    cluster.sync();
+    if (rank == 0 && warp == 1 && prev_row >= 0) {
+        const float pr = (lane < kCS) ? cluster.map_shared_rank(slot, lane)->p[(it - 1) & 1] : 0.f;
+        const float c = warp_sum(pr);
+        if (lane == 0 && !failed) c_star[prev_row] = c;
+    }
     cluster.sync();
     // after a timeout, give any copy still in flight a bounded chance to land
     if (failed && tid == 0) {
@@ -241,8 +320,8 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
 template <bool kBF16>
 size_t tv_smem_bytes(int slice) {
     using Tr = TVTraits<kBF16>;
-    return static_cast<size_t>(Tr::kStages) * 2 * slice * Tr::kESZ + Tr::kStages * 8 +
-           2 * kWarps * sizeof(float) + sizeof(Slot) + 128;
+    return static_cast<size_t>(Tr::kStages) * 2 * slice * Tr::kESZ + 32 + kWarps * sizeof(float4) +
+           sizeof(Slot) + 128;
 }
 
 template <bool kBF16>
