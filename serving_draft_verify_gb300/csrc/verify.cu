@@ -271,251 +271,172 @@ __device__ __noinline__ void decide_row(int n, int row, int b, int k, int gamma,
 
 // ------------------------------------------------------------- rows pass ---
 // CTA c takes blocks [c per, (c+1) per) of the padded scheduled rows laid end
-// to end, one piece per row it touches.  Warp 0 (one lane) streams the pieces
-// into a ring of shared-memory chunks with bulk copies (complete_tx mbarriers);
-// eight consumer warps reduce each chunk, kRQ quads of 4 blocks per warp: per
-// 64-token block the logsumexp of t / T and a Gumbel key for a draw from p_t
-// (greedy: the argmax of t).  One Philox call per lane covers the warp's
-// kRQ quads (lane (sub, part) keeps the word of block sub of quad part) and
-// one pass of all lanes finishes the kRQ x 4 blocks.  Per piece the CTA's best
-// and (max, sum) go to the row's slot; the CTA that completes a row decides it.
-constexpr int kRowsConsumers = 8;                         // consumer warps
-constexpr int kRowsThreads = 32 * (1 + kRowsConsumers);
-constexpr int kRowsChunkBytes = 32768;
-constexpr int kRowsStages = 3;
-constexpr int kRowsCtasPerSm = 2;
-constexpr size_t kRowsSmem = 1024 + kRowsStages * kRowsChunkBytes + 2 * kRowsStages * 8 + 256;
+// to end, one piece per row it touches; per piece a warp covers 4 quads of 4
+// consecutive blocks per step, 8 lanes per block, 8 logits per lane.  Per
+// 64-token block: the logsumexp of t / T and a Gumbel key for a draw from p_t
+// (greedy: the argmax of t); per piece the CTA's best and its (max, sum).
+// Sixteen lanes finish the 16 blocks of a step, one block each.
+constexpr int kRowsCtasPerSm = 3;
 
 template <bool kBF16>
-__global__ void __launch_bounds__(kRowsThreads, kRowsCtasPerSm)
+__global__ void __launch_bounds__(256, kRowsCtasPerSm)
 verify_rows(int gamma, int V, const void* __restrict__ t, const int32_t* __restrict__ x,
             const float* __restrict__ lse_d, const float* __restrict__ logp_d, const int32_t* __restrict__ ell,
             float cscale, int greedy, uint64_t seed, int32_t* __restrict__ n_accept, int32_t* __restrict__ next_token,
             VerifyWs ws) {
-    constexpr int ESZ = kBF16 ? 2 : 4;
-    constexpr int kChunkBlocks = kRowsChunkBytes / (64 * ESZ);     // 256 (bf16) or 128 (fp32)
-    constexpr int kRQ = kChunkBlocks / 4 / kRowsConsumers;         // quads per warp per chunk: 8 or 4
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    uint8_t* smem = smem_raw + (((raw + 127u) & ~127u) - raw);
-    uint8_t* ring = smem;
-    uint64_t* full = reinterpret_cast<uint64_t*>(ring + kRowsStages * kRowsChunkBytes);
-    uint64_t* empty = full + kRowsStages;
-    float* rk = reinterpret_cast<float*>(empty + kRowsStages);    // [kRowsConsumers] x 4
-    float* rm = rk + kRowsConsumers;
-    float* rs = rm + kRowsConsumers;
-    int* ri = reinterpret_cast<int*>(rs + kRowsConsumers);
-    int* s_last = ri + kRowsConsumers;
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    __shared__ float rk[8], rm[8], rs[8];
+    __shared__ int ri[8];
+    __shared__ int s_last;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sub = lane >> 3, part = lane & 7;
     const int nblk = (V + 63) / 64, npad = padded_blocks(V);
     const int N = ws.plan[0], per = ws.plan[1];
     const long long total = static_cast<long long>(N) * npad;
-    if (tid == 0) {
-        for (int q = 0; q < kRowsStages; ++q) { mbar_init(&full[q], 1); mbar_init(&empty[q], kRowsConsumers); }
-        fence_mbar_init();
-    }
-    __syncthreads();
-
-    // the chunk sequence of this CTA (identical walk for the producer and the consumers)
-    auto for_chunks = [&](auto&& fn) {
-        for (long long c = blockIdx.x; c * per < total; c += gridDim.x) {
-            long long g = c * per;
-            const long long gend = min(total, g + per);
-            while (g < gend) {
-                const int n = static_cast<int>(g / npad);
-                const int lo = static_cast<int>(g - static_cast<long long>(n) * npad);
-                const int hi_pad = static_cast<int>(min(static_cast<long long>(npad), lo + (gend - g)));
-                const int slot = static_cast<int>(c - static_cast<long long>(n) * npad / per);
-                for (int c0 = lo; c0 < hi_pad; c0 += kChunkBlocks) {
-                    const int c1 = min(hi_pad, c0 + kChunkBlocks);
-                    fn(n, slot, lo, hi_pad, c0, c1);
-                }
-                g += hi_pad - lo;
-            }
-        }
-    };
-
-    if (warp == 0) {
-        // ------------------------------------------------------- producer
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
-            int stage = 0;
-            uint32_t phase = 0;
-            bool failed = false;
-            for_chunks([&](int n, int, int, int, int c0, int c1) {
-                if (failed) return;
-                if (!mbar_wait(&empty[stage], phase ^ 1u)) {
-                    failed = true;
-                    set_status(ws.status, DSPARK_ERR_TIMEOUT, 20);
-                    return;
-                }
-                const int row = ws.rows[n];
-                const int v0 = c0 * 64, v1 = min(c1 * 64, V);
-                const uint32_t bytes = (v1 > v0) ? static_cast<uint32_t>(v1 - v0) * ESZ : 0u;
-                if (bytes > 0) {
-                    mbar_arrive_expect_tx(&full[stage], bytes);
-                    bulk_g2s(ring + stage * kRowsChunkBytes,
-                             static_cast<const uint8_t*>(t) + (static_cast<size_t>(row) * V + v0) * ESZ, bytes,
-                             &full[stage], pol);
-                } else {
-                    mbar_arrive(&full[stage]);            // a piece of padding blocks only
-                }
-                if (++stage == kRowsStages) { stage = 0; phase ^= 1u; }
-            });
-        }
-        __syncwarp();
-        return;
-    }
-
-    // ---------------------------------------------------------- consumers
-    const int cw = warp - 1;                              // consumer warp 0..7
-    const int sub = lane >> 3, part = lane & 7;
-    auto csync = [] { asm volatile("bar.sync 1, %0;" ::"n"(32 * kRowsConsumers) : "memory"); };
-    int stage = 0;
-    uint32_t phase = 0;
-    bool failed = false;
-    float best = -INFINITY, M = -INFINITY, S = 0.f;
-    int best_i = 0x7FFFFFFF;
-    float txk = 0.f;
-    bool have_tx = false;
-    int row = 0, b = 0, k = 0, xk = -1;
-    for_chunks([&](int n, int slot, int lo, int hi_pad, int c0, int c1) {
-        if (c0 == lo) {                                   // a new piece
-            row = ws.rows[n];
-            b = row / (gamma + 1);
-            k = row % (gamma + 1) + 1;
+    const uint64_t pol = policy_evict_first();
+    for (long long c = blockIdx.x; c * per < total; c += gridDim.x) {
+        long long g = c * per;
+        const long long gend = min(total, g + per);
+        while (g < gend) {
+            const int n = static_cast<int>(g / npad);
+            const int lo = static_cast<int>(g - static_cast<long long>(n) * npad);
+            const int hi_pad = static_cast<int>(min(static_cast<long long>(npad), lo + (gend - g)));
+            const int hi = min(hi_pad, nblk);
+            const int slot = static_cast<int>(c - static_cast<long long>(n) * npad / per);
+            const int row = ws.rows[n];
+            const int b = row / (gamma + 1), k = row % (gamma + 1) + 1;
+            const size_t rowoff = static_cast<size_t>(row) * V;
+            // x_k of a decided row: the lane that loads it keeps t[x_k] for the decision
             int e = ell[b];
             e = e < 0 ? 0 : (e > gamma ? gamma : e);
-            xk = (k <= e) ? x[b * gamma + k - 1] : -1;    // its lane keeps t[x_k] for the decision
-            best = -INFINITY; M = -INFINITY; S = 0.f; best_i = 0x7FFFFFFF;
-            have_tx = false;
-        }
-        if (!failed && !mbar_wait(&full[stage], phase)) {
-            failed = true;
-            set_status(ws.status, DSPARK_ERR_TIMEOUT, 21);
-        }
-        const int hi = min(hi_pad, nblk);
-        const uint8_t* buf = ring + stage * kRowsChunkBytes;
-        // this warp's kRQ quads of the chunk: blocks c0 + 4 (cw kRQ + j) + sub
-        const int q0 = c0 / 4 + cw * kRQ;                 // row-level quad index of j = 0
-        float mq[kRQ], sq[kRQ];
+            const int xk = (k <= e) ? x[b * gamma + k - 1] : -1;
+            float txk = 0.f;
+            bool have_tx = false;
+            float best = -INFINITY, M = -INFINITY, S = 0.f;
+            int best_i = 0x7FFFFFFF;
+            // each warp takes 4 consecutive quads per step; all loads of a step are issued first
+            constexpr int kU = 4;
+            for (int q0 = lo / 4 + warp * kU; q0 * 4 < hi; q0 += 8 * kU) {
+                float y[kU][8];
 #pragma unroll
-        for (int j = 0; j < kRQ; ++j) {
-            const int blk = (q0 + j) * 4 + sub;
-            const int v = blk * 64 + part * 8;
-            float y[8];
+                for (int u = 0; u < kU; ++u) {
+                    const int blk = (q0 + u) * 4 + sub;
+                    const int v = blk * 64 + part * 8;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) y[i] = -INFINITY;
-            if (!failed && blk < hi && blk < c1) {
-                const uint8_t* src = buf + static_cast<size_t>(v - c0 * 64) * ESZ;
-                if constexpr (kBF16) {
-                    if (v < V) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(src);
-                        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+                    for (int i = 0; i < 8; ++i) y[u][i] = -INFINITY;
+                    if (blk < hi) {
+                        if constexpr (kBF16) {
+                            if (v < V) {
+                                uint32_t w[4];
+                                eng::ld_u32x4(static_cast<const uint16_t*>(t) + rowoff + v, w, pol);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) { y[2 * i] = bf16lo(wv[i]); y[2 * i + 1] = bf16hi(wv[i]); }
-                    }
-                } else {
+                                for (int i = 0; i < 4; ++i) { y[u][2 * i] = bf16lo(w[i]); y[u][2 * i + 1] = bf16hi(w[i]); }
+                            }
+                        } else {
 #pragma unroll
-                    for (int hq = 0; hq < 2; ++hq) {
-                        if (v + 4 * hq < V) {
-                            const float4 w = *reinterpret_cast<const float4*>(src + 16 * hq);
-                            y[4 * hq] = w.x; y[4 * hq + 1] = w.y; y[4 * hq + 2] = w.z; y[4 * hq + 3] = w.w;
+                            for (int hq = 0; hq < 2; ++hq) {
+                                if (v + 4 * hq < V) {
+                                    uint32_t w[4];
+                                    eng::ld_u32x4(static_cast<const float*>(t) + rowoff + v + 4 * hq, w, pol);
+#pragma unroll
+                                    for (int i = 0; i < 4; ++i) y[u][4 * hq + i] = __uint_as_float(w[i]);
+                                }
+                            }
                         }
                     }
                 }
-                const int d = xk - v;                     // rare: one lane of one step
-                if (static_cast<unsigned>(d) < 8u) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        if (i == d) txk = y[i];
-                    have_tx = true;
+                for (int u = 0; u < kU; ++u) {
+                    const int d = xk - (((q0 + u) * 4 + sub) * 64 + part * 8);
+                    if (static_cast<unsigned>(d) < 8u && (q0 + u) * 4 + sub < hi) {   // rare: one lane, one step
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            if (i == d) txk = y[u][i];
+                        have_tx = true;
+                    }
+                }
+                if (greedy) {
+#pragma unroll
+                    for (int u = 0; u < kU; ++u) {
+                        const int v = ((q0 + u) * 4 + sub) * 64 + part * 8;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            if (y[u][i] > best) { best = y[u][i]; best_i = v + i; }
+                    }
+                    continue;
+                }
+                // per block (quad u, sub): max and sum of 2^(y c - m c) over its 8 lanes
+                float mq[kU], sq[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    float m = y[u][0];
+#pragma unroll
+                    for (int i = 1; i < 8; ++i) m = fmaxf(m, y[u][i]);
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                    const float mc = m * cscale;
+                    float sum = 0.f;
+                    if (m > -INFINITY) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) sum += fast_exp2(fmaf(y[u][i], cscale, -mc));
+                    }
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+                    mq[u] = mc;
+                    sq[u] = sum;
+                }
+                // lane (sub, part < 4) finishes block (quad q0 + part, sub): its Philox
+                // counter is that quad's, its word the block's
+                const int pu = part & 3;
+                const U4 pw = philox4x32_10(U4{static_cast<uint32_t>(q0 + pu), static_cast<uint32_t>(k),
+                                               static_cast<uint32_t>(b), kStreamTargetBlock},
+                                            static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+                const uint32_t word = sub == 0 ? pw.x : sub == 1 ? pw.y : sub == 2 ? pw.z : pw.w;
+                const float m = pu == 0 ? mq[0] : pu == 1 ? mq[1] : pu == 2 ? mq[2] : mq[3];
+                const float sum = pu == 0 ? sq[0] : pu == 1 ? sq[1] : pu == 2 ? sq[2] : sq[3];
+                const int blk = (q0 + pu) * 4 + sub;
+                if (part < 4 && blk < hi && sum > 0.f) {
+                    const float key = (m + log2f(sum)) * kLn2 + gumbel_of(uniform_open(word));
+                    if (key > best || (key == best && blk < best_i)) { best = key; best_i = blk; }
+                    lse_merge(M, S, m, sum);
                 }
             }
-            if (greedy) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (y[i] > best) { best = y[i]; best_i = v + i; }
-                mq[j] = 0.f;
-                sq[j] = 0.f;
-            } else {
-                float m = y[0];
-#pragma unroll
-                for (int i = 1; i < 8; ++i) m = fmaxf(m, y[i]);
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                const float mc = m * cscale;
-                float sum = 0.f;
-                if (m > -INFINITY) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) sum += fast_exp2(fmaf(y[i], cscale, -mc));
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, best_i, o);
+                const float om = __shfl_xor_sync(0xffffffffu, M, o);
+                const float os = __shfl_xor_sync(0xffffffffu, S, o);
+                if (ob > best || (ob == best && oi < best_i)) { best = ob; best_i = oi; }
+                lse_merge(M, S, om, os);
+            }
+            if (have_tx) ws.tx[row] = txk;
+            if (lane == 0) { rk[warp] = best; ri[warp] = best_i; rm[warp] = M; rs[warp] = S; }
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                float bk = -INFINITY, m = -INFINITY, s = 0.f;
+                int bi = 0x7FFFFFFF;
+                for (int w = 0; w < 8; ++w) {
+                    if (rk[w] > bk || (rk[w] == bk && ri[w] < bi)) { bk = rk[w]; bi = ri[w]; }
+                    lse_merge(m, s, rm[w], rs[w]);
                 }
-                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-                mq[j] = mc;
-                sq[j] = sum;
+                if (!greedy) ws.part[static_cast<size_t>(row) * kNchMax + slot] = make_float2(m, s);
+                if (bk > -INFINITY) atomicMax(&ws.wt[row], pack_key(bk, static_cast<uint32_t>(bi)));
+                // the CTA that completes the row makes its decision
+                const long long g0 = static_cast<long long>(n) * npad;
+                const int ncta = static_cast<int>((g0 + npad - 1) / per - g0 / per) + 1;
+                __threadfence();
+                s_last = atomicAdd(ws.row_cnt + n, 1) == ncta - 1;
+                __threadfence();
             }
+            __syncthreads();                              // rk..ri are rewritten by the next piece
+            if (s_last && warp == 0)
+                decide_row<kBF16>(n, row, b, k, gamma, V, per, npad, t, x, lse_d, logp_d, ell, cscale, greedy, seed,
+                                  n_accept, next_token, ws);
+            g += hi_pad - lo;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[stage]);
-        if (++stage == kRowsStages) { stage = 0; phase ^= 1u; }
-        if (!greedy) {
-            // lane (sub, part) finishes block (quad q0 + part, sub) for part < kRQ: the
-            // Philox counter is that quad's, the word the block's
-            const int pu = part % kRQ;
-            const U4 pw = philox4x32_10(U4{static_cast<uint32_t>(q0 + pu), static_cast<uint32_t>(k),
-                                           static_cast<uint32_t>(b), kStreamTargetBlock},
-                                        static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
-            const uint32_t word = sub == 0 ? pw.x : sub == 1 ? pw.y : sub == 2 ? pw.z : pw.w;
-            float m = mq[0], sum = sq[0];
-#pragma unroll
-            for (int j = 1; j < kRQ; ++j)
-                if (pu == j) { m = mq[j]; sum = sq[j]; }
-            const int blk = (q0 + pu) * 4 + sub;
-            if (part < kRQ && blk < hi && blk < c1 && sum > 0.f) {
-                const float key = (m + log2f(sum)) * kLn2 + gumbel_of(uniform_open(word));
-                if (key > best || (key == best && blk < best_i)) { best = key; best_i = blk; }
-                lse_merge(M, S, m, sum);
-            }
-        }
-        if (c1 < hi_pad) return;                          // the piece continues in the next chunk
-        // ------------------------------------------------- end of a piece
-        if (have_tx) ws.tx[row] = txk;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, best_i, o);
-            const float om = __shfl_xor_sync(0xffffffffu, M, o);
-            const float os = __shfl_xor_sync(0xffffffffu, S, o);
-            if (ob > best || (ob == best && oi < best_i)) { best = ob; best_i = oi; }
-            lse_merge(M, S, om, os);
-        }
-        if (lane == 0) { rk[cw] = best; ri[cw] = best_i; rm[cw] = M; rs[cw] = S; }
-        csync();
-        if (cw == 0 && lane == 0) {
-            float bk = -INFINITY, mm = -INFINITY, ss = 0.f;
-            int bi = 0x7FFFFFFF;
-            for (int w = 0; w < kRowsConsumers; ++w) {
-                if (rk[w] > bk || (rk[w] == bk && ri[w] < bi)) { bk = rk[w]; bi = ri[w]; }
-                lse_merge(mm, ss, rm[w], rs[w]);
-            }
-            if (!greedy) ws.part[static_cast<size_t>(row) * kNchMax + slot] = make_float2(mm, ss);
-            if (bk > -INFINITY) atomicMax(&ws.wt[row], pack_key(bk, static_cast<uint32_t>(bi)));
-            // the CTA that completes the row makes its decision
-            const long long g0 = static_cast<long long>(n) * npad;
-            const int ncta = static_cast<int>((g0 + npad - 1) / per - g0 / per) + 1;
-            __threadfence();
-            *s_last = atomicAdd(ws.row_cnt + n, 1) == ncta - 1;
-            __threadfence();
-        }
-        csync();                                          // rk..ri are rewritten by the next piece
-        if (*s_last && cw == 0)
-            decide_row<kBF16>(n, row, b, k, gamma, V, per, npad, t, x, lse_d, logp_d, ell, cscale, greedy, seed,
-                              n_accept, next_token, ws);
-    });
+    }
 }
 
 // ---------------------------------------------------- residual, CUDA cores ---
@@ -623,26 +544,16 @@ extern "C" dspark_status_t dspark_verify(int B, int gamma, int V, int r, dspark_
     const int nblk = (V + 63) / 64;
     // plan, then the persistent rows pass (all resident CTAs) with the per-row
     // decisions and per-request outcomes made by the CTAs that finish them
-    static OncePerDevice once;
-    if (once.run(current_device(), [] {
-            cudaError_t e = cudaFuncSetAttribute(verify_rows<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(kRowsSmem));
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(verify_rows<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kRowsSmem));
-            return e;
-        }) != cudaSuccess)
-        return DSPARK_ERR_CUDA;
     const int rgrid = kRowsCtasPerSm * sm_count(current_device());
     verify_plan<<<1, kPlanThreads, 0, s>>>(B, gamma, V, rgrid, ell, ws);
     dspark_status_t stt = launch_status();
     if (stt != DSPARK_OK) return stt;
     if (bf)
-        verify_rows<true><<<rgrid, kRowsThreads, kRowsSmem, s>>>(gamma, V, t_logits, x, lse_d, logp_d, ell, cscale,
-                                                                greedy, seed, n_accept, next_token, ws);
+        verify_rows<true><<<rgrid, 256, 0, s>>>(gamma, V, t_logits, x, lse_d, logp_d, ell, cscale, greedy, seed,
+                                                n_accept, next_token, ws);
     else
-        verify_rows<false><<<rgrid, kRowsThreads, kRowsSmem, s>>>(gamma, V, t_logits, x, lse_d, logp_d, ell, cscale,
-                                                                 greedy, seed, n_accept, next_token, ws);
+        verify_rows<false><<<rgrid, 256, 0, s>>>(gamma, V, t_logits, x, lse_d, logp_d, ell, cscale, greedy, seed,
+                                                 n_accept, next_token, ws);
     if ((stt = launch_status()) != DSPARK_OK || greedy) return stt;
 
     eng::FinishArgs f{};
