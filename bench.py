@@ -3,7 +3,9 @@ scheduler -> verification, on the Qwen3-8B-shaped serving workload
 (B = 64 requests, gamma = 7, V = 151936, H = 4096, r = 256, bf16, T = 0.7),
 synthetic seeded inputs.
 
-One step = one round through the library's C ABI (all kernels on one stream).
+One step = one round through the library's C ABI (all kernels on one stream),
+captured once in a CUDA graph and replayed (--no-graph launches the calls
+directly every step).
 The timed region holds exactly K steps; the L2 is flushed (a 512 MiB write)
 between steps, outside each step's CUDA-event pair.  The JSON line also
 reports the dominant kernel's roofline (the draft engine, one cooperative
@@ -50,7 +52,7 @@ def engine_source_hash():
     reported while the kernel it was measured on is unchanged."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("engine.cuh", "draft.cu", "tc.cuh", "common.cuh"):
+    for f in ("engine.cuh", "tc.cuh", "common.cuh"):   # the draft engine kernel's device code
         with open(os.path.join(ROOT, "serving_draft_verify_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -205,11 +207,42 @@ def run_gpu(args):
         barrier()
         return [s.elapsed_time(e) for s, e in evs], phases
 
-    # main arm, T = 0.7, with per-phase-launch timing of the draft phase kernel
+    def graphed(fn):
+        """fn's launches captured once in a CUDA graph (the library's calls are plain
+        stream work); returns the replay, or None if capture is not possible."""
+        if args.no_graph:
+            return None
+        fn()                                              # one-time attribute setup outside capture
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        try:
+            with torch.cuda.graph(g):
+                fn()
+        except Exception:
+            torch.cuda.synchronize()
+            return None
+        return g.replay
+
+    # main arm, T = 0.7, the round replayed from a CUDA graph; the library's events
+    # around the draft launch are captured with it and time that launch every step
     clocks = ClockSampler(smi_index(local))
     dsv._binding.phase_timing(True)
+    main_round = graphed(lambda: round_(inp, T))
+    use_graph = main_round is not None
+    if not use_graph:
+        main_round = lambda: round_(inp, T)
+    stream = torch.cuda.current_stream()
     clocks.start()
-    times, phase_ms = timed(lambda: round_(inp, T), args.steps, args.warmup, phase_times=True)
+    times, phase_ms = timed(main_round, args.steps, args.warmup, phase_times=True)
+    engine_timing = "events around the draft launch, captured with the replayed round"
+    if not phase_ms:                                      # events in the graph not timeable here
+        _, phase_ms = timed(lambda: round_(inp, T), args.steps, args.warmup, phase_times=True)
+        engine_timing = "events around the draft launch, in as many directly launched rounds"
     clk = clocks.stop()
     dsv._binding.phase_timing(False)
     assert dsv.workspace_status(ws_d) == 0 and dsv.workspace_status(ws_v) == 0
@@ -240,10 +273,11 @@ def run_gpu(args):
                 "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "traffic": args.phase_traffic if args.phase_traffic is not None else recorded_engine_traffic(),
                 "peak_kind": f"{peak_kind} (copy bandwidth)", "bytes_per_launch": int(launch_bytes),
-                "avg_launch_us": round(phase_avg * 1e3, 2), "launches_timed": len(ph)}
+                "avg_launch_us": round(phase_avg * 1e3, 2), "launches_timed": len(ph), "timing": engine_timing}
 
     # greedy round (same workload, T = 0)
-    g_times, _ = timed(lambda: round_(inp, 0.0), max(3, args.steps // 2), args.warmup)
+    greedy_round = graphed(lambda: round_(inp, 0.0)) or (lambda: round_(inp, 0.0))
+    g_times, _ = timed(greedy_round, max(3, args.steps // 2), args.warmup)
     greedy = {"value": B * G * len(g_times) / (sum(g_times) * 1e-3), "unit": "rows/s",
               "ms_per_step": sum(g_times) / len(g_times)}
 
@@ -265,7 +299,7 @@ def run_gpu(args):
         res_host["n_accept"].copy_(outv["n_accept"], non_blocking=True)
         res_host["next_token"].copy_(outv["next_token"], non_blocking=True)
 
-    e_times, _ = timed(e2e_round, args.steps, args.warmup)
+    e_times, _ = timed(graphed(e2e_round) or e2e_round, args.steps, args.warmup)
     e2e = {"value": B * G * args.steps * world / (sum(e_times) * 1e-3), "unit": "rows/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
@@ -287,7 +321,7 @@ def run_gpu(args):
     line = {"metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; shapes of the Qwen3-8B draft setting)",
-            "config": workload_config(world),
+            "config": dict(workload_config(world), cuda_graph=use_graph),
             "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / peak, "roofline": roofline, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps, "clocks": clk,
             "extra": {"greedy_round": greedy, "accept_rate_tv": tv,
@@ -393,6 +427,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--skip-tv", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch the round's calls directly, without a CUDA graph")
     ap.add_argument("--phase-traffic", type=float, default=None,
                     help="dram bytes per draft phase launch from an ncu capture (reported as roofline.traffic)")
     args = ap.parse_args()

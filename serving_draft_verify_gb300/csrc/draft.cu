@@ -379,6 +379,7 @@ extern "C" dspark_status_t dspark_draft_block(int B, int gamma, int V, int H, in
     if (!aligned16(U) || !aligned16(W1) || !aligned16(W2)) return DSPARK_ERR_INVALID_ARGUMENT;
     if (workspace == nullptr || !aligned256(workspace)) return DSPARK_ERR_INVALID_ARGUMENT;
     if (workspace_bytes < dspark_draft_block_workspace_size(B, gamma, V, r)) return DSPARK_ERR_WORKSPACE_TOO_SMALL;
+    clear_stale_error();
     return draft_block_impl(B, gamma, V, H, r, dt, U, h, W1, W2, w, bias, x0, temperature, seed, x, lse_d, logp_d,
                             c, a, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -390,6 +391,7 @@ extern "C" dspark_status_t dspark_debug_draft_logits(int B, int V, int r, const 
     if (B <= 0 || V <= 0 || V % 8 != 0 || r <= 0) return DSPARK_ERR_INVALID_ARGUMENT;
     if (!U_k || !W1 || !W2 || !prev || !z || !workspace || !aligned256(workspace)) return DSPARK_ERR_INVALID_ARGUMENT;
     if (workspace_bytes < dspark_draft_block_workspace_size(B, 1, V, r)) return DSPARK_ERR_WORKSPACE_TOO_SMALL;
+    clear_stale_error();
     return debug_tc_logits(B, V, r, U_k, W1, W2, prev, z, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -411,10 +413,16 @@ extern "C" dspark_status_t dspark_debug_force_phase_launches(int enable) {
 extern "C" int dspark_debug_phase_times(float* ms, int n) {
     if (!g_timing.on || g_timing.recorded == 0 || ms == nullptr) return 0;
     const int m = g_timing.recorded < n ? g_timing.recorded : n;
-    if (cudaEventSynchronize(g_timing.ev[2 * (g_timing.recorded - 1) + 1]) != cudaSuccess) return 0;
+    if (cudaEventSynchronize(g_timing.ev[2 * (g_timing.recorded - 1) + 1]) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
     for (int i = 0; i < m; ++i) {
         float t = 0.f;
-        cudaEventElapsedTime(&t, g_timing.ev[2 * i], g_timing.ev[2 * i + 1]);
+        if (cudaEventElapsedTime(&t, g_timing.ev[2 * i], g_timing.ev[2 * i + 1]) != cudaSuccess) {
+            cudaGetLastError();                           // not timeable: report nothing
+            return 0;
+        }
         ms[i] = t;
     }
     return m;

@@ -34,6 +34,11 @@ inline int sm_count(int dev) {
 }
 
 // Launch-error check mapped to a status.
+// Drops an error left by an earlier, unrelated runtime call (not a sticky one:
+// those persist and fail the next launch), so that launch_status() reports
+// this library's launches only.  Called at the top of each entry point.
+inline void clear_stale_error() { cudaGetLastError(); }
+
 inline dspark_status_t launch_status() {
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;

@@ -337,6 +337,7 @@ extern "C" dspark_status_t dspark_schedule_prefix(int B, int gamma, const float*
     if (!a || !sps || !ell || !n_sched || !theta) return DSPARK_ERR_INVALID_ARGUMENT;
     if (workspace == nullptr || !aligned256(workspace)) return DSPARK_ERR_INVALID_ARGUMENT;
     if (workspace_bytes < dspark_schedule_prefix_workspace_size(B, gamma)) return DSPARK_ERR_WORKSPACE_TOO_SMALL;
+    clear_stale_error();
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     static OncePerDevice once;
     if (once.run(current_device(), [] {

@@ -390,6 +390,7 @@ extern "C" dspark_status_t dspark_accept_rate_tv(int64_t rows, int V, dspark_dty
     if (d == nullptr || t == nullptr || c_star == nullptr) return DSPARK_ERR_INVALID_ARGUMENT;
     if (!aligned16(d) || !aligned16(t)) return DSPARK_ERR_INVALID_ARGUMENT;
     if (V > 163840) return DSPARK_ERR_UNSUPPORTED;
+    clear_stale_error();
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (clear_status(workspace, s) != DSPARK_OK) return DSPARK_ERR_CUDA;
     StatusBlock* st = static_cast<StatusBlock*>(workspace);

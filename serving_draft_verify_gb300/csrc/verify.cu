@@ -536,6 +536,7 @@ extern "C" dspark_status_t dspark_verify(int B, int gamma, int V, int r, dspark_
     if (!aligned16(t_logits) || !aligned16(U) || !aligned16(W1) || !aligned16(W2)) return DSPARK_ERR_INVALID_ARGUMENT;
     if (workspace == nullptr || !aligned256(workspace)) return DSPARK_ERR_INVALID_ARGUMENT;
     if (workspace_bytes < dspark_verify_workspace_size(B, gamma, V, r)) return DSPARK_ERR_WORKSPACE_TOO_SMALL;
+    clear_stale_error();
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const VerifyWs ws = verify_ws(workspace, B, gamma);
     const int greedy = (temperature == 0.f);
