@@ -102,3 +102,34 @@ def test_tv_missing_half_is_caught(monkeypatch):
                         lambda d, t: 1.0 - np.sum(np.abs(tv.softmax(d) - tv.softmax(t)), axis=-1))
     assert _fails(T_tv.test_disjoint_supports_give_zero)
     assert _fails(T_tv.test_two_point_closed_form)
+
+
+def test_loss_ce_without_logsumexp_is_caught(monkeypatch):
+    from oracle import loss as L
+    import tests.test_oracle_loss as T_loss
+    monkeypatch.setattr(L, "logsumexp_rows", lambda x: np.max(np.asarray(x, np.float64), axis=-1))
+    assert _fails(T_loss.test_closed_forms)
+
+
+def test_loss_bce_sign_slip_is_caught(monkeypatch):
+    from oracle import loss as L
+    import tests.test_oracle_loss as T_loss
+    orig = L.softplus
+    monkeypatch.setattr(L, "softplus", lambda s: orig(-np.asarray(s, np.float64)))
+    assert _fails(T_loss.test_grad_s_matches_central_differences)
+
+
+def test_loss_l1_gradient_without_the_softmax_mean_is_caught(monkeypatch):
+    from oracle import loss as L
+    import tests.test_oracle_loss as T_loss
+
+    def bad_grad(d, t, target, conf_logit, omega, alpha_ce=L.ALPHA_CE, alpha_l1=L.ALPHA_L1, alpha_conf=L.ALPHA_CONF):
+        p_d, p_t = L.softmax(d), L.softmax(t)
+        g = np.asarray(omega, np.float64)[:, None] * alpha_l1 * 0.5 * p_d * np.sign(p_d - p_t)
+        R = p_d.shape[0]
+        oh = np.zeros_like(p_d)
+        oh[np.arange(R), target] = 1.0
+        g += np.asarray(omega, np.float64)[:, None] * alpha_ce * (p_d - oh)
+        return g, np.zeros(R)
+    monkeypatch.setattr(L, "dspark_loss_grad", bad_grad)
+    assert _fails(T_loss.test_grad_d_matches_central_differences)
