@@ -314,7 +314,22 @@ def run_gpu(args):
         tv_ms = sum(tv_times) / len(tv_times)
         tv = {"rows": d_.shape[0], "ms": tv_ms, "rows_per_s": d_.shape[0] / (tv_ms * 1e-3),
               "achieved_gbs": tvb / (tv_ms * 1e-3) / 1e9, "frac_of_peak": tvb / (tv_ms * 1e-3) / 1e9 / peak}
-        del d_, t_
+        # the joint training loss with its gradient on the same rows: d, t read, dL/dd written
+        tgt_, s_, k_ = wl.make_loss_inputs(wl.TV_TRAIN, device=dev)
+        w_ = torch.exp(-(k_.double() - 1.0) / 4.0)      # position weights, normalised to a weighted mean
+        om_ = (w_ / w_.sum()).float()
+        lout = dict(row=torch.empty((d_.shape[0], 4), dtype=torch.float32, device=dev),
+                    loss=torch.empty(1, dtype=torch.float32, device=dev),
+                    grad_d=torch.empty_like(d_), grad_conf=torch.empty(d_.shape[0], dtype=torch.float32, device=dev))
+        ws_l = torch.empty(1 << 16, dtype=torch.uint8, device=dev)
+        l_times, _ = timed(lambda: dsv.dspark_training_loss(d_, t_, tgt_, s_, om_, out=lout, workspace=ws_l), 5, 3)
+        lb = 3 * d_.numel() * 2
+        l_ms = sum(l_times) / len(l_times)
+        tv["training_loss"] = {"ms": l_ms, "rows_per_s": d_.shape[0] / (l_ms * 1e-3),
+                               "bytes_per_row": 3 * d_.shape[1] * 2,
+                               "achieved_gbs": lb / (l_ms * 1e-3) / 1e9,
+                               "frac_of_peak": lb / (l_ms * 1e-3) / 1e9 / peak}
+        del d_, t_, lout
     # draft: the cooperative engine launch; schedule: 1; verify: plan, rows, residual (+ final token)
     launches_per_step = 1 + 1 + 3
 

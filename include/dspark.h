@@ -7,6 +7,7 @@
  *   dspark_schedule_prefix  hardware-aware prefix scheduler (Algorithm 1)
  *   dspark_verify           rejection-sampling verification + residual/bonus token
  *   dspark_accept_rate_tv   c* = 1 - 1/2 ||softmax(d) - softmax(t)||_1 per row
+ *   dspark_training_loss    joint CE + L1 + BCE loss per row, and its gradient
  *
  * Sources (cited per call): the DeepSpec / DSpark walkthrough at
  * wangjunjian.com ("DSpark" post, sections 2.1, 3.2, 3.3, 8.2) and the
@@ -205,6 +206,46 @@ dspark_status_t dspark_accept_rate_tv(int64_t rows, int V, dspark_dtype_t dt,
                                       const void* d, const void* t, float* c_star,
                                       void* workspace, size_t workspace_bytes,
                                       dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Joint training loss of the drafter and its gradient (DeepSpec walkthrough
+ * section 7.2, `compute_dspark_loss`; position weights from
+ * `_build_loss_weight_mask`).  For each row, with p = softmax over the full
+ * vocabulary (no temperature):
+ *   ce   = logsumexp(d) - d[target]
+ *   c*   = sum_v min(p_d(v), p_t(v))            (= 1 - 1/2 ||p_d - p_t||_1, eq. 8)
+ *   bce  = softplus(s) - c* s                    (BCE with logits, target c*)
+ *   row  = omega (alpha_ce ce + alpha_l1 (1 - c*) + alpha_conf bce)
+ *   loss = sum over rows of row
+ * and, with c* held fixed as the BCE's target and sgn_v = sign(p_d(v) - p_t(v)),
+ *   grad_d[v]  = omega (alpha_ce (p_d(v) - [v = target])
+ *                      + alpha_l1 / 2 p_d(v) (sgn_v - sum_u p_d(u) sgn_u))
+ *   grad_conf  = omega alpha_conf (sigmoid(s) - c*).
+ * The page's weights are alpha_ce = 0.1, alpha_l1 = 0.9, alpha_conf = 1.0 and
+ * the position weight of block position k is exp(-(k - 1) / 4); the caller
+ * folds position weights and any normalisation into omega (omega = w_k /
+ * sum w gives the weighted mean).
+ *
+ *   d, t [rows][V] in `dt` (draft and target logits); target [rows] int32 in
+ *   [0, V); conf_logit [rows] float32 (the confidence head's logit s); omega
+ *   [rows] float32.
+ *   row_out [rows][4] float32: (ce, c*, bce, row); loss [1] float32 (summed
+ *   in a fixed order: the same inputs give the same bits).
+ *   grad_d [rows][V] in `dt`, or NULL to skip it; grad_conf [rows] float32, or
+ *   NULL.  Every byte of d and t is read once; grad_d is written from
+ *   registers in the same pass.
+ *   A target id outside [0, V) sets DSPARK_ERR_DEVICE_CHECK (that row's ce is
+ *   then +inf).  rows == 0 writes loss = 0.  Requires V <= 163840.
+ * ------------------------------------------------------------------------ */
+size_t dspark_training_loss_workspace_size(int64_t rows, int V);
+
+dspark_status_t dspark_training_loss(int64_t rows, int V, dspark_dtype_t dt,
+                                     const void* d, const void* t, const int32_t* target,
+                                     const float* conf_logit, const float* omega,
+                                     float alpha_ce, float alpha_l1, float alpha_conf,
+                                     float* row_out, float* loss, void* grad_d, float* grad_conf,
+                                     void* workspace, size_t workspace_bytes,
+                                     dspark_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -10,6 +10,7 @@ from ._binding import (  # noqa: F401
     SAMPLE_BLOCK,
     MAX_GAMMA,
     dspark_accept_rate_tv,
+    dspark_training_loss,
     dspark_draft_block,
     dspark_schedule_prefix,
     dspark_verify,

@@ -39,6 +39,9 @@ _SIGNATURES = {
                                _c_float, _c_u64, _p, _p, _p, _c_size, _p]),
     "dspark_accept_rate_tv_workspace_size": (_c_size, [_c_i64, _c_int]),
     "dspark_accept_rate_tv": (_c_int, [_c_i64, _c_int, _c_int, _p, _p, _p, _p, _c_size, _p]),
+    "dspark_training_loss_workspace_size": (_c_size, [_c_i64, _c_int]),
+    "dspark_training_loss": (_c_int, [_c_i64, _c_int, _c_int, _p, _p, _p, _p, _p, _c_float, _c_float, _c_float,
+                                      _p, _p, _p, _p, _p, _c_size, _p]),
     "dspark_debug_draft_logits": (_c_int, [_c_int, _c_int, _c_int, _p, _p, _p, _p, _p, _p, _c_size, _p]),
     "dspark_debug_enable_phase_timing": (_c_int, [_c_int]),
     "dspark_debug_phase_times": (_c_int, [_p, _c_int]),
@@ -148,6 +151,41 @@ def dspark_accept_rate_tv(d, t, c_star=None, workspace=None, stream=None):
            lib.dspark_accept_rate_tv(rows, V, dt, _ptr(d), _ptr(t), _ptr(c_star), _ptr(ws), _nbytes(ws),
                                      _stream(stream)))
     return c_star
+
+
+def dspark_training_loss(d, t, target, conf_logit, omega, alpha_ce=0.1, alpha_l1=0.9, alpha_conf=1.0,
+                         grad=True, out=None, workspace=None, stream=None):
+    """Joint loss; returns dict row [rows, 4] (ce, c*, bce, row), loss [1] and,
+    with grad=True, grad_d [rows, V] (d's dtype) and grad_conf [rows]."""
+    lib = load()
+    rows, V = d.shape
+    _need(d, (rows, V), name="d")
+    _need(t, (rows, V), d.dtype, name="t")
+    _need(target, (rows,), torch.int32, name="target")
+    _need(conf_logit, (rows,), torch.float32, name="conf_logit")
+    _need(omega, (rows,), torch.float32, name="omega")
+    dt = _dtype_code(d, t)
+    dev = d.device
+    if out is None:
+        out = dict(row=torch.empty((rows, 4), dtype=torch.float32, device=dev),
+                   loss=torch.empty(1, dtype=torch.float32, device=dev))
+        if grad:
+            out["grad_d"] = torch.empty((rows, V), dtype=d.dtype, device=dev)
+            out["grad_conf"] = torch.empty(rows, dtype=torch.float32, device=dev)
+    _need(out["row"], (rows, 4), torch.float32, name="row")
+    _need(out["loss"], (1,), torch.float32, name="loss")
+    gd, gc = out.get("grad_d"), out.get("grad_conf")
+    if gd is not None:
+        _need(gd, (rows, V), d.dtype, name="grad_d")
+    if gc is not None:
+        _need(gc, (rows,), torch.float32, name="grad_conf")
+    ws = _workspace(lib.dspark_training_loss_workspace_size(rows, V), dev, workspace)
+    _check("dspark_training_loss",
+           lib.dspark_training_loss(rows, V, dt, _ptr(d), _ptr(t), _ptr(target), _ptr(conf_logit), _ptr(omega),
+                                    float(alpha_ce), float(alpha_l1), float(alpha_conf), _ptr(out["row"]),
+                                    _ptr(out["loss"]), _ptr(gd), _ptr(gc), _ptr(ws), _nbytes(ws),
+                                    _stream(stream)))
+    return out
 
 
 def dspark_draft_block(U, h, W1, W2, w, bias, x0, temperature, seed, out=None, workspace=None,

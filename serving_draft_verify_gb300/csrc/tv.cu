@@ -69,6 +69,12 @@ __device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigne
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+// Two floats -> a bf16 pair (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -79,9 +85,28 @@ __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
 // values only after the cluster barrier of row it+1, which every CTA reaches
 // only after its reads of row it-1's values, so parity it+1 is free.
 struct Slot {
-    float4 ms[2];           // slice max (log2 units) and sum of 2^(y - m) of d and t: (md, sd, mt, st)
+    float4 ms[2];           // slice max and sum of 2^((x - m) log2e) of d and t: (md, sd, mt, st)
+    float4 q[2];            // loss mode: partials (sum min(p_d, p_t), sum p_d sign(p_d - p_t), d[target] or -inf)
     float p[2];             // CTA partial of sum min(p_d, p_t)
     float pad[2];
+};
+
+// The training loss (loss mode of the kernel): per row, with p = softmax,
+//   ce = logsumexp(d) - d[target], c* = sum min(p_d, p_t), l1 = 1 - c*,
+//   bce = softplus(s) - c* s, row = omega (a_ce ce + a_l1 l1 + a_conf bce),
+//   dL/dd_v = omega (a_ce (p_d(v) - [v = target]) + a_l1 / 2 p_d(v) (sgn_v - sum_u p_d(u) sgn_u)),
+//   dL/ds = omega a_conf (sigmoid(s) - c*), sgn_v = sign(p_d(v) - p_t(v)).
+struct LossArgs {
+    const int32_t* target;  // [rows]
+    const float* s;         // [rows] confidence head logits
+    const float* omega;     // [rows] row weights
+    float a_ce, a_l1, a_conf;
+    float* row_out;         // [rows][4] (ce, c*, bce, row)
+    void* grad;             // [rows][V] dL/dd (input dtype), or null
+    float* grad_s;          // [rows] dL/ds, or null
+    float* cl_part;         // [clusters] each cluster's sum of row totals
+    unsigned int* cl_done;  // clusters finished (starts at 0)
+    float* loss;            // [1] sum of row totals
 };
 
 // (m, s) with s a sum of 2^((x - m) log2e): merge across a warp.
@@ -101,10 +126,10 @@ __device__ __forceinline__ void warp_lse(float& m, float& s) {
     }
 }
 
-template <bool kBF16>
+template <bool kBF16, bool kLoss>
 __global__ void __launch_bounds__(kThreads, 1)
 tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* __restrict__ c_star,
-          int64_t rows, int V, int slice, StatusBlock* status) {
+          int64_t rows, int V, int slice, StatusBlock* status, LossArgs la) {
     using Tr = TVTraits<kBF16>;
     constexpr int EPG = Tr::kEPG, ESZ = Tr::kESZ, STAGES = Tr::kStages, GMAX = Tr::kGMax;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -156,6 +181,7 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
     bool failed = false;
     int it = 0;
     int64_t prev_row = -1;                                // row whose partials wait in the slots
+    float cl_sum = 0.f;                                   // loss mode: this cluster's row totals, in row order
     for (int64_t row = cid; row < rows; row += ncl, ++it) {
         const int s = it % STAGES;
         const uint32_t par = static_cast<uint32_t>(it / STAGES) & 1u;
@@ -205,6 +231,20 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
         // a thread without a finite logit keeps reference 0 so that its terms are 0
         const float md = (mxd > -INFINITY) ? mxd : 0.f;
         const float mt = (mxt > -INFINITY) ? mxt : 0.f;
+        // loss mode: the target's logit, from the CTA whose slice holds it
+        int tgt = -1;
+        float dtgt = -INFINITY;
+        if constexpr (kLoss) {
+            tgt = la.target[row];
+            if (tgt < 0 || tgt >= V) {
+                if (tid == 0 && rank == 0) set_status(status, DSPARK_ERR_DEVICE_CHECK, 30);
+                tgt = -1;
+            }
+            if (tid == 0 && !failed && tgt >= lo && tgt < lo + len) {
+                const uint8_t* src = buf + (2 * s) * stage_bytes + static_cast<size_t>(tgt - lo) * ESZ;
+                dtgt = kBF16 ? bf16lo(*reinterpret_cast<const uint16_t*>(src)) : *reinterpret_cast<const float*>(src);
+            }
+        }
 
         // B: e in registers (packed pairs), the thread's sums
         unsigned long long ed[GMAX * EPG / 2], et[GMAX * EPG / 2];
@@ -263,7 +303,7 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
         cluster.sync();                                   // slices' (m, s) and the previous row's partials
 
         // the previous row's c*: rank 0 sums its CTAs' partials in rank order
-        if (rank == 0 && warp == 1 && prev_row >= 0) {
+        if (!kLoss && rank == 0 && warp == 1 && prev_row >= 0) {
             const float pr = (lane < kCS) ? cluster.map_shared_rank(slot, lane)->p[(it - 1) & 1] : 0.f;
             const float c = warp_sum(pr);
             if (lane == 0 && !failed) c_star[prev_row] = c;
@@ -285,29 +325,108 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
 
         // C: sum of min(p_d, p_t) over this thread's elements, from registers
         const unsigned long long al = pk(alpha, alpha), be = pk(beta, beta);
-        unsigned long long pp = pk(0.f, 0.f);
+        unsigned long long pp = pk(0.f, 0.f), sp = pk(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < GMAX * EPG / 2; ++i) {
             const float2 x = upk(mul2(ed[i], al)), y = upk(mul2(et[i], be));
             pp = add2(pp, pk(fminf(x.x, y.x), fminf(x.y, y.y)));
+            if constexpr (kLoss) {
+                const float s0 = x.x > y.x ? x.x : (x.x < y.x ? -x.x : 0.f);   // p_d sign(p_d - p_t)
+                const float s1 = x.y > y.y ? x.y : (x.y < y.y ? -x.y : 0.f);
+                sp = add2(sp, pk(s0, s1));
+            }
         }
         float p = warp_sum(upk(pp).x + upk(pp).y);
+        float sgs = kLoss ? warp_sum(upk(sp).x + upk(sp).y) : 0.f;
         __syncthreads();                                  // red is free again
-        if (lane == 0) red[warp].x = p;
+        if (lane == 0) { red[warp].x = p; red[warp].y = sgs; }
         __syncthreads();
         if (warp == 0) {
             float q = (lane < kWarps) ? red[lane].x : 0.f;
             q = warp_sum(q);
-            if (lane == 0) slot->p[it & 1] = q;
+            if constexpr (kLoss) {
+                float q2 = (lane < kWarps) ? red[lane].y : 0.f;
+                q2 = warp_sum(q2);
+                if (lane == 0) slot->q[it & 1] = make_float4(q, q2, dtgt, 0.f);
+            } else {
+                if (lane == 0) slot->p[it & 1] = q;
+            }
+        }
+        if constexpr (kLoss) {
+            cluster.sync();                               // this row's partials, every CTA
+            float c0 = 0.f, c1 = 0.f, c2 = -INFINITY;
+            if (lane < kCS) {
+                const float4 rq = cluster.map_shared_rank(slot, lane)->q[it & 1];
+                c0 = rq.x; c1 = rq.y; c2 = rq.z;
+            }
+            // rank order within each reduction: every warp gets the same sums
+            const float cstar = warp_sum(c0), sbar = warp_sum(c1), dt_t = warp_max(c2);
+            // D: dL/dd from registers
+            const float om = la.omega[row];
+            if (la.grad != nullptr && !failed) {
+                const float ka = om * la.a_ce, kl = 0.5f * om * la.a_l1;
+#pragma unroll
+                for (int gi = 0; gi < GMAX; ++gi) {
+                    const int g = tid + gi * kThreads;
+                    if (g < ngroups) {
+                        float gv[EPG];
+#pragma unroll
+                        for (int e = 0; e < EPG; e += 2) {
+                            const float2 x = upk(mul2(ed[(gi * EPG + e) / 2], al));
+                            const float2 y = upk(mul2(et[(gi * EPG + e) / 2], be));
+                            const float sg0 = x.x > y.x ? 1.f : (x.x < y.x ? -1.f : 0.f);
+                            const float sg1 = x.y > y.y ? 1.f : (x.y < y.y ? -1.f : 0.f);
+                            const int v = lo + g * EPG + e;
+                            gv[e] = ka * (x.x - (v == tgt ? 1.f : 0.f)) + kl * x.x * (sg0 - sbar);
+                            gv[e + 1] = ka * (x.y - (v + 1 == tgt ? 1.f : 0.f)) + kl * x.y * (sg1 - sbar);
+                        }
+                        uint8_t* dst = static_cast<uint8_t*>(la.grad) + (static_cast<size_t>(row) * V + lo + g * EPG) * ESZ;
+                        if constexpr (kBF16) {
+                            uint4 o;
+                            o.x = pack_bf16(gv[0], gv[1]); o.y = pack_bf16(gv[2], gv[3]);
+                            o.z = pack_bf16(gv[4], gv[5]); o.w = pack_bf16(gv[6], gv[7]);
+                            *reinterpret_cast<uint4*>(dst) = o;
+                        } else {
+                            *reinterpret_cast<float4*>(dst) = make_float4(gv[0], gv[1], gv[2], gv[3]);
+                        }
+                    }
+                }
+            }
+            if (rank == 0 && warp == 0 && lane == 0 && !failed) {
+                const float sv = la.s[row];
+                const float ce = (Md + log2f(Sd) * kLn2) - dt_t;   // natural-log logsumexp minus d[target]
+                const float sp_ = fmaxf(sv, 0.f) + log1pf(expf(-fabsf(sv)));
+                const float bce = sp_ - cstar * sv;
+                const float tot = om * (la.a_ce * ce + la.a_l1 * (1.f - cstar) + la.a_conf * bce);
+                reinterpret_cast<float4*>(la.row_out)[row] = make_float4(ce, cstar, bce, tot);
+                if (la.grad_s != nullptr) la.grad_s[row] = om * la.a_conf * (1.f / (1.f + expf(-sv)) - cstar);
+                cl_sum += tot;
+                if (c_star != nullptr) c_star[row] = cstar;
+            }
         }
         prev_row = row;
     }
     // the last row's c*, and no CTA leaves while a peer may still read its shared memory
     cluster.sync();
-    if (rank == 0 && warp == 1 && prev_row >= 0) {
+    if (!kLoss && rank == 0 && warp == 1 && prev_row >= 0) {
         const float pr = (lane < kCS) ? cluster.map_shared_rank(slot, lane)->p[(it - 1) & 1] : 0.f;
         const float c = warp_sum(pr);
         if (lane == 0 && !failed) c_star[prev_row] = c;
+    }
+    if constexpr (kLoss) {
+        // the loss: each cluster's sum of its rows, then the last cluster to finish adds
+        // the clusters' sums in cluster order
+        if (rank == 0 && tid == 0) {
+            la.cl_part[cid] = cl_sum;
+            __threadfence();
+            const bool last = atomicAdd(la.cl_done, 1u) == static_cast<unsigned>(ncl) - 1u;
+            if (last) {
+                __threadfence();
+                float tot = 0.f;
+                for (int64_t c = 0; c < ncl; ++c) tot += __ldcg(la.cl_part + c);
+                *la.loss = tot;
+            }
+        }
     }
     cluster.sync();
     // after a timeout, give any copy still in flight a bounded chance to land
@@ -324,9 +443,13 @@ size_t tv_smem_bytes(int slice) {
            sizeof(Slot) + 128;
 }
 
-template <bool kBF16>
+// Clusters of the loss launch are at most this many (their partial sums live in
+// the workspace).
+constexpr int kMaxLossClusters = 1024;
+
+template <bool kBF16, bool kLoss>
 dspark_status_t launch_tv(int64_t rows, int V, const void* d, const void* t, float* c_star,
-                          StatusBlock* status, cudaStream_t stream) {
+                          StatusBlock* status, const LossArgs& la, cudaStream_t stream) {
     using Tr = TVTraits<kBF16>;
     const int per = (V + kCS - 1) / kCS;
     const int slice = (per + Tr::kEPG - 1) / Tr::kEPG * Tr::kEPG;
@@ -334,10 +457,10 @@ dspark_status_t launch_tv(int64_t rows, int V, const void* d, const void* t, flo
     const size_t smem = tv_smem_bytes<kBF16>(slice);
     if (smem > 227 * 1024) return DSPARK_ERR_UNSUPPORTED;
     const int dev = current_device();
+    auto* kern = tv_kernel<kBF16, kLoss>;
     static OncePerDevice once;
-    if (once.run(dev, [] {
-            return cudaFuncSetAttribute(tv_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        227 * 1024);
+    if (once.run(dev, [kern] {
+            return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         }) != cudaSuccess)
         return DSPARK_ERR_CUDA;
 
@@ -354,17 +477,17 @@ dspark_status_t launch_tv(int64_t rows, int V, const void* d, const void* t, flo
     cfg.numAttrs = 1;
     cfg.gridDim = dim3(kCS * 256);
     int max_clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, tv_kernel<kBF16>, &cfg) != cudaSuccess ||
-        max_clusters < 1) {
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess || max_clusters < 1) {
         cudaGetLastError();
         max_clusters = sm_count(dev) / kCS;
         if (max_clusters < 1) max_clusters = 1;
     }
+    if (max_clusters > kMaxLossClusters) max_clusters = kMaxLossClusters;
     const int64_t ncl = rows < max_clusters ? rows : max_clusters;
     cfg.gridDim = dim3(static_cast<unsigned>(ncl * kCS));
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, tv_kernel<kBF16>, static_cast<const uint8_t*>(d),
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t*>(d),
                                              static_cast<const uint8_t*>(t), c_star, rows, V, slice,
-                                             status);
+                                             status, la);
     return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 
@@ -394,6 +517,58 @@ extern "C" dspark_status_t dspark_accept_rate_tv(int64_t rows, int V, dspark_dty
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (clear_status(workspace, s) != DSPARK_OK) return DSPARK_ERR_CUDA;
     StatusBlock* st = static_cast<StatusBlock*>(workspace);
-    return dt == DSPARK_BF16 ? launch_tv<true>(rows, V, d, t, c_star, st, s)
-                             : launch_tv<false>(rows, V, d, t, c_star, st, s);
+    const LossArgs none{};
+    return dt == DSPARK_BF16 ? launch_tv<true, false>(rows, V, d, t, c_star, st, none, s)
+                             : launch_tv<false, false>(rows, V, d, t, c_star, st, none, s);
+}
+
+// Workspace of the loss: status block | cluster counter (own 256 bytes) | one
+// float per cluster.
+extern "C" size_t dspark_training_loss_workspace_size(int64_t rows, int V) {
+    (void)rows;
+    (void)V;
+    return kStatusBytes + 256 + static_cast<size_t>(kMaxLossClusters) * sizeof(float);
+}
+
+extern "C" dspark_status_t dspark_training_loss(int64_t rows, int V, dspark_dtype_t dt, const void* d,
+                                                const void* t, const int32_t* target, const float* conf_logit,
+                                                const float* omega, float alpha_ce, float alpha_l1,
+                                                float alpha_conf, float* row_out, float* loss, void* grad_d,
+                                                float* grad_conf, void* workspace, size_t workspace_bytes,
+                                                dspark_stream_t stream) {
+    if (rows < 0 || V <= 0 || (dt != DSPARK_F32 && dt != DSPARK_BF16)) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (V % (dt == DSPARK_BF16 ? 8 : 4) != 0) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (workspace == nullptr || !aligned256(workspace)) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (workspace_bytes < dspark_training_loss_workspace_size(rows, V)) return DSPARK_ERR_WORKSPACE_TOO_SMALL;
+    if (loss == nullptr) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (V > 163840) return DSPARK_ERR_UNSUPPORTED;
+    if (rows > 0) {
+        if (d == nullptr || t == nullptr || target == nullptr || conf_logit == nullptr || omega == nullptr ||
+            row_out == nullptr)
+            return DSPARK_ERR_INVALID_ARGUMENT;
+        if (!aligned16(d) || !aligned16(t) || !aligned16(row_out)) return DSPARK_ERR_INVALID_ARGUMENT;
+        if (grad_d != nullptr && !aligned16(grad_d)) return DSPARK_ERR_INVALID_ARGUMENT;
+    }
+    clear_stale_error();
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // status and the cluster counter
+    if (cudaMemsetAsync(workspace, 0, kStatusBytes + 256, s) != cudaSuccess) return DSPARK_ERR_CUDA;
+    if (rows == 0) return cudaMemsetAsync(loss, 0, sizeof(float), s) == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+    StatusBlock* st = static_cast<StatusBlock*>(workspace);
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    LossArgs la{};
+    la.target = target;
+    la.s = conf_logit;
+    la.omega = omega;
+    la.a_ce = alpha_ce;
+    la.a_l1 = alpha_l1;
+    la.a_conf = alpha_conf;
+    la.row_out = row_out;
+    la.grad = grad_d;
+    la.grad_s = grad_conf;
+    la.cl_done = reinterpret_cast<unsigned int*>(base + kStatusBytes);
+    la.cl_part = reinterpret_cast<float*>(base + kStatusBytes + 256);
+    la.loss = loss;
+    return dt == DSPARK_BF16 ? launch_tv<true, true>(rows, V, d, t, nullptr, st, la, s)
+                             : launch_tv<false, true>(rows, V, d, t, nullptr, st, la, s);
 }

@@ -19,7 +19,8 @@ config overrides it):
 
 The high-concurrency config draws one peak rate per request from Beta(5, 2).
 TV rows: d like U (peak rate 0.7), t = d + N(0, sigma_row^2) with sigma_row ~
-U(0.1, 2.0) per row.
+U(0.1, 2.0) per row.  Training-loss rows add a uniform target token, a
+N(0, 2^2) confidence logit and the block position (row mod 16) + 1.
 """
 from dataclasses import dataclass, field, replace
 
@@ -138,6 +139,24 @@ def make_tv_inputs(cfg, device="cpu", rows=None):
         noise = torch.randn((r1 - r0, cfg.V), generator=gen, device=dev) * sigma[r0:r1, None]
         t[r0:r1] = (d[r0:r1].float() + noise).to(dt)
     return d, t
+
+
+LOSS_BLOCK = 16   # training block size: rows are (sequence, anchor, block position k)
+
+
+def make_loss_inputs(cfg, device="cpu", rows=None):
+    """The training loss's per-row inputs beside make_tv_inputs' (d, t):
+    target [rows] int32 ~ uniform over the vocabulary, conf_logit [rows]
+    float32 ~ N(0, 2^2) (the confidence head's logit), and the block position
+    k [rows] int64 = row mod 16 + 1 (rows are sequence x anchor x position)."""
+    dev = torch.device(device)
+    n = cfg.rows if rows is None else rows
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(cfg.seed + 1000)
+    target = torch.randint(0, cfg.V, (n,), generator=gen, device=dev).to(torch.int32)
+    conf_logit = torch.randn((n,), generator=gen, device=dev) * 2.0
+    k = torch.arange(n, device=dev) % LOSS_BLOCK + 1
+    return target, conf_logit, k
 
 
 def to_f64(x):
