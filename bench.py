@@ -434,6 +434,46 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def run_tv_only(args):
+    """The accept-rate TV and training-loss kernels alone on `args.tv_rows` rows of
+    the training workload (a small case for profiling); prints one JSON line."""
+    import torch
+    import serving_draft_verify_gb300 as dsv
+    from serving_draft_verify_gb300 import workloads as wl
+
+    dev = torch.device("cuda", 0)
+    dsv.load()
+    cfg = wl.scaled(wl.TV_TRAIN, rows=args.tv_rows)
+    d, t = wl.make_tv_inputs(cfg, device=dev)
+    tgt, s, k = wl.make_loss_inputs(cfg, device=dev)
+    w = torch.exp(-(k.double() - 1.0) / 4.0)
+    om = (w / w.sum()).float()
+    cst = torch.empty(cfg.rows, dtype=torch.float32, device=dev)
+    lout = dict(row=torch.empty((cfg.rows, 4), dtype=torch.float32, device=dev),
+                loss=torch.empty(1, dtype=torch.float32, device=dev),
+                grad_d=torch.empty_like(d), grad_conf=torch.empty(cfg.rows, dtype=torch.float32, device=dev))
+    ws = torch.empty(1 << 16, dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    res = {"workload": f"{cfg.name}: {cfg.rows} x {cfg.V} {cfg.dtype}"}
+    kernels = (("accept_rate_tv", lambda: dsv.dspark_accept_rate_tv(d, t, c_star=cst, workspace=ws), 2),
+               ("training_loss", lambda: dsv.dspark_training_loss(d, t, tgt, s, om, out=lout, workspace=ws), 3))
+    for name, fn, nb in kernels:
+        for _ in range(args.warmup):
+            fn()
+        ms = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+        m = sum(ms) / len(ms)
+        res[name] = {"ms": m, "gbs": nb * d.numel() * d.element_size() / (m * 1e-3) / 1e9}
+    print(json.dumps(res))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -445,10 +485,14 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch the round's calls directly, without a CUDA graph")
     ap.add_argument("--phase-traffic", type=float, default=None,
                     help="dram bytes per draft phase launch from an ncu capture (reported as roofline.traffic)")
+    ap.add_argument("--tv-rows", type=int, default=None,
+                    help="time only the TV and training-loss kernels on this many training rows")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "native":
         args.warmup = 3
-    if args.impl == "reference":
+    if args.tv_rows is not None:
+        run_tv_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

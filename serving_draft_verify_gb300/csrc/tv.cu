@@ -1,17 +1,25 @@
 // dspark_accept_rate_tv: c* = 1 - 1/2 ||softmax(d) - softmax(t)||_1 per row
 // (DeepSpec walkthrough, section 3.3, paper eq. 8 / `_compute_accept_rate_3d`),
-// computed as sum_v min(p_d(v), p_t(v)).
+// computed as sum_v exp(min(d_v - L_d, t_v - L_t)) with L = logsumexp of the row;
+// and dspark_training_loss (section 7.2, `compute_dspark_loss`), the same pass
+// extended to the joint loss and its gradient.
 //
-// One HBM pass per row.  A thread-block cluster of kCS CTAs owns one row at a
-// time; each CTA bulk-copies its 1/kCS slice of d and t into shared memory
-// (double-buffered, so the next row streams in while this one is reduced):
-//   A. each thread's max of its d and t elements (packed bf16 max);
-//   B. e_d = 2^(d log2e - m_d), e_t likewise, kept in registers as packed
-//      float pairs; the thread's sums, merged per warp and per CTA;
-//   -- one cluster barrier per row: the CTAs' (m, s) through distributed shared
-//      memory (and the previous row's partials, which rank 0 sums into c*) --
-//   C. sum min(e_d 2^(m_d - L_d), e_t 2^(m_t - L_t)) from registers (no exp).
-// Two exponentials per logit pair; every byte of d and t is read once from HBM.
+// One HBM pass per row.  A thread-block cluster of cs CTAs (the smallest of 1, 2,
+// 4, 8, 16 whose slices fit; 4 for bf16 rows of the Qwen3 vocabulary) owns one
+// row at a time; each CTA bulk-copies its 1/cs slice of d and t into shared
+// memory.  Slices stream through three slots in the order d_0, t_0, d_1, t_1, ...,
+// so row i+1's d lands while row i is reduced:
+//   AB. per tensor: each thread's max (packed bf16 max) and sum of
+//       2^((x - m) log2e) over its elements (held in registers between the two);
+//       merged per warp, per CTA;
+//   -- cluster barrier: the CTAs' (m, s) through distributed shared memory (and
+//      the previous row's partials, which rank 0 sums into c*) --
+//   C.  sum of 2^(min(d - L_d, t - L_t) log2e) from shared memory;
+//   loss mode: C also sums p_d over d - t < L_d - L_t and over ties, a second
+//   cluster barrier exchanges them with the target logit, and pass D writes
+//   dL/dd from shared memory.
+// Three exponentials per logit pair (four with the gradient); every byte of d
+// and t is read once from HBM.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -22,16 +30,17 @@ namespace cg = cooperative_groups;
 namespace dspark {
 namespace {
 
-constexpr int kCS = 8;          // CTAs per cluster (one row per cluster)
-constexpr int kThreads = 512;
+constexpr int kMaxCS = 16;      // CTAs per cluster at most (one row per cluster)
+constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
+constexpr int kSlots = 3;       // slice slots: d_i, t_i and d_{i+1} resident at once
+constexpr int kGMax = 5;        // 16-byte groups per thread and slice (a slot holds at most 5 x 1024 x 16 B)
+constexpr size_t kSmemCap = 227 * 1024;
 
 template <bool kBF16>
 struct TVTraits {
     static constexpr int kEPG = kBF16 ? 8 : 4;   // elements per 16-byte group
     static constexpr int kESZ = kBF16 ? 2 : 4;
-    static constexpr int kStages = kBF16 ? 2 : 1;     // at most 2: their mbarriers fit in 16 bytes
-    static constexpr int kGMax = kBF16 ? 5 : 10;  // groups per thread held in registers
 };
 
 template <bool kBF16>
@@ -81,12 +90,12 @@ __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
     return d;
 }
 
-// One CTA's exchange slot, double-buffered by row parity: a CTA writes row it+1's
-// values only after the cluster barrier of row it+1, which every CTA reaches
-// only after its reads of row it-1's values, so parity it+1 is free.
+// One CTA's exchange slot, double-buffered by row parity: a CTA writes row it+2's
+// values only after a cluster barrier that every CTA reaches after its reads of
+// row it's values.
 struct Slot {
-    float4 ms[2];           // slice max and sum of 2^((x - m) log2e) of d and t: (md, sd, mt, st)
-    float4 q[2];            // loss mode: partials (sum min(p_d, p_t), sum p_d sign(p_d - p_t), d[target] or -inf)
+    float4 ms[2];           // slice (max, sum of 2^((x - max) log2e)) of d and t: (md, sd, mt, st)
+    float4 q[2];            // loss mode: (sum of 2^(min) terms, sum p_d over d - t < L_d - L_t, over ties, d[target] or -inf)
     float p[2];             // CTA partial of sum min(p_d, p_t)
     float pad[2];
 };
@@ -96,6 +105,8 @@ struct Slot {
 //   bce = softplus(s) - c* s, row = omega (a_ce ce + a_l1 l1 + a_conf bce),
 //   dL/dd_v = omega (a_ce (p_d(v) - [v = target]) + a_l1 / 2 p_d(v) (sgn_v - sum_u p_d(u) sgn_u)),
 //   dL/ds = omega a_conf (sigmoid(s) - c*), sgn_v = sign(p_d(v) - p_t(v)).
+// sum_u p_d(u) sgn_u = 1 - 2 P_lt - P_eq, with P_lt (P_eq) the p_d mass where
+// p_d < p_t (p_d = p_t): pass C's terms there are p_d itself.
 struct LossArgs {
     const int32_t* target;  // [rows]
     const float* s;         // [rows] confidence head logits
@@ -126,111 +137,132 @@ __device__ __forceinline__ void warp_lse(float& m, float& s) {
     }
 }
 
+// This thread's (max, sum of 2^((x - max) log2e)) over its groups of a slice.
+// e = 2^((x - m) log2e): the difference is formed first, so it is exactly 0 at the
+// max and <= 0 elsewhere, whatever the magnitude of x; a thread without a finite
+// logit keeps reference 0 so that its terms are 0.
+template <bool kBF16>
+__device__ __forceinline__ void thread_lse(const uint4* __restrict__ g, int ngroups, int tid, float& m_out,
+                                           float& s_out) {
+    constexpr int EPG = TVTraits<kBF16>::kEPG;
+    float mx = -INFINITY;
+    if constexpr (kBF16) {
+        uint32_t am = 0xFF80FF80u;                        // (-inf, -inf)
+#pragma unroll
+        for (int j = 0; j < kGMax; ++j) {
+            const int gi = tid + j * kThreads;
+            if (gi < ngroups) {
+                const uint4 v = g[gi];
+                am = bmax2(am, bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w)));
+            }
+        }
+        mx = fmaxf(bf16lo(am), bf16hi(am));
+    } else {
+#pragma unroll
+        for (int j = 0; j < kGMax; ++j) {
+            const int gi = tid + j * kThreads;
+            if (gi < ngroups) {
+                const uint4 v = g[gi];
+                mx = fmaxf(mx, fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                                     fmaxf(__uint_as_float(v.z), __uint_as_float(v.w))));
+            }
+        }
+    }
+    const float m = (mx > -INFINITY) ? mx : 0.f;
+    const unsigned long long L2E = pk(kLog2e, kLog2e), nm = pk(-m, -m);
+    unsigned long long acc = pk(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < kGMax; ++j) {
+        const int gi = tid + j * kThreads;
+        if (gi < ngroups) {
+            float a[EPG];
+            unpack<kBF16>(g[gi], a);                      // second read of the slice from shared memory
+#pragma unroll
+            for (int e = 0; e < EPG; e += 2) {
+                const float2 y = upk(mul2(add2(pk(a[e], a[e + 1]), nm), L2E));
+                acc = add2(acc, pk(fast_exp2(y.x), fast_exp2(y.y)));
+            }
+        }
+    }
+    m_out = m;
+    s_out = upk(acc).x + upk(acc).y;
+}
+
 template <bool kBF16, bool kLoss>
 __global__ void __launch_bounds__(kThreads, 1)
 tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* __restrict__ c_star,
           int64_t rows, int V, int slice, StatusBlock* status, LossArgs la) {
     using Tr = TVTraits<kBF16>;
-    constexpr int EPG = Tr::kEPG, ESZ = Tr::kESZ, STAGES = Tr::kStages, GMAX = Tr::kGMax;
+    constexpr int EPG = Tr::kEPG, ESZ = Tr::kESZ;
     extern __shared__ __align__(128) uint8_t smem[];
     cg::cluster_group cluster = cg::this_cluster();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cs = static_cast<int>(cluster.num_blocks());
     const uint32_t rank = cluster.block_rank();
-    const int64_t cid = blockIdx.x / kCS;
-    const int64_t ncl = gridDim.x / kCS;
+    const int64_t cid = blockIdx.x / cs;
+    const int64_t ncl = gridDim.x / cs;
     const int lo = static_cast<int>(rank) * slice;
     const int len = max(0, min(V, lo + slice) - lo);
     const uint32_t bytes = static_cast<uint32_t>(len) * ESZ;
     const int ngroups = len / EPG;
-    const size_t stage_bytes = static_cast<size_t>(slice) * ESZ;
+    const size_t slot_bytes = static_cast<size_t>(slice) * ESZ;
+    const int64_t my_rows = (cid < rows) ? (rows - 1 - cid) / ncl + 1 : 0;
+    const int64_t Q = 2 * my_rows;                        // slices this CTA streams: d_0, t_0, d_1, ...
 
-    // shared memory: data stages (each a multiple of 16 bytes) | mbarriers (16 B) | pad |
-    // red (16-byte aligned float4 per warp) | slot
+    // shared memory: slots (each a multiple of 16 bytes) | mbarriers (32 B) |
+    // red_ab, red_c (16-byte aligned float4 per warp) | exchange slot
     uint8_t* buf = smem;
-    const size_t data_bytes = static_cast<size_t>(STAGES) * 2 * stage_bytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + data_bytes);
-    float4* red = reinterpret_cast<float4*>(smem + data_bytes + 32);   // (md, sd, mt, st) / partials
-    Slot* slot = reinterpret_cast<Slot*>(red + kWarps);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSlots * slot_bytes);
+    float4* red_ab = reinterpret_cast<float4*>(smem + kSlots * slot_bytes + 32);   // (md, sd, mt, st) per warp
+    float4* red_c = red_ab + kWarps;                                               // pass C partials per warp
+    Slot* slot = reinterpret_cast<Slot*>(red_c + kWarps);
 
     if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+        for (int s = 0; s < kSlots; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
     }
     __syncthreads();
     const uint64_t pol = policy_evict_first();
-    int pend_it[STAGES];   // iteration whose copy is in flight on stage s, or -1
-#pragma unroll
-    for (int s = 0; s < STAGES; ++s) pend_it[s] = -1;
-    auto issue = [&](int64_t row, int s) {
-        mbar_arrive_expect_tx(&bars[s], 2 * bytes);
+    // slice q: tensor q & 1 (d, t) of this cluster's row q >> 1, in slot q % kSlots
+    auto issue = [&](int64_t q) {
+        const int s = static_cast<int>(q % kSlots);
+        const int64_t row = cid + (q >> 1) * ncl;
+        mbar_arrive_expect_tx(&bars[s], bytes);
         if (bytes) {
-            const size_t off = (static_cast<size_t>(row) * V + lo) * ESZ;
-            bulk_g2s(buf + (2 * s) * stage_bytes, d + off, bytes, &bars[s], pol);
-            bulk_g2s(buf + (2 * s + 1) * stage_bytes, t + off, bytes, &bars[s], pol);
+            const uint8_t* src = (q & 1) ? t : d;
+            bulk_g2s(buf + s * slot_bytes, src + (static_cast<size_t>(row) * V + lo) * ESZ, bytes, &bars[s], pol);
         }
     };
-#pragma unroll
-    for (int s = 0; s < STAGES; ++s) {
-        const int64_t row = cid + s * ncl;
-        if (row < rows) {
-            if (tid == 0) issue(row, s);
-            pend_it[s] = s;
-        }
-    }
+    int64_t q_issued = Q < kSlots ? Q : kSlots;           // slices issued so far (same value in every thread)
+    int64_t q_landed = 0;                                 // slices waited for
+    if (tid == 0)
+        for (int64_t q = 0; q < q_issued; ++q) issue(q);
 
     bool failed = false;
-    int it = 0;
-    int64_t prev_row = -1;                                // row whose partials wait in the slots
-    float cl_sum = 0.f;                                   // loss mode: this cluster's row totals, in row order
-    for (int64_t row = cid; row < rows; row += ncl, ++it) {
-        const int s = it % STAGES;
-        const uint32_t par = static_cast<uint32_t>(it / STAGES) & 1u;
+    auto wait_slice = [&](int64_t q) {
         bool bad = false;
         if (!failed) {
-            bad = !mbar_wait(&bars[s], par);
-            if (!bad) pend_it[s] = -1;
+            bad = !mbar_wait(&bars[q % kSlots], static_cast<uint32_t>(q / kSlots) & 1u);
+            if (!bad) q_landed = q + 1;
         }
         if (__syncthreads_or(bad)) {
             if (!failed && tid == 0) set_status(status, DSPARK_ERR_TIMEOUT, 1);
             failed = true;
         }
-        const uint4* dg = reinterpret_cast<const uint4*>(buf + (2 * s) * stage_bytes);
-        const uint4* tg = reinterpret_cast<const uint4*>(buf + (2 * s + 1) * stage_bytes);
+    };
 
-        // A: this thread's maxima (bf16: packed, exact)
-        float mxd = -INFINITY, mxt = -INFINITY;
-        if constexpr (kBF16) {
-            uint32_t ad = 0xFF80FF80u, at = 0xFF80FF80u;  // (-inf, -inf)
-#pragma unroll
-            for (int gi = 0; gi < GMAX; ++gi) {
-                const int g = tid + gi * kThreads;
-                if (!failed && g < ngroups) {
-                    const uint4 a = dg[g], b = tg[g];
-                    ad = bmax2(bmax2(ad, a.x), bmax2(a.y, bmax2(a.z, a.w)));
-                    at = bmax2(bmax2(at, b.x), bmax2(b.y, bmax2(b.z, b.w)));
-                }
-            }
-            mxd = fmaxf(bf16lo(ad), bf16hi(ad));
-            mxt = fmaxf(bf16lo(at), bf16hi(at));
-        } else {
-#pragma unroll
-            for (int gi = 0; gi < GMAX; ++gi) {
-                const int g = tid + gi * kThreads;
-                if (!failed && g < ngroups) {
-                    float a[EPG], b[EPG];
-                    unpack<kBF16>(dg[g], a);
-                    unpack<kBF16>(tg[g], b);
-#pragma unroll
-                    for (int e = 0; e < EPG; ++e) { mxd = fmaxf(mxd, a[e]); mxt = fmaxf(mxt, b[e]); }
-                }
-            }
-        }
-        // e = 2^((x - m) log2e): the difference is formed first, so it is exactly 0 at
-        // the max and <= 0 elsewhere, whatever the magnitude of x (a multiply-add of
-        // x log2e - m log2e would leave the product's rounding error in the exponent);
-        // a thread without a finite logit keeps reference 0 so that its terms are 0
-        const float md = (mxd > -INFINITY) ? mxd : 0.f;
-        const float mt = (mxt > -INFINITY) ? mxt : 0.f;
+    float cl_sum = 0.f;                                   // loss mode: this cluster's row totals, in row order
+    int64_t prev_row = -1;                                // row whose partials wait in the slots
+    int it = 0;
+    for (int64_t row = cid; row < rows; row += ncl, ++it) {
+        const int64_t qd = 2 * static_cast<int64_t>(it), qt = qd + 1;
+        const uint4* dg = reinterpret_cast<const uint4*>(buf + (qd % kSlots) * slot_bytes);
+        const uint4* tg = reinterpret_cast<const uint4*>(buf + (qt % kSlots) * slot_bytes);
+
+        // AB: the slices' (max, sum) of d, then of t
+        wait_slice(qd);
+        float md = 0.f, sd = 0.f, mt = 0.f, st = 0.f;
+        if (!failed) thread_lse<kBF16>(dg, ngroups, tid, md, sd);
         // loss mode: the target's logit, from the CTA whose slice holds it
         int tgt = -1;
         float dtgt = -INFINITY;
@@ -241,60 +273,18 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
                 tgt = -1;
             }
             if (tid == 0 && !failed && tgt >= lo && tgt < lo + len) {
-                const uint8_t* src = buf + (2 * s) * stage_bytes + static_cast<size_t>(tgt - lo) * ESZ;
+                const uint8_t* src = reinterpret_cast<const uint8_t*>(dg) + static_cast<size_t>(tgt - lo) * ESZ;
                 dtgt = kBF16 ? bf16lo(*reinterpret_cast<const uint16_t*>(src)) : *reinterpret_cast<const float*>(src);
             }
         }
-
-        // B: e in registers (packed pairs), the thread's sums
-        unsigned long long ed[GMAX * EPG / 2], et[GMAX * EPG / 2];
-        const unsigned long long L2E = pk(kLog2e, kLog2e);
-        const unsigned long long nmd = pk(-md, -md), nmt = pk(-mt, -mt);
-        unsigned long long sdp = pk(0.f, 0.f), stp = pk(0.f, 0.f);
-#pragma unroll
-        for (int gi = 0; gi < GMAX; ++gi) {
-            const int g = tid + gi * kThreads;
-            if (!failed && g < ngroups) {
-                float a[EPG], b[EPG];
-                unpack<kBF16>(dg[g], a);
-                unpack<kBF16>(tg[g], b);
-#pragma unroll
-                for (int e = 0; e < EPG; e += 2) {
-                    const float2 ya = upk(mul2(add2(pk(a[e], a[e + 1]), nmd), L2E));
-                    const float2 yb = upk(mul2(add2(pk(b[e], b[e + 1]), nmt), L2E));
-                    const unsigned long long va = pk(fast_exp2(ya.x), fast_exp2(ya.y));
-                    const unsigned long long vb = pk(fast_exp2(yb.x), fast_exp2(yb.y));
-                    ed[(gi * EPG + e) / 2] = va;
-                    et[(gi * EPG + e) / 2] = vb;
-                    sdp = add2(sdp, va);
-                    stp = add2(stp, vb);
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < EPG; e += 2) { ed[(gi * EPG + e) / 2] = 0ull; et[(gi * EPG + e) / 2] = 0ull; }
-            }
-        }
-        float tmd = md, tsd = upk(sdp).x + upk(sdp).y;
-        float tmt = mt, tst = upk(stp).x + upk(stp).y;
-        float wmd = tmd, wsd = tsd, wmt = tmt, wst = tst;
-        warp_lse(wmd, wsd);
-        warp_lse(wmt, wst);
-        if (lane == 0) red[warp] = make_float4(wmd, wsd, wmt, wst);
-        __syncthreads();                                  // every thread is past its reads of this stage
-
-        // refill this stage with the row STAGES iterations ahead
-        {
-            const int64_t nrow = row + STAGES * ncl;
-            if (!failed && nrow < rows) {
-                if (tid == 0) {
-                    fence_proxy_async_smem();
-                    issue(nrow, s);
-                }
-                pend_it[s] = it + STAGES;
-            }
-        }
+        warp_lse(md, sd);
+        wait_slice(qt);
+        if (!failed) thread_lse<kBF16>(tg, ngroups, tid, mt, st);
+        warp_lse(mt, st);
+        if (lane == 0) red_ab[warp] = make_float4(md, sd, mt, st);
+        __syncthreads();
         if (warp == 0) {
-            float4 r = (lane < kWarps) ? red[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 r = red_ab[lane];
             float a = r.x, b = r.y, c = r.z, e = r.w;
             warp_lse(a, b);
             warp_lse(c, e);
@@ -304,13 +294,13 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
 
         // the previous row's c*: rank 0 sums its CTAs' partials in rank order
         if (!kLoss && rank == 0 && warp == 1 && prev_row >= 0) {
-            const float pr = (lane < kCS) ? cluster.map_shared_rank(slot, lane)->p[(it - 1) & 1] : 0.f;
+            const float pr = (lane < cs) ? cluster.map_shared_rank(slot, lane)->p[(it - 1) & 1] : 0.f;
             const float c = warp_sum(pr);
             if (lane == 0 && !failed) c_star[prev_row] = c;
         }
-        // every warp combines the kCS slots itself: lane r reads CTA r's slot
+        // every warp combines the cs slots itself: lane r reads CTA r's slot
         float rmd = -INFINITY, rsd = 0.f, rmt = -INFINITY, rst = 0.f;
-        if (lane < kCS) {
+        if (lane < cs) {
             const float4 rs = cluster.map_shared_rank(slot, lane)->ms[it & 1];
             rsd = rs.y; rst = rs.w;
             rmd = rsd > 0.f ? rs.x : -INFINITY;            // empty slices do not set the reference
@@ -319,68 +309,100 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
         const float Md = warp_max(rmd), Mt = warp_max(rmt);
         const float Sd = warp_sum(rsd > 0.f ? rsd * exp2f((rmd - Md) * kLog2e) : 0.f);
         const float St = warp_sum(rst > 0.f ? rst * exp2f((rmt - Mt) * kLog2e) : 0.f);
-        // p = e 2^((m_thread - M) log2e) / S
-        const float alpha = (tsd > 0.f) ? exp2f((tmd - Md) * kLog2e - log2f(Sd)) : 0.f;
-        const float beta = (tst > 0.f) ? exp2f((tmt - Mt) * kLog2e - log2f(St)) : 0.f;
+        const float lsd = log2f(Sd) * kLn2, lst = log2f(St) * kLn2;
+        const float Ld = Md + lsd, Lt = Mt + lst;         // natural-log logsumexp
+        // p_d < p_t  <=>  d - t < L_d - L_t: the difference of the two logsumexps formed
+        // from their parts, so that it keeps the precision of a small number
+        const float dL = (Md - Mt) + (lsd - lst);
 
-        // C: sum of min(p_d, p_t) over this thread's elements, from registers
-        const unsigned long long al = pk(alpha, alpha), be = pk(beta, beta);
-        unsigned long long pp = pk(0.f, 0.f), sp = pk(0.f, 0.f);
+        // C: sum of 2^(min(d - L_d, t - L_t) log2e); loss mode also the p_d mass where
+        // d - L_d < t - L_t and where they tie
+        const unsigned long long L2E = pk(kLog2e, kLog2e), nLd = pk(-Ld, -Ld), nLt = pk(-Lt, -Lt);
+        unsigned long long pc = pk(0.f, 0.f);
+        float plt = 0.f, peq = 0.f;
+        if (!failed) {
 #pragma unroll
-        for (int i = 0; i < GMAX * EPG / 2; ++i) {
-            const float2 x = upk(mul2(ed[i], al)), y = upk(mul2(et[i], be));
-            pp = add2(pp, pk(fminf(x.x, y.x), fminf(x.y, y.y)));
-            if constexpr (kLoss) {
-                const float s0 = x.x > y.x ? x.x : (x.x < y.x ? -x.x : 0.f);   // p_d sign(p_d - p_t)
-                const float s1 = x.y > y.y ? x.y : (x.y < y.y ? -x.y : 0.f);
-                sp = add2(sp, pk(s0, s1));
+            for (int j = 0; j < kGMax; ++j) {
+                const int gi = tid + j * kThreads;
+                if (gi < ngroups) {
+                    float a[EPG], b[EPG];
+                    unpack<kBF16>(dg[gi], a);
+                    unpack<kBF16>(tg[gi], b);
+#pragma unroll
+                    for (int e = 0; e < EPG; e += 2) {
+                        const float2 x = upk(add2(pk(a[e], a[e + 1]), nLd));
+                        const float2 y = upk(add2(pk(b[e], b[e + 1]), nLt));
+                        const float2 z = upk(mul2(pk(fminf(x.x, y.x), fminf(x.y, y.y)), L2E));
+                        const float e0 = fast_exp2(z.x), e1 = fast_exp2(z.y);
+                        pc = add2(pc, pk(e0, e1));
+                        if constexpr (kLoss) {
+                            const float r0 = a[e] - b[e], r1 = a[e + 1] - b[e + 1];
+                            plt += (r0 < dL ? e0 : 0.f) + (r1 < dL ? e1 : 0.f);
+                            peq += (r0 == dL ? e0 : 0.f) + (r1 == dL ? e1 : 0.f);
+                        }
+                    }
+                }
             }
         }
-        float p = warp_sum(upk(pp).x + upk(pp).y);
-        float sgs = kLoss ? warp_sum(upk(sp).x + upk(sp).y) : 0.f;
-        __syncthreads();                                  // red is free again
-        if (lane == 0) { red[warp].x = p; red[warp].y = sgs; }
-        __syncthreads();
-        if (warp == 0) {
-            float q = (lane < kWarps) ? red[lane].x : 0.f;
-            q = warp_sum(q);
-            if constexpr (kLoss) {
-                float q2 = (lane < kWarps) ? red[lane].y : 0.f;
-                q2 = warp_sum(q2);
-                if (lane == 0) slot->q[it & 1] = make_float4(q, q2, dtgt, 0.f);
-            } else {
+        const float p = warp_sum(upk(pc).x + upk(pc).y);
+        if constexpr (kLoss) {
+            plt = warp_sum(plt);
+            peq = warp_sum(peq);
+        }
+        if (lane == 0) red_c[warp] = make_float4(p, plt, peq, 0.f);
+        __syncthreads();                                  // every thread is past pass C
+        if constexpr (!kLoss) {
+            // both slots of this row are free: refill them two slices ahead
+            if (!failed) {
+                const int64_t q_next = qd + kSlots + 2 < Q ? qd + kSlots + 2 : Q;
+                if (tid == 0 && q_issued < q_next) {
+                    fence_proxy_async_smem();
+                    for (int64_t q = q_issued; q < q_next; ++q) issue(q);
+                }
+                if (q_issued < q_next) q_issued = q_next;
+            }
+            if (warp == 0) {
+                const float q = warp_sum(red_c[lane].x);
                 if (lane == 0) slot->p[it & 1] = q;
             }
-        }
-        if constexpr (kLoss) {
-            cluster.sync();                               // this row's partials, every CTA
-            float c0 = 0.f, c1 = 0.f, c2 = -INFINITY;
-            if (lane < kCS) {
-                const float4 rq = cluster.map_shared_rank(slot, lane)->q[it & 1];
-                c0 = rq.x; c1 = rq.y; c2 = rq.z;
+        } else {
+            if (warp == 0) {
+                const float4 r = red_c[lane];
+                const float q0 = warp_sum(r.x), q1 = warp_sum(r.y), q2 = warp_sum(r.z);
+                if (lane == 0) slot->q[it & 1] = make_float4(q0, q1, q2, dtgt);
             }
-            // rank order within each reduction: every warp gets the same sums
-            const float cstar = warp_sum(c0), sbar = warp_sum(c1), dt_t = warp_max(c2);
-            // D: dL/dd from registers
+            cluster.sync();                               // this row's partials, every CTA
+            float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = -INFINITY;
+            if (lane < cs) {
+                const float4 rq = cluster.map_shared_rank(slot, lane)->q[it & 1];
+                c0 = rq.x; c1 = rq.y; c2 = rq.z; c3 = rq.w;
+            }
+            // the same sums, in rank order, in every warp
+            const float cstar = warp_sum(c0), p_lt = warp_sum(c1), p_eq = warp_sum(c2), dt_t = warp_max(c3);
+            const float sbar = 1.f - 2.f * p_lt - p_eq;   // sum_u p_d(u) sign(p_d(u) - p_t(u))
             const float om = la.omega[row];
+            // D: dL/dd from shared memory
             if (la.grad != nullptr && !failed) {
                 const float ka = om * la.a_ce, kl = 0.5f * om * la.a_l1;
 #pragma unroll
-                for (int gi = 0; gi < GMAX; ++gi) {
-                    const int g = tid + gi * kThreads;
-                    if (g < ngroups) {
-                        float gv[EPG];
+                for (int j = 0; j < kGMax; ++j) {
+                    const int gi = tid + j * kThreads;
+                    if (gi < ngroups) {
+                        float a[EPG], b[EPG], gv[EPG];
+                        unpack<kBF16>(dg[gi], a);
+                        unpack<kBF16>(tg[gi], b);
 #pragma unroll
                         for (int e = 0; e < EPG; e += 2) {
-                            const float2 x = upk(mul2(ed[(gi * EPG + e) / 2], al));
-                            const float2 y = upk(mul2(et[(gi * EPG + e) / 2], be));
-                            const float sg0 = x.x > y.x ? 1.f : (x.x < y.x ? -1.f : 0.f);
-                            const float sg1 = x.y > y.y ? 1.f : (x.y < y.y ? -1.f : 0.f);
-                            const int v = lo + g * EPG + e;
-                            gv[e] = ka * (x.x - (v == tgt ? 1.f : 0.f)) + kl * x.x * (sg0 - sbar);
-                            gv[e + 1] = ka * (x.y - (v + 1 == tgt ? 1.f : 0.f)) + kl * x.y * (sg1 - sbar);
+                            const float2 z = upk(mul2(add2(pk(a[e], a[e + 1]), nLd), L2E));
+                            const float p0 = fast_exp2(z.x), p1 = fast_exp2(z.y);
+                            const float r0 = a[e] - b[e], r1 = a[e + 1] - b[e + 1];
+                            const float sg0 = r0 > dL ? 1.f : (r0 < dL ? -1.f : 0.f);
+                            const float sg1 = r1 > dL ? 1.f : (r1 < dL ? -1.f : 0.f);
+                            const int v = lo + gi * EPG + e;
+                            gv[e] = ka * (p0 - (v == tgt ? 1.f : 0.f)) + kl * p0 * (sg0 - sbar);
+                            gv[e + 1] = ka * (p1 - (v + 1 == tgt ? 1.f : 0.f)) + kl * p1 * (sg1 - sbar);
                         }
-                        uint8_t* dst = static_cast<uint8_t*>(la.grad) + (static_cast<size_t>(row) * V + lo + g * EPG) * ESZ;
+                        uint8_t* dst = static_cast<uint8_t*>(la.grad) + (static_cast<size_t>(row) * V + lo + gi * EPG) * ESZ;
                         if constexpr (kBF16) {
                             uint4 o;
                             o.x = pack_bf16(gv[0], gv[1]); o.y = pack_bf16(gv[2], gv[3]);
@@ -392,16 +414,24 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
                     }
                 }
             }
-            if (rank == 0 && warp == 0 && lane == 0 && !failed) {
+            if (rank == 0 && tid == 0 && !failed) {
                 const float sv = la.s[row];
-                const float ce = (Md + log2f(Sd) * kLn2) - dt_t;   // natural-log logsumexp minus d[target]
-                const float sp_ = fmaxf(sv, 0.f) + log1pf(expf(-fabsf(sv)));
-                const float bce = sp_ - cstar * sv;
+                const float ce = Ld - dt_t;
+                const float sp = fmaxf(sv, 0.f) + log1pf(expf(-fabsf(sv)));   // softplus
+                const float bce = sp - cstar * sv;
                 const float tot = om * (la.a_ce * ce + la.a_l1 * (1.f - cstar) + la.a_conf * bce);
                 reinterpret_cast<float4*>(la.row_out)[row] = make_float4(ce, cstar, bce, tot);
                 if (la.grad_s != nullptr) la.grad_s[row] = om * la.a_conf * (1.f / (1.f + expf(-sv)) - cstar);
                 cl_sum += tot;
-                if (c_star != nullptr) c_star[row] = cstar;
+            }
+            __syncthreads();                              // every thread is past pass D
+            if (!failed) {
+                const int64_t q_next = qd + kSlots + 2 < Q ? qd + kSlots + 2 : Q;
+                if (tid == 0 && q_issued < q_next) {
+                    fence_proxy_async_smem();
+                    for (int64_t q = q_issued; q < q_next; ++q) issue(q);
+                }
+                if (q_issued < q_next) q_issued = q_next;
             }
         }
         prev_row = row;
@@ -409,7 +439,7 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
     // the last row's c*, and no CTA leaves while a peer may still read its shared memory
     cluster.sync();
     if (!kLoss && rank == 0 && warp == 1 && prev_row >= 0) {
-        const float pr = (lane < kCS) ? cluster.map_shared_rank(slot, lane)->p[(it - 1) & 1] : 0.f;
+        const float pr = (lane < cs) ? cluster.map_shared_rank(slot, lane)->p[(it - 1) & 1] : 0.f;
         const float c = warp_sum(pr);
         if (lane == 0 && !failed) c_star[prev_row] = c;
     }
@@ -429,21 +459,32 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
         }
     }
     cluster.sync();
-    // after a timeout, give any copy still in flight a bounded chance to land
-    if (failed && tid == 0) {
-        for (int s = 0; s < STAGES; ++s)
-            if (pend_it[s] >= 0) mbar_wait(&bars[s], static_cast<uint32_t>(pend_it[s] / STAGES) & 1u);
-    }
+    // after a timeout, give every copy still in flight a bounded chance to land
+    if (failed && tid == 0)
+        for (int64_t q = q_landed; q < q_issued; ++q)
+            mbar_wait(&bars[q % kSlots], static_cast<uint32_t>(q / kSlots) & 1u);
 }
 
+// Shared memory beyond the slots: mbarriers, two float4 per warp, the exchange slot, slack.
+constexpr size_t kTvExtraSmem = 32 + 2 * kWarps * sizeof(float4) + sizeof(Slot) + 128;
+
+// The cluster size: the smallest of 1, 2, 4, 8, 16 whose slices fit three slots in
+// shared memory.  Returns 0 if none does.
 template <bool kBF16>
-size_t tv_smem_bytes(int slice) {
+int tv_cluster_size(int V, int* slice_out) {
     using Tr = TVTraits<kBF16>;
-    return static_cast<size_t>(Tr::kStages) * 2 * slice * Tr::kESZ + 32 + kWarps * sizeof(float4) +
-           sizeof(Slot) + 128;
+    for (int cs = 1; cs <= kMaxCS; cs *= 2) {
+        const int per = (V + cs - 1) / cs;
+        const int slice = (per + Tr::kEPG - 1) / Tr::kEPG * Tr::kEPG;
+        if (kSlots * static_cast<size_t>(slice) * Tr::kESZ + kTvExtraSmem <= kSmemCap) {
+            *slice_out = slice;
+            return cs;
+        }
+    }
+    return 0;
 }
 
-// Clusters of the loss launch are at most this many (their partial sums live in
+// Clusters of a loss launch are at most this many (their partial sums live in
 // the workspace).
 constexpr int kMaxLossClusters = 1024;
 
@@ -451,23 +492,26 @@ template <bool kBF16, bool kLoss>
 dspark_status_t launch_tv(int64_t rows, int V, const void* d, const void* t, float* c_star,
                           StatusBlock* status, const LossArgs& la, cudaStream_t stream) {
     using Tr = TVTraits<kBF16>;
-    const int per = (V + kCS - 1) / kCS;
-    const int slice = (per + Tr::kEPG - 1) / Tr::kEPG * Tr::kEPG;
-    if (slice / Tr::kEPG > Tr::kGMax * kThreads) return DSPARK_ERR_UNSUPPORTED;
-    const size_t smem = tv_smem_bytes<kBF16>(slice);
-    if (smem > 227 * 1024) return DSPARK_ERR_UNSUPPORTED;
+    int slice = 0;
+    const int cs = tv_cluster_size<kBF16>(V, &slice);
+    if (cs == 0) return DSPARK_ERR_UNSUPPORTED;
+    if (slice / Tr::kEPG > kGMax * kThreads) return DSPARK_ERR_UNSUPPORTED;
+    const size_t smem = kSlots * static_cast<size_t>(slice) * Tr::kESZ + kTvExtraSmem;
     const int dev = current_device();
     auto* kern = tv_kernel<kBF16, kLoss>;
     static OncePerDevice once;
     if (once.run(dev, [kern] {
-            return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(kSmemCap));
+            if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            return e;
         }) != cudaSuccess)
         return DSPARK_ERR_CUDA;
 
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCS;
+    attr[0].val.clusterDim.x = cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.blockDim = dim3(kThreads);
@@ -475,16 +519,16 @@ dspark_status_t launch_tv(int64_t rows, int V, const void* d, const void* t, flo
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cfg.gridDim = dim3(kCS * 256);
+    cfg.gridDim = dim3(cs * 256);
     int max_clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess || max_clusters < 1) {
         cudaGetLastError();
-        max_clusters = sm_count(dev) / kCS;
+        max_clusters = sm_count(dev) / cs;
         if (max_clusters < 1) max_clusters = 1;
     }
     if (max_clusters > kMaxLossClusters) max_clusters = kMaxLossClusters;
     const int64_t ncl = rows < max_clusters ? rows : max_clusters;
-    cfg.gridDim = dim3(static_cast<unsigned>(ncl * kCS));
+    cfg.gridDim = dim3(static_cast<unsigned>(ncl * cs));
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t*>(d),
                                              static_cast<const uint8_t*>(t), c_star, rows, V, slice,
                                              status, la);
