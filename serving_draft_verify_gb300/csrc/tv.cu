@@ -4,14 +4,14 @@
 // and dspark_training_loss (section 7.2, `compute_dspark_loss`), the same pass
 // extended to the joint loss and its gradient.
 //
-// One HBM pass per row.  A thread-block cluster of cs CTAs (the smallest of 1, 2,
-// 4, 8, 16 whose slices fit; 4 for bf16 rows of the Qwen3 vocabulary) owns one
-// row at a time; each CTA bulk-copies its 1/cs slice of d and t into shared
-// memory.  Slices stream through three slots in the order d_0, t_0, d_1, t_1, ...,
-// so row i+1's d lands while row i is reduced:
+// One HBM pass per row.  A thread-block cluster of cs CTAs of 512 threads (cs the
+// smallest of 1, 2, 4, 8, 16 whose slices fit; 4 for bf16 rows of the Qwen3
+// vocabulary) owns one row at a time; each CTA bulk-copies its 1/cs slice of d
+// and t into shared memory.  Slices stream through three slots in the order d_0,
+// t_0, d_1, t_1, ..., so row i+1's d lands while row i is reduced:
 //   AB. per tensor: each thread's max (packed bf16 max) and sum of
-//       2^((x - m) log2e) over its elements (held in registers between the two);
-//       merged per warp, per CTA;
+//       2^((x - m) log2e) over its elements (two reads of shared memory); merged
+//       per warp (max, then rescaled sum), per CTA;
 //   -- cluster barrier: the CTAs' (m, s) through distributed shared memory (and
 //      the previous row's partials, which rank 0 sums into c*) --
 //   C.  sum of 2^(min(d - L_d, t - L_t) log2e) from shared memory;
@@ -31,10 +31,10 @@ namespace dspark {
 namespace {
 
 constexpr int kMaxCS = 16;      // CTAs per cluster at most (one row per cluster)
-constexpr int kThreads = 1024;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kSlots = 3;       // slice slots: d_i, t_i and d_{i+1} resident at once
-constexpr int kGMax = 5;        // 16-byte groups per thread and slice (a slot holds at most 5 x 1024 x 16 B)
+constexpr int kGMax = 10;       // 16-byte groups per thread and slice (a slot holds at most 10 x 512 x 16 B)
 constexpr size_t kSmemCap = 227 * 1024;
 
 template <bool kBF16>
@@ -120,21 +120,20 @@ struct LossArgs {
     float* loss;            // [1] sum of row totals
 };
 
-// (m, s) with s a sum of 2^((x - m) log2e): merge across a warp.
+// (m, s) with s a sum of 2^((x - m) log2e): merge across a warp (the warp's max of
+// the m that carry mass, then the rescaled sum).
 __device__ __forceinline__ void warp_lse(float& m, float& s) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float om = __shfl_xor_sync(0xffffffffu, m, o);
-        const float os = __shfl_xor_sync(0xffffffffu, s, o);
-        if (os > 0.f) {
-            if (s <= 0.f) { m = om; s = os; }
-            else {
-                const float M = fmaxf(m, om);
-                s = s * fast_exp2((m - M) * kLog2e) + os * fast_exp2((om - M) * kLog2e);
-                m = M;
-            }
-        }
-    }
+    const float M = warp_max(s > 0.f ? m : -INFINITY);
+    const float r = s > 0.f ? s * fast_exp2((m - M) * kLog2e) : 0.f;
+    s = warp_sum(r);
+    m = M > -INFINITY ? M : 0.f;
+}
+
+// log2 on the special-function unit (lg2.approx.ftz: absolute error about 2^-22).
+__device__ __forceinline__ float fast_log2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // This thread's (max, sum of 2^((x - max) log2e)) over its groups of a slice.
@@ -284,7 +283,7 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
         if (lane == 0) red_ab[warp] = make_float4(md, sd, mt, st);
         __syncthreads();
         if (warp == 0) {
-            const float4 r = red_ab[lane];
+            const float4 r = lane < kWarps ? red_ab[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
             float a = r.x, b = r.y, c = r.z, e = r.w;
             warp_lse(a, b);
             warp_lse(c, e);
@@ -307,9 +306,9 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
             rmt = rst > 0.f ? rs.z : -INFINITY;
         }
         const float Md = warp_max(rmd), Mt = warp_max(rmt);
-        const float Sd = warp_sum(rsd > 0.f ? rsd * exp2f((rmd - Md) * kLog2e) : 0.f);
-        const float St = warp_sum(rst > 0.f ? rst * exp2f((rmt - Mt) * kLog2e) : 0.f);
-        const float lsd = log2f(Sd) * kLn2, lst = log2f(St) * kLn2;
+        const float Sd = warp_sum(rsd > 0.f ? rsd * fast_exp2((rmd - Md) * kLog2e) : 0.f);
+        const float St = warp_sum(rst > 0.f ? rst * fast_exp2((rmt - Mt) * kLog2e) : 0.f);
+        const float lsd = fast_log2(Sd) * kLn2, lst = fast_log2(St) * kLn2;
         const float Ld = Md + lsd, Lt = Mt + lst;         // natural-log logsumexp
         // p_d < p_t  <=>  d - t < L_d - L_t: the difference of the two logsumexps formed
         // from their parts, so that it keeps the precision of a small number
@@ -362,12 +361,12 @@ tv_kernel(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* _
                 if (q_issued < q_next) q_issued = q_next;
             }
             if (warp == 0) {
-                const float q = warp_sum(red_c[lane].x);
+                const float q = warp_sum(lane < kWarps ? red_c[lane].x : 0.f);
                 if (lane == 0) slot->p[it & 1] = q;
             }
         } else {
             if (warp == 0) {
-                const float4 r = red_c[lane];
+                const float4 r = lane < kWarps ? red_c[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
                 const float q0 = warp_sum(r.x), q1 = warp_sum(r.y), q2 = warp_sum(r.z);
                 if (lane == 0) slot->q[it & 1] = make_float4(q0, q1, q2, dtgt);
             }
