@@ -133,3 +133,25 @@ def test_loss_l1_gradient_without_the_softmax_mean_is_caught(monkeypatch):
         return g, np.zeros(R)
     monkeypatch.setattr(L, "dspark_loss_grad", bad_grad)
     assert _fails(T_loss.test_grad_d_matches_central_differences)
+
+
+def test_rounds_sharing_one_key_is_caught(monkeypatch):
+    from oracle import rounds as R
+    import tests.test_oracle_rounds as T_rounds
+    monkeypatch.setattr(R, "round_seed", lambda seed, i: int(seed))
+    assert _fails(T_rounds.test_rounds_draw_with_their_own_keys)
+
+
+def test_rounds_dropping_the_verifier_token_is_caught(monkeypatch):
+    from oracle import rounds as R
+    import tests.test_oracle_rounds as T_rounds
+
+    def bad(x, n_accept, next_token):
+        x = np.asarray(x, np.int64)
+        out = np.full((x.shape[0], x.shape[1] + 1), -1, np.int64)
+        for b in range(x.shape[0]):
+            out[b, :int(n_accept[b])] = x[b, :int(n_accept[b])]
+        return out
+    monkeypatch.setattr(R, "emitted_tokens", bad)
+    assert _fails(T_rounds.test_anchor_is_the_last_emitted_token)
+    assert _fails(T_rounds.test_agreeing_target_accepts_every_scheduled_token)
