@@ -330,6 +330,30 @@ def run_gpu(args):
                                "achieved_gbs": lb / (l_ms * 1e-3) / 1e9,
                                "frac_of_peak": lb / (l_ms * 1e-3) / 1e9 / peak}
         del d_, t_, lout
+    # several rounds with the anchor carried (the last emitted token), one CUDA graph over
+    # a pool of 8 synthetic rounds of the same shape
+    multi = None
+    if not args.skip_rounds:
+        R, P = 32, 8
+        pool_ = wl.make_round_pool(cfg, P, device=dev)
+        anchor_ = pool_["x0"].clone()
+        ws_r = torch.empty(lib.dspark_decode_rounds_workspace_size(B, G, V, r), dtype=torch.uint8, device=dev)
+        rout = dict(tokens=torch.empty((R, B, G + 1), dtype=torch.int32, device=dev),
+                    n_emitted=torch.empty((R, B), dtype=torch.int32, device=dev),
+                    stats=torch.empty((R, 2), dtype=torch.float64, device=dev))
+
+        def rounds_call():
+            anchor_.copy_(pool_["x0"])
+            dsv.dspark_decode_rounds(pool_["U"], pool_["h"], pool_["t"], pool_["W1"], pool_["W2"], pool_["w"], 0.0,
+                                     pool_["sps"], anchor_, R, T, seed, out=rout, workspace=ws_r)
+        rounds_fn = graphed(rounds_call)
+        r_times, _ = timed(rounds_fn or rounds_call, 10, 3)
+        r_ms = sum(r_times) / len(r_times)
+        st_ = rout["stats"].cpu()
+        multi = {"rounds": R, "pool": P, "cuda_graph": rounds_fn is not None, "ms_per_round": r_ms / R,
+                 "emitted_tokens_per_s": float(rout["n_emitted"].sum().item()) / (r_ms * 1e-3),
+                 "E_tau": float(st_[:, 0].mean()), "realised_tau": float(st_[:, 1].mean())}
+        del pool_
     # draft: the cooperative engine launch; schedule: 1; verify: plan, rows, residual (+ final token)
     launches_per_step = 1 + 1 + 3
 
@@ -339,7 +363,7 @@ def run_gpu(args):
             "config": dict(workload_config(world), cuda_graph=use_graph),
             "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / peak, "roofline": roofline, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps, "clocks": clk,
-            "extra": {"greedy_round": greedy, "accept_rate_tv": tv,
+            "extra": {"greedy_round": greedy, "accept_rate_tv": tv, "multi_round": multi,
                       "accepted_per_request": float(nacc.mean()), "scheduled_rows": int((ell + 1).sum())}}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, T, seed)
@@ -481,6 +505,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--skip-tv", action="store_true")
+    ap.add_argument("--skip-rounds", action="store_true", help="skip the multi-round extra")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the round's calls directly, without a CUDA graph")
     ap.add_argument("--phase-traffic", type=float, default=None,

@@ -2,15 +2,16 @@
  * dspark.h -- C ABI of the DSpark draft / schedule / verify / accept-rate path
  * for one NVIDIA GB300 GPU (sm_103a).
  *
- * Four operations, each a hand-written CUDA kernel sequence:
+ * Six operations, each a hand-written CUDA kernel sequence:
  *   dspark_draft_block      semi-autoregressive draft block, confidence, survival
  *   dspark_schedule_prefix  hardware-aware prefix scheduler (Algorithm 1)
  *   dspark_verify           rejection-sampling verification + residual/bonus token
  *   dspark_accept_rate_tv   c* = 1 - 1/2 ||softmax(d) - softmax(t)||_1 per row
  *   dspark_training_loss    joint CE + L1 + BCE loss per row, and its gradient
+ *   dspark_decode_rounds    draft -> schedule -> verify rounds, anchor carried
  *
  * Sources (cited per call): the DeepSpec / DSpark walkthrough at
- * wangjunjian.com ("DSpark" post, sections 2.1, 3.2, 3.3, 8.2) and the
+ * wangjunjian.com ("DSpark" post, sections 2.1, 3.2, 3.3, 7.2, 8.1-8.3) and the
  * Qwen3.8-27B-DSpark model-card explainer at dpshk.com (AcceptRatePredictor,
  * config.json fields).
  *
@@ -206,6 +207,59 @@ dspark_status_t dspark_accept_rate_tv(int64_t rows, int V, dspark_dtype_t dt,
                                       const void* d, const void* t, float* c_star,
                                       void* workspace, size_t workspace_bytes,
                                       dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Several decoding rounds in a row (DeepSpec walkthrough sections 8.1 / 8.3,
+ * `generate_decoding_sample`: propose, verify, emit, continue from the new
+ * context), all enqueued on `stream` with no host synchronisation, so that a
+ * caller can capture them in one CUDA graph.  Round i (i = 0 .. rounds-1):
+ *   1. dspark_draft_block on pool slot p = i mod pool, x0 = anchor, seed + i;
+ *   2. dspark_schedule_prefix on its survivals a;
+ *   3. dspark_verify of the scheduled prefix against slot p's target rows;
+ *   4. emit x[b][0 .. n_accept-1] then next_token[b]; anchor[b] = next_token[b]
+ *      (the last token emitted is the next round's anchor).
+ * The synthetic slots stand in for the target model's next context; the
+ * carried state is the anchor.  Every round keys its draws with seed + i
+ * (64-bit wrap-around).
+ *
+ *   U [pool][B][gamma][V], h [pool][B][gamma][H], t_logits [pool][B][gamma+1][V],
+ *   W1/W2 [V][r], w [H + r] in `dt`; sps as for dspark_schedule_prefix.
+ *   anchor [B] int32: in, the first round's anchors; out, the last emitted tokens.
+ *   Outputs: tokens [rounds][B][gamma+1] int32 (emitted tokens, then -1);
+ *   n_emitted [rounds][B] int32 (n_accept + 1); stats [rounds][2] double:
+ *   E[tau] = sum_b (1 + sum_{j <= l_b} a[b][j-1]) / B, the expected emitted
+ *   tokens per request that the scheduler maximises, and the realised
+ *   sum_b n_emitted[b] / B.
+ *   trace (host pointer, may be NULL; any member may be NULL): per-round copies
+ *   of the draft outputs x, lse_d, logp_d, c, a [rounds][B][gamma] and of ell,
+ *   n_accept, next_token [rounds][B].
+ * Requirements are those of the three calls.  The workspace holds their
+ * workspaces and the round's intermediates; a sub-call's device error is copied
+ * to this workspace's status with detail 1000 * stage + the sub-call's detail
+ * (stage 1 draft, 2 schedule, 3 verify).  rounds == 0 launches nothing.
+ * ------------------------------------------------------------------------ */
+typedef struct dspark_round_trace {
+    int32_t* x;
+    float* lse_d;
+    float* logp_d;
+    float* c;
+    float* a;
+    int32_t* ell;
+    int32_t* n_accept;
+    int32_t* next_token;
+} dspark_round_trace_t;
+
+size_t dspark_decode_rounds_workspace_size(int B, int gamma, int V, int r);
+
+dspark_status_t dspark_decode_rounds(int rounds, int pool, int B, int gamma, int V, int H, int r,
+                                     dspark_dtype_t dt, const void* U, const void* h,
+                                     const void* t_logits, const void* W1, const void* W2,
+                                     const void* w, float bias, const double* sps, int32_t* anchor,
+                                     float temperature, uint64_t seed, int32_t* tokens,
+                                     int32_t* n_emitted, double* stats,
+                                     const dspark_round_trace_t* trace,
+                                     void* workspace, size_t workspace_bytes,
+                                     dspark_stream_t stream);
 
 /* ------------------------------------------------------------------------ *
  * Joint training loss of the drafter and its gradient (DeepSpec walkthrough

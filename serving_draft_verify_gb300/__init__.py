@@ -11,6 +11,7 @@ from ._binding import (  # noqa: F401
     MAX_GAMMA,
     dspark_accept_rate_tv,
     dspark_training_loss,
+    dspark_decode_rounds,
     dspark_draft_block,
     dspark_schedule_prefix,
     dspark_verify,

@@ -42,6 +42,10 @@ _SIGNATURES = {
     "dspark_training_loss_workspace_size": (_c_size, [_c_i64, _c_int]),
     "dspark_training_loss": (_c_int, [_c_i64, _c_int, _c_int, _p, _p, _p, _p, _p, _c_float, _c_float, _c_float,
                                       _p, _p, _p, _p, _p, _c_size, _p]),
+    "dspark_decode_rounds_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "dspark_decode_rounds": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _p, _p, _p,
+                                      _p, _p, _p, _c_float, _p, _p, _c_float, _c_u64, _p, _p, _p, _p, _p, _c_size,
+                                      _p]),
     "dspark_debug_draft_logits": (_c_int, [_c_int, _c_int, _c_int, _p, _p, _p, _p, _p, _p, _c_size, _p]),
     "dspark_debug_enable_phase_timing": (_c_int, [_c_int]),
     "dspark_debug_phase_times": (_c_int, [_p, _c_int]),
@@ -185,6 +189,63 @@ def dspark_training_loss(d, t, target, conf_logit, omega, alpha_ce=0.1, alpha_l1
                                     float(alpha_ce), float(alpha_l1), float(alpha_conf), _ptr(out["row"]),
                                     _ptr(out["loss"]), _ptr(gd), _ptr(gc), _ptr(ws), _nbytes(ws),
                                     _stream(stream)))
+    return out
+
+
+class _RoundTrace(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("x", "lse_d", "logp_d", "c", "a", "ell", "n_accept", "next_token")]
+
+
+def dspark_decode_rounds(U, h, t, W1, W2, w, bias, sps, anchor, rounds, temperature, seed, trace=False, out=None,
+                         workspace=None, stream=None):
+    """`rounds` draft -> schedule -> verify rounds over the pool U [P, B, gamma, V],
+    h [P, B, gamma, H], t [P, B, gamma+1, V]; `anchor` [B] int32 is updated in place
+    to the last emitted tokens.  Returns dict tokens [rounds, B, gamma+1],
+    n_emitted [rounds, B], stats [rounds, 2] (E[tau], realised tokens per request)
+    and, with trace=True, the per-round x, lse_d, logp_d, c, a, ell, n_accept,
+    next_token."""
+    lib = load()
+    P, B, G, V = U.shape
+    H = h.shape[-1]
+    r = W1.shape[-1]
+    _need(U, (P, B, G, V), name="U")
+    _need(h, (P, B, G, H), U.dtype, name="h")
+    _need(t, (P, B, G + 1, V), U.dtype, name="t")
+    _need(W1, (V, r), U.dtype, name="W1")
+    _need(W2, (V, r), U.dtype, name="W2")
+    _need(w, (H + r,), U.dtype, name="w")
+    _need(sps, (B * (G + 1) + 1,), torch.float64, name="sps")
+    _need(anchor, (B,), torch.int32, name="anchor")
+    dt = _dtype_code(U, h, t, W1, W2, w)
+    dev = U.device
+    if out is None:
+        out = dict(tokens=torch.empty((rounds, B, G + 1), dtype=torch.int32, device=dev),
+                   n_emitted=torch.empty((rounds, B), dtype=torch.int32, device=dev),
+                   stats=torch.empty((rounds, 2), dtype=torch.float64, device=dev))
+        if trace:
+            for k in ("x",):
+                out[k] = torch.empty((rounds, B, G), dtype=torch.int32, device=dev)
+            for k in ("lse_d", "logp_d", "c", "a"):
+                out[k] = torch.empty((rounds, B, G), dtype=torch.float32, device=dev)
+            for k in ("ell", "n_accept", "next_token"):
+                out[k] = torch.empty((rounds, B), dtype=torch.int32, device=dev)
+    _need(out["tokens"], (rounds, B, G + 1), torch.int32, name="tokens")
+    _need(out["n_emitted"], (rounds, B), torch.int32, name="n_emitted")
+    _need(out["stats"], (rounds, 2), torch.float64, name="stats")
+    tr = None
+    if any(n in out for n, _ in _RoundTrace._fields_):
+        for n, _ in _RoundTrace._fields_:
+            if n in out:
+                _need(out[n], (rounds, B, G) if n in ("x", "lse_d", "logp_d", "c", "a") else (rounds, B),
+                      torch.int32 if n in ("x", "ell", "n_accept", "next_token") else torch.float32, name=n)
+        tr = _RoundTrace(*[out[n].data_ptr() if n in out else None for n, _ in _RoundTrace._fields_])
+    ws = _workspace(lib.dspark_decode_rounds_workspace_size(B, G, V, r), dev, workspace)
+    _check("dspark_decode_rounds",
+           lib.dspark_decode_rounds(rounds, P, B, G, V, H, r, dt, _ptr(U), _ptr(h), _ptr(t), _ptr(W1), _ptr(W2),
+                                    _ptr(w), float(bias), _ptr(sps), _ptr(anchor), float(temperature),
+                                    int(seed) & ((1 << 64) - 1), _ptr(out["tokens"]), _ptr(out["n_emitted"]),
+                                    _ptr(out["stats"]), ctypes.addressof(tr) if tr is not None else None, _ptr(ws),
+                                    _nbytes(ws), _stream(stream)))
     return out
 
 

@@ -141,6 +141,25 @@ def make_tv_inputs(cfg, device="cpu", rows=None):
     return d, t
 
 
+def make_round_pool(cfg, pool, device="cpu"):
+    """A pool of `pool` synthetic rounds for multi-round decoding: slot 0 is
+    make_draft_inputs(cfg); slot p > 0 draws U, h and t the same way from seed
+    cfg.seed + 7919 p.  W1, W2, w, bias, x0 and the SPS table are slot 0's.
+    Returns dict U [P, B, gamma, V], h [P, B, gamma, H], t [P, B, gamma+1, V] and
+    the shared tensors."""
+    base = make_draft_inputs(cfg, device=device)
+    Us, hs, ts = [base["U"]], [base["h"]], [base["t"]]
+    for p in range(1, pool):
+        g = make_draft_inputs(replace(cfg, seed=cfg.seed + 7919 * p), device=device)
+        Us.append(g["U"])
+        hs.append(g["h"])
+        ts.append(g["t"])
+        del g
+    out = dict(base)
+    out["U"], out["h"], out["t"] = torch.stack(Us), torch.stack(hs), torch.stack(ts)
+    return out
+
+
 LOSS_BLOCK = 16   # training block size: rows are (sequence, anchor, block position k)
 
 
