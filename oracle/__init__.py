@@ -16,12 +16,13 @@ Modules
   tv        c* = 1 - 1/2 ||softmax(d) - softmax(t)||_1
   loss      the joint training loss (CE + L1 + BCE, position weights) and its gradient
   rounds    several draft -> schedule -> verify rounds with the anchor carried
+  heads     the gated and recurrent sequential heads (the rank-r row behind the bias)
 
 Parity status: every function is pinned by tests/test_oracle_*.py against
 closed forms, brute force, the generator's published vectors or distribution
 tests; none is "parity unpinned".
 """
-from . import philox, sampling, draft, schedule, verify, tv, loss, rounds  # noqa: F401
+from . import philox, sampling, draft, schedule, verify, tv, loss, rounds, heads  # noqa: F401
 from .draft import draft_block, markov_bias, confidence, draft_logits  # noqa: F401
 from .schedule import schedule_prefix  # noqa: F401
 from .verify import verify as verify_round  # noqa: F401

@@ -37,7 +37,7 @@ def confidence(w, bias, h_k, W1_prev):
     return 1.0 / (1.0 + np.exp(-logit))
 
 
-def draft_block(U, h, W1, W2, w, bias, x0, temperature, seed, forced_tokens=None, requests=None):
+def draft_block(U, h, W1, W2, w, bias, x0, temperature, seed, forced_tokens=None, requests=None, head=None):
     """One draft block for B requests.
 
     U[B, gamma, V], h[B, gamma, H], W1/W2[V, r], w[H + r], x0[B].
@@ -45,7 +45,10 @@ def draft_block(U, h, W1, W2, w, bias, x0, temperature, seed, forced_tokens=None
     (teacher forcing), so each position can be checked on its own.
     requests[B] (optional): the request index b that keys each row's random
     draws (default 0..B-1), so a sample of rows can be checked on its own.
-    Returns a dict of x, lse_d, logp_d, c, a [B, gamma] and margin [B, gamma].
+    head (optional): an oracle.heads.Head (gated or recurrent) whose e_k replaces
+    W1[x_{k-1}] in the bias B_k = W2 . e_k (section 3.2's other two heads).
+    Returns a dict of x, lse_d, logp_d, c, a [B, gamma], margin [B, gamma] and
+    E [B, gamma, r] (the e_k of every position).
     """
     U = np.asarray(U, dtype=np.float64)
     B, gamma, V = U.shape
@@ -60,8 +63,16 @@ def draft_block(U, h, W1, W2, w, bias, x0, temperature, seed, forced_tokens=None
     req = np.arange(B)
     keys = req if requests is None else np.asarray(requests, dtype=np.int64)
     T = float(temperature)
+    W1f = np.asarray(W1, np.float64)
+    E = np.zeros((B, gamma, W1f.shape[1]))
+    state = None if head is None else head.start(B, W1f.shape[1])
     for k in range(1, gamma + 1):
-        z = U[:, k - 1, :] + markov_bias(W1, W2, prev)
+        if head is None:
+            E[:, k - 1, :] = W1f[prev]
+            z = U[:, k - 1, :] + markov_bias(W1, W2, prev)
+        else:
+            E[:, k - 1, :], state = head.step(W1f[prev], np.asarray(h, np.float64)[:, k - 1, :], state)
+            z = U[:, k - 1, :] + E[:, k - 1, :] @ np.asarray(W2, np.float64).T
         if T > 0.0:
             l = z / T
             L = logsumexp(l, axis=-1)
@@ -77,15 +88,18 @@ def draft_block(U, h, W1, W2, w, bias, x0, temperature, seed, forced_tokens=None
         surv = surv * c[:, k - 1]
         a[:, k - 1] = surv
         prev = tok if forced_tokens is None else np.asarray(forced_tokens, np.int64)[:, k - 1]
-    return dict(x=x, lse_d=lse_d, logp_d=logp_d, c=c, a=a, margin=margin)
+    return dict(x=x, lse_d=lse_d, logp_d=logp_d, c=c, a=a, margin=margin, E=E)
 
 
-def draft_logits(U, W1, W2, x0, tokens, b, k):
+def draft_logits(U, W1, W2, x0, tokens, b, k, E=None):
     """z = U_k + B_k for request rows b at (1-based) position k, given the tokens
-    x[b, 1..gamma] (x_{k-1} is x0 for k = 1).  Used by the residual of verify."""
+    x[b, 1..gamma] (x_{k-1} is x0 for k = 1), or given E [B, gamma, r], the e_k a
+    gated or recurrent head used.  Used by the residual of verify."""
     U = np.asarray(U, dtype=np.float64)
     b = np.asarray(b, dtype=np.int64)
     k = np.asarray(k, dtype=np.int64)
+    if E is not None:
+        return U[b, k - 1, :] + np.asarray(E, np.float64)[b, k - 1, :] @ np.asarray(W2, np.float64).T
     tokens = np.asarray(tokens, dtype=np.int64)
     x0 = np.asarray(x0, dtype=np.int64)
     prev = np.where(k == 1, x0[b], tokens[b, np.maximum(k - 2, 0)])

@@ -23,7 +23,7 @@ from .sampling import two_level_gumbel, greedy, logsumexp
 from .draft import draft_logits
 
 
-def verify(t_logits, U, W1, W2, x0, x, lse_d, logp_d, ell, temperature, seed, requests=None):
+def verify(t_logits, U, W1, W2, x0, x, lse_d, logp_d, ell, temperature, seed, requests=None, E=None):
     """Return dict(n_accept[B], next_token[B], margin[B]).
 
     t_logits[B, gamma+1, V], U[B, gamma, V], W1/W2[V, r], x0[B], x[B, gamma],
@@ -86,7 +86,7 @@ def verify(t_logits, U, W1, W2, x0, x, lse_d, logp_d, ell, temperature, seed, re
         if len(res_rows):
             trow = t_logits[res_rows, k - 1, :] / T
             p_t = np.exp(trow - logsumexp(trow, axis=-1)[:, None])
-            z = draft_logits(U, W1, W2, x0, x, res_rows, np.full(len(res_rows), k))
+            z = draft_logits(U, W1, W2, x0, x, res_rows, np.full(len(res_rows), k), E=E)
             p_d = np.exp(z / T - lse_d[res_rows, k - 1][:, None])
             q = np.maximum(0.0, p_t - p_d)
             has_mass = np.sum(q, axis=-1) > 0.0

@@ -93,7 +93,7 @@ def test_resampling_from_target_on_reject_is_caught(monkeypatch):
     # a classic slip: on a rejection draw from p_t instead of max(0, p_t - p_d)
     import oracle.verify as V
     monkeypatch.setattr(V, "draft_logits",
-                        lambda U, W1, W2, x0, tokens, b, k: np.full((len(b), np.shape(U)[-1]), -np.inf))
+                        lambda U, W1, W2, x0, tokens, b, k, E=None: np.full((len(b), np.shape(U)[-1]), -np.inf))
     assert _fails(T_verify.test_first_emitted_token_follows_target)
 
 
@@ -155,3 +155,27 @@ def test_rounds_dropping_the_verifier_token_is_caught(monkeypatch):
     monkeypatch.setattr(R, "emitted_tokens", bad)
     assert _fails(T_rounds.test_anchor_is_the_last_emitted_token)
     assert _fails(T_rounds.test_agreeing_target_accepts_every_scheduled_token)
+
+
+def test_heads_inverted_gate_is_caught(monkeypatch):
+    from oracle import heads as Hd
+    import tests.test_oracle_heads as T_heads
+    orig = Hd.sigmoid
+    monkeypatch.setattr(Hd, "sigmoid", lambda x: 1.0 - orig(x))
+    assert _fails(T_heads.test_saturated_gates_reduce_to_closed_forms)
+
+
+def test_heads_state_not_carried_is_caught(monkeypatch):
+    from oracle import heads as Hd
+    import tests.test_oracle_heads as T_heads
+    orig = Hd.Head.step
+    monkeypatch.setattr(Hd.Head, "step", lambda self, W1p, hk, st: orig(self, W1p, hk, np.zeros_like(st)))
+    assert _fails(T_heads.test_rnn_half_gate_is_the_unrolled_sum)
+
+
+def test_heads_gate_on_the_next_hidden_state_is_caught(monkeypatch):
+    from oracle import heads as Hd
+    import tests.test_oracle_heads as T_heads
+    orig = Hd.Head.step
+    monkeypatch.setattr(Hd.Head, "step", lambda self, W1p, hk, st: orig(self, W1p, np.roll(hk, 1, axis=0), st))
+    assert _fails(T_heads.test_gate_reads_h_of_its_own_position)
