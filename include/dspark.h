@@ -9,6 +9,7 @@
  *   dspark_accept_rate_tv   c* = 1 - 1/2 ||softmax(d) - softmax(t)||_1 per row
  *   dspark_training_loss    joint CE + L1 + BCE loss per row, and its gradient
  *   dspark_decode_rounds    draft -> schedule -> verify rounds, anchor carried
+ * (and _ex variants of the draft and verify calls for the gated / RNN heads)
  *
  * Sources (cited per call): the DeepSpec / DSpark walkthrough at
  * wangjunjian.com ("DSpark" post, sections 2.1, 3.2, 3.3, 7.2, 8.1-8.3) and the
@@ -207,6 +208,62 @@ dspark_status_t dspark_accept_rate_tv(int64_t rows, int V, dspark_dtype_t dt,
                                       const void* d, const void* t, float* c_star,
                                       void* workspace, size_t workspace_bytes,
                                       dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Sequential heads beyond the Markov head (DeepSpec walkthrough section 3.2,
+ * the three heads of markov_head.py).  Every head adds a bias
+ *   B_k(v) = W2[v] . e_k                  (the output projection of eq. 5)
+ * to the parallel logits U_k; the heads differ in the rank-r vector e_k:
+ *   DSPARK_HEAD_MARKOV  e_k = W1[x_{k-1}]                      (VanillaMarkovHead, eq. 5)
+ *   DSPARK_HEAD_GATED   e_k = sigmoid(Wg . [h_k ; W1[x_{k-1}]]) (*) W1[x_{k-1}]
+ *                       (GatedMarkovHead: a hidden-state gate on the Markov row)
+ *   DSPARK_HEAD_RNN     s_k = g (*) s_{k-1} + (1 - g) (*) tanh(Wc . z_k),
+ *                       g = sigmoid(Wg . z_k), z_k = [s_{k-1} ; W1[x_{k-1}] ; h_k],
+ *                       s_0 = 0, e_k = s_k          (RNNHead, GRU-like, eq. 6)
+ * with (*) the element-wise product, s_k in R^r, and h_k = h[b][k-1].
+ *   Wg: GATED [r][H + r] (columns: h, then W1 row); RNN [r][2r + H] (columns: s,
+ *       W1 row, h); Wc: RNN [r][2r + H]; in the call's dtype, rows 16-byte aligned.
+ *   E [B][gamma][r] in the call's dtype: the e_k each position used, written by
+ *   dspark_draft_block_ex and read by dspark_verify_ex (the residual rebuilds
+ *   z_k from it).  e_k is formed in float32 (the RNN state stays float32) and
+ *   rounded to the dtype, as W1 rows are, before the projection.
+ * The Markov kind ignores Wg, Wc and E.
+ * ------------------------------------------------------------------------ */
+typedef enum dspark_head_kind {
+    DSPARK_HEAD_MARKOV = 0,
+    DSPARK_HEAD_GATED = 1,
+    DSPARK_HEAD_RNN = 2
+} dspark_head_kind_t;
+
+typedef struct dspark_head {
+    int kind;        /* dspark_head_kind_t */
+    const void* Wg;
+    const void* Wc;
+    void* E;
+} dspark_head_t;
+
+/* dspark_draft_block with a sequential head (NULL: the Markov head).  Gated
+ * and RNN heads run one launch per position with a head kernel before each.
+ * Requires H > 0 for them.  Workspace: dspark_draft_block_ex_workspace_size. */
+size_t dspark_draft_block_ex_workspace_size(int B, int gamma, int V, int r, int kind);
+
+dspark_status_t dspark_draft_block_ex(int B, int gamma, int V, int H, int r, dspark_dtype_t dt,
+                                      const void* U, const void* h, const void* W1, const void* W2,
+                                      const void* w, float bias, const int32_t* x0,
+                                      float temperature, uint64_t seed, const dspark_head_t* head,
+                                      int32_t* x, float* lse_d, float* logp_d, float* c, float* a,
+                                      void* workspace, size_t workspace_bytes, dspark_stream_t stream);
+
+/* dspark_verify for a draft made with a sequential head: the residual's p_d
+ * is rebuilt from head->E (NULL or the Markov kind: from W1[x_{k-1}]).  The
+ * workspace is dspark_verify's. */
+dspark_status_t dspark_verify_ex(int B, int gamma, int V, int r, dspark_dtype_t dt,
+                                 const void* t_logits, const void* U, const void* W1, const void* W2,
+                                 const int32_t* x0, const int32_t* x, const float* lse_d,
+                                 const float* logp_d, const int32_t* ell, float temperature,
+                                 uint64_t seed, const dspark_head_t* head, int32_t* n_accept,
+                                 int32_t* next_token, void* workspace, size_t workspace_bytes,
+                                 dspark_stream_t stream);
 
 /* ------------------------------------------------------------------------ *
  * Several decoding rounds in a row (DeepSpec walkthrough sections 8.1 / 8.3,

@@ -12,6 +12,11 @@ from ._binding import (  # noqa: F401
     dspark_accept_rate_tv,
     dspark_training_loss,
     dspark_decode_rounds,
+    dspark_draft_block_ex,
+    dspark_verify_ex,
+    HEAD_MARKOV,
+    HEAD_GATED,
+    HEAD_RNN,
     dspark_draft_block,
     dspark_schedule_prefix,
     dspark_verify,

@@ -46,6 +46,11 @@ _SIGNATURES = {
     "dspark_decode_rounds": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _p, _p, _p,
                                       _p, _p, _p, _c_float, _p, _p, _c_float, _c_u64, _p, _p, _p, _p, _p, _c_size,
                                       _p]),
+    "dspark_draft_block_ex_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
+    "dspark_draft_block_ex": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _p, _p, _p, _p, _p,
+                                       _c_float, _p, _c_float, _c_u64, _p, _p, _p, _p, _p, _p, _p, _c_size, _p]),
+    "dspark_verify_ex": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _p, _p, _p, _p, _p, _p, _p, _p, _p,
+                                  _c_float, _c_u64, _p, _p, _p, _p, _c_size, _p]),
     "dspark_debug_draft_logits": (_c_int, [_c_int, _c_int, _c_int, _p, _p, _p, _p, _p, _p, _c_size, _p]),
     "dspark_debug_enable_phase_timing": (_c_int, [_c_int]),
     "dspark_debug_phase_times": (_c_int, [_p, _c_int]),
@@ -277,6 +282,62 @@ def dspark_draft_block(U, h, W1, W2, w, bias, x0, temperature, seed, out=None, w
     return out
 
 
+HEAD_MARKOV, HEAD_GATED, HEAD_RNN = 0, 1, 2
+
+
+class _Head(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("Wg", ctypes.c_void_p), ("Wc", ctypes.c_void_p), ("E", ctypes.c_void_p)]
+
+
+def _head_struct(head, B, G, H, r, dtype, dev):
+    """ctypes head descriptor from a dict {kind, Wg, Wc, E}; allocates E if absent."""
+    kind = int(head["kind"])
+    if kind == HEAD_MARKOV:
+        return _Head(kind, None, None, None), None
+    ldw = H + r if kind == HEAD_GATED else 2 * r + H
+    _need(head["Wg"], (r, ldw), dtype, name="Wg")
+    if kind == HEAD_RNN:
+        _need(head["Wc"], (r, ldw), dtype, name="Wc")
+    E = head.get("E")
+    if E is None:
+        E = torch.empty((B, G, r), dtype=dtype, device=dev)
+    _need(E, (B, G, r), dtype, name="E")
+    Wc = head.get("Wc")
+    return _Head(kind, head["Wg"].data_ptr(), Wc.data_ptr() if Wc is not None else None, E.data_ptr()), E
+
+
+def dspark_draft_block_ex(U, h, W1, W2, w, bias, x0, temperature, seed, head, out=None, workspace=None,
+                          stream=None):
+    """Draft block with a sequential head: head = dict(kind=HEAD_GATED or HEAD_RNN,
+    Wg=[r, H+r] or [r, 2r+H], Wc=[r, 2r+H] (RNN), E=[B, gamma, r] (optional)).
+    Returns dict x, lse_d, logp_d, c, a and E (the rank-r rows the bias used)."""
+    lib = load()
+    B, G, V = U.shape
+    H = h.shape[-1]
+    r = W1.shape[-1]
+    _need(U, (B, G, V), name="U")
+    _need(h, (B, G, H), U.dtype, name="h")
+    _need(W1, (V, r), U.dtype, name="W1")
+    _need(W2, (V, r), U.dtype, name="W2")
+    _need(w, (H + r,), U.dtype, name="w")
+    _need(x0, (B,), torch.int32, name="x0")
+    dt = _dtype_code(U, h, W1, W2, w)
+    dev = U.device
+    hs, E = _head_struct(head, B, G, H, r, U.dtype, dev)
+    if out is None:
+        out = dict(x=torch.empty((B, G), dtype=torch.int32, device=dev),
+                   **{k: torch.empty((B, G), dtype=torch.float32, device=dev)
+                      for k in ("lse_d", "logp_d", "c", "a")})
+    ws = _workspace(lib.dspark_draft_block_ex_workspace_size(B, G, V, r, int(head["kind"])), dev, workspace)
+    _check("dspark_draft_block_ex",
+           lib.dspark_draft_block_ex(B, G, V, H, r, dt, _ptr(U), _ptr(h), _ptr(W1), _ptr(W2), _ptr(w),
+                                     float(bias), _ptr(x0), float(temperature), int(seed) & (2**64 - 1),
+                                     ctypes.addressof(hs), _ptr(out["x"]), _ptr(out["lse_d"]), _ptr(out["logp_d"]),
+                                     _ptr(out["c"]), _ptr(out["a"]), _ptr(ws), _nbytes(ws), _stream(stream)))
+    out["E"] = E
+    return out
+
+
 def dspark_draft_block_noalloc(U, h, W1, W2, w, bias, x0, temperature, seed, out, stream=None):
     """dspark_draft_block with the library's fixed internal scratch (no workspace);
     for hosts that forbid device allocation.  `out` must hold preallocated
@@ -392,3 +453,37 @@ def phase_times():
     buf = (ctypes.c_float * 64)()
     n = load().dspark_debug_phase_times(ctypes.cast(buf, ctypes.c_void_p), 64)
     return [buf[i] for i in range(n)]
+
+
+def dspark_verify_ex(t_logits, U, W1, W2, x0, x, lse_d, logp_d, ell, temperature, seed, head, out=None,
+                     workspace=None, stream=None):
+    """Verification of a draft made with a sequential head: head = dict(kind, E)
+    where E [B, gamma, r] holds the rows the draft's bias used."""
+    lib = load()
+    B, G, V = U.shape
+    r = W1.shape[-1]
+    _need(t_logits, (B, G + 1, V), U.dtype, name="t_logits")
+    _need(U, (B, G, V), name="U")
+    _need(W1, (V, r), U.dtype, name="W1")
+    _need(W2, (V, r), U.dtype, name="W2")
+    _need(x0, (B,), torch.int32, name="x0")
+    _need(x, (B, G), torch.int32, name="x")
+    _need(lse_d, (B, G), torch.float32, name="lse_d")
+    _need(logp_d, (B, G), torch.float32, name="logp_d")
+    _need(ell, (B,), torch.int32, name="ell")
+    dt = _dtype_code(t_logits, U, W1, W2)
+    dev = U.device
+    kind = int(head["kind"])
+    if kind != HEAD_MARKOV:
+        _need(head["E"], (B, G, r), U.dtype, name="E")
+    hs = _Head(kind, None, None, head["E"].data_ptr() if kind != HEAD_MARKOV else None)
+    if out is None:
+        out = dict(n_accept=torch.empty(B, dtype=torch.int32, device=dev),
+                   next_token=torch.empty(B, dtype=torch.int32, device=dev))
+    ws = _workspace(lib.dspark_verify_workspace_size(B, G, V, r), dev, workspace)
+    _check("dspark_verify_ex",
+           lib.dspark_verify_ex(B, G, V, r, dt, _ptr(t_logits), _ptr(U), _ptr(W1), _ptr(W2), _ptr(x0),
+                                _ptr(x), _ptr(lse_d), _ptr(logp_d), _ptr(ell), float(temperature),
+                                int(seed) & (2**64 - 1), ctypes.addressof(hs), _ptr(out["n_accept"]),
+                                _ptr(out["next_token"]), _ptr(ws), _nbytes(ws), _stream(stream)))
+    return out

@@ -1,6 +1,7 @@
 // dspark_draft_block: the semi-autoregressive draft block of DSpark
 // (DeepSpec walkthrough, section 3.2 stage two, `sample_block_tokens`):
-//   for k = 1..gamma:  z_k = U_k + W2 . W1[x_{k-1}]   (VanillaMarkovHead, eq. 5)
+//   for k = 1..gamma:  z_k = U_k + W2 . W1[x_{k-1}]   (VanillaMarkovHead, eq. 5;
+//                      dspark_draft_block_ex: W2 . e_k of a gated or recurrent head)
 //                      x_k ~ softmax(z_k / T)          (two-level Gumbel-max)
 // plus the confidence head and survival product (section 3.3).
 //
@@ -72,7 +73,8 @@ constexpr int kSimtThreads = 256;
 template <bool kBF16>
 __global__ void __launch_bounds__(kSimtThreads)
 draft_phase_simt(int B, int gamma, int V, int r, int k, const void* __restrict__ U,
-                 const void* __restrict__ W1, const void* __restrict__ W2, const int32_t* __restrict__ x0,
+                 const void* __restrict__ W1, const void* __restrict__ E, const void* __restrict__ W2,
+                 const int32_t* __restrict__ x0,
                  const int32_t* __restrict__ x, float cscale, int greedy, uint64_t seed, int nchunk,
                  DraftWs ws) {
     __shared__ float e[256];
@@ -81,7 +83,8 @@ draft_phase_simt(int B, int gamma, int V, int r, int k, const void* __restrict__
     const int b = blockIdx.y, chunk = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int prev = prev_token(x0, x, b, gamma, k, V, ws.status);
-    for (int j = threadIdx.x; j < r; j += blockDim.x) e[j] = ld_elem<kBF16>(W1, static_cast<size_t>(prev) * r + j);
+    const void* erow = eng::bias_row<kBF16>(E, W1, b, gamma, k, r, prev);
+    for (int j = threadIdx.x; j < r; j += blockDim.x) e[j] = ld_elem<kBF16>(erow, j);
     __syncthreads();
     const int nblk = (V + 63) / 64;
     const int lo = static_cast<int>(static_cast<long long>(chunk) * nblk / nchunk);
@@ -146,7 +149,8 @@ draft_phase_simt(int B, int gamma, int V, int r, int k, const void* __restrict__
 template <bool kBF16, int kCPL>
 __global__ void __launch_bounds__(64)
 draft_winner(int B, int gamma, int V, int r, int k, const void* __restrict__ U, const void* __restrict__ W1,
-             const void* __restrict__ W2, const int32_t* __restrict__ x0, int32_t* __restrict__ x,
+             const void* __restrict__ E, const void* __restrict__ W2, const int32_t* __restrict__ x0,
+             int32_t* __restrict__ x,
              float cscale, int greedy, uint64_t seed, DraftWs ws) {
     __shared__ float sbest[2], sy[2];
     __shared__ int sidx[2];
@@ -167,7 +171,7 @@ draft_winner(int B, int gamma, int V, int r, int k, const void* __restrict__ U, 
         if (threadIdx.x == 0) { x[b * gamma + k - 1] = static_cast<int>(idx); ws.ytok[slot] = 0.f; }
         return;
     }
-    const float z = eng::block_logit<kBF16, kCPL>(b, gamma, k, V, r, static_cast<int>(idx), U, W1, W2, x0, x,
+    const float z = eng::block_logit<kBF16, kCPL>(b, gamma, k, V, r, static_cast<int>(idx), U, W1, E, W2, x0, x,
                                                   ws.status);
     const int v = static_cast<int>(idx) * 64 + warp * 32 + lane;
     float score = -INFINITY, yv = 0.f;
@@ -222,6 +226,131 @@ draft_finalize(int B, int gamma, int V, int H, int r, const void* __restrict__ h
     }
 }
 
+// ============================================================= heads ====
+// Gated and recurrent heads (section 3.2, markov_head.py): the rank-r row e_k
+// behind position k's bias, written to E [B][gamma][r] before that position's
+// phase launch.  The h_k columns of Wg (and Wc) do not depend on the drawn
+// tokens, so their products with every h_k are formed once up front.
+struct HeadCtx {
+    int kind;                        // dspark_head_kind_t
+    const void* Wg;
+    const void* Wc;
+    void* E;                         // [B][gamma][r] in the call's dtype
+    float* hg;                       // [B * gamma][r]: Wg's h columns . h_k
+    float* hc;                       // [B * gamma][r]: Wc's h columns . h_k (RNN)
+    float* state;                    // [B][r]: the RNN state s_{k-1}
+};
+
+constexpr int kHpTile = 32, kHpK = 64;
+
+// out[m][j] = sum_{i < H} h[m][i] W[j][col + i] for m < M, j < r (W rows of ldw
+// elements).  32 x 32 outputs per CTA, 2 x 2 per thread, K in steps of 64
+// through shared memory; every output summed in i order.
+template <bool kBF16>
+__global__ void __launch_bounds__(256)
+head_hproj(int M, int H, int r, int ldw, int col, const void* __restrict__ h, const void* __restrict__ W,
+           float* __restrict__ out) {
+    __shared__ float As[kHpK][kHpTile + 1];
+    __shared__ float Bs[kHpK][kHpTile + 1];
+    const int tid = threadIdx.x;
+    const int m0 = blockIdx.x * kHpTile, j0 = blockIdx.y * kHpTile;
+    const int ty = tid >> 4, tx = tid & 15;
+    float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    for (int k0 = 0; k0 < H; k0 += kHpK) {
+        for (int e = tid; e < kHpTile * kHpK; e += 256) {
+            const int rr = e / kHpK, kk = e % kHpK;
+            const int m = m0 + rr, j = j0 + rr, i = k0 + kk;
+            As[kk][rr] = (m < M && i < H) ? ld_elem<kBF16>(h, static_cast<size_t>(m) * H + i) : 0.f;
+            Bs[kk][rr] = (j < r && i < H) ? ld_elem<kBF16>(W, static_cast<size_t>(j) * ldw + col + i) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int kk = 0; kk < kHpK; ++kk) {
+            const float a0 = As[kk][2 * ty], a1 = As[kk][2 * ty + 1];
+            const float b0 = Bs[kk][2 * tx], b1 = Bs[kk][2 * tx + 1];
+            acc[0][0] = fmaf(a0, b0, acc[0][0]);
+            acc[0][1] = fmaf(a0, b1, acc[0][1]);
+            acc[1][0] = fmaf(a1, b0, acc[1][0]);
+            acc[1][1] = fmaf(a1, b1, acc[1][1]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int m = m0 + 2 * ty + i, jj = j0 + 2 * tx + j;
+            if (m < M && jj < r) out[static_cast<size_t>(m) * r + jj] = acc[i][j];
+        }
+}
+
+// e_k of every request (one CTA each, one warp per output row of Wg / Wc):
+//   gated  e = sigmoid(hg + Wg[:, H:H+r] . W1[x_{k-1}]) * W1[x_{k-1}]
+//   RNN    g = sigmoid(hg + Wg[:, 0:r] . s + Wg[:, r:2r] . W1[x_{k-1}]),
+//          s' = g * s + (1 - g) * tanh(hc + Wc[:, 0:r] . s + Wc[:, r:2r] . W1[x_{k-1}]), e = s'
+// with s = s_{k-1} (0 at k = 1); e rounded to the dtype into E.
+template <bool kBF16>
+__global__ void __launch_bounds__(256)
+head_step(int kind, int B, int gamma, int V, int H, int r, int k, const void* __restrict__ W1,
+          const void* __restrict__ Wg, const void* __restrict__ Wc, const int32_t* __restrict__ x0,
+          const int32_t* __restrict__ x, const float* __restrict__ hg, const float* __restrict__ hc,
+          float* __restrict__ state, void* __restrict__ E, StatusBlock* st) {
+    __shared__ float xr[256], sv[256], pg[256], pc[256];
+    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool rnn = (kind == DSPARK_HEAD_RNN);
+    const int prev = prev_token(x0, x, b, gamma, k, V, st);
+    for (int j = tid; j < r; j += 256) {
+        xr[j] = ld_elem<kBF16>(W1, static_cast<size_t>(prev) * r + j);
+        sv[j] = (rnn && k > 1) ? state[static_cast<size_t>(b) * r + j] : 0.f;
+    }
+    __syncthreads();
+    const size_t row = static_cast<size_t>(b) * gamma + (k - 1);
+    const size_t ldw = rnn ? static_cast<size_t>(2 * r + H) : static_cast<size_t>(H + r);
+    for (int j = warp; j < r; j += 8) {
+        float ag = 0.f, ac = 0.f;
+        const size_t wr = static_cast<size_t>(j) * ldw;
+        if (!rnn) {
+            for (int i = lane; i < r; i += 32) ag = fmaf(ld_elem<kBF16>(Wg, wr + H + i), xr[i], ag);
+        } else {
+            for (int i = lane; i < r; i += 32) {
+                ag = fmaf(ld_elem<kBF16>(Wg, wr + i), sv[i], ag);
+                ag = fmaf(ld_elem<kBF16>(Wg, wr + r + i), xr[i], ag);
+                ac = fmaf(ld_elem<kBF16>(Wc, wr + i), sv[i], ac);
+                ac = fmaf(ld_elem<kBF16>(Wc, wr + r + i), xr[i], ac);
+            }
+        }
+        ag = warp_sum(ag);
+        ac = warp_sum(ac);
+        if (lane == 0) {
+            pg[j] = ag + hg[row * r + j];
+            if (rnn) pc[j] = ac + hc[row * r + j];
+        }
+    }
+    __syncthreads();
+    for (int j = tid; j < r; j += 256) {
+        const float g = 1.f / (1.f + expf(-pg[j]));
+        float e;
+        if (!rnn) {
+            e = g * xr[j];
+        } else {
+            e = g * sv[j] + (1.f - g) * tanhf(pc[j]);
+            state[static_cast<size_t>(b) * r + j] = e;
+        }
+        if constexpr (kBF16)
+            static_cast<uint16_t*>(E)[row * r + j] = __bfloat16_as_ushort(__float2bfloat16_rn(e));
+        else
+            static_cast<float*>(E)[row * r + j] = e;
+    }
+}
+
+template <bool kBF16>
+dspark_status_t launch_hproj(int M, int H, int r, int ldw, int col, const void* h, const void* W, float* out,
+                             cudaStream_t s) {
+    const dim3 grid((M + kHpTile - 1) / kHpTile, (r + kHpTile - 1) / kHpTile);
+    head_hproj<kBF16><<<grid, 256, 0, s>>>(M, H, r, ldw, col, h, W, out);
+    return launch_status();
+}
+
 // ====================================================== host launch ====
 // Phase-launch timing hook (see dspark_debug.h).
 struct PhaseTiming {
@@ -241,23 +370,25 @@ int simt_chunks(int V) {
 bool g_force_phase_launches = false;
 
 template <bool kBF16>
-dspark_status_t launch_winner(int B, int gamma, int V, int r, int k, const void* U, const void* W1, const void* W2,
-                              const int32_t* x0, int32_t* x, float cscale, int greedy, uint64_t seed, DraftWs ws,
-                              cudaStream_t s) {
+dspark_status_t launch_winner(int B, int gamma, int V, int r, int k, const void* U, const void* W1, const void* E,
+                              const void* W2, const int32_t* x0, int32_t* x, float cscale, int greedy, uint64_t seed,
+                              DraftWs ws, cudaStream_t s) {
     if (kBF16 || r <= 128)
-        draft_winner<kBF16, 1><<<B, 64, 0, s>>>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale, greedy, seed, ws);
+        draft_winner<kBF16, 1><<<B, 64, 0, s>>>(B, gamma, V, r, k, U, W1, E, W2, x0, x, cscale, greedy, seed, ws);
     else
-        draft_winner<kBF16, 2><<<B, 64, 0, s>>>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale, greedy, seed, ws);
+        draft_winner<kBF16, 2><<<B, 64, 0, s>>>(B, gamma, V, r, k, U, W1, E, W2, x0, x, cscale, greedy, seed, ws);
     return launch_status();
 }
 
 }  // namespace
 
 // Full draft block on `s`.
+// hd: a gated or recurrent head (null: the Markov head).
 dspark_status_t draft_block_impl(int B, int gamma, int V, int H, int r, dspark_dtype_t dt, const void* U,
                                  const void* h, const void* W1, const void* W2, const void* w, float bias,
                                  const int32_t* x0, float temperature, uint64_t seed, int32_t* x, float* lse_d,
-                                 float* logp_d, float* c, float* a, void* workspace, cudaStream_t s) {
+                                 float* logp_d, float* c, float* a, void* workspace, cudaStream_t s,
+                                 const HeadCtx* hd) {
     size_t clear = 0;
     const DraftWs ws = draft_ws(workspace, B, gamma, &clear);
     if (cudaMemsetAsync(workspace, 0, clear, s) != cudaSuccess) return DSPARK_ERR_CUDA;   // status .. words
@@ -265,6 +396,19 @@ dspark_status_t draft_block_impl(int B, int gamma, int V, int H, int r, dspark_d
     const float cscale = greedy ? 1.f : kLog2e / temperature;
     const bool tcp = eng::use_tc_path(dt, r);
     const bool bf = (dt == DSPARK_BF16);
+    const void* E = hd ? hd->E : nullptr;
+    if (hd) {
+        // the h_k products of the head's gate (and candidate) matrices, once
+        const int M = B * gamma;
+        const bool rnn = hd->kind == DSPARK_HEAD_RNN;
+        const int ldw = rnn ? 2 * r + H : H + r, col = rnn ? 2 * r : 0;
+        dspark_status_t st = bf ? launch_hproj<true>(M, H, r, ldw, col, h, hd->Wg, hd->hg, s)
+                                : launch_hproj<false>(M, H, r, ldw, col, h, hd->Wg, hd->hg, s);
+        if (st == DSPARK_OK && rnn)
+            st = bf ? launch_hproj<true>(M, H, r, ldw, col, h, hd->Wc, hd->hc, s)
+                    : launch_hproj<false>(M, H, r, ldw, col, h, hd->Wc, hd->hc, s);
+        if (st != DSPARK_OK) return st;
+    }
     CUtensorMap map;
     int nM = 1, P = 1, nchunk = 1;
     eng::TcParams p{};
@@ -274,12 +418,14 @@ dspark_status_t draft_block_impl(int B, int gamma, int V, int H, int r, dspark_d
         nchunk = P;
         p.B = B; p.gamma = gamma; p.V = V; p.r = r;
         p.U = static_cast<const uint16_t*>(U); p.W1 = static_cast<const uint16_t*>(W1);
+        p.E = static_cast<const uint16_t*>(E);
         p.W2 = static_cast<const uint16_t*>(W2);
         p.x0 = x0; p.x = x; p.cscale = cscale; p.greedy = greedy; p.seed = seed; p.P = P; p.ws = ws;
     } else {
         nchunk = simt_chunks(V);
     }
-    const bool one_launch = tcp && !g_force_phase_launches && nM * P <= sm_count(current_device());
+    // a head kernel runs between positions: one launch per position
+    const bool one_launch = tcp && !hd && !g_force_phase_launches && nM * P <= sm_count(current_device());
     dspark_status_t stt = DSPARK_OK;
     if (one_launch) {
         // every position, x_gamma and the finalize in one cooperative launch
@@ -297,6 +443,15 @@ dspark_status_t draft_block_impl(int B, int gamma, int V, int H, int r, dspark_d
         return stt;
     } else {
         for (int k = 1; k <= gamma; ++k) {
+            if (hd) {
+                if (bf)
+                    head_step<true><<<B, 256, 0, s>>>(hd->kind, B, gamma, V, H, r, k, W1, hd->Wg, hd->Wc, x0, x,
+                                                      hd->hg, hd->hc, hd->state, hd->E, ws.status);
+                else
+                    head_step<false><<<B, 256, 0, s>>>(hd->kind, B, gamma, V, H, r, k, W1, hd->Wg, hd->Wc, x0, x,
+                                                       hd->hg, hd->hc, hd->state, hd->E, ws.status);
+                if ((stt = launch_status()) != DSPARK_OK) return stt;
+            }
             if (g_timing.on) cudaEventRecord(g_timing.ev[2 * (k - 1)], s);
             if (tcp) {
                 p.k = p.k_last = k;
@@ -304,11 +459,11 @@ dspark_status_t draft_block_impl(int B, int gamma, int V, int H, int r, dspark_d
             } else {
                 dim3 grid(nchunk, B);
                 if (bf)
-                    draft_phase_simt<true><<<grid, kSimtThreads, 0, s>>>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale,
-                                                                         greedy, seed, nchunk, ws);
+                    draft_phase_simt<true><<<grid, kSimtThreads, 0, s>>>(B, gamma, V, r, k, U, W1, E, W2, x0, x,
+                                                                         cscale, greedy, seed, nchunk, ws);
                 else
-                    draft_phase_simt<false><<<grid, kSimtThreads, 0, s>>>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale,
-                                                                          greedy, seed, nchunk, ws);
+                    draft_phase_simt<false><<<grid, kSimtThreads, 0, s>>>(B, gamma, V, r, k, U, W1, E, W2, x0, x,
+                                                                          cscale, greedy, seed, nchunk, ws);
                 stt = launch_status();
             }
             if (g_timing.on) {
@@ -316,8 +471,8 @@ dspark_status_t draft_block_impl(int B, int gamma, int V, int H, int r, dspark_d
                 g_timing.recorded = k;
             }
             if (stt != DSPARK_OK) return stt;
-            stt = bf ? launch_winner<true>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale, greedy, seed, ws, s)
-                     : launch_winner<false>(B, gamma, V, r, k, U, W1, W2, x0, x, cscale, greedy, seed, ws, s);
+            stt = bf ? launch_winner<true>(B, gamma, V, r, k, U, W1, E, W2, x0, x, cscale, greedy, seed, ws, s)
+                     : launch_winner<false>(B, gamma, V, r, k, U, W1, E, W2, x0, x, cscale, greedy, seed, ws, s);
             if (stt != DSPARK_OK) return stt;
         }
     }
@@ -381,7 +536,69 @@ extern "C" dspark_status_t dspark_draft_block(int B, int gamma, int V, int H, in
     if (workspace_bytes < dspark_draft_block_workspace_size(B, gamma, V, r)) return DSPARK_ERR_WORKSPACE_TOO_SMALL;
     clear_stale_error();
     return draft_block_impl(B, gamma, V, H, r, dt, U, h, W1, W2, w, bias, x0, temperature, seed, x, lse_d, logp_d,
-                            c, a, workspace, reinterpret_cast<cudaStream_t>(stream));
+                            c, a, workspace, reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+// Workspace of dspark_draft_block_ex: dspark_draft_block's, then (gated, RNN) the
+// h_k products of Wg [B gamma][r] float, and (RNN) those of Wc and the state [B][r].
+static size_t draft_ex_layout(int B, int gamma, int V, int r, int kind, size_t* o_hg, size_t* o_hc, size_t* o_st) {
+    size_t o = round_up(dspark_draft_block_workspace_size(B, gamma, V, r), 256);
+    const size_t rows = static_cast<size_t>(B) * gamma * r * 4;
+    *o_hg = *o_hc = *o_st = 0;
+    if (kind == DSPARK_HEAD_GATED || kind == DSPARK_HEAD_RNN) {
+        *o_hg = o;
+        o += round_up(rows, 256);
+    }
+    if (kind == DSPARK_HEAD_RNN) {
+        *o_hc = o;
+        o += round_up(rows, 256);
+        *o_st = o;
+        o += round_up(static_cast<size_t>(B) * r * 4, 256);
+    }
+    return o;
+}
+
+extern "C" size_t dspark_draft_block_ex_workspace_size(int B, int gamma, int V, int r, int kind) {
+    if (B <= 0 || gamma <= 0 || V <= 0 || r <= 0) return kStatusBytes;
+    size_t a, b, c;
+    return draft_ex_layout(B, gamma, V, r, kind, &a, &b, &c);
+}
+
+extern "C" dspark_status_t dspark_draft_block_ex(int B, int gamma, int V, int H, int r, dspark_dtype_t dt,
+                                                 const void* U, const void* h, const void* W1, const void* W2,
+                                                 const void* w, float bias, const int32_t* x0, float temperature,
+                                                 uint64_t seed, const dspark_head_t* head, int32_t* x, float* lse_d,
+                                                 float* logp_d, float* c, float* a, void* workspace,
+                                                 size_t workspace_bytes, dspark_stream_t stream) {
+    const int kind = head ? head->kind : DSPARK_HEAD_MARKOV;
+    if (kind == DSPARK_HEAD_MARKOV)
+        return dspark_draft_block(B, gamma, V, H, r, dt, U, h, W1, W2, w, bias, x0, temperature, seed, x, lse_d,
+                                  logp_d, c, a, workspace, workspace_bytes, stream);
+    if (kind != DSPARK_HEAD_GATED && kind != DSPARK_HEAD_RNN) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (B <= 0 || B > 65535 || gamma <= 0 || gamma > DSPARK_MAX_GAMMA || V <= 0 || H <= 0 || r <= 0 || r > 256)
+        return DSPARK_ERR_INVALID_ARGUMENT;
+    if (dt != DSPARK_F32 && dt != DSPARK_BF16) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (!(temperature >= 0.f) || temperature == INFINITY) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (V % (dt == DSPARK_BF16 ? 8 : 4) != 0 || r % 8 != 0) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (!U || !h || !W1 || !W2 || !w || !x0 || !x || !lse_d || !logp_d || !c || !a) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (!head->Wg || !head->E || (kind == DSPARK_HEAD_RNN && !head->Wc)) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (!aligned16(U) || !aligned16(W1) || !aligned16(W2) || !aligned16(head->E)) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (workspace == nullptr || !aligned256(workspace)) return DSPARK_ERR_INVALID_ARGUMENT;
+    size_t ohg, ohc, ost;
+    if (workspace_bytes < draft_ex_layout(B, gamma, V, r, kind, &ohg, &ohc, &ost))
+        return DSPARK_ERR_WORKSPACE_TOO_SMALL;
+    clear_stale_error();
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    HeadCtx hd{};
+    hd.kind = kind;
+    hd.Wg = head->Wg;
+    hd.Wc = head->Wc;
+    hd.E = head->E;
+    hd.hg = reinterpret_cast<float*>(base + ohg);
+    hd.hc = kind == DSPARK_HEAD_RNN ? reinterpret_cast<float*>(base + ohc) : nullptr;
+    hd.state = kind == DSPARK_HEAD_RNN ? reinterpret_cast<float*>(base + ost) : nullptr;
+    return draft_block_impl(B, gamma, V, H, r, dt, U, h, W1, W2, w, bias, x0, temperature, seed, x, lse_d, logp_d,
+                            c, a, workspace, reinterpret_cast<cudaStream_t>(stream), &hd);
 }
 
 extern "C" dspark_status_t dspark_debug_draft_logits(int B, int V, int r, const void* U_k, const void* W1,

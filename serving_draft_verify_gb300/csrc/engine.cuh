@@ -17,8 +17,9 @@
 //               M = 128 request rows, N = 128 tokens, K = r, fp32 in TMEM;
 //   warps 4-11  two epilogue warpgroups, each with two TMEM accumulators, so
 //               the MMA of the next tile overlaps the epilogue of this one.
-// The A operand (rows W1[x_{k_b-1}], gathered into shared memory with the
-// same swizzle) is built by warps 1-11 at the start of every position.
+// The A operand (rows W1[x_{k_b-1}], or the rows E[b][k_b] of a gated or
+// recurrent head, gathered into shared memory with the same swizzle) is built
+// by warps 1-11 at the start of every position.
 //
 // Draft launches may cover positions k .. k_last (a cooperative launch, all
 // CTAs resident, TMEM and barriers set up once, the producer streaming W2
@@ -141,10 +142,11 @@ __device__ __forceinline__ void tree_reduce(float* v) {
 // warp w rebuilds tokens blk*64 + 32w + (0..31); each lane loads one or two
 // 16-byte chunks of every W2 row (coalesced rows) and a transpose-reduce
 // leaves token (32w + lane)'s dot product in that lane.  Returns z for the
-// lane's token (-inf past V).  prev: x_{k-1}, already checked against V.
+// lane's token (-inf past V).  erow: the rank-r row behind the bias of (b, k)
+// (bias_row).
 template <bool kBF16, int kCPL>
-__device__ __forceinline__ float block_logit_prev(int b, int gamma, int k, int V, int r, int blk, int prev,
-                                                  const void* U, const void* W1, const void* W2) {
+__device__ __forceinline__ float block_logit_prev(int b, int gamma, int k, int V, int r, int blk, const void* erow,
+                                                  const void* U, const void* W2) {
     constexpr int EPC = kBF16 ? 8 : 4;                    // elements per 16-byte chunk
     const int warp = (threadIdx.x >> 5) & 1, lane = threadIdx.x & 31;
     const int nch = r / EPC;
@@ -158,7 +160,7 @@ __device__ __forceinline__ float block_logit_prev(int b, int gamma, int k, int V
         const int c = lane + 32 * cc;
 #pragma unroll
         for (int q = 0; q < EPC; ++q)
-            e[cc][q] = (c < nch) ? ld_elem<kBF16>(W1, static_cast<size_t>(prev) * r + c * EPC + q) : 0.f;
+            e[cc][q] = (c < nch) ? ld_elem<kBF16>(erow, static_cast<size_t>(c) * EPC + q) : 0.f;
     }
     const uint64_t pol = policy_evict_last();
     float part[32];
@@ -203,12 +205,23 @@ __device__ __forceinline__ float block_logit_prev(int b, int gamma, int k, int V
     return part[0] + u;
 }
 
+// The rank-r row behind the bias of position k of request b: W1[x_{k-1}] for the
+// Markov head (E null), else row (b, k) of the rows E [B][gamma][r] that a
+// gated or recurrent head produced.
+template <bool kBF16>
+__device__ __forceinline__ const void* bias_row(const void* E, const void* W1, int b, int gamma, int k, int r,
+                                                int prev) {
+    const size_t row = E ? static_cast<size_t>(b) * gamma + (k - 1) : static_cast<size_t>(prev);
+    return static_cast<const uint8_t*>(E ? E : W1) + row * r * (kBF16 ? 2 : 4);
+}
+
 template <bool kBF16, int kCPL>
 __device__ __forceinline__ float block_logit(int b, int gamma, int k, int V, int r, int blk, const void* U,
-                                             const void* W1, const void* W2, const int32_t* x0, const int32_t* x,
-                                             StatusBlock* st) {
+                                             const void* W1, const void* E, const void* W2, const int32_t* x0,
+                                             const int32_t* x, StatusBlock* st) {
     const int prev = prev_token(x0, x, b, gamma, k, V, st);
-    return block_logit_prev<kBF16, kCPL>(b, gamma, k, V, r, blk, prev, U, W1, W2);
+    return block_logit_prev<kBF16, kCPL>(b, gamma, k, V, r, blk, bias_row<kBF16>(E, W1, b, gamma, k, r, prev), U,
+                                         W2);
 }
 
 // ===================================================== tcgen05 engine ====
@@ -240,6 +253,7 @@ struct TcParams {
     int B, gamma, V, r, k;           // k: the position of every row (kDraft)
     const uint16_t* U;               // [B][gamma][V]
     const uint16_t* W1;              // [V][r]
+    const uint16_t* E;               // [B][gamma][r] bias rows of a gated / recurrent head, or null (W1[x_{k-1}])
     const uint16_t* W2;              // [V][r] (the redraw of the winning block reads rows directly)
     const int32_t* x0;               // [B]
     int32_t* x;                      // [B][gamma]; kDraft writes x_{k-1} here (CTA 0 of each M-tile)
@@ -427,7 +441,8 @@ __device__ __forceinline__ bool pair_any(bool v, int bar) {
 // (bonus row, stream 5) inside that row's winning block.
 template <bool kBF16, int kCPL>
 __device__ __forceinline__ void finish_pair(const FinishArgs& f, int b, int gamma, int V, int r, const void* U,
-                                            const void* W1, const void* W2, const int32_t* x0, const int32_t* x,
+                                            const void* W1, const void* E, const void* W2, const int32_t* x0,
+                                            const int32_t* x,
                                             float cscale, uint64_t seed, StatusBlock* st, int bar, float* xch,
                                             int* xchi) {
     const int lane = threadIdx.x & 31, wp = (threadIdx.x >> 5) & 1;
@@ -439,7 +454,7 @@ __device__ __forceinline__ void finish_pair(const FinishArgs& f, int b, int gamm
     int v = 0x7FFFFFFF;
     if (residual) {
         const int blk = static_cast<int>(unpack_idx(rw));
-        const float z = block_logit<kBF16, kCPL>(b, gamma, kr, V, r, blk, U, W1, W2, x0, x, st);
+        const float z = block_logit<kBF16, kCPL>(b, gamma, kr, V, r, blk, U, W1, E, W2, x0, x, st);
         v = blk * 64 + wp * 32 + lane;
         if (z > -INFINITY) {
             const float yd = z * cscale;
@@ -597,7 +612,8 @@ __device__ __forceinline__ void pair_draw(const TcParams& p, int b, int k, int b
     int bi = 0x7FFFFFFF;
     if (ok) {
         const int blk = static_cast<int>(idx);
-        const float z = block_logit_prev<true, 1>(b, p.gamma, k, p.V, p.r, blk, prev, p.U, p.W1, p.W2);
+        const float z = block_logit_prev<true, 1>(b, p.gamma, k, p.V, p.r, blk,
+                                                  bias_row<true>(p.E, p.W1, b, p.gamma, k, p.r, prev), p.U, p.W2);
         const int v = blk * 64 + wp * 32 + lane;
         if (z > -INFINITY) {
             yv = z * p.cscale;
@@ -813,7 +829,11 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                     if (lane < cpr) {
                         const int slab = lane >> 3, c = lane & 7;
                         uint8_t* dst = sA + slab * kASlabBytes + (row >> 3) * 1024 + (row & 7) * 128 + ((c ^ (row & 7)) << 4);
-                        if (prev >= 0) cp_async16(dst, p.W1 + static_cast<size_t>(prev) * p.r + lane * 8);
+                        if (prev >= 0) {
+                            const uint16_t* src = p.E ? p.E + (static_cast<size_t>(m0 + rr) * p.gamma + (row_k(m0 + rr, k) - 1)) * p.r
+                                                      : p.W1 + static_cast<size_t>(prev) * p.r;
+                            cp_async16(dst, src + lane * 8);
+                        }
                         else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
                     }
                 }
@@ -1041,7 +1061,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
             if (warp >= 2 && *s_fail == 0) {
                 const int pair = (warp - 2) >> 1;
                 for (int b = blockIdx.x + pair * gridDim.x; b < p.B; b += 5 * gridDim.x)
-                    finish_pair<true, 1>(p.fin, b, p.gamma, p.V, p.r, p.U, p.W1, p.W2, p.x0, p.x, p.cscale, p.seed,
+                    finish_pair<true, 1>(p.fin, b, p.gamma, p.V, p.r, p.U, p.W1, p.E, p.W2, p.x0, p.x, p.cscale, p.seed,
                                          st, 2 + pair, reinterpret_cast<float*>(xch + 2 * pair), xchi + 2 * pair);
             }
         }

@@ -443,7 +443,8 @@ verify_rows(int gamma, int V, const void* __restrict__ t, const int32_t* __restr
 template <bool kBF16>
 __global__ void __launch_bounds__(256)
 residual_simt(int B, int gamma, int V, int r, const void* __restrict__ t, const void* __restrict__ U,
-              const void* __restrict__ W1, const void* __restrict__ W2, const int32_t* __restrict__ x0,
+              const void* __restrict__ W1, const void* __restrict__ E, const void* __restrict__ W2,
+              const int32_t* __restrict__ x0,
               const int32_t* __restrict__ x, float cscale, uint64_t seed, int nchunk, VerifyWs ws) {
     __shared__ float e[256];
     __shared__ float rk[8];
@@ -453,7 +454,8 @@ residual_simt(int B, int gamma, int V, int r, const void* __restrict__ t, const 
     if (k <= 0) return;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int prev = prev_token(x0, x, b, gamma, k, V, ws.status);
-    for (int j = threadIdx.x; j < r; j += blockDim.x) e[j] = ld_elem<kBF16>(W1, static_cast<size_t>(prev) * r + j);
+    const void* erow = eng::bias_row<kBF16>(E, W1, b, gamma, k, r, prev);
+    for (int j = threadIdx.x; j < r; j += blockDim.x) e[j] = ld_elem<kBF16>(erow, j);
     __syncthreads();
     const float lt2 = ws.lt2[b], ld2 = ws.ld2[b];
     const int nblk = (V + 63) / 64;
@@ -500,11 +502,11 @@ residual_simt(int B, int gamma, int V, int r, const void* __restrict__ t, const 
 template <bool kBF16, int kCPL>
 __global__ void __launch_bounds__(64)
 verify_finish(int gamma, int V, int r, eng::FinishArgs f, const void* __restrict__ U, const void* __restrict__ W1,
-              const void* __restrict__ W2, const int32_t* __restrict__ x0, const int32_t* __restrict__ x, float cscale,
-              uint64_t seed, StatusBlock* st) {
+              const void* __restrict__ E, const void* __restrict__ W2, const int32_t* __restrict__ x0,
+              const int32_t* __restrict__ x, float cscale, uint64_t seed, StatusBlock* st) {
     __shared__ float xch[2];
     __shared__ int xchi[2];
-    eng::finish_pair<kBF16, kCPL>(f, blockIdx.x, gamma, V, r, U, W1, W2, x0, x, cscale, seed, st, 1, xch, xchi);
+    eng::finish_pair<kBF16, kCPL>(f, blockIdx.x, gamma, V, r, U, W1, E, W2, x0, x, cscale, seed, st, 1, xch, xchi);
 }
 
 }  // namespace
@@ -519,12 +521,12 @@ extern "C" size_t dspark_verify_workspace_size(int B, int gamma, int V, int r) {
     return verify_ws_layout(B, gamma).total;
 }
 
-extern "C" dspark_status_t dspark_verify(int B, int gamma, int V, int r, dspark_dtype_t dt, const void* t_logits,
-                                         const void* U, const void* W1, const void* W2, const int32_t* x0,
-                                         const int32_t* x, const float* lse_d, const float* logp_d,
-                                         const int32_t* ell, float temperature, uint64_t seed, int32_t* n_accept,
-                                         int32_t* next_token, void* workspace, size_t workspace_bytes,
-                                         dspark_stream_t stream) {
+// E: the bias rows [B][gamma][r] of a gated or recurrent head, or null (Markov head).
+static dspark_status_t verify_impl(int B, int gamma, int V, int r, dspark_dtype_t dt, const void* t_logits,
+                                   const void* U, const void* W1, const void* E, const void* W2, const int32_t* x0,
+                                   const int32_t* x, const float* lse_d, const float* logp_d, const int32_t* ell,
+                                   float temperature, uint64_t seed, int32_t* n_accept, int32_t* next_token,
+                                   void* workspace, size_t workspace_bytes, dspark_stream_t stream) {
     if (B <= 0 || gamma <= 0 || gamma > DSPARK_MAX_GAMMA || V <= 0 || r <= 0 || r > 256 || r % 8 != 0)
         return DSPARK_ERR_INVALID_ARGUMENT;
     if (static_cast<long long>(B) * (gamma + 1) > 65535) return DSPARK_ERR_UNSUPPORTED;
@@ -570,6 +572,7 @@ extern "C" dspark_status_t dspark_verify(int B, int gamma, int V, int r, dspark_
         eng::TcParams p{};
         p.B = B; p.gamma = gamma; p.V = V; p.r = r; p.k = 1;
         p.U = static_cast<const uint16_t*>(U); p.W1 = static_cast<const uint16_t*>(W1);
+        p.E = static_cast<const uint16_t*>(E);
         p.W2 = static_cast<const uint16_t*>(W2); p.k_last = 1;
         p.x0 = x0; p.x = const_cast<int32_t*>(x); p.cscale = cscale; p.greedy = 0;   // read only here
         p.seed = seed; p.P = P;
@@ -584,16 +587,42 @@ extern "C" dspark_status_t dspark_verify(int B, int gamma, int V, int r, dspark_
         int nchunk = (nblk + 7) / 8;
         if (nchunk > 256) nchunk = 256;
         const dim3 g(nchunk, B);
-        if (bf) residual_simt<true><<<g, 256, 0, s>>>(B, gamma, V, r, t_logits, U, W1, W2, x0, x, cscale, seed, nchunk, ws);
-        else residual_simt<false><<<g, 256, 0, s>>>(B, gamma, V, r, t_logits, U, W1, W2, x0, x, cscale, seed, nchunk, ws);
+        if (bf) residual_simt<true><<<g, 256, 0, s>>>(B, gamma, V, r, t_logits, U, W1, E, W2, x0, x, cscale, seed, nchunk, ws);
+        else residual_simt<false><<<g, 256, 0, s>>>(B, gamma, V, r, t_logits, U, W1, E, W2, x0, x, cscale, seed, nchunk, ws);
         if ((stt = launch_status()) != DSPARK_OK) return stt;
     }
     if (drawn) return DSPARK_OK;
     if (bf)
-        verify_finish<true, 1><<<B, 64, 0, s>>>(gamma, V, r, f, U, W1, W2, x0, x, cscale, seed, ws.status);
+        verify_finish<true, 1><<<B, 64, 0, s>>>(gamma, V, r, f, U, W1, E, W2, x0, x, cscale, seed, ws.status);
     else if (r <= 128)
-        verify_finish<false, 1><<<B, 64, 0, s>>>(gamma, V, r, f, U, W1, W2, x0, x, cscale, seed, ws.status);
+        verify_finish<false, 1><<<B, 64, 0, s>>>(gamma, V, r, f, U, W1, E, W2, x0, x, cscale, seed, ws.status);
     else
-        verify_finish<false, 2><<<B, 64, 0, s>>>(gamma, V, r, f, U, W1, W2, x0, x, cscale, seed, ws.status);
+        verify_finish<false, 2><<<B, 64, 0, s>>>(gamma, V, r, f, U, W1, E, W2, x0, x, cscale, seed, ws.status);
     return launch_status();
+}
+
+extern "C" dspark_status_t dspark_verify(int B, int gamma, int V, int r, dspark_dtype_t dt, const void* t_logits,
+                                         const void* U, const void* W1, const void* W2, const int32_t* x0,
+                                         const int32_t* x, const float* lse_d, const float* logp_d,
+                                         const int32_t* ell, float temperature, uint64_t seed, int32_t* n_accept,
+                                         int32_t* next_token, void* workspace, size_t workspace_bytes,
+                                         dspark_stream_t stream) {
+    return verify_impl(B, gamma, V, r, dt, t_logits, U, W1, nullptr, W2, x0, x, lse_d, logp_d, ell, temperature,
+                       seed, n_accept, next_token, workspace, workspace_bytes, stream);
+}
+
+extern "C" dspark_status_t dspark_verify_ex(int B, int gamma, int V, int r, dspark_dtype_t dt, const void* t_logits,
+                                            const void* U, const void* W1, const void* W2, const int32_t* x0,
+                                            const int32_t* x, const float* lse_d, const float* logp_d,
+                                            const int32_t* ell, float temperature, uint64_t seed,
+                                            const dspark_head_t* head, int32_t* n_accept, int32_t* next_token,
+                                            void* workspace, size_t workspace_bytes, dspark_stream_t stream) {
+    const void* E = nullptr;
+    if (head != nullptr && head->kind != DSPARK_HEAD_MARKOV) {
+        if (head->kind != DSPARK_HEAD_GATED && head->kind != DSPARK_HEAD_RNN) return DSPARK_ERR_INVALID_ARGUMENT;
+        if (head->E == nullptr || !aligned16(head->E)) return DSPARK_ERR_INVALID_ARGUMENT;
+        E = head->E;
+    }
+    return verify_impl(B, gamma, V, r, dt, t_logits, U, W1, E, W2, x0, x, lse_d, logp_d, ell, temperature, seed,
+                       n_accept, next_token, workspace, workspace_bytes, stream);
 }

@@ -160,6 +160,20 @@ def make_round_pool(cfg, pool, device="cpu"):
     return out
 
 
+def make_head_weights(cfg, kind, device="cpu"):
+    """Weights of a gated (kind 1) or recurrent (kind 2) sequential head in the
+    config's dtype: Wg [r, H + r] (gated) or Wg, Wc [r, 2r + H] (recurrent), each
+    entry ~ N(0, 1 / (row length)) so that a gate's pre-activation is O(1)."""
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(cfg.seed + 31 * kind)
+    dt = _torch_dtype(cfg.dtype)
+    ld = cfg.H + cfg.r if kind == 1 else 2 * cfg.r + cfg.H
+    Wg = (torch.randn((cfg.r, ld), generator=gen, device=dev) / ld ** 0.5).to(dt)
+    Wc = (torch.randn((cfg.r, ld), generator=gen, device=dev) / ld ** 0.5).to(dt) if kind == 2 else None
+    return Wg, Wc
+
+
 LOSS_BLOCK = 16   # training block size: rows are (sequence, anchor, block position k)
 
 
