@@ -330,6 +330,23 @@ def run_gpu(args):
                                "achieved_gbs": lb / (l_ms * 1e-3) / 1e9,
                                "frac_of_peak": lb / (l_ms * 1e-3) / 1e9 / peak}
         del d_, t_, lout
+    # the draft block with the gated and recurrent heads (one launch per position plus a
+    # head kernel between positions), same workload
+    heads_x = None
+    if not args.skip_heads:
+        heads_x = {}
+        for kind, name in ((1, "gated"), (2, "rnn")):
+            Wg_, Wc_ = wl.make_head_weights(cfg, kind, device=dev)
+            head_ = dict(kind=kind, Wg=Wg_, Wc=Wc_, E=torch.empty((B, G, r), dtype=inp["U"].dtype, device=dev))
+            ws_h = torch.empty(lib.dspark_draft_block_ex_workspace_size(B, G, V, r, kind), dtype=torch.uint8,
+                               device=dev)
+
+            def head_call():
+                dsv.dspark_draft_block_ex(inp["U"], inp["h"], inp["W1"], inp["W2"], inp["w"], 0.0, inp["x0"], T,
+                                          seed, head_, out=outd, workspace=ws_h)
+            h_fn = graphed(head_call)
+            h_times, _ = timed(h_fn or head_call, 20, 3)
+            heads_x[name] = {"draft_ms": sum(h_times) / len(h_times), "cuda_graph": h_fn is not None}
     # several rounds with the anchor carried (the last emitted token), one CUDA graph over
     # a pool of 8 synthetic rounds of the same shape
     multi = None
@@ -363,7 +380,7 @@ def run_gpu(args):
             "config": dict(workload_config(world), cuda_graph=use_graph),
             "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / peak, "roofline": roofline, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps, "clocks": clk,
-            "extra": {"greedy_round": greedy, "accept_rate_tv": tv, "multi_round": multi,
+            "extra": {"greedy_round": greedy, "accept_rate_tv": tv, "multi_round": multi, "heads": heads_x,
                       "accepted_per_request": float(nacc.mean()), "scheduled_rows": int((ell + 1).sum())}}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, T, seed)
@@ -506,6 +523,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--skip-tv", action="store_true")
     ap.add_argument("--skip-rounds", action="store_true", help="skip the multi-round extra")
+    ap.add_argument("--skip-heads", action="store_true", help="skip the gated / recurrent head extra")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the round's calls directly, without a CUDA graph")
     ap.add_argument("--phase-traffic", type=float, default=None,
