@@ -236,98 +236,199 @@ struct HeadCtx {
     const void* Wg;
     const void* Wc;
     void* E;                         // [B][gamma][r] in the call's dtype
-    float* hg;                       // [B * gamma][r]: Wg's h columns . h_k
-    float* hc;                       // [B * gamma][r]: Wc's h columns . h_k (RNN)
+    float* hg;                       // [kHpSplits][B * gamma][r]: split-K partials of Wg's h columns . h_k
+    float* hc;                       // [kHpSplits][B * gamma][r]: the same for Wc (RNN)
     float* state;                    // [B][r]: the RNN state s_{k-1}
 };
 
-constexpr int kHpTile = 32, kHpK = 64;
+constexpr int kHpTile = 64, kHpK = 32;   // 64 x 64 outputs per CTA, K in steps of 32
+constexpr int kHpSplits = 5;             // split-K partials, summed in order by head_step
 
-// out[m][j] = sum_{i < H} h[m][i] W[j][col + i] for m < M, j < r (W rows of ldw
-// elements).  32 x 32 outputs per CTA, 2 x 2 per thread, K in steps of 64
-// through shared memory; every output summed in i order.
+// Loads 8 consecutive elements (a 16-byte bf16 group when vec) as floats; elements
+// at or past `n` read as 0.
+template <bool kBF16>
+__device__ __forceinline__ void load8(const void* base, size_t i, int n, bool vec, float* o) {
+    if (kBF16 && vec && n >= 8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + i);
+        o[0] = bf16lo(v.x); o[1] = bf16hi(v.x); o[2] = bf16lo(v.y); o[3] = bf16hi(v.y);
+        o[4] = bf16lo(v.z); o[5] = bf16hi(v.z); o[6] = bf16lo(v.w); o[7] = bf16hi(v.w);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = (e < n) ? ld_elem<kBF16>(base, i + e) : 0.f;
+    }
+}
+
+// part[split][m][j] = sum over this split's i of h[m][i] W[j][col + i], m < M, j < r
+// (W rows of ldw elements).  Each thread owns 4 x 4 outputs; every output sums its
+// i in order, and head_step adds the splits in order.
 template <bool kBF16>
 __global__ void __launch_bounds__(256)
-head_hproj(int M, int H, int r, int ldw, int col, const void* __restrict__ h, const void* __restrict__ W,
-           float* __restrict__ out) {
-    __shared__ float As[kHpK][kHpTile + 1];
-    __shared__ float Bs[kHpK][kHpTile + 1];
+head_hproj(int M, int H, int r, int ldw, int col, int vec, const void* __restrict__ h, const void* __restrict__ W,
+           float* __restrict__ part) {
+    __shared__ __align__(16) float As[kHpK][kHpTile];
+    __shared__ __align__(16) float Bs[kHpK][kHpTile];
     const int tid = threadIdx.x;
-    const int m0 = blockIdx.x * kHpTile, j0 = blockIdx.y * kHpTile;
+    const int m0 = blockIdx.x * kHpTile, j0 = blockIdx.y * kHpTile, split = blockIdx.z;
+    const int nk = (H + kHpK - 1) / kHpK;
+    const int c0 = split * nk / kHpSplits, c1 = (split + 1) * nk / kHpSplits;
     const int ty = tid >> 4, tx = tid & 15;
-    float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-    for (int k0 = 0; k0 < H; k0 += kHpK) {
-        for (int e = tid; e < kHpTile * kHpK; e += 256) {
-            const int rr = e / kHpK, kk = e % kHpK;
-            const int m = m0 + rr, j = j0 + rr, i = k0 + kk;
-            As[kk][rr] = (m < M && i < H) ? ld_elem<kBF16>(h, static_cast<size_t>(m) * H + i) : 0.f;
-            Bs[kk][rr] = (j < r && i < H) ? ld_elem<kBF16>(W, static_cast<size_t>(j) * ldw + col + i) : 0.f;
+    const int lr = tid >> 2, lk = (tid & 3) * 8;       // loader: row lr of the tile, k offset lk
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    const int m = m0 + lr, j = j0 + lr;
+    // chunk c's operands, loaded one chunk ahead of their use
+    auto fetch = [&](int c, float* va, float* vb) {
+        const int i0 = c * kHpK + lk;
+        const int n = H - i0;
+        if (c < c1 && m < M) load8<kBF16>(h, static_cast<size_t>(m) * H + i0, n, vec, va);
+        else for (int e = 0; e < 8; ++e) va[e] = 0.f;
+        if (c < c1 && j < r) load8<kBF16>(W, static_cast<size_t>(j) * ldw + col + i0, n, vec, vb);
+        else for (int e = 0; e < 8; ++e) vb[e] = 0.f;
+    };
+    float va[8], vb[8];
+    fetch(c0, va, vb);
+    for (int c = c0; c < c1; ++c) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            As[lk + e][lr] = va[e];
+            Bs[lk + e][lr] = vb[e];
         }
         __syncthreads();
+        fetch(c + 1, va, vb);
 #pragma unroll 8
         for (int kk = 0; kk < kHpK; ++kk) {
-            const float a0 = As[kk][2 * ty], a1 = As[kk][2 * ty + 1];
-            const float b0 = Bs[kk][2 * tx], b1 = Bs[kk][2 * tx + 1];
-            acc[0][0] = fmaf(a0, b0, acc[0][0]);
-            acc[0][1] = fmaf(a0, b1, acc[0][1]);
-            acc[1][0] = fmaf(a1, b0, acc[1][0]);
-            acc[1][1] = fmaf(a1, b1, acc[1][1]);
+            const float4 a = *reinterpret_cast<const float4*>(&As[kk][4 * ty]);
+            const float4 b = *reinterpret_cast<const float4*>(&Bs[kk][4 * tx]);
+            const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) acc[i][jj] = fmaf(av[i], bv[jj], acc[i][jj]);
         }
         __syncthreads();
     }
+    float* out = part + static_cast<size_t>(split) * M * r;
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int m = m0 + 2 * ty + i, jj = j0 + 2 * tx + j;
-            if (m < M && jj < r) out[static_cast<size_t>(m) * r + jj] = acc[i][j];
+        for (int jj = 0; jj < 4; ++jj) {
+            const int m = m0 + 4 * ty + i, j = j0 + 4 * tx + jj;
+            if (m < M && j < r) out[static_cast<size_t>(m) * r + j] = acc[i][jj];
         }
 }
+
+constexpr int kStepThreads = 512;
 
 // e_k of every request (one CTA each, one warp per output row of Wg / Wc):
 //   gated  e = sigmoid(hg + Wg[:, H:H+r] . W1[x_{k-1}]) * W1[x_{k-1}]
 //   RNN    g = sigmoid(hg + Wg[:, 0:r] . s + Wg[:, r:2r] . W1[x_{k-1}]),
 //          s' = g * s + (1 - g) * tanh(hc + Wc[:, 0:r] . s + Wc[:, r:2r] . W1[x_{k-1}]), e = s'
-// with s = s_{k-1} (0 at k = 1); e rounded to the dtype into E.
+// with s = s_{k-1} (0 at k = 1) and hg, hc the sums of the split-K partials (in
+// split order); e rounded to the dtype into E.
 template <bool kBF16>
-__global__ void __launch_bounds__(256)
-head_step(int kind, int B, int gamma, int V, int H, int r, int k, const void* __restrict__ W1,
+__global__ void __launch_bounds__(kStepThreads)
+head_step(int kind, int B, int gamma, int V, int H, int r, int k, int vec, const void* __restrict__ W1,
           const void* __restrict__ Wg, const void* __restrict__ Wc, const int32_t* __restrict__ x0,
           const int32_t* __restrict__ x, const float* __restrict__ hg, const float* __restrict__ hc,
           float* __restrict__ state, void* __restrict__ E, StatusBlock* st) {
     __shared__ float xr[256], sv[256], pg[256], pc[256];
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int kWarpsS = kStepThreads / 32;
     const bool rnn = (kind == DSPARK_HEAD_RNN);
     const int prev = prev_token(x0, x, b, gamma, k, V, st);
-    for (int j = tid; j < r; j += 256) {
+    for (int j = tid; j < r; j += kStepThreads) {
         xr[j] = ld_elem<kBF16>(W1, static_cast<size_t>(prev) * r + j);
         sv[j] = (rnn && k > 1) ? state[static_cast<size_t>(b) * r + j] : 0.f;
     }
     __syncthreads();
     const size_t row = static_cast<size_t>(b) * gamma + (k - 1);
+    const size_t M = static_cast<size_t>(B) * gamma;
     const size_t ldw = rnn ? static_cast<size_t>(2 * r + H) : static_cast<size_t>(H + r);
-    for (int j = warp; j < r; j += 8) {
-        float ag = 0.f, ac = 0.f;
-        const size_t wr = static_cast<size_t>(j) * ldw;
-        if (!rnn) {
-            for (int i = lane; i < r; i += 32) ag = fmaf(ld_elem<kBF16>(Wg, wr + H + i), xr[i], ag);
-        } else {
-            for (int i = lane; i < r; i += 32) {
-                ag = fmaf(ld_elem<kBF16>(Wg, wr + i), sv[i], ag);
-                ag = fmaf(ld_elem<kBF16>(Wg, wr + r + i), xr[i], ag);
-                ac = fmaf(ld_elem<kBF16>(Wc, wr + i), sv[i], ac);
-                ac = fmaf(ld_elem<kBF16>(Wc, wr + r + i), xr[i], ac);
+    if (!rnn) {
+        // rows j = warp + 16 i, their loads issued together; each lane takes elements
+        // g = 8 lane + 256 t of a row, t < ceil(r / 256)
+        constexpr int kRows = 4;
+        for (int j0 = warp; j0 < r; j0 += kWarpsS * kRows) {
+            float acc[kRows];
+#pragma unroll
+            for (int q = 0; q < kRows; ++q) acc[q] = 0.f;
+            for (int g = lane * 8; g < r; g += 256) {
+                float w8[kRows][8];
+#pragma unroll
+                for (int q = 0; q < kRows; ++q) {
+                    const int j = j0 + q * kWarpsS;
+                    if (j < r) load8<kBF16>(Wg, static_cast<size_t>(j) * ldw + H + g, r - g, vec, w8[q]);
+                }
+#pragma unroll
+                for (int q = 0; q < kRows; ++q)
+                    if (j0 + q * kWarpsS < r)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[q] = fmaf(w8[q][e], (g + e < r) ? xr[g + e] : 0.f, acc[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < kRows; ++q) {
+                const int j = j0 + q * kWarpsS;
+                const float ag = warp_sum(acc[q]);
+                if (lane == 0 && j < r) {
+                    float hs = 0.f;
+                    for (int p = 0; p < kHpSplits; ++p) hs += hg[(p * M + row) * r + j];
+                    pg[j] = ag + hs;
+                }
             }
         }
-        ag = warp_sum(ag);
-        ac = warp_sum(ac);
-        if (lane == 0) {
-            pg[j] = ag + hg[row * r + j];
-            if (rnn) pc[j] = ac + hc[row * r + j];
+    }
+    if (rnn) {
+        // rows j = warp + 16 i, two at a time: the four segments of each (Wg and Wc over
+        // s and over the W1 row) loaded together
+        constexpr int kRows = 2;
+        for (int j0 = warp; j0 < r; j0 += kWarpsS * kRows) {
+            float ag[kRows], ac[kRows];
+#pragma unroll
+            for (int q = 0; q < kRows; ++q) ag[q] = ac[q] = 0.f;
+            for (int g = lane * 8; g < r; g += 256) {
+                float w8[kRows][4][8];
+#pragma unroll
+                for (int q = 0; q < kRows; ++q) {
+                    const int j = j0 + q * kWarpsS;
+                    if (j < r) {
+                        const size_t wr = static_cast<size_t>(j) * ldw;
+                        load8<kBF16>(Wg, wr + g, r - g, vec, w8[q][0]);
+                        load8<kBF16>(Wg, wr + r + g, r - g, vec, w8[q][1]);
+                        load8<kBF16>(Wc, wr + g, r - g, vec, w8[q][2]);
+                        load8<kBF16>(Wc, wr + r + g, r - g, vec, w8[q][3]);
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < kRows; ++q)
+                    if (j0 + q * kWarpsS < r)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float s_ = (g + e < r) ? sv[g + e] : 0.f, x_ = (g + e < r) ? xr[g + e] : 0.f;
+                            ag[q] = fmaf(w8[q][1][e], x_, fmaf(w8[q][0][e], s_, ag[q]));
+                            ac[q] = fmaf(w8[q][3][e], x_, fmaf(w8[q][2][e], s_, ac[q]));
+                        }
+            }
+#pragma unroll
+            for (int q = 0; q < kRows; ++q) {
+                const int j = j0 + q * kWarpsS;
+                const float a1 = warp_sum(ag[q]), a2 = warp_sum(ac[q]);
+                if (lane == 0 && j < r) {
+                    float hs = 0.f, cs = 0.f;
+                    for (int p = 0; p < kHpSplits; ++p) {
+                        hs += hg[(p * M + row) * r + j];
+                        cs += hc[(p * M + row) * r + j];
+                    }
+                    pg[j] = a1 + hs;
+                    pc[j] = a2 + cs;
+                }
+            }
         }
     }
     __syncthreads();
-    for (int j = tid; j < r; j += 256) {
+    for (int j = tid; j < r; j += kStepThreads) {
         const float g = 1.f / (1.f + expf(-pg[j]));
         float e;
         if (!rnn) {
@@ -344,10 +445,10 @@ head_step(int kind, int B, int gamma, int V, int H, int r, int k, const void* __
 }
 
 template <bool kBF16>
-dspark_status_t launch_hproj(int M, int H, int r, int ldw, int col, const void* h, const void* W, float* out,
-                             cudaStream_t s) {
-    const dim3 grid((M + kHpTile - 1) / kHpTile, (r + kHpTile - 1) / kHpTile);
-    head_hproj<kBF16><<<grid, 256, 0, s>>>(M, H, r, ldw, col, h, W, out);
+dspark_status_t launch_hproj(int M, int H, int r, int ldw, int col, int vec, const void* h, const void* W,
+                             float* part, cudaStream_t s) {
+    const dim3 grid((M + kHpTile - 1) / kHpTile, (r + kHpTile - 1) / kHpTile, kHpSplits);
+    head_hproj<kBF16><<<grid, 256, 0, s>>>(M, H, r, ldw, col, vec, h, W, part);
     return launch_status();
 }
 
@@ -397,16 +498,19 @@ dspark_status_t draft_block_impl(int B, int gamma, int V, int H, int r, dspark_d
     const bool tcp = eng::use_tc_path(dt, r);
     const bool bf = (dt == DSPARK_BF16);
     const void* E = hd ? hd->E : nullptr;
+    // 16-byte loads of h and of the head's weight rows (bf16) when every row segment is aligned
+    const int hd_vec = hd && bf && H % 8 == 0 && r % 8 == 0 && aligned16(h) && aligned16(hd->Wg) &&
+                       (hd->Wc == nullptr || aligned16(hd->Wc));
     if (hd) {
         // the h_k products of the head's gate (and candidate) matrices, once
         const int M = B * gamma;
         const bool rnn = hd->kind == DSPARK_HEAD_RNN;
         const int ldw = rnn ? 2 * r + H : H + r, col = rnn ? 2 * r : 0;
-        dspark_status_t st = bf ? launch_hproj<true>(M, H, r, ldw, col, h, hd->Wg, hd->hg, s)
-                                : launch_hproj<false>(M, H, r, ldw, col, h, hd->Wg, hd->hg, s);
+        dspark_status_t st = bf ? launch_hproj<true>(M, H, r, ldw, col, hd_vec, h, hd->Wg, hd->hg, s)
+                                : launch_hproj<false>(M, H, r, ldw, col, hd_vec, h, hd->Wg, hd->hg, s);
         if (st == DSPARK_OK && rnn)
-            st = bf ? launch_hproj<true>(M, H, r, ldw, col, h, hd->Wc, hd->hc, s)
-                    : launch_hproj<false>(M, H, r, ldw, col, h, hd->Wc, hd->hc, s);
+            st = bf ? launch_hproj<true>(M, H, r, ldw, col, hd_vec, h, hd->Wc, hd->hc, s)
+                    : launch_hproj<false>(M, H, r, ldw, col, hd_vec, h, hd->Wc, hd->hc, s);
         if (st != DSPARK_OK) return st;
     }
     CUtensorMap map;
@@ -445,11 +549,13 @@ dspark_status_t draft_block_impl(int B, int gamma, int V, int H, int r, dspark_d
         for (int k = 1; k <= gamma; ++k) {
             if (hd) {
                 if (bf)
-                    head_step<true><<<B, 256, 0, s>>>(hd->kind, B, gamma, V, H, r, k, W1, hd->Wg, hd->Wc, x0, x,
-                                                      hd->hg, hd->hc, hd->state, hd->E, ws.status);
+                    head_step<true><<<B, kStepThreads, 0, s>>>(hd->kind, B, gamma, V, H, r, k, hd_vec, W1, hd->Wg,
+                                                               hd->Wc, x0, x, hd->hg, hd->hc, hd->state, hd->E,
+                                                               ws.status);
                 else
-                    head_step<false><<<B, 256, 0, s>>>(hd->kind, B, gamma, V, H, r, k, W1, hd->Wg, hd->Wc, x0, x,
-                                                       hd->hg, hd->hc, hd->state, hd->E, ws.status);
+                    head_step<false><<<B, kStepThreads, 0, s>>>(hd->kind, B, gamma, V, H, r, k, hd_vec, W1, hd->Wg,
+                                                                hd->Wc, x0, x, hd->hg, hd->hc, hd->state, hd->E,
+                                                                ws.status);
                 if ((stt = launch_status()) != DSPARK_OK) return stt;
             }
             if (g_timing.on) cudaEventRecord(g_timing.ev[2 * (k - 1)], s);
@@ -540,10 +646,11 @@ extern "C" dspark_status_t dspark_draft_block(int B, int gamma, int V, int H, in
 }
 
 // Workspace of dspark_draft_block_ex: dspark_draft_block's, then (gated, RNN) the
-// h_k products of Wg [B gamma][r] float, and (RNN) those of Wc and the state [B][r].
+// split-K partials of the h_k products of Wg [splits][B gamma][r] float, and (RNN)
+// those of Wc and the state [B][r].
 static size_t draft_ex_layout(int B, int gamma, int V, int r, int kind, size_t* o_hg, size_t* o_hc, size_t* o_st) {
     size_t o = round_up(dspark_draft_block_workspace_size(B, gamma, V, r), 256);
-    const size_t rows = static_cast<size_t>(B) * gamma * r * 4;
+    const size_t rows = static_cast<size_t>(kHpSplits) * B * gamma * r * 4;
     *o_hg = *o_hc = *o_st = 0;
     if (kind == DSPARK_HEAD_GATED || kind == DSPARK_HEAD_RNN) {
         *o_hg = o;
