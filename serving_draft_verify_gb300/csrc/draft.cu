@@ -242,7 +242,7 @@ struct HeadCtx {
 };
 
 constexpr int kHpTile = 64, kHpK = 32;   // 64 x 64 outputs per CTA, K in steps of 32
-constexpr int kHpSplits = 5;             // split-K partials, summed in order by head_step
+constexpr int kHpSplits = 10;            // split-K partials, summed in order by head_step
 
 // Loads 8 consecutive elements (a 16-byte bf16 group when vec) as floats; elements
 // at or past `n` read as 0.
@@ -334,18 +334,26 @@ head_step(int kind, int B, int gamma, int V, int H, int r, int k, int vec, const
           const void* __restrict__ Wg, const void* __restrict__ Wc, const int32_t* __restrict__ x0,
           const int32_t* __restrict__ x, const float* __restrict__ hg, const float* __restrict__ hc,
           float* __restrict__ state, void* __restrict__ E, StatusBlock* st) {
-    __shared__ float xr[256], sv[256], pg[256], pc[256];
+    __shared__ float xr[256], sv[256], pg[256], pc[256], hsum[256], csum[256];
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int kWarpsS = kStepThreads / 32;
     const bool rnn = (kind == DSPARK_HEAD_RNN);
     const int prev = prev_token(x0, x, b, gamma, k, V, st);
+    const size_t row = static_cast<size_t>(b) * gamma + (k - 1);
+    const size_t M = static_cast<size_t>(B) * gamma;
     for (int j = tid; j < r; j += kStepThreads) {
         xr[j] = ld_elem<kBF16>(W1, static_cast<size_t>(prev) * r + j);
         sv[j] = (rnn && k > 1) ? state[static_cast<size_t>(b) * r + j] : 0.f;
+        // the h_k products: the split-K partials summed in split order
+        float hs = 0.f, cs = 0.f;
+        for (int p = 0; p < kHpSplits; ++p) {
+            hs += hg[(p * M + row) * r + j];
+            if (rnn) cs += hc[(p * M + row) * r + j];
+        }
+        hsum[j] = hs;
+        csum[j] = cs;
     }
     __syncthreads();
-    const size_t row = static_cast<size_t>(b) * gamma + (k - 1);
-    const size_t M = static_cast<size_t>(B) * gamma;
     const size_t ldw = rnn ? static_cast<size_t>(2 * r + H) : static_cast<size_t>(H + r);
     if (!rnn) {
         // rows j = warp + 16 i, their loads issued together; each lane takes elements
@@ -372,11 +380,7 @@ head_step(int kind, int B, int gamma, int V, int H, int r, int k, int vec, const
             for (int q = 0; q < kRows; ++q) {
                 const int j = j0 + q * kWarpsS;
                 const float ag = warp_sum(acc[q]);
-                if (lane == 0 && j < r) {
-                    float hs = 0.f;
-                    for (int p = 0; p < kHpSplits; ++p) hs += hg[(p * M + row) * r + j];
-                    pg[j] = ag + hs;
-                }
+                if (lane == 0 && j < r) pg[j] = ag + hsum[j];
             }
         }
     }
@@ -416,13 +420,8 @@ head_step(int kind, int B, int gamma, int V, int H, int r, int k, int vec, const
                 const int j = j0 + q * kWarpsS;
                 const float a1 = warp_sum(ag[q]), a2 = warp_sum(ac[q]);
                 if (lane == 0 && j < r) {
-                    float hs = 0.f, cs = 0.f;
-                    for (int p = 0; p < kHpSplits; ++p) {
-                        hs += hg[(p * M + row) * r + j];
-                        cs += hc[(p * M + row) * r + j];
-                    }
-                    pg[j] = a1 + hs;
-                    pc[j] = a2 + cs;
+                    pg[j] = a1 + hsum[j];
+                    pc[j] = a2 + csum[j];
                 }
             }
         }
