@@ -38,6 +38,10 @@ WORKLOAD = ("Qwen3-8B-shaped serving round: B=64, gamma=7 (verify width 8), V=15
 FALLBACK_HBM_GBS = 6800.0
 
 
+NOMINAL_HBM_GBS = 8000.0     # the pages' roofline figure for the part
+FALLBACK_BF16_SUSTAINED_TFLOPS = 1700.0
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -45,6 +49,17 @@ def peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """Sustained dense bf16 TFLOP/s (for a kernel timed inside a long step) and its source."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops_sustained" in d:
+            return float(d["bf16_tflops_sustained"]), "measured (sustained)"
+    return FALLBACK_BF16_SUSTAINED_TFLOPS, "fallback (sustained)"
 
 
 def engine_source_hash():
@@ -275,6 +290,39 @@ def run_gpu(args):
                 "peak_kind": f"{peak_kind} (copy bandwidth)", "bytes_per_launch": int(launch_bytes),
                 "avg_launch_us": round(phase_avg * 1e3, 2), "launches_timed": len(ph), "timing": engine_timing}
 
+    # per-call device times of the round, launched directly (events between the calls,
+    # L2 flushed before each round): draft, schedule (latency) and verify with its
+    # algorithmic bytes (the scheduled target rows, plus U and t rows of rejected
+    # requests are not counted)
+    ev_ = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    call_us = [[], [], []]
+    for it_ in range(max(10, min(args.steps, 100)) + 3):
+        flush.zero_()
+        ev_[0].record(stream)
+        dsv.dspark_draft_block(inp["U"], inp["h"], inp["W1"], inp["W2"], inp["w"], 0.0, inp["x0"], T, seed,
+                               out=outd, workspace=ws_d)
+        ev_[1].record(stream)
+        dsv.dspark_schedule_prefix(outd["a"], inp["sps"], out=outs, workspace=ws_s)
+        ev_[2].record(stream)
+        dsv.dspark_verify(inp["t"], inp["U"], inp["W1"], inp["W2"], inp["x0"], outd["x"], outd["lse_d"],
+                          outd["logp_d"], outs["ell"], T, seed, out=outv, workspace=ws_v)
+        ev_[3].record(stream)
+        torch.cuda.synchronize()
+        if it_ >= 3:
+            for i_ in range(3):
+                call_us[i_].append(ev_[i_].elapsed_time(ev_[i_ + 1]) * 1e3)
+    med_ = [statistics.median(x) for x in call_us]
+    ver_bytes = int((outs["ell"].cpu().long() + 1).sum()) * V * 2
+    bias_flops = 2.0 * B * G * V * r
+    tpk, tpk_kind = tensor_peak()
+    breakdown = {"timing": "CUDA events between directly launched calls, median",
+                 "draft_us": med_[0], "schedule_us": med_[1], "verify_us": med_[2],
+                 "verify_algorithmic_bytes": ver_bytes, "verify_gbs": ver_bytes / (med_[2] * 1e-6) / 1e9,
+                 "draft_bias_tflops": bias_flops / (phase_avg * 1e-3) / 1e12,
+                 "draft_bias_frac_of_tensor_peak": bias_flops / (phase_avg * 1e-3) / 1e12 / tpk,
+                 "tensor_peak_tflops": tpk, "tensor_peak_kind": tpk_kind,
+                 "draft_frac_of_nominal_8tbs": launch_bytes / (phase_avg * 1e-3) / 1e9 / NOMINAL_HBM_GBS}
+
     # greedy round (same workload, T = 0)
     greedy_round = graphed(lambda: round_(inp, 0.0)) or (lambda: round_(inp, 0.0))
     g_times, _ = timed(greedy_round, max(3, args.steps // 2), args.warmup)
@@ -380,7 +428,8 @@ def run_gpu(args):
             "config": dict(workload_config(world), cuda_graph=use_graph),
             "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / peak, "roofline": roofline, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps, "clocks": clk,
-            "extra": {"greedy_round": greedy, "accept_rate_tv": tv, "multi_round": multi, "heads": heads_x,
+            "extra": {"greedy_round": greedy, "per_call": breakdown, "accept_rate_tv": tv, "multi_round": multi,
+                      "heads": heads_x,
                       "accepted_per_request": float(nacc.mean()), "scheduled_rows": int((ell + 1).sum())}}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, T, seed)

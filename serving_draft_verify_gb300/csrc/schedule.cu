@@ -90,18 +90,18 @@ schedule_kernel(const float* __restrict__ a, const double* __restrict__ sps, int
                 int32_t* __restrict__ ell, int32_t* __restrict__ n_sched, double* __restrict__ theta,
                 StatusBlock* status) {
     extern __shared__ __align__(16) uint8_t smem[];
-    uint32_t* key[2] = {reinterpret_cast<uint32_t*>(smem), reinterpret_cast<uint32_t*>(smem) + kMaxPairs};
-    uint16_t* val[2] = {reinterpret_cast<uint16_t*>(smem + 2 * kMaxPairs * 4),
-                        reinterpret_cast<uint16_t*>(smem + 2 * kMaxPairs * 4) + kMaxPairs};
-    uint16_t* hist = reinterpret_cast<uint16_t*>(smem + 2 * kMaxPairs * 6);   // [256][kWarps]
-    __shared__ unsigned long long wsum[3 * kWarps];
-    __shared__ int red_min[kWarps];
-    __shared__ uint32_t bad_seen;
-
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = B * gamma;
     const int R = (n + kThreads - 1) / kThreads;      // rounds per warp chunk
     const int npad = R * kThreads;
+    // shared memory (sized by the launch to npad): keys [2][npad] | values [2][npad] | hist
+    uint32_t* key[2] = {reinterpret_cast<uint32_t*>(smem), reinterpret_cast<uint32_t*>(smem) + npad};
+    uint16_t* val[2] = {reinterpret_cast<uint16_t*>(smem + 2 * npad * 4),
+                        reinterpret_cast<uint16_t*>(smem + 2 * npad * 4) + npad};
+    uint16_t* hist = reinterpret_cast<uint16_t*>(smem + 2 * npad * 6);   // [256][kWarps] (radix path)
+    __shared__ unsigned long long wsum[3 * kWarps];
+    __shared__ int red_min[kWarps];
+    __shared__ uint32_t bad_seen;
     if (tid == 0) {
         bad_seen = 0;
         status->code = 0u;                            // this call's status starts clear
@@ -131,27 +131,41 @@ schedule_kernel(const float* __restrict__ a, const double* __restrict__ sps, int
     int src = 0;
     if (n <= kThreads) {
         // 2a. up to 1024 pairs: rank by counting.  rank(i) = #{j : k_j < k_i} +
-        //     #{j < i : k_j == k_i}, a stable order; one pair per thread.
-        if (tid < n) {
-            const uint32_t ki = key[0][tid];
-            const int wbase = warp * 32;
+        //     #{j < i : k_j == k_i}, a stable order.  Each pair gets `per` threads
+        //     (as many as fit in the block, at most 8), each counting over its share
+        //     of the keys in groups of four; the partial counts meet in shared memory.
+        int* rk = reinterpret_cast<int*>(hist);          // [n] ranks (the radix histogram is unused here)
+        const int per = min(8, kThreads / n);
+        const int i = tid % n, part = tid / n;
+        for (int e = tid; e < n; e += kThreads) rk[e] = 0;
+        __syncthreads();
+        if (part < per) {
+            const uint32_t ki = key[0][i];
             const int n4 = (n + 3) / 4;                   // keys past n are ~0: never counted
+            const int j0 = part * n4 / per, j1 = (part + 1) * n4 / per;
             const uint4* k4 = reinterpret_cast<const uint4*>(key[0]);
+            // groups wholly before the 32 keys around i (j < i: count k_j <= k_i), those
+            // wholly after them (j > i: count k_j < k_i), and the eight groups in between
+            const int ib = i & ~31;
             int rank = 0;
-            for (int j4 = 0; j4 < wbase / 4; ++j4) {      // j < tid: count k_j <= k_i
+            for (int j4 = j0; j4 < min(j1, ib / 4); ++j4) {
                 const uint4 q = k4[j4];
                 rank += (q.x <= ki) + (q.y <= ki) + (q.z <= ki) + (q.w <= ki);
             }
-            for (int j = wbase; j < wbase + 32 && j < n; ++j) {
+            for (int j = 4 * max(j0, ib / 4); j < 4 * min(j1, (ib + 32) / 4) && j < n; ++j) {
                 const uint32_t kj = key[0][j];
-                rank += (kj < ki) || (kj == ki && j < tid);
+                rank += (kj < ki) || (kj == ki && j < i);
             }
-            for (int j4 = (wbase + 32) / 4; j4 < n4; ++j4) {   // j > tid: count k_j < k_i
+            for (int j4 = max(j0, (ib + 32) / 4); j4 < j1; ++j4) {
                 const uint4 q = k4[j4];
                 rank += (q.x < ki) + (q.y < ki) + (q.z < ki) + (q.w < ki);
             }
-            key[1][rank] = ki;
-            val[1][rank] = static_cast<uint16_t>(tid);
+            atomicAdd(&rk[i], rank);
+        }
+        __syncthreads();
+        if (tid < n) {
+            key[1][rk[tid]] = key[0][tid];
+            val[1][rk[tid]] = static_cast<uint16_t>(tid);
         }
         src = 1;
         __syncthreads();
@@ -315,7 +329,12 @@ schedule_kernel(const float* __restrict__ a, const double* __restrict__ sps, int
     for (int b = tid; b < B; b += kThreads) ell[b] = cnt[b];
 }
 
-constexpr size_t kSmem = 2 * kMaxPairs * 4 + 2 * kMaxPairs * 2 + 256 * kWarps * 2;
+// Shared memory for npad padded pairs: keys and values double-buffered, the radix
+// histogram (or the ranks of the counting path).
+constexpr size_t smem_bytes(int npad) {
+    return 2 * static_cast<size_t>(npad) * 4 + 2 * static_cast<size_t>(npad) * 2 + 256 * kWarps * 2;
+}
+constexpr size_t kSmem = smem_bytes(kMaxPairs);
 
 }  // namespace
 }  // namespace dspark
@@ -345,7 +364,8 @@ extern "C" dspark_status_t dspark_schedule_prefix(int B, int gamma, const float*
                                         static_cast<int>(kSmem));
         }) != cudaSuccess)
         return DSPARK_ERR_CUDA;
-    schedule_kernel<<<1, kThreads, kSmem, s>>>(a, sps, B, gamma, ell, n_sched, theta,
-                                                 static_cast<StatusBlock*>(workspace));
+    const int npad = (B * gamma + kThreads - 1) / kThreads * kThreads;
+    schedule_kernel<<<1, kThreads, smem_bytes(npad), s>>>(a, sps, B, gamma, ell, n_sched, theta,
+                                                          static_cast<StatusBlock*>(workspace));
     return launch_status();
 }
