@@ -93,3 +93,32 @@ def test_markov_kind_is_the_plain_call(dsv):
     b = dsv.dspark_draft_block_ex(g["U"], g["h"], g["W1"], g["W2"], g["w"], 0.0, g["x0"], 0.7, 4, dict(kind=0))
     for k in ("x", "lse_d", "logp_d", "c", "a"):
         assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("kind", [1, 2], ids=["gated", "rnn"])
+def test_heads_full_qwen3_size_sampled_requests(dsv, kind):
+    """B = 64, gamma = 7, V = 151936, H = 4096, r = 256, bf16, T = 0.7: four sampled
+    requests against the teacher-forced oracle (each keyed by its own index)."""
+    cfg = wl.QWEN3_8B
+    inp = wl.make_draft_inputs(cfg, device="cuda")
+    Wg, Wc = wl.make_head_weights(cfg, kind, device="cuda")
+    out = dsv.dspark_draft_block_ex(inp["U"], inp["h"], inp["W1"], inp["W2"], inp["w"], 0.0, inp["x0"],
+                                    cfg.temperature, cfg.seed, dict(kind=kind, Wg=Wg, Wc=Wc))
+    torch.cuda.synchronize()
+    rows = np.array([0, 17, 40, 63])
+    idx = torch.from_numpy(rows).cuda()
+    gx = npy(out["x"])
+    head = oheads.Head(kind, Wg=wl.to_f64(Wg), Wc=None if Wc is None else wl.to_f64(Wc), bf16=True)
+    ref = oracle.draft_block(wl.to_f64(inp["U"][idx]), wl.to_f64(inp["h"][idx]), wl.to_f64(inp["W1"]),
+                             wl.to_f64(inp["W2"]), wl.to_f64(inp["w"]), 0.0, npy(inp["x0"])[rows], cfg.temperature,
+                             cfg.seed, forced_tokens=gx[rows], requests=rows, head=head)
+    gE = wl.to_f64(out["E"][idx])
+    mag = np.maximum(np.abs(gE), np.abs(ref["E"]))
+    assert np.all(np.abs(gE - ref["E"]) <= np.exp2(np.floor(np.log2(np.maximum(mag, 1e-30))) - 7))
+    exempt = ref["margin"] < MARGIN
+    assert not ((gx[rows] != ref["x"]) & ~exempt).any()
+    same = gx[rows] == ref["x"]
+    for k in ("c", "a"):
+        assert np.abs(npy(out[k])[rows] - ref[k]).max() <= FTOL["bf16"], k
+    for k in ("lse_d", "logp_d"):
+        assert np.abs(npy(out[k])[rows] - ref[k])[same].max(initial=0.0) <= FTOL["bf16"], k

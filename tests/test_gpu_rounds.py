@@ -112,3 +112,39 @@ def test_rounds_zero_and_pool_of_one(dsv):
     got, final = _run(dsv, g, 3, 1.0, 5, trace=True)
     assert np.all(got["n_emitted"] >= 1) and np.all(got["n_emitted"] <= cfg.gamma + 1)
     assert np.array_equal(final, got["next_token"][2])
+
+
+def test_rounds_full_qwen3_size_sampled_requests(dsv):
+    """Two rounds of the Qwen3-8B-shaped workload (B = 64, V = 151936, bf16, T = 0.7, pool of
+    2): four sampled requests of each round against the teacher-forced oracle, and the whole
+    batch's bookkeeping exactly."""
+    cfg = wl.QWEN3_8B
+    g = wl.make_round_pool(cfg, 2, device="cuda")
+    R, T = 2, cfg.temperature
+    anchor = g["x0"].clone()
+    out = dsv.dspark_decode_rounds(g["U"], g["h"], g["t"], g["W1"], g["W2"], g["w"], 0.0, g["sps"], anchor, R, T,
+                                   cfg.seed, trace=True)
+    torch.cuda.synchronize()
+    got = {k: npy(v) for k, v in out.items()}
+    rows = np.array([0, 21, 42, 63])
+    idx = torch.from_numpy(rows).cuda()
+    anchors = [npy(g["x0"])] + [got["next_token"][i] for i in range(R - 1)]
+    W1, W2, w = wl.to_f64(g["W1"]), wl.to_f64(g["W2"]), wl.to_f64(g["w"])
+    for i in range(R):
+        s = orounds.round_seed(cfg.seed, i)
+        U = wl.to_f64(g["U"][i][idx])
+        d = oracle.draft_block(U, wl.to_f64(g["h"][i][idx]), W1, W2, w, 0.0, anchors[i][rows], T, s,
+                               forced_tokens=got["x"][i][rows], requests=rows)
+        assert not ((got["x"][i][rows] != d["x"]) & ~(d["margin"] < MARGIN)).any(), ("round", i)
+        assert np.abs(got["a"][i][rows] - d["a"]).max() <= FTOL["bf16"]
+        # the scheduler over the whole batch, on the GPU's survivals: exact
+        ell, _, _ = oracle.schedule_prefix(got["a"][i], npy(g["sps"]))
+        assert np.array_equal(ell, got["ell"][i]), ("round", i, "ell")
+        v = oracle.verify_round(wl.to_f64(g["t"][i][idx]), U, W1, W2, anchors[i][rows], got["x"][i][rows],
+                                got["lse_d"][i][rows], got["logp_d"][i][rows], ell[rows], T, s, requests=rows)
+        bad = ((got["n_accept"][i][rows] != v["n_accept"]) | (got["next_token"][i][rows] != v["next_token"])) \
+            & ~(v["margin"] < MARGIN)
+        assert not bad.any(), ("round", i, "verify")
+        tok = orounds.emitted_tokens(got["x"][i], got["n_accept"][i], got["next_token"][i])
+        assert np.array_equal(got["tokens"][i], tok)
+    assert np.array_equal(npy(anchor), got["next_token"][R - 1])
