@@ -176,7 +176,11 @@ dspark_status_t dspark_schedule_prefix(int B, int gamma, const float* a, const d
  * round).  temperature == 0: accept iff x_k == argmax t_k, next_token =
  * argmax t at the stop row.
  *
- *   t_logits [B][gamma+1][V], U [B][gamma][V], W1/W2 [V][r] in `dt`;
+ *   t_logits [B][gamma+1][V], U [B][gamma][V], W1/W2 [V][r] in `dt`.
+ *   t_logits may also point to pinned (page-locked, registered) host memory:
+ *   the kernels then read only the rows verification needs, the scheduled
+ *   prefix and its stop row, over the host link.  Unregistered host memory
+ *   returns DSPARK_ERR_INVALID_ARGUMENT;
  *   x0 [B], x [B][gamma] int32; lse_d, logp_d [B][gamma] float32 (from the
  *   draft); ell [B] int32 in 0..gamma.
  *   Outputs: n_accept [B] int32 in 0..ell[b]; next_token [B] int32.  The

@@ -116,9 +116,9 @@ def _check(name, status):
         raise DSparkError(name, status)
 
 
-def _need(t, shape, dtype=None, name="tensor"):
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+def _need(t, shape, dtype=None, name="tensor", host_ok=False):
+    if not t.is_cuda and not (host_ok and t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor" + (" or pinned host memory" if host_ok else ""))
     if tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
     if dtype is not None and t.dtype != dtype:
@@ -384,11 +384,13 @@ def dspark_schedule_prefix(a, sps, out=None, workspace=None, stream=None):
 
 def dspark_verify(t_logits, U, W1, W2, x0, x, lse_d, logp_d, ell, temperature, seed, out=None,
                   workspace=None, stream=None):
-    """Verification; returns dict n_accept [B], next_token [B] (int32)."""
+    """Verification; returns dict n_accept [B], next_token [B] (int32).  t_logits may be a
+    pinned host tensor: the kernels then read the rows verification needs (the scheduled
+    prefix and its bonus row) over the host link, and no others."""
     lib = load()
     B, G, V = U.shape
     r = W1.shape[-1]
-    _need(t_logits, (B, G + 1, V), U.dtype, name="t_logits")
+    _need(t_logits, (B, G + 1, V), U.dtype, name="t_logits", host_ok=True)
     _need(U, (B, G, V), name="U")
     _need(W1, (V, r), U.dtype, name="W1")
     _need(W2, (V, r), U.dtype, name="W2")
@@ -458,11 +460,11 @@ def phase_times():
 def dspark_verify_ex(t_logits, U, W1, W2, x0, x, lse_d, logp_d, ell, temperature, seed, head, out=None,
                      workspace=None, stream=None):
     """Verification of a draft made with a sequential head: head = dict(kind, E)
-    where E [B, gamma, r] holds the rows the draft's bias used."""
+    where E [B, gamma, r] holds the rows the draft's bias used (t_logits as for dspark_verify)."""
     lib = load()
     B, G, V = U.shape
     r = W1.shape[-1]
-    _need(t_logits, (B, G + 1, V), U.dtype, name="t_logits")
+    _need(t_logits, (B, G + 1, V), U.dtype, name="t_logits", host_ok=True)
     _need(U, (B, G, V), name="U")
     _need(W1, (V, r), U.dtype, name="W1")
     _need(W2, (V, r), U.dtype, name="W2")

@@ -119,3 +119,22 @@ def test_verify_full_size_sampled(dsv, key, temperature, nrows):
     assert np.all((gv["n_accept"] >= 0) & (gv["n_accept"] <= ell))
     del inp
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("temperature", [None, 0.0])
+def test_verify_reads_target_rows_from_pinned_host_memory(dsv, temperature):
+    """t_logits in pinned host memory: the same outputs, bit for bit, as from device memory."""
+    cfg = wl.scaled(wl.QWEN3_8B, B=32, V=8192, H=64)
+    inp = wl.make_draft_inputs(cfg)
+    d = gpu_draft(dsv, inp, temperature=temperature)
+    T = cfg.temperature if temperature is None else temperature
+    g = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    rng = np.random.default_rng(3)
+    ell = torch.as_tensor(rng.integers(0, cfg.gamma + 1, cfg.B), dtype=torch.int32).cuda()
+    a = dsv.dspark_verify(g["t"], g["U"], g["W1"], g["W2"], g["x0"], d["x"], d["lse_d"], d["logp_d"], ell, T,
+                          cfg.seed)
+    t_host = inp["t"].clone().pin_memory()
+    b = dsv.dspark_verify(t_host, g["U"], g["W1"], g["W2"], g["x0"], d["x"], d["lse_d"], d["logp_d"], ell, T,
+                          cfg.seed)
+    torch.cuda.synchronize()
+    assert torch.equal(a["n_accept"], b["n_accept"]) and torch.equal(a["next_token"], b["next_token"])
