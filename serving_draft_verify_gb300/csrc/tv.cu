@@ -4,7 +4,7 @@
 // and dspark_training_loss (section 7.2, `compute_dspark_loss`), the same pass
 // extended to the joint loss and its gradient.
 //
-// One HBM pass per row.  A thread-block cluster of cs CTAs of 512 threads (cs the
+// One HBM pass per row.  A thread-block cluster of cs CTAs of 640 threads (cs the
 // smallest of 1, 2, 4, 8, 16 whose slices fit; 4 for bf16 rows of the Qwen3
 // vocabulary) owns one row at a time; each CTA bulk-copies its 1/cs slice of d
 // and t into shared memory.  Slices stream through three slots in the order d_0,
@@ -31,10 +31,10 @@ namespace dspark {
 namespace {
 
 constexpr int kMaxCS = 16;      // CTAs per cluster at most (one row per cluster)
-constexpr int kThreads = 512;
+constexpr int kThreads = 640;
 constexpr int kWarps = kThreads / 32;
 constexpr int kSlots = 3;       // slice slots: d_i, t_i and d_{i+1} resident at once
-constexpr int kGMax = 10;       // 16-byte groups per thread and slice (a slot holds at most 10 x 512 x 16 B)
+constexpr int kGMax = 8;        // 16-byte groups per thread and slice (a slot holds at most 8 x 640 x 16 B)
 constexpr size_t kSmemCap = 227 * 1024;
 
 template <bool kBF16>
