@@ -285,6 +285,7 @@ dspark_status_t dspark_verify_ex(int B, int gamma, int V, int r, dspark_dtype_t 
  *
  *   U [pool][B][gamma][V], h [pool][B][gamma][H], t_logits [pool][B][gamma+1][V],
  *   W1/W2 [V][r], w [H + r] in `dt`; sps as for dspark_schedule_prefix.
+ *   t_logits may be pinned host memory, as for dspark_verify.
  *   anchor [B] int32: in, the first round's anchors; out, the last emitted tokens.
  *   Outputs: tokens [rounds][B][gamma+1] int32 (emitted tokens, then -1);
  *   n_emitted [rounds][B] int32 (n_accept + 1); stats [rounds][2] double:

@@ -215,7 +215,7 @@ def dspark_decode_rounds(U, h, t, W1, W2, w, bias, sps, anchor, rounds, temperat
     r = W1.shape[-1]
     _need(U, (P, B, G, V), name="U")
     _need(h, (P, B, G, H), U.dtype, name="h")
-    _need(t, (P, B, G + 1, V), U.dtype, name="t")
+    _need(t, (P, B, G + 1, V), U.dtype, name="t", host_ok=True)   # pinned host: rows read in place
     _need(W1, (V, r), U.dtype, name="W1")
     _need(W2, (V, r), U.dtype, name="W2")
     _need(w, (H + r,), U.dtype, name="w")

@@ -148,3 +148,18 @@ def test_rounds_full_qwen3_size_sampled_requests(dsv):
         tok = orounds.emitted_tokens(got["x"][i], got["n_accept"][i], got["next_token"][i])
         assert np.array_equal(got["tokens"][i], tok)
     assert np.array_equal(npy(anchor), got["next_token"][R - 1])
+
+
+def test_rounds_with_target_logits_in_pinned_host_memory(dsv):
+    """The target-logit pool in pinned host memory: bit-identical rounds."""
+    cfg = wl.scaled(wl.QWEN3_8B, B=16, V=4096, H=64)
+    g = wl.make_round_pool(cfg, 2)
+    cu = {k: g[k].cuda() for k in ("U", "h", "t", "W1", "W2", "w", "sps")}
+    outs = []
+    for t in (cu["t"], g["t"].clone().pin_memory()):
+        anchor = g["x0"].clone().cuda()
+        o = dsv.dspark_decode_rounds(cu["U"], cu["h"], t, cu["W1"], cu["W2"], cu["w"], 0.0, cu["sps"], anchor, 3,
+                                     0.7, 99)
+        torch.cuda.synchronize()
+        outs.append((npy(o["tokens"]), npy(anchor)))
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
