@@ -119,10 +119,7 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 struct U4 {
     uint32_t x, y, z, w;
 };
-// Out of line (one copy per module): the tile epilogues call it for every tile, so
-// its code stays in the instruction caches for the token draws that follow a
-// vocabulary-wide stream (inlined copies there were fetched cold from DRAM).
-static __device__ __noinline__ U4 philox4x32_10(U4 c, uint32_t k0, uint32_t k1) {
+__device__ __forceinline__ U4 philox4x32_10_inline(U4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
     for (int i = 0; i < 10; ++i) {
         const uint32_t lo0 = 0xD2511F53u * c.x;
@@ -134,6 +131,13 @@ static __device__ __noinline__ U4 philox4x32_10(U4 c, uint32_t k0, uint32_t k1) 
         k1 += 0xBB67AE85u;
     }
     return c;
+}
+// Out of line (one copy per module): the draft engine's tile epilogues call it for
+// every tile, so its code stays in the instruction caches for the token draws that
+// follow a vocabulary-wide stream (inlined copies there were fetched cold from DRAM).
+// Kernels without that pattern (the verify rows pass) call the inline form.
+static __device__ __noinline__ U4 philox4x32_10(U4 c, uint32_t k0, uint32_t k1) {
+    return philox4x32_10_inline(c, k0, k1);
 }
 enum Stream : uint32_t {
     kStreamDraftToken = 0,
@@ -162,11 +166,12 @@ __device__ __forceinline__ float uniform_accept(uint32_t w) {
 }
 // Standard Gumbel variate -ln(-ln u).  For u near 1, -ln u is formed as
 // -log1p(u - 1) (u - 1 is exact there) to keep its relative accuracy.
-// Out of line for the same reason as philox4x32_10.
-static __device__ __noinline__ float gumbel_of(float u) {
+__device__ __forceinline__ float gumbel_of_inline(float u) {
     const float e = (u > 0.5f) ? -log1pf(u - 1.0f) : -logf(u);
     return -logf(e);
 }
+// Out of line for the same reason as philox4x32_10.
+static __device__ __noinline__ float gumbel_of(float u) { return gumbel_of_inline(u); }
 
 // ------------------------------------------------------------ reductions ---
 __device__ __forceinline__ float warp_max(float v) {

@@ -389,7 +389,7 @@ verify_rows(int gamma, int V, const void* __restrict__ t, const int32_t* __restr
                 // lane (sub, part < 4) finishes block (quad q0 + part, sub): its Philox
                 // counter is that quad's, its word the block's
                 const int pu = part & 3;
-                const U4 pw = philox4x32_10(U4{static_cast<uint32_t>(q0 + pu), static_cast<uint32_t>(k),
+                const U4 pw = philox4x32_10_inline(U4{static_cast<uint32_t>(q0 + pu), static_cast<uint32_t>(k),
                                                static_cast<uint32_t>(b), kStreamTargetBlock},
                                             static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
                 const uint32_t word = sub == 0 ? pw.x : sub == 1 ? pw.y : sub == 2 ? pw.z : pw.w;
@@ -397,7 +397,7 @@ verify_rows(int gamma, int V, const void* __restrict__ t, const int32_t* __restr
                 const float sum = pu == 0 ? sq[0] : pu == 1 ? sq[1] : pu == 2 ? sq[2] : sq[3];
                 const int blk = (q0 + pu) * 4 + sub;
                 if (part < 4 && blk < hi && sum > 0.f) {
-                    const float key = (m + log2f(sum)) * kLn2 + gumbel_of(uniform_open(word));
+                    const float key = (m + log2f(sum)) * kLn2 + gumbel_of_inline(uniform_open(word));
                     if (key > best || (key == best && blk < best_i)) { best = key; best_i = blk; }
                     lse_merge(M, S, m, sum);
                 }
