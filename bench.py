@@ -387,8 +387,8 @@ def run_gpu(args):
         return t0.elapsed_time(t1)
 
     e2e_run(args.warmup)
-    e_ms = e2e_run(args.steps)
-    e2e = {"value": B * G * args.steps * world / (e_ms * 1e-3), "unit": "rows/s",
+    e_ms, e_rows = aggregate(e2e_run(args.steps), B * G * args.steps, world, dev)   # slowest rank, all rows
+    e2e = {"value": e_rows / (e_ms * 1e-3), "unit": "rows/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "pipelined": "step i+1's upload overlaps step i's round (two device input sets)",
            "target_rows": "read by verification from pinned host memory (the scheduled rows only)",
