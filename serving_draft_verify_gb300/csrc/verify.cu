@@ -275,8 +275,28 @@ __device__ __noinline__ void decide_row(int n, int row, int b, int k, int gamma,
 // consecutive blocks per step, 8 lanes per block, 8 logits per lane.  Per
 // 64-token block: the logsumexp of t / T and a Gumbel key for a draw from p_t
 // (greedy: the argmax of t); per piece the CTA's best and its (max, sum).
-// Sixteen lanes finish the 16 blocks of a step, one block each.
+// Sixteen lanes finish the 16 blocks of a step, one block each.  The Philox
+// words of a block key come one step early from the other sixteen lanes: every
+// second step runs one Philox sequence for two steps' quads.
 constexpr int kRowsCtasPerSm = 3;
+
+// Two float32 lanes in one 64-bit register (Blackwell f32x2 arithmetic); each
+// lane of fma2 is one fused multiply-add with a single rounding, as fmaf.
+__device__ __forceinline__ unsigned long long pk2(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 upk2(unsigned long long v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
 
 template <bool kBF16>
 __global__ void __launch_bounds__(256, kRowsCtasPerSm)
@@ -315,7 +335,9 @@ verify_rows(int gamma, int V, const void* __restrict__ t, const int32_t* __restr
             int best_i = 0x7FFFFFFF;
             // each warp takes 4 consecutive quads per step; all loads of a step are issued first
             constexpr int kU = 4;
-            for (int q0 = lo / 4 + warp * kU; q0 * 4 < hi; q0 += 8 * kU) {
+            int step = 0;                                 // this warp's steps in the piece
+            uint32_t next_word = 0u;                      // lanes part >= 4: the next step's Philox word
+            for (int q0 = lo / 4 + warp * kU; q0 * 4 < hi; q0 += 8 * kU, ++step) {
                 float y[kU][8];
 #pragma unroll
                 for (int u = 0; u < kU; ++u) {
@@ -377,8 +399,13 @@ verify_rows(int gamma, int V, const void* __restrict__ t, const int32_t* __restr
                     const float mc = m * cscale;
                     float sum = 0.f;
                     if (m > -INFINITY) {
+                        const unsigned long long c2 = pk2(cscale, cscale), nm2 = pk2(-mc, -mc);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) sum += fast_exp2(fmaf(y[u][i], cscale, -mc));
+                        for (int i = 0; i < 8; i += 2) {
+                            const float2 z = upk2(fma2(pk2(y[u][i], y[u][i + 1]), c2, nm2));
+                            sum += fast_exp2(z.x);
+                            sum += fast_exp2(z.y);
+                        }
                     }
                     sum += __shfl_xor_sync(0xffffffffu, sum, 1);
                     sum += __shfl_xor_sync(0xffffffffu, sum, 2);
@@ -387,12 +414,21 @@ verify_rows(int gamma, int V, const void* __restrict__ t, const int32_t* __restr
                     sq[u] = sum;
                 }
                 // lane (sub, part < 4) finishes block (quad q0 + part, sub): its Philox
-                // counter is that quad's, its word the block's
+                // counter is that quad's, its word the block's.  On even steps lane
+                // (sub, part + 4) draws the word of the same block of the next step
+                // (quad q0 + 8 kU + part) and hands it down four lanes a step later.
                 const int pu = part & 3;
-                const U4 pw = philox4x32_10_inline(U4{static_cast<uint32_t>(q0 + pu), static_cast<uint32_t>(k),
-                                               static_cast<uint32_t>(b), kStreamTargetBlock},
-                                            static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
-                const uint32_t word = sub == 0 ? pw.x : sub == 1 ? pw.y : sub == 2 ? pw.z : pw.w;
+                uint32_t word;
+                if ((step & 1) == 0) {
+                    const int qp = q0 + pu + (part >= 4 ? 8 * kU : 0);
+                    const U4 pw = philox4x32_10_inline(U4{static_cast<uint32_t>(qp), static_cast<uint32_t>(k),
+                                                          static_cast<uint32_t>(b), kStreamTargetBlock},
+                                                       static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+                    word = sub == 0 ? pw.x : sub == 1 ? pw.y : sub == 2 ? pw.z : pw.w;
+                    next_word = word;
+                } else {
+                    word = __shfl_down_sync(0xffffffffu, next_word, 4);
+                }
                 const float m = pu == 0 ? mq[0] : pu == 1 ? mq[1] : pu == 2 ? mq[2] : mq[3];
                 const float sum = pu == 0 ? sq[0] : pu == 1 ? sq[1] : pu == 2 ? sq[2] : sq[3];
                 const int blk = (q0 + pu) * 4 + sub;
