@@ -6,6 +6,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/dspark.h"
@@ -16,21 +17,22 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Current device and its SM count (cached per device).
+// Current device and its SM count (cached per device; calls from several host
+// threads may fill an entry at once, all with the same value).
 inline int current_device() {
     int dev = 0;
     cudaGetDevice(&dev);
     return dev;
 }
 inline int sm_count(int dev) {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64];                    // static storage: starts at 0
     if (dev < 0 || dev >= 64) return 0;
-    if (cache[dev] == 0) {
-        int n = 0;
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cache[dev] = n;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
 }
 
 // Launch-error check mapped to a status.
