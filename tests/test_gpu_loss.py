@@ -1,7 +1,7 @@
 """GPU parity of dspark_training_loss against the oracle (float64 loss and
 gradient).
 
-Tolerances (spec bar: 2e-3 for bf16 inputs, 1e-5 for fp32), applied
+Tolerances (the parity bar: 2e-3 for bf16 inputs, 1e-5 for fp32), applied
 relative to each quantity's scale: ce and the row totals relative to
 max(1, |value|); c*, bce and grad_conf absolute; grad_d element-wise against
 the element's own terms, omega (a_ce (p_d + [v = target]) + a_l1 p_d), with

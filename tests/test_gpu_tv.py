@@ -1,6 +1,6 @@
 """GPU parity of dspark_accept_rate_tv against the oracle (float64 c*).
 
-Tolerance (spec bar): 2e-3 absolute for bf16 inputs, 1e-5 for fp32.
+Tolerance (the parity bar): 2e-3 absolute for bf16 inputs, 1e-5 for fp32.
 The kernel sums fp32 terms, so it is also held to a tighter 1e-4 / 2e-6 that
 documents its expected accuracy."""
 import numpy as np
