@@ -70,3 +70,58 @@ def test_host_checks_reject_before_launch(lib):
     assert g(0, 7, fake, fake, fake, fake, fake, fake, 256, None) == 1        # B = 0
     assert g(4, 33, fake, fake, fake, fake, fake, fake, 256, None) == 1       # gamma > 32
     assert g(1024, 17, fake, fake, fake, fake, fake, fake, 256, None) == 2    # more than 16384 pairs
+
+
+def test_host_checks_of_the_other_entry_points(lib):
+    # only arguments each entry point rejects in its first checks, before any CUDA call
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    i, f32, u64, sz = ctypes.c_int, ctypes.c_float, ctypes.c_uint64, ctypes.c_size_t
+
+    d = lib.dspark_draft_block
+    d.restype = i
+    d.argtypes = [i] * 6 + [P] * 5 + [f32, P, f32, u64] + [P] * 6 + [sz, P]
+
+    def draft(B=4, G=7, V=64, H=8, r=16, dt=1, T=1.0):
+        return d(B, G, V, H, r, dt, fake, fake, fake, fake, fake, 0.0, fake, T, 1,
+                 fake, fake, fake, fake, fake, fake, 1 << 30, None)
+    assert draft(B=0) == 1 and draft(B=65536) == 1
+    assert draft(G=0) == 1 and draft(G=33) == 1
+    assert draft(r=264) == 1 and draft(r=12) == 1               # r > 256, r % 8 != 0
+    assert draft(dt=7) == 1
+    assert draft(T=-1.0) == 1 and draft(T=float("nan")) == 1 and draft(T=float("inf")) == 1
+    assert draft(V=60) == 1                                     # bf16 rows need V % 8 == 0
+
+    v = lib.dspark_verify
+    v.restype = i
+    v.argtypes = [i] * 5 + [P] * 9 + [f32, u64] + [P] * 3 + [sz, P]
+
+    def verify(B=4, G=7, V=64, r=16, dt=1, T=1.0):
+        return v(B, G, V, r, dt, fake, fake, fake, fake, fake, fake, fake, fake, fake, T, 1,
+                 fake, fake, fake, 1 << 30, None)
+    assert verify(B=0) == 1 and verify(G=33) == 1 and verify(r=12) == 1 and verify(dt=7) == 1
+    assert verify(B=65535, G=1) == 2                            # more than 65535 target rows
+    assert verify(T=-0.5) == 1 and verify(V=60) == 1
+
+    lo = lib.dspark_training_loss
+    lo.restype = i
+    lo.argtypes = [ctypes.c_int64, i, i] + [P] * 5 + [f32] * 3 + [P] * 5 + [sz, P]
+
+    def loss(rows=4, V=64, dt=1, ws=fake, ws_bytes=1 << 20, out=fake):
+        return lo(rows, V, dt, fake, fake, fake, fake, fake, 0.1, 0.9, 1.0, fake, out, None, None,
+                  ws, ws_bytes, None)
+    assert loss(rows=-1) == 1 and loss(V=60) == 1 and loss(dt=7) == 1
+    assert loss(ws=None) == 1 and loss(ws=P(0x1010)) == 1        # workspace missing / not 256-byte aligned
+    assert loss(ws_bytes=16) == 3
+    assert loss(out=None) == 1                                  # no loss output
+    assert loss(V=163848) == 2
+
+    r = lib.dspark_decode_rounds
+    r.restype = i
+    r.argtypes = [i] * 8 + [P] * 6 + [f32, P, P, f32, u64] + [P] * 5 + [sz, P]
+
+    def rounds(n=2, pool=1, B=4, G=7, dt=1):
+        return r(n, pool, B, G, 64, 8, 16, dt, fake, fake, fake, fake, fake, fake, 0.0, fake, fake, 1.0, 1,
+                 fake, fake, fake, None, fake, 1 << 30, None)
+    assert rounds(n=-1) == 1 and rounds(pool=0) == 1 and rounds(B=0) == 1 and rounds(G=0) == 1
+    assert rounds(dt=7) == 1
