@@ -179,3 +179,15 @@ def test_heads_gate_on_the_next_hidden_state_is_caught(monkeypatch):
     orig = Hd.Head.step
     monkeypatch.setattr(Hd.Head, "step", lambda self, W1p, hk, st: orig(self, W1p, np.roll(hk, 1, axis=0), st))
     assert _fails(T_heads.test_gate_reads_h_of_its_own_position)
+
+
+def test_residual_rebuilt_from_the_wrong_previous_token_is_caught(monkeypatch):
+    # the rejected row's draft logits rebuilt with x_k in place of x_{k-1} (for k = 1: x_1, not the anchor)
+    import oracle.verify as V
+    orig = V.draft_logits
+
+    def bad(U, W1, W2, x0, tokens, b, k, E=None):
+        t = np.asarray(tokens)
+        return orig(U, W1, W2, t[:, 0], t, b, k, E=E)
+    monkeypatch.setattr(V, "draft_logits", bad)
+    assert _fails(T_verify.test_token_after_a_rejection_follows_the_residual)

@@ -58,6 +58,21 @@ def test_first_emitted_token_follows_target():
     assert abs(acc - cstar) < 4.5 * np.sqrt(cstar * (1 - cstar) / R)
 
 
+def test_token_after_a_rejection_follows_the_residual():
+    """Given a rejection at position 1, the emitted token follows the residual
+    law norm(max(0, p_t - p_d)) of the rejection sampler, in closed form here."""
+    R, V, G, r, T = 60000, 70, 3, 8, 1.0
+    U1, t1, W1, W2, d, out = _round(R, V, G, r, T, seed=11, ell=G)
+    rej = out["n_accept"] == 0
+    p_t = _softmax(t1[0] / T)
+    p_d = _softmax((U1[0] + W2 @ W1[3]) / T)
+    q = np.maximum(0.0, p_t - p_d)
+    assert rej.sum() > 5000
+    assert _chi2_p(out["next_token"][rej], q / q.sum()) > 1e-3
+    # the sample has the power to tell the residual from p_t itself
+    assert _chi2_p(out["next_token"][rej], p_t) < 1e-6
+
+
 def test_second_token_follows_target_given_first_accepted():
     R, V, G, r, T = 80000, 40, 3, 8, 0.9
     U1, t1, W1, W2, d, out = _round(R, V, G, r, T, seed=5, ell=G, rng_seed=1)
