@@ -191,3 +191,11 @@ def test_residual_rebuilt_from_the_wrong_previous_token_is_caught(monkeypatch):
         return orig(U, W1, W2, t[:, 0], t, b, k, E=E)
     monkeypatch.setattr(V, "draft_logits", bad)
     assert _fails(T_verify.test_token_after_a_rejection_follows_the_residual)
+
+
+def test_temperature_on_the_base_logits_only_is_caught(monkeypatch):
+    # l = U / T + B instead of (U + B) / T: the bias scaled by T before the division
+    orig = draft.markov_bias
+    T = 0.8                                                   # the strong-bias test's temperature
+    monkeypatch.setattr(draft, "markov_bias", lambda W1, W2, prev: T * orig(W1, W2, prev))
+    assert _fails(T_draft.test_draft_sample_distribution_with_strong_bias)
