@@ -199,3 +199,28 @@ def test_temperature_on_the_base_logits_only_is_caught(monkeypatch):
     T = 0.8                                                   # the strong-bias test's temperature
     monkeypatch.setattr(draft, "markov_bias", lambda W1, W2, prev: T * orig(W1, W2, prev))
     assert _fails(T_draft.test_draft_sample_distribution_with_strong_bias)
+
+
+def test_expected_tokens_without_the_bonus_token_is_caught(monkeypatch):
+    # E = sum of the scheduled survivals only, dropping each request's certain token
+    # (reading 3: E = sum_b (1 + sum_{j <= l_b} a_{b,j}))
+    from fractions import Fraction
+
+    def bad(a, sps):
+        a = np.asarray(a, np.float32)
+        B, G = a.shape
+        pairs = sorted(((b, j) for b in range(B) for j in range(1, G + 1)),
+                       key=lambda p: (-float(a[p[0], p[1] - 1]), p[0], p[1]))
+        ell, E, N = np.zeros(B, np.int64), Fraction(0), B
+        best = float(E) / N * sps[N]
+        for b, j in pairs:
+            E_new = E + Fraction(float(a[b, j - 1]))
+            th = float(E_new) / (N + 1) * sps[N + 1]
+            if th > best:
+                ell[b] += 1
+                E, N, best = E_new, N + 1, th
+            else:
+                break
+        return ell, N, best
+    monkeypatch.setattr(schedule, "schedule_prefix", bad)
+    assert _fails(T_sched.test_greedy_stop_is_global_optimum_for_rational_sps)
