@@ -551,7 +551,9 @@ def run_reference(args):
     for _ in range(args.warmup):
         pass                                              # the oracle has nothing to warm
     times = []
-    nreq = 4                                              # requests per step (a fraction of a second of oracle work)
+    # requests per step: about 0.06 s of oracle work each, so that even a long run
+    # (--steps 500) stays near a minute of host time
+    nreq = 4 if args.steps <= 200 else (2 if args.steps <= 400 else 1)
     f64 = oracle_inputs(inp)
     for _ in range(args.steps):
         times.append(oracle_round(f64, cfg.temperature, cfg.seed, nreq))
