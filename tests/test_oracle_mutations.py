@@ -224,3 +224,16 @@ def test_expected_tokens_without_the_bonus_token_is_caught(monkeypatch):
         return ell, N, best
     monkeypatch.setattr(schedule, "schedule_prefix", bad)
     assert _fails(T_sched.test_greedy_stop_is_global_optimum_for_rational_sps)
+
+
+def test_philox_swapped_multipliers_are_caught(monkeypatch):
+    import tests.test_oracle_philox as T_philox
+    monkeypatch.setattr(philox, "_M0", philox._M1)
+    monkeypatch.setattr(philox, "_M1", philox._M0)
+    assert _fails(lambda: [T_philox.test_known_answer_vectors(r) for r in T_philox._kat_rows()])
+
+
+def test_philox_missing_key_bump_is_caught(monkeypatch):
+    import tests.test_oracle_philox as T_philox
+    monkeypatch.setattr(philox, "_W1", np.uint64(0))
+    assert _fails(lambda: [T_philox.test_known_answer_vectors(r) for r in T_philox._kat_rows()])
