@@ -237,3 +237,12 @@ def test_philox_missing_key_bump_is_caught(monkeypatch):
     import tests.test_oracle_philox as T_philox
     monkeypatch.setattr(philox, "_W1", np.uint64(0))
     assert _fails(lambda: [T_philox.test_known_answer_vectors(r) for r in T_philox._kat_rows()])
+
+
+def test_loss_position_weight_off_by_one_is_caught(monkeypatch):
+    # exp(-k / gamma) instead of exp(-(k - 1) / gamma): the first position no longer weighs 1
+    from oracle import loss as L
+    import tests.test_oracle_loss as T_loss
+    monkeypatch.setattr(L, "position_weights",
+                        lambda k, decay=L.DECAY_GAMMA: np.exp(-np.asarray(k, np.float64) / decay))
+    assert _fails(T_loss.test_position_weights)
