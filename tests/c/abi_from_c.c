@@ -1,4 +1,4 @@
-/* Plain C99 use of the C ABI: the header compiles as C, the library links from
+/* Plain C99 use of the C ABI: both headers compile as C, the library links from
  * C, and the host-side checks answer without a GPU (no call here reaches a
  * kernel: each passes an argument the entry point rejects before any CUDA
  * call).  Exit status 0 on success. */
@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include "dspark.h"
+#include "dspark_debug.h"
 
 static int check(const char* what, int got, int want) {
     if (got != want) {
