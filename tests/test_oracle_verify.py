@@ -133,3 +133,32 @@ def test_greedy_agreement_and_first_disagreement():
     assert np.array_equal(out["n_accept"], np.minimum(cut, ell))
     stop = np.minimum(cut, ell)
     assert np.array_equal(out["next_token"], np.argmax(t[np.arange(R), stop], axis=-1))
+
+
+def test_rejection_with_an_empty_residual_draws_from_the_target():
+    """Reading 7: a residual with no mass falls back to a draw from p_t.  With the
+    target row equal to the draft logits (p_t = p_d) and the caller's logp_d
+    raised by 1, every test accepts with probability 1/e, and each rejected row's
+    residual max(0, p_t - p_d) is zero everywhere."""
+    rng = np.random.default_rng(8)
+    R, V, G, r, H, T = 40000, 24, 1, 4, 2, 1.0
+    U1 = rng.normal(0, 1.0, (G, V))
+    W1 = rng.normal(0, 0.5, (V, r))
+    W2 = rng.normal(0, 0.5, (V, r))
+    x0 = np.full(R, 5)
+    U = np.broadcast_to(U1, (R, G, V))
+    d = draft.draft_block(U, np.zeros((R, G, H)), W1, W2, np.zeros(H + r), 0.0, x0, T, seed=13)
+    # the target row is the draft's own logits, rebuilt as verification rebuilds them,
+    # so p_t and p_d agree bit for bit and the residual is exactly empty
+    z1 = verify.draft_logits(U, W1, W2, x0, d["x"], np.arange(1), np.ones(1, int))[0]
+    from oracle.sampling import logsumexp
+    p_d = np.exp(z1 / T - d["lse_d"][0, 0])
+    p_t = np.exp(z1 / T - logsumexp((z1 / T)[None], axis=-1)[0])   # as verification forms p_t
+    assert np.all(np.maximum(0.0, p_t - p_d) == 0.0)
+    t = np.empty((R, G + 1, V))
+    t[:, 0] = z1
+    t[:, 1] = rng.normal(0, 1.0, V)
+    out = verify.verify(t, U, W1, W2, x0, d["x"], d["lse_d"], d["logp_d"] + 1.0, np.full(R, G), T, seed=13)
+    rej = out["n_accept"] == 0
+    assert abs(1.0 - rej.mean() - np.exp(-1.0)) < 4.5 * np.sqrt(np.exp(-1.0) * (1 - np.exp(-1.0)) / R)
+    assert _chi2_p(out["next_token"][rej], _softmax(z1 / T)) > 1e-3
