@@ -9,7 +9,7 @@ share no code.  Every function names the passage of the DeepSpec walkthrough
 
 Modules
   philox    Philox4x32-10 (Salmon et al., SC'11) and the uniforms / Gumbel draws
-  sampling  two-level Gumbel-max: an exact sampler of a softmax
+  sampling  Gumbel-max over the vocabulary, noise keyed by vocabulary index
   draft     Markov bias, draft sampling, confidence head, survival product
   schedule  Algorithm 1, literal, with an exact sum of survivals
   verify    rejection-sampling verification, residual and bonus tokens
@@ -27,4 +27,4 @@ from .draft import draft_block, markov_bias, confidence, draft_logits  # noqa: F
 from .schedule import schedule_prefix  # noqa: F401
 from .verify import verify as verify_round  # noqa: F401
 from .tv import accept_rate_tv  # noqa: F401
-from .sampling import two_level_gumbel, SAMPLE_BLOCK  # noqa: F401
+from .sampling import gumbel_max  # noqa: F401

@@ -18,7 +18,7 @@ Everything is float64; inputs arrive as exact float64 copies of bf16/fp32.
 import numpy as np
 
 from . import philox
-from .sampling import two_level_gumbel, greedy, logsumexp
+from .sampling import gumbel_max, greedy, logsumexp
 
 
 def markov_bias(W1, W2, prev):
@@ -76,8 +76,7 @@ def draft_block(U, h, W1, W2, w, bias, x0, temperature, seed, forced_tokens=None
         if T > 0.0:
             l = z / T
             L = logsumexp(l, axis=-1)
-            tok, mar = two_level_gumbel(l, seed, keys, k, philox.STREAM_DRAFT_BLOCK,
-                                        philox.STREAM_DRAFT_TOKEN)
+            tok, mar = gumbel_max(l, seed, keys, k, philox.STREAM_DRAFT_TOKEN)
             lse_d[:, k - 1] = L
             logp_d[:, k - 1] = l[req, tok] - L
         else:

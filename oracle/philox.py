@@ -26,13 +26,11 @@ _W0 = np.uint64(0x9E3779B9)
 _W1 = np.uint64(0xBB67AE85)
 
 # One stream per independent draw of a round.
-STREAM_DRAFT_TOKEN = 0     # within-block Gumbel noise of the draft sample
-STREAM_ACCEPT = 1          # acceptance uniform u of the rejection test
-STREAM_RESIDUAL_TOKEN = 2  # within-block Gumbel noise of the residual sample
-STREAM_DRAFT_BLOCK = 3     # block-level Gumbel noise of the draft sample
-STREAM_RESIDUAL_BLOCK = 4  # block-level Gumbel noise of the residual sample
-STREAM_TARGET_TOKEN = 5    # within-block Gumbel noise of a sample from p_t
-STREAM_TARGET_BLOCK = 6    # block-level Gumbel noise of a sample from p_t
+STREAM_DRAFT_TOKEN = 0     # Gumbel noise of the draft sample x_k, one word per vocabulary index
+STREAM_ACCEPT = 1          # acceptance uniform u of the rejection test (index 0)
+STREAM_VERIFY_TOKEN = 2    # Gumbel noise of the token the verifier emits: the residual draw at the
+                           # rejected position, the bonus draw from p_t at row l* + 1, or the draw
+                           # from p_t when a residual has no mass (only one of them per request)
 
 
 def philox4x32_10(c0, c1, c2, c3, k0, k1):
@@ -73,6 +71,18 @@ def draw_words(seed, b, k, stream, index):
     sel = (index & np.uint64(3)).astype(np.int64)
     out = np.choose(sel, words)
     return out.astype(np.uint64)
+
+
+def row_words(seed, b, k, stream, V):
+    """[R, V] words of requests b[R] at position k for indices 0 .. V-1: the same
+    values as draw_words, with each Philox block computed once for its four words."""
+    seed = int(seed) & 0xFFFFFFFFFFFFFFFF
+    b = np.atleast_1d(np.asarray(b, dtype=np.uint64))
+    nq = -(-int(V) // 4)
+    c0 = np.arange(nq, dtype=np.uint64)[None, :]
+    words = philox4x32_10(c0, np.uint64(k), b[:, None], np.uint64(stream), seed & 0xFFFFFFFF, seed >> 32)
+    out = np.stack(words, axis=-1).reshape(b.shape[0], nq * 4)     # word v & 3 of block v >> 2
+    return out[:, :int(V)]
 
 
 def uniform_open(words):

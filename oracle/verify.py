@@ -11,15 +11,19 @@ the bonus row of request b is row l*_b + 1.
 
 Readings: p_t = softmax(t_k / T) and p_d = softmax((U_k + B_k) / T), with the
 draft's own log-normaliser lse_d and log p_d(x_k) passed in from the draft
-step; the residual is drawn by the two-level Gumbel-max of oracle.sampling
-over ln q; if q has no mass (p_t <= p_d everywhere) the token is drawn from
-p_t at that row.  T = 0 is greedy: accept iff x_k = argmax t_k, and the next
+step; the residual is drawn by the Gumbel-max of oracle.sampling over ln q;
+if q has no mass (p_t <= p_d everywhere) the token is drawn from p_t at that
+row.  Every token the verifier emits (residual, bonus, or that fallback) takes
+its noise from one stream (STREAM_VERIFY_TOKEN) at (b, row of the draw): a
+request draws exactly one such token per round, and the stream is separate
+from the draft's noise and from the acceptance uniforms, so the draw is
+independent of every event that led to it.  T = 0 is greedy: accept iff x_k = argmax t_k, and the next
 token is argmax t at the stop row.  Ties go to the lowest index.
 """
 import numpy as np
 
 from . import philox
-from .sampling import two_level_gumbel, greedy, logsumexp
+from .sampling import gumbel_max, greedy, logsumexp
 from .draft import draft_logits
 
 
@@ -94,16 +98,14 @@ def verify(t_logits, U, W1, W2, x0, x, lse_d, logp_d, ell, temperature, seed, re
                 logq = np.where(q > 0.0, np.log(q), -np.inf)
             if np.any(has_mass):
                 r = res_rows[has_mass]
-                tok, mar = two_level_gumbel(logq[has_mass], seed, keys[r], k,
-                                            philox.STREAM_RESIDUAL_BLOCK,
-                                            philox.STREAM_RESIDUAL_TOKEN)
+                tok, mar = gumbel_max(logq[has_mass], seed, keys[r], k, philox.STREAM_VERIFY_TOKEN)
                 next_token[r] = tok
                 margin[r] = np.minimum(margin[r], mar)
             fallback = res_rows[~has_mass]
         from_target = np.concatenate([bonus_rows, fallback])
         if len(from_target):
-            tok, mar = two_level_gumbel(t_logits[from_target, k - 1, :] / T, seed, keys[from_target], k,
-                                        philox.STREAM_TARGET_BLOCK, philox.STREAM_TARGET_TOKEN)
+            tok, mar = gumbel_max(t_logits[from_target, k - 1, :] / T, seed, keys[from_target], k,
+                                  philox.STREAM_VERIFY_TOKEN)
             next_token[from_target] = tok
             margin[from_target] = np.minimum(margin[from_target], mar)
     return dict(n_accept=n_accept, next_token=next_token, margin=margin)

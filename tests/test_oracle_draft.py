@@ -1,5 +1,5 @@
 """Pins for oracle.sampling and oracle.draft: distribution tests of the
-two-level Gumbel sampler, closed forms of the Markov bias / confidence head /
+Gumbel-max sampler and a brute-force restatement of it, closed forms of the Markov bias / confidence head /
 survival product built from structured weights, and a deterministic chain that
 shows the bias of step k uses x_{k-1}."""
 import numpy as np
@@ -24,40 +24,84 @@ def _chi2_p(samples, probs):
     return stats.chisquare(obs, exp).pvalue
 
 
-def test_two_level_gumbel_matches_softmax():
-    # three blocks, the last one ragged, and some zero-weight entries
+def test_gumbel_max_matches_softmax():
+    # a ragged vocabulary (not a multiple of the 4 words of a Philox block) with
+    # zero-weight entries
     rng = np.random.default_rng(10)
     V = 150
     logw = rng.normal(0, 1.5, V)
     logw[[3, 70, 149]] = -np.inf
     R = 100000
-    tok, _ = sampling.two_level_gumbel(np.broadcast_to(logw, (R, V)), 123, np.arange(R), 1,
-                                       philox.STREAM_DRAFT_BLOCK, philox.STREAM_DRAFT_TOKEN)
+    tok, _ = sampling.gumbel_max(np.broadcast_to(logw, (R, V)), 123, np.arange(R), 1, philox.STREAM_DRAFT_TOKEN)
     p = np.exp(logw - logw[np.isfinite(logw)].max())
     p /= p.sum()
     assert np.all(np.isfinite(logw[tok]))
     assert _chi2_p(tok, p) > 1e-3
 
 
-def test_two_level_gumbel_detects_a_wrong_law():
+def test_gumbel_max_detects_a_wrong_law():
     # sanity of the test itself: the same draws do not fit a tempered law
     rng = np.random.default_rng(11)
     V = 150
     logw = rng.normal(0, 1.5, V)
     R = 100000
-    tok, _ = sampling.two_level_gumbel(np.broadcast_to(logw, (R, V)), 5, np.arange(R), 2,
-                                       philox.STREAM_DRAFT_BLOCK, philox.STREAM_DRAFT_TOKEN)
+    tok, _ = sampling.gumbel_max(np.broadcast_to(logw, (R, V)), 5, np.arange(R), 2, philox.STREAM_DRAFT_TOKEN)
     p_wrong = np.exp(0.8 * (logw - logw.max()))
     p_wrong /= p_wrong.sum()
     assert _chi2_p(tok, p_wrong) < 1e-6
 
 
-def test_two_level_gumbel_single_finite_entry_and_dead_row():
+def test_gumbel_max_single_finite_entry_and_dead_row():
     V = 200
     logw = np.full((2, V), -np.inf)
     logw[0, 131] = 0.0
-    tok, _ = sampling.two_level_gumbel(logw, 1, np.arange(2), 1, 3, 0)
+    tok, _ = sampling.gumbel_max(logw, 1, np.arange(2), 1, philox.STREAM_VERIFY_TOKEN)
     assert tok[0] == 131 and tok[1] == -1
+
+
+def test_gumbel_max_is_the_literal_definition():
+    """Brute force, one scalar at a time with Python's own math.log: for every
+    index v, the word (v & 3) of Philox(seed; (v >> 2, k, b, stream)), the uniform
+    ((w >> 9) + 1/2) 2^-23, the Gumbel -ln(-ln u), then the first maximum of
+    lw_v + G.  The vectorised sampler must give the same tokens and margins."""
+    import math
+    rng = np.random.default_rng(12)
+    seed, k, stream = 0xDEADBEEF12345678, 3, philox.STREAM_DRAFT_TOKEN
+    R, V = 6, 37
+    logw = rng.normal(0, 2.0, (R, V))
+    logw[2, :] = 0.0                      # only the noise decides
+    logw[4, 5] = -np.inf
+    b = np.array([0, 1, 7, 1000, 65535, 3])
+    tok, mar = sampling.gumbel_max(logw, seed, b, k, stream)
+    for i in range(R):
+        best, second, arg = -math.inf, -math.inf, -1
+        for v in range(V):
+            words = philox.philox4x32_10(v >> 2, k, int(b[i]), stream, seed & 0xFFFFFFFF, seed >> 32)
+            w = int(words[v & 3])
+            u = ((w >> 9) + 0.5) * 2.0 ** -23
+            score = float(logw[i, v]) - math.log(-math.log(u))
+            if score > best:
+                best, second, arg = score, best, v
+            elif score > second:
+                second = score
+        assert tok[i] == arg
+        assert abs(mar[i] - (best - second)) < 1e-12
+
+
+def test_gumbel_max_noise_is_keyed_by_index_request_position_stream():
+    """Changing any of seed, request, position or stream changes the draw for a
+    flat log-weight row (where only the noise decides) in most cases, and the
+    same key always gives the same draw."""
+    V, R = 64, 400
+    flat = np.zeros((R, V))
+    base, _ = sampling.gumbel_max(flat, 9, np.arange(R), 2, 0)
+    again, _ = sampling.gumbel_max(flat, 9, np.arange(R), 2, 0)
+    assert np.array_equal(base, again)
+    for other in (sampling.gumbel_max(flat, 10, np.arange(R), 2, 0)[0],
+                  sampling.gumbel_max(flat, 9, np.arange(R) + 1, 2, 0)[0],
+                  sampling.gumbel_max(flat, 9, np.arange(R), 3, 0)[0],
+                  sampling.gumbel_max(flat, 9, np.arange(R), 2, 1)[0]):
+        assert np.mean(other == base) < 0.1
 
 
 def test_greedy_lowest_index_on_ties():

@@ -21,15 +21,34 @@ def _fails(fn):
 
 def test_gumbel_sign_slip_is_caught(monkeypatch):
     monkeypatch.setattr(philox, "gumbel", lambda u: np.log(-np.log(np.asarray(u, np.float64))))
-    assert _fails(T_draft.test_two_level_gumbel_matches_softmax)
+    assert _fails(T_draft.test_gumbel_max_matches_softmax)
 
 
-def test_block_level_dropped_is_caught(monkeypatch):
-    # choosing the block by its max logit instead of its logsumexp
-    orig = sampling.logsumexp
-    monkeypatch.setattr(sampling, "logsumexp", lambda x, axis=-1: np.max(x, axis=axis))
-    assert _fails(T_draft.test_two_level_gumbel_matches_softmax)
-    monkeypatch.setattr(sampling, "logsumexp", orig)
+def test_one_word_per_philox_block_is_caught(monkeypatch):
+    # the four indices of a Philox block sharing one word (word 0) instead of word v & 3
+    orig = philox.row_words
+
+    def bad(seed, b, k, stream, V):
+        w = orig(seed, b, k, stream, -(-V // 4) * 4)
+        return np.repeat(w[:, 0::4], 4, axis=1)[:, :V]
+    monkeypatch.setattr(philox, "row_words", bad)
+    assert _fails(T_draft.test_gumbel_max_matches_softmax)
+    assert _fails(T_draft.test_gumbel_max_is_the_literal_definition)
+
+
+def test_noise_keyed_without_the_request_is_caught(monkeypatch):
+    # every request of a batch drawing the same noise (request index dropped from the counter)
+    orig = philox.row_words
+    monkeypatch.setattr(philox, "row_words", lambda seed, b, k, stream, V: orig(seed, np.zeros_like(b), k, stream, V))
+    assert _fails(T_draft.test_gumbel_max_matches_softmax)
+    assert _fails(T_draft.test_gumbel_max_noise_is_keyed_by_index_request_position_stream)
+
+
+def test_verifier_token_on_the_draft_stream_is_caught(monkeypatch):
+    # the residual drawn with the same noise that proposed x_k (stream 0 at (b, k)):
+    # the residual draw is then tied to the rejected proposal and loses its law
+    monkeypatch.setattr(philox, "STREAM_VERIFY_TOKEN", philox.STREAM_DRAFT_TOKEN)
+    assert _fails(T_verify.test_token_after_a_rejection_follows_the_residual)
 
 
 def test_transposed_bias_is_caught(monkeypatch):

@@ -37,6 +37,16 @@ def test_draw_words_layout():
     assert [int(x) for x in w] == [int(x) for x in blk0] + [int(x) for x in blk1]
 
 
+def test_row_words_equal_draw_words():
+    # the per-row fast path computes each Philox block once; the words are the same
+    seed = 0xFEEDFACE00C0FFEE
+    b = np.array([0, 3, 1023])
+    for V in (1, 5, 8, 37):
+        rows = philox.row_words(seed, b, 6, philox.STREAM_VERIFY_TOKEN, V)
+        ref = philox.draw_words(seed, b[:, None], 6, philox.STREAM_VERIFY_TOKEN, np.arange(V)[None, :])
+        assert rows.shape == (3, V) and np.array_equal(rows, ref)
+
+
 def test_uniform_ranges_exact():
     w = np.array([0, 0xFFFFFFFF, 0x00000200, 0x80000000], dtype=np.uint64)
     u = philox.uniform_open(w)
