@@ -1,7 +1,9 @@
 """Benchmark of the DSpark serving round on GB300: draft block -> prefix
-scheduler -> verification, on the Qwen3-8B-shaped serving workload
-(B = 64 requests, gamma = 7, V = 151936, H = 4096, r = 256, bf16, T = 0.7),
-synthetic seeded inputs.
+scheduler -> verification, on the high-concurrency workload (B = 1024
+requests, gamma = 16, V = 151936, H = 4096, r = 256, bf16, T = 1.0, per-request
+peak rate ~ Beta(5, 2)), synthetic seeded inputs; the Qwen3-8B-shaped (B = 64,
+gamma = 7, T = 0.7 and greedy) and 27B-draft-shaped (B = 256, gamma = 7)
+serving rounds are reported under `extra`, each with its own roofline.
 
 One step = one round through the library's C ABI (all kernels on one stream),
 captured once in a CUDA graph and replayed (--no-graph launches the calls
@@ -9,10 +11,12 @@ directly every step).
 The timed region holds exactly K steps; the L2 is flushed (a 512 MiB write)
 between steps, outside each step's CUDA-event pair.  The JSON line also
 reports the dominant kernel's roofline (the draft engine, one cooperative
-launch per draft call: timed with CUDA events the library records around it), an
-end-to-end number through the same C-ABI calls with inputs copied from pinned
-host memory each step, the oracle timed on the host cores on a bounded sample,
-and extra lines for greedy decoding and the accept-rate TV kernel.
+launch per draft call: timed with CUDA events the library records around it,
+against the measured copy bandwidth and, for its bias GEMM, the measured
+sustained bf16 tensor rate), an end-to-end number through the same C-ABI
+calls with inputs copied from pinned host memory each step, the oracle timed
+on the host cores on a bounded sample, and the oracle's teacher-forced check
+of a sample of the GPU's draws with the exempt decisions counted.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -33,8 +37,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "draft+verify rows/s over B·γ×V logits; achieved HBM GB/s vs GB300 peak"
-WORKLOAD = ("Qwen3-8B-shaped serving round: B=64, gamma=7 (verify width 8), V=151936, H=4096, r=256, "
-            "bf16, T=0.7, seed 1")
+WORKLOAD = ("high-concurrency serving round: B=1024 requests, gamma=16, V=151936, H=4096, r=256, bf16, "
+            "T=1.0, per-request peak rate ~ Beta(5,2), seed 4")
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -161,6 +165,59 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------- GPU arm ---
+def draft_launch_bytes(B, G, V, H, r):
+    """Algorithmic bytes of one draft engine launch (all positions): U, W2 once, h
+    (the confidence head reads it in the same launch) and the W1 rows."""
+    return B * G * V * 2 + V * r * 2 + B * G * H * 2 + B * G * r * 2
+
+
+class Serving:
+    """One serving config on the GPU: inputs, workspaces, outputs and the round."""
+
+    def __init__(self, dsv, lib, cfg, dev, T=None):
+        from serving_draft_verify_gb300 import workloads as wl
+        import torch
+        self.dsv, self.cfg, self.dev = dsv, cfg, dev
+        self.inp = wl.make_draft_inputs(cfg, device=dev)
+        self.T = cfg.temperature if T is None else T
+        B, G, V, r = cfg.B, cfg.gamma, cfg.V, cfg.r
+        self.ws_d = torch.empty(lib.dspark_draft_block_workspace_size(B, G, V, r), dtype=torch.uint8, device=dev)
+        self.ws_s = torch.empty(lib.dspark_schedule_prefix_workspace_size(B, G), dtype=torch.uint8, device=dev)
+        self.ws_v = torch.empty(lib.dspark_verify_workspace_size(B, G, V, r), dtype=torch.uint8, device=dev)
+        self.outd = dict(x=torch.empty((B, G), dtype=torch.int32, device=dev),
+                         **{k: torch.empty((B, G), dtype=torch.float32, device=dev)
+                            for k in ("lse_d", "logp_d", "c", "a")})
+        self.outs = dict(ell=torch.empty(B, dtype=torch.int32, device=dev),
+                         n_sched=torch.empty(1, dtype=torch.int32, device=dev),
+                         theta=torch.empty(1, dtype=torch.float64, device=dev))
+        self.outv = dict(n_accept=torch.empty(B, dtype=torch.int32, device=dev),
+                         next_token=torch.empty(B, dtype=torch.int32, device=dev))
+
+    def draft(self, g=None, T=None):
+        g = self.inp if g is None else g
+        self.dsv.dspark_draft_block(g["U"], g["h"], g["W1"], g["W2"], g["w"], 0.0, g["x0"],
+                                    self.T if T is None else T, self.cfg.seed, out=self.outd, workspace=self.ws_d)
+
+    def schedule(self, g=None):
+        g = self.inp if g is None else g
+        self.dsv.dspark_schedule_prefix(self.outd["a"], g["sps"], out=self.outs, workspace=self.ws_s)
+
+    def verify(self, g=None, T=None):
+        g = self.inp if g is None else g
+        o = self.outd
+        self.dsv.dspark_verify(g["t"], g["U"], g["W1"], g["W2"], g["x0"], o["x"], o["lse_d"], o["logp_d"],
+                               self.outs["ell"], self.T if T is None else T, self.cfg.seed, out=self.outv,
+                               workspace=self.ws_v)
+
+    def round(self, g=None, T=None):
+        self.draft(g, T)
+        self.schedule(g)
+        self.verify(g, T)
+
+    def status_ok(self):
+        return self.dsv.workspace_status(self.ws_d) == 0 and self.dsv.workspace_status(self.ws_v) == 0
+
+
 def run_gpu(args):
     import torch
     import serving_draft_verify_gb300 as dsv
@@ -174,30 +231,10 @@ def run_gpu(args):
         dist.init_process_group("nccl")
     dsv.load()
     lib = dsv._binding.load()
-    cfg = wl.QWEN3_8B
-    inp = wl.make_draft_inputs(cfg, device=dev)
-    B, G, V, H, r = cfg.B, cfg.gamma, cfg.V, cfg.H, cfg.r
-    T, seed = cfg.temperature, cfg.seed
     stream = torch.cuda.current_stream()
-
-    ws_d = torch.empty(lib.dspark_draft_block_workspace_size(B, G, V, r), dtype=torch.uint8, device=dev)
-    ws_s = torch.empty(lib.dspark_schedule_prefix_workspace_size(B, G), dtype=torch.uint8, device=dev)
-    ws_v = torch.empty(lib.dspark_verify_workspace_size(B, G, V, r), dtype=torch.uint8, device=dev)
-    outd = dict(x=torch.empty((B, G), dtype=torch.int32, device=dev),
-                **{k: torch.empty((B, G), dtype=torch.float32, device=dev) for k in ("lse_d", "logp_d", "c", "a")})
-    outs = dict(ell=torch.empty(B, dtype=torch.int32, device=dev), n_sched=torch.empty(1, dtype=torch.int32, device=dev),
-                theta=torch.empty(1, dtype=torch.float64, device=dev))
-    outv = dict(n_accept=torch.empty(B, dtype=torch.int32, device=dev),
-                next_token=torch.empty(B, dtype=torch.int32, device=dev))
-
-    def round_(g, temperature):
-        dsv.dspark_draft_block(g["U"], g["h"], g["W1"], g["W2"], g["w"], 0.0, g["x0"], temperature, seed,
-                               out=outd, workspace=ws_d)
-        dsv.dspark_schedule_prefix(outd["a"], g["sps"], out=outs, workspace=ws_s)
-        dsv.dspark_verify(g["t"], g["U"], g["W1"], g["W2"], g["x0"], outd["x"], outd["lse_d"], outd["logp_d"],
-                          outs["ell"], temperature, seed, out=outv, workspace=ws_v)
-
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    peak, peak_kind = peaks()
+    tpk, tpk_kind = tensor_peak()
 
     def barrier():
         torch.cuda.synchronize()
@@ -243,157 +280,205 @@ def run_gpu(args):
             return None
         return g.replay
 
-    # main arm, T = 0.7, the round replayed from a CUDA graph; the library's events
-    # around the draft launch are captured with it and time that launch every step
+    def measure(sv, steps, warmup, clocks=None):
+        """Round throughput of one serving config, the draft engine's roofline from the
+        library's events, and per-call device times (directly launched calls)."""
+        cfg = sv.cfg
+        B, G, V, H, r = cfg.B, cfg.gamma, cfg.V, cfg.H, cfg.r
+        dsv._binding.phase_timing(True)
+        rnd = graphed(sv.round)
+        use_graph = rnd is not None
+        if not use_graph:
+            rnd = sv.round
+        if clocks is not None:
+            clocks.start()
+        times, phase_ms = timed(rnd, steps, warmup, phase_times=True)
+        engine_timing = "events around the draft launch, captured with the replayed round"
+        if not phase_ms:                                  # events in the graph not timeable here
+            _, phase_ms = timed(sv.round, steps, warmup, phase_times=True)
+            engine_timing = "events around the draft launch, in as many directly launched rounds"
+        clk = clocks.stop() if clocks is not None else None
+        dsv._binding.phase_timing(False)
+        assert sv.status_ok()
+        total_ms = sum(times)
+        ell = sv.outs["ell"].cpu().numpy()
+        nacc = sv.outv["n_accept"].cpu().numpy()
+        n_rej = int((nacc < ell).sum())
+        sched_rows = int((ell + 1).sum())
+        round_bytes = draft_launch_bytes(B, G, V, H, r) + sched_rows * V * 2 + n_rej * 2 * V * 2
+        per_call = max(len(phase_ms) // steps, 1) if steps else 1
+        launch_bytes = draft_launch_bytes(B, G, V, H, r) / per_call
+        phase_avg = sum(phase_ms) / len(phase_ms) if phase_ms else float("nan")
+        achieved = launch_bytes / (phase_avg * 1e-3) / 1e9
+        flops = 2.0 * B * G * V * r / per_call
+        tflops = flops / (phase_avg * 1e-3) / 1e12
+        roof = {"bound": "hbm", "kernel": "bias_engine_tc<kDraft> (draft block, all positions, one launch)",
+                "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": None, "peak_kind": f"{peak_kind} copy bandwidth",
+                "bytes_per_launch": int(launch_bytes), "avg_launch_us": round(phase_avg * 1e3, 2),
+                "launches_timed": len(phase_ms), "timing": engine_timing,
+                "tensor": {"flops_per_launch": flops, "achieved_tflops": round(tflops, 1), "peak_tflops": tpk,
+                           "frac": round(tflops / tpk, 4), "peak_kind": tpk_kind}}
+        # per-call device times, launched directly (events between the calls, L2 flushed first)
+        ev_ = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        call_us = [[], [], []]
+        for it_ in range(min(max(10, steps), 40) + 3):
+            flush.zero_()
+            ev_[0].record(stream)
+            sv.draft()
+            ev_[1].record(stream)
+            sv.schedule()
+            ev_[2].record(stream)
+            sv.verify()
+            ev_[3].record(stream)
+            torch.cuda.synchronize()
+            if it_ >= 3:
+                for i_ in range(3):
+                    call_us[i_].append(ev_[i_].elapsed_time(ev_[i_ + 1]) * 1e3)
+        med = [statistics.median(x) for x in call_us]
+        ver_bytes = sched_rows * V * 2
+        out = {"workload": cfg.name, "B": B, "gamma": G, "V": V, "H": H, "r": r, "temperature": sv.T,
+               "rows_per_s": B * G * steps / (total_ms * 1e-3), "ms_per_step": total_ms / steps, "steps": steps,
+               "cuda_graph": use_graph, "round_hbm_gbs": round_bytes * steps / (total_ms * 1e-3) / 1e9,
+               "roofline": roof,
+               "per_call": {"timing": "CUDA events between directly launched calls, median",
+                            "draft_us": med[0], "schedule_us": med[1], "verify_us": med[2],
+                            "verify_algorithmic_bytes": ver_bytes,
+                            "verify_gbs": ver_bytes / (med[2] * 1e-6) / 1e9,
+                            "verify_frac": ver_bytes / (med[2] * 1e-6) / 1e9 / peak},
+               "scheduled_rows": sched_rows, "rejected_requests": n_rej,
+               "accepted_per_request": float(nacc.mean())}
+        return out, clk
+
+    def parity_sample(sv, nreq):
+        """The oracle, teacher-forced on the GPU's draft tokens and verifying the GPU's
+        own draft outputs, on the first nreq requests: mismatches beyond the exempt
+        decisions (oracle margin < 1e-4), and the exempt counts."""
+        import numpy as np
+        import oracle
+        rows = np.arange(nreq)
+        inp = sv.inp
+        idx = torch.from_numpy(rows).to(inp["U"].device)
+        f64 = wl.to_f64
+        dn = {k: v.cpu().numpy() for k, v in sv.outd.items()}
+        ell = sv.outs["ell"].cpu().numpy()
+        ref = oracle.draft_block(f64(inp["U"][idx]), f64(inp["h"][idx]), f64(inp["W1"]), f64(inp["W2"]),
+                                 f64(inp["w"]), 0.0, inp["x0"].cpu().numpy()[rows], sv.T, sv.cfg.seed,
+                                 forced_tokens=dn["x"][rows], requests=rows)
+        ex_d = ref["margin"] < 1e-4
+        mis_d = int(((dn["x"][rows] != ref["x"]) & ~ex_d).sum())
+        vr = oracle.verify_round(f64(inp["t"][idx]), f64(inp["U"][idx]), f64(inp["W1"]), f64(inp["W2"]),
+                                 inp["x0"].cpu().numpy()[rows], dn["x"][rows], dn["lse_d"][rows],
+                                 dn["logp_d"][rows], ell[rows], sv.T, sv.cfg.seed, requests=rows)
+        ex_v = vr["margin"] < 1e-4
+        na = sv.outv["n_accept"].cpu().numpy()[rows]
+        nt = sv.outv["next_token"].cpu().numpy()[rows]
+        mis_v = int((((na != vr["n_accept"]) | (nt != vr["next_token"])) & ~ex_v).sum())
+        return {"requests": int(nreq), "draft_tokens": int(ex_d.size), "draft_exempt": int(ex_d.sum()),
+                "draft_mismatches": mis_d, "verify_requests": int(ex_v.size), "verify_exempt": int(ex_v.sum()),
+                "verify_mismatches": mis_v}
+
+    # ------------------------------------------------ headline: high concurrency
+    cfg = wl.HIGH_CONC
+    sv = Serving(dsv, lib, cfg, dev)
+    B, G, V, H, r = cfg.B, cfg.gamma, cfg.V, cfg.H, cfg.r
     clocks = ClockSampler(smi_index(local))
-    dsv._binding.phase_timing(True)
-    main_round = graphed(lambda: round_(inp, T))
-    use_graph = main_round is not None
-    if not use_graph:
-        main_round = lambda: round_(inp, T)
-    stream = torch.cuda.current_stream()
-    clocks.start()
-    times, phase_ms = timed(main_round, args.steps, args.warmup, phase_times=True)
-    engine_timing = "events around the draft launch, captured with the replayed round"
-    if not phase_ms:                                      # events in the graph not timeable here
-        _, phase_ms = timed(lambda: round_(inp, T), args.steps, args.warmup, phase_times=True)
-        engine_timing = "events around the draft launch, in as many directly launched rounds"
-    clk = clocks.stop()
-    dsv._binding.phase_timing(False)
-    assert dsv.workspace_status(ws_d) == 0 and dsv.workspace_status(ws_v) == 0
-    total_ms, rows = aggregate(sum(times), B * G * args.steps, world, dev)
+    head, clk = measure(sv, args.steps, args.warmup, clocks=clocks)
+    total_ms, rows = aggregate(head["ms_per_step"] * args.steps, B * G * args.steps, world, dev)
     value = rows / (total_ms * 1e-3)
     ms_per_step = total_ms / args.steps
-
-    # algorithmic bytes of one round: U and h once, W2 once per draft call, W1 rows,
-    # the scheduled target rows, and the residual rows (U and t) of rejected requests
-    ell = outs["ell"].cpu().numpy()
-    nacc = outv["n_accept"].cpu().numpy()
-    n_rej = int((nacc < ell).sum())
-    round_bytes = (B * G * V * 2 + V * r * 2 + B * G * H * 2 + B * G * r * 2 + int((ell + 1).sum()) * V * 2
-                   + n_rej * 2 * V * 2)
-    hbm_gbs = round_bytes * args.steps / (total_ms * 1e-3) / 1e9
-    peak, peak_kind = peaks()
-
-    # dominant kernel: the draft engine, one cooperative launch per draft call that
-    # covers all gamma positions (the library records CUDA events around it on the
-    # launching stream).  Algorithmic bytes of one launch: U, W2 once, W1 rows.
-    launch_bytes = B * G * V * 2 + V * r * 2 + B * G * r * 2
-    per_call = len(phase_ms) // args.steps if args.steps else 0
-    launch_bytes /= max(per_call, 1)
-    ph = sorted(phase_ms)
-    phase_avg = sum(ph) / len(ph) if ph else float("nan")
-    achieved = launch_bytes / (phase_avg * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": "bias_engine_tc<kDraft> (draft block, all positions)",
-                "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "traffic": args.phase_traffic if args.phase_traffic is not None else recorded_engine_traffic(),
-                "peak_kind": f"{peak_kind} (copy bandwidth)", "bytes_per_launch": int(launch_bytes),
-                "avg_launch_us": round(phase_avg * 1e3, 2), "launches_timed": len(ph), "timing": engine_timing}
-
-    # per-call device times of the round, launched directly (events between the calls,
-    # L2 flushed before each round): draft, schedule (latency) and verify with its
-    # algorithmic bytes (the scheduled target rows, plus U and t rows of rejected
-    # requests are not counted)
-    ev_ = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-    call_us = [[], [], []]
-    for it_ in range(max(10, min(args.steps, 100)) + 3):
-        flush.zero_()
-        ev_[0].record(stream)
-        dsv.dspark_draft_block(inp["U"], inp["h"], inp["W1"], inp["W2"], inp["w"], 0.0, inp["x0"], T, seed,
-                               out=outd, workspace=ws_d)
-        ev_[1].record(stream)
-        dsv.dspark_schedule_prefix(outd["a"], inp["sps"], out=outs, workspace=ws_s)
-        ev_[2].record(stream)
-        dsv.dspark_verify(inp["t"], inp["U"], inp["W1"], inp["W2"], inp["x0"], outd["x"], outd["lse_d"],
-                          outd["logp_d"], outs["ell"], T, seed, out=outv, workspace=ws_v)
-        ev_[3].record(stream)
-        torch.cuda.synchronize()
-        if it_ >= 3:
-            for i_ in range(3):
-                call_us[i_].append(ev_[i_].elapsed_time(ev_[i_ + 1]) * 1e3)
-    med_ = [statistics.median(x) for x in call_us]
-    ver_bytes = int((outs["ell"].cpu().long() + 1).sum()) * V * 2
-    bias_flops = 2.0 * B * G * V * r
-    tpk, tpk_kind = tensor_peak()
-    breakdown = {"timing": "CUDA events between directly launched calls, median",
-                 "draft_us": med_[0], "schedule_us": med_[1], "verify_us": med_[2],
-                 "verify_algorithmic_bytes": ver_bytes, "verify_gbs": ver_bytes / (med_[2] * 1e-6) / 1e9,
-                 "draft_bias_tflops": bias_flops / (phase_avg * 1e-3) / 1e12,
-                 "draft_bias_frac_of_tensor_peak": bias_flops / (phase_avg * 1e-3) / 1e12 / tpk,
-                 "tensor_peak_tflops": tpk, "tensor_peak_kind": tpk_kind,
-                 "draft_frac_of_nominal_8tbs": launch_bytes / (phase_avg * 1e-3) / 1e9 / NOMINAL_HBM_GBS}
-
-    # greedy round (same workload, T = 0)
-    greedy_round = graphed(lambda: round_(inp, 0.0)) or (lambda: round_(inp, 0.0))
-    g_times, _ = timed(greedy_round, max(3, args.steps // 2), args.warmup)
-    greedy = {"value": B * G * len(g_times) / (sum(g_times) * 1e-3), "unit": "rows/s",
-              "ms_per_step": sum(g_times) / len(g_times)}
+    roofline = dict(head["roofline"])
+    roofline["traffic"] = args.phase_traffic if args.phase_traffic is not None else recorded_engine_traffic()
 
     # end to end: every step takes its inputs from pinned host memory and reads its results
     # (x, n_accept, next_token) back.  U, h, x0 and SPS are uploaded (the draft reads all of
     # them); the target logits stay in host memory and verification reads, over the host
-    # link, only the rows it needs (the scheduled prefix and its stop row: 135 of 512 rows
-    # here).  The link (~200 GB/s) dominates, so the steps are pipelined: step i+1's upload
-    # runs on a copy stream into the other of two device input sets while step i's round
-    # computes.  Four host copies of t are cycled so that no step can find another step's
-    # target rows in L2.  Timed over all K steps (events before the first upload and after
-    # the last read-back): whole-job throughput.
-    host = {k: inp[k].cpu().pin_memory() for k in ("U", "h", "x0", "sps")}
-    host_t = [inp["t"].cpu().pin_memory() for _ in range(4)]
-    dev_sets = [{k: torch.empty_like(inp[k]) for k in host} for _ in range(2)]
-    t_rows_bytes = int((outs["ell"].cpu().long() + 1).sum()) * V * 2
-    h2d = sum(v.numel() * v.element_size() for v in host.values()) + t_rows_bytes
-    res_host = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
-                 for k, v in (("x", outd["x"]), ("n_accept", outv["n_accept"]), ("next_token", outv["next_token"]))}
-                for _ in range(2)]
-    d2h = sum(v.numel() * v.element_size() for v in res_host[0].values())
-    copy_stream = torch.cuda.Stream(device=dev)
+    # link, only the rows it needs (the scheduled prefix and its stop row).  The link
+    # dominates, so the steps are pipelined: step i+1's upload runs on a copy stream into
+    # the other of two device input sets while step i's round computes.  Enough host copies
+    # of t are cycled that no step can find another step's target rows in L2.  Timed over
+    # all K steps (events before the first upload and after the last read-back).
+    e2e = None
+    if not args.skip_e2e:
+        host = {k: sv.inp[k].cpu().pin_memory() for k in ("U", "h", "x0", "sps")}
+        t_rows_bytes = head["scheduled_rows"] * V * 2
+        n_tcopies = max(1, min(4, -(-2 * 129 * 2 ** 20 // max(t_rows_bytes, 1))))
+        host_t = [sv.inp["t"].cpu().pin_memory() for _ in range(n_tcopies)]
+        dev_sets = [{k: torch.empty_like(sv.inp[k]) for k in host} for _ in range(2)]
+        h2d = sum(v.numel() * v.element_size() for v in host.values()) + t_rows_bytes
+        res_host = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                     for k, v in (("x", sv.outd["x"]), ("n_accept", sv.outv["n_accept"]),
+                                  ("next_token", sv.outv["next_token"]))} for _ in range(2)]
+        d2h = sum(v.numel() * v.element_size() for v in res_host[0].values())
+        copy_stream = torch.cuda.Stream(device=dev)
 
-    def e2e_run(nsteps):
-        """nsteps pipelined end-to-end steps; returns the elapsed ms (device events)."""
-        copied = [torch.cuda.Event() for _ in range(2)]
-        freed = [torch.cuda.Event() for _ in range(2)]
-        for f in freed:
-            f.record(stream)
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier()
-        t0.record(stream)
-        copy_stream.wait_event(t0)
+        def e2e_run(nsteps):
+            copied = [torch.cuda.Event() for _ in range(2)]
+            freed = [torch.cuda.Event() for _ in range(2)]
+            for f in freed:
+                f.record(stream)
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            barrier()
+            t0.record(stream)
+            copy_stream.wait_event(t0)
 
-        def upload(i):
-            sl = i % 2
-            copy_stream.wait_event(freed[sl])            # the round that read this set is done
-            with torch.cuda.stream(copy_stream):
-                for k in host:
-                    dev_sets[sl][k].copy_(host[k], non_blocking=True)
-            copied[sl].record(copy_stream)
+            def upload(i):
+                sl = i % 2
+                copy_stream.wait_event(freed[sl])        # the round that read this set is done
+                with torch.cuda.stream(copy_stream):
+                    for k in host:
+                        dev_sets[sl][k].copy_(host[k], non_blocking=True)
+                copied[sl].record(copy_stream)
 
-        upload(0)
-        for i in range(nsteps):
-            sl = i % 2
-            if i + 1 < nsteps:
-                upload(i + 1)
-            stream.wait_event(copied[sl])
-            g_ = dict(inp)
-            g_.update(dev_sets[sl])
-            g_["t"] = host_t[i % len(host_t)]
-            round_(g_, T)
-            freed[sl].record(stream)
-            for k in ("x", "n_accept", "next_token"):
-                src_ = outd["x"] if k == "x" else outv[k]
-                res_host[sl][k].copy_(src_, non_blocking=True)
-        t1.record(stream)
-        barrier()
-        return t0.elapsed_time(t1)
+            upload(0)
+            for i in range(nsteps):
+                sl = i % 2
+                if i + 1 < nsteps:
+                    upload(i + 1)
+                stream.wait_event(copied[sl])
+                g_ = dict(sv.inp)
+                g_.update(dev_sets[sl])
+                g_["t"] = host_t[i % len(host_t)]
+                sv.round(g_)
+                freed[sl].record(stream)
+                for k in ("x", "n_accept", "next_token"):
+                    src_ = sv.outd["x"] if k == "x" else sv.outv[k]
+                    res_host[sl][k].copy_(src_, non_blocking=True)
+            t1.record(stream)
+            barrier()
+            return t0.elapsed_time(t1)
 
-    e2e_run(args.warmup)
-    e_ms, e_rows = aggregate(e2e_run(args.steps), B * G * args.steps, world, dev)   # slowest rank, all rows
-    e2e = {"value": e_rows / (e_ms * 1e-3), "unit": "rows/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "pipelined": "step i+1's upload overlaps step i's round (two device input sets)",
-           "target_rows": "read by verification from pinned host memory (the scheduled rows only)",
-           "l2": "no flush: every step uploads 140 MB of fresh inputs and reads its target rows from "
-                 "one of four host copies (623 MB together, more than L2)"}
+        e2e_steps = max(3, min(args.steps, args.e2e_steps))
+        e2e_run(min(args.warmup, 3))
+        e_ms, e_rows = aggregate(e2e_run(e2e_steps), B * G * e2e_steps, world, dev)
+        e2e = {"value": e_rows / (e_ms * 1e-3), "unit": "rows/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "pipelined": "step i+1's upload overlaps step i's round (two device input sets)",
+               "target_rows": "read by verification from pinned host memory (the scheduled rows only)",
+               "l2": f"no flush: every step uploads {h2d / 1e9:.2f} GB of fresh inputs and reads its target rows "
+                     f"from one of {n_tcopies} host copies"}
+        del host, host_t, dev_sets
+    parity = None if args.no_cpu_baseline or world > 1 else parity_sample(sv, args.parity_requests)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(sv.inp, sv.T, cfg.seed)
+    del sv
+    torch.cuda.empty_cache()
+
+    # ------------------------------------------------ the other serving configs
+    extra_cfgs = {}
+    if not args.skip_extra_configs:
+        for key, c_, T_ in (("qwen3_8b", wl.QWEN3_8B, None), ("qwen3_8b_greedy", wl.QWEN3_8B, 0.0),
+                            ("draft_27b", wl.DRAFT_27B, None)):
+            sv_ = Serving(dsv, lib, c_, dev, T=T_)
+            res, _ = measure(sv_, max(10, min(args.steps, 200)), args.warmup)
+            if rank == 0 and world == 1 and not args.no_cpu_baseline:
+                res["parity_sample"] = parity_sample(sv_, min(c_.B, 16))
+                res["cpu_baseline"] = cpu_baseline(sv_.inp, sv_.T, c_.seed, min_seconds=3.0, max_rounds=4,
+                                                   nreq=min(c_.B, 16))
+            extra_cfgs[key] = res
+            del sv_
+            torch.cuda.empty_cache()
 
     # accept-rate TV on the training workload (16384 x 151936 bf16 rows)
     tv = None
@@ -422,44 +507,54 @@ def run_gpu(args):
                                "achieved_gbs": lb / (l_ms * 1e-3) / 1e9,
                                "frac_of_peak": lb / (l_ms * 1e-3) / 1e9 / peak}
         del d_, t_, lout
+        torch.cuda.empty_cache()
     # the draft block with the gated and recurrent heads (one launch per position plus a
-    # head kernel between positions), same workload
+    # head kernel between positions), on the Qwen3-8B-shaped workload
     heads_x = None
     if not args.skip_heads:
         heads_x = {}
+        c8 = wl.QWEN3_8B
+        sv8 = Serving(dsv, lib, c8, dev)
         for kind, name in ((1, "gated"), (2, "rnn")):
-            Wg_, Wc_ = wl.make_head_weights(cfg, kind, device=dev)
-            head_ = dict(kind=kind, Wg=Wg_, Wc=Wc_, E=torch.empty((B, G, r), dtype=inp["U"].dtype, device=dev))
-            ws_h = torch.empty(lib.dspark_draft_block_ex_workspace_size(B, G, V, r, kind), dtype=torch.uint8,
-                               device=dev)
+            Wg_, Wc_ = wl.make_head_weights(c8, kind, device=dev)
+            head_ = dict(kind=kind, Wg=Wg_, Wc=Wc_, E=torch.empty((c8.B, c8.gamma, c8.r), dtype=torch.bfloat16,
+                                                                  device=dev))
+            ws_h = torch.empty(lib.dspark_draft_block_ex_workspace_size(c8.B, c8.gamma, c8.V, c8.r, kind),
+                               dtype=torch.uint8, device=dev)
+            g8 = sv8.inp
 
             def head_call():
-                dsv.dspark_draft_block_ex(inp["U"], inp["h"], inp["W1"], inp["W2"], inp["w"], 0.0, inp["x0"], T,
-                                          seed, head_, out=outd, workspace=ws_h)
+                dsv.dspark_draft_block_ex(g8["U"], g8["h"], g8["W1"], g8["W2"], g8["w"], 0.0, g8["x0"], sv8.T,
+                                          c8.seed, head_, out=sv8.outd, workspace=ws_h)
             h_fn = graphed(head_call)
             h_times, _ = timed(h_fn or head_call, 20, 3)
-            heads_x[name] = {"draft_ms": sum(h_times) / len(h_times), "cuda_graph": h_fn is not None}
+            heads_x[name] = {"workload": c8.name, "draft_ms": sum(h_times) / len(h_times),
+                             "cuda_graph": h_fn is not None}
+        del sv8
     # several rounds with the anchor carried (the last emitted token), one CUDA graph over
-    # a pool of 8 synthetic rounds of the same shape
+    # a pool of 8 synthetic rounds of the Qwen3-8B shape
     multi = None
     if not args.skip_rounds:
+        c8 = wl.QWEN3_8B
         R, P = 32, 8
-        pool_ = wl.make_round_pool(cfg, P, device=dev)
+        pool_ = wl.make_round_pool(c8, P, device=dev)
         anchor_ = pool_["x0"].clone()
-        ws_r = torch.empty(lib.dspark_decode_rounds_workspace_size(B, G, V, r), dtype=torch.uint8, device=dev)
-        rout = dict(tokens=torch.empty((R, B, G + 1), dtype=torch.int32, device=dev),
-                    n_emitted=torch.empty((R, B), dtype=torch.int32, device=dev),
+        ws_r = torch.empty(lib.dspark_decode_rounds_workspace_size(c8.B, c8.gamma, c8.V, c8.r), dtype=torch.uint8,
+                           device=dev)
+        rout = dict(tokens=torch.empty((R, c8.B, c8.gamma + 1), dtype=torch.int32, device=dev),
+                    n_emitted=torch.empty((R, c8.B), dtype=torch.int32, device=dev),
                     stats=torch.empty((R, 2), dtype=torch.float64, device=dev))
 
         def rounds_call():
             anchor_.copy_(pool_["x0"])
             dsv.dspark_decode_rounds(pool_["U"], pool_["h"], pool_["t"], pool_["W1"], pool_["W2"], pool_["w"], 0.0,
-                                     pool_["sps"], anchor_, R, T, seed, out=rout, workspace=ws_r)
+                                     pool_["sps"], anchor_, R, c8.temperature, c8.seed, out=rout, workspace=ws_r)
         rounds_fn = graphed(rounds_call)
         r_times, _ = timed(rounds_fn or rounds_call, 10, 3)
         r_ms = sum(r_times) / len(r_times)
         st_ = rout["stats"].cpu()
-        multi = {"rounds": R, "pool": P, "cuda_graph": rounds_fn is not None, "ms_per_round": r_ms / R,
+        multi = {"workload": c8.name, "rounds": R, "pool": P, "cuda_graph": rounds_fn is not None,
+                 "ms_per_round": r_ms / R,
                  "emitted_tokens_per_s": float(rout["n_emitted"].sum().item()) / (r_ms * 1e-3),
                  "E_tau": float(st_[:, 0].mean()), "realised_tau": float(st_[:, 1].mean())}
         del pool_
@@ -468,15 +563,19 @@ def run_gpu(args):
 
     line = {"metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; shapes of the Qwen3-8B draft setting)",
-            "config": dict(workload_config(world), cuda_graph=use_graph),
-            "hbm_gbs": hbm_gbs, "hbm_frac": hbm_gbs / peak, "roofline": roofline, "e2e": e2e,
-            "gpu_launches": launches_per_step * args.steps, "clocks": clk,
-            "extra": {"greedy_round": greedy, "per_call": breakdown, "accept_rate_tv": tv, "multi_round": multi,
-                      "heads": heads_x,
-                      "accepted_per_request": float(nacc.mean()), "scheduled_rows": int((ell + 1).sum())}}
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(inp, T, seed)
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; shapes of the pages' high-concurrency serving setting)",
+            "config": dict(workload_config(world), cuda_graph=head["cuda_graph"]),
+            "hbm_gbs": head["round_hbm_gbs"], "hbm_frac": head["round_hbm_gbs"] / peak, "roofline": roofline,
+            "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clk,
+            "extra": {"per_call": head["per_call"], "scheduled_rows": head["scheduled_rows"],
+                      "rejected_requests": head["rejected_requests"],
+                      "accepted_per_request": head["accepted_per_request"],
+                      "exempt": parity,
+                      "serving_configs": extra_cfgs, "accept_rate_tv": tv, "multi_round": multi,
+                      "heads": heads_x}}
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -487,7 +586,7 @@ def run_gpu(args):
 # ------------------------------------------------------------ oracle ---
 def workload_config(world):
     from serving_draft_verify_gb300 import workloads as wl
-    c = wl.QWEN3_8B
+    c = wl.HIGH_CONC
     return {"workload": WORKLOAD, "B": c.B, "gamma": c.gamma, "V": c.V, "H": c.H, "r": c.r,
             "temperature": c.temperature, "l2": "flushed between steps (512 MiB write outside the timed step)",
             "parallelism": "replicas" if world > 1 else "single GPU"}
@@ -500,11 +599,13 @@ def host_threads():
         return os.cpu_count()
 
 
-def oracle_inputs(inp):
-    """The round's inputs as float64 numpy arrays (converted once)."""
+def oracle_inputs(inp, nreq=None):
+    """The round's inputs (the first `nreq` requests) as float64 numpy arrays."""
     from serving_draft_verify_gb300 import workloads as wl
-    out = {k: wl.to_f64(inp[k]) for k in ("U", "h", "t", "W1", "W2", "w")}
-    out["x0"] = inp["x0"].cpu().numpy()
+    n = inp["U"].shape[0] if nreq is None else nreq
+    out = {k: wl.to_f64(inp[k][:n]) for k in ("U", "h", "t")}
+    out.update({k: wl.to_f64(inp[k]) for k in ("W1", "W2", "w")})
+    out["x0"] = inp["x0"][:n].cpu().numpy()
     return out
 
 
@@ -526,35 +627,38 @@ def oracle_round(f64, T, seed, nreq):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(inp, T, seed, min_seconds=10.0, max_rounds=24):
-    """The oracle on the host cores: whole 64-request rounds of the same workload,
-    repeated until at least `min_seconds` of work (at most `max_rounds`)."""
-    f64 = oracle_inputs(inp)
+def cpu_baseline(inp, T, seed, min_seconds=10.0, max_rounds=24, nreq=16):
+    """The oracle on the host cores: rounds (draft, schedule over the sample, verify)
+    of the first `nreq` requests of the same workload, repeated until at least
+    `min_seconds` of work (at most `max_rounds`)."""
+    f64 = oracle_inputs(inp, nreq)
     B, G = f64["U"].shape[0], f64["U"].shape[1]
     spent, n = 0.0, 0
     while n < max_rounds and (n == 0 or spent < min_seconds):
         spent += oracle_round(f64, T, seed, B)
         n += 1
     return {"value": n * B * G / spent, "unit": "rows/s", "cores": host_threads(), "kind": "oracle",
-            "sample": f"{n} full rounds (draft, schedule, verify) of all {B} requests x {G} positions, "
-                      f"float64 numpy (BLAS threads up to the core count); {spent:.1f} s"}
+            "sample": f"{n} rounds (draft, schedule over the sample, verify) of the first {B} requests x {G} "
+                      f"positions, float64 numpy (BLAS threads up to the core count); {spent:.1f} s"}
 
 
 def run_reference(args):
     world, rank, local = dist_setup()
     if rank != 0:
         return
-    import torch
     from serving_draft_verify_gb300 import workloads as wl
-    cfg = wl.QWEN3_8B
-    inp = wl.make_draft_inputs(cfg, device="cpu")
+    cfg = wl.HIGH_CONC
+    # requests per step: one or two requests' full rounds (16 positions over the whole
+    # vocabulary), so that even a long run stays within a few minutes.  The sample is an
+    # instance of the same workload with B = nreq (every per-request shape and value
+    # distribution of the config; W1, W2, w of the same shapes), so that the 10 GB of
+    # the full batch are not drawn on the host for two of its requests.
+    nreq = 2 if args.steps <= 100 else 1
+    inp = wl.make_draft_inputs(wl.scaled(cfg, B=nreq), device="cpu")
     for _ in range(args.warmup):
         pass                                              # the oracle has nothing to warm
     times = []
-    # requests per step: about 0.06 s of oracle work each, so that even a long run
-    # (--steps 500) stays near a minute of host time
-    nreq = 4 if args.steps <= 200 else (2 if args.steps <= 400 else 1)
-    f64 = oracle_inputs(inp)
+    f64 = oracle_inputs(inp, nreq)
     for _ in range(args.steps):
         times.append(oracle_round(f64, cfg.temperature, cfg.seed, nreq))
     total = sum(times)
@@ -564,8 +668,9 @@ def run_reference(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded)", "config": workload_config(1),
             "cpu_baseline": {"value": value, "unit": "rows/s", "cores": host_threads(), "kind": "oracle",
-                             "sample": f"{nreq} of {cfg.B} requests x {cfg.gamma} positions per step, one "
-                                       f"round each (draft, schedule over the sample, verify)"},
+                             "sample": f"{nreq} request(s) x {cfg.gamma} positions per step of the same "
+                                       f"workload (a B = {nreq} instance), one round each (draft, schedule over "
+                                       f"the sample, verify)"},
             "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
@@ -613,7 +718,7 @@ def run_tv_only(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--skip-tv", action="store_true")
@@ -621,6 +726,12 @@ def main():
     ap.add_argument("--skip-heads", action="store_true", help="skip the gated / recurrent head extra")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the round's calls directly, without a CUDA graph")
+    ap.add_argument("--skip-e2e", action="store_true", help="skip the end-to-end (host memory) measurement")
+    ap.add_argument("--e2e-steps", type=int, default=40, help="steps of the end-to-end measurement (at most --steps)")
+    ap.add_argument("--skip-extra-configs", action="store_true",
+                    help="skip the Qwen3-8B-shaped and 27B-draft-shaped serving rounds")
+    ap.add_argument("--parity-requests", type=int, default=8,
+                    help="requests of the headline round the oracle re-checks (exempt decisions reported)")
     ap.add_argument("--phase-traffic", type=float, default=None,
                     help="dram bytes per draft phase launch from an ncu capture (reported as roofline.traffic)")
     ap.add_argument("--tv-rows", type=int, default=None,

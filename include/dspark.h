@@ -38,13 +38,14 @@
  *     verifies position k, and t_logits[b][gamma] the bonus row.
  *   - Random draws use Philox4x32-10 (Salmon et al., SC'11) keyed by
  *     (seed_lo, seed_hi) with counter (index >> 2, k, b, stream), output word
- *     index & 3.  Streams: 0 draft token, 1 accept uniform, 2 residual token,
- *     3 draft block, 4 residual block, 5 target token, 6 target block.
- *   - Sampling from a softmax uses an exact two-level Gumbel-max over blocks
- *     of DSPARK_SAMPLE_BLOCK consecutive vocabulary indices: pick the block by
- *     argmax(logsumexp(block) + Gumbel), then the token inside it by
- *     argmax(logit + Gumbel); ties go to the lowest index.  This draws token v
- *     with probability exactly softmax(.)_v.
+ *     index & 3.  Streams: 0 draft token (index = vocabulary index), 1 accept
+ *     uniform (index 0), 2 the token verification emits (residual, bonus, or
+ *     the draw from p_t when a residual has no mass; one per request).
+ *   - Sampling from a softmax is Gumbel-max over the whole vocabulary: the
+ *     token argmax_v(lw_v - ln(-ln u_v)) with u_v = ((w_v >> 9) + 1/2) 2^-23
+ *     from the word of index v, lw the log-weights (logits / T, or ln q of the
+ *     residual q); ties go to the lowest index.  This draws token v with
+ *     probability exactly softmax(lw)_v.
  */
 #ifndef DSPARK_H
 #define DSPARK_H
@@ -56,7 +57,6 @@
 extern "C" {
 #endif
 
-#define DSPARK_SAMPLE_BLOCK 64
 #define DSPARK_MAX_GAMMA 32
 
 typedef enum {
@@ -118,16 +118,21 @@ dspark_status_t dspark_draft_block(int B, int gamma, int V, int H, int r, dspark
  * and results are those of dspark_draft_block; the scratch lives in a fixed
  * 4 MiB array inside the library's device image, held by every GPU that loads
  * the library until the process exits.
- *   - Calls whose dspark_draft_block_workspace_size(B, gamma, V, r) exceeds
- *     4 MiB return DSPARK_ERR_UNSUPPORTED (B * gamma up to about 2000).
+ *   - Arguments are checked as dspark_draft_block checks them
+ *     (DSPARK_ERR_INVALID_ARGUMENT); then calls whose
+ *     dspark_draft_block_workspace_size(B, gamma, V, r) exceeds 4 MiB return
+ *     DSPARK_ERR_UNSUPPORTED (B * gamma up to about 2100), and so do calls on
+ *     a device ordinal of 64 or more.
  *   - All calls share the one array: calls that overlap on the GPU (other
  *     streams, other host threads) race and corrupt each other's results.
  *     Each call clears what must start at zero.
  *   - The first call on a device looks up the array's device address with
  *     cudaGetSymbolAddress (with that device current); make that first call
  *     before any stream capture.
- *   - Device-side checks (token ids out of range) record their status in the
- *     internal array, which the caller cannot read: validate x0 beforehand.
+ *   - Device-side status (a token id out of range, or a bounded wait that
+ *     ran out) is recorded in the internal array, which the caller cannot
+ *     read: such a call still returns DSPARK_OK with unfinished outputs.
+ *     Validate x0 beforehand; a timeout needs a GPU that stalls for seconds.
  * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
  * ------------------------------------------------------------------------ */
 dspark_status_t dspark_draft_block_noalloc(int B, int gamma, int V, int H, int r, dspark_dtype_t dt,

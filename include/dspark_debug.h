@@ -54,6 +54,19 @@ dspark_status_t dspark_debug_force_phase_launches(int enable);
 dspark_status_t dspark_debug_bounded_wait(void* workspace, size_t workspace_bytes, uint64_t limit_ns,
                                           dspark_stream_t stream);
 
+/* Test hook for the sampler's noise: E[i] = -ln u_i for u_i = ((words[i] >> 9)
+ * + 1/2) 2^-23, computed on the GPU by the same routine the draws use (the
+ * Gumbel variate of the draw is -ln E).  words [n] uint32, E [n] float32,
+ * device pointers; n >= 0.  Asynchronous on `stream`. */
+dspark_status_t dspark_debug_exp_draws(const uint32_t* words, float* E, int64_t n, dspark_stream_t stream);
+
+/* Test hook for the per-row Philox4x32-10 of the draws: out[4 i + j] = word j
+ * of Philox(key (seed_lo, seed_hi); counter (q0 + i, k, b, stream)) for
+ * i < n, computed on the GPU by the routine the draws use.  out [4 n] uint32
+ * device pointer; n >= 0.  Asynchronous on `stream`. */
+dspark_status_t dspark_debug_philox_rows(uint64_t seed, uint32_t k, uint32_t b, uint32_t stream, uint32_t q0,
+                                         int64_t n, uint32_t* out, dspark_stream_t stream_);
+
 #ifdef __cplusplus
 }
 #endif

@@ -7,7 +7,6 @@ include/dspark.h); this package holds its build script, the ctypes binding
 from ._binding import (  # noqa: F401
     DSparkError,
     LIB_PATH,
-    SAMPLE_BLOCK,
     MAX_GAMMA,
     dspark_accept_rate_tv,
     dspark_training_loss,

@@ -17,7 +17,6 @@ LIB_PATH = os.path.join(_HERE, "_build", "libdspark.so")
 DSPARK_OK = 0
 DSPARK_F32 = 0
 DSPARK_BF16 = 1
-SAMPLE_BLOCK = 64
 MAX_GAMMA = 32
 
 _c_int, _c_i64, _c_u64, _c_size, _c_float = (ctypes.c_int, ctypes.c_int64, ctypes.c_uint64,
@@ -56,6 +55,9 @@ _SIGNATURES = {
     "dspark_debug_phase_times": (_c_int, [_p, _c_int]),
     "dspark_debug_force_phase_launches": (_c_int, [_c_int]),
     "dspark_debug_bounded_wait": (_c_int, [_p, _c_size, ctypes.c_uint64, _p]),
+    "dspark_debug_exp_draws": (_c_int, [_p, _p, _c_i64, _p]),
+    "dspark_debug_philox_rows": (_c_int, [_c_u64, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
+                                          ctypes.c_uint32, _c_i64, _p, _p]),
 }
 
 _lib = None
@@ -448,6 +450,25 @@ def bounded_wait(limit_ns, workspace=None, stream=None):
     _check("dspark_debug_bounded_wait", lib.dspark_debug_bounded_wait(_ptr(ws), _nbytes(ws), int(limit_ns),
                                                                       _stream(stream)))
     return ws
+
+
+def exp_draws(words, stream=None):
+    """E = -ln u of the sampler's noise for uint32 words (an int32 / int64 CUDA tensor
+    holding the 32-bit patterns), computed by the library's device routine."""
+    w = words.to(torch.int32).contiguous()
+    E = torch.empty(w.shape, dtype=torch.float32, device=w.device)
+    _check("dspark_debug_exp_draws", load().dspark_debug_exp_draws(_ptr(w), _ptr(E), w.numel(), _stream(stream)))
+    return E
+
+
+def philox_rows(seed, k, b, stream_id, q0, n, device="cuda", stream=None):
+    """[n, 4] words of Philox4x32-10 at counters (q0 + i, k, b, stream_id) (int64 tensor
+    of the unsigned 32-bit values), computed by the library's per-row device routine."""
+    out = torch.empty((int(n), 4), dtype=torch.int32, device=device)
+    _check("dspark_debug_philox_rows",
+           load().dspark_debug_philox_rows(int(seed) & (2 ** 64 - 1), int(k), int(b), int(stream_id), int(q0),
+                                           int(n), _ptr(out), _stream(stream)))
+    return out.to(torch.int64) & 0xFFFFFFFF
 
 
 def phase_times():

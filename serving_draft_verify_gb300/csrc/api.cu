@@ -1,7 +1,51 @@
-// C-ABI helpers that belong to no single operation: status strings and the
-// device status read-back.
+// C-ABI helpers that belong to no single operation: status strings, the
+// device status read-back, and the test hooks of the sampler's noise.
 #include "common.cuh"
 #include "host_common.h"
+#include "../../include/dspark_debug.h"
+
+namespace dspark {
+namespace {
+__global__ void debug_exp_draws(const uint32_t* __restrict__ w, float* __restrict__ E, int64_t n) {
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        E[i] = exp_draw(w[i]);
+}
+__global__ void debug_philox_rows(uint64_t seed, uint32_t k, uint32_t b, uint32_t stream, uint32_t q0, int64_t n,
+                                  uint32_t* __restrict__ out) {
+    const PhiloxRow pr = philox_row_setup(seed, k, b, stream);
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const U4 r = philox_row(pr, q0 + static_cast<uint32_t>(i));
+        out[4 * i] = r.x;
+        out[4 * i + 1] = r.y;
+        out[4 * i + 2] = r.z;
+        out[4 * i + 3] = r.w;
+    }
+}
+}  // namespace
+}  // namespace dspark
+
+extern "C" dspark_status_t dspark_debug_exp_draws(const uint32_t* words, float* E, int64_t n,
+                                                  dspark_stream_t stream) {
+    if (n < 0 || (n > 0 && (words == nullptr || E == nullptr))) return DSPARK_ERR_INVALID_ARGUMENT;
+    dspark::clear_stale_error();
+    if (n == 0) return DSPARK_OK;
+    const int64_t blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+    dspark::debug_exp_draws<<<static_cast<int>(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(words, E, n);
+    return dspark::launch_status();
+}
+
+extern "C" dspark_status_t dspark_debug_philox_rows(uint64_t seed, uint32_t k, uint32_t b, uint32_t stream,
+                                                    uint32_t q0, int64_t n, uint32_t* out, dspark_stream_t stream_) {
+    if (n < 0 || (n > 0 && out == nullptr)) return DSPARK_ERR_INVALID_ARGUMENT;
+    dspark::clear_stale_error();
+    if (n == 0) return DSPARK_OK;
+    const int64_t blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+    dspark::debug_philox_rows<<<static_cast<int>(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream_)>>>(
+        seed, k, b, stream, q0, n, out);
+    return dspark::launch_status();
+}
 
 extern "C" const char* dspark_status_string(dspark_status_t s) {
     switch (s) {

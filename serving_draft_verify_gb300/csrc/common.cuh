@@ -113,6 +113,8 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 }
 
 // ---------------------------------------------------------------- Philox ---
+constexpr float kLn2f = 0.69314718055994531f;
+
 // Philox4x32-10 (Salmon et al., SC'11): per round, 32x32->64 products of
 // c0 and c2 with the two round multipliers, the high halves xored into the
 // other words with the round key, key bumped by the Weyl constants.
@@ -132,21 +134,14 @@ __device__ __forceinline__ U4 philox4x32_10_inline(U4 c, uint32_t k0, uint32_t k
     }
     return c;
 }
-// Out of line (one copy per module): the draft engine's tile epilogues call it for
-// every tile, so its code stays in the instruction caches for the token draws that
-// follow a vocabulary-wide stream (inlined copies there were fetched cold from DRAM).
-// Kernels without that pattern (the verify rows pass) call the inline form.
 static __device__ __noinline__ U4 philox4x32_10(U4 c, uint32_t k0, uint32_t k1) {
     return philox4x32_10_inline(c, k0, k1);
 }
 enum Stream : uint32_t {
-    kStreamDraftToken = 0,
-    kStreamAccept = 1,
-    kStreamResidualToken = 2,
-    kStreamDraftBlock = 3,
-    kStreamResidualBlock = 4,
-    kStreamTargetToken = 5,
-    kStreamTargetBlock = 6,
+    kStreamDraftToken = 0,    // Gumbel noise of the draft token x_k, one word per vocabulary index
+    kStreamAccept = 1,        // acceptance uniform of the rejection test (index 0)
+    kStreamVerifyToken = 2,   // Gumbel noise of the token verification emits (residual, bonus or
+                              // the draw from p_t when a residual has no mass; one per request)
 };
 // The 32-bit word keyed by (seed, request b, position k, stream, index).
 __device__ __forceinline__ uint32_t draw_word(uint64_t seed, uint32_t b, uint32_t k, uint32_t stream,
@@ -156,6 +151,58 @@ __device__ __forceinline__ uint32_t draw_word(uint64_t seed, uint32_t b, uint32_
     const uint32_t sel = index & 3u;
     return sel == 0 ? r.x : sel == 1 ? r.y : sel == 2 ? r.z : r.w;
 }
+
+// Philox4x32-10 for the counters (q, k, b, stream) of one row (k, b, stream
+// fixed, q varying).  The first round's product of the third counter word (b)
+// and the second round's product of the first word (which after round one no
+// longer depends on q) are the same for every q: they are formed once here,
+// so a call costs eighteen 32x32->64 products instead of twenty.  The result
+// is bit-identical to philox4x32_10({q, k, b, stream}, key).
+struct PhiloxRow {
+    uint32_t k0, k1;     // key
+    uint32_t r1_x;       // round 1: word x (constant)
+    uint32_t r1_y;       // round 1: word y (constant)
+    uint32_t r1_z;       // round 1: word z = hi(M0 q) ^ r1_z
+    uint32_t r2_y;       // round 2: word y ^ key (constant part of the new x)
+    uint32_t r2_hi0;     // round 2: hi(M0 r1_x) ^ key1 (xored with lo(M0 q) into the new z)
+    uint32_t r2_lo0;     // round 2: lo(M0 r1_x) (the new w)
+};
+__device__ __forceinline__ PhiloxRow philox_row_setup(uint64_t seed, uint32_t k, uint32_t b, uint32_t stream) {
+    PhiloxRow r;
+    r.k0 = static_cast<uint32_t>(seed);
+    r.k1 = static_cast<uint32_t>(seed >> 32);
+    const uint32_t lo1 = 0xCD9E8D57u * b, hi1 = __umulhi(0xCD9E8D57u, b);
+    r.r1_x = hi1 ^ k ^ r.k0;
+    r.r1_y = lo1;
+    r.r1_z = stream ^ r.k1;
+    const uint32_t k0b = r.k0 + 0x9E3779B9u, k1b = r.k1 + 0xBB67AE85u;
+    r.r2_y = r.r1_y ^ k0b;
+    r.r2_hi0 = __umulhi(0xD2511F53u, r.r1_x) ^ k1b;
+    r.r2_lo0 = 0xD2511F53u * r.r1_x;
+    return r;
+}
+__device__ __forceinline__ U4 philox_row(const PhiloxRow& r, uint32_t q) {
+    // round 1: only the product of q varies
+    const uint32_t lo0 = 0xD2511F53u * q, hi0 = __umulhi(0xD2511F53u, q);
+    const uint32_t z1 = hi0 ^ r.r1_z;
+    // round 2: the product of word x is constant, the product of z1 varies
+    const uint32_t lo1 = 0xCD9E8D57u * z1, hi1 = __umulhi(0xCD9E8D57u, z1);
+    U4 c{hi1 ^ r.r2_y, lo1, r.r2_hi0 ^ lo0, r.r2_lo0};
+    uint32_t k0 = r.k0 + 2u * 0x9E3779B9u, k1 = r.k1 + 2u * 0xBB67AE85u;
+#pragma unroll
+    for (int i = 2; i < 10; ++i) {
+        const uint32_t a0 = 0xD2511F53u * c.x, b0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t a1 = 0xCD9E8D57u * c.z, b1 = __umulhi(0xCD9E8D57u, c.z);
+        c = U4{b1 ^ c.y ^ k0, a1, b0 ^ c.w ^ k1, a0};
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+__device__ __forceinline__ uint32_t u4_word(const U4& r, uint32_t sel) {
+    return sel == 0 ? r.x : sel == 1 ? r.y : sel == 2 ? r.z : r.w;
+}
+
 // u in (0, 1): ((w >> 9) + 1/2) * 2^-23 (exact in float32).
 __device__ __forceinline__ float uniform_open(uint32_t w) {
     return (static_cast<float>(w >> 9) + 0.5f) * 1.1920928955078125e-07f;
@@ -164,14 +211,31 @@ __device__ __forceinline__ float uniform_open(uint32_t w) {
 __device__ __forceinline__ float uniform_accept(uint32_t w) {
     return static_cast<float>(w >> 8) * 5.9604644775390625e-08f;
 }
-// Standard Gumbel variate -ln(-ln u).  For u near 1, -ln u is formed as
-// -log1p(u - 1) (u - 1 is exact there) to keep its relative accuracy.
-__device__ __forceinline__ float gumbel_of_inline(float u) {
-    const float e = (u > 0.5f) ? -log1pf(u - 1.0f) : -logf(u);
-    return -logf(e);
+
+// log2 on the special-function unit (lg2.approx.ftz: absolute error about 2^-22
+// for arguments in [1/2, 2]).
+__device__ __forceinline__ float fast_log2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
-// Out of line for the same reason as philox4x32_10.
-static __device__ __noinline__ float gumbel_of(float u) { return gumbel_of_inline(u); }
+
+// The exponential variate E = -ln u of the Gumbel draw G = -ln(-ln u) = -ln E,
+// for u = ((w >> 9) + 1/2) 2^-23.  Draws compare e_v / E_v (or lw_v - log2 E_v),
+// so E must keep its relative accuracy where it is small, i.e. for u near 1.
+// u and s = 1 - u are both exact in float32 (odd multiples of 2^-24).  For
+// s < 1/16, E = -ln(1 - s) is its Taylor series s + s^2/2 + s^3/3 + s^4/4 + s^5/5
+// (the next term is below 1.7e-7 of the sum); otherwise -ln u >= 0.0645 and the
+// special-function log2 (absolute error ~2^-22) keeps the relative error of E
+// below ~3e-6.  A GPU test checks every one of the 2^23 values against float64.
+__device__ __forceinline__ float exp_draw(uint32_t w) {
+    const float f = __uint_as_float((w >> 9) | 0x3F800000u);   // 1 + m 2^-23
+    const float u = f - 0.999999940395355225f;                 // (m + 1/2) 2^-23, exact
+    const float s = 1.0f - u;                                  // exact
+    const float series = s * fmaf(s, fmaf(s, fmaf(s, fmaf(s, 0.2f, 0.25f), 0.333333343f), 0.5f), 1.0f);
+    const float viaLog = -kLn2f * fast_log2(u);
+    return (s < 0.0625f) ? series : viaLog;
+}
 
 // ------------------------------------------------------------ reductions ---
 __device__ __forceinline__ float warp_max(float v) {

@@ -2,21 +2,20 @@
 // (DeepSpec walkthrough, section 3.2 stage two, `sample_block_tokens`):
 //   for k = 1..gamma:  z_k = U_k + W2 . W1[x_{k-1}]   (VanillaMarkovHead, eq. 5;
 //                      dspark_draft_block_ex: W2 . e_k of a gated or recurrent head)
-//                      x_k ~ softmax(z_k / T)          (two-level Gumbel-max)
+//                      x_k ~ softmax(z_k / T)          (Gumbel-max over the vocabulary)
 // plus the confidence head and survival product (section 3.3).
 //
 // Tensor-core path (bf16, r % 64 == 0): one cooperative launch of the bias
 // engine (engine.cuh) runs every position; between positions its CTAs meet at
-// a grid barrier and draw x_{k-1} (second Gumbel level) for the requests each
-// owns, publishing each token as it is drawn.  After the last position the
-// same launch draws x_gamma and finalizes the requests each CTA owns.
+// a grid barrier, after which each request's published winner is x_{k-1}.
+// After the last position the same launch writes x_gamma and finalizes the
+// requests each CTA owns.
 // CUDA-core path (and the tensor-core path when the grid cannot be
-// co-resident): per position a phase kernel (every 64-token block's
-// logsumexp and Gumbel key, the CTA's best block by atomicMax, its (max, sum)
-// partial) and a winner kernel (two warps per request: z on the winning block
-// and the token inside it).
-// There, after the last position a finalize kernel forms lse_d / logp_d and
-// the confidence c_k and survival a_k.
+// co-resident): per position a phase kernel (the Gumbel-max draw and the
+// (max, sum) of each chunk of the vocabulary, the chunk's winner published by
+// atomicMax) and a winner kernel that writes x_k.  There, after the last
+// position a finalize kernel forms lse_d / logp_d and the confidence c_k and
+// survival a_k.
 #include "engine.cuh"
 #include "../../include/dspark_debug.h"
 
@@ -28,48 +27,47 @@ using eng::ld_elem;
 using eng::pack_key;
 using eng::prev_token;
 using eng::unpack_idx;
+using eng::Best;
+using eng::best_take;
 using DraftWs = eng::Ws;
 
-// Workspace: status | grid-barrier counter | tagged tokens [B] | words [gamma][B] |
-// partials [gamma][B][kMaxChunks] | ytok [gamma][B].  The first four are
-// cleared by every call.
-inline size_t draft_ws_layout(int B, int gamma, size_t* o_bar, size_t* o_xw, size_t* o_words, size_t* o_part,
-                              size_t* o_ytok) {
+// Workspace: status | grid-barrier counter | words [gamma][B] | partials
+// [gamma][B][kMaxChunks] (max, sum) | y of each chunk's best token
+// [gamma][B][kMaxChunks].  The first three are cleared by every call; the
+// chunk entries are written before they are read.
+inline size_t draft_ws_layout(int B, int gamma, size_t* o_bar, size_t* o_words, size_t* o_part, size_t* o_yb) {
     size_t o = kStatusBytes;
     *o_bar = o;
     o += 256;
-    *o_xw = o;
-    o += round_up(static_cast<size_t>(B) * 8, 256);
     *o_words = o;
     o += round_up(static_cast<size_t>(gamma) * B * 8, 256);
     *o_part = o;
     o += round_up(static_cast<size_t>(gamma) * B * kMaxChunks * 8, 256);
-    *o_ytok = o;
-    o += round_up(static_cast<size_t>(gamma) * B * 4, 256);
+    *o_yb = o;
+    o += round_up(static_cast<size_t>(gamma) * B * kMaxChunks * 4, 256);
     return o;
 }
 
 inline DraftWs draft_ws(void* workspace, int B, int gamma, size_t* clear_bytes) {
-    size_t ob, ox, ow, op, oy;
-    draft_ws_layout(B, gamma, &ob, &ox, &ow, &op, &oy);
+    size_t ob, ow, op, oy;
+    draft_ws_layout(B, gamma, &ob, &ow, &op, &oy);
     uint8_t* wsb = static_cast<uint8_t*>(workspace);
     *clear_bytes = op;
     return DraftWs{reinterpret_cast<StatusBlock*>(wsb), reinterpret_cast<unsigned long long*>(wsb + ow),
                    reinterpret_cast<float2*>(wsb + op), reinterpret_cast<float*>(wsb + oy),
-                   reinterpret_cast<unsigned int*>(wsb + ob), reinterpret_cast<unsigned long long*>(wsb + ox)};
+                   reinterpret_cast<unsigned int*>(wsb + ob)};
 }
 
 namespace {
 
-// Block key: logsumexp of the block in natural units plus a Gumbel draw.
-__device__ __forceinline__ float block_key(float m, float s, uint64_t seed, int b, int k, int blk) {
-    const float u = uniform_open(draw_word(seed, b, k, kStreamDraftBlock, static_cast<uint32_t>(blk)));
-    return (m + log2f(s)) * kLn2 + gumbel_of(u);
-}
-
 // ==================================================== CUDA-core phase ====
 constexpr int kSimtThreads = 256;
 
+// Position k of request b (blockIdx.y), chunk blockIdx.x of the vocabulary's
+// 64-token blocks: y = (U_k + W2 . e) * cscale per token (e = W1[x_{k-1}] or
+// the head's row), the chunk's (max, sum) of 2^y and its Gumbel-max winner
+// (key y_v - log2 E_v, stream 0; greedy: the largest y).  Lane l of a warp
+// takes tokens 64 blk + 2 l and + 1 of each block the warp visits.
 template <bool kBF16>
 __global__ void __launch_bounds__(kSimtThreads)
 draft_phase_simt(int B, int gamma, int V, int r, int k, const void* __restrict__ U,
@@ -78,7 +76,7 @@ draft_phase_simt(int B, int gamma, int V, int r, int k, const void* __restrict__
                  const int32_t* __restrict__ x, float cscale, int greedy, uint64_t seed, int nchunk,
                  DraftWs ws) {
     __shared__ float e[256];
-    __shared__ float rk[kSimtThreads / 32], rm[kSimtThreads / 32], rs[kSimtThreads / 32];
+    __shared__ float rk[kSimtThreads / 32], rm[kSimtThreads / 32], rs[kSimtThreads / 32], ry[kSimtThreads / 32];
     __shared__ int ri[kSimtThreads / 32];
     const int b = blockIdx.y, chunk = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -90,131 +88,99 @@ draft_phase_simt(int B, int gamma, int V, int r, int k, const void* __restrict__
     const int lo = static_cast<int>(static_cast<long long>(chunk) * nblk / nchunk);
     const int hi = static_cast<int>(static_cast<long long>(chunk + 1) * nblk / nchunk);
     const size_t urow = (static_cast<size_t>(b) * gamma + (k - 1)) * V;
-    float best = -INFINITY, M = -INFINITY, S = 0.f;
-    int best_i = 0x7FFFFFFF;
+    const PhiloxRow pr = philox_row_setup(seed, static_cast<uint32_t>(k), static_cast<uint32_t>(b), kStreamDraftToken);
+    Best best{-INFINITY, 0x7FFFFFFF, 0.f};
+    float M = -INFINITY, S = 0.f;
     for (int blk = lo + warp; blk < hi; blk += kSimtThreads / 32) {
+        const int v = blk * 64 + 2 * lane;
         float y[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int v = blk * 64 + h * 32 + lane;
-            if (v < V) {
+            if (v + h < V) {
                 float acc = 0.f;
-                for (int j = 0; j < r; ++j) acc = fmaf(ld_elem<kBF16>(W2, static_cast<size_t>(v) * r + j), e[j], acc);
-                y[h] = (ld_elem<kBF16>(U, urow + v) + acc) * cscale;
+                for (int j = 0; j < r; ++j)
+                    acc = fmaf(ld_elem<kBF16>(W2, static_cast<size_t>(v + h) * r + j), e[j], acc);
+                y[h] = (ld_elem<kBF16>(U, urow + v + h) + acc) * cscale;
             } else {
                 y[h] = -INFINITY;
             }
         }
         if (greedy) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int v = blk * 64 + h * 32 + lane;
-                if (y[h] > best || (y[h] == best && v < best_i)) { best = y[h]; best_i = v; }
-            }
+            for (int h = 0; h < 2; ++h) best_take(best, y[h], v + h, y[h]);
         } else {
             const float mb = warp_max(fmaxf(y[0], y[1]));
-            const float sb = warp_sum(exp2f(y[0] - mb) + exp2f(y[1] - mb));
-            const float key = block_key(mb, sb, seed, b, k, blk);
-            if (key > best) { best = key; best_i = blk; }   // blocks ascend per warp
+            const float sb = warp_sum(fast_exp2(y[0] - mb) + fast_exp2(y[1] - mb));
             lse_merge(M, S, mb, sb);
-        }
-    }
-    if (greedy) {
-        // warp argmax, lowest index on ties
+            // the two tokens share a Philox block (v is even): words (v & 3) and (v & 3) + 1
+            const U4 pw = philox_row(pr, static_cast<uint32_t>(v) >> 2);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, best_i, o);
-            if (ob > best || (ob == best && oi < best_i)) { best = ob; best_i = oi; }
+            for (int h = 0; h < 2; ++h)
+                if (y[h] > -INFINITY)
+                    best_take(best, y[h] - fast_log2(exp_draw(u4_word(pw, (v + h) & 3))), v + h, y[h]);
         }
     }
-    if (lane == 0) { rk[warp] = best; ri[warp] = best_i; rm[warp] = M; rs[warp] = S; }
+    // warp: best (lowest index on ties)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ok = __shfl_xor_sync(0xffffffffu, best.key, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, best.idx, o);
+        const float oy = __shfl_xor_sync(0xffffffffu, best.y, o);
+        best_take(best, ok, oi, oy);
+    }
+    if (lane == 0) { rk[warp] = best.key; ri[warp] = best.idx; ry[warp] = best.y; rm[warp] = M; rs[warp] = S; }
     __syncthreads();
     if (threadIdx.x == 0) {
-        float bk = -INFINITY, m = -INFINITY, s = 0.f;
-        int bi = 0x7FFFFFFF;
+        Best cb{-INFINITY, 0x7FFFFFFF, 0.f};
+        float m = -INFINITY, s = 0.f;
         for (int w = 0; w < kSimtThreads / 32; ++w) {
-            if (rk[w] > bk || (rk[w] == bk && ri[w] < bi)) { bk = rk[w]; bi = ri[w]; }
+            best_take(cb, rk[w], ri[w], ry[w]);
             lse_merge(m, s, rm[w], rs[w]);
         }
         const size_t slot = static_cast<size_t>(k - 1) * B + b;
-        if (!greedy) ws.part[slot * kMaxChunks + chunk] = make_float2(m, s);
-        if (bk > -INFINITY) atomicMax(&ws.words[slot], pack_key(bk, static_cast<uint32_t>(bi)));
+        if (!greedy) {
+            ws.part[slot * kMaxChunks + chunk] = make_float2(m, s);
+            ws.ybest[slot * kMaxChunks + chunk] = cb.y;
+        }
+        if (cb.key > -INFINITY) atomicMax(&ws.words[slot], pack_key(cb.key, static_cast<uint32_t>(cb.idx)));
     }
 }
 
 // ============================================================ winner ====
-// Two warps per request: the token inside the winning 64-token block (greedy:
-// the argmax token itself) and y at that token.
-template <bool kBF16, int kCPL>
-__global__ void __launch_bounds__(64)
-draft_winner(int B, int gamma, int V, int r, int k, const void* __restrict__ U, const void* __restrict__ W1,
-             const void* __restrict__ E, const void* __restrict__ W2, const int32_t* __restrict__ x0,
-             int32_t* __restrict__ x,
-             float cscale, int greedy, uint64_t seed, DraftWs ws) {
-    __shared__ float sbest[2], sy[2];
-    __shared__ int sidx[2];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b = blockIdx.x;
-    const size_t slot = static_cast<size_t>(k - 1) * B + b;
-    const unsigned long long word = ws.words[slot];
-    if (word == 0ull) {
-        if (threadIdx.x == 0) { set_status(ws.status, DSPARK_ERR_DEVICE_CHECK, 3); x[b * gamma + k - 1] = 0; }
-        return;
-    }
+// x_k of every request: the token of its published winner.
+__global__ void __launch_bounds__(256)
+draft_winner(int B, int gamma, int V, int k, int32_t* __restrict__ x, DraftWs ws) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const unsigned long long word = ws.words[static_cast<size_t>(k - 1) * B + b];
     const uint32_t idx = unpack_idx(word);
-    if (idx >= static_cast<uint32_t>(greedy ? V : (V + 63) / 64)) {   // never produced by the phase kernels
-        if (threadIdx.x == 0) { set_status(ws.status, DSPARK_ERR_DEVICE_CHECK, 8); x[b * gamma + k - 1] = 0; }
-        return;
+    int tok = static_cast<int>(idx);
+    if (word == 0ull || idx >= static_cast<uint32_t>(V)) {   // never produced by the phase kernels
+        set_status(ws.status, DSPARK_ERR_DEVICE_CHECK, word == 0ull ? 3 : 8);
+        tok = 0;
     }
-    if (greedy) {
-        if (threadIdx.x == 0) { x[b * gamma + k - 1] = static_cast<int>(idx); ws.ytok[slot] = 0.f; }
-        return;
-    }
-    const float z = eng::block_logit<kBF16, kCPL>(b, gamma, k, V, r, static_cast<int>(idx), U, W1, E, W2, x0, x,
-                                                  ws.status);
-    const int v = static_cast<int>(idx) * 64 + warp * 32 + lane;
-    float score = -INFINITY, yv = 0.f;
-    if (z > -INFINITY) {
-        yv = z * cscale;
-        const float g = gumbel_of(uniform_open(draw_word(seed, b, k, kStreamDraftToken, static_cast<uint32_t>(v))));
-        score = yv + g * kLog2e;
-    }
-    int bi = (z > -INFINITY) ? v : 0x7FFFFFFF;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float os = __shfl_xor_sync(0xffffffffu, score, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        const float oy = __shfl_xor_sync(0xffffffffu, yv, o);
-        if (os > score || (os == score && oi < bi)) { score = os; bi = oi; yv = oy; }
-    }
-    if (lane == 0) { sbest[warp] = score; sidx[warp] = bi; sy[warp] = yv; }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int w = 0;
-        if (sbest[1] > sbest[0] || (sbest[1] == sbest[0] && sidx[1] < sidx[0])) w = 1;
-        x[b * gamma + k - 1] = (sidx[w] == 0x7FFFFFFF) ? 0 : sidx[w];
-        ws.ytok[slot] = sy[w];
-    }
+    x[b * gamma + k - 1] = tok;
 }
 
 // ========================================================== finalize ====
 // One CTA per request, one warp per position k (eng::finalize_position: lse_d,
 // logp_d and the confidence c_k); thread 0 then forms the float32 survival
 // product in k order.  Used by the per-position path; the cooperative launch
-// does the same work in its tail.
+// does the same work in its tail.  unit / nunits: the tokens per unit and the
+// units that the nchunk chunks of the phase launches split.
 template <bool kBF16>
 __global__ void __launch_bounds__(1024, 1)
 draft_finalize(int B, int gamma, int V, int H, int r, const void* __restrict__ h, const void* __restrict__ W1,
                const void* __restrict__ w, float bias, const int32_t* __restrict__ x0,
-               const int32_t* __restrict__ x, int greedy, int nchunk, float* __restrict__ lse_d,
-               float* __restrict__ logp_d, float* __restrict__ c, float* __restrict__ a, DraftWs ws) {
+               const int32_t* __restrict__ x, int greedy, int nchunk, int unit, int nunits,
+               float* __restrict__ lse_d, float* __restrict__ logp_d, float* __restrict__ c, float* __restrict__ a,
+               DraftWs ws) {
     const int warp = threadIdx.x >> 5;
     const int b = blockIdx.x;
     const int k = warp + 1;
     if (k <= gamma)
-        eng::finalize_position<kBF16>(b, k, B, gamma, V, H, r, h, W1, w, bias, x0, x, greedy, nchunk, ws.part,
-                                      ws.ytok, lse_d, logp_d, c, ws.status);
+        eng::finalize_position<kBF16>(b, k, B, gamma, V, H, r, h, W1, w, bias, x0, x, greedy, nchunk, unit, nunits,
+                                      ws.part, ws.ybest, lse_d, logp_d, c, ws.status);
     __syncthreads();
     if (threadIdx.x == 0) {
         float surv = 1.f;
@@ -469,14 +435,8 @@ int simt_chunks(int V) {
 
 bool g_force_phase_launches = false;
 
-template <bool kBF16>
-dspark_status_t launch_winner(int B, int gamma, int V, int r, int k, const void* U, const void* W1, const void* E,
-                              const void* W2, const int32_t* x0, int32_t* x, float cscale, int greedy, uint64_t seed,
-                              DraftWs ws, cudaStream_t s) {
-    if (kBF16 || r <= 128)
-        draft_winner<kBF16, 1><<<B, 64, 0, s>>>(B, gamma, V, r, k, U, W1, E, W2, x0, x, cscale, greedy, seed, ws);
-    else
-        draft_winner<kBF16, 2><<<B, 64, 0, s>>>(B, gamma, V, r, k, U, W1, E, W2, x0, x, cscale, greedy, seed, ws);
+dspark_status_t launch_winner(int B, int gamma, int V, int k, int32_t* x, DraftWs ws, cudaStream_t s) {
+    draft_winner<<<(B + 255) / 256, 256, 0, s>>>(B, gamma, V, k, x, ws);
     return launch_status();
 }
 
@@ -576,18 +536,21 @@ dspark_status_t draft_block_impl(int B, int gamma, int V, int H, int r, dspark_d
                 g_timing.recorded = k;
             }
             if (stt != DSPARK_OK) return stt;
-            stt = bf ? launch_winner<true>(B, gamma, V, r, k, U, W1, E, W2, x0, x, cscale, greedy, seed, ws, s)
-                     : launch_winner<false>(B, gamma, V, r, k, U, W1, E, W2, x0, x, cscale, greedy, seed, ws, s);
+            stt = launch_winner(B, gamma, V, k, x, ws, s);
             if (stt != DSPARK_OK) return stt;
         }
     }
     const int fthreads = 32 * gamma;
+    // the chunks of the phase launches: P ranges of 128-token tiles (tensor cores) or
+    // nchunk ranges of 64-token blocks (CUDA cores)
+    const int unit = tcp ? eng::kBN : 64;
+    const int nunits = (V + unit - 1) / unit;
     if (bf)
-        draft_finalize<true><<<B, fthreads, 0, s>>>(B, gamma, V, H, r, h, W1, w, bias, x0, x, greedy, nchunk, lse_d,
-                                                     logp_d, c, a, ws);
+        draft_finalize<true><<<B, fthreads, 0, s>>>(B, gamma, V, H, r, h, W1, w, bias, x0, x, greedy, nchunk, unit,
+                                                     nunits, lse_d, logp_d, c, a, ws);
     else
-        draft_finalize<false><<<B, fthreads, 0, s>>>(B, gamma, V, H, r, h, W1, w, bias, x0, x, greedy, nchunk, lse_d,
-                                                      logp_d, c, a, ws);
+        draft_finalize<false><<<B, fthreads, 0, s>>>(B, gamma, V, H, r, h, W1, w, bias, x0, x, greedy, nchunk, unit,
+                                                      nunits, lse_d, logp_d, c, a, ws);
     return launch_status();
 }
 
@@ -619,8 +582,8 @@ extern "C" size_t dspark_draft_block_workspace_size(int B, int gamma, int V, int
     (void)r;
     (void)V;
     if (B <= 0 || gamma <= 0 || V <= 0) return kStatusBytes;
-    size_t ob, ox, ow, op, oy;
-    return draft_ws_layout(B, gamma, &ob, &ox, &ow, &op, &oy);
+    size_t ob, ow, op, oy;
+    return draft_ws_layout(B, gamma, &ob, &ow, &op, &oy);
 }
 
 extern "C" dspark_status_t dspark_draft_block(int B, int gamma, int V, int H, int r, dspark_dtype_t dt,

@@ -3,12 +3,21 @@
 //   z_b = U[b][k_b-1] + W2 . W1[x_{k_b-1}]       (VanillaMarkovHead, eq. 5;
 //                                                 DeepSpec walkthrough 3.2)
 // tile by tile on the tensor cores and reduces them in its epilogue:
-//   kDraft     per 64-token block: logsumexp of z / T and a Gumbel block key
-//              (draft sampling), or the running argmax of z (greedy);
-//   kResidual  per 64-token block: the mass of max(0, p_t - p_d) and a Gumbel
-//              block key (the residual draw of verification, section 8.2).
-// Each CTA publishes its best block per row with a 64-bit atomicMax of
-// (key, ~block) and, for kDraft, its (max, sum) partial.
+//   kDraft     the running (max, sum) of 2^y, y = z log2e / T (the draft's
+//              log-normaliser), and the Gumbel-max draw over the vocabulary:
+//              the token maximising y_v - log2 E_v, E_v = -ln u_v with u_v
+//              from the Philox word of (request, position, index v, stream 0);
+//              greedy: the running argmax of z;
+//   kResidual  the Gumbel-max draw from the residual max(0, p_t - p_d)
+//              (section 8.2): the token maximising q_v / E_v, stream 2.
+// Inside a 32-token sub-block the draw is an exponential race: with
+// e_v = 2^(y_v - m) (already formed for the sum) the winner maximises e_v / E_v,
+// compared by cross-multiplication, so one logarithm per token (inside E_v) is
+// all the draw adds; the sub-block's winner enters the thread's running best
+// as the key y_v - log2 E_v.
+// Each CTA publishes its best token per row with a 64-bit atomicMax of
+// (key, ~token) and, for kDraft, its (max, sum) partial and the y of its best
+// token (for log p_d of the token that wins overall).
 //
 // Layout of one CTA (384 threads, one CTA per SM):
 //   warp 0      TMA producer: W2 tiles [128 tokens x 64 K] into a slab ring
@@ -24,9 +33,8 @@
 // Draft launches may cover positions k .. k_last (a cooperative launch, all
 // CTAs resident, TMEM and barriers set up once, the producer streaming W2
 // straight through all positions).  Between positions the grid meets at a
-// bounded counter barrier; then CTA c draws x_{k} for requests b = c (mod
-// grid) from the published block winners (pairs of warps rebuild z on the
-// winning block from W2 rows), and the grid meets again before x_{k} is read.
+// bounded counter barrier; the published word of each request then names
+// x_{k} directly, and every CTA reads the tokens of its own M-tile.
 #pragma once
 
 #include <cuda.h>
@@ -41,15 +49,14 @@
 namespace dspark {
 namespace eng {
 
-constexpr int kMaxChunks = 256;   // partial slots per (position, request)
+constexpr int kMaxChunks = 160;   // partial slots per (position, request): at least the SM count
 
 struct Ws {
     StatusBlock* status;
-    unsigned long long* words;   // [positions][B] best (key, ~block) or (value, ~token)
+    unsigned long long* words;   // [positions][B] best (key, ~token)
     float2* part;                // [positions][B][kMaxChunks] (max, sum) of y = z log2e / T
-    float* ytok;                 // [positions][B] y of the drawn token
+    float* ybest;                // [positions][B][kMaxChunks] y of each chunk's best token
     unsigned int* gbar;          // grid-barrier counter of the multi-position draft launch (starts at 0)
-    unsigned long long* xw;      // [B] (k << 32) | x_k, the last token drawn in the running launch (starts at 0)
 };
 
 // ------------------------------------------------------------ helpers ---
@@ -61,6 +68,12 @@ __device__ __forceinline__ unsigned long long pack_key(float key, uint32_t idx) 
     return (static_cast<unsigned long long>(f2ord(key)) << 32) | static_cast<uint32_t>(~idx);
 }
 __device__ __forceinline__ uint32_t unpack_idx(unsigned long long w) { return ~static_cast<uint32_t>(w); }
+
+// Chunk c of `nchunk` that covers unit u when `nunits` units are split into
+// the contiguous ranges [c nunits / nchunk, (c + 1) nunits / nchunk).
+__host__ __device__ __forceinline__ int chunk_of(int u, int nunits, int nchunk) {
+    return static_cast<int>(((static_cast<long long>(u) + 1) * nchunk - 1) / nunits);
+}
 
 template <bool kBF16>
 __device__ __forceinline__ float ld_elem(const void* p, size_t i) {
@@ -98,113 +111,6 @@ __device__ __forceinline__ void lse_merge(float& m1, float& s1, float m2, float 
     m1 = M;
 }
 
-// After v[i] (i < 32) is given in every lane, lane l ends with sum over lanes of
-// v[l] in v[0] (a butterfly that halves the live values at every stage).
-__device__ __forceinline__ void transpose_reduce32(float* v) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) {
-        const bool up = (lane & s) != 0;
-#pragma unroll
-        for (int i = 0; i < s; ++i) {
-            const float send = up ? v[i] : v[i + s];
-            const float keep = up ? v[i + s] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
-        }
-    }
-}
-
-// N (8, 16 or 32) partial sums v[0..N) per lane, summed over the 32 lanes: lane
-// l ends with the total of v[l % N] in v[0].  Lanes pair by the same bits, in
-// the same order (16, 8, 4, 2, 1), as in transpose_reduce32, so the totals are
-// bit-identical to it; levels above N/2 add without halving.
-template <int N>
-__device__ __forceinline__ void tree_reduce(float* v) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int s = 16; s >= N; s >>= 1) {
-#pragma unroll
-        for (int i = 0; i < N; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], s);
-    }
-#pragma unroll
-    for (int s = N / 2; s >= 1; s >>= 1) {
-        const bool up = (lane & s) != 0;
-#pragma unroll
-        for (int i = 0; i < s; ++i) {
-            const float send = up ? v[i] : v[i + s];
-            const float keep = up ? v[i + s] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
-        }
-    }
-}
-
-// Two warps per request: z for the 64 tokens of block `blk` of row (b, k):
-// warp w rebuilds tokens blk*64 + 32w + (0..31); each lane loads one or two
-// 16-byte chunks of every W2 row (coalesced rows) and a transpose-reduce
-// leaves token (32w + lane)'s dot product in that lane.  Returns z for the
-// lane's token (-inf past V).  erow: the rank-r row behind the bias of (b, k)
-// (bias_row).
-template <bool kBF16, int kCPL>
-__device__ __forceinline__ float block_logit_prev(int b, int gamma, int k, int V, int r, int blk, const void* erow,
-                                                  const void* U, const void* W2) {
-    constexpr int EPC = kBF16 ? 8 : 4;                    // elements per 16-byte chunk
-    const int warp = (threadIdx.x >> 5) & 1, lane = threadIdx.x & 31;
-    const int nch = r / EPC;
-    const int vbase = blk * 64 + warp * 32;
-    const int vl = vbase + lane;
-    const size_t urow = (static_cast<size_t>(b) * gamma + (k - 1)) * V;
-    const float u = (vl < V) ? ld_elem<kBF16>(U, urow + vl) : 0.f;
-    float e[kCPL][EPC];
-#pragma unroll
-    for (int cc = 0; cc < kCPL; ++cc) {
-        const int c = lane + 32 * cc;
-#pragma unroll
-        for (int q = 0; q < EPC; ++q)
-            e[cc][q] = (c < nch) ? ld_elem<kBF16>(erow, static_cast<size_t>(c) * EPC + q) : 0.f;
-    }
-    const uint64_t pol = policy_evict_last();
-    float part[32];
-    constexpr int kBatch = 32 / kCPL;
-#pragma unroll
-    for (int i0 = 0; i0 < 32; i0 += kBatch) {
-        uint4 raw[kBatch][kCPL];
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-            const int v = vbase + i0 + i;
-#pragma unroll
-            for (int cc = 0; cc < kCPL; ++cc) {
-                const int c = lane + 32 * cc;
-                raw[i][cc] = make_uint4(0, 0, 0, 0);
-                if (v < V && c < nch)
-                    ld_u32x4(static_cast<const uint8_t*>(W2) + (static_cast<size_t>(v) * r + c * EPC) * (kBF16 ? 2 : 4),
-                             &raw[i][cc].x, pol);
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-            float acc = 0.f;
-#pragma unroll
-            for (int cc = 0; cc < kCPL; ++cc) {
-                const uint32_t wv[4] = {raw[i][cc].x, raw[i][cc].y, raw[i][cc].z, raw[i][cc].w};
-                if constexpr (kBF16) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        acc = fmaf(bf16lo(wv[q]), e[cc][2 * q], acc);
-                        acc = fmaf(bf16hi(wv[q]), e[cc][2 * q + 1], acc);
-                    }
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) acc = fmaf(__uint_as_float(wv[q]), e[cc][q], acc);
-                }
-            }
-            part[i0 + i] = acc;
-        }
-    }
-    transpose_reduce32(part);
-    if (vl >= V) return -INFINITY;
-    return part[0] + u;
-}
-
 // The rank-r row behind the bias of position k of request b: W1[x_{k-1}] for the
 // Markov head (E null), else row (b, k) of the rows E [B][gamma][r] that a
 // gated or recurrent head produced.
@@ -215,80 +121,51 @@ __device__ __forceinline__ const void* bias_row(const void* E, const void* W1, i
     return static_cast<const uint8_t*>(E ? E : W1) + row * r * (kBF16 ? 2 : 4);
 }
 
-template <bool kBF16, int kCPL>
-__device__ __forceinline__ float block_logit(int b, int gamma, int k, int V, int r, int blk, const void* U,
-                                             const void* W1, const void* E, const void* W2, const int32_t* x0,
-                                             const int32_t* x, StatusBlock* st) {
-    const int prev = prev_token(x0, x, b, gamma, k, V, st);
-    return block_logit_prev<kBF16, kCPL>(b, gamma, k, V, r, blk, bias_row<kBF16>(E, W1, b, gamma, k, r, prev), U,
-                                         W2);
-}
-
-// ===================================================== tcgen05 engine ====
-constexpr int kBM = 128;              // request rows per M-tile (TMEM lanes)
-constexpr int kBN = 128;              // vocabulary columns per tile
-constexpr int kBK = 64;               // K per smem slab (128 bytes of bf16)
-constexpr int kStages = 8;            // W2 slab ring
-constexpr int kEpiWG = 2;             // epilogue warpgroups, two TMEM buffers each
-constexpr int kTcThreads = 128 * (1 + kEpiWG);
-constexpr int kSlabBytes = kBN * kBK * 2;     // 16 KB
-constexpr int kASlabBytes = kBM * kBK * 2;    // 16 KB
-
-enum Mode : int { kDraft = 0, kResidual = 1 };
-
-// What the final token draw of verification reads and writes (section 8.2:
-// the residual draw after a rejection, or a draw from p_t at the stop row).
-struct FinishArgs {
-    const uint16_t* T;               // t_logits [B][gamma+1][V]
-    const int32_t* krow;             // [B] rejected position (0: none)
-    const int32_t* stop;             // [B] row of the final draw
-    const float* lt2;                // [B]
-    const float* ld2;                // [B]
-    const unsigned long long* res_word;   // [B] residual block winner
-    const unsigned long long* wt;    // [B][gamma+1] target-row block winner
-    int32_t* next_token;             // [B]
-};
-
-struct TcParams {
-    int B, gamma, V, r, k;           // k: the position of every row (kDraft)
-    const uint16_t* U;               // [B][gamma][V]
-    const uint16_t* W1;              // [V][r]
-    const uint16_t* E;               // [B][gamma][r] bias rows of a gated / recurrent head, or null (W1[x_{k-1}])
-    const uint16_t* W2;              // [V][r] (the redraw of the winning block reads rows directly)
-    const int32_t* x0;               // [B]
-    int32_t* x;                      // [B][gamma]; kDraft writes x_{k-1} here (CTA 0 of each M-tile)
-    float cscale;                    // log2e / T (1 for greedy)
-    int greedy;
-    uint64_t seed;
-    int P;                           // CTAs per M-tile
-    Ws ws;
-    float* debug_z;                  // kDraft: write y to [B][V] instead of reducing
-    int k_last;                      // kDraft: positions k .. k_last in one (cooperative) launch
-    // kDraft with fuse_tail: the launch also draws x_gamma and finalizes
-    // (lse_d, logp_d, confidence c and survival a), as draft_finalize does
-    int fuse_tail;
-    int H;
-    const uint16_t* h;               // [B][gamma][H]
-    const uint16_t* w;               // [H + r]
-    float bias;
-    float* lse_d;
-    float* logp_d;
-    float* c;
-    float* a;
-    // kResidual with fuse_tail: the launch also draws the final token
-    FinishArgs fin;
-    // kResidual
-    const int32_t* krow;             // [B] rejected position k_b (0: row inactive)
-    const uint16_t* T;               // t_logits [B][gamma+1][V]
-    const float* lt2;                // [B] log2-sum-exp2 of t / T at row k_b (log2 units)
-    const float* ld2;                // [B] lse_d[b][k_b-1] * log2e
-};
-
-struct RowRes {
+// Running Gumbel-max state of one thread: the best key so far (log2 units),
+// its token and its y.  Tokens reach a thread in ascending order, so a strict
+// comparison keeps the lowest index on ties.
+struct Best {
     float key;
     int idx;
-    float m, s;
+    float y;
 };
+__device__ __forceinline__ void best_take(Best& b, float key, int idx, float y) {
+    if (key > b.key || (key == b.key && idx < b.idx)) { b.key = key; b.idx = idx; b.y = y; }
+}
+
+// The flat Gumbel-max draw over 32 consecutive tokens v0 .. v0+31 (v0 a
+// multiple of 4) with log2-weights y (-inf: no mass), and their (max, sum):
+// e_v = 2^(y_v - m), the winner maximises e_v / E_v (cross-multiplied), and
+// enters `best` with key y_v - log2 E_v.  `pr` holds the row's Philox
+// constants; word v & 3 of block v >> 2 keys index v.
+__device__ __forceinline__ void draw32(const float* y, int v0, const PhiloxRow& pr, Best& best, float& M,
+                                       float& S) {
+    float m4[4] = {y[0], y[1], y[2], y[3]};
+#pragma unroll
+    for (int w = 4; w < 32; ++w) m4[w & 3] = fmaxf(m4[w & 3], y[w]);
+    const float mb = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+    if (!(mb > -INFINITY)) return;                        // no finite logit: no mass
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+    float eb = 0.f, Eb = 1.f, yb = 0.f;
+    int jb = 0;
+    const uint32_t q0 = static_cast<uint32_t>(v0) >> 2;
+#pragma unroll
+    for (int qq = 0; qq < 8; ++qq) {
+        const U4 pw = philox_row(pr, q0 + qq);
+        const uint32_t wv[4] = {pw.x, pw.y, pw.z, pw.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = 4 * qq + j;
+            const float e = fast_exp2(y[i] - mb);
+            s4[j] += e;
+            const float E = exp_draw(wv[j]);
+            if (e * Eb > eb * E) { eb = e; Eb = E; yb = y[i]; jb = i; }
+        }
+    }
+    best_take(best, yb - fast_log2(Eb), v0 + jb, yb);
+    lse_merge(M, S, mb, (s4[0] + s4[1]) + (s4[2] + s4[3]));
+}
+
 // Grid barrier of the multi-position draft launch (cooperative launch: every CTA
 // is resident).  Epoch e is complete once the counter reaches e * gridDim.x;
 // every CTA arrives once per epoch.  Waits are bounded (kWaitLimitNs).
@@ -309,25 +186,6 @@ __device__ __forceinline__ bool grid_wait(const unsigned int* ctr, unsigned int 
         __nanosleep(64);
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
-    return true;
-}
-
-// Waits (bounded) until the tagged token word of a request carries position k.
-__device__ __forceinline__ bool wait_token(const unsigned long long* xw, int k, int* tok) {
-    auto load = [&]() {
-        unsigned long long v;
-        asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(xw) : "memory");
-        return v;
-    };
-    unsigned long long v = load();
-    if (static_cast<uint32_t>(v >> 32) != static_cast<uint32_t>(k)) {
-        const uint64_t t0 = globaltimer_ns();
-        while (static_cast<uint32_t>((v = load()) >> 32) != static_cast<uint32_t>(k)) {
-            __nanosleep(32);
-            if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-        }
-    }
-    *tok = static_cast<int>(static_cast<uint32_t>(v));
     return true;
 }
 
@@ -376,28 +234,32 @@ __device__ __forceinline__ float dot_row(const void* a, size_t a_off, const void
 
 // One warp finalizes position k of request b (DeepSpec walkthrough 3.3,
 // AcceptRatePredictor): lse_d = logsumexp(z / T) from the nchunk (max, sum)
-// partials, logp_d = y(x_k) - lse_d, and the confidence
-// c = sigmoid(w . [h_k ; W1[x_{k-1}]] + bias), written by lane 0.
+// partials, logp_d = y(x_k) - lse_d with y(x_k) taken from the chunk that
+// covers x_k (its best token is x_k: the overall winner is the best of the
+// chunk it lies in), and the confidence c = sigmoid(w . [h_k ; W1[x_{k-1}]] + bias),
+// written by lane 0.  Chunk c covers units [c nunits / nchunk, (c+1) nunits /
+// nchunk) of `unit` tokens each.
 template <bool kBF16>
 __device__ __forceinline__ void finalize_position(int b, int k, int B, int gamma, int V, int H, int r, const void* h,
                                                   const void* W1, const void* w, float bias, const int32_t* x0,
-                                                  const int32_t* x, int greedy, int nchunk, const float2* part,
-                                                  const float* ytok, float* lse_d, float* logp_d, float* c,
-                                                  StatusBlock* st) {
+                                                  const int32_t* x, int greedy, int nchunk, int unit, int nunits,
+                                                  const float2* part, const float* ybest, float* lse_d,
+                                                  float* logp_d, float* c, StatusBlock* st) {
     const int lane = threadIdx.x & 31;
     const size_t slot = static_cast<size_t>(k - 1) * B + b;
     const size_t o = static_cast<size_t>(b) * gamma + (k - 1);
     float L = 0.f, lp = 0.f;
     if (!greedy) {
         float m = -INFINITY, s = 0.f;
-        float2 pr[kMaxChunks / 32];                       // every partial of this lane in flight at once
+        constexpr int kPer = (kMaxChunks + 31) / 32;
+        float2 pr[kPer];                                  // every partial of this lane in flight at once
 #pragma unroll
-        for (int u = 0; u < kMaxChunks / 32; ++u) {
+        for (int u = 0; u < kPer; ++u) {
             const int ch = lane + 32 * u;
             pr[u] = (ch < nchunk) ? __ldcg(part + slot * kMaxChunks + ch) : make_float2(0.f, 0.f);
         }
 #pragma unroll
-        for (int u = 0; u < kMaxChunks / 32; ++u)
+        for (int u = 0; u < kPer; ++u)
             if (lane + 32 * u < nchunk) lse_merge(m, s, pr[u].x, pr[u].y);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
@@ -406,8 +268,11 @@ __device__ __forceinline__ void finalize_position(int b, int k, int B, int gamma
             lse_merge(m, s, om, os);
         }
         const float L2 = m + log2f(s);
+        int tok = __ldcg(x + o);
+        if (tok < 0 || tok >= V) tok = 0;                 // reported where x was written
+        const float ytok = __ldcg(ybest + slot * kMaxChunks + chunk_of(tok / unit, nunits, nchunk));
         L = L2 * kLn2;
-        lp = (__ldcg(ytok + slot) - L2) * kLn2;
+        lp = (ytok - L2) * kLn2;
     }
     const int prev = prev_token(x0, x, b, gamma, k, V, st);
     float acc = dot_row<kBF16>(w, 0, h, o * H, H, lane);
@@ -419,6 +284,70 @@ __device__ __forceinline__ void finalize_position(int b, int k, int B, int gamma
         logp_d[o] = lp;
     }
 }
+
+// ===================================================== tcgen05 engine ====
+constexpr int kBM = 128;              // request rows per M-tile (TMEM lanes)
+constexpr int kBN = 128;              // vocabulary columns per tile
+constexpr int kBK = 64;               // K per smem slab (128 bytes of bf16)
+constexpr int kStages = 8;            // W2 slab ring
+constexpr int kEpiWG = 2;             // epilogue warpgroups, two TMEM buffers each
+constexpr int kTcThreads = 128 * (1 + kEpiWG);
+constexpr int kSlabBytes = kBN * kBK * 2;     // 16 KB
+constexpr int kASlabBytes = kBM * kBK * 2;    // 16 KB
+
+enum Mode : int { kDraft = 0, kResidual = 1 };
+
+// What the final-token step of verification reads and writes (section 8.2):
+// a request rejected at k takes the residual's winner, or, when the residual
+// has no mass, a draw from p_t at row k (stream 2 at (b, k)).  Requests with
+// no rejection got their bonus token from the rows pass.
+struct FinishArgs {
+    const uint16_t* T;               // t_logits [B][gamma+1][V] (bf16, or fp32 read through Tf)
+    const float* Tf;                 // the same rows when they are fp32 (else null)
+    const int32_t* krow;             // [B] rejected position (0: none)
+    const unsigned long long* res_word;   // [B] residual winner (key, ~token), 0: no mass
+    int32_t* next_token;             // [B]
+};
+
+struct TcParams {
+    int B, gamma, V, r, k;           // k: the position of every row (kDraft)
+    const uint16_t* U;               // [B][gamma][V]
+    const uint16_t* W1;              // [V][r]
+    const uint16_t* E;               // [B][gamma][r] bias rows of a gated / recurrent head, or null (W1[x_{k-1}])
+    const uint16_t* W2;              // [V][r]
+    const int32_t* x0;               // [B]
+    int32_t* x;                      // [B][gamma]; kDraft writes x_{k-1} here (CTA 0 of each M-tile)
+    float cscale;                    // log2e / T (1 for greedy)
+    int greedy;
+    uint64_t seed;
+    int P;                           // CTAs per M-tile
+    Ws ws;
+    float* debug_z;                  // kDraft: write y to [B][V] instead of reducing
+    int k_last;                      // kDraft: positions k .. k_last in one (cooperative) launch
+    // kDraft with fuse_tail: the launch also writes x_gamma and finalizes
+    // (lse_d, logp_d, confidence c and survival a), as draft_finalize does
+    int fuse_tail;
+    int H;
+    const uint16_t* h;               // [B][gamma][H]
+    const uint16_t* w;               // [H + r]
+    float bias;
+    float* lse_d;
+    float* logp_d;
+    float* c;
+    float* a;
+    // kResidual with fuse_tail: the launch also writes the final tokens
+    FinishArgs fin;
+    // kResidual
+    const int32_t* krow;             // [B] rejected position k_b (0: row inactive)
+    const uint16_t* T;               // t_logits [B][gamma+1][V]
+    const float* lt2;                // [B] log2-sum-exp2 of t / T at row k_b (log2 units)
+    const float* ld2;                // [B] lse_d[b][k_b-1] * log2e
+};
+
+struct RowRes {
+    Best best;
+    float m, s;
+};
 
 // OR of `v` over the 64 threads of named barrier `bar`.
 __device__ __forceinline__ bool pair_any(bool v, int bar) {
@@ -435,218 +364,53 @@ __device__ __forceinline__ bool pair_any(bool v, int bar) {
 }
 
 // The final token of request b (two warps, named barrier `bar`; xch/xchi: a
-// 2-entry exchange): if a draft token was rejected at k and the residual
-// max(0, p_t - p_d) has mass, the token inside the residual's winning block
-// (second Gumbel level, stream 2); otherwise a draw from p_t at the stop row
-// (bonus row, stream 5) inside that row's winning block.
-template <bool kBF16, int kCPL>
-__device__ __forceinline__ void finish_pair(const FinishArgs& f, int b, int gamma, int V, int r, const void* U,
-                                            const void* W1, const void* E, const void* W2, const int32_t* x0,
-                                            const int32_t* x,
-                                            float cscale, uint64_t seed, StatusBlock* st, int bar, float* xch,
-                                            int* xchi) {
-    const int lane = threadIdx.x & 31, wp = (threadIdx.x >> 5) & 1;
+// 2-entry exchange) when its draft was rejected at k = krow[b]: the residual's
+// winner, or -- if the residual has no mass after rounding -- a Gumbel-max draw
+// from p_t = softmax(t_k / T) over the whole row (stream 2 at (b, k)), taken
+// by the two warps together.  Requests with no rejection are left alone: the
+// rows pass wrote their bonus token.
+template <bool kBF16>
+__device__ __forceinline__ void finish_pair(const FinishArgs& f, int b, int gamma, int V, float cscale, uint64_t seed,
+                                            StatusBlock* st, int bar, float* xch, int* xchi) {
+    const int lane = threadIdx.x & 31, wp = (threadIdx.x >> 5) & 1, pt = threadIdx.x & 63;
     const int kr = f.krow[b];
-    const unsigned long long rw = (kr > 0) ? __ldcg(f.res_word + b) : 0ull;
-    const uint32_t nblk = static_cast<uint32_t>((V + 63) / 64);
-    bool residual = rw != 0ull && unpack_idx(rw) < nblk;
-    float score = -INFINITY;
-    int v = 0x7FFFFFFF;
-    if (residual) {
-        const int blk = static_cast<int>(unpack_idx(rw));
-        const float z = block_logit<kBF16, kCPL>(b, gamma, kr, V, r, blk, U, W1, E, W2, x0, x, st);
-        v = blk * 64 + wp * 32 + lane;
-        if (z > -INFINITY) {
-            const float yd = z * cscale;
-            const float yt = ld_elem<kBF16>(f.T, (static_cast<size_t>(b) * (gamma + 1) + (kr - 1)) * V + v) * cscale;
-            const float qv = fast_exp2(yt - f.lt2[b]) - fast_exp2(yd - f.ld2[b]);
-            if (qv > 0.f) {
-                const float g =
-                    gumbel_of(uniform_open(draw_word(seed, b, kr, kStreamResidualToken, static_cast<uint32_t>(v))));
-                score = log2f(qv) * kLn2 + g;
-            }
-        }
-        if (!pair_any(score > -INFINITY, bar)) residual = false;   // no mass left after rounding
+    if (kr <= 0) return;
+    const unsigned long long rw = __ldcg(f.res_word + b);
+    if (rw != 0ull && unpack_idx(rw) < static_cast<uint32_t>(V)) {
+        if (pt == 0) f.next_token[b] = static_cast<int>(unpack_idx(rw));
+        return;
     }
-    bool bad = false;
-    if (!residual) {
-        const int srow = (kr > 0) ? kr : f.stop[b];
-        const unsigned long long w = __ldcg(f.wt + static_cast<size_t>(b) * (gamma + 1) + srow - 1);
-        if (w == 0ull || unpack_idx(w) >= nblk) {
-            if (threadIdx.x % 64 == 0) set_status(st, DSPARK_ERR_DEVICE_CHECK, w == 0ull ? 7 : 9);
-            bad = true;
-        } else {
-            const int blk = static_cast<int>(unpack_idx(w));
-            v = blk * 64 + wp * 32 + lane;
-            score = -INFINITY;
+    // no residual mass: the draw from p_t at row kr, four consecutive tokens per thread and step
+    const PhiloxRow pr = philox_row_setup(seed, static_cast<uint32_t>(kr), static_cast<uint32_t>(b), kStreamVerifyToken);
+    const size_t row = (static_cast<size_t>(b) * (gamma + 1) + (kr - 1)) * V;
+    Best best{-INFINITY, 0x7FFFFFFF, 0.f};
+    for (int q = pt; q * 4 < V; q += 64) {
+        const U4 pw = philox_row(pr, static_cast<uint32_t>(q));
+        const uint32_t wv[4] = {pw.x, pw.y, pw.z, pw.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int v = 4 * q + j;
             if (v < V) {
-                const float yt = ld_elem<kBF16>(f.T, (static_cast<size_t>(b) * (gamma + 1) + (srow - 1)) * V + v) * cscale;
-                const float g =
-                    gumbel_of(uniform_open(draw_word(seed, b, srow, kStreamTargetToken, static_cast<uint32_t>(v))));
-                score = yt + g * kLog2e;
+                const float y = (kBF16 ? ld_elem<true>(f.T, row + v) : f.Tf[row + v]) * cscale;
+                best_take(best, y - fast_log2(exp_draw(wv[j])), v, y);
             }
         }
     }
-    int bi = (score > -INFINITY) ? v : 0x7FFFFFFF;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-        const float os = __shfl_xor_sync(0xffffffffu, score, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (os > score || (os == score && oi < bi)) { score = os; bi = oi; }
+        const float ok = __shfl_xor_sync(0xffffffffu, best.key, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, best.idx, o);
+        best_take(best, ok, oi, 0.f);
     }
-    if (lane == 0) { xch[wp] = score; xchi[wp] = bi; }
+    if (lane == 0) { xch[wp] = best.key; xchi[wp] = best.idx; }
     asm volatile("bar.sync %0, 64;" ::"r"(bar) : "memory");
-    if (wp == 0 && lane == 0) {
+    if (pt == 0) {
         int w = 0;
         if (xch[1] > xch[0] || (xch[1] == xch[0] && xchi[1] < xchi[0])) w = 1;
-        f.next_token[b] = (bad || xchi[w] == 0x7FFFFFFF) ? 0 : xchi[w];
-    }
-    asm volatile("bar.sync %0, 64;" ::"r"(bar) : "memory");
-}
-
-// Draw x_k for request b with a group of G = 4 or 8 warps (group warp gw,
-// named barrier `bar` over 32 G threads).  Each warp rebuilds z on 64 / G
-// tokens of the winning block: lane c multiplies the c-th 16-byte chunk of
-// each W2 row by the same chunk of e = W1[x_{k-1}], kept in shared memory
-// (e_s, float[r]) since this CTA drew x_{k-1}; a butterfly over the lanes sums
-// the chunks (the same order as the two-warp draw, so z is bit-identical).
-// The second Gumbel level (stream 0) picks the token; the group leader
-// publishes it ((k << 32) | x_k word, x, ytok) and the group refills e_s with
-// W1[x_k] for the next draw.  g: [3 G] words of exchange space.
-template <int G>
-__device__ __forceinline__ void group_draw(const TcParams& p, int b, int k, int gw, int bar, float* e_s, float* g) {
-    constexpr int NT = 64 / G;                            // tokens per warp
-    const int lane = threadIdx.x & 31;
-    float* gsc = g;
-    float* gy = g + G;
-    int* gix = reinterpret_cast<int*>(g + 2 * G);
-    const size_t slot = static_cast<size_t>(k - 1) * p.B + b;
-    const unsigned long long word = __ldcg(p.ws.words + slot);
-    const uint32_t idx = unpack_idx(word);
-    const bool ok = word != 0ull && idx < static_cast<uint32_t>((p.V + 63) / 64);
-    float score = -INFINITY, yv = 0.f;
-    int bi = 0x7FFFFFFF;
-    if (ok) {
-        const int vbase = static_cast<int>(idx) * 64 + gw * NT;
-        const int vl = vbase + (lane & (NT - 1));
-        const int nch = p.r / 8;
-        const float u = (lane < NT && vl < p.V)
-                            ? bf16lo(p.U[(static_cast<size_t>(b) * p.gamma + (k - 1)) * p.V + vl])
-                            : 0.f;
-        const uint64_t pol = policy_evict_last();
-        uint4 raw[NT];
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            raw[t] = make_uint4(0, 0, 0, 0);
-            if (vbase + t < p.V && lane < nch)
-                ld_u32x4(p.W2 + static_cast<size_t>(vbase + t) * p.r + lane * 8, &raw[t].x, pol);
-        }
-        float e[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) e[q] = (lane < nch) ? e_s[lane * 8 + q] : 0.f;
-        float part[NT];
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            const uint32_t wv[4] = {raw[t].x, raw[t].y, raw[t].z, raw[t].w};
-            float acc = 0.f;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                acc = fmaf(bf16lo(wv[q]), e[2 * q], acc);
-                acc = fmaf(bf16hi(wv[q]), e[2 * q + 1], acc);
-            }
-            part[t] = acc;
-        }
-        tree_reduce<NT>(part);
-        if (lane < NT && vl < p.V) {
-            yv = (part[0] + u) * p.cscale;
-            const float gum = gumbel_of(uniform_open(draw_word(p.seed, b, k, kStreamDraftToken, static_cast<uint32_t>(vl))));
-            score = yv + gum * kLog2e;
-            bi = vl;
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float os = __shfl_xor_sync(0xffffffffu, score, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        const float oy = __shfl_xor_sync(0xffffffffu, yv, o);
-        if (os > score || (os == score && oi < bi)) { score = os; bi = oi; yv = oy; }
-    }
-    if (lane == 0) { gsc[gw] = score; gix[gw] = bi; gy[gw] = yv; }
-    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(32 * G) : "memory");
-    if (gw == 0 && lane == 0) {
-        int w = 0;
-        for (int q = 1; q < G; ++q)
-            if (gsc[q] > gsc[w] || (gsc[q] == gsc[w] && gix[q] < gix[w])) w = q;
-        int tok = gix[w];
-        if (tok == 0x7FFFFFFF) { set_status(p.ws.status, DSPARK_ERR_DEVICE_CHECK, 3); tok = 0; }
-        const unsigned long long tagged = (static_cast<unsigned long long>(k) << 32) | static_cast<uint32_t>(tok);
-        asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p.ws.xw + b), "l"(tagged) : "memory");
-        p.x[b * p.gamma + k - 1] = tok;
-        p.ws.ytok[slot] = gy[w];
-        gix[0] = tok;
-    }
-    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(32 * G) : "memory");
-    // e for the next draw: W1[x_k] (also the next position's A row, so bring it into L2 too)
-    const int tok = gix[0];
-    for (int j = gw * 32 + lane; j < p.r / 2; j += 32 * G) {
-        const uint32_t w2 = reinterpret_cast<const uint32_t*>(p.W1 + static_cast<size_t>(tok) * p.r)[j];
-        e_s[2 * j] = bf16lo(w2);
-        e_s[2 * j + 1] = bf16hi(w2);
-    }
-    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(32 * G) : "memory");
-}
-
-// Draw x_k for request b inside a running multi-position launch: a pair of
-// warps (named barrier `bar`, 64 threads) rebuilds z on the winning block from
-// W2 rows and takes the second Gumbel level (stream 0); the even warp's lane 0
-// writes x and ytok.  xch/xchi: this pair's 2-entry exchange slots.
-__device__ __forceinline__ void pair_draw(const TcParams& p, int b, int k, int bar, float2* xch, int* xchi) {
-    const int lane = threadIdx.x & 31, wp = (threadIdx.x >> 5) & 1;
-    const size_t slot = static_cast<size_t>(k - 1) * p.B + b;
-    // independent L2 reads first: the winning block, and x_{k-1} for W1
-    const unsigned long long word = __ldcg(p.ws.words + slot);
-    const int prev = prev_token(p.x0, p.x, b, p.gamma, k, p.V, p.ws.status);
-    const uint32_t idx = unpack_idx(word);
-    const bool ok = word != 0ull && idx < static_cast<uint32_t>((p.V + 63) / 64);
-    float score = -INFINITY, yv = 0.f;
-    int bi = 0x7FFFFFFF;
-    if (ok) {
-        const int blk = static_cast<int>(idx);
-        const float z = block_logit_prev<true, 1>(b, p.gamma, k, p.V, p.r, blk,
-                                                  bias_row<true>(p.E, p.W1, b, p.gamma, k, p.r, prev), p.U, p.W2);
-        const int v = blk * 64 + wp * 32 + lane;
-        if (z > -INFINITY) {
-            yv = z * p.cscale;
-            const float g = gumbel_of(uniform_open(draw_word(p.seed, b, k, kStreamDraftToken, static_cast<uint32_t>(v))));
-            score = yv + g * kLog2e;
-            bi = v;
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float os = __shfl_xor_sync(0xffffffffu, score, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        const float oy = __shfl_xor_sync(0xffffffffu, yv, o);
-        if (os > score || (os == score && oi < bi)) { score = os; bi = oi; yv = oy; }
-    }
-    if (lane == 0) { xch[wp] = make_float2(score, yv); xchi[wp] = bi; }
-    asm volatile("bar.sync %0, 64;" ::"r"(bar) : "memory");
-    if (wp == 0 && lane == 0) {
-        int w = 0;
-        if (xch[1].x > xch[0].x || (xch[1].x == xch[0].x && xchi[1] < xchi[0])) w = 1;
         int tok = xchi[w];
-        if (tok == 0x7FFFFFFF) { set_status(p.ws.status, DSPARK_ERR_DEVICE_CHECK, 3); tok = 0; }
-        // the tagged word carries the token itself: no ordering with other stores is needed
-        const unsigned long long tagged = (static_cast<unsigned long long>(k) << 32) | static_cast<uint32_t>(tok);
-        asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p.ws.xw + b), "l"(tagged) : "memory");
-        p.x[b * p.gamma + k - 1] = tok;
-        p.ws.ytok[slot] = xch[w].y;
-        xchi[0] = tok;
+        if (tok < 0 || tok >= V) { set_status(st, DSPARK_ERR_DEVICE_CHECK, 7); tok = 0; }
+        f.next_token[b] = tok;
     }
-    asm volatile("bar.sync %0, 64;" ::"r"(bar) : "memory");
-    // W1[x_k] is the next position's A row and the next draw's e: bring it into L2
-    if (wp == 0 && lane * 128 < p.r * 2)
-        prefetch_l2(reinterpret_cast<const uint8_t*>(p.W1) + static_cast<size_t>(xchi[0]) * p.r * 2 + lane * 128);
     asm volatile("bar.sync %0, 64;" ::"r"(bar) : "memory");
 }
 
@@ -666,11 +430,9 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2 * kEpiWG);
     RowRes* rowres = reinterpret_cast<RowRes*>(tmem_slot + 4);   // [kEpiWG][128]
     int* s_prev = reinterpret_cast<int*>(rowres + kEpiWG * kBM);   // [128] x_{k-1} per request row
-    float2* xch = reinterpret_cast<float2*>(s_prev + kBM);        // [10] pair exchange
+    float* xch = reinterpret_cast<float*>(s_prev + kBM);          // [10] pair exchange
     int* xchi = reinterpret_cast<int*>(xch + 10);                 // [10]
     int* s_fail = xchi + 10;
-    float* e_s = reinterpret_cast<float*>(s_fail + 4);           // [2][256] W1 row of the last token drawn
-    float* gx = e_s + 2 * 256;                                     // [2][3 * 8] group-draw exchange
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = blockIdx.x / p.P, pc = blockIdx.x % p.P;
@@ -682,7 +444,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
     StatusBlock* st = p.ws.status;
     // Row replication: with at most 64 requests the A tile holds every request
     // twice (TMEM lanes 0-63 and 64-127) and the two copies reduce different
-    // 64-token blocks of each tile, so all epilogue warps have work.
+    // 64-token halves of each tile, so all epilogue warps have work.
     const int R = (p.B <= 64) ? 2 : 1;
     const int rpc = kBM / R;                              // request rows per copy
     const int nrows = min(rpc, p.B - m0);                 // requests of this M-tile
@@ -740,80 +502,37 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
             }
             pro_sync();
         };
+        // the published winner of request b at position k: its token
+        auto winner = [&](int b, int k) -> int {
+            const unsigned long long w = __ldcg(p.ws.words + static_cast<size_t>(k - 1) * p.B + b);
+            const uint32_t idx = unpack_idx(w);
+            if (w == 0ull || idx >= static_cast<uint32_t>(p.V)) {
+                set_status(st, DSPARK_ERR_DEVICE_CHECK, 3);
+                return 0;
+            }
+            return static_cast<int>(idx);
+        };
         // per-thread pipeline state that continues across positions
         int mma_stage = 0;
         uint32_t mma_phase = 0;
         bool failed = false;
-        // requests b = blockIdx.x + j * gridDim.x < B, j < nown, belong to this CTA: it draws their
-        // tokens (with one group of 8 or two of 4 warps when it owns at most two, keeping e = W1[x]
-        // in shared memory; with pairs of warps otherwise) and finalizes them
-        const int cta = static_cast<int>(blockIdx.x), ncta = static_cast<int>(gridDim.x);
-        const int nown = (cta < p.B) ? (p.B - 1 - cta) / ncta + 1 : 0;
-        const bool grouped = kMode == kDraft && !p.greedy && nown <= 2 && (multi || p.fuse_tail);
-        auto draw_owned = [&](int kd) {
-            if (*s_fail != 0) return;
-            if (grouped) {
-                if (warp >= 4) {
-                    if (nown == 1)
-                        group_draw<8>(p, cta, kd, warp - 4, 2, e_s, gx);
-                    else if (nown == 2)
-                        group_draw<4>(p, cta + ((warp - 4) >> 2) * ncta, kd, (warp - 4) & 3, 2 + ((warp - 4) >> 2),
-                                      e_s + ((warp - 4) >> 2) * 256, gx + ((warp - 4) >> 2) * 24);
-                }
-            } else if (warp >= 2) {
-                const int pair = (warp - 2) >> 1;
-                for (int b = cta + pair * ncta; b < p.B; b += 5 * ncta)
-                    pair_draw(p, b, kd, 2 + pair, xch + 2 * pair, xchi + 2 * pair);
-            }
-        };
 
         for (int k = k0; k <= k1; ++k) {
             const int base = (k - k0) * ntiles;           // running index of this position's first tile
             // ---------------------------------------------- prologue: x_{k-1}
             if (kMode == kDraft && multi && k > k0) {
                 wait_all();                               // every CTA published position k-1
-                if (!p.greedy) {
-                    // second Gumbel level for x_{k-1}, spread over the grid (owned requests)
-                    draw_owned(k - 1);
-                    // x_{k-1} of this M-tile's requests, as their drawers publish them
-                    for (int rr = ptid; rr < nrows; rr += kPro) {
-                        int tok = 0;
-                        if (*s_fail == 0 && !wait_token(p.ws.xw + m0 + rr, k - 1, &tok)) {
-                            set_status(st, DSPARK_ERR_TIMEOUT, 14);
-                            *s_fail = 1;
-                        }
-                        if (tok < 0 || tok >= p.V) { set_status(st, DSPARK_ERR_DEVICE_CHECK, 2); tok = 0; }
-                        s_prev[rr] = tok;
-                    }
-                } else {
-                    for (int rr = ptid; rr < nrows; rr += kPro) {
-                        const int b = m0 + rr;
-                        const unsigned long long w = __ldcg(p.ws.words + static_cast<size_t>(k - 2) * p.B + b);
-                        const uint32_t idx = unpack_idx(w);
-                        int tok = static_cast<int>(idx);
-                        if (w == 0ull || idx >= static_cast<uint32_t>(p.V)) {
-                            set_status(st, DSPARK_ERR_DEVICE_CHECK, 3);
-                            tok = 0;
-                        }
-                        s_prev[rr] = tok;
-                        if (pc == 0) p.x[b * p.gamma + k - 2] = tok;
-                    }
+                for (int rr = ptid; rr < nrows; rr += kPro) {
+                    const int b = m0 + rr;
+                    const int tok = (*s_fail == 0) ? winner(b, k - 1) : 0;
+                    s_prev[rr] = tok;
+                    if (pc == 0) p.x[b * p.gamma + k - 2] = tok;
                 }
             } else {
                 for (int rr = ptid; rr < nrows; rr += kPro) {
                     const int b = m0 + rr;
                     const int kb = row_k(b, k);
                     s_prev[rr] = (kb > 0) ? prev_token(p.x0, p.x, b, p.gamma, kb, p.V, st) : -1;
-                }
-                if (grouped && warp >= 4) {                // e of the first draw: W1[x_{k0-1}]
-                    for (int j = 0; j < nown; ++j) {
-                        const int prev = prev_token(p.x0, p.x, cta + j * ncta, p.gamma, k, p.V, st);
-                        for (int i = tid - 128; i < p.r / 2; i += kTcThreads - 128) {
-                            const uint32_t w2 = reinterpret_cast<const uint32_t*>(p.W1 + static_cast<size_t>(prev) * p.r)[i];
-                            e_s[j * 256 + 2 * i] = bf16lo(w2);
-                            e_s[j * 256 + 2 * i + 1] = bf16hi(w2);
-                        }
-                    }
                 }
             }
             pro_sync();
@@ -885,8 +604,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                 const int kb = (rr < nrows) ? row_k(b, k) : 0;
                 const bool valid = rr < nrows && kb > 0;
                 const bool warp_live = ((q * 32) % rpc) < nrows;
-                // U rows stay in L2 (normal policy): the token draw after this position
-                // re-reads the 64 values of each winning block
+                // U rows stay in L2 (normal policy) for the draft; the residual reads them once
                 const uint64_t pol = (kMode == kDraft) ? policy_evict_normal() : policy_evict_first();
                 const uint16_t* urow = p.U + (static_cast<size_t>(valid ? b : 0) * p.gamma + (valid ? kb - 1 : 0)) * p.V;
                 float ld2 = 0.f, lt2 = 0.f;
@@ -898,25 +616,32 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                         trow = p.T + (static_cast<size_t>(b) * (p.gamma + 1) + (kb - 1)) * p.V;
                     }
                 }
-                float best = -INFINITY, M = -INFINITY, S = 0.f;
-                int best_i = 0x7FFFFFFF;
+                const PhiloxRow prow =
+                    philox_row_setup(p.seed, static_cast<uint32_t>(kb), static_cast<uint32_t>(b),
+                                     (kMode == kDraft) ? kStreamDraftToken : kStreamVerifyToken);
+                Best best{-INFINITY, 0x7FFFFFFF, 0.f};
+                float M = -INFINITY, S = 0.f;
+                float qb = 0.f, Eq = 1.f;                 // kResidual: the running winner's q and E
                 const int i0 = ((eg - base) % kEpiWG + kEpiWG) % kEpiWG;   // this WG's first local tile
 
-                uint32_t u[2][32];                        // U of the two 64-token blocks of one tile
-                auto load_blk = [&](const uint16_t* src, int t, int hb, uint32_t* dst) {
-                    const int v0 = t * kBN + hb * 64;
+                uint32_t u[2][32];                        // U of the two 64-token halves of one tile
+                // 16-byte loads of tokens v0 .. v0 + 8 n - 1 (zero past V or for an idle row)
+                auto load_n = [&](const uint16_t* src, int v0, int n, uint32_t* dst) {
 #pragma unroll
                     for (int g8 = 0; g8 < 8; ++g8) {
+                        if (g8 >= n) break;
                         if (valid && v0 + g8 * 8 < p.V) ld_u32x4(src + v0 + g8 * 8, dst + g8 * 4, pol);
                         else { dst[g8 * 4] = dst[g8 * 4 + 1] = dst[g8 * 4 + 2] = dst[g8 * 4 + 3] = 0u; }
                     }
+                };
+                auto load_blk = [&](const uint16_t* src, int t, int hb, uint32_t* dst) {
+                    load_n(src, t * kBN + hb * 64, 8, dst);
                 };
                 auto mine = [&](int hb) -> bool { return R == 1 || hb == copy; };
                 if (kMode == kDraft && i0 < ntiles && warp_live) {
                     if (mine(0)) load_blk(urow, t_lo + i0, 0, u[0]);
                     if (mine(1)) load_blk(urow, t_lo + i0, 1, u[1]);
                 }
-                const uint32_t stream = (kMode == kDraft) ? kStreamDraftBlock : kStreamResidualBlock;
                 for (int i = i0; i < ntiles; i += kEpiWG) {
                     const int t = t_lo + i;
                     const int use = (base + i) / kEpiWG;
@@ -928,83 +653,71 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                     tc::fence_after_sync();
                     const bool have_next = (i + kEpiWG < ntiles);
                     const int tnext = t + kEpiWG;
-                    // the two blocks 2t and 2t+1 share one Philox counter (index >> 2)
-                    U4 pw{0, 0, 0, 0};
-                    if (!p.greedy && warp_live)
-                        pw = philox4x32_10(U4{static_cast<uint32_t>(t >> 1), static_cast<uint32_t>(kb),
-                                              static_cast<uint32_t>(b), stream},
-                                           static_cast<uint32_t>(p.seed), static_cast<uint32_t>(p.seed >> 32));
 #pragma unroll
                     for (int hb = 0; hb < 2; ++hb) {
-                        const int v0 = t * kBN + hb * 64;
-                        if (!mine(hb) || !warp_live || failed || v0 >= p.V) continue;   // warp-uniform
-                        float y[64];
-                        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kBN + hb * 64;
+                        const int vh = t * kBN + hb * 64;
+                        if (!mine(hb) || !warp_live || failed || vh >= p.V) continue;   // warp-uniform
                         uint32_t tt[32];
                         if constexpr (kMode == kResidual) {
                             load_blk(urow, t, hb, u[hb]);
                             load_blk(trow, t, hb, tt);
                         }
-                        tc::tmem_ld32(taddr, y);
-                        tc::tmem_ld32(taddr + 32, y + 32);
-                        tc::tmem_ld_wait();
 #pragma unroll
-                        for (int w = 0; w < 32; ++w) {
-                            y[2 * w] = (y[2 * w] + bf16lo(u[hb][w])) * p.cscale;
-                            y[2 * w + 1] = (y[2 * w + 1] + bf16hi(u[hb][w])) * p.cscale;
-                        }
-                        if (kMode == kDraft && have_next) load_blk(urow, tnext, hb, u[hb]);
-                        const int blk = 2 * t + hb;
-                        const uint32_t wsel = static_cast<uint32_t>(blk) & 3u;
-                        const uint32_t rword = wsel == 0 ? pw.x : wsel == 1 ? pw.y : wsel == 2 ? pw.z : pw.w;
-                        if constexpr (kMode == kDraft) {
-                            if (v0 + 64 > p.V) {
+                        for (int sb = 0; sb < 2; ++sb) {  // two 32-token sub-blocks of the half
+                            const int v0 = vh + sb * 32;
+                            float y[32];
+                            const uint32_t taddr =
+                                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kBN + hb * 64 + sb * 32;
+                            tc::tmem_ld32(taddr, y);
+                            tc::tmem_ld_wait();
+                            const uint32_t* uh = u[hb] + sb * 16;
 #pragma unroll
-                                for (int w = 0; w < 64; ++w)
+                            for (int w = 0; w < 16; ++w) {
+                                y[2 * w] = (y[2 * w] + bf16lo(uh[w])) * p.cscale;
+                                y[2 * w + 1] = (y[2 * w + 1] + bf16hi(uh[w])) * p.cscale;
+                            }
+                            // this sub-block's U words are consumed: fetch the next tile's
+                            // (in flight while this sub-block is reduced)
+                            if (kMode == kDraft && have_next) load_n(urow, tnext * kBN + hb * 64 + sb * 32, 4, u[hb] + sb * 16);
+                            if (v0 + 32 > p.V) {
+#pragma unroll
+                                for (int w = 0; w < 32; ++w)
                                     if (v0 + w >= p.V) y[w] = -INFINITY;
                             }
-                            if (p.debug_z != nullptr) {
-                                if (valid)                // copies own disjoint blocks
-                                    for (int w = 0; w < 64; ++w)
-                                        if (v0 + w < p.V) p.debug_z[static_cast<size_t>(b) * p.V + v0 + w] = y[w];
-                                continue;
-                            }
-                            if (p.greedy) {
+                            if constexpr (kMode == kDraft) {
+                                if (p.debug_z != nullptr) {
+                                    if (valid)            // copies own disjoint halves
+                                        for (int w = 0; w < 32; ++w)
+                                            if (v0 + w < p.V) p.debug_z[static_cast<size_t>(b) * p.V + v0 + w] = y[w];
+                                    continue;
+                                }
+                                if (p.greedy) {
 #pragma unroll
-                                for (int w = 0; w < 64; ++w)
-                                    if (y[w] > best) { best = y[w]; best_i = v0 + w; }
+                                    for (int w = 0; w < 32; ++w)
+                                        if (y[w] > best.key) { best.key = y[w]; best.idx = v0 + w; }
+                                } else {
+                                    draw32(y, v0, prow, best, M, S);
+                                }
                             } else {
-                                float m4[4] = {y[0], y[1], y[2], y[3]};
+                                // residual q = max(0, p_t - p_d), p_d = 2^(y - ld2), p_t = 2^(t c - lt2);
+                                // the winner maximises q_v / E_v over the thread's tokens
+                                const uint32_t* th = tt + sb * 16;
+                                const uint32_t qbase = static_cast<uint32_t>(v0) >> 2;
 #pragma unroll
-                                for (int w = 4; w < 64; ++w) m4[w & 3] = fmaxf(m4[w & 3], y[w]);
-                                const float mb = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-                                if (!(mb > -INFINITY)) continue;   // a block without a finite logit has no mass
-                                float s4[4] = {0.f, 0.f, 0.f, 0.f};
+                                for (int qq = 0; qq < 8; ++qq) {
+                                    const U4 pw = philox_row(prow, qbase + qq);
+                                    const uint32_t wv[4] = {pw.x, pw.y, pw.z, pw.w};
 #pragma unroll
-                                for (int w = 0; w < 64; ++w) s4[w & 3] += fast_exp2(y[w] - mb);
-                                const float sb = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-                                const float key = (mb + log2f(sb)) * kLn2 + gumbel_of(uniform_open(rword));
-                                if (key > best || (key == best && blk < best_i)) { best = key; best_i = blk; }
-                                lse_merge(M, S, mb, sb);
-                            }
-                        } else {
-                            // residual mass q = max(0, p_t - p_d), p_d = 2^(y - ld2), p_t = 2^(t c - lt2)
-                            float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                            for (int w = 0; w < 32; ++w) {
-                                const float pd0 = fast_exp2(y[2 * w] - ld2), pd1 = fast_exp2(y[2 * w + 1] - ld2);
-                                const float pt0 = fast_exp2(bf16lo(tt[w]) * p.cscale - lt2);
-                                const float pt1 = fast_exp2(bf16hi(tt[w]) * p.cscale - lt2);
-                                float q0 = fmaxf(pt0 - pd0, 0.f), q1 = fmaxf(pt1 - pd1, 0.f);
-                                if (v0 + 2 * w >= p.V) q0 = 0.f;
-                                if (v0 + 2 * w + 1 >= p.V) q1 = 0.f;
-                                s4[(2 * w) & 3] += q0;
-                                s4[(2 * w + 1) & 3] += q1;
-                            }
-                            const float Q = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-                            if (Q > 0.f) {
-                                const float key = log2f(Q) * kLn2 + gumbel_of(uniform_open(rword));
-                                if (key > best || (key == best && blk < best_i)) { best = key; best_i = blk; }
+                                    for (int j = 0; j < 4; ++j) {
+                                        const int w = 4 * qq + j;
+                                        const float tv = (w & 1) ? bf16hi(th[w >> 1]) : bf16lo(th[w >> 1]);
+                                        const float pd = fast_exp2(y[w] - ld2);
+                                        const float ptv = fast_exp2(tv * p.cscale - lt2);
+                                        const float qv = (v0 + w < p.V) ? fmaxf(ptv - pd, 0.f) : 0.f;
+                                        const float E = exp_draw(wv[j]);
+                                        if (qv * Eq > qb * E) { qb = qv; Eq = E; best.idx = v0 + w; }
+                                    }
+                                }
                             }
                         }
                     }
@@ -1012,6 +725,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&tempty[buf]);
                 }
+                if (kMode == kResidual && qb > 0.f) best.key = fast_log2(qb) - fast_log2(Eq);
                 // the next position's first U tile of this lane does not depend on x_k:
                 // bring it into L2 while the grid hands over
                 if (kMode == kDraft && k < k1 && valid && warp_live) {
@@ -1025,7 +739,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                         }
                     }
                 }
-                rowres[eg * kBM + lrow] = RowRes{best, best_i, M, S};
+                rowres[eg * kBM + lrow] = RowRes{best, M, S};
             }
             pro_sync();
 
@@ -1034,20 +748,24 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                 const int rr = (warp - 4) * 32 + lane;
                 const int b = m0 + rr;
                 if (rr < nrows && row_k(b, k) > 0) {
-                    RowRes r0{-INFINITY, 0x7FFFFFFF, -INFINITY, 0.f};
+                    Best b0{-INFINITY, 0x7FFFFFFF, 0.f};
+                    float m = -INFINITY, s = 0.f;
                     for (int e = 0; e < kEpiWG; ++e)
                         for (int c = 0; c < R; ++c) {
                             const RowRes r1 = rowres[e * kBM + c * rpc + rr];
-                            if (r1.key > r0.key || (r1.key == r0.key && r1.idx < r0.idx)) { r0.key = r1.key; r0.idx = r1.idx; }
-                            lse_merge(r0.m, r0.s, r1.m, r1.s);
+                            best_take(b0, r1.best.key, r1.best.idx, r1.best.y);
+                            lse_merge(m, s, r1.m, r1.s);
                         }
                     const size_t slot = static_cast<size_t>(k - 1) * p.B + b;
-                    if (kMode == kDraft && !p.greedy) p.ws.part[slot * kMaxChunks + pc] = make_float2(r0.m, r0.s);
-                    if (r0.key > -INFINITY) atomicMax(&p.ws.words[slot], pack_key(r0.key, static_cast<uint32_t>(r0.idx)));
-                    // greedy: the next A row is one of the CTAs' best tokens; bring ours into L2
-                    if (kMode == kDraft && p.greedy && k < k1 && r0.idx >= 0 && r0.idx < p.V)
+                    if (kMode == kDraft && !p.greedy) {
+                        p.ws.part[slot * kMaxChunks + pc] = make_float2(m, s);
+                        p.ws.ybest[slot * kMaxChunks + pc] = b0.y;
+                    }
+                    if (b0.key > -INFINITY) atomicMax(&p.ws.words[slot], pack_key(b0.key, static_cast<uint32_t>(b0.idx)));
+                    // the next A row is one of the CTAs' best tokens; bring ours into L2
+                    if (kMode == kDraft && k < k1 && b0.idx >= 0 && b0.idx < p.V)
                         for (int off = 0; off < p.r * 2; off += 128)
-                            prefetch_l2(reinterpret_cast<const uint8_t*>(p.W1) + static_cast<size_t>(r0.idx) * p.r * 2 + off);
+                            prefetch_l2(reinterpret_cast<const uint8_t*>(p.W1) + static_cast<size_t>(b0.idx) * p.r * 2 + off);
                 }
             }
             if (kMode == kDraft && multi && k < k1) arrive();
@@ -1057,43 +775,34 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
         if (kMode == kResidual && p.fuse_tail) {
             // ------------------------------------------------ final tokens
             arrive();
-            wait_all();                                   // every CTA published its residual blocks
+            wait_all();                                   // every CTA published its residual winners
             if (warp >= 2 && *s_fail == 0) {
                 const int pair = (warp - 2) >> 1;
                 for (int b = blockIdx.x + pair * gridDim.x; b < p.B; b += 5 * gridDim.x)
-                    finish_pair<true, 1>(p.fin, b, p.gamma, p.V, p.r, p.U, p.W1, p.E, p.W2, p.x0, p.x, p.cscale, p.seed,
-                                         st, 2 + pair, reinterpret_cast<float*>(xch + 2 * pair), xchi + 2 * pair);
+                    finish_pair<true>(p.fin, b, p.gamma, p.V, p.cscale, p.seed, st, 2 + pair, xch + 2 * pair,
+                                      xchi + 2 * pair);
             }
         }
         if (kMode == kDraft && p.fuse_tail && p.debug_z == nullptr) {
             // ------------------------------------------ x_gamma and finalize
+            const int cta = static_cast<int>(blockIdx.x), ncta = static_cast<int>(gridDim.x);
+            const int nown = (cta < p.B) ? (p.B - 1 - cta) / ncta + 1 : 0;
             arrive();
             wait_all();                                   // every CTA published the last position
-            if (!p.greedy) {
-                draw_owned(k1);
-            } else {
-                for (int j = ptid; j < nown; j += kPro) {
-                    const int b = blockIdx.x + j * gridDim.x;
-                    const unsigned long long w = __ldcg(p.ws.words + static_cast<size_t>(k1 - 1) * p.B + b);
-                    const uint32_t idx = unpack_idx(w);
-                    int tok = static_cast<int>(idx);
-                    if (w == 0ull || idx >= static_cast<uint32_t>(p.V)) {
-                        set_status(st, DSPARK_ERR_DEVICE_CHECK, 3);
-                        tok = 0;
-                    }
-                    p.x[b * p.gamma + k1 - 1] = tok;
-                }
+            for (int j = ptid; j < nown; j += kPro) {
+                const int b = cta + j * ncta;
+                p.x[b * p.gamma + k1 - 1] = (*s_fail == 0) ? winner(b, k1) : 0;
             }
             pro_sync();
             // one warp per (owned request, position)
             for (int item = warp - 1; item < nown * p.gamma; item += kPro / 32) {
-                const int b = blockIdx.x + (item / p.gamma) * gridDim.x, k = item % p.gamma + 1;
+                const int b = cta + (item / p.gamma) * ncta, k = item % p.gamma + 1;
                 finalize_position<true>(b, k, p.B, p.gamma, p.V, p.H, p.r, p.h, p.W1, p.w, p.bias, p.x0, p.x,
-                                        p.greedy, p.P, p.ws.part, p.ws.ytok, p.lse_d, p.logp_d, p.c, st);
+                                        p.greedy, p.P, kBN, NT, p.ws.part, p.ws.ybest, p.lse_d, p.logp_d, p.c, st);
             }
             pro_sync();
             for (int j = ptid; j < nown; j += kPro) {     // survival a_k = prod c_1..c_k, in k order
-                const int b = blockIdx.x + j * gridDim.x;
+                const int b = cta + j * ncta;
                 float surv = 1.f;
                 for (int kk = 0; kk < p.gamma; ++kk) {
                     const size_t o = static_cast<size_t>(b) * p.gamma + kk;
@@ -1113,8 +822,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
 }
 
 constexpr size_t kTcSmem = 1024 + 4 * kASlabBytes + kStages * kSlabBytes + (2 * kStages + 4 * kEpiWG) * 8 + 16 +
-                           kEpiWG * kBM * sizeof(RowRes) + kBM * 4 + 10 * 8 + 10 * 4 + 16 + 2 * 256 * 4 +
-                           2 * 24 * 4 + 16;
+                           kEpiWG * kBM * sizeof(RowRes) + kBM * 4 + 10 * 4 + 10 * 4 + 16;
 
 // ------------------------------------------------------------ host side ---
 inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {

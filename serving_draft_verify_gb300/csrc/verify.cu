@@ -5,16 +5,18 @@
 //
 //   plan    clears the per-call words and lists the scheduled rows;
 //   rows    one pass over every scheduled target row (b, k), k <= l*_b + 1:
-//           per 64-token block the logsumexp of t / T and a Gumbel key for a
-//           draw from p_t (streams 6 / 5); greedy: the argmax of t;
-//   chain   one warp per request: p_t(x_k) / p_d(x_k) against u (stream 1),
-//           stop at the first rejection;
+//           rows k <= l*_b: the logsumexp of t / T (for p_t(x_k) and the
+//           residual); row l*_b + 1: the Gumbel-max draw from p_t over the
+//           vocabulary (stream 2), the bonus token if nothing is rejected;
+//           greedy: the argmax of t;
+//   decide  by the CTA that completes a row: p_t(x_k) / p_d(x_k) against u
+//           (stream 1); by the CTA that completes a request: n_accept, and
+//           the bonus token, or the rejected position for the residual;
 //   residual for the rejected rows only: the bias engine in its residual mode
-//           (z rebuilt exactly as the draft built it), per block the mass of
-//           max(0, p_t - p_d) and a Gumbel key (stream 4);
-//   finish  two warps per request: the token inside the winning block --
-//           residual (stream 2), or a draw from p_t (stream 5) for the bonus
-//           row or a residual without mass.
+//           (z rebuilt exactly as the draft built it), the Gumbel-max draw
+//           from max(0, p_t - p_d) over the vocabulary (stream 2);
+//   finish  a rejected request takes the residual's winner, or, if the
+//           residual has no mass, a draw from p_t at that row (stream 2).
 #include <algorithm>
 
 #include "engine.cuh"
@@ -22,6 +24,8 @@
 namespace dspark {
 namespace {
 
+using eng::Best;
+using eng::best_take;
 using eng::ld_elem;
 using eng::lse_merge;
 using eng::pack_key;
@@ -35,13 +39,12 @@ struct VerifyWs {
     int32_t* rows;                 // [B][gamma+1] scheduled rows b*(gamma+1)+k-1, compacted in b order
     int32_t* first;                // [B] index of request b's first row in `rows`
     int32_t* plan;                 // [0] N scheduled rows, [1] blocks per rows-pass CTA
-    unsigned long long* wt;        // [B][gamma+1] target-row word: draw key (T > 0) or argmax (T = 0)
+    unsigned long long* wt;        // [B][gamma+1] row l*_b + 1: Gumbel-max winner (T > 0); every row: argmax (T = 0)
     float2* part;                  // [B][gamma+1][kNchMax] (max, sum) of t log2e / T
-    unsigned long long* res_word;  // [B] residual draw key
+    unsigned long long* res_word;  // [B] residual winner (key, ~token)
     int32_t* krow;                 // [B] rejected position (0: none)
     float* lt2;                    // [B] log2-sum-exp2 of t / T at the rejected row
     float* ld2;                    // [B] lse_d at the rejected row, log2 units
-    int32_t* stop;                 // [B] row of the final draw
     int32_t* row_cnt;              // [N] rows-pass CTAs done with compacted row n
     int32_t* req_cnt;              // [B] rows of request b whose decision is made
     int32_t* dec;                  // [B][gamma+1] acceptance of x_k at row k (k <= l*_b)
@@ -51,9 +54,9 @@ struct VerifyWs {
 };
 
 // Workspace: status | plan | gbar | wt | res_word | row_cnt | req_cnt (cleared by
-// the plan kernel) | part | krow | lt2 | ld2 | stop | rows | first | dec | lt2row | tx.
+// the plan kernel) | part | krow | lt2 | ld2 | rows | first | dec | lt2row | tx.
 struct VerifyLayout {
-    size_t plan, gbar, wt, res_word, row_cnt, req_cnt, part, krow, lt2, ld2, stop, rows, first, dec, lt2row, tx, total;
+    size_t plan, gbar, wt, res_word, row_cnt, req_cnt, part, krow, lt2, ld2, rows, first, dec, lt2row, tx, total;
 };
 
 VerifyLayout verify_ws_layout(int B, int gamma) {
@@ -71,7 +74,6 @@ VerifyLayout verify_ws_layout(int B, int gamma) {
     take(L.krow, nb * 4);
     take(L.lt2, nb * 4);
     take(L.ld2, nb * 4);
-    take(L.stop, nb * 4);
     take(L.rows, rows * 4);
     take(L.first, nb * 4);
     take(L.dec, rows * 4);
@@ -95,7 +97,6 @@ VerifyWs verify_ws(void* workspace, int B, int gamma) {
     ws.krow = reinterpret_cast<int32_t*>(w + L.krow);
     ws.lt2 = reinterpret_cast<float*>(w + L.lt2);
     ws.ld2 = reinterpret_cast<float*>(w + L.ld2);
-    ws.stop = reinterpret_cast<int32_t*>(w + L.stop);
     ws.row_cnt = reinterpret_cast<int32_t*>(w + L.row_cnt);
     ws.req_cnt = reinterpret_cast<int32_t*>(w + L.req_cnt);
     ws.dec = reinterpret_cast<int32_t*>(w + L.dec);
@@ -191,8 +192,9 @@ verify_plan(int B, int gamma, int V, int rows_ctas, const int32_t* __restrict__ 
 // One warp, run by the rows-pass CTA that finished row (b, k) last: for
 // k <= l*_b the acceptance test of x_k (u < p_t(x_k) / p_d(x_k), u from
 // stream 1; greedy: x_k == argmax t_k), and, if this was the last of request
-// b's l*_b + 1 rows, the request's outcome: n_accept, the stop row, and what
-// the final draw needs (greedy: the token itself).
+// b's l*_b + 1 rows, the request's outcome: n_accept, and either the final
+// token (greedy: argmax t at the stop row; T > 0 with nothing rejected: the
+// bonus row's Gumbel-max winner) or the rejected position for the residual.
 template <bool kBF16>
 __device__ __noinline__ void decide_row(int n, int row, int b, int k, int gamma, int V, int per, int npad,
                                         const void* __restrict__ t, const int32_t* __restrict__ x,
@@ -254,17 +256,15 @@ __device__ __noinline__ void decide_row(int n, int row, int b, int k, int gamma,
     if (lane == 0) {
         const int nacc = rej ? rej - 1 : e;
         n_accept[b] = nacc;
-        const int srow = nacc + 1;                        // row of the final draw
-        ws.stop[b] = srow;
-        if (greedy) {
-            const unsigned long long w = __ldcg(ws.wt + static_cast<size_t>(b) * (gamma + 1) + srow - 1);
-            if (w == 0ull) set_status(ws.status, DSPARK_ERR_DEVICE_CHECK, 6);
+        ws.krow[b] = greedy ? 0 : rej;
+        if (greedy || rej == 0) {
+            // greedy: argmax t at the stop row nacc + 1; otherwise the bonus row e + 1's draw
+            const unsigned long long w = __ldcg(ws.wt + static_cast<size_t>(b) * (gamma + 1) + nacc);
+            if (w == 0ull || unpack_idx(w) >= static_cast<uint32_t>(V)) set_status(ws.status, DSPARK_ERR_DEVICE_CHECK, 6);
             next_token[b] = (w == 0ull || unpack_idx(w) >= static_cast<uint32_t>(V)) ? 0 : static_cast<int>(unpack_idx(w));
-            ws.krow[b] = 0;
         } else {
-            ws.krow[b] = rej;
-            ws.lt2[b] = rej ? __ldcg(ws.lt2row + b * (gamma + 1) + rej - 1) : 0.f;
-            ws.ld2[b] = rej ? lse_d[b * gamma + rej - 1] * kLog2e : 0.f;
+            ws.lt2[b] = __ldcg(ws.lt2row + b * (gamma + 1) + rej - 1);
+            ws.ld2[b] = lse_d[b * gamma + rej - 1] * kLog2e;
         }
     }
 }
@@ -272,31 +272,14 @@ __device__ __noinline__ void decide_row(int n, int row, int b, int k, int gamma,
 // ------------------------------------------------------------- rows pass ---
 // CTA c takes blocks [c per, (c+1) per) of the padded scheduled rows laid end
 // to end, one piece per row it touches; per piece a warp covers 4 quads of 4
-// consecutive blocks per step, 8 lanes per block, 8 logits per lane.  Per
-// 64-token block: the logsumexp of t / T and a Gumbel key for a draw from p_t
-// (greedy: the argmax of t); per piece the CTA's best and its (max, sum).
-// Sixteen lanes finish the 16 blocks of a step, one block each.  The Philox
-// words of a block key come one step early from the other sixteen lanes: every
-// second step runs one Philox sequence for two steps' quads.
+// consecutive 64-token blocks per step, 8 lanes per block, 8 logits per lane
+// (all loads of a step issued first).  What a piece reduces depends on its row:
+//   T = 0            the argmax of t;
+//   rows k <= l*_b   the (max, sum) of 2^(t log2e / T), online per lane;
+//   row  l*_b + 1    the Gumbel-max winner over the row: the token maximising
+//                    t_v log2e / T - log2 E_v, E_v = -ln u_v (stream 2).
+// Per piece the CTA publishes its (max, sum) or its winner (atomicMax).
 constexpr int kRowsCtasPerSm = 3;
-
-// Two float32 lanes in one 64-bit register (Blackwell f32x2 arithmetic); each
-// lane of fma2 is one fused multiply-add with a single rounding, as fmaf.
-__device__ __forceinline__ unsigned long long pk2(float lo, float hi) {
-    unsigned long long r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ float2 upk2(unsigned long long v) {
-    float2 r;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-    return r;
-}
-__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
-    unsigned long long d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
 
 template <bool kBF16>
 __global__ void __launch_bounds__(256, kRowsCtasPerSm)
@@ -329,15 +312,13 @@ verify_rows(int gamma, int V, const void* __restrict__ t, const int32_t* __restr
             int e = ell[b];
             e = e < 0 ? 0 : (e > gamma ? gamma : e);
             const int xk = (k <= e) ? x[b * gamma + k - 1] : -1;
+            const bool draw = !greedy && k == e + 1;      // the bonus row's Gumbel-max draw
             float txk = 0.f;
             bool have_tx = false;
             float best = -INFINITY, M = -INFINITY, S = 0.f;
             int best_i = 0x7FFFFFFF;
-            // each warp takes 4 consecutive quads per step; all loads of a step are issued first
             constexpr int kU = 4;
-            int step = 0;                                 // this warp's steps in the piece
-            uint32_t next_word = 0u;                      // lanes part >= 4: the next step's Philox word
-            for (int q0 = lo / 4 + warp * kU; q0 * 4 < hi; q0 += 8 * kU, ++step) {
+            for (int q0 = lo / 4 + warp * kU; q0 * 4 < hi; q0 += 8 * kU) {
                 float y[kU][8];
 #pragma unroll
                 for (int u = 0; u < kU; ++u) {
@@ -384,68 +365,59 @@ verify_rows(int gamma, int V, const void* __restrict__ t, const int32_t* __restr
                         for (int i = 0; i < 8; ++i)
                             if (y[u][i] > best) { best = y[u][i]; best_i = v + i; }
                     }
-                    continue;
-                }
-                // per block (quad u, sub): max and sum of 2^(y c - m c) over its 8 lanes
-                float mq[kU], sq[kU];
+                } else if (draw) {
+                    // the row's Philox constants, formed per step (cheaper than holding them in registers)
+                    const PhiloxRow pr = philox_row_setup(seed, static_cast<uint32_t>(k), static_cast<uint32_t>(b),
+                                                          kStreamVerifyToken);
 #pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    float m = y[u][0];
+                    for (int u = 0; u < kU; ++u) {
+                        const int v = ((q0 + u) * 4 + sub) * 64 + part * 8;
+                        if (v >= V) continue;
 #pragma unroll
-                    for (int i = 1; i < 8; ++i) m = fmaxf(m, y[u][i]);
-                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                    const float mc = m * cscale;
-                    float sum = 0.f;
-                    if (m > -INFINITY) {
-                        const unsigned long long c2 = pk2(cscale, cscale), nm2 = pk2(-mc, -mc);
+                        for (int h = 0; h < 2; ++h) {
+                            const U4 pw = philox_row(pr, (static_cast<uint32_t>(v) >> 2) + h);
+                            const uint32_t wv[4] = {pw.x, pw.y, pw.z, pw.w};
 #pragma unroll
-                        for (int i = 0; i < 8; i += 2) {
-                            const float2 z = upk2(fma2(pk2(y[u][i], y[u][i + 1]), c2, nm2));
-                            sum += fast_exp2(z.x);
-                            sum += fast_exp2(z.y);
+                            for (int i = 0; i < 4; ++i) {
+                                const float key = y[u][4 * h + i] * cscale - fast_log2(exp_draw(wv[i]));
+                                if (key > best) { best = key; best_i = v + 4 * h + i; }   // -inf past V never wins
+                            }
                         }
                     }
-                    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-                    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-                    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-                    mq[u] = mc;
-                    sq[u] = sum;
-                }
-                // lane (sub, part < 4) finishes block (quad q0 + part, sub): its Philox
-                // counter is that quad's, its word the block's.  On even steps lane
-                // (sub, part + 4) draws the word of the same block of the next step
-                // (quad q0 + 8 kU + part) and hands it down four lanes a step later.
-                const int pu = part & 3;
-                uint32_t word;
-                if ((step & 1) == 0) {
-                    const int qp = q0 + pu + (part >= 4 ? 8 * kU : 0);
-                    const U4 pw = philox4x32_10_inline(U4{static_cast<uint32_t>(qp), static_cast<uint32_t>(k),
-                                                          static_cast<uint32_t>(b), kStreamTargetBlock},
-                                                       static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
-                    word = sub == 0 ? pw.x : sub == 1 ? pw.y : sub == 2 ? pw.z : pw.w;
-                    next_word = word;
                 } else {
-                    word = __shfl_down_sync(0xffffffffu, next_word, 4);
-                }
-                const float m = pu == 0 ? mq[0] : pu == 1 ? mq[1] : pu == 2 ? mq[2] : mq[3];
-                const float sum = pu == 0 ? sq[0] : pu == 1 ? sq[1] : pu == 2 ? sq[2] : sq[3];
-                const int blk = (q0 + pu) * 4 + sub;
-                if (part < 4 && blk < hi && sum > 0.f) {
-                    const float key = (m + log2f(sum)) * kLn2 + gumbel_of_inline(uniform_open(word));
-                    if (key > best || (key == best && blk < best_i)) { best = key; best_i = blk; }
-                    lse_merge(M, S, m, sum);
+                    // online (max, sum) of 2^(y c) per lane: a new maximum rescales the sum
+#pragma unroll
+                    for (int u = 0; u < kU; ++u) {
+                        float m = y[u][0];
+#pragma unroll
+                        for (int i = 1; i < 8; ++i) m = fmaxf(m, y[u][i]);
+                        if (!(m > -INFINITY)) continue;
+                        const float mc = m * cscale;
+                        if (mc > M) {
+                            S = (S > 0.f) ? S * fast_exp2(M - mc) : 0.f;
+                            M = mc;
+                        }
+                        float s = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) s += fast_exp2(fmaf(y[u][i], cscale, -M));
+                        S += s;
+                    }
                 }
             }
+            if (greedy || draw) {
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, best_i, o);
-                const float om = __shfl_xor_sync(0xffffffffu, M, o);
-                const float os = __shfl_xor_sync(0xffffffffu, S, o);
-                if (ob > best || (ob == best && oi < best_i)) { best = ob; best_i = oi; }
-                lse_merge(M, S, om, os);
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+                    const int oi = __shfl_xor_sync(0xffffffffu, best_i, o);
+                    if (ob > best || (ob == best && oi < best_i)) { best = ob; best_i = oi; }
+                }
+            } else {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float om = __shfl_xor_sync(0xffffffffu, M, o);
+                    const float os = __shfl_xor_sync(0xffffffffu, S, o);
+                    lse_merge(M, S, om, os);
+                }
             }
             if (have_tx) ws.tx[row] = txk;
             if (lane == 0) { rk[warp] = best; ri[warp] = best_i; rm[warp] = M; rs[warp] = S; }
@@ -457,7 +429,7 @@ verify_rows(int gamma, int V, const void* __restrict__ t, const int32_t* __restr
                     if (rk[w] > bk || (rk[w] == bk && ri[w] < bi)) { bk = rk[w]; bi = ri[w]; }
                     lse_merge(m, s, rm[w], rs[w]);
                 }
-                if (!greedy) ws.part[static_cast<size_t>(row) * kNchMax + slot] = make_float2(m, s);
+                if (!greedy && !draw) ws.part[static_cast<size_t>(row) * kNchMax + slot] = make_float2(m, s);
                 if (bk > -INFINITY) atomicMax(&ws.wt[row], pack_key(bk, static_cast<uint32_t>(bi)));
                 // the CTA that completes the row makes its decision
                 const long long g0 = static_cast<long long>(n) * npad;
@@ -476,6 +448,10 @@ verify_rows(int gamma, int V, const void* __restrict__ t, const int32_t* __restr
 }
 
 // ---------------------------------------------------- residual, CUDA cores ---
+// Request b (blockIdx.y) rejected at k, chunk blockIdx.x of the 64-token
+// blocks: per token q = max(0, p_t - p_d) with p_d rebuilt from U_k + W2 . e,
+// and the Gumbel-max winner of ln q (stream 2): the token maximising q_v / E_v
+// (cross-multiplied), published with key log2 q - log2 E.
 template <bool kBF16>
 __global__ void __launch_bounds__(256)
 residual_simt(int B, int gamma, int V, int r, const void* __restrict__ t, const void* __restrict__ U,
@@ -499,27 +475,33 @@ residual_simt(int B, int gamma, int V, int r, const void* __restrict__ t, const 
     const int hi = static_cast<int>(static_cast<long long>(chunk + 1) * nblk / nchunk);
     const size_t urow = (static_cast<size_t>(b) * gamma + (k - 1)) * V;
     const size_t trow = (static_cast<size_t>(b) * (gamma + 1) + (k - 1)) * V;
-    float best = -INFINITY;
-    int best_i = 0x7FFFFFFF;
+    const PhiloxRow pr = philox_row_setup(seed, static_cast<uint32_t>(k), static_cast<uint32_t>(b), kStreamVerifyToken);
+    float qb = 0.f, Eb = 1.f;
+    int ib = 0x7FFFFFFF;
     for (int blk = lo + warp; blk < hi; blk += 8) {
-        float qs = 0.f;
+        const int v = blk * 64 + 2 * lane;
+        const U4 pw = philox_row(pr, static_cast<uint32_t>(v) >> 2);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int v = blk * 64 + h * 32 + lane;
-            if (v < V) {
+            if (v + h < V) {
                 float acc = 0.f;
-                for (int j = 0; j < r; ++j) acc = fmaf(ld_elem<kBF16>(W2, static_cast<size_t>(v) * r + j), e[j], acc);
-                const float yd = (ld_elem<kBF16>(U, urow + v) + acc) * cscale;
-                const float yt = ld_elem<kBF16>(t, trow + v) * cscale;
-                qs += fmaxf(fast_exp2(yt - lt2) - fast_exp2(yd - ld2), 0.f);
+                for (int j = 0; j < r; ++j)
+                    acc = fmaf(ld_elem<kBF16>(W2, static_cast<size_t>(v + h) * r + j), e[j], acc);
+                const float yd = (ld_elem<kBF16>(U, urow + v + h) + acc) * cscale;
+                const float yt = ld_elem<kBF16>(t, trow + v + h) * cscale;
+                const float q = fmaxf(fast_exp2(yt - lt2) - fast_exp2(yd - ld2), 0.f);
+                const float Ev = exp_draw(u4_word(pw, (v + h) & 3));
+                if (q * Eb > qb * Ev) { qb = q; Eb = Ev; ib = v + h; }   // tokens ascend per thread
             }
         }
-        const float Q = warp_sum(qs);
-        if (Q > 0.f) {
-            const float u = uniform_open(draw_word(seed, b, k, kStreamResidualBlock, static_cast<uint32_t>(blk)));
-            const float key = log2f(Q) * kLn2 + gumbel_of(u);
-            if (key > best) { best = key; best_i = blk; }   // blocks ascend per warp
-        }
+    }
+    float best = (qb > 0.f) ? fast_log2(qb) - fast_log2(Eb) : -INFINITY;
+    int best_i = ib;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, best_i, o);
+        if (ob > best || (ob == best && oi < best_i)) { best = ob; best_i = oi; }
     }
     if (lane == 0) { rk[warp] = best; ri[warp] = best_i; }
     __syncthreads();
@@ -534,15 +516,13 @@ residual_simt(int B, int gamma, int V, int r, const void* __restrict__ t, const 
 
 // ----------------------------------------------------------- finish pass ---
 // Two warps per request (T > 0): eng::finish_pair, for the paths whose
-// residual launch does not draw the final token itself.
-template <bool kBF16, int kCPL>
+// residual launch does not write the final token itself.
+template <bool kBF16>
 __global__ void __launch_bounds__(64)
-verify_finish(int gamma, int V, int r, eng::FinishArgs f, const void* __restrict__ U, const void* __restrict__ W1,
-              const void* __restrict__ E, const void* __restrict__ W2, const int32_t* __restrict__ x0,
-              const int32_t* __restrict__ x, float cscale, uint64_t seed, StatusBlock* st) {
+verify_finish(int gamma, int V, eng::FinishArgs f, float cscale, uint64_t seed, StatusBlock* st) {
     __shared__ float xch[2];
     __shared__ int xchi[2];
-    eng::finish_pair<kBF16, kCPL>(f, blockIdx.x, gamma, V, r, U, W1, E, W2, x0, x, cscale, seed, st, 1, xch, xchi);
+    eng::finish_pair<kBF16>(f, blockIdx.x, gamma, V, cscale, seed, st, 1, xch, xchi);
 }
 
 }  // namespace
@@ -610,10 +590,12 @@ static dspark_status_t verify_impl(int B, int gamma, int V, int r, dspark_dtype_
     if ((stt = launch_status()) != DSPARK_OK || greedy) return stt;
 
     eng::FinishArgs f{};
-    f.T = static_cast<const uint16_t*>(t_logits);
-    f.krow = ws.krow; f.stop = ws.stop; f.lt2 = ws.lt2; f.ld2 = ws.ld2;
-    f.res_word = ws.res_word; f.wt = ws.wt; f.next_token = next_token;
-    bool drawn = false;                                   // final tokens drawn by the residual launch
+    f.T = bf ? static_cast<const uint16_t*>(t_logits) : nullptr;
+    f.Tf = bf ? nullptr : static_cast<const float*>(t_logits);
+    f.krow = ws.krow;
+    f.res_word = ws.res_word;
+    f.next_token = next_token;
+    bool drawn = false;                                   // final tokens written by the residual launch
     if (eng::use_tc_path(dt, r)) {
         CUtensorMap map;
         if (!eng::encode_w2_map(&map, W2, V, r)) return DSPARK_ERR_CUDA;
@@ -626,9 +608,9 @@ static dspark_status_t verify_impl(int B, int gamma, int V, int r, dspark_dtype_
         p.W2 = static_cast<const uint16_t*>(W2); p.k_last = 1;
         p.x0 = x0; p.x = const_cast<int32_t*>(x); p.cscale = cscale; p.greedy = 0;   // read only here
         p.seed = seed; p.P = P;
-        p.ws = eng::Ws{ws.status, ws.res_word, nullptr, nullptr, ws.gbar, nullptr};
+        p.ws = eng::Ws{ws.status, ws.res_word, nullptr, nullptr, ws.gbar};
         p.krow = ws.krow; p.T = static_cast<const uint16_t*>(t_logits); p.lt2 = ws.lt2; p.ld2 = ws.ld2;
-        // with a co-resident grid the same launch draws the final tokens
+        // with a co-resident grid the same launch writes the final tokens
         drawn = nM * P <= sm_count(current_device());
         p.fuse_tail = drawn ? 1 : 0;
         p.fin = f;
@@ -643,11 +625,9 @@ static dspark_status_t verify_impl(int B, int gamma, int V, int r, dspark_dtype_
     }
     if (drawn) return DSPARK_OK;
     if (bf)
-        verify_finish<true, 1><<<B, 64, 0, s>>>(gamma, V, r, f, U, W1, E, W2, x0, x, cscale, seed, ws.status);
-    else if (r <= 128)
-        verify_finish<false, 1><<<B, 64, 0, s>>>(gamma, V, r, f, U, W1, E, W2, x0, x, cscale, seed, ws.status);
+        verify_finish<true><<<B, 64, 0, s>>>(gamma, V, f, cscale, seed, ws.status);
     else
-        verify_finish<false, 2><<<B, 64, 0, s>>>(gamma, V, r, f, U, W1, E, W2, x0, x, cscale, seed, ws.status);
+        verify_finish<false><<<B, 64, 0, s>>>(gamma, V, f, cscale, seed, ws.status);
     return launch_status();
 }
 

@@ -9,3 +9,21 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+
+
+def pytest_terminal_summary(terminalreporter):
+    """The parity tests' exempt decisions (oracle margin below 1e-4), per test."""
+    try:
+        from tests.gpu_harness import EXEMPT
+    except Exception:
+        return
+    if not EXEMPT:
+        return
+    tr = terminalreporter
+    tr.section("exempt decisions (oracle margin < 1e-4)")
+    tot_e = tot_n = 0
+    for test, kind, e, n in EXEMPT:
+        tr.write_line(f"{e:6d} / {n:8d}  {kind:16s} {test}")
+        tot_e += e
+        tot_n += n
+    tr.write_line(f"{tot_e:6d} / {tot_n:8d}  in all")

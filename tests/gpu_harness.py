@@ -9,6 +9,16 @@ from serving_draft_verify_gb300 import workloads as wl
 MARGIN = 1e-4
 FTOL = {"bf16": 2e-3, "f32": 1e-5}
 
+# Exempt decisions (oracle margin below MARGIN) seen by the parity tests of this
+# session: (test id, kind, exempt, decisions checked).  conftest prints them in
+# the terminal summary.
+EXEMPT = []
+
+
+def report_exempt(kind, exempt, checked):
+    import os
+    EXEMPT.append((os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0], kind, int(exempt), int(checked)))
+
 
 def npy(t):
     return t.detach().cpu().numpy()
@@ -82,14 +92,21 @@ def compare_draft(gpu, ref, dtype, rows=None):
     for k in ("lse_d", "logp_d"):
         err = np.abs(gpu[k][rows] - ref[k])[same].max(initial=0.0)
         assert err <= FTOL["bf16"], (k, err)
+    report_exempt("draft tokens", exempt.sum(), exempt.size)
     return int(exempt.sum())
 
 
-def compare_verify(gpu, ref, rows=None):
+def compare_verify(gpu, ref, rows=None, exact=False):
+    """exact: no exemption at all.  Greedy verification compares the same bf16 / fp32
+    target values on both sides and breaks ties by the lowest index on both, so its
+    decisions agree even where the top-2 gap is zero (exact ties are common among
+    bf16 logits); the near-tie count is still reported."""
     rows = np.arange(gpu["n_accept"].shape[0]) if rows is None else np.asarray(rows)
-    exempt = ref["margin"] < MARGIN
+    near = ref["margin"] < MARGIN
+    exempt = np.zeros_like(near) if exact else near
     bad = ((gpu["n_accept"][rows] != ref["n_accept"]) | (gpu["next_token"][rows] != ref["next_token"])) & ~exempt
     assert not bad.any(), (f"{bad.sum()} verify mismatches; first rows {rows[bad][:5]}: gpu "
                            f"{gpu['n_accept'][rows][bad][:5]}/{gpu['next_token'][rows][bad][:5]} oracle "
                            f"{ref['n_accept'][bad][:5]}/{ref['next_token'][bad][:5]}")
+    report_exempt("verify requests" + (" (exact)" if exact else ""), near.sum(), near.size)
     return int(exempt.sum())

@@ -43,7 +43,7 @@ def test_draft_and_verify_at_edge_lengths(dsv, name, cfg, changes, temperature):
     for ell in (np.full(cfg.B, cfg.gamma), np.zeros(cfg.B, int), rng.integers(0, cfg.gamma + 1, cfg.B)):
         g = gpu_verify(dsv, inp, d, ell, temperature=temperature)
         vref = oracle_verify(inp, dn, ell, temperature=temperature)
-        exempt += compare_verify(g, vref)
+        exempt += compare_verify(g, vref, exact=(temperature == 0.0))
         assert np.all((g["n_accept"] >= 0) & (g["n_accept"] <= ell))
         assert np.all((g["next_token"] >= 0) & (g["next_token"] < cfg.V))
-    assert exempt <= max(2, 3 * cfg.B // 10)
+    assert exempt <= max(2, (dn["x"].size + 3 * cfg.B) // 20)

@@ -46,7 +46,7 @@ def test_verify_parity_small(dsv, name, cfg, changes, temperature):
     for ell in _ells(cfg.B, cfg.gamma, rng):
         g = gpu_verify(dsv, inp, d, ell, temperature=temperature)
         ref = oracle_verify(inp, dn, ell, temperature=temperature)
-        exempt += compare_verify(g, ref)
+        exempt += compare_verify(g, ref, exact=(temperature == 0.0))
         assert np.all((g["n_accept"] >= 0) & (g["n_accept"] <= ell))
         assert np.all((g["next_token"] >= 0) & (g["next_token"] < cfg.V))
     assert exempt <= max(2, 3 * cfg.B // 20)
@@ -99,11 +99,14 @@ def test_verify_lossless_chi_square(dsv):
     assert stats.chisquare(obs, exp).pvalue > 1e-3
 
 
-@pytest.mark.parametrize("key,temperature,nrows", [("qwen3_8b", 0.7, 16), ("qwen3_8b", 0.0, 16),
-                                                   ("draft_27b", None, 8), ("high_conc", None, 6)])
-def test_verify_full_size_sampled(dsv, key, temperature, nrows):
-    """Full-size round (draft -> schedule -> verify) on the GPU; sampled requests
-    are verified again by the oracle from the GPU's draft outputs."""
+@pytest.mark.parametrize("key,temperature", [("qwen3_8b", 0.7), ("qwen3_8b", 0.0), ("draft_27b", None),
+                                             ("high_conc", None)])
+def test_verify_full_size(dsv, key, temperature):
+    """Full-size round (draft -> schedule -> verify) on the GPU; requests are
+    verified again by the oracle from the GPU's draft outputs (all of them up to
+    B = 256; at B = 1024, 152 spread over every M-tile and CTA residue plus the
+    request with the longest prefix)."""
+    from tests.test_gpu_draft import full_size_rows
     cfg = wl.DRAFT_CONFIGS[key]
     inp = wl.make_draft_inputs(cfg, device="cuda")
     d = gpu_draft(dsv, inp, temperature=temperature)
@@ -111,11 +114,12 @@ def test_verify_full_size_sampled(dsv, key, temperature, nrows):
     ell = npy(sch["ell"])
     gv = gpu_verify(dsv, inp, d, ell, temperature=temperature)
     dn = {k: npy(v) for k, v in d.items()}
-    rng = np.random.default_rng(1)
-    rows = rng.choice(cfg.B, nrows, replace=False)
-    rows[0] = int(np.argmax(ell))
+    rows = full_size_rows(cfg.B, key)
+    if rows.size < cfg.B:
+        rows = np.unique(np.append(rows, int(np.argmax(ell))))
     ref = oracle_verify(inp, dn, ell, temperature=temperature, rows=rows)
-    compare_verify(gv, ref, rows=rows)
+    exempt = compare_verify(gv, ref, rows=rows, exact=(temperature == 0.0))
+    assert exempt <= max(2, rows.size // 20)
     assert np.all((gv["n_accept"] >= 0) & (gv["n_accept"] <= ell))
     del inp
     torch.cuda.empty_cache()
