@@ -715,6 +715,40 @@ def run_tv_only(args):
     print(json.dumps(res))
 
 
+def run_draft_only(args):
+    """dspark_draft_block alone on a high-concurrency-shaped case (B x gamma of the
+    full vocabulary), for profiling one kernel on a small case; prints one JSON line
+    with the per-call time (CUDA events, L2 flushed between calls)."""
+    import torch
+    import serving_draft_verify_gb300 as dsv
+    from serving_draft_verify_gb300 import workloads as wl
+
+    dev = torch.device("cuda", 0)
+    dsv.load()
+    lib = dsv._binding.load()
+    B, G = (int(x) for x in args.draft_case.split(":"))
+    T = wl.HIGH_CONC.temperature if args.draft_temperature is None else args.draft_temperature
+    sv = Serving(dsv, lib, wl.scaled(wl.HIGH_CONC, B=B, gamma=G), dev, T=T)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        sv.draft()
+    ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        sv.draft()
+        b.record()
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    assert dsv.workspace_status(sv.ws_d) == 0
+    m = statistics.median(ms)
+    cfg = sv.cfg
+    nb = draft_launch_bytes(cfg.B, cfg.gamma, cfg.V, cfg.H, cfg.r)
+    print(json.dumps({"workload": f"draft block, B={B} gamma={G} V={cfg.V} r={cfg.r} T={T}", "median_ms": m,
+                      "gbs": nb / (m * 1e-3) / 1e9, "logits_per_ms": B * G * cfg.V / m}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -734,6 +768,9 @@ def main():
                     help="requests of the headline round the oracle re-checks (exempt decisions reported)")
     ap.add_argument("--phase-traffic", type=float, default=None,
                     help="dram bytes per draft phase launch from an ncu capture (reported as roofline.traffic)")
+    ap.add_argument("--draft-case", default=None,
+                    help="B:gamma -- time only dspark_draft_block on that high-concurrency-shaped case")
+    ap.add_argument("--draft-temperature", type=float, default=None, help="temperature of --draft-case")
     ap.add_argument("--tv-rows", type=int, default=None,
                     help="time only the TV and training-loss kernels on this many training rows")
     args = ap.parse_args()
@@ -741,6 +778,8 @@ def main():
         args.warmup = 3
     if args.tv_rows is not None:
         run_tv_only(args)
+    elif args.draft_case is not None:
+        run_draft_only(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

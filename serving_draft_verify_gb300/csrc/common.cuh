@@ -121,13 +121,19 @@ constexpr float kLn2f = 0.69314718055994531f;
 struct U4 {
     uint32_t x, y, z, w;
 };
+// The full 64-bit product of two 32-bit words as (lo, hi), one mul.wide.u32.
+__device__ __forceinline__ void mul_wide(uint32_t a, uint32_t b, uint32_t& lo, uint32_t& hi) {
+    uint64_t p;
+    asm("mul.wide.u32 %0, %1, %2;" : "=l"(p) : "r"(a), "r"(b));
+    lo = static_cast<uint32_t>(p);
+    hi = static_cast<uint32_t>(p >> 32);
+}
 __device__ __forceinline__ U4 philox4x32_10_inline(U4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
     for (int i = 0; i < 10; ++i) {
-        const uint32_t lo0 = 0xD2511F53u * c.x;
-        const uint32_t hi0 = __umulhi(0xD2511F53u, c.x);
-        const uint32_t lo1 = 0xCD9E8D57u * c.z;
-        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z);
+        uint32_t lo0, hi0, lo1, hi1;
+        mul_wide(0xD2511F53u, c.x, lo0, hi0);
+        mul_wide(0xCD9E8D57u, c.z, lo1, hi1);
         c = U4{hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0};
         k0 += 0x9E3779B9u;
         k1 += 0xBB67AE85u;
@@ -171,28 +177,33 @@ __device__ __forceinline__ PhiloxRow philox_row_setup(uint64_t seed, uint32_t k,
     PhiloxRow r;
     r.k0 = static_cast<uint32_t>(seed);
     r.k1 = static_cast<uint32_t>(seed >> 32);
-    const uint32_t lo1 = 0xCD9E8D57u * b, hi1 = __umulhi(0xCD9E8D57u, b);
+    uint32_t lo1, hi1;
+    mul_wide(0xCD9E8D57u, b, lo1, hi1);
     r.r1_x = hi1 ^ k ^ r.k0;
     r.r1_y = lo1;
     r.r1_z = stream ^ r.k1;
     const uint32_t k0b = r.k0 + 0x9E3779B9u, k1b = r.k1 + 0xBB67AE85u;
     r.r2_y = r.r1_y ^ k0b;
-    r.r2_hi0 = __umulhi(0xD2511F53u, r.r1_x) ^ k1b;
-    r.r2_lo0 = 0xD2511F53u * r.r1_x;
+    uint32_t lo0, hi0;
+    mul_wide(0xD2511F53u, r.r1_x, lo0, hi0);
+    r.r2_hi0 = hi0 ^ k1b;
+    r.r2_lo0 = lo0;
     return r;
 }
 __device__ __forceinline__ U4 philox_row(const PhiloxRow& r, uint32_t q) {
     // round 1: only the product of q varies
-    const uint32_t lo0 = 0xD2511F53u * q, hi0 = __umulhi(0xD2511F53u, q);
+    uint32_t lo0, hi0, lo1, hi1;
+    mul_wide(0xD2511F53u, q, lo0, hi0);
     const uint32_t z1 = hi0 ^ r.r1_z;
     // round 2: the product of word x is constant, the product of z1 varies
-    const uint32_t lo1 = 0xCD9E8D57u * z1, hi1 = __umulhi(0xCD9E8D57u, z1);
+    mul_wide(0xCD9E8D57u, z1, lo1, hi1);
     U4 c{hi1 ^ r.r2_y, lo1, r.r2_hi0 ^ lo0, r.r2_lo0};
     uint32_t k0 = r.k0 + 2u * 0x9E3779B9u, k1 = r.k1 + 2u * 0xBB67AE85u;
 #pragma unroll
     for (int i = 2; i < 10; ++i) {
-        const uint32_t a0 = 0xD2511F53u * c.x, b0 = __umulhi(0xD2511F53u, c.x);
-        const uint32_t a1 = 0xCD9E8D57u * c.z, b1 = __umulhi(0xCD9E8D57u, c.z);
+        uint32_t a0, b0, a1, b1;
+        mul_wide(0xD2511F53u, c.x, a0, b0);
+        mul_wide(0xCD9E8D57u, c.z, a1, b1);
         c = U4{b1 ^ c.y ^ k0, a1, b0 ^ c.w ^ k1, a0};
         k0 += 0x9E3779B9u;
         k1 += 0xBB67AE85u;

@@ -19,13 +19,15 @@
 // (key, ~token) and, for kDraft, its (max, sum) partial and the y of its best
 // token (for log p_d of the token that wins overall).
 //
-// Layout of one CTA (384 threads, one CTA per SM):
+// Layout of one CTA (512 threads, one CTA per SM):
 //   warp 0      TMA producer: W2 tiles [128 tokens x 64 K] into a slab ring
 //               (128-byte swizzle, L2 evict-last so W2 stays resident);
 //   warp 1      TMEM allocator and MMA issuer: tcgen05.mma kind::f16,
 //               M = 128 request rows, N = 128 tokens, K = r, fp32 in TMEM;
-//   warps 4-11  two epilogue warpgroups, each with two TMEM accumulators, so
-//               the MMA of the next tile overlaps the epilogue of this one.
+//   warps 4-15  three epilogue warpgroups sharing four TMEM accumulators in
+//               rotation (a position's tile i: warpgroup i mod 3; the launch's
+//               tile g: accumulator g mod 4), so the MMA of the next tile
+//               overlaps the epilogues of the others.
 // The A operand (rows W1[x_{k_b-1}], or the rows E[b][k_b] of a gated or
 // recurrent head, gathered into shared memory with the same swizzle) is built
 // by warps 1-11 at the start of every position.
@@ -133,37 +135,89 @@ __device__ __forceinline__ void best_take(Best& b, float key, int idx, float y) 
     if (key > b.key || (key == b.key && idx < b.idx)) { b.key = key; b.idx = idx; b.y = y; }
 }
 
+// s = 1 - u for u = ((w >> 9) + 1/2) 2^-23: exact in float32, and a lower bound
+// of E = -ln u (since -ln(1 - s) >= s).
+__device__ __forceinline__ float one_minus_u(uint32_t w) {
+    return __uint_as_float(((~w) >> 9) | 0x3F800000u) - 0.999999940395355225f;
+}
+// f = s + (1 - 2^-24) = 1 + m' 2^-23 in [1, 2), exact: comparing f < X + (1 - 2^-24) tests
+// s < X without forming s (the rounding of the sum is covered by the caller's slack).
+__device__ __forceinline__ float one_minus_u_shifted(uint32_t w) {
+    return __uint_as_float(((~w) >> 9) | 0x3F800000u);
+}
+
 // The flat Gumbel-max draw over 32 consecutive tokens v0 .. v0+31 (v0 a
-// multiple of 4) with log2-weights y (-inf: no mass), and their (max, sum):
-// e_v = 2^(y_v - m), the winner maximises e_v / E_v (cross-multiplied), and
-// enters `best` with key y_v - log2 E_v.  `pr` holds the row's Philox
-// constants; word v & 3 of block v >> 2 keys index v.
+// multiple of 4) with log2-weights y (-inf: no mass), and their (max, sum).
+// Token v beats the running best iff y_v - log2 E_v > best.key, i.e. iff
+// E_v < 2^(y_v - best.key) = e_v R with e_v = 2^(y_v - m) (formed for the
+// sum anyway) and R = 2^(m - best.key).  Since E_v >= s_v = 1 - u_v, a token
+// with s_v >= e_v R (R raised by 2^-10 to cover the rounding of e_v, R and E_v)
+// cannot win, and only the rare others (a warp enters the branch when any lane
+// has one) take E_v and the exact comparison of keys.  Tokens are visited in
+// ascending order and a key must be strictly larger to win: ties keep the
+// lowest index.  `pr` holds the row's Philox constants; word v & 3 of block
+// v >> 2 keys index v.
 __device__ __forceinline__ void draw32(const float* y, int v0, const PhiloxRow& pr, Best& best, float& M,
                                        float& S) {
     float m4[4] = {y[0], y[1], y[2], y[3]};
 #pragma unroll
     for (int w = 4; w < 32; ++w) m4[w & 3] = fmaxf(m4[w & 3], y[w]);
     const float mb = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-    if (!(mb > -INFINITY)) return;                        // no finite logit: no mass
+    const bool live = mb > -INFINITY;                     // no finite logit: no mass, no candidate
+    const float mref = live ? mb : 0.f;
+    constexpr float kSlack = 1.0009765625f;               // 1 + 2^-10
+    // s_v < e_v R  <=>  f_v < e_v R + (1 - 2^-24); 2^-23 more covers the rounding of that sum
+    constexpr float kShift = 0.999999940395355225f + 1.1920928955078125e-07f;
+    float R = live ? fast_exp2(mb - best.key) * kSlack : 0.f;   // +inf while nothing is drawn yet
+    // per half of 16 tokens: its four Philox blocks first (independent chains the scheduler
+    // can overlap), then the sum and the candidates (a bit per token), then -- rare -- E_v
+    // and the exact comparison for the candidates, in ascending order (one body per group
+    // of four tokens)
     float s4[4] = {0.f, 0.f, 0.f, 0.f};
-    float eb = 0.f, Eb = 1.f, yb = 0.f;
-    int jb = 0;
     const uint32_t q0 = static_cast<uint32_t>(v0) >> 2;
 #pragma unroll
-    for (int qq = 0; qq < 8; ++qq) {
-        const U4 pw = philox_row(pr, q0 + qq);
-        const uint32_t wv[4] = {pw.x, pw.y, pw.z, pw.w};
+    for (int hh = 0; hh < 2; ++hh) {
+        uint32_t wv[16];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int i = 4 * qq + j;
-            const float e = fast_exp2(y[i] - mb);
-            s4[j] += e;
-            const float E = exp_draw(wv[j]);
-            if (e * Eb > eb * E) { eb = e; Eb = E; yb = y[i]; jb = i; }
+        for (int qq = 0; qq < 4; ++qq) {
+            const U4 pw = philox_row(pr, q0 + 4 * hh + qq);
+            wv[4 * qq] = pw.x;
+            wv[4 * qq + 1] = pw.y;
+            wv[4 * qq + 2] = pw.z;
+            wv[4 * qq + 3] = pw.w;
+        }
+        uint32_t cmask = 0u;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float e = fast_exp2(y[16 * hh + i] - mref);
+            s4[i & 3] += e;
+            if (one_minus_u_shifted(wv[i]) < fmaf(e, R, kShift)) cmask |= 1u << i;   // 0 * inf = NaN: false
+        }
+        if (__any_sync(0xffffffffu, cmask != 0u)) {
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                if ((cmask >> (4 * qq)) & 0xFu) {
+                    const int g = 16 * hh + 4 * qq;
+#pragma unroll 1
+                    for (int j = 0; j < 4; ++j) {
+                        const float yj = j == 0 ? y[g] : j == 1 ? y[g + 1] : j == 2 ? y[g + 2] : y[g + 3];
+                        const uint32_t wj = j == 0 ? wv[4 * qq] : j == 1 ? wv[4 * qq + 1]
+                                                       : j == 2 ? wv[4 * qq + 2] : wv[4 * qq + 3];
+                        if ((cmask >> (4 * qq + j)) & 1u) {
+                            const float key = yj - fast_log2(exp_draw(wj));
+                            if (key > best.key) {
+                                best.key = key;
+                                best.idx = v0 + g + j;
+                                best.y = yj;
+                                R = fast_exp2(mb - key) * kSlack;
+                            }
+                        }
+                    }
+                }
+            }
         }
     }
-    best_take(best, yb - fast_log2(Eb), v0 + jb, yb);
-    lse_merge(M, S, mb, (s4[0] + s4[1]) + (s4[2] + s4[3]));
+    if (live) lse_merge(M, S, mb, (s4[0] + s4[1]) + (s4[2] + s4[3]));
 }
 
 // Grid barrier of the multi-position draft launch (cooperative launch: every CTA
@@ -290,8 +344,10 @@ constexpr int kBM = 128;              // request rows per M-tile (TMEM lanes)
 constexpr int kBN = 128;              // vocabulary columns per tile
 constexpr int kBK = 64;               // K per smem slab (128 bytes of bf16)
 constexpr int kStages = 8;            // W2 slab ring
-constexpr int kEpiWG = 2;             // epilogue warpgroups, two TMEM buffers each
+constexpr int kEpiWG = 3;             // epilogue warpgroups
+constexpr int kTmemBufs = 4;          // TMEM accumulators of kBN columns (all 512), used in rotation
 constexpr int kTcThreads = 128 * (1 + kEpiWG);
+constexpr int kPairs = (kTcThreads / 32 - 2) / 2;   // warp pairs of the residual launch's final step
 constexpr int kSlabBytes = kBN * kBK * 2;     // 16 KB
 constexpr int kASlabBytes = kBM * kBK * 2;    // 16 KB
 
@@ -425,14 +481,14 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
     uint8_t* sB = smem + 4 * kASlabBytes;                 // kStages x 16 KB
     uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kSlabBytes);
     uint64_t* empty = full + kStages;
-    uint64_t* tfull = empty + kStages;                    // [2 * kEpiWG]
-    uint64_t* tempty = tfull + 2 * kEpiWG;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2 * kEpiWG);
+    uint64_t* tfull = empty + kStages;                    // [kTmemBufs]
+    uint64_t* tempty = tfull + kTmemBufs;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + kTmemBufs);
     RowRes* rowres = reinterpret_cast<RowRes*>(tmem_slot + 4);   // [kEpiWG][128]
     int* s_prev = reinterpret_cast<int*>(rowres + kEpiWG * kBM);   // [128] x_{k-1} per request row
-    float* xch = reinterpret_cast<float*>(s_prev + kBM);          // [10] pair exchange
-    int* xchi = reinterpret_cast<int*>(xch + 10);                 // [10]
-    int* s_fail = xchi + 10;
+    float* xch = reinterpret_cast<float*>(s_prev + kBM);          // [2 kPairs] pair exchange
+    int* xchi = reinterpret_cast<int*>(xch + 2 * kPairs);         // [2 kPairs]
+    int* s_fail = xchi + 2 * kPairs;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = blockIdx.x / p.P, pc = blockIdx.x % p.P;
@@ -455,7 +511,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-        for (int e = 0; e < 2 * kEpiWG; ++e) { mbar_init(&tfull[e], 1); mbar_init(&tempty[e], 4); }
+        for (int e = 0; e < kTmemBufs; ++e) { mbar_init(&tfull[e], 1); mbar_init(&tempty[e], 4); }
         *s_fail = 0;
         fence_mbar_init();
         tc::prefetch_tmap(&tmW2);
@@ -569,10 +625,13 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                     constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN);
                     const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
                     for (int i = 0; i < ntiles && !failed; ++i) {
+                        // the position's tile i, the launch's tile gi, goes to accumulator
+                        // gi mod kTmemBufs and is reduced by warpgroup i mod kEpiWG (the same
+                        // warpgroup whichever launch runs the position, so that every path
+                        // sums in the same order)
                         const int gi = base + i;
-                        const int eg = gi % kEpiWG, use = gi / kEpiWG;
-                        const int buf = eg * 2 + (use & 1);
-                        const uint32_t par = static_cast<uint32_t>(use >> 1) & 1u;
+                        const int buf = gi % kTmemBufs;
+                        const uint32_t par = static_cast<uint32_t>(gi / kTmemBufs) & 1u;
                         if (!mbar_wait(&tempty[buf], par ^ 1u)) { failed = true; break; }
                         tc::fence_after_sync();
                         const uint32_t d = tmem_base + static_cast<uint32_t>(buf * kBN);
@@ -622,101 +681,98 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                 Best best{-INFINITY, 0x7FFFFFFF, 0.f};
                 float M = -INFINITY, S = 0.f;
                 float qb = 0.f, Eq = 1.f;                 // kResidual: the running winner's q and E
-                const int i0 = ((eg - base) % kEpiWG + kEpiWG) % kEpiWG;   // this WG's first local tile
+                const int i0 = eg;                        // this WG's tiles: eg, eg + kEpiWG, ...
 
-                uint32_t u[2][32];                        // U of the two 64-token halves of one tile
-                // 16-byte loads of tokens v0 .. v0 + 8 n - 1 (zero past V or for an idle row)
-                auto load_n = [&](const uint16_t* src, int v0, int n, uint32_t* dst) {
+                // The thread's sub-blocks of 32 tokens: four per tile (two per tile and copy when
+                // each request is held twice).  One compact loop body serves them all; the U
+                // words of the next sub-block (this tile's next, or the next tile's first) are
+                // loaded one sub-block ahead, so the load has a sub-block's work to land.
+                const int nsub = (R == 1) ? 4 : 2;
+                const int soff = (R == 1) ? 0 : copy * 64;   // token offset of the first sub-block in a tile
+                auto load16 = [&](const uint16_t* src, int v0, uint32_t* dst) {
 #pragma unroll
-                    for (int g8 = 0; g8 < 8; ++g8) {
-                        if (g8 >= n) break;
+                    for (int g8 = 0; g8 < 4; ++g8) {
                         if (valid && v0 + g8 * 8 < p.V) ld_u32x4(src + v0 + g8 * 8, dst + g8 * 4, pol);
                         else { dst[g8 * 4] = dst[g8 * 4 + 1] = dst[g8 * 4 + 2] = dst[g8 * 4 + 3] = 0u; }
                     }
                 };
-                auto load_blk = [&](const uint16_t* src, int t, int hb, uint32_t* dst) {
-                    load_n(src, t * kBN + hb * 64, 8, dst);
-                };
-                auto mine = [&](int hb) -> bool { return R == 1 || hb == copy; };
-                if (kMode == kDraft && i0 < ntiles && warp_live) {
-                    if (mine(0)) load_blk(urow, t_lo + i0, 0, u[0]);
-                    if (mine(1)) load_blk(urow, t_lo + i0, 1, u[1]);
-                }
+                uint32_t un[16];                          // U words of the next sub-block (kDraft)
+                if (kMode == kDraft && i0 < ntiles) load16(urow, (t_lo + i0) * kBN + soff, un);
                 for (int i = i0; i < ntiles; i += kEpiWG) {
                     const int t = t_lo + i;
-                    const int use = (base + i) / kEpiWG;
-                    const int buf = eg * 2 + (use & 1);
-                    const uint32_t par = static_cast<uint32_t>(use >> 1) & 1u;
+                    const int buf = (base + i) % kTmemBufs;
+                    const uint32_t par = static_cast<uint32_t>((base + i) / kTmemBufs) & 1u;
                     bool bad = false;
                     if (!failed) bad = !mbar_wait(&tfull[buf], par);
+                    // warp-uniform: the draw's warp votes need every lane on the same path
+                    bad = __any_sync(0xffffffffu, bad);
                     if (bad) { failed = true; set_status(st, DSPARK_ERR_TIMEOUT, 12); }
                     tc::fence_after_sync();
                     const bool have_next = (i + kEpiWG < ntiles);
                     const int tnext = t + kEpiWG;
-#pragma unroll
-                    for (int hb = 0; hb < 2; ++hb) {
-                        const int vh = t * kBN + hb * 64;
-                        if (!mine(hb) || !warp_live || failed || vh >= p.V) continue;   // warp-uniform
-                        uint32_t tt[32];
-                        if constexpr (kMode == kResidual) {
-                            load_blk(urow, t, hb, u[hb]);
-                            load_blk(trow, t, hb, tt);
+#pragma unroll 1
+                    for (int j = 0; j < nsub; ++j) {
+                        const int off = soff + 32 * j;
+                        const int v0 = t * kBN + off;
+                        // the next sub-block's U (this tile's next, or the next tile's first)
+                        const int vn = (j + 1 < nsub) ? v0 + 32 : (have_next ? tnext * kBN + soff : -1);
+                        if (!warp_live || failed || v0 >= p.V) {  // warp-uniform
+                            if (kMode == kDraft && vn >= 0) load16(urow, vn, un);
+                            continue;
                         }
+                        uint32_t tt[16];
+                        if constexpr (kMode == kResidual) {
+                            load16(urow, v0, un);
+                            load16(trow, v0, tt);
+                        }
+                        float y[32];
+                        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kBN + off;
+                        tc::tmem_ld32(taddr, y);
+                        tc::tmem_ld_wait();
 #pragma unroll
-                        for (int sb = 0; sb < 2; ++sb) {  // two 32-token sub-blocks of the half
-                            const int v0 = vh + sb * 32;
-                            float y[32];
-                            const uint32_t taddr =
-                                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kBN + hb * 64 + sb * 32;
-                            tc::tmem_ld32(taddr, y);
-                            tc::tmem_ld_wait();
-                            const uint32_t* uh = u[hb] + sb * 16;
+                        for (int w = 0; w < 16; ++w) {
+                            y[2 * w] = (y[2 * w] + bf16lo(un[w])) * p.cscale;
+                            y[2 * w + 1] = (y[2 * w + 1] + bf16hi(un[w])) * p.cscale;
+                        }
+                        // this sub-block's U words are consumed: fetch the next one's, in flight
+                        // while this sub-block is reduced
+                        if (kMode == kDraft && vn >= 0) load16(urow, vn, un);
+                        if (v0 + 32 > p.V) {
 #pragma unroll
-                            for (int w = 0; w < 16; ++w) {
-                                y[2 * w] = (y[2 * w] + bf16lo(uh[w])) * p.cscale;
-                                y[2 * w + 1] = (y[2 * w + 1] + bf16hi(uh[w])) * p.cscale;
+                            for (int w = 0; w < 32; ++w)
+                                if (v0 + w >= p.V) y[w] = -INFINITY;
+                        }
+                        if constexpr (kMode == kDraft) {
+                            if (p.debug_z != nullptr) {
+                                if (valid)                // copies own disjoint halves
+                                    for (int w = 0; w < 32; ++w)
+                                        if (v0 + w < p.V) p.debug_z[static_cast<size_t>(b) * p.V + v0 + w] = y[w];
+                                continue;
                             }
-                            // this sub-block's U words are consumed: fetch the next tile's
-                            // (in flight while this sub-block is reduced)
-                            if (kMode == kDraft && have_next) load_n(urow, tnext * kBN + hb * 64 + sb * 32, 4, u[hb] + sb * 16);
-                            if (v0 + 32 > p.V) {
+                            if (p.greedy) {
 #pragma unroll
                                 for (int w = 0; w < 32; ++w)
-                                    if (v0 + w >= p.V) y[w] = -INFINITY;
-                            }
-                            if constexpr (kMode == kDraft) {
-                                if (p.debug_z != nullptr) {
-                                    if (valid)            // copies own disjoint halves
-                                        for (int w = 0; w < 32; ++w)
-                                            if (v0 + w < p.V) p.debug_z[static_cast<size_t>(b) * p.V + v0 + w] = y[w];
-                                    continue;
-                                }
-                                if (p.greedy) {
-#pragma unroll
-                                    for (int w = 0; w < 32; ++w)
-                                        if (y[w] > best.key) { best.key = y[w]; best.idx = v0 + w; }
-                                } else {
-                                    draw32(y, v0, prow, best, M, S);
-                                }
+                                    if (y[w] > best.key) { best.key = y[w]; best.idx = v0 + w; }
                             } else {
-                                // residual q = max(0, p_t - p_d), p_d = 2^(y - ld2), p_t = 2^(t c - lt2);
-                                // the winner maximises q_v / E_v over the thread's tokens
-                                const uint32_t* th = tt + sb * 16;
-                                const uint32_t qbase = static_cast<uint32_t>(v0) >> 2;
+                                draw32(y, v0, prow, best, M, S);
+                            }
+                        } else {
+                            // residual q = max(0, p_t - p_d), p_d = 2^(y - ld2), p_t = 2^(t c - lt2);
+                            // the winner maximises q_v / E_v over the thread's tokens
+                            const uint32_t qbase = static_cast<uint32_t>(v0) >> 2;
 #pragma unroll
-                                for (int qq = 0; qq < 8; ++qq) {
-                                    const U4 pw = philox_row(prow, qbase + qq);
-                                    const uint32_t wv[4] = {pw.x, pw.y, pw.z, pw.w};
+                            for (int qq = 0; qq < 8; ++qq) {
+                                const U4 pw = philox_row(prow, qbase + qq);
+                                const uint32_t wv[4] = {pw.x, pw.y, pw.z, pw.w};
 #pragma unroll
-                                    for (int j = 0; j < 4; ++j) {
-                                        const int w = 4 * qq + j;
-                                        const float tv = (w & 1) ? bf16hi(th[w >> 1]) : bf16lo(th[w >> 1]);
-                                        const float pd = fast_exp2(y[w] - ld2);
-                                        const float ptv = fast_exp2(tv * p.cscale - lt2);
-                                        const float qv = (v0 + w < p.V) ? fmaxf(ptv - pd, 0.f) : 0.f;
-                                        const float E = exp_draw(wv[j]);
-                                        if (qv * Eq > qb * E) { qb = qv; Eq = E; best.idx = v0 + w; }
-                                    }
+                                for (int jj = 0; jj < 4; ++jj) {
+                                    const int w = 4 * qq + jj;
+                                    const float tv = (w & 1) ? bf16hi(tt[w >> 1]) : bf16lo(tt[w >> 1]);
+                                    const float pd = fast_exp2(y[w] - ld2);
+                                    const float ptv = fast_exp2(tv * p.cscale - lt2);
+                                    const float qv = (v0 + w < p.V) ? fmaxf(ptv - pd, 0.f) : 0.f;
+                                    const float E = exp_draw(wv[jj]);
+                                    if (qv * Eq > qb * E) { qb = qv; Eq = E; best.idx = v0 + w; }
                                 }
                             }
                         }
@@ -729,13 +785,12 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                 // the next position's first U tile of this lane does not depend on x_k:
                 // bring it into L2 while the grid hands over
                 if (kMode == kDraft && k < k1 && valid && warp_live) {
-                    const int inext = ((eg - (base + ntiles)) % kEpiWG + kEpiWG) % kEpiWG;
+                    const int inext = eg;                 // its first tile of the next position
                     if (inext < ntiles) {
-                        const uint16_t* un = p.U + (static_cast<size_t>(b) * p.gamma + k) * p.V;
-#pragma unroll
-                        for (int hb = 0; hb < 2; ++hb) {
-                            const int v0 = (t_lo + inext) * kBN + hb * 64;
-                            if (mine(hb) && v0 < p.V) prefetch_l2(un + v0);
+                        const uint16_t* unx = p.U + (static_cast<size_t>(b) * p.gamma + k) * p.V;
+                        for (int off = soff; off < soff + 32 * nsub; off += 64) {
+                            const int v0 = (t_lo + inext) * kBN + off;
+                            if (v0 < p.V) prefetch_l2(unx + v0);
                         }
                     }
                 }
@@ -778,7 +833,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
             wait_all();                                   // every CTA published its residual winners
             if (warp >= 2 && *s_fail == 0) {
                 const int pair = (warp - 2) >> 1;
-                for (int b = blockIdx.x + pair * gridDim.x; b < p.B; b += 5 * gridDim.x)
+                for (int b = blockIdx.x + pair * gridDim.x; b < p.B; b += kPairs * gridDim.x)
                     finish_pair<true>(p.fin, b, p.gamma, p.V, p.cscale, p.seed, st, 2 + pair, xch + 2 * pair,
                                       xchi + 2 * pair);
             }
@@ -821,8 +876,8 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
     }
 }
 
-constexpr size_t kTcSmem = 1024 + 4 * kASlabBytes + kStages * kSlabBytes + (2 * kStages + 4 * kEpiWG) * 8 + 16 +
-                           kEpiWG * kBM * sizeof(RowRes) + kBM * 4 + 10 * 4 + 10 * 4 + 16;
+constexpr size_t kTcSmem = 1024 + 4 * kASlabBytes + kStages * kSlabBytes + (2 * kStages + 2 * kTmemBufs) * 8 + 16 +
+                           kEpiWG * kBM * sizeof(RowRes) + kBM * 4 + 2 * kPairs * 4 + 2 * kPairs * 4 + 16;
 
 // ------------------------------------------------------------ host side ---
 inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {

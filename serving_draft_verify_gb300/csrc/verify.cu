@@ -369,18 +369,31 @@ verify_rows(int gamma, int V, const void* __restrict__ t, const int32_t* __restr
                     // the row's Philox constants, formed per step (cheaper than holding them in registers)
                     const PhiloxRow pr = philox_row_setup(seed, static_cast<uint32_t>(k), static_cast<uint32_t>(b),
                                                           kStreamVerifyToken);
+                    // token v beats the lane's best iff y_v c - log2 E_v > best; E_v >= s_v = 1 - u_v,
+                    // so only tokens with s_v < 2^(y_v c - best) (raised by 2^-10 for rounding) can,
+                    // and only those take E_v (a warp enters when any lane has one).  -inf past V
+                    // gives 2^-inf = 0: never a candidate.
+                    constexpr float kSlack = 1.0009765625f;
 #pragma unroll
                     for (int u = 0; u < kU; ++u) {
                         const int v = ((q0 + u) * 4 + sub) * 64 + part * 8;
-                        if (v >= V) continue;
+                        uint32_t wv[8];
+                        uint32_t cmask = 0u;
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             const U4 pw = philox_row(pr, (static_cast<uint32_t>(v) >> 2) + h);
-                            const uint32_t wv[4] = {pw.x, pw.y, pw.z, pw.w};
+                            wv[4 * h] = pw.x; wv[4 * h + 1] = pw.y; wv[4 * h + 2] = pw.z; wv[4 * h + 3] = pw.w;
+                        }
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float key = y[u][4 * h + i] * cscale - fast_log2(exp_draw(wv[i]));
-                                if (key > best) { best = key; best_i = v + 4 * h + i; }   // -inf past V never wins
+                        for (int i = 0; i < 8; ++i)
+                            if (eng::one_minus_u(wv[i]) < fast_exp2(y[u][i] * cscale - best) * kSlack) cmask |= 1u << i;
+                        if (__any_sync(0xffffffffu, cmask != 0u)) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                if ((cmask >> i) & 1u) {
+                                    const float key = y[u][i] * cscale - fast_log2(exp_draw(wv[i]));
+                                    if (key > best) { best = key; best_i = v + i; }
+                                }
                             }
                         }
                     }
