@@ -146,35 +146,60 @@ __device__ __forceinline__ float one_minus_u_shifted(uint32_t w) {
     return __uint_as_float(((~w) >> 9) | 0x3F800000u);
 }
 
+// Two float32 lanes in one 64-bit register (Blackwell f32x2 arithmetic); each lane
+// of an f32x2 operation is rounded once, exactly as its float32 counterpart.
+__device__ __forceinline__ unsigned long long f2pack(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(unsigned long long v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f2add(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f2fma(unsigned long long a, unsigned long long b,
+                                                    unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 // The flat Gumbel-max draw over 32 consecutive tokens v0 .. v0+31 (v0 a
-// multiple of 4) with log2-weights y (-inf: no mass), and their (max, sum).
+// multiple of 4), given their raw logits s (-inf: no mass) and the scale c > 0
+// (y = s c in log2 units), and their (max, sum) of 2^y.
 // Token v beats the running best iff y_v - log2 E_v > best.key, i.e. iff
-// E_v < 2^(y_v - best.key) = e_v R with e_v = 2^(y_v - m) (formed for the
-// sum anyway) and R = 2^(m - best.key).  Since E_v >= s_v = 1 - u_v, a token
-// with s_v >= e_v R (R raised by 2^-10 to cover the rounding of e_v, R and E_v)
+// E_v < 2^(y_v - best.key) = e_v R with e_v = 2^(y_v - m) (formed for the sum
+// anyway) and R = 2^(m - best.key).  Since E_v >= s_v = 1 - u_v, a token with
+// s_v >= e_v R (R raised by 2^-10 to cover the rounding of e_v, R and E_v)
 // cannot win, and only the rare others (a warp enters the branch when any lane
 // has one) take E_v and the exact comparison of keys.  Tokens are visited in
 // ascending order and a key must be strictly larger to win: ties keep the
 // lowest index.  `pr` holds the row's Philox constants; word v & 3 of block
 // v >> 2 keys index v.
-__device__ __forceinline__ void draw32(const float* y, int v0, const PhiloxRow& pr, Best& best, float& M,
+__device__ __forceinline__ void draw32(const float* s, float c, int v0, const PhiloxRow& pr, Best& best, float& M,
                                        float& S) {
-    float m4[4] = {y[0], y[1], y[2], y[3]};
+    float m4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-    for (int w = 4; w < 32; ++w) m4[w & 3] = fmaxf(m4[w & 3], y[w]);
-    const float mb = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-    const bool live = mb > -INFINITY;                     // no finite logit: no mass, no candidate
+    for (int w = 4; w < 32; ++w) m4[w & 3] = fmaxf(m4[w & 3], s[w]);
+    const float mraw = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+    const bool live = mraw > -INFINITY;                   // no finite logit: no mass, no candidate
+    const float mb = mraw * c;                            // the sub-block's max of y
     const float mref = live ? mb : 0.f;
     constexpr float kSlack = 1.0009765625f;               // 1 + 2^-10
     // s_v < e_v R  <=>  f_v < e_v R + (1 - 2^-24); 2^-23 more covers the rounding of that sum
     constexpr float kShift = 0.999999940395355225f + 1.1920928955078125e-07f;
-    float R = live ? fast_exp2(mb - best.key) * kSlack : 0.f;   // +inf while nothing is drawn yet
-    // per half of 16 tokens: its four Philox blocks first (independent chains the scheduler
-    // can overlap), then the sum and the candidates (a bit per token), then -- rare -- E_v
-    // and the exact comparison for the candidates, in ascending order (one body per group
-    // of four tokens)
-    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+    const float R = live ? fast_exp2(mb - best.key) * kSlack : 0.f;   // +inf while nothing is drawn yet
+    const unsigned long long c2 = f2pack(c, c), nm2 = f2pack(-mref, -mref);
+    unsigned long long sum2 = f2pack(0.f, 0.f);
     const uint32_t q0 = static_cast<uint32_t>(v0) >> 2;
+    // per half of 16 tokens: its four Philox blocks first (independent chains the scheduler
+    // can overlap), then the sum (e = 2^(s c - m), two tokens per f32x2 operation) and the
+    // candidates (a bit per token), then -- rare -- E_v and the exact comparison for the
+    // candidates, in ascending order
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
         uint32_t wv[16];
@@ -188,10 +213,13 @@ __device__ __forceinline__ void draw32(const float* y, int v0, const PhiloxRow& 
         }
         uint32_t cmask = 0u;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float e = fast_exp2(y[16 * hh + i] - mref);
-            s4[i & 3] += e;
-            if (one_minus_u_shifted(wv[i]) < fmaf(e, R, kShift)) cmask |= 1u << i;   // 0 * inf = NaN: false
+        for (int i = 0; i < 16; i += 2) {
+            float a0, a1;
+            f2unpack(f2fma(f2pack(s[16 * hh + i], s[16 * hh + i + 1]), c2, nm2), a0, a1);
+            const float e0 = fast_exp2(a0), e1 = fast_exp2(a1);
+            sum2 = f2add(sum2, f2pack(e0, e1));
+            if (one_minus_u_shifted(wv[i]) < fmaf(e0, R, kShift)) cmask |= 1u << i;       // 0 * inf = NaN: false
+            if (one_minus_u_shifted(wv[i + 1]) < fmaf(e1, R, kShift)) cmask |= 2u << i;
         }
         if (__any_sync(0xffffffffu, cmask != 0u)) {
 #pragma unroll
@@ -200,16 +228,16 @@ __device__ __forceinline__ void draw32(const float* y, int v0, const PhiloxRow& 
                     const int g = 16 * hh + 4 * qq;
 #pragma unroll 1
                     for (int j = 0; j < 4; ++j) {
-                        const float yj = j == 0 ? y[g] : j == 1 ? y[g + 1] : j == 2 ? y[g + 2] : y[g + 3];
+                        const float sj = j == 0 ? s[g] : j == 1 ? s[g + 1] : j == 2 ? s[g + 2] : s[g + 3];
                         const uint32_t wj = j == 0 ? wv[4 * qq] : j == 1 ? wv[4 * qq + 1]
                                                        : j == 2 ? wv[4 * qq + 2] : wv[4 * qq + 3];
                         if ((cmask >> (4 * qq + j)) & 1u) {
+                            const float yj = sj * c;
                             const float key = yj - fast_log2(exp_draw(wj));
                             if (key > best.key) {
                                 best.key = key;
                                 best.idx = v0 + g + j;
                                 best.y = yj;
-                                R = fast_exp2(mb - key) * kSlack;
                             }
                         }
                     }
@@ -217,7 +245,9 @@ __device__ __forceinline__ void draw32(const float* y, int v0, const PhiloxRow& 
             }
         }
     }
-    if (live) lse_merge(M, S, mb, (s4[0] + s4[1]) + (s4[2] + s4[3]));
+    float sl, sh;
+    f2unpack(sum2, sl, sh);
+    if (live) lse_merge(M, S, mb, sl + sh);
 }
 
 // Grid barrier of the multi-position draft launch (cooperative launch: every CTA
@@ -398,6 +428,8 @@ struct TcParams {
     const uint16_t* T;               // t_logits [B][gamma+1][V]
     const float* lt2;                // [B] log2-sum-exp2 of t / T at row k_b (log2 units)
     const float* ld2;                // [B] lse_d[b][k_b-1] * log2e
+    const int32_t* rej_list;         // [B] the rejected requests (first *rej_count entries, any order)
+    const int32_t* rej_count;        // [1]
 };
 
 struct RowRes {
@@ -491,19 +523,30 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
     int* s_fail = xchi + 2 * kPairs;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = blockIdx.x / p.P, pc = blockIdx.x % p.P;
-    const int m0 = g * kBM;
+    // The rows of the launch: every request (kDraft), or the rejected ones, listed on
+    // the device by verification's rows pass (kResidual): nact of them, rows
+    // compacted so that the whole grid works on the M-tiles that exist.
+    const int nact = (kMode == kResidual) ? min(max(__ldcg(p.rej_count), 0), p.B) : p.B;
+    // Row replication: with at most 64 rows the A tile holds every row twice (TMEM
+    // lanes 0-63 and 64-127) and the two copies reduce different 64-token halves of
+    // each tile, so all epilogue warps have work.
+    const int R = (nact <= 64) ? 2 : 1;
+    const int rpc = kBM / R;                              // request rows per copy
+    const int nM = max(1, (nact + kBM - 1) / kBM);        // M-tiles (one when R = 2)
     const int NT = (p.V + kBN - 1) / kBN;
-    const int t_lo = static_cast<int>(static_cast<long long>(pc) * NT / p.P);
-    const int t_hi = static_cast<int>(static_cast<long long>(pc + 1) * NT / p.P);
+    // CTAs per M-tile: the host's P for the draft; for the residual, as many as the
+    // grid gives each existing M-tile (CTAs past them stay idle)
+    const int P = (kMode == kResidual) ? max(1, min(static_cast<int>(gridDim.x) / nM, NT)) : p.P;
+    const int g = blockIdx.x / P, pc = blockIdx.x % P;
+    const int m0 = g * kBM;
+    const bool idle = g >= nM;
+    const int t_lo = idle ? 0 : static_cast<int>(static_cast<long long>(pc) * NT / P);
+    const int t_hi = idle ? 0 : static_cast<int>(static_cast<long long>(pc + 1) * NT / P);
     const int ntiles = t_hi - t_lo;
     StatusBlock* st = p.ws.status;
-    // Row replication: with at most 64 requests the A tile holds every request
-    // twice (TMEM lanes 0-63 and 64-127) and the two copies reduce different
-    // 64-token halves of each tile, so all epilogue warps have work.
-    const int R = (p.B <= 64) ? 2 : 1;
-    const int rpc = kBM / R;                              // request rows per copy
-    const int nrows = min(rpc, p.B - m0);                 // requests of this M-tile
+    const int nrows = idle ? 0 : max(0, min(rpc, nact - m0));   // rows of this M-tile
+    // the request behind row m0 + rr
+    auto req = [&](int rr) -> int { return (kMode == kResidual) ? __ldcg(p.rej_list + m0 + rr) : m0 + rr; };
     const int k0 = p.k;
     const int k1 = (kMode == kDraft && p.k_last > p.k) ? p.k_last : p.k;
     const bool multi = k1 > k0;                           // positions k0..k1, grid barriers between
@@ -579,14 +622,14 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
             if (kMode == kDraft && multi && k > k0) {
                 wait_all();                               // every CTA published position k-1
                 for (int rr = ptid; rr < nrows; rr += kPro) {
-                    const int b = m0 + rr;
+                    const int b = req(rr);
                     const int tok = (*s_fail == 0) ? winner(b, k - 1) : 0;
                     s_prev[rr] = tok;
                     if (pc == 0) p.x[b * p.gamma + k - 2] = tok;
                 }
             } else {
                 for (int rr = ptid; rr < nrows; rr += kPro) {
-                    const int b = m0 + rr;
+                    const int b = req(rr);
                     const int kb = row_k(b, k);
                     s_prev[rr] = (kb > 0) ? prev_token(p.x0, p.x, b, p.gamma, kb, p.V, st) : -1;
                 }
@@ -605,7 +648,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                         const int slab = lane >> 3, c = lane & 7;
                         uint8_t* dst = sA + slab * kASlabBytes + (row >> 3) * 1024 + (row & 7) * 128 + ((c ^ (row & 7)) << 4);
                         if (prev >= 0) {
-                            const uint16_t* src = p.E ? p.E + (static_cast<size_t>(m0 + rr) * p.gamma + (row_k(m0 + rr, k) - 1)) * p.r
+                            const uint16_t* src = p.E ? p.E + (static_cast<size_t>(req(rr)) * p.gamma + (row_k(req(rr), k) - 1)) * p.r
                                                       : p.W1 + static_cast<size_t>(prev) * p.r;
                             cp_async16(dst, src + lane * 8);
                         }
@@ -659,7 +702,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                 const int lrow = q * 32 + lane;           // TMEM lane = A row
                 const int copy = lrow / rpc;              // which copy of the request rows
                 const int rr = lrow % rpc;                // request row within the M-tile
-                const int b = m0 + rr;
+                const int b = (rr < nrows) ? req(rr) : 0;
                 const int kb = (rr < nrows) ? row_k(b, k) : 0;
                 const bool valid = rr < nrows && kb > 0;
                 const bool warp_live = ((q * 32) % rpc) < nrows;
@@ -729,11 +772,11 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kBN + off;
                         tc::tmem_ld32(taddr, y);
                         tc::tmem_ld_wait();
+                        // raw logits z = acc + U (two tokens per f32x2 add); the draw scales by cscale
 #pragma unroll
-                        for (int w = 0; w < 16; ++w) {
-                            y[2 * w] = (y[2 * w] + bf16lo(un[w])) * p.cscale;
-                            y[2 * w + 1] = (y[2 * w + 1] + bf16hi(un[w])) * p.cscale;
-                        }
+                        for (int w = 0; w < 16; ++w)
+                            f2unpack(f2add(f2pack(y[2 * w], y[2 * w + 1]), f2pack(bf16lo(un[w]), bf16hi(un[w]))),
+                                     y[2 * w], y[2 * w + 1]);
                         // this sub-block's U words are consumed: fetch the next one's, in flight
                         // while this sub-block is reduced
                         if (kMode == kDraft && vn >= 0) load16(urow, vn, un);
@@ -746,15 +789,15 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                             if (p.debug_z != nullptr) {
                                 if (valid)                // copies own disjoint halves
                                     for (int w = 0; w < 32; ++w)
-                                        if (v0 + w < p.V) p.debug_z[static_cast<size_t>(b) * p.V + v0 + w] = y[w];
+                                        if (v0 + w < p.V) p.debug_z[static_cast<size_t>(b) * p.V + v0 + w] = y[w] * p.cscale;
                                 continue;
                             }
-                            if (p.greedy) {
+                            if (p.greedy) {                // cscale = 1
 #pragma unroll
                                 for (int w = 0; w < 32; ++w)
                                     if (y[w] > best.key) { best.key = y[w]; best.idx = v0 + w; }
                             } else {
-                                draw32(y, v0, prow, best, M, S);
+                                draw32(y, p.cscale, v0, prow, best, M, S);
                             }
                         } else {
                             // residual q = max(0, p_t - p_d), p_d = 2^(y - ld2), p_t = 2^(t c - lt2);
@@ -768,7 +811,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                                 for (int jj = 0; jj < 4; ++jj) {
                                     const int w = 4 * qq + jj;
                                     const float tv = (w & 1) ? bf16hi(tt[w >> 1]) : bf16lo(tt[w >> 1]);
-                                    const float pd = fast_exp2(y[w] - ld2);
+                                    const float pd = fast_exp2(fmaf(y[w], p.cscale, -ld2));
                                     const float ptv = fast_exp2(tv * p.cscale - lt2);
                                     const float qv = (v0 + w < p.V) ? fmaxf(ptv - pd, 0.f) : 0.f;
                                     const float E = exp_draw(wv[jj]);
@@ -801,7 +844,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
             // --------------------------------------- publish this position
             if (warp >= 4 && warp < 8 && p.debug_z == nullptr) {
                 const int rr = (warp - 4) * 32 + lane;
-                const int b = m0 + rr;
+                const int b = (rr < nrows) ? req(rr) : 0;
                 if (rr < nrows && row_k(b, k) > 0) {
                     Best b0{-INFINITY, 0x7FFFFFFF, 0.f};
                     float m = -INFINITY, s = 0.f;
@@ -853,7 +896,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
             for (int item = warp - 1; item < nown * p.gamma; item += kPro / 32) {
                 const int b = cta + (item / p.gamma) * ncta, k = item % p.gamma + 1;
                 finalize_position<true>(b, k, p.B, p.gamma, p.V, p.H, p.r, p.h, p.W1, p.w, p.bias, p.x0, p.x,
-                                        p.greedy, p.P, kBN, NT, p.ws.part, p.ws.ybest, p.lse_d, p.logp_d, p.c, st);
+                                        p.greedy, P, kBN, NT, p.ws.part, p.ws.ybest, p.lse_d, p.logp_d, p.c, st);
             }
             pro_sync();
             for (int j = ptid; j < nown; j += kPro) {     // survival a_k = prod c_1..c_k, in k order

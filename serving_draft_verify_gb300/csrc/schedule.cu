@@ -3,19 +3,24 @@
 // survival a_{b,j} descending, scan them greedily while
 // Theta = (E / N) * SPS(N) rises, stop at the first pair that does not raise it.
 //
-// One CTA of 1024 threads, everything in shared memory (B * gamma <= 16384):
+// schedule_sort, one CTA of 1024 threads, everything in shared memory
+// (B * gamma <= 16384):
 //   1. keys k = ~bits(a) (ascending k = descending a), values = pair index
 //      b * gamma + j - 1, padded with k = ~0 to a multiple of 1024;
 //   2. stable LSD radix sort, four 8-bit passes; within a warp, equal digits
-//      are ranked with __match_any_sync, so ties keep (b, j) order;
+//      are ranked with __match_any_sync, so ties keep (b, j) order (up to 1024
+//      pairs: a stable rank by counting instead);
 //   3. exact prefix sums of a * 2^149 (each float32 a in [0, 1] is an integer
-//      below 2^150 at that scale) in 192-bit integers, plus B * 2^149; each
-//      thread owns ceil(n / 1024) consecutive sorted positions;
-//   4. E_n = the prefix rounded once to double (round-to-nearest-even),
-//      Theta_n = (E_n / (B + n)) * sps[B + n] with IEEE double ops, every n
-//      in parallel (the SPS entries are loaded up front);
-//   5. n* = (first n with !(Theta_n > Theta_{n-1})) - 1, block-wide min;
-//   6. l*_b = number of pairs of request b among the first n* sorted pairs.
+//      below 2^150 at that scale) in 192-bit integers, plus B * 2^149;
+//   4. E_m = the prefix of the first m sorted pairs rounded once to double
+//      (round-to-nearest-even, assembled from its bits: no floating-point
+//      arithmetic), and the request of every sorted pair, to the workspace.
+// schedule_theta, a grid over the pairs:
+//   5. Theta_m = (E_m / (B + m)) * sps[B + m] with IEEE double ops, every m in
+//      parallel, and the first m with !(Theta_m > Theta_{m-1}) (atomicMin);
+//   6. the CTA that finishes last: n* (the pairs before that first drop),
+//      Theta_best = Theta_{n*}, N = B + n*, and l*_b = the number of pairs of
+//      request b among the first n* sorted pairs.
 #include "common.cuh"
 #include "host_common.h"
 
@@ -61,7 +66,9 @@ __device__ __forceinline__ U192 scaled_survival(uint32_t bits) {
     }
     return r;
 }
-// round(v) to double (nearest, ties to even), times 2^-149.  v > 0 here.
+// round(v) to double (nearest, ties to even), times 2^-149, assembled from its
+// bits (an exponent field and a 52-bit fraction).  Here v >= B 2^149 >= 2^149,
+// so the result is a normal double >= 1.
 __device__ __forceinline__ double u192_to_double_scaled(U192 v) {
     int hb;   // index of the highest set bit
     if (v.w2) hb = 191 - __clzll(v.w2);
@@ -81,14 +88,36 @@ __device__ __forceinline__ double u192_to_double_scaled(U192 v) {
     unsigned long long mant = a2 >> 11;                 // 53 bits, top bit set
     const bool round = (a2 >> 10) & 1ull;
     const bool sticky = (a2 & 0x3FFull) != 0 || a1 != 0 || a0 != 0;
-    if (round && (sticky || (mant & 1ull))) mant += 1;   // 2^53 is still exact
-    return scalbn(static_cast<double>(mant), hb - 52 - 149);
+    if (round && (sticky || (mant & 1ull))) mant += 1;
+    int e = hb - 149;                                   // value = mant 2^(e - 52)
+    if (mant >> 53) { mant >>= 1; e += 1; }             // the rounding carried into bit 53
+    const unsigned long long bits =
+        (static_cast<unsigned long long>(e + 1023) << 52) | (mant & 0xFFFFFFFFFFFFFull);
+    return __longlong_as_double(static_cast<long long>(bits));
+}
+
+// The scheduler's scratch: the first-drop word and the done counter of
+// schedule_theta, E_m for m = 0..n (double) and the request of each sorted pair.
+struct SchedWs {
+    int32_t* first_fail;
+    uint32_t* done;
+    double* Ed;                  // [n + 1]
+    int32_t* req;                // [n]
+};
+inline size_t sched_ws_layout(int n, size_t* o_ctl, size_t* o_ed, size_t* o_req) {
+    size_t o = kStatusBytes;
+    *o_ctl = o;
+    o += 256;
+    *o_ed = o;
+    o += round_up(static_cast<size_t>(n + 1) * 8, 256);
+    *o_req = o;
+    o += round_up(static_cast<size_t>(n) * 4, 256);
+    return o;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-schedule_kernel(const float* __restrict__ a, const double* __restrict__ sps, int B, int gamma,
-                int32_t* __restrict__ ell, int32_t* __restrict__ n_sched, double* __restrict__ theta,
-                StatusBlock* status) {
+schedule_sort(const float* __restrict__ a, int B, int gamma, int32_t* __restrict__ ell, StatusBlock* status,
+              SchedWs ws) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = B * gamma;
@@ -261,72 +290,70 @@ schedule_kernel(const float* __restrict__ a, const double* __restrict__ sps, int
         if (lane >= 1) excl = add192(excl, y);
     }
 
-    // 4-5. Theta_m for every m, each thread for its own positions, and the
-    //      first m with !(Theta_m > Theta_{m-1}); Theta_{p0} (the comparison
-    //      of a thread's first position) comes from the thread before it.
-    auto theta_at = [&](int m, U192 E, double sps_n) -> double {   // m pairs taken; E = scaled sum + B
-        const double Ed = u192_to_double_scaled(E);
-        return __dmul_rn(__ddiv_rn(Ed, static_cast<double>(B + m)), sps_n);
-    };
-    const bool active = p0 < n;
-    int first_fail = 0x7FFFFFFF;
-    double th_first = 0.0, th_last = 0.0, fail_prev = 0.0;
-    if (active) {
+    // 4. E_m for the thread's positions (m = p0 + q + 1 pairs taken), E_0 = B, the
+    //    request of each sorted pair; ell cleared for schedule_theta's counts
+    if (p0 < n) {
         U192 run = excl;
-        double prev = 0.0;
-        for (int q0 = 0; q0 < PT; q0 += 4) {
-            double sp[4];                             // four SPS loads in flight at once
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int m = p0 + q0 + u + 1;
-                sp[u] = (q0 + u < PT && m <= n) ? sps[B + m] : 0.0;
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int q = q0 + u, m = p0 + q + 1;
-                if (q < PT && m <= n) {
-                    run = add192(run, scaled_survival(~skey[m - 1]));
-                    const double th = theta_at(m, run, sp[u]);
-                    if (q == 0) th_first = th;
-                    else if (first_fail == 0x7FFFFFFF && !(th > prev)) { first_fail = m; fail_prev = prev; }
-                    prev = th;
-                    th_last = th;
-                }
-            }
+        for (int q = 0; q < PT && p0 + q < n; ++q) {
+            const int m = p0 + q + 1;
+            run = add192(run, scaled_survival(~skey[m - 1]));
+            ws.Ed[m] = u192_to_double_scaled(run);
+            ws.req[m - 1] = sval[m - 1] / gamma;
         }
     }
-    __shared__ double wlast[kWarps];
-    double before = __shfl_up_sync(0xffffffffu, th_last, 1);   // Theta_{p0} from the thread before
-    if (lane == 31) wlast[warp] = th_last;
-    __syncthreads();
-    if (lane == 0 && warp > 0) before = wlast[warp - 1];
-    if (tid == 0) before = theta_at(0, excl, sps[B]);           // Theta_0: every request at its bonus row
-    if (active && !(th_first > before)) { first_fail = p0 + 1; fail_prev = before; }
-    int fmin = first_fail;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) fmin = min(fmin, __shfl_xor_sync(0xffffffffu, fmin, o));
-    if (lane == 0) red_min[warp] = fmin;
-    __syncthreads();
-    int nfail = 0x7FFFFFFF;
-    for (int q = 0; q < kWarps; ++q) nfail = min(nfail, red_min[q]);
-    const int nstar = (nfail == 0x7FFFFFFF) ? n : nfail - 1;
-    // Theta_{n*}: the failing comparison's left side, or the last Theta
-    if (nfail != 0x7FFFFFFF && first_fail == nfail) {
-        *theta = fail_prev;
-        *n_sched = B + nstar;
+    if (tid == 0) {
+        ws.Ed[0] = static_cast<double>(B);
+        *ws.first_fail = 0x7FFFFFFF;
+        *ws.done = 0u;
     }
-    if (nfail == 0x7FFFFFFF && active && p0 + PT >= n) {
-        *theta = th_last;
-        *n_sched = B + nstar;
-    }
+    for (int b = tid; b < B; b += kThreads) ell[b] = 0;
+}
 
-    // 6. per-request counts among the first n* sorted pairs (reuse key[src ^ 1])
-    int* cnt = reinterpret_cast<int*>(key[src ^ 1]);
-    for (int b = tid; b < B; b += kThreads) cnt[b] = 0;
+// 5-6.  Thread m (1..n) forms Theta_m and compares it with Theta_{m-1} (from the
+// lane before it; lane 0 forms that one itself); the first failing m goes to an
+// atomicMin.  The CTA that finishes last reads n*, writes N and Theta_best and
+// counts the pairs of each request among the first n*.
+constexpr int kThetaThreads = 256;
+
+__device__ __forceinline__ double theta_of(const SchedWs& ws, const double* sps, int B, int m) {
+    return __dmul_rn(__ddiv_rn(__ldcg(ws.Ed + m), static_cast<double>(B + m)), sps[B + m]);
+}
+
+__global__ void __launch_bounds__(kThetaThreads)
+schedule_theta(const double* __restrict__ sps, int B, int gamma, int32_t* __restrict__ ell,
+               int32_t* __restrict__ n_sched, double* __restrict__ theta, SchedWs ws) {
+    __shared__ int red[kThetaThreads / 32];
+    __shared__ bool last;
+    const int n = B * gamma;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int m = blockIdx.x * kThetaThreads + threadIdx.x + 1;
+    int fail = 0x7FFFFFFF;
+    double th = 0.0;
+    if (m <= n) th = theta_of(ws, sps, B, m);
+    double before = __shfl_up_sync(0xffffffffu, th, 1);
+    if (lane == 0 && m <= n) before = theta_of(ws, sps, B, m - 1);
+    if (m <= n && !(th > before)) fail = m;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) fail = min(fail, __shfl_xor_sync(0xffffffffu, fail, o));
+    if (lane == 0) red[warp] = fail;
     __syncthreads();
-    for (int p = tid; p < nstar; p += kThreads) atomicAdd(&cnt[sval[p] / gamma], 1);
+    if (threadIdx.x == 0) {
+        int f = 0x7FFFFFFF;
+        for (int w = 0; w < kThetaThreads / 32; ++w) f = min(f, red[w]);
+        if (f != 0x7FFFFFFF) atomicMin(ws.first_fail, f);
+        __threadfence();
+        last = atomicAdd(ws.done, 1u) == gridDim.x - 1;
+    }
     __syncthreads();
-    for (int b = tid; b < B; b += kThreads) ell[b] = cnt[b];
+    if (!last) return;
+    __threadfence();
+    const int ff = atomicAdd(ws.first_fail, 0);
+    const int nstar = (ff == 0x7FFFFFFF) ? n : ff - 1;
+    if (threadIdx.x == 0) {
+        *n_sched = B + nstar;
+        *theta = theta_of(ws, sps, B, nstar);
+    }
+    for (int q = threadIdx.x; q < nstar; q += kThetaThreads) atomicAdd(&ell[__ldcg(ws.req + q)], 1);
 }
 
 // Shared memory for npad padded pairs: keys and values double-buffered, the radix
@@ -342,9 +369,9 @@ constexpr size_t kSmem = smem_bytes(kMaxPairs);
 using namespace dspark;
 
 extern "C" size_t dspark_schedule_prefix_workspace_size(int B, int gamma) {
-    (void)B;
-    (void)gamma;
-    return kStatusBytes;
+    if (B <= 0 || gamma <= 0 || static_cast<long long>(B) * gamma > kMaxPairs) return kStatusBytes;
+    size_t oc, oe, orq;
+    return sched_ws_layout(B * gamma, &oc, &oe, &orq);
 }
 
 extern "C" dspark_status_t dspark_schedule_prefix(int B, int gamma, const float* a, const double* sps,
@@ -360,12 +387,21 @@ extern "C" dspark_status_t dspark_schedule_prefix(int B, int gamma, const float*
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     static OncePerDevice once;
     if (once.run(current_device(), [] {
-            return cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            return cudaFuncSetAttribute(schedule_sort, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(kSmem));
         }) != cudaSuccess)
         return DSPARK_ERR_CUDA;
-    const int npad = (B * gamma + kThreads - 1) / kThreads * kThreads;
-    schedule_kernel<<<1, kThreads, smem_bytes(npad), s>>>(a, sps, B, gamma, ell, n_sched, theta,
-                                                          static_cast<StatusBlock*>(workspace));
+    const int n = B * gamma;
+    const int npad = (n + kThreads - 1) / kThreads * kThreads;
+    size_t oc, oe, orq;
+    sched_ws_layout(n, &oc, &oe, &orq);
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    const SchedWs ws{reinterpret_cast<int32_t*>(w + oc), reinterpret_cast<uint32_t*>(w + oc + 16),
+                     reinterpret_cast<double*>(w + oe), reinterpret_cast<int32_t*>(w + orq)};
+    schedule_sort<<<1, kThreads, smem_bytes(npad), s>>>(a, B, gamma, ell, static_cast<StatusBlock*>(workspace), ws);
+    dspark_status_t st = launch_status();
+    if (st != DSPARK_OK) return st;
+    schedule_theta<<<(n + kThetaThreads - 1) / kThetaThreads, kThetaThreads, 0, s>>>(sps, B, gamma, ell, n_sched,
+                                                                                    theta, ws);
     return launch_status();
 }

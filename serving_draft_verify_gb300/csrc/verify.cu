@@ -12,9 +12,11 @@
 //   decide  by the CTA that completes a row: p_t(x_k) / p_d(x_k) against u
 //           (stream 1); by the CTA that completes a request: n_accept, and
 //           the bonus token, or the rejected position for the residual;
-//   residual for the rejected rows only: the bias engine in its residual mode
-//           (z rebuilt exactly as the draft built it), the Gumbel-max draw
-//           from max(0, p_t - p_d) over the vocabulary (stream 2);
+//   residual for the rejected rows only (listed by the rows pass as it decides
+//           them, so the launch's grid covers just those rows): the bias
+//           engine in its residual mode (z rebuilt exactly as the draft built
+//           it), the Gumbel-max draw from max(0, p_t - p_d) over the
+//           vocabulary (stream 2);
 //   finish  a rejected request takes the residual's winner, or, if the
 //           residual has no mass, a draw from p_t at that row (stream 2).
 #include <algorithm>
@@ -51,12 +53,16 @@ struct VerifyWs {
     float* lt2row;                 // [B][gamma+1] log2-sum-exp2 of t / T per decided row
     float* tx;                     // [B][gamma+1] t[b][k][x_k] for k <= l*_b, picked up by the rows pass
     unsigned int* gbar;            // grid barrier of the residual launch
+    int32_t* rej_count;            // [1] rejected requests so far
+    int32_t* rej_list;             // [B] the rejected requests, in the order their outcomes were decided
 };
 
-// Workspace: status | plan | gbar | wt | res_word | row_cnt | req_cnt (cleared by
-// the plan kernel) | part | krow | lt2 | ld2 | rows | first | dec | lt2row | tx.
+// Workspace: status | plan | gbar | rej_count | wt | res_word | row_cnt | req_cnt
+// (cleared by the plan kernel) | part | krow | lt2 | ld2 | rows | first | dec |
+// lt2row | tx | rej_list.
 struct VerifyLayout {
-    size_t plan, gbar, wt, res_word, row_cnt, req_cnt, part, krow, lt2, ld2, rows, first, dec, lt2row, tx, total;
+    size_t plan, gbar, rej_count, wt, res_word, row_cnt, req_cnt, part, krow, lt2, ld2, rows, first, dec, lt2row, tx,
+        rej_list, total;
 };
 
 VerifyLayout verify_ws_layout(int B, int gamma) {
@@ -66,6 +72,7 @@ VerifyLayout verify_ws_layout(int B, int gamma) {
     auto take = [&](size_t& off, size_t bytes) { off = o; o += round_up(bytes, 256); };
     take(L.plan, 16);
     take(L.gbar, 16);
+    take(L.rej_count, 16);
     take(L.wt, rows * 8);
     take(L.res_word, nb * 8);
     take(L.row_cnt, rows * 4);
@@ -79,6 +86,7 @@ VerifyLayout verify_ws_layout(int B, int gamma) {
     take(L.dec, rows * 4);
     take(L.lt2row, rows * 4);
     take(L.tx, rows * 4);
+    take(L.rej_list, nb * 4);
     L.total = o;
     return L;
 }
@@ -103,6 +111,8 @@ VerifyWs verify_ws(void* workspace, int B, int gamma) {
     ws.lt2row = reinterpret_cast<float*>(w + L.lt2row);
     ws.tx = reinterpret_cast<float*>(w + L.tx);
     ws.gbar = reinterpret_cast<unsigned int*>(w + L.gbar);
+    ws.rej_count = reinterpret_cast<int32_t*>(w + L.rej_count);
+    ws.rej_list = reinterpret_cast<int32_t*>(w + L.rej_list);
     return ws;
 }
 
@@ -144,7 +154,7 @@ verify_plan(int B, int gamma, int V, int rows_ctas, const int32_t* __restrict__ 
         ws.req_cnt[i] = 0;
     }
     if (tid < static_cast<int>(kStatusBytes / 4)) reinterpret_cast<uint32_t*>(ws.status)[tid] = 0u;
-    if (tid == 0) *ws.gbar = 0u;
+    if (tid == 0) { *ws.gbar = 0u; *ws.rej_count = 0; }
     if (tid == 0) carry = 0;
     __syncthreads();
     for (int base = 0; base < B; base += kPlanThreads) {
@@ -265,6 +275,7 @@ __device__ __noinline__ void decide_row(int n, int row, int b, int k, int gamma,
         } else {
             ws.lt2[b] = __ldcg(ws.lt2row + b * (gamma + 1) + rej - 1);
             ws.ld2[b] = lse_d[b * gamma + rej - 1] * kLog2e;
+            ws.rej_list[atomicAdd(ws.rej_count, 1)] = b;   // a row of the residual launch
         }
     }
 }
@@ -279,7 +290,10 @@ __device__ __noinline__ void decide_row(int n, int row, int b, int k, int gamma,
 //   row  l*_b + 1    the Gumbel-max winner over the row: the token maximising
 //                    t_v log2e / T - log2 E_v, E_v = -ln u_v (stream 2).
 // Per piece the CTA publishes its (max, sum) or its winner (atomicMax).
-constexpr int kRowsCtasPerSm = 3;
+#ifndef DSPARK_ROWS_CTAS_PER_SM
+#define DSPARK_ROWS_CTAS_PER_SM 3
+#endif
+constexpr int kRowsCtasPerSm = DSPARK_ROWS_CTAS_PER_SM;   // resident rows-pass CTAs per SM
 
 template <bool kBF16>
 __global__ void __launch_bounds__(256, kRowsCtasPerSm)
@@ -623,6 +637,7 @@ static dspark_status_t verify_impl(int B, int gamma, int V, int r, dspark_dtype_
         p.seed = seed; p.P = P;
         p.ws = eng::Ws{ws.status, ws.res_word, nullptr, nullptr, ws.gbar};
         p.krow = ws.krow; p.T = static_cast<const uint16_t*>(t_logits); p.lt2 = ws.lt2; p.ld2 = ws.ld2;
+        p.rej_list = ws.rej_list; p.rej_count = ws.rej_count;
         // with a co-resident grid the same launch writes the final tokens
         drawn = nM * P <= sm_count(current_device());
         p.fuse_tail = drawn ? 1 : 0;

@@ -24,7 +24,7 @@ def _sps(B, G, alpha=20.0, beta=0.05):
 
 def _run(dsv, a, sps):
     a = np.asarray(a, np.float32)
-    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    ws = torch.empty(dsv.load().dspark_schedule_prefix_workspace_size(*a.shape), dtype=torch.uint8, device="cuda")
     out = dsv.dspark_schedule_prefix(torch.from_numpy(a).cuda(), torch.from_numpy(np.asarray(sps)).cuda(),
                                      workspace=ws)
     assert dsv.workspace_status(ws) == 0
@@ -94,6 +94,6 @@ def test_schedule_non_concave_table_stops_at_first_drop(dsv):
 
 def test_schedule_rejects_out_of_range_survival(dsv):
     a = torch.tensor([[0.5, float("nan")], [1.5, 0.2]], device="cuda")
-    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    ws = torch.empty(dsv.load().dspark_schedule_prefix_workspace_size(2, 2), dtype=torch.uint8, device="cuda")
     dsv.dspark_schedule_prefix(a, torch.ones(7, dtype=torch.float64, device="cuda"), workspace=ws)
     assert dsv.workspace_status(ws) == 6        # DSPARK_ERR_DEVICE_CHECK
