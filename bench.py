@@ -390,60 +390,34 @@ def run_gpu(args):
     roofline = dict(head["roofline"])
     roofline["traffic"] = args.phase_traffic if args.phase_traffic is not None else recorded_engine_traffic()
 
-    # end to end: every step takes its inputs from pinned host memory and reads its results
-    # (x, n_accept, next_token) back.  U, h, x0 and SPS are uploaded (the draft reads all of
-    # them); the target logits stay in host memory and verification reads, over the host
-    # link, only the rows it needs (the scheduled prefix and its stop row).  The link
-    # dominates, so the steps are pipelined: step i+1's upload runs on a copy stream into
-    # the other of two device input sets while step i's round computes.  Enough host copies
-    # of t are cycled that no step can find another step's target rows in L2.  Timed over
-    # all K steps (events before the first upload and after the last read-back).
+    # end to end: every step's per-call inputs (U, h, x0, the SPS table and the target
+    # logits t) are in pinned host memory and go to the C-ABI calls as host buffers: the
+    # kernels read them over the host link inside the timed region, each byte they need
+    # once (t only in its scheduled rows; the weights W1, W2, w stay resident on the
+    # device).  Each step's results (x, n_accept, next_token) are copied back to pinned
+    # host memory.  Two host input sets alternate between steps; every step streams more
+    # than 5 GB, so nothing of a step's inputs is still in L2 for the next.
     e2e = None
     if not args.skip_e2e:
-        host = {k: sv.inp[k].cpu().pin_memory() for k in ("U", "h", "x0", "sps")}
+        host_sets = [{k: sv.inp[k].cpu().pin_memory() for k in ("U", "h", "x0", "sps", "t")} for _ in range(2)]
         t_rows_bytes = head["scheduled_rows"] * V * 2
-        n_tcopies = max(1, min(4, -(-2 * 129 * 2 ** 20 // max(t_rows_bytes, 1))))
-        host_t = [sv.inp["t"].cpu().pin_memory() for _ in range(n_tcopies)]
-        dev_sets = [{k: torch.empty_like(sv.inp[k]) for k in host} for _ in range(2)]
-        h2d = sum(v.numel() * v.element_size() for v in host.values()) + t_rows_bytes
-        res_host = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
-                     for k, v in (("x", sv.outd["x"]), ("n_accept", sv.outv["n_accept"]),
-                                  ("next_token", sv.outv["next_token"]))} for _ in range(2)]
-        d2h = sum(v.numel() * v.element_size() for v in res_host[0].values())
-        copy_stream = torch.cuda.Stream(device=dev)
+        h2d = sum(host_sets[0][k].numel() * host_sets[0][k].element_size() for k in ("U", "h", "x0", "sps")) \
+            + t_rows_bytes
+        res_host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                    for k, v in (("x", sv.outd["x"]), ("n_accept", sv.outv["n_accept"]),
+                                 ("next_token", sv.outv["next_token"]))}
+        d2h = sum(v.numel() * v.element_size() for v in res_host.values())
 
         def e2e_run(nsteps):
-            copied = [torch.cuda.Event() for _ in range(2)]
-            freed = [torch.cuda.Event() for _ in range(2)]
-            for f in freed:
-                f.record(stream)
             t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             barrier()
             t0.record(stream)
-            copy_stream.wait_event(t0)
-
-            def upload(i):
-                sl = i % 2
-                copy_stream.wait_event(freed[sl])        # the round that read this set is done
-                with torch.cuda.stream(copy_stream):
-                    for k in host:
-                        dev_sets[sl][k].copy_(host[k], non_blocking=True)
-                copied[sl].record(copy_stream)
-
-            upload(0)
             for i in range(nsteps):
-                sl = i % 2
-                if i + 1 < nsteps:
-                    upload(i + 1)
-                stream.wait_event(copied[sl])
                 g_ = dict(sv.inp)
-                g_.update(dev_sets[sl])
-                g_["t"] = host_t[i % len(host_t)]
+                g_.update(host_sets[i % 2])
                 sv.round(g_)
-                freed[sl].record(stream)
                 for k in ("x", "n_accept", "next_token"):
-                    src_ = sv.outd["x"] if k == "x" else sv.outv[k]
-                    res_host[sl][k].copy_(src_, non_blocking=True)
+                    res_host[k].copy_(sv.outd["x"] if k == "x" else sv.outv[k], non_blocking=True)
             t1.record(stream)
             barrier()
             return t0.elapsed_time(t1)
@@ -451,13 +425,12 @@ def run_gpu(args):
         e2e_steps = max(3, min(args.steps, args.e2e_steps))
         e2e_run(min(args.warmup, 3))
         e_ms, e_rows = aggregate(e2e_run(e2e_steps), B * G * e2e_steps, world, dev)
+        assert sv.status_ok()
         e2e = {"value": e_rows / (e_ms * 1e-3), "unit": "rows/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-               "pipelined": "step i+1's upload overlaps step i's round (two device input sets)",
-               "target_rows": "read by verification from pinned host memory (the scheduled rows only)",
-               "l2": f"no flush: every step uploads {h2d / 1e9:.2f} GB of fresh inputs and reads its target rows "
-                     f"from one of {n_tcopies} host copies"}
-        del host, host_t, dev_sets
+               "inputs": "pinned host buffers passed to the C-ABI calls; the kernels read them over the host link",
+               "l2": "no flush: every step reads more than 5 GB of host inputs"}
+        del host_sets
     parity = None if args.no_cpu_baseline or world > 1 else parity_sample(sv, args.parity_requests)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

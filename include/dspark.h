@@ -96,6 +96,9 @@ dspark_status_t dspark_workspace_status(const void* workspace, dspark_stream_t s
  *   on ties) and writes lse_d = logp_d = 0.
  *   Outputs [B][gamma]: x (int32 tokens), lse_d = logsumexp(z_k / T),
  *   logp_d = z_k[x_k] / T - lse_d, c, a (float32).
+ *   U, h and x0 may also point to pinned (page-locked, registered) host
+ *   memory: the kernels then read them over the host link, each byte once.
+ *   Unregistered host memory returns DSPARK_ERR_INVALID_ARGUMENT.
  * Requires 1 <= B <= 65535, 1 <= gamma <= DSPARK_MAX_GAMMA, r % 8 == 0 and
  * r <= 256.  bf16 inputs with r % 64 == 0 run the bias on tensor cores.
  * An anchor or token id outside [0, V) sets DSPARK_ERR_DEVICE_CHECK in the
@@ -155,7 +158,8 @@ dspark_status_t dspark_draft_block_noalloc(int B, int gamma, int V, int H, int r
  *
  *   a [B][gamma] float32 survivals, each in [0, 1] and non-increasing in j
  *     (as dspark_draft_block writes them);
- *   sps [B*(gamma+1) + 1] double, sps[N] the verification throughput at N rows;
+ *   sps [B*(gamma+1) + 1] double, sps[N] the verification throughput at N rows
+ *     (device memory, or pinned host memory read through its mapping);
  *   outputs: ell [B] int32 (l*_b in 0..gamma), n_sched [1] int32 (N),
  *   theta [1] double (Theta_best).
  * Requires B * gamma <= 16384.  A value of a outside [0, 1] sets
@@ -182,10 +186,10 @@ dspark_status_t dspark_schedule_prefix(int B, int gamma, const float* a, const d
  * argmax t at the stop row.
  *
  *   t_logits [B][gamma+1][V], U [B][gamma][V], W1/W2 [V][r] in `dt`.
- *   t_logits may also point to pinned (page-locked, registered) host memory:
- *   the kernels then read only the rows verification needs, the scheduled
- *   prefix and its stop row, over the host link.  Unregistered host memory
- *   returns DSPARK_ERR_INVALID_ARGUMENT;
+ *   t_logits, U and x0 may also point to pinned (page-locked, registered)
+ *   host memory: the kernels then read only the rows verification needs (the
+ *   scheduled prefix and its stop row; U rows of rejected requests) over the
+ *   host link.  Unregistered host memory returns DSPARK_ERR_INVALID_ARGUMENT;
  *   x0 [B], x [B][gamma] int32; lse_d, logp_d [B][gamma] float32 (from the
  *   draft); ell [B] int32 in 0..gamma.
  *   Outputs: n_accept [B] int32 in 0..ell[b]; next_token [B] int32.  The

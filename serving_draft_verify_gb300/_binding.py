@@ -221,7 +221,7 @@ def dspark_decode_rounds(U, h, t, W1, W2, w, bias, sps, anchor, rounds, temperat
     _need(W1, (V, r), U.dtype, name="W1")
     _need(W2, (V, r), U.dtype, name="W2")
     _need(w, (H + r,), U.dtype, name="w")
-    _need(sps, (B * (G + 1) + 1,), torch.float64, name="sps")
+    _need(sps, (B * (G + 1) + 1,), torch.float64, name="sps", host_ok=True)
     _need(anchor, (B,), torch.int32, name="anchor")
     dt = _dtype_code(U, h, t, W1, W2, w)
     dev = U.device
@@ -258,19 +258,20 @@ def dspark_decode_rounds(U, h, t, W1, W2, w, bias, sps, anchor, rounds, temperat
 
 def dspark_draft_block(U, h, W1, W2, w, bias, x0, temperature, seed, out=None, workspace=None,
                        stream=None):
-    """Draft block; returns dict x, lse_d, logp_d, c, a (each [B, gamma])."""
+    """Draft block; returns dict x, lse_d, logp_d, c, a (each [B, gamma]).  U, h and x0 may
+    be pinned host tensors: the kernels then read them over the host link (each byte once)."""
     lib = load()
     B, G, V = U.shape
     H = h.shape[-1]
     r = W1.shape[-1]
-    _need(U, (B, G, V), name="U")
-    _need(h, (B, G, H), U.dtype, name="h")
+    _need(U, (B, G, V), name="U", host_ok=True)
+    _need(h, (B, G, H), U.dtype, name="h", host_ok=True)
     _need(W1, (V, r), U.dtype, name="W1")
     _need(W2, (V, r), U.dtype, name="W2")
     _need(w, (H + r,), U.dtype, name="w")
-    _need(x0, (B,), torch.int32, name="x0")
+    _need(x0, (B,), torch.int32, name="x0", host_ok=True)
     dt = _dtype_code(U, h, W1, W2, w)
-    dev = U.device
+    dev = W1.device
     if out is None:
         out = dict(x=torch.empty((B, G), dtype=torch.int32, device=dev),
                    **{k: torch.empty((B, G), dtype=torch.float32, device=dev)
@@ -371,7 +372,7 @@ def dspark_schedule_prefix(a, sps, out=None, workspace=None, stream=None):
     lib = load()
     B, G = a.shape
     _need(a, (B, G), torch.float32, name="a")
-    _need(sps, (B * (G + 1) + 1,), torch.float64, name="sps")
+    _need(sps, (B * (G + 1) + 1,), torch.float64, name="sps", host_ok=True)
     dev = a.device
     if out is None:
         out = dict(ell=torch.empty(B, dtype=torch.int32, device=dev),
@@ -386,23 +387,24 @@ def dspark_schedule_prefix(a, sps, out=None, workspace=None, stream=None):
 
 def dspark_verify(t_logits, U, W1, W2, x0, x, lse_d, logp_d, ell, temperature, seed, out=None,
                   workspace=None, stream=None):
-    """Verification; returns dict n_accept [B], next_token [B] (int32).  t_logits may be a
-    pinned host tensor: the kernels then read the rows verification needs (the scheduled
-    prefix and its bonus row) over the host link, and no others."""
+    """Verification; returns dict n_accept [B], next_token [B] (int32).  t_logits, U and x0
+    may be pinned host tensors: the kernels then read the rows verification needs (the
+    scheduled prefix and its bonus row; U rows of rejected requests only) over the host
+    link, and no others."""
     lib = load()
     B, G, V = U.shape
     r = W1.shape[-1]
     _need(t_logits, (B, G + 1, V), U.dtype, name="t_logits", host_ok=True)
-    _need(U, (B, G, V), name="U")
+    _need(U, (B, G, V), name="U", host_ok=True)
     _need(W1, (V, r), U.dtype, name="W1")
     _need(W2, (V, r), U.dtype, name="W2")
-    _need(x0, (B,), torch.int32, name="x0")
+    _need(x0, (B,), torch.int32, name="x0", host_ok=True)
     _need(x, (B, G), torch.int32, name="x")
     _need(lse_d, (B, G), torch.float32, name="lse_d")
     _need(logp_d, (B, G), torch.float32, name="logp_d")
     _need(ell, (B,), torch.int32, name="ell")
     dt = _dtype_code(t_logits, U, W1, W2)
-    dev = U.device
+    dev = W1.device
     if out is None:
         out = dict(n_accept=torch.empty(B, dtype=torch.int32, device=dev),
                    next_token=torch.empty(B, dtype=torch.int32, device=dev))
@@ -495,7 +497,7 @@ def dspark_verify_ex(t_logits, U, W1, W2, x0, x, lse_d, logp_d, ell, temperature
     _need(logp_d, (B, G), torch.float32, name="logp_d")
     _need(ell, (B,), torch.int32, name="ell")
     dt = _dtype_code(t_logits, U, W1, W2)
-    dev = U.device
+    dev = W1.device
     kind = int(head["kind"])
     if kind != HEAD_MARKOV:
         _need(head["E"], (B, G, r), U.dtype, name="E")

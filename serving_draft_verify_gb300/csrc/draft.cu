@@ -603,6 +603,14 @@ extern "C" dspark_status_t dspark_draft_block(int B, int gamma, int V, int H, in
     if (workspace == nullptr || !aligned256(workspace)) return DSPARK_ERR_INVALID_ARGUMENT;
     if (workspace_bytes < dspark_draft_block_workspace_size(B, gamma, V, r)) return DSPARK_ERR_WORKSPACE_TOO_SMALL;
     clear_stale_error();
+    // the per-call inputs U, h and x0 may be in registered host memory: the kernels read
+    // them through the mapping's device address, each byte once, over the host link
+    if (!device_view(U, &U) || (H > 0 && !device_view(h, &h))) return DSPARK_ERR_INVALID_ARGUMENT;
+    {
+        const void* v = x0;
+        if (!device_view(v, &v)) return DSPARK_ERR_INVALID_ARGUMENT;
+        x0 = static_cast<const int32_t*>(v);
+    }
     return draft_block_impl(B, gamma, V, H, r, dt, U, h, W1, W2, w, bias, x0, temperature, seed, x, lse_d, logp_d,
                             c, a, workspace, reinterpret_cast<cudaStream_t>(stream), nullptr);
 }

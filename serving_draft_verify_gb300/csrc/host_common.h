@@ -51,6 +51,26 @@ inline dspark_status_t clear_status(void* workspace, cudaStream_t stream) {
     return cudaMemsetAsync(workspace, 0, 16, stream) == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 
+// The address kernels use for `p`: p itself for device (or managed) memory, the
+// mapping's device address for page-locked host memory registered with CUDA (the
+// kernels then read it over the host link, only the bytes they touch), and false
+// for ordinary host memory, which a kernel cannot reach.
+inline bool device_view(const void* p, const void** out) {
+    cudaPointerAttributes pa{};
+    if (cudaPointerGetAttributes(&pa, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (pa.type == cudaMemoryTypeUnregistered) return false;
+    if (pa.type == cudaMemoryTypeHost) {
+        if (pa.devicePointer == nullptr || !aligned16(pa.devicePointer)) return false;
+        *out = pa.devicePointer;
+        return true;
+    }
+    *out = p;
+    return true;
+}
+
 // Once-per-device flag for one-time kernel attribute setup.
 struct OncePerDevice {
     std::mutex mu;

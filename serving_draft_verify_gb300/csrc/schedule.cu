@@ -8,7 +8,7 @@
 //   1. keys k = ~bits(a) (ascending k = descending a), values = pair index
 //      b * gamma + j - 1, padded with k = ~0 to a multiple of 1024;
 //   2. stable LSD radix sort, four 8-bit passes; within a warp, equal digits
-//      are ranked with __match_any_sync, so ties keep (b, j) order (up to 1024
+//      are ranked by a ballot per digit bit, so ties keep (b, j) order (up to 1024
 //      pairs: a stable rank by counting instead);
 //   3. exact prefix sums of a * 2^149 (each float32 a in [0, 1] is an integer
 //      below 2^150 at that scale) in 192-bit integers, plus B * 2^149;
@@ -115,6 +115,19 @@ inline size_t sched_ws_layout(int n, size_t* o_ctl, size_t* o_ed, size_t* o_req)
     return o;
 }
 
+// The lanes of this warp whose 8-bit digit equals this lane's: one ballot per
+// bit, each lane keeping the lanes that agree with it on that bit.
+__device__ __forceinline__ uint32_t match_digit8(uint32_t dg) {
+    uint32_t peers = 0xffffffffu;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        const bool bit = (dg >> b) & 1u;
+        const uint32_t bal = __ballot_sync(0xffffffffu, bit);
+        peers &= bit ? bal : ~bal;
+    }
+    return peers;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 schedule_sort(const float* __restrict__ a, int B, int gamma, int32_t* __restrict__ ell, StatusBlock* status,
               SchedWs ws) {
@@ -207,7 +220,7 @@ schedule_sort(const float* __restrict__ a, int B, int gamma, int32_t* __restrict
         for (int rd = 0; rd < R; ++rd) {
             const int e = base + rd * 32 + lane;
             const uint32_t dg = (key[src][e] >> shift) & 0xFFu;
-            const uint32_t peers = __match_any_sync(0xffffffffu, dg);
+            const uint32_t peers = match_digit8(dg);
             if (lane == __ffs(peers) - 1) hist[dg * kWarps + warp] += __popc(peers);
             __syncwarp();
         }
@@ -239,7 +252,7 @@ schedule_sort(const float* __restrict__ a, int B, int gamma, int32_t* __restrict
             const uint32_t k = key[src][e];
             const uint16_t v = val[src][e];
             const uint32_t dg = (k >> shift) & 0xFFu;
-            const uint32_t peers = __match_any_sync(0xffffffffu, dg);
+            const uint32_t peers = match_digit8(dg);
             const int rank = __popc(peers & ((1u << lane) - 1u));
             const int pos = hist[dg * kWarps + warp] + rank;
             key[src ^ 1][pos] = k;
@@ -384,6 +397,11 @@ extern "C" dspark_status_t dspark_schedule_prefix(int B, int gamma, const float*
     if (workspace == nullptr || !aligned256(workspace)) return DSPARK_ERR_INVALID_ARGUMENT;
     if (workspace_bytes < dspark_schedule_prefix_workspace_size(B, gamma)) return DSPARK_ERR_WORKSPACE_TOO_SMALL;
     clear_stale_error();
+    {   // the SPS table may be in registered host memory (read through its mapping)
+        const void* v = sps;
+        if (!device_view(v, &v)) return DSPARK_ERR_INVALID_ARGUMENT;
+        sps = static_cast<const double*>(v);
+    }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     static OncePerDevice once;
     if (once.run(current_device(), [] {

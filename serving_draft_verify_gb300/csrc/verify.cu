@@ -582,19 +582,13 @@ static dspark_status_t verify_impl(int B, int gamma, int V, int r, dspark_dtype_
     if (workspace == nullptr || !aligned256(workspace)) return DSPARK_ERR_INVALID_ARGUMENT;
     if (workspace_bytes < dspark_verify_workspace_size(B, gamma, V, r)) return DSPARK_ERR_WORKSPACE_TOO_SMALL;
     clear_stale_error();
+    // target rows (and U, x0, x) may be in registered host memory: the kernels read them
+    // through the mapping's device address (only the rows verification needs cross the link)
+    if (!device_view(t_logits, &t_logits) || !device_view(U, &U)) return DSPARK_ERR_INVALID_ARGUMENT;
     {
-        // target rows in registered host memory: the kernels read them through the
-        // mapping's device address (only the rows verification needs cross the link)
-        cudaPointerAttributes pa{};
-        if (cudaPointerGetAttributes(&pa, t_logits) != cudaSuccess) {
-            cudaGetLastError();
-            return DSPARK_ERR_INVALID_ARGUMENT;
-        }
-        if (pa.type == cudaMemoryTypeUnregistered) return DSPARK_ERR_INVALID_ARGUMENT;
-        if (pa.type == cudaMemoryTypeHost) {
-            if (pa.devicePointer == nullptr || !aligned16(pa.devicePointer)) return DSPARK_ERR_INVALID_ARGUMENT;
-            t_logits = pa.devicePointer;
-        }
+        const void* v = x0;
+        if (!device_view(v, &v)) return DSPARK_ERR_INVALID_ARGUMENT;
+        x0 = static_cast<const int32_t*>(v);
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const VerifyWs ws = verify_ws(workspace, B, gamma);

@@ -146,3 +146,19 @@ def test_draft_one_launch_equals_per_position(dsv, key, changes, temperature):
         assert np.array_equal(one[name], per[name]), name
     del inp
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("temperature", [None, 0.0])
+def test_draft_reads_inputs_from_pinned_host_memory(dsv, temperature):
+    """U, h and x0 in pinned host memory (read by the kernels over the host link): the
+    same outputs, bit for bit, as from device memory."""
+    cfg = wl.scaled(wl.QWEN3_8B, B=40, V=8192, H=64)
+    inp = wl.make_draft_inputs(cfg)
+    T = cfg.temperature if temperature is None else temperature
+    g = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    a = dsv.dspark_draft_block(g["U"], g["h"], g["W1"], g["W2"], g["w"], 0.0, g["x0"], T, cfg.seed)
+    host = {k: inp[k].clone().pin_memory() for k in ("U", "h", "x0")}
+    b = dsv.dspark_draft_block(host["U"], host["h"], g["W1"], g["W2"], g["w"], 0.0, host["x0"], T, cfg.seed)
+    torch.cuda.synchronize()
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
