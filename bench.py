@@ -688,6 +688,43 @@ def run_tv_only(args):
     print(json.dumps(res))
 
 
+def run_round_case(args):
+    """One draft -> schedule -> verify round on a high-concurrency-shaped case (B x gamma
+    of the full vocabulary), for profiling the round's kernels on a small case; prints
+    one JSON line with the per-call times (CUDA events, L2 flushed before each round)."""
+    import torch
+    import serving_draft_verify_gb300 as dsv
+    from serving_draft_verify_gb300 import workloads as wl
+
+    dev = torch.device("cuda", 0)
+    dsv.load()
+    lib = dsv._binding.load()
+    B, G = (int(x) for x in args.round_case.split(":"))
+    sv = Serving(dsv, lib, wl.scaled(wl.HIGH_CONC, B=B, gamma=G), dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    us = [[], [], []]
+    for it in range(args.warmup + args.steps):
+        flush.zero_()
+        ev[0].record()
+        sv.draft()
+        ev[1].record()
+        sv.schedule()
+        ev[2].record()
+        sv.verify()
+        ev[3].record()
+        torch.cuda.synchronize()
+        if it >= args.warmup:
+            for i in range(3):
+                us[i].append(ev[i].elapsed_time(ev[i + 1]) * 1e3)
+    assert sv.status_ok()
+    ell = sv.outs["ell"].cpu()
+    print(json.dumps({"workload": f"round, B={B} gamma={G} V={sv.cfg.V} r={sv.cfg.r} T={sv.T}",
+                      "draft_us": statistics.median(us[0]), "schedule_us": statistics.median(us[1]),
+                      "verify_us": statistics.median(us[2]), "scheduled_rows": int((ell + 1).sum()),
+                      "rejected": int((sv.outv["n_accept"].cpu() < ell).sum())}))
+
+
 def run_draft_only(args):
     """dspark_draft_block alone on a high-concurrency-shaped case (B x gamma of the
     full vocabulary), for profiling one kernel on a small case; prints one JSON line
@@ -744,6 +781,8 @@ def main():
     ap.add_argument("--draft-case", default=None,
                     help="B:gamma -- time only dspark_draft_block on that high-concurrency-shaped case")
     ap.add_argument("--draft-temperature", type=float, default=None, help="temperature of --draft-case")
+    ap.add_argument("--round-case", default=None,
+                    help="B:gamma -- time only the round's three calls on that high-concurrency-shaped case")
     ap.add_argument("--tv-rows", type=int, default=None,
                     help="time only the TV and training-loss kernels on this many training rows")
     args = ap.parse_args()
@@ -753,6 +792,8 @@ def main():
         run_tv_only(args)
     elif args.draft_case is not None:
         run_draft_only(args)
+    elif args.round_case is not None:
+        run_round_case(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -182,10 +182,11 @@ __device__ __forceinline__ unsigned long long f2fma(unsigned long long a, unsign
 // v >> 2 keys index v.
 __device__ __forceinline__ void draw32(const float* s, float c, int v0, const PhiloxRow& pr, Best& best, float& M,
                                        float& S) {
-    float m4[4] = {s[0], s[1], s[2], s[3]};
+    float m8[8];
 #pragma unroll
-    for (int w = 4; w < 32; ++w) m4[w & 3] = fmaxf(m4[w & 3], s[w]);
-    const float mraw = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+    for (int w = 0; w < 8; ++w) m8[w] = fmaxf(fmaxf(s[w], s[w + 8]), fmaxf(s[w + 16], s[w + 24]));
+    const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
     const bool live = mraw > -INFINITY;                   // no finite logit: no mass, no candidate
     const float mb = mraw * c;                            // the sub-block's max of y
     const float mref = live ? mb : 0.f;
@@ -194,7 +195,7 @@ __device__ __forceinline__ void draw32(const float* s, float c, int v0, const Ph
     constexpr float kShift = 0.999999940395355225f + 1.1920928955078125e-07f;
     const float R = live ? fast_exp2(mb - best.key) * kSlack : 0.f;   // +inf while nothing is drawn yet
     const unsigned long long c2 = f2pack(c, c), nm2 = f2pack(-mref, -mref);
-    unsigned long long sum2 = f2pack(0.f, 0.f);
+    unsigned long long sum2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};   // two chains of partial sums
     const uint32_t q0 = static_cast<uint32_t>(v0) >> 2;
     // per half of 16 tokens: its four Philox blocks first (independent chains the scheduler
     // can overlap), then the sum (e = 2^(s c - m), two tokens per f32x2 operation) and the
@@ -211,16 +212,17 @@ __device__ __forceinline__ void draw32(const float* s, float c, int v0, const Ph
             wv[4 * qq + 2] = pw.z;
             wv[4 * qq + 3] = pw.w;
         }
-        uint32_t cmask = 0u;
+        uint32_t cm[4] = {0u, 0u, 0u, 0u};                // four independent chains of candidate bits
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
             float a0, a1;
             f2unpack(f2fma(f2pack(s[16 * hh + i], s[16 * hh + i + 1]), c2, nm2), a0, a1);
             const float e0 = fast_exp2(a0), e1 = fast_exp2(a1);
-            sum2 = f2add(sum2, f2pack(e0, e1));
-            if (one_minus_u_shifted(wv[i]) < fmaf(e0, R, kShift)) cmask |= 1u << i;       // 0 * inf = NaN: false
-            if (one_minus_u_shifted(wv[i + 1]) < fmaf(e1, R, kShift)) cmask |= 2u << i;
+            sum2[(i >> 1) & 1] = f2add(sum2[(i >> 1) & 1], f2pack(e0, e1));
+            if (one_minus_u_shifted(wv[i]) < fmaf(e0, R, kShift)) cm[(i >> 1) & 3] |= 1u << i;   // 0 * inf = NaN: false
+            if (one_minus_u_shifted(wv[i + 1]) < fmaf(e1, R, kShift)) cm[(i >> 1) & 3] |= 2u << i;
         }
+        const uint32_t cmask = (cm[0] | cm[1]) | (cm[2] | cm[3]);
         if (__any_sync(0xffffffffu, cmask != 0u)) {
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {
@@ -246,7 +248,7 @@ __device__ __forceinline__ void draw32(const float* s, float c, int v0, const Ph
         }
     }
     float sl, sh;
-    f2unpack(sum2, sl, sh);
+    f2unpack(f2add(sum2[0], sum2[1]), sl, sh);
     if (live) lse_merge(M, S, mb, sl + sh);
 }
 
@@ -706,7 +708,8 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                 const int kb = (rr < nrows) ? row_k(b, k) : 0;
                 const bool valid = rr < nrows && kb > 0;
                 const bool warp_live = ((q * 32) % rpc) < nrows;
-                // U rows stay in L2 (normal policy) for the draft; the residual reads them once
+                // U rows with the normal policy for the draft (a thread reads the two halves of
+                // each 128-byte line one sub-block apart), evict-first for the residual
                 const uint64_t pol = (kMode == kDraft) ? policy_evict_normal() : policy_evict_first();
                 const uint16_t* urow = p.U + (static_cast<size_t>(valid ? b : 0) * p.gamma + (valid ? kb - 1 : 0)) * p.V;
                 float ld2 = 0.f, lt2 = 0.f;
