@@ -530,9 +530,10 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
     // compacted so that the whole grid works on the M-tiles that exist.
     const int nact = (kMode == kResidual) ? min(max(__ldcg(p.rej_count), 0), p.B) : p.B;
     // Row replication: with at most 64 rows the A tile holds every row twice (TMEM
-    // lanes 0-63 and 64-127) and the two copies reduce different 64-token halves of
-    // each tile, so all epilogue warps have work.
-    const int R = (nact <= 64) ? 2 : 1;
+    // lanes 0-63 and 64-127), with at most 32 four times (lanes 32 c .. 32 c + 31 for
+    // copy c), and the copies reduce different parts (halves, quarters) of each tile,
+    // so more epilogue lanes have work at small batches.
+    const int R = (nact <= 32) ? 4 : (nact <= 64) ? 2 : 1;
     const int rpc = kBM / R;                              // request rows per copy
     const int nM = max(1, (nact + kBM - 1) / kBM);        // M-tiles (one when R = 2)
     const int NT = (p.V + kBN - 1) / kBN;
@@ -644,7 +645,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                 // one warp per A row, one lane per 16-byte chunk (r / 8 <= 32 chunks)
                 const int cpr = p.r / 8;
                 for (int row = ptid >> 5; row < kBM; row += kPro / 32) {
-                    const int rr = row & (rpc - 1);       // rpc is 64 or 128
+                    const int rr = row & (rpc - 1);       // rpc is 32, 64 or 128
                     const int prev = (rr < nrows) ? s_prev[rr] : -1;
                     if (lane < cpr) {
                         const int slab = lane >> 3, c = lane & 7;
@@ -729,12 +730,13 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                 float qb = 0.f, Eq = 1.f;                 // kResidual: the running winner's q and E
                 const int i0 = eg;                        // this WG's tiles: eg, eg + kEpiWG, ...
 
-                // The thread's sub-blocks of 32 tokens: four per tile (two per tile and copy when
-                // each request is held twice).  One compact loop body serves them all; the U
-                // words of the next sub-block (this tile's next, or the next tile's first) are
-                // loaded one sub-block ahead, so the load has a sub-block's work to land.
-                const int nsub = (R == 1) ? 4 : 2;
-                const int soff = (R == 1) ? 0 : copy * 64;   // token offset of the first sub-block in a tile
+                // The thread's sub-blocks of 32 tokens: four per tile (two or one per tile and
+                // copy when each request is held twice or four times).  One compact loop body
+                // serves them all; the U words of the next sub-block (this tile's next, or the
+                // next tile's first) are loaded one sub-block ahead, so the load has a
+                // sub-block's work to land.
+                const int nsub = kBN / 32 / R;            // this copy's share of a tile: kBN / R tokens
+                const int soff = copy * (kBN / R);        // token offset of the first sub-block in a tile
                 auto load16 = [&](const uint16_t* src, int v0, uint32_t* dst) {
 #pragma unroll
                     for (int g8 = 0; g8 < 4; ++g8) {

@@ -218,3 +218,44 @@ def test_loss_full_training_size_sampled_rows(dsv):
                 d64, t64, tg, s64, om64, torch.bfloat16)
     tot = out["row"][:, 3].double().sum().item()
     assert abs(float(out["loss"][0]) - tot) <= 1e-5 * max(1.0, abs(tot))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("V", [1024, 151936])
+def test_gradient_signs_exact_beyond_the_tie_band(dsv, dtype, V):
+    """The tie band of _check_grad (|p_d - p_t| <= 1e-5 max(p_d, p_t)) is no wider than
+    needed: rows whose decisive log ratios sit just outside it must get every sign of
+    sign(p_d - p_t) exactly as float64 does, with no tie allowance at all.
+
+    Row: d = 0 everywhere; t = +h on the first half of the vocabulary and -h on the
+    second.  Then L_d - L_t = -ln cosh h, and every token's |ln(p_d / p_t)| is
+    h -/+ ln cosh h, about h: margins from 1.2e-5 (just beyond the band) to 1e-3.
+    A wrong sign on either half moves sum_u p_d(u) sgn_u by about 1, and with it
+    every element of the row's gradient by about half its scale, far beyond the
+    tolerance.  The kernel's own sums here are of exact terms (ones, and e^(+-h)
+    whose total differs from V by less than float32 resolves), so its decision
+    error is far below h and these rows must pass the exact check."""
+    hs = [1.2e-5, 2e-5, 5e-5, 1e-4, 1e-3]
+    rows = len(hs)
+    d = np.zeros((rows, V), np.float64)
+    t = np.zeros((rows, V), np.float64)
+    for r, h in enumerate(hs):
+        h = float(torch.tensor(h, dtype=dtype).double())   # representable in the input dtype
+        t[r, :V // 2] = h
+        t[r, V // 2:] = -h
+    dt_, tt_ = torch.from_numpy(d).to(dtype), torch.from_numpy(t).to(dtype)
+    target = torch.tensor([(r * 7919 + 13) % V for r in range(rows)], dtype=torch.int32)
+    s = torch.linspace(-1.0, 1.0, rows)
+    omega = torch.full((rows,), 1.0 / rows)
+    got = _run(dsv, dt_, tt_, target, s, omega)
+    d64, t64 = wl.to_f64(dt_), wl.to_f64(tt_)
+    p_d, p_t = oracle.tv.softmax(d64), oracle.tv.softmax(t64)
+    lr = np.abs(np.log(p_d / p_t))
+    assert np.all(lr > 1.1e-5), lr.min()                  # every token beyond the band
+    want_gd, _ = oloss.dspark_loss_grad(d64, t64, target.numpy(), s.double().numpy(), omega.double().numpy())
+    onehot = np.zeros_like(d64)
+    onehot[np.arange(rows), target.numpy()] = 1.0
+    om = omega.double().numpy()[:, None]
+    scale = np.abs(om) * (abs(oloss.ALPHA_CE) * (p_d + onehot) + abs(oloss.ALPHA_L1) * p_d) + 1e-30
+    err = np.abs(got["grad_d"].double().numpy() - want_gd)
+    assert np.all(err <= GRAD_REL[dtype] * scale), np.max(err / scale)
