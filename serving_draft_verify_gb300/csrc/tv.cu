@@ -73,6 +73,11 @@ __device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigne
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
 __device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
     unsigned long long d;
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
@@ -534,6 +539,209 @@ dspark_status_t launch_tv(int64_t rows, int V, const void* d, const void* t, flo
     return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 
+// ------------------------------------------------------- accept rate, two passes
+// dspark_accept_rate_tv's kernel: one CTA of 1024 threads per SM takes rows in
+// turn.  Pass 1 streams the row's d and t from HBM (L2 evict-last) and forms each
+// thread's online (max, sum of 2^((x - max) log2e)) of both; a block reduction
+// gives L_d and L_t; pass 2 streams the same row again -- from L2, where pass 1
+// left it (a CTA's row is 607,744 B for bf16 and V = 151936, so one row per SM,
+// 92 MB in all, stays within the L2) -- with the evict-first policy, summing
+// 2^(min(d - L_d, t - L_t) log2e).  No clusters, and each logit pair costs about
+// half the instructions of the single-pass kernel's three readings of shared
+// memory.
+//
+// Loads: every thread copies its own 16-byte groups into its own slots of a ring
+// in shared memory with cp.async (no block barrier guards a slot: only the thread
+// that copied it reads it), kTv2Stages - 1 groups of d and of t ahead of the one
+// it is summing: 96 KB in flight per SM.
+constexpr int kTv2Threads = 1024;
+constexpr int kTv2Stages = 4;
+constexpr size_t kTv2Smem = static_cast<size_t>(kTv2Stages) * 2 * kTv2Threads * 16;
+
+// The group's max (raw units), -inf if it has no finite element.
+template <bool kBF16>
+__device__ __forceinline__ float group_max(const uint4 v) {
+    if constexpr (kBF16) {
+        const uint32_t m = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
+        return fmaxf(bf16lo(m), bf16hi(m));
+    } else {
+        return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                     fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+    }
+}
+
+// (m, s) += the group's elements, s a sum of 2^((x - m) log2e): a larger group
+// max first rescales s (rare once m has settled).  For bf16 the exponent is one
+// fused x log2e - (m log2e): every term carries the rounding error r of m log2e
+// (|r| <= ulp(m log2e) / 2, a relative 1e-5 at |m| = 100, inside the bf16 bound).
+// For float32, whose bound is tighter, x - m is formed first, so the maximum's
+// term is exactly 1.
+template <bool kBF16>
+__device__ __forceinline__ void group_lse(const uint4 v, float& m, float& s) {
+    constexpr int EPG = TVTraits<kBF16>::kEPG;
+    const float gm = group_max<kBF16>(v);
+    if (!(gm > -INFINITY)) return;                        // no mass in this group
+    if (gm > m) {
+        s = (s > 0.f) ? s * fast_exp2((m - gm) * kLog2e) : 0.f;
+        m = gm;
+    }
+    float a[EPG];
+    unpack<kBF16>(v, a);
+    const unsigned long long L2E = pk(kLog2e, kLog2e);
+    const unsigned long long nm = kBF16 ? pk(-m * kLog2e, -m * kLog2e) : pk(-m, -m);
+    unsigned long long acc = pk(0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < EPG; e += 2) {
+        const float2 y = kBF16 ? upk(fma2(pk(a[e], a[e + 1]), L2E, nm)) : upk(mul2(add2(pk(a[e], a[e + 1]), nm), L2E));
+        acc = add2(acc, pk(fast_exp2(y.x), fast_exp2(y.y)));
+    }
+    s += upk(acc).x + upk(acc).y;
+}
+
+// Block-wide merge of every thread's (m, s) pair for d and t: all threads get (L_d, L_t)
+// in natural units.
+__device__ __forceinline__ float2 block_lse2(float md, float sd, float mt, float st, float4* red, float2* fin) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    warp_lse(md, sd);
+    warp_lse(mt, st);
+    if (lane == 0) red[warp] = make_float4(md, sd, mt, st);
+    __syncthreads();
+    if (warp == 0) {
+        float4 r = (lane < kTv2Threads / 32) ? red[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+        warp_lse(r.x, r.y);
+        warp_lse(r.z, r.w);
+        if (lane == 0) {
+            const float Ld = (r.y > 0.f) ? r.x + fast_log2(r.y) * kLn2 : -INFINITY;
+            const float Lt = (r.w > 0.f) ? r.z + fast_log2(r.w) * kLn2 : -INFINITY;
+            *fin = make_float2(Ld, Lt);
+        }
+    }
+    __syncthreads();
+    return *fin;
+}
+
+// One 16-byte asynchronous copy global -> shared with an L2 policy (cp.async.cg).
+__device__ __forceinline__ void cp16_hint(void* dst, const void* src, uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// One pass over a row: a thread's groups i = 0 .. nmine - 1 (group tid + i T) of d
+// and t go through its ring, copied kTv2Stages - 1 groups ahead of the one that
+// body(vd, vt) sums.  Each issue commits one cp.async group, empty past the last,
+// so that "group i has landed" is always wait_group(S - 2) after i + S - 1 commits.
+template <class F>
+__device__ __forceinline__ void tv2_pass(const uint4* gd, const uint4* gt, int nmine, uint4* ring, uint64_t pol,
+                                         F&& body) {
+    const int tid = threadIdx.x;
+    auto issue = [&](int i) {
+        if (i < nmine) {
+            const int g = tid + i * kTv2Threads;
+            uint4* slot = ring + static_cast<size_t>(i % kTv2Stages) * 2 * kTv2Threads + tid;
+            cp16_hint(slot, gd + g, pol);
+            cp16_hint(slot + kTv2Threads, gt + g, pol);
+        }
+        cp_commit();
+    };
+#pragma unroll
+    for (int i = 0; i < kTv2Stages - 1; ++i) issue(i);
+    for (int i = 0; i < nmine; ++i) {
+        cp_wait<kTv2Stages - 2>();                        // group i has landed
+        const uint4* slot = ring + static_cast<size_t>(i % kTv2Stages) * 2 * kTv2Threads + tid;
+        const uint4 vd = slot[0], vt = slot[kTv2Threads];
+        issue(i + kTv2Stages - 1);                        // refills the slot read one group ago
+        body(vd, vt);
+    }
+    cp_wait<0>();
+}
+
+template <bool kBF16>
+__global__ void __launch_bounds__(kTv2Threads, 1)
+tv_two_pass(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float* __restrict__ c_star, int64_t rows,
+            int V) {
+    using Tr = TVTraits<kBF16>;
+    constexpr int EPG = Tr::kEPG, ESZ = Tr::kESZ;
+    extern __shared__ __align__(16) uint8_t tv2_smem[];
+    uint4* ring = reinterpret_cast<uint4*>(tv2_smem);
+    __shared__ float4 red[kTv2Threads / 32];
+    __shared__ float2 fin;
+    __shared__ float red2[kTv2Threads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ngroups = V / EPG;
+    const int nmine = (ngroups > tid) ? (ngroups - tid + kTv2Threads - 1) / kTv2Threads : 0;
+    const uint64_t keep = policy_evict_last(), drop = policy_evict_first();
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const uint4* gd = reinterpret_cast<const uint4*>(d + static_cast<size_t>(row) * V * ESZ);
+        const uint4* gt = reinterpret_cast<const uint4*>(t + static_cast<size_t>(row) * V * ESZ);
+        // pass 1: (max, sum) of d and t, from HBM
+        float md = -INFINITY, sd = 0.f, mt = -INFINITY, st = 0.f;
+        tv2_pass(gd, gt, nmine, ring, keep, [&](const uint4 vd, const uint4 vt) {
+            group_lse<kBF16>(vd, md, sd);
+            group_lse<kBF16>(vt, mt, st);
+        });
+        if (!(md > -INFINITY)) { md = 0.f; sd = 0.f; }
+        if (!(mt > -INFINITY)) { mt = 0.f; st = 0.f; }
+        const float2 L = block_lse2(md, sd, mt, st, red, &fin);
+        // pass 2: sum of 2^(min(d - L_d, t - L_t) log2e), from L2 (for bf16 the
+        // exponents are the fused d log2e - L_d log2e and t log2e - L_t log2e)
+        unsigned long long acc = pk(0.f, 0.f);
+        if (L.x > -INFINITY && L.y > -INFINITY) {
+            const unsigned long long L2E = pk(kLog2e, kLog2e);
+            const float sc = kBF16 ? kLog2e : 1.f;
+            const unsigned long long nLd = pk(-L.x * sc, -L.x * sc), nLt = pk(-L.y * sc, -L.y * sc);
+            tv2_pass(gd, gt, nmine, ring, drop, [&](const uint4 vd, const uint4 vt) {
+                float a[EPG], b[EPG];
+                unpack<kBF16>(vd, a);
+                unpack<kBF16>(vt, b);
+#pragma unroll
+                for (int e = 0; e < EPG; e += 2) {
+                    if constexpr (kBF16) {
+                        const float2 x = upk(fma2(pk(a[e], a[e + 1]), L2E, nLd));
+                        const float2 y = upk(fma2(pk(b[e], b[e + 1]), L2E, nLt));
+                        acc = add2(acc, pk(fast_exp2(fminf(x.x, y.x)), fast_exp2(fminf(x.y, y.y))));
+                    } else {
+                        const float2 x = upk(add2(pk(a[e], a[e + 1]), nLd));
+                        const float2 y = upk(add2(pk(b[e], b[e + 1]), nLt));
+                        const float2 z = upk(mul2(pk(fminf(x.x, y.x), fminf(x.y, y.y)), L2E));
+                        acc = add2(acc, pk(fast_exp2(z.x), fast_exp2(z.y)));
+                    }
+                }
+            });
+        }
+        float part = upk(acc).x + upk(acc).y;
+        part = warp_sum(part);
+        if (lane == 0) red2[warp] = part;
+        __syncthreads();
+        if (warp == 0) {
+            float v = (lane < kTv2Threads / 32) ? red2[lane] : 0.f;
+            v = warp_sum(v);
+            if (lane == 0) c_star[row] = v;
+        }
+        // red, fin and red2 are rewritten by the next row after a barrier in block_lse2
+    }
+}
+
+template <bool kBF16>
+dspark_status_t launch_tv_two_pass(int64_t rows, int V, const void* d, const void* t, float* c_star,
+                                   cudaStream_t stream) {
+    const int dev = current_device();
+    static OncePerDevice once;
+    if (once.run(dev, [] {
+            return cudaFuncSetAttribute(tv_two_pass<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(kTv2Smem));
+        }) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+    const int sms = sm_count(dev);
+    const int64_t grid = rows < sms ? rows : sms;
+    tv_two_pass<kBF16><<<static_cast<unsigned>(grid), kTv2Threads, kTv2Smem, stream>>>(
+        static_cast<const uint8_t*>(d), static_cast<const uint8_t*>(t), c_star, rows, V);
+    return launch_status();
+}
+
 }  // namespace
 }  // namespace dspark
 
@@ -555,14 +763,11 @@ extern "C" dspark_status_t dspark_accept_rate_tv(int64_t rows, int V, dspark_dty
     if (rows == 0) return DSPARK_OK;
     if (d == nullptr || t == nullptr || c_star == nullptr) return DSPARK_ERR_INVALID_ARGUMENT;
     if (!aligned16(d) || !aligned16(t)) return DSPARK_ERR_INVALID_ARGUMENT;
-    if (V > 163840) return DSPARK_ERR_UNSUPPORTED;
     clear_stale_error();
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (clear_status(workspace, s) != DSPARK_OK) return DSPARK_ERR_CUDA;
-    StatusBlock* st = static_cast<StatusBlock*>(workspace);
-    const LossArgs none{};
-    return dt == DSPARK_BF16 ? launch_tv<true, false>(rows, V, d, t, c_star, st, none, s)
-                             : launch_tv<false, false>(rows, V, d, t, c_star, st, none, s);
+    return dt == DSPARK_BF16 ? launch_tv_two_pass<true>(rows, V, d, t, c_star, s)
+                             : launch_tv_two_pass<false>(rows, V, d, t, c_star, s);
 }
 
 // Workspace of the loss: status block | cluster counter (own 256 bytes) | one

@@ -70,6 +70,17 @@ def test_tv_special_cases(dsv):
         assert np.max(np.abs(got - want)) < 1e-5
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("offset", [-120.0, 60.0, 100.0])
+def test_tv_large_logits(dsv, dtype, offset):
+    """Logits far from 0: the bf16 path forms its exponents as x log2e - L log2e in
+    one fused step, so every term carries the rounding of L log2e (largest at large
+    |L|); both dtypes must still meet the tight bound."""
+    cfg = wl.scaled(wl.TV_TRAIN, V=151936)
+    d, t = wl.make_tv_inputs(cfg, rows=9)
+    _check(dsv, (d.float() + offset).to(dtype), (t.float() + offset).to(dtype))
+
+
 def test_tv_empty_and_one_row(dsv):
     out = torch.full((0,), 7.0, device="cuda")
     d = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
