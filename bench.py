@@ -531,8 +531,8 @@ def run_gpu(args):
                  "emitted_tokens_per_s": float(rout["n_emitted"].sum().item()) / (r_ms * 1e-3),
                  "E_tau": float(st_[:, 0].mean()), "realised_tau": float(st_[:, 1].mean())}
         del pool_
-    # draft: the cooperative engine launch; schedule: 1; verify: plan, rows, residual (+ final token)
-    launches_per_step = 1 + 1 + 3
+    # draft: the cooperative engine launch; schedule: chunks, rank, scan; verify: plan, rows, residual
+    launches_per_step = 1 + 3 + 3
 
     line = {"metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",

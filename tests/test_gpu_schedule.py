@@ -97,3 +97,35 @@ def test_schedule_rejects_out_of_range_survival(dsv):
     ws = torch.empty(dsv.load().dspark_schedule_prefix_workspace_size(2, 2), dtype=torch.uint8, device="cuda")
     dsv.dspark_schedule_prefix(a, torch.ones(7, dtype=torch.float64, device="cuda"), workspace=ws)
     assert dsv.workspace_status(ws) == 6        # DSPARK_ERR_DEVICE_CHECK
+
+
+def test_schedule_workspace_reuse_and_late_chunk_error(dsv):
+    """One workspace through calls of different sizes: the per-chunk sums, flags and
+    counters are cleared by each call; an out-of-range survival in the last chunk of
+    a many-chunk batch is reported, and the next valid call reports a clear status."""
+    lib = dsv.load()
+    ws = torch.empty(lib.dspark_schedule_prefix_workspace_size(1024, 16), dtype=torch.uint8, device="cuda")
+    rng = np.random.default_rng(21)
+
+    def call(a, sps):
+        out = dsv.dspark_schedule_prefix(torch.from_numpy(a).cuda(), torch.from_numpy(sps).cuda(), workspace=ws)
+        torch.cuda.synchronize()
+        return out
+
+    for B, G in ((1024, 16), (37, 3), (1000, 9), (5, 1)):
+        a = _survival(rng.beta(5, 2, (B, G)))
+        sps = _sps(B, G, 2.0, 0.01)
+        out = call(a, sps)
+        assert dsv.workspace_status(ws) == 0
+        ell, n, th = schedule.schedule_prefix(a, sps)
+        assert np.array_equal(out["ell"].cpu().numpy(), ell) and int(out["n_sched"].item()) == n
+        assert out["theta"].item() == th
+    B, G = 1000, 9
+    a = _survival(rng.beta(5, 2, (B, G)))
+    bad = a.copy()
+    bad[B - 1, G - 1] = np.float32(np.nan)                  # pair 8999: the last of 71 chunks
+    call(bad, _sps(B, G))
+    assert dsv.workspace_status(ws) == 6
+    out = call(a, _sps(B, G))
+    assert dsv.workspace_status(ws) == 0
+    assert np.array_equal(out["ell"].cpu().numpy(), schedule.schedule_prefix(a, _sps(B, G))[0])
