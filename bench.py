@@ -725,6 +725,9 @@ def run_round_case(args):
                       "rejected": int((sv.outv["n_accept"].cpu() < ell).sum())}))
 
 
+DRAFT_PATHS = {"auto": 0, "tcgen05": 1, "gemv": 2}
+
+
 def run_draft_only(args):
     """dspark_draft_block alone on a high-concurrency-shaped case (B x gamma of the
     full vocabulary), for profiling one kernel on a small case; prints one JSON line
@@ -737,6 +740,7 @@ def run_draft_only(args):
     dsv.load()
     lib = dsv._binding.load()
     B, G = (int(x) for x in args.draft_case.split(":"))
+    dsv._binding.set_draft_path(DRAFT_PATHS[args.draft_path])
     T = wl.HIGH_CONC.temperature if args.draft_temperature is None else args.draft_temperature
     sv = Serving(dsv, lib, wl.scaled(wl.HIGH_CONC, B=B, gamma=G), dev, T=T)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -755,7 +759,8 @@ def run_draft_only(args):
     m = statistics.median(ms)
     cfg = sv.cfg
     nb = draft_launch_bytes(cfg.B, cfg.gamma, cfg.V, cfg.H, cfg.r)
-    print(json.dumps({"workload": f"draft block, B={B} gamma={G} V={cfg.V} r={cfg.r} T={T}", "median_ms": m,
+    print(json.dumps({"workload": f"draft block, B={B} gamma={G} V={cfg.V} r={cfg.r} T={T}",
+                      "path": args.draft_path, "median_ms": m,
                       "gbs": nb / (m * 1e-3) / 1e9, "logits_per_ms": B * G * cfg.V / m}))
 
 
@@ -781,6 +786,8 @@ def main():
     ap.add_argument("--draft-case", default=None,
                     help="B:gamma -- time only dspark_draft_block on that high-concurrency-shaped case")
     ap.add_argument("--draft-temperature", type=float, default=None, help="temperature of --draft-case")
+    ap.add_argument("--draft-path", default="auto", choices=sorted(DRAFT_PATHS),
+                    help="draft path of --draft-case: by batch size, the tcgen05 engine, or the CUDA-core GEMV")
     ap.add_argument("--round-case", default=None,
                     help="B:gamma -- time only the round's three calls on that high-concurrency-shaped case")
     ap.add_argument("--tv-rows", type=int, default=None,

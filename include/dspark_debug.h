@@ -44,6 +44,17 @@ int dspark_debug_phase_times(float* ms, int n);
  * co-resident).  Results are identical either way.  Process-wide flag. */
 dspark_status_t dspark_debug_force_phase_launches(int enable);
 
+/* Test hook: which path dspark_draft_block takes for bf16 weights with the
+ * Markov head (r % 64 == 0, r <= 256).  mode 0 (default): by batch size -- the
+ * tcgen05 engine at every B, since it measured faster than the CUDA-core GEMV
+ * path (W2 streamed once per position for all requests, L2-resident) down to
+ * B = 1; 1: always the tcgen05 engine; 2: the GEMV path wherever it applies
+ * (B <= 32), the calls it cannot take returning DSPARK_ERR_UNSUPPORTED.  Both paths draw the same tokens from the same
+ * Philox words; their logits differ only in the summation order of the
+ * rank-r product.  Process-wide flag; DSPARK_ERR_INVALID_ARGUMENT for other
+ * modes. */
+dspark_status_t dspark_debug_set_draft_path(int mode);
+
 /* Test hook for the bounded waits: one thread waits at the grid barrier kept
  * in a draft workspace (dspark_draft_block_workspace_size(1, 1, 1, 8) bytes,
  * 256-byte aligned) for an arrival that never comes, giving up after

@@ -54,6 +54,7 @@ _SIGNATURES = {
     "dspark_debug_enable_phase_timing": (_c_int, [_c_int]),
     "dspark_debug_phase_times": (_c_int, [_p, _c_int]),
     "dspark_debug_force_phase_launches": (_c_int, [_c_int]),
+    "dspark_debug_set_draft_path": (_c_int, [_c_int]),
     "dspark_debug_bounded_wait": (_c_int, [_p, _c_size, ctypes.c_uint64, _p]),
     "dspark_debug_exp_draws": (_c_int, [_p, _p, _c_i64, _p]),
     "dspark_debug_philox_rows": (_c_int, [_c_u64, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
@@ -443,6 +444,12 @@ def force_phase_launches(enable):
     """Test hook: the tensor-core draft path launches per position instead of
     its single cooperative launch."""
     _check("dspark_debug_force_phase_launches", load().dspark_debug_force_phase_launches(1 if enable else 0))
+
+
+def set_draft_path(mode):
+    """Test hook: 0 chooses the draft path by batch size, 1 always takes the
+    tcgen05 engine, 2 the CUDA-core GEMV path wherever it applies."""
+    _check("dspark_debug_set_draft_path", load().dspark_debug_set_draft_path(int(mode)))
 
 
 def bounded_wait(limit_ns, workspace=None, stream=None):

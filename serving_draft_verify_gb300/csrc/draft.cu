@@ -17,6 +17,7 @@
 // position a finalize kernel forms lse_d / logp_d and the confidence c_k and
 // survival a_k.
 #include "engine.cuh"
+#include "gemv.cuh"
 #include "../../include/dspark_debug.h"
 
 namespace dspark {
@@ -434,6 +435,14 @@ int simt_chunks(int V) {
 }
 
 bool g_force_phase_launches = false;
+// 0: choose by batch size; 1: always the tensor-core path; 2: the CUDA-core GEMV
+// path wherever it applies (test hook)
+int g_draft_path = 0;
+// Up to this many requests the bf16 Markov-head draft runs on the CUDA-core GEMV
+// path.  Measured on the Qwen3 shape (V 151936, r 256, gamma 7, T 0.7), the
+// tcgen05 engine was faster at every batch size from 1 to 32 (161 against 188 us
+// at B = 1, 176 against 675 us at B = 16), so the default never takes it.
+constexpr int kGemvMaxBatch = 0;
 
 dspark_status_t launch_winner(int B, int gamma, int V, int k, int32_t* x, DraftWs ws, cudaStream_t s) {
     draft_winner<<<(B + 255) / 256, 256, 0, s>>>(B, gamma, V, k, x, ws);
@@ -472,6 +481,25 @@ dspark_status_t draft_block_impl(int B, int gamma, int V, int H, int r, dspark_d
                     : launch_hproj<false>(M, H, r, ldw, col, hd_vec, h, hd->Wc, hd->hc, s);
         if (st != DSPARK_OK) return st;
     }
+    const bool gemv_ok = tcp && !hd && gemv::supported(dt, B, r);
+    if (gemv_ok && (g_draft_path == 2 || (g_draft_path == 0 && B <= kGemvMaxBatch))) {
+        // every position, x_gamma and the finalize in one cooperative launch
+        gemv::Params gp{};
+        gp.B = B; gp.gamma = gamma; gp.V = V; gp.H = H; gp.r = r;
+        gp.U = static_cast<const uint16_t*>(U); gp.W1 = static_cast<const uint16_t*>(W1);
+        gp.W2 = static_cast<const uint16_t*>(W2); gp.h = static_cast<const uint16_t*>(h);
+        gp.w = static_cast<const uint16_t*>(w); gp.bias = bias; gp.x0 = x0; gp.x = x;
+        gp.cscale = cscale; gp.greedy = greedy; gp.seed = seed;
+        gp.lse_d = lse_d; gp.logp_d = logp_d; gp.c = c; gp.a = a; gp.ws = ws;
+        if (g_timing.on) cudaEventRecord(g_timing.ev[0], s);
+        const dspark_status_t stg = gemv::launch(gp, gemv::grid_for(V), s);
+        if (g_timing.on) {
+            cudaEventRecord(g_timing.ev[1], s);
+            g_timing.recorded = 1;
+        }
+        return stg;
+    }
+    if (g_draft_path == 2) return DSPARK_ERR_UNSUPPORTED;
     CUtensorMap map;
     int nM = 1, P = 1, nchunk = 1;
     eng::TcParams p{};
@@ -696,6 +724,12 @@ extern "C" dspark_status_t dspark_debug_enable_phase_timing(int enable) {
     }
     g_timing.on = enable != 0;
     g_timing.recorded = 0;
+    return DSPARK_OK;
+}
+
+extern "C" dspark_status_t dspark_debug_set_draft_path(int mode) {
+    if (mode < 0 || mode > 2) return DSPARK_ERR_INVALID_ARGUMENT;
+    g_draft_path = mode;
     return DSPARK_OK;
 }
 
