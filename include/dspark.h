@@ -213,7 +213,7 @@ dspark_status_t dspark_verify(int B, int gamma, int V, int r, dspark_dtype_t dt,
  * sum_v min(p_d(v), p_t(v)), which is the same quantity.
  *
  *   d, t [rows][V] in `dt`; c_star [rows] float32.  Each row needs at least
- *   one finite logit.  rows == 0 launches nothing.  Requires V <= 163840.
+ *   one finite logit.  rows == 0 launches nothing.
  * ------------------------------------------------------------------------ */
 size_t dspark_accept_rate_tv_workspace_size(int64_t rows, int V);
 
@@ -360,7 +360,7 @@ dspark_status_t dspark_decode_rounds(int rounds, int pool, int B, int gamma, int
  *   NULL.  Every byte of d and t is read once; grad_d is written from
  *   registers in the same pass.
  *   A target id outside [0, V) sets DSPARK_ERR_DEVICE_CHECK (that row's ce is
- *   then +inf).  rows == 0 writes loss = 0.  Requires V <= 163840.
+ *   then +inf).  rows == 0 writes loss = 0.
  * ------------------------------------------------------------------------ */
 size_t dspark_training_loss_workspace_size(int64_t rows, int V);
 

@@ -114,7 +114,6 @@ def test_host_checks_of_the_other_entry_points(lib):
     assert loss(ws=None) == 1 and loss(ws=P(0x1010)) == 1        # workspace missing / not 256-byte aligned
     assert loss(ws_bytes=16) == 3
     assert loss(out=None) == 1                                  # no loss output
-    assert loss(V=163848) == 2
 
     r = lib.dspark_decode_rounds
     r.restype = i

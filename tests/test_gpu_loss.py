@@ -108,7 +108,7 @@ def _check_grad(got_gd, got_gc, d64, t64, target, s, omega, dtype, kw=None):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("V", [8, 1024, 5000, 151936])
+@pytest.mark.parametrize("V", [8, 1024, 5000, 151936, 262144])
 def test_loss_parity_seeded_rows(dsv, dtype, V):
     cfg = wl.scaled(wl.TV_TRAIN, V=V)
     rows = 37

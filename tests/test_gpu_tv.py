@@ -35,7 +35,7 @@ def _check(dsv, d, t):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("V", [8, 1024, 5000, 151936])
+@pytest.mark.parametrize("V", [8, 1024, 5000, 151936, 262144])
 def test_tv_parity_seeded_rows(dsv, dtype, V):
     cfg = wl.scaled(wl.TV_TRAIN, V=V)
     d, t = wl.make_tv_inputs(cfg, rows=37)
