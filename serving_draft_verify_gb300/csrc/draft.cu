@@ -438,10 +438,11 @@ bool g_force_phase_launches = false;
 // 0: choose by batch size; 1: always the tensor-core path; 2: the CUDA-core GEMV
 // path wherever it applies (test hook)
 int g_draft_path = 0;
-// Up to this many requests the bf16 Markov-head draft runs on the CUDA-core GEMV
-// path.  Measured on the Qwen3 shape (V 151936, r 256, gamma 7, T 0.7), the
-// tcgen05 engine was faster at every batch size from 1 to 32 (161 against 188 us
-// at B = 1, 176 against 675 us at B = 16), so the default never takes it.
+// Up to this many requests the bf16 Markov-head draft runs on the small-batch
+// GEMV path.  Measured on the Qwen3 shape (V 151936, r 256, gamma 7, T 0.7), the
+// tcgen05 engine was faster at every batch size from 1 to 64 (161 against 209 us
+// at B = 1, 176 against 239 us at B = 16, 274 against 531 us at B = 64), so the
+// default never takes it.
 constexpr int kGemvMaxBatch = 0;
 
 dspark_status_t launch_winner(int B, int gamma, int V, int k, int32_t* x, DraftWs ws, cudaStream_t s) {

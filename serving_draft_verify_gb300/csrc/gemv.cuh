@@ -1,27 +1,29 @@
-// The draft block's CUDA-core path for small batches (DeepSpec walkthrough,
-// section 3.2 stage two, `sample_block_tokens`; VanillaMarkovHead, eq. 5):
-// for k = 1..gamma, z_k[b][v] = U_k[b][v] + W2[v] . W1[x_{k-1}[b]], then the
-// Gumbel-max draw of x_k from softmax(z_k / T) -- the same computation as the
-// tcgen05 engine, for batches too small to fill its 128-row tiles.
+// The draft block's path for small batches (DeepSpec walkthrough, section 3.2
+// stage two, `sample_block_tokens`; VanillaMarkovHead, eq. 5): for k = 1..gamma,
+// z_k[b][v] = U_k[b][v] + W2[v] . W1[x_{k-1}[b]], then the Gumbel-max draw of x_k
+// from softmax(z_k / T) -- the same computation as the tcgen05 engine, for
+// batches too small to fill its 128-row tiles.
 //
 // Below a few dozen requests the rank-r contraction is a matrix-vector product
-// per request: each 512-byte row of W2 (r = 256 bf16) meets B rows of W1, so the
-// position streams W2 once (78 MB for the Qwen3 vocabulary, kept in L2 with the
-// evict-last policy so that the next position reads it from there) and the work
-// per byte is B r / 512 MACs.  One cooperative launch covers every position:
-//   * one CTA per SM owns a contiguous range of 64-token tiles (the partition
-//     the finalize maps tokens to, as for the other paths); a producer warp
-//     bulk-copies each tile's W2 rows (32 KB) and the B rows of U_k over it into
-//     a ring of four slots, running ahead across positions (neither depends
-//     on x);
-//   * each of 16 warps takes four tokens of a tile, eight lanes per token, each
-//     lane holding r / 8 of the row's weights in registers and reading the B
-//     rows W1[x_{k-1}] from shared memory, permuted so that the eight lanes of a
-//     token read 128 contiguous bytes;
-//   * the four tokens' dot products meet in shared memory, and lane b draws them
-//     for request b: y = (z + U) * cscale, key = y - log2(-ln u) with u from
-//     word v & 3 of Philox(counter (v >> 2, k, b, 0)) -- one Philox block per
-//     four tokens -- exactly the engine's draw;
+// per request: each 512-byte row of W2 (r = 256 bf16) meets B rows of W1, so a
+// position streams W2 once (78 MB for the Qwen3 vocabulary; it stays in L2 from
+// one position to the next) and does B r MACs per row.  One cooperative launch
+// covers every position:
+//   * one CTA per SM owns a contiguous range of 64-token tiles (the partition the
+//     finalize maps tokens to, as for the other paths); a producer warp loads
+//     each tile's W2 rows with TMA (4 boxes of 64 rows x 64 k, 128-byte swizzle)
+//     and bulk-copies U_k of every request over the tile, into a four-slot ring,
+//     running ahead across positions (neither depends on x);
+//   * the product runs as warp-level bf16 MMAs with float32 accumulation
+//     (m16n8k16: 16 tokens x 8 requests x 16 k): warp w takes the tile's 16-token
+//     block w mod 4 and the 8-request blocks w / 4, w / 4 + 4, its A fragments
+//     read from the swizzled tile with ldmatrix, its B fragments (the requests'
+//     W1 rows, in fragment order) from shared memory, built once per position;
+//   * s = z + U_k goes to shared memory, and the CTA's threads then draw: thread
+//     (b, g) takes four consecutive tokens of request b, y = s * cscale, key =
+//     y - log2(-ln u) with u from word v & 3 of Philox(counter (v >> 2, k, b, 0))
+//     -- exactly the engine's draw -- and the 16 threads of a request merge
+//     their (max, sum) and best token at the end of the position;
 //   * per position every CTA publishes its (max, sum) partials, its best token's
 //     y and its winner (atomicMax), then meets the others at a grid barrier;
 //     x_{k-1} is the published winner.  After the last position the same launch
@@ -29,6 +31,7 @@
 //     confidence c_k and the survival a_k).
 #pragma once
 #include "engine.cuh"
+#include "tc.cuh"
 
 namespace dspark {
 namespace gemv {
@@ -44,13 +47,17 @@ using eng::ld_u32x4;
 constexpr int kWarps = 16;                       // compute warps; warp kWarps is the producer
 constexpr int kCompute = kWarps * 32;
 constexpr int kThreads = kCompute + 32;
-constexpr int kMaxB = 32;                        // one request per lane in the draw
+constexpr int kMaxB = 64;                        // 8 request blocks of 8
+constexpr int kMaxNB = kMaxB / 8;
 constexpr int kMaxR = 256;
-constexpr int kTile = 4 * kWarps;                // tokens per tile (the chunk partition's unit)
-constexpr int kStages = 4;                       // W2 tile ring
-constexpr size_t kTileBytes = static_cast<size_t>(kTile) * kMaxR * 2;     // W2 rows of a tile
-constexpr size_t kStageBytes = kTileBytes + static_cast<size_t>(kMaxB) * kTile * 2;   // + U_k of every request
-constexpr size_t kSmem = kStages * kStageBytes + static_cast<size_t>(kMaxB) * kMaxR * 4;   // ring | W1 rows
+constexpr int kTile = 64;                        // tokens per tile (the chunk partition's unit)
+constexpr int kStages = 4;                       // tile ring
+constexpr size_t kBoxBytes = 64 * 128;           // one TMA box: 64 rows x 64 k of bf16, swizzled
+constexpr size_t kW2Bytes = kMaxR / 64 * kBoxBytes;                 // a tile's W2 rows (32 KB)
+constexpr size_t kStageBytes = kW2Bytes + static_cast<size_t>(kMaxB) * kTile * 2;   // + U_k of every request
+constexpr size_t kFragBytes = static_cast<size_t>(kMaxNB) * (kMaxR / 16) * 32 * 8;  // B fragments
+constexpr size_t kZBytes = static_cast<size_t>(kMaxB) * kTile * 4;  // s = z + U of a tile
+constexpr size_t kSmem = 1024 + kStages * kStageBytes + kFragBytes + kZBytes;
 
 struct Params {
     int B, gamma, V, H, r;
@@ -72,46 +79,54 @@ struct Params {
     eng::Ws ws;
 };
 
-// Element j = 64 i + 8 s + 4 hh + q of a W1 row (i < r / 64, s < 8, hh < 2,
-// q < 4) sits at float ((2 i + hh) 8 + s) 4 + q of its shared-memory row: lane s
-// of a token reads its two 16-byte halves at (2 i + hh) 128 + 16 s bytes.
-__device__ __forceinline__ int eperm(int j) {
-    const int i = j >> 6, s = (j >> 3) & 7, hh = (j >> 2) & 1, q = j & 3;
-    return (((2 * i + hh) << 3) + s) * 4 + q;
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& a0, uint32_t& a1, uint32_t& a2,
+                                            uint32_t& a3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                 : "r"(addr));
+}
+// D += A B for one m16n8k16 bf16 tile, float32 accumulators.
+__device__ __forceinline__ void mma_bf16_16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-draft_gemv(Params p) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t* ring = smem;                                  // [kStages]: W2 [kTile][r] | U_k [B][kTile], bf16
-    float* es = reinterpret_cast<float*>(smem + kStages * kStageBytes);   // [B][r] float32, permuted rows
-    __shared__ __align__(16) float zt[kWarps][kMaxB][4];  // a warp's four tokens' dot products
-    __shared__ float rm[kWarps][kMaxB], rs[kWarps][kMaxB], rk[kWarps][kMaxB], ry[kWarps][kMaxB];
-    __shared__ int ri[kWarps][kMaxB];
+draft_gemv(const __grid_constant__ CUtensorMap tmW2, Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);   // 1024-byte aligned for the swizzle
+    uint8_t* ring = smem;                                 // [kStages]: W2 boxes | U_k [B][kTile] bf16
+    uint2* frag = reinterpret_cast<uint2*>(smem + kStages * kStageBytes);   // [nb][k16][lane]
+    float* zs = reinterpret_cast<float*>(smem + kStages * kStageBytes + kFragBytes);   // [B][kTile]
     __shared__ int s_prev[kMaxB];
     __shared__ int s_fail;
     __shared__ int s_ring_dead;                           // a tile wait timed out: the producer stopped
     __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
     StatusBlock* st = p.ws.status;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int t = lane >> 3, s = lane & 7;                // token of the warp's four, r-slice of the lane
-    const int nq = p.r / 64;                              // 16-byte pieces per lane (1..4)
+    const int nk16 = p.r / 16;                            // k steps of 16
+    const int nslab = p.r / 64;                           // TMA boxes per tile
+    const int NB = (p.B + 7) / 8;
     const int chunk = blockIdx.x, nchunk = gridDim.x;
     const int ntiles = (p.V + kTile - 1) / kTile;
     const int j_lo = static_cast<int>(static_cast<long long>(chunk) * ntiles / nchunk);
     const int j_hi = static_cast<int>(static_cast<long long>(chunk + 1) * ntiles / nchunk);
-    const size_t row_bytes = static_cast<size_t>(p.r) * 2;
     const uint64_t keep = policy_evict_last(), drop = policy_evict_first();
     if (tid == 0) {
         s_fail = 0;
         s_ring_dead = 0;
         for (int i = 0; i < kStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kWarps); }
         fence_mbar_init();
+        tc::prefetch_tmap(&tmW2);
     }
     __syncthreads();
 
     if (warp == kWarps) {
-        // ------------------------------------------------ producer: W2 tiles
+        // ------------------------------------------------ producer: W2 and U tiles
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
@@ -120,13 +135,14 @@ draft_gemv(Params p) {
                 for (int j = j_lo; j < j_hi; ++j) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u)) { failed = true; break; }
                     const int rows = min(kTile, p.V - j * kTile);   // a multiple of 8 (V % 8 == 0)
-                    const uint32_t wbytes = static_cast<uint32_t>(rows * row_bytes), ubytes = rows * 2u;
+                    const uint32_t ubytes = rows * 2u;
                     uint8_t* dst = ring + stage * kStageBytes;
-                    mbar_arrive_expect_tx(&full[stage], wbytes + p.B * ubytes);
-                    bulk_g2s(dst, reinterpret_cast<const uint8_t*>(p.W2) + j * kTile * row_bytes, wbytes,
-                             &full[stage], keep);
+                    // TMA counts the whole box (rows past V are zero-filled)
+                    mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(nslab * kBoxBytes) + p.B * ubytes);
+                    for (int sl = 0; sl < nslab; ++sl)
+                        tc::tma_load_2d(dst + sl * kBoxBytes, &tmW2, sl * 64, j * kTile, &full[stage], keep);
                     for (int b = 0; b < p.B; ++b)             // U_k[b] over the tile's tokens
-                        bulk_g2s(dst + kTileBytes + b * (kTile * 2),
+                        bulk_g2s(dst + kW2Bytes + b * (kTile * 2),
                                  p.U + (static_cast<size_t>(b) * p.gamma + (k - 1)) * p.V + j * kTile, ubytes,
                                  &full[stage], drop);
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -160,11 +176,16 @@ draft_gemv(Params p) {
         }
         return static_cast<int>(idx);
     };
+    // the draw's items: thread (b, g) takes request b, tokens 4 g .. 4 g + 3 of each
+    // tile; up to two requests per thread (b and b + 32)
+    const int gq = tid & 15;
+    const int nreq = (tid >> 4) + 32 < p.B ? 2 : ((tid >> 4) < p.B ? 1 : 0);
+    const int mb = warp & 3;                              // this warp's 16-token block of a tile
     int cstage = 0;
     uint32_t cphase = 0;
 
     for (int k = 1; k <= p.gamma; ++k) {
-        // ------------------------------------------------ x_{k-1} and its W1 rows
+        // ------------------------------------------------ x_{k-1}; the B fragments
         if (k > 1) wait_all();                            // every CTA published position k-1
         if (tid < p.B) {
             const int b = tid;
@@ -178,26 +199,31 @@ draft_gemv(Params p) {
             s_prev[b] = tok;
         }
         csync();
-        for (int item = tid; item < p.B * (p.r / 8); item += kCompute) {
-            const int b = item / (p.r / 8), j8 = item % (p.r / 8);
-            uint32_t wv[4];
-            ld_u32x4(p.W1 + static_cast<size_t>(s_prev[b]) * p.r + j8 * 8, wv, keep);
-            float* dst = es + b * p.r;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                dst[eperm(j8 * 8 + 2 * q)] = bf16lo(wv[q]);
-                dst[eperm(j8 * 8 + 2 * q + 1)] = bf16hi(wv[q]);
+        // fragment (nb, kk, lane): request n = 8 nb + lane / 4, k = 16 kk + 2 (lane % 4) (+ 8)
+        for (int item = tid; item < NB * nk16 * 32; item += kCompute) {
+            const int ln = item & 31, kk = (item >> 5) % nk16, nb = (item >> 5) / nk16;
+            const int n = nb * 8 + (ln >> 2), kq = kk * 16 + 2 * (ln & 3);
+            uint2 f = make_uint2(0u, 0u);
+            if (n < p.B) {
+                const uint32_t* row = reinterpret_cast<const uint32_t*>(p.W1 + static_cast<size_t>(s_prev[n]) * p.r);
+                f = make_uint2(__ldg(row + kq / 2), __ldg(row + kq / 2 + 4));
             }
+            frag[(nb * (kMaxR / 16) + kk) * 32 + ln] = f;
         }
         csync();
 
-        // ------------------------------------------------ this CTA's tiles
-        const PhiloxRow pr = philox_row_setup(p.seed, static_cast<uint32_t>(k), static_cast<uint32_t>(lane),
-                                              kStreamDraftToken);
-        Best best{-INFINITY, 0x7FFFFFFF, 0.f};
-        float M = -INFINITY, S = 0.f;
+        PhiloxRow pr[2];
+        Best best[2];
+        float M[2], S[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            pr[q] = philox_row_setup(p.seed, static_cast<uint32_t>(k), static_cast<uint32_t>((tid >> 4) + 32 * q),
+                                     kStreamDraftToken);
+            best[q] = Best{-INFINITY, 0x7FFFFFFF, 0.f};
+            M[q] = -INFINITY;
+            S[q] = 0.f;
+        }
         for (int j = j_lo; j < j_hi; ++j) {
-            const int v0 = j * kTile + 4 * warp;          // this warp's four tokens
             // every issued tile is waited for (no copy may be left in flight at exit),
             // after a failed grid barrier too; only a ring that stopped is skipped
             bool bad = false;
@@ -208,105 +234,106 @@ draft_gemv(Params p) {
                 s_ring_dead = 1;
                 s_fail = 1;
             }
-            // this lane's r / 8 weights of token v0 + t, as float32 pairs
-            unsigned long long wf[16];
-            {
-                const uint8_t* row = ring + cstage * kStageBytes + (4 * warp + t) * row_bytes;
+            const uint8_t* stg = ring + cstage * kStageBytes;
+            // z for tokens 16 mb .. + 15 and request blocks warp / 4, warp / 4 + 4
+            const int nb0 = warp >> 2;
+            if (s_fail == 0 && nb0 < NB) {
+                const bool two = nb0 + 4 < NB;
+                float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+                const int arow = mb * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;   // ldmatrix row of this lane
+                for (int kk = 0; kk < nk16; ++kk) {
+                    const int chk = (kk & 3) * 2 + (lane >> 4);                    // 16-byte chunk in the box row
+                    const uint32_t addr = smem_u32(stg + (kk >> 2) * kBoxBytes + arow * 128 +
+                                                   ((chk ^ (arow & 7)) << 4));
+                    uint32_t a0, a1, a2, a3;
+                    ldmatrix_x4(addr, a0, a1, a2, a3);
+                    const uint2 f0 = frag[(nb0 * (kMaxR / 16) + kk) * 32 + lane];
+                    mma_bf16_16816(c0, a0, a1, a2, a3, f0.x, f0.y);
+                    if (two) {
+                        const uint2 f1 = frag[((nb0 + 4) * (kMaxR / 16) + kk) * 32 + lane];
+                        mma_bf16_16816(c1, a0, a1, a2, a3, f1.x, f1.y);
+                    }
+                }
+                // s = z + U_k: rows g, g + 8 of the block, requests 2 (lane % 4) (+ 1) of each request block
+                const int g = lane >> 2, cq = 2 * (lane & 3);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    uint4 q4 = make_uint4(0u, 0u, 0u, 0u);
-                    if (i < nq) q4 = *reinterpret_cast<const uint4*>(row + i * 128 + s * 16);
-                    wf[4 * i] = eng::f2pack(bf16lo(q4.x), bf16hi(q4.x));
-                    wf[4 * i + 1] = eng::f2pack(bf16lo(q4.y), bf16hi(q4.y));
-                    wf[4 * i + 2] = eng::f2pack(bf16lo(q4.z), bf16hi(q4.z));
-                    wf[4 * i + 3] = eng::f2pack(bf16lo(q4.w), bf16hi(q4.w));
+                for (int h = 0; h < 2; ++h) {
+                    if (h == 1 && !two) break;
+                    const float* c = h ? c1 : c0;
+                    const int nbase = (nb0 + 4 * h) * 8 + cq;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int n = nbase + (e & 1), row = mb * 16 + g + (e >> 1) * 8;
+                        if (n < p.B) {
+                            const uint16_t u = *reinterpret_cast<const uint16_t*>(stg + kW2Bytes + n * (kTile * 2) +
+                                                                                  row * 2);
+                            zs[n * kTile + row] = c[e] + __uint_as_float(static_cast<uint32_t>(u) << 16);
+                        }
+                    }
                 }
             }
-            // U_k of request `lane` at the warp's four tokens
-            uint2 u2 = make_uint2(0u, 0u);
-            if (lane < p.B)
-                u2 = *reinterpret_cast<const uint2*>(ring + cstage * kStageBytes + kTileBytes + lane * (kTile * 2) +
-                                                     (4 * warp) * 2);
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[cstage]);   // this warp's rows are in registers
+            if (lane == 0) mbar_arrive(&empty[cstage]);   // this warp is done with the slot
             if (++cstage == kStages) { cstage = 0; cphase ^= 1u; }
-            if (s_fail != 0) continue;
-            // dot products with every request's W1 row; the eight lanes of a token meet by xor
-            for (int b = 0; b < p.B; ++b) {
-                const float4* er = reinterpret_cast<const float4*>(es + b * p.r);
-                unsigned long long acc0 = eng::f2pack(0.f, 0.f), acc1 = acc0;   // two chains
+            csync();                                      // the tile's s is complete
+            if (s_fail == 0) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    if (i < nq) {
-                        const float4 e0 = er[(2 * i) * 8 + s], e1 = er[(2 * i + 1) * 8 + s];
-                        acc0 = eng::f2fma(wf[4 * i], eng::f2pack(e0.x, e0.y), acc0);
-                        acc1 = eng::f2fma(wf[4 * i + 1], eng::f2pack(e0.z, e0.w), acc1);
-                        acc0 = eng::f2fma(wf[4 * i + 2], eng::f2pack(e1.x, e1.y), acc0);
-                        acc1 = eng::f2fma(wf[4 * i + 3], eng::f2pack(e1.z, e1.w), acc1);
-                    }
-                }
-                float lo, hi;
-                eng::f2unpack(eng::f2add(acc0, acc1), lo, hi);
-                float dot = lo + hi;
-                dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-                dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-                dot += __shfl_xor_sync(0xffffffffu, dot, 4);
-                if (s == (b & 7)) zt[warp][b][t] = dot;
-            }
-            __syncwarp();
-            if (lane < p.B) {
-                const int b = lane;
-                const float4 z4 = *reinterpret_cast<const float4*>(&zt[warp][b][0]);
-                float y[4] = {(z4.x + bf16lo(u2.x)) * p.cscale, (z4.y + bf16hi(u2.x)) * p.cscale,
-                              (z4.z + bf16lo(u2.y)) * p.cscale, (z4.w + bf16hi(u2.y)) * p.cscale};
+                for (int q = 0; q < 2; ++q) {
+                    if (q >= nreq) break;
+                    const int b = (tid >> 4) + 32 * q, v0 = j * kTile + 4 * gq;
+                    const float4 s4 = *reinterpret_cast<const float4*>(zs + b * kTile + 4 * gq);
+                    float y[4] = {s4.x * p.cscale, s4.y * p.cscale, s4.z * p.cscale, s4.w * p.cscale};
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    if (v0 + q >= p.V) y[q] = -INFINITY;
-                if (p.greedy) {
+                    for (int e = 0; e < 4; ++e)
+                        if (v0 + e >= p.V) y[e] = -INFINITY;
+                    if (p.greedy) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) best_take(best, y[q], v0 + q, y[q]);
-                } else {
-                    const float m4 = fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3]));
-                    if (m4 > -INFINITY) {
-                        const float s4 = fast_exp2(y[0] - m4) + fast_exp2(y[1] - m4) + fast_exp2(y[2] - m4) +
-                                         fast_exp2(y[3] - m4);
-                        lse_merge(M, S, m4, s4);
-                        const U4 pw = philox_row(pr, static_cast<uint32_t>(v0) >> 2);
-                        const uint32_t wd[4] = {pw.x, pw.y, pw.z, pw.w};
+                        for (int e = 0; e < 4; ++e) best_take(best[q], y[e], v0 + e, y[e]);
+                    } else {
+                        const float m4 = fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3]));
+                        if (m4 > -INFINITY) {
+                            const float s4s = fast_exp2(y[0] - m4) + fast_exp2(y[1] - m4) + fast_exp2(y[2] - m4) +
+                                              fast_exp2(y[3] - m4);
+                            lse_merge(M[q], S[q], m4, s4s);
+                            const U4 pw = philox_row(pr[q], static_cast<uint32_t>(v0) >> 2);
+                            const uint32_t wd[4] = {pw.x, pw.y, pw.z, pw.w};
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            if (y[q] > -INFINITY) best_take(best, y[q] - fast_log2(exp_draw(wd[q])), v0 + q, y[q]);
+                            for (int e = 0; e < 4; ++e)
+                                if (y[e] > -INFINITY)
+                                    best_take(best[q], y[e] - fast_log2(exp_draw(wd[e])), v0 + e, y[e]);
+                        }
                     }
                 }
             }
-            __syncwarp();                                 // zt is rewritten by the next tile
+            csync();                                      // zs is rewritten by the next tile
         }
 
         // ------------------------------------------------ this CTA's partials
-        if (lane < p.B) {
-            rm[warp][lane] = M;
-            rs[warp][lane] = S;
-            rk[warp][lane] = best.key;
-            ri[warp][lane] = best.idx;
-            ry[warp][lane] = best.y;
-        }
-        csync();
-        if (tid < p.B && s_fail == 0) {
-            const int b = tid;
-            Best cb{-INFINITY, 0x7FFFFFFF, 0.f};
-            float m = -INFINITY, sum = 0.f;
-            for (int wi = 0; wi < kWarps; ++wi) {
-                best_take(cb, rk[wi][b], ri[wi][b], ry[wi][b]);
-                lse_merge(m, sum, rm[wi][b], rs[wi][b]);
+        // the 16 threads of a request (a half warp) merge in a fixed order
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) {
+                const float ok = __shfl_xor_sync(0xffffffffu, best[q].key, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, best[q].idx, o);
+                const float oy = __shfl_xor_sync(0xffffffffu, best[q].y, o);
+                const float om = __shfl_xor_sync(0xffffffffu, M[q], o);
+                const float os = __shfl_xor_sync(0xffffffffu, S[q], o);
+                best_take(best[q], ok, oi, oy);
+                lse_merge(M[q], S[q], om, os);
             }
-            const size_t slot = static_cast<size_t>(k - 1) * p.B + b;
-            if (!p.greedy) {
-                p.ws.part[slot * kMaxChunks + chunk] = make_float2(m, sum);
-                p.ws.ybest[slot * kMaxChunks + chunk] = cb.y;
+            if (gq == 0 && q < nreq && s_fail == 0) {
+                const int b = (tid >> 4) + 32 * q;
+                const size_t slot = static_cast<size_t>(k - 1) * p.B + b;
+                if (!p.greedy) {
+                    p.ws.part[slot * kMaxChunks + chunk] = make_float2(M[q], S[q]);
+                    p.ws.ybest[slot * kMaxChunks + chunk] = best[q].y;
+                }
+                if (best[q].key > -INFINITY)
+                    atomicMax(&p.ws.words[slot], pack_key(best[q].key, static_cast<uint32_t>(best[q].idx)));
             }
-            if (cb.key > -INFINITY) atomicMax(&p.ws.words[slot], pack_key(cb.key, static_cast<uint32_t>(cb.idx)));
         }
-        arrive();                                         // position k published (rm .. ri are reused after a barrier)
+        arrive();                                         // position k published
     }
 
     // ---------------------------------------------------- x_gamma and finalize
@@ -335,6 +362,19 @@ draft_gemv(Params p) {
     }
 }
 
+// 2-D map over W2 [V][r] bf16: box {64 k, 64 rows}, 128-byte swizzle, zero fill.
+inline bool encode_w2_map(CUtensorMap* map, const void* W2, int V, int r) {
+    auto enc = eng::tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(r), static_cast<cuuint64_t>(V)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(r) * 2};
+    const cuuint32_t box[2] = {64, kTile};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W2), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The path applies to bf16 weights with r a multiple of 64 up to 256 (the
 // engine's ranks) and B up to kMaxB.
 inline bool supported(dspark_dtype_t dt, int B, int r) {
@@ -357,17 +397,19 @@ inline dspark_status_t launch(const Params& p, int grid, cudaStream_t s) {
                                         static_cast<int>(kSmem));
         }) != cudaSuccess)
         return DSPARK_ERR_CUDA;
+    CUtensorMap map;
+    if (!encode_w2_map(&map, p.W2, p.V, p.r)) return DSPARK_ERR_CUDA;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kStages * kStageBytes + static_cast<size_t>(p.B) * p.r * 4;
+    cfg.dynamicSmemBytes = kSmem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, draft_gemv, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, draft_gemv, map, p) != cudaSuccess) {
         cudaGetLastError();
         return DSPARK_ERR_CUDA;
     }

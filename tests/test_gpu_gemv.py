@@ -1,9 +1,9 @@
-"""GPU parity of the draft block's CUDA-core GEMV path (small batches) and of the
-tcgen05 engine against the oracle at the same batch sizes (B = 1 .. 32), and of
-the two paths against each other.
+"""GPU parity of the draft block's small-batch GEMV path and of the tcgen05
+engine against the oracle at the same batch sizes (B = 1 .. 64), and of the
+two paths against each other.
 
-The GEMV path forms z = U_k + W2 . W1[x_{k-1}] with float32 sums of another
-order than the tensor cores; tokens must match the oracle exactly except
+The GEMV path forms z = U_k + W2 . W1[x_{k-1}] with warp-level MMAs whose
+float32 sums run in another order than the tcgen05 engine's; tokens must match the oracle exactly except
 decisions whose oracle margin is below 1e-4 (counted and reported), and the
 float outputs within the bf16 bar (2e-3)."""
 import numpy as np
@@ -38,7 +38,9 @@ CASES = [
     ("B4_r256", dict(B=4, gamma=7, V=6000, H=64)),
     ("B16_r256", dict(B=16, gamma=5, V=4000, H=64)),
     ("B17_r256", dict(B=17, gamma=3, V=3000, H=64)),
-    ("B32_r256", dict(B=32, gamma=3, V=2056, H=32)),                 # the path's largest batch, V % 32 = 8
+    ("B32_r256", dict(B=32, gamma=3, V=2056, H=32)),                 # V % 64 = 8: a ragged last tile
+    ("B40_r128", dict(B=40, gamma=3, V=3000, H=32, r=128)),          # two requests per drawing thread
+    ("B64_r256", dict(B=64, gamma=2, V=2048, H=32)),                 # the path's largest batch
     ("B5_r64", dict(B=5, gamma=4, V=1000, H=32, r=64)),
     ("B3_r192", dict(B=3, gamma=6, V=1544, H=32, r=192)),
 ]
@@ -101,7 +103,7 @@ def test_default_path_is_the_measured_faster_one(dsv):
 
 
 def test_gemv_unsupported_shapes_report(dsv):
-    cfg = wl.scaled(wl.QWEN3_8B, B=33, gamma=2, V=1000, H=32)
+    cfg = wl.scaled(wl.QWEN3_8B, B=65, gamma=2, V=1000, H=32)
     inp = wl.make_draft_inputs(cfg)
     with pytest.raises(RuntimeError):
         run(dsv, inp, 2)
