@@ -448,7 +448,7 @@ def force_phase_launches(enable):
 
 def set_draft_path(mode):
     """Test hook: 0 chooses the draft path by batch size, 1 always takes the
-    tcgen05 engine, 2 the small-batch GEMV path wherever it applies (B <= 64)."""
+    tcgen05 engine, 2 the small-batch GEMV path wherever it applies (B <= 16)."""
     _check("dspark_debug_set_draft_path", load().dspark_debug_set_draft_path(int(mode)))
 
 

@@ -439,11 +439,11 @@ bool g_force_phase_launches = false;
 // path wherever it applies (test hook)
 int g_draft_path = 0;
 // Up to this many requests the bf16 Markov-head draft runs on the small-batch
-// GEMV path.  Measured on the Qwen3 shape (V 151936, r 256, gamma 7, T 0.7), the
-// tcgen05 engine was faster at every batch size from 1 to 64 (161 against 209 us
-// at B = 1, 176 against 239 us at B = 16, 274 against 531 us at B = 64), so the
-// default never takes it.
-constexpr int kGemvMaxBatch = 0;
+// GEMV path.  Measured on the Qwen3 shape (V 151936, r 256, gamma 7, T 0.7):
+//   B            1     2     4     8     9    12    16
+//   GEMV path  122   125   133   149   170   186   204 us
+//   tcgen05    162   166   167   172   174   176   178 us
+constexpr int kGemvMaxBatch = 9;
 
 dspark_status_t launch_winner(int B, int gamma, int V, int k, int32_t* x, DraftWs ws, cudaStream_t s) {
     draft_winner<<<(B + 255) / 256, 256, 0, s>>>(B, gamma, V, k, x, ws);
@@ -493,7 +493,7 @@ dspark_status_t draft_block_impl(int B, int gamma, int V, int H, int r, dspark_d
         gp.cscale = cscale; gp.greedy = greedy; gp.seed = seed;
         gp.lse_d = lse_d; gp.logp_d = logp_d; gp.c = c; gp.a = a; gp.ws = ws;
         if (g_timing.on) cudaEventRecord(g_timing.ev[0], s);
-        const dspark_status_t stg = gemv::launch(gp, gemv::grid_for(V), s);
+        const dspark_status_t stg = gemv::launch(gp, gemv::grid_for(V), in_host_memory(U), s);
         if (g_timing.on) {
             cudaEventRecord(g_timing.ev[1], s);
             g_timing.recorded = 1;

@@ -47,7 +47,8 @@ using eng::ld_u32x4;
 constexpr int kWarps = 16;                       // compute warps; warp kWarps is the producer
 constexpr int kCompute = kWarps * 32;
 constexpr int kThreads = kCompute + 32;
-constexpr int kMaxB = 64;                        // 8 request blocks of 8
+constexpr int kGroups = 4;                       // warp groups, each with its own ring slot and tiles
+constexpr int kMaxB = 16;                        // 2 request blocks of 8
 constexpr int kMaxNB = kMaxB / 8;
 constexpr int kMaxR = 256;
 constexpr int kTile = 64;                        // tokens per tile (the chunk partition's unit)
@@ -56,7 +57,7 @@ constexpr size_t kBoxBytes = 64 * 128;           // one TMA box: 64 rows x 64 k 
 constexpr size_t kW2Bytes = kMaxR / 64 * kBoxBytes;                 // a tile's W2 rows (32 KB)
 constexpr size_t kStageBytes = kW2Bytes + static_cast<size_t>(kMaxB) * kTile * 2;   // + U_k of every request
 constexpr size_t kFragBytes = static_cast<size_t>(kMaxNB) * (kMaxR / 16) * 32 * 8;  // B fragments
-constexpr size_t kZBytes = static_cast<size_t>(kMaxB) * kTile * 4;  // s = z + U of a tile
+constexpr size_t kZBytes = static_cast<size_t>(kGroups) * kMaxB * kTile * 4;   // s = z + U, a tile per group
 constexpr size_t kSmem = 1024 + kStages * kStageBytes + kFragBytes + kZBytes;
 
 struct Params {
@@ -94,6 +95,9 @@ __device__ __forceinline__ void mma_bf16_16816(float* c, uint32_t a0, uint32_t a
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// kUHost: U in page-locked host memory, read with loads (bulk copies read device
+// memory only).
+template <bool kUHost>
 __global__ void __launch_bounds__(kThreads, 1)
 draft_gemv(const __grid_constant__ CUtensorMap tmW2, Params p) {
     extern __shared__ uint8_t smem_raw[];
@@ -101,8 +105,10 @@ draft_gemv(const __grid_constant__ CUtensorMap tmW2, Params p) {
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);   // 1024-byte aligned for the swizzle
     uint8_t* ring = smem;                                 // [kStages]: W2 boxes | U_k [B][kTile] bf16
     uint2* frag = reinterpret_cast<uint2*>(smem + kStages * kStageBytes);   // [nb][k16][lane]
-    float* zs = reinterpret_cast<float*>(smem + kStages * kStageBytes + kFragBytes);   // [B][kTile]
+    float* zs = reinterpret_cast<float*>(smem + kStages * kStageBytes + kFragBytes);   // [group][B][kTile]
     __shared__ int s_prev[kMaxB];
+    __shared__ float pm[kGroups][kMaxB], ps[kGroups][kMaxB], pk[kGroups][kMaxB], py[kGroups][kMaxB];
+    __shared__ int pi[kGroups][kMaxB];
     __shared__ int s_fail;
     __shared__ int s_ring_dead;                           // a tile wait timed out: the producer stopped
     __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
@@ -119,7 +125,7 @@ draft_gemv(const __grid_constant__ CUtensorMap tmW2, Params p) {
     if (tid == 0) {
         s_fail = 0;
         s_ring_dead = 0;
-        for (int i = 0; i < kStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kWarps); }
+        for (int i = 0; i < kStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kWarps / kGroups); }
         fence_mbar_init();
         tc::prefetch_tmap(&tmW2);
     }
@@ -138,10 +144,11 @@ draft_gemv(const __grid_constant__ CUtensorMap tmW2, Params p) {
                     const uint32_t ubytes = rows * 2u;
                     uint8_t* dst = ring + stage * kStageBytes;
                     // TMA counts the whole box (rows past V are zero-filled)
-                    mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(nslab * kBoxBytes) + p.B * ubytes);
+                    const uint32_t utx = kUHost ? 0u : p.B * ubytes;
+                    mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(nslab * kBoxBytes) + utx);
                     for (int sl = 0; sl < nslab; ++sl)
                         tc::tma_load_2d(dst + sl * kBoxBytes, &tmW2, sl * 64, j * kTile, &full[stage], keep);
-                    for (int b = 0; b < p.B; ++b)             // U_k[b] over the tile's tokens
+                    for (int b = 0; b < (kUHost ? 0 : p.B); ++b)   // U_k[b] over the tile's tokens
                         bulk_g2s(dst + kW2Bytes + b * (kTile * 2),
                                  p.U + (static_cast<size_t>(b) * p.gamma + (k - 1)) * p.V + j * kTile, ubytes,
                                  &full[stage], drop);
@@ -176,13 +183,19 @@ draft_gemv(const __grid_constant__ CUtensorMap tmW2, Params p) {
         }
         return static_cast<int>(idx);
     };
-    // the draw's items: thread (b, g) takes request b, tokens 4 g .. 4 g + 3 of each
-    // tile; up to two requests per thread (b and b + 32)
-    const int gq = tid & 15;
-    const int nreq = (tid >> 4) + 32 < p.B ? 2 : ((tid >> 4) < p.B ? 1 : 0);
-    const int mb = warp & 3;                              // this warp's 16-token block of a tile
-    int cstage = 0;
-    uint32_t cphase = 0;
+    // warp group grp (warps 4 grp .. 4 grp + 3) owns ring slot grp: tile i of a
+    // position is the (n0 + i)-th tile the producer loads (n0 = (k - 1) T), so it
+    // lands in slot (n0 + i) mod 4 and the group of that slot takes it
+    const int grp = warp >> 2, w4 = warp & 3, t128 = tid & 127;
+    auto gsync = [grp] { asm volatile("bar.sync %0, %1;" ::"r"(2 + grp), "n"(kCompute / kGroups) : "memory"); };
+    // the draw's items in the group: thread (b, g) takes request b (and b + 8),
+    // tokens 4 g .. 4 g + 3 of the tile
+    const int gq = t128 & 15, bq = t128 >> 4;
+    const int nreq = bq + 8 < p.B ? 2 : (bq < p.B ? 1 : 0);
+    const int T = j_hi - j_lo;
+    uint32_t cphase = 0;                                  // parity of this group's next wait on its slot
+    float* zsg = zs + grp * (kMaxB * kTile);
+    const uint8_t* stg = ring + grp * kStageBytes;
 
     for (int k = 1; k <= p.gamma; ++k) {
         // ------------------------------------------------ x_{k-1}; the B fragments
@@ -217,71 +230,72 @@ draft_gemv(const __grid_constant__ CUtensorMap tmW2, Params p) {
         float M[2], S[2];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-            pr[q] = philox_row_setup(p.seed, static_cast<uint32_t>(k), static_cast<uint32_t>((tid >> 4) + 32 * q),
+            pr[q] = philox_row_setup(p.seed, static_cast<uint32_t>(k), static_cast<uint32_t>(bq + 8 * q),
                                      kStreamDraftToken);
             best[q] = Best{-INFINITY, 0x7FFFFFFF, 0.f};
             M[q] = -INFINITY;
             S[q] = 0.f;
         }
-        for (int j = j_lo; j < j_hi; ++j) {
+        const int n0 = static_cast<int>((static_cast<long long>(k - 1) * T) % kGroups);
+        for (int i = (grp - n0 + kGroups) % kGroups; i < T; i += kGroups) {
+            const int j = j_lo + i;
             // every issued tile is waited for (no copy may be left in flight at exit),
             // after a failed grid barrier too; only a ring that stopped is skipped
             bool bad = false;
-            if (s_ring_dead == 0) bad = !mbar_wait(&full[cstage], cphase);
+            if (s_ring_dead == 0) bad = !mbar_wait(&full[grp], cphase);
+            cphase ^= 1u;
             bad = __any_sync(0xffffffffu, bad);
             if (bad && lane == 0) {
                 set_status(st, DSPARK_ERR_TIMEOUT, 16);
                 s_ring_dead = 1;
                 s_fail = 1;
             }
-            const uint8_t* stg = ring + cstage * kStageBytes;
-            // z for tokens 16 mb .. + 15 and request blocks warp / 4, warp / 4 + 4
-            const int nb0 = warp >> 2;
-            if (s_fail == 0 && nb0 < NB) {
-                const bool two = nb0 + 4 < NB;
-                float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-                const int arow = mb * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;   // ldmatrix row of this lane
+            // z for tokens 16 w4 .. + 15 and every request block
+            if (s_fail == 0) {
+                float c[kMaxNB][4] = {};
+                const int arow = w4 * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;   // ldmatrix row of this lane
                 for (int kk = 0; kk < nk16; ++kk) {
                     const int chk = (kk & 3) * 2 + (lane >> 4);                    // 16-byte chunk in the box row
                     const uint32_t addr = smem_u32(stg + (kk >> 2) * kBoxBytes + arow * 128 +
                                                    ((chk ^ (arow & 7)) << 4));
                     uint32_t a0, a1, a2, a3;
                     ldmatrix_x4(addr, a0, a1, a2, a3);
-                    const uint2 f0 = frag[(nb0 * (kMaxR / 16) + kk) * 32 + lane];
-                    mma_bf16_16816(c0, a0, a1, a2, a3, f0.x, f0.y);
-                    if (two) {
-                        const uint2 f1 = frag[((nb0 + 4) * (kMaxR / 16) + kk) * 32 + lane];
-                        mma_bf16_16816(c1, a0, a1, a2, a3, f1.x, f1.y);
+#pragma unroll
+                    for (int nb = 0; nb < kMaxNB; ++nb) {
+                        if (nb < NB) {
+                            const uint2 f = frag[(nb * (kMaxR / 16) + kk) * 32 + lane];
+                            mma_bf16_16816(c[nb], a0, a1, a2, a3, f.x, f.y);
+                        }
                     }
                 }
                 // s = z + U_k: rows g, g + 8 of the block, requests 2 (lane % 4) (+ 1) of each request block
                 const int g = lane >> 2, cq = 2 * (lane & 3);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (h == 1 && !two) break;
-                    const float* c = h ? c1 : c0;
-                    const int nbase = (nb0 + 4 * h) * 8 + cq;
+                for (int nb = 0; nb < kMaxNB; ++nb) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int n = nbase + (e & 1), row = mb * 16 + g + (e >> 1) * 8;
-                        if (n < p.B) {
-                            const uint16_t u = *reinterpret_cast<const uint16_t*>(stg + kW2Bytes + n * (kTile * 2) +
-                                                                                  row * 2);
-                            zs[n * kTile + row] = c[e] + __uint_as_float(static_cast<uint32_t>(u) << 16);
+                        const int n = nb * 8 + cq + (e & 1), row = w4 * 16 + g + (e >> 1) * 8;
+                        if (nb < NB && n < p.B) {
+                            const int v = j * kTile + row;
+                            uint16_t u;
+                            if constexpr (kUHost)
+                                u = v < p.V ? p.U[(static_cast<size_t>(n) * p.gamma + (k - 1)) * p.V + v] : uint16_t(0);
+                            else
+                                u = *reinterpret_cast<const uint16_t*>(stg + kW2Bytes + n * (kTile * 2) + row * 2);
+                            zsg[n * kTile + row] = c[nb][e] + __uint_as_float(static_cast<uint32_t>(u) << 16);
                         }
                     }
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[cstage]);   // this warp is done with the slot
-            if (++cstage == kStages) { cstage = 0; cphase ^= 1u; }
-            csync();                                      // the tile's s is complete
+            if (lane == 0) mbar_arrive(&empty[grp]);      // this warp is done with the slot
+            gsync();                                      // the tile's s is complete
             if (s_fail == 0) {
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     if (q >= nreq) break;
-                    const int b = (tid >> 4) + 32 * q, v0 = j * kTile + 4 * gq;
-                    const float4 s4 = *reinterpret_cast<const float4*>(zs + b * kTile + 4 * gq);
+                    const int b = bq + 8 * q, v0 = j * kTile + 4 * gq;
+                    const float4 s4 = *reinterpret_cast<const float4*>(zsg + b * kTile + 4 * gq);
                     float y[4] = {s4.x * p.cscale, s4.y * p.cscale, s4.z * p.cscale, s4.w * p.cscale};
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
@@ -305,11 +319,12 @@ draft_gemv(const __grid_constant__ CUtensorMap tmW2, Params p) {
                     }
                 }
             }
-            csync();                                      // zs is rewritten by the next tile
+            gsync();                                      // zsg is rewritten by the group's next tile
         }
 
         // ------------------------------------------------ this CTA's partials
-        // the 16 threads of a request (a half warp) merge in a fixed order
+        // the 16 threads of a request in a group (a half warp) merge, then thread b
+        // merges the groups in group order
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
 #pragma unroll
@@ -322,18 +337,32 @@ draft_gemv(const __grid_constant__ CUtensorMap tmW2, Params p) {
                 best_take(best[q], ok, oi, oy);
                 lse_merge(M[q], S[q], om, os);
             }
-            if (gq == 0 && q < nreq && s_fail == 0) {
-                const int b = (tid >> 4) + 32 * q;
-                const size_t slot = static_cast<size_t>(k - 1) * p.B + b;
-                if (!p.greedy) {
-                    p.ws.part[slot * kMaxChunks + chunk] = make_float2(M[q], S[q]);
-                    p.ws.ybest[slot * kMaxChunks + chunk] = best[q].y;
-                }
-                if (best[q].key > -INFINITY)
-                    atomicMax(&p.ws.words[slot], pack_key(best[q].key, static_cast<uint32_t>(best[q].idx)));
+            if (gq == 0 && q < nreq) {
+                const int b = bq + 8 * q;
+                pm[grp][b] = M[q];
+                ps[grp][b] = S[q];
+                pk[grp][b] = best[q].key;
+                pi[grp][b] = best[q].idx;
+                py[grp][b] = best[q].y;
             }
         }
-        arrive();                                         // position k published
+        csync();
+        if (tid < p.B && s_fail == 0) {
+            const int b = tid;
+            Best cb{-INFINITY, 0x7FFFFFFF, 0.f};
+            float m = -INFINITY, sum = 0.f;
+            for (int gg = 0; gg < kGroups; ++gg) {
+                best_take(cb, pk[gg][b], pi[gg][b], py[gg][b]);
+                lse_merge(m, sum, pm[gg][b], ps[gg][b]);
+            }
+            const size_t slot = static_cast<size_t>(k - 1) * p.B + b;
+            if (!p.greedy) {
+                p.ws.part[slot * kMaxChunks + chunk] = make_float2(m, sum);
+                p.ws.ybest[slot * kMaxChunks + chunk] = cb.y;
+            }
+            if (cb.key > -INFINITY) atomicMax(&p.ws.words[slot], pack_key(cb.key, static_cast<uint32_t>(cb.idx)));
+        }
+        arrive();                                         // position k published (pm .. py reused after a barrier)
     }
 
     // ---------------------------------------------------- x_gamma and finalize
@@ -390,10 +419,11 @@ inline int grid_for(int V) {
     return g < 1 ? 1 : g;
 }
 
-inline dspark_status_t launch(const Params& p, int grid, cudaStream_t s) {
+template <bool kUHost>
+dspark_status_t launch_as(const Params& p, int grid, cudaStream_t s) {
     static OncePerDevice once;
     if (once.run(current_device(), [] {
-            return cudaFuncSetAttribute(draft_gemv, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            return cudaFuncSetAttribute(draft_gemv<kUHost>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(kSmem));
         }) != cudaSuccess)
         return DSPARK_ERR_CUDA;
@@ -409,11 +439,16 @@ inline dspark_status_t launch(const Params& p, int grid, cudaStream_t s) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, draft_gemv, map, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, draft_gemv<kUHost>, map, p) != cudaSuccess) {
         cudaGetLastError();
         return DSPARK_ERR_CUDA;
     }
     return DSPARK_OK;
+}
+
+// u_host: U is page-locked host memory (read through its mapping with loads).
+inline dspark_status_t launch(const Params& p, int grid, bool u_host, cudaStream_t s) {
+    return u_host ? launch_as<true>(p, grid, s) : launch_as<false>(p, grid, s);
 }
 
 }  // namespace gemv

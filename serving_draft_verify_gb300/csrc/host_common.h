@@ -71,6 +71,16 @@ inline bool device_view(const void* p, const void** out) {
     return true;
 }
 
+// True if p (or the device address of a mapping) lies in page-locked host memory.
+inline bool in_host_memory(const void* p) {
+    cudaPointerAttributes pa{};
+    if (cudaPointerGetAttributes(&pa, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return pa.type == cudaMemoryTypeHost;
+}
+
 // Once-per-device flag for one-time kernel attribute setup.
 struct OncePerDevice {
     std::mutex mu;

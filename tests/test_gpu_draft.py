@@ -148,11 +148,12 @@ def test_draft_one_launch_equals_per_position(dsv, key, changes, temperature):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("B", [40, 5])                   # the tcgen05 engine; the small-batch path
 @pytest.mark.parametrize("temperature", [None, 0.0])
-def test_draft_reads_inputs_from_pinned_host_memory(dsv, temperature):
+def test_draft_reads_inputs_from_pinned_host_memory(dsv, temperature, B):
     """U, h and x0 in pinned host memory (read by the kernels over the host link): the
     same outputs, bit for bit, as from device memory."""
-    cfg = wl.scaled(wl.QWEN3_8B, B=40, V=8192, H=64)
+    cfg = wl.scaled(wl.QWEN3_8B, B=B, V=8192, H=64)
     inp = wl.make_draft_inputs(cfg)
     T = cfg.temperature if temperature is None else temperature
     g = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}

@@ -1,5 +1,5 @@
 """GPU parity of the draft block's small-batch GEMV path and of the tcgen05
-engine against the oracle at the same batch sizes (B = 1 .. 64), and of the
+engine against the oracle at the same batch sizes (B = 1 .. 16), and of the
 two paths against each other.
 
 The GEMV path forms z = U_k + W2 . W1[x_{k-1}] with warp-level MMAs whose
@@ -14,6 +14,8 @@ from serving_draft_verify_gb300 import workloads as wl
 from tests.gpu_harness import compare_draft, npy, oracle_draft, report_exempt
 
 pytestmark = pytest.mark.gpu
+
+GEMV_MAX_B = 16
 
 
 @pytest.fixture(scope="module")
@@ -36,11 +38,10 @@ def run(dsv, inp, mode, temperature=None):
 CASES = [
     ("B1_r256", dict(B=1, gamma=7, V=5000, H=64)),
     ("B4_r256", dict(B=4, gamma=7, V=6000, H=64)),
-    ("B16_r256", dict(B=16, gamma=5, V=4000, H=64)),
-    ("B17_r256", dict(B=17, gamma=3, V=3000, H=64)),
-    ("B32_r256", dict(B=32, gamma=3, V=2056, H=32)),                 # V % 64 = 8: a ragged last tile
-    ("B40_r128", dict(B=40, gamma=3, V=3000, H=32, r=128)),          # two requests per drawing thread
-    ("B64_r256", dict(B=64, gamma=2, V=2048, H=32)),                 # the path's largest batch
+    ("B9_r128", dict(B=9, gamma=3, V=3000, H=32, r=128)),            # two requests per drawing thread
+    ("B16_r256", dict(B=16, gamma=5, V=4000, H=64)),                 # the path's largest batch
+    ("B13_r256", dict(B=13, gamma=3, V=2056, H=32)),                 # V % 64 = 8: a ragged last tile
+    ("B17_r256", dict(B=17, gamma=3, V=3000, H=64)),                 # engine only
     ("B5_r64", dict(B=5, gamma=4, V=1000, H=32, r=64)),
     ("B3_r192", dict(B=3, gamma=6, V=1544, H=32, r=192)),
 ]
@@ -50,6 +51,8 @@ CASES = [
 @pytest.mark.parametrize("temperature", [None, 0.0, 1.7])
 @pytest.mark.parametrize("mode", [1, 2], ids=["tcgen05", "gemv"])
 def test_gemv_and_engine_parity(dsv, name, changes, temperature, mode):
+    if mode == 2 and changes["B"] > GEMV_MAX_B:
+        pytest.skip(f"the GEMV path takes B <= {GEMV_MAX_B}")
     cfg = wl.scaled(wl.QWEN3_8B, **changes)
     inp = wl.make_draft_inputs(cfg)
     gpu = run(dsv, inp, mode, temperature)
@@ -91,19 +94,19 @@ def test_gemv_full_vocabulary_every_request(dsv):
 
 
 def test_default_path_is_the_measured_faster_one(dsv):
-    """mode 0 takes the tcgen05 engine at every batch size (it measured faster
-    than the GEMV path from B = 1 up): bit-identical to forcing the engine."""
-    for B in (1, 16, 17):
+    """mode 0 takes the GEMV path up to B = 9 (it measured faster there) and the
+    tcgen05 engine above: bit-identical to forcing that path."""
+    for B, mode in ((1, 2), (9, 2), (10, 1), (16, 1)):
         cfg = wl.scaled(wl.QWEN3_8B, B=B, gamma=3, V=2000, H=32)
         inp = wl.make_draft_inputs(cfg)
         auto = run(dsv, inp, 0)
-        forced = run(dsv, inp, 1)
+        forced = run(dsv, inp, mode)
         for k in ("x", "lse_d", "logp_d", "c", "a"):
             assert np.array_equal(auto[k], forced[k]), (B, k)
 
 
 def test_gemv_unsupported_shapes_report(dsv):
-    cfg = wl.scaled(wl.QWEN3_8B, B=65, gamma=2, V=1000, H=32)
+    cfg = wl.scaled(wl.QWEN3_8B, B=GEMV_MAX_B + 1, gamma=2, V=1000, H=32)
     inp = wl.make_draft_inputs(cfg)
     with pytest.raises(RuntimeError):
         run(dsv, inp, 2)
