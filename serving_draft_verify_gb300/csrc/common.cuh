@@ -210,6 +210,39 @@ __device__ __forceinline__ U4 philox_row(const PhiloxRow& r, uint32_t q) {
     }
     return c;
 }
+// The round keys of one seed (the key bumped by the Weyl constants each round),
+// formed on the host: kept in a kernel's parameters, they enter the rounds as
+// constant operands instead of being re-derived per block.
+struct PhiloxKeys {
+    uint32_t k0[10], k1[10];
+};
+inline PhiloxKeys philox_keys(uint64_t seed) {
+    PhiloxKeys K;
+    uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+    for (int i = 0; i < 10; ++i) {
+        K.k0[i] = k0;
+        K.k1[i] = k1;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return K;
+}
+// philox_row with the round keys taken from K (the seed philox_row_setup got).
+__device__ __forceinline__ U4 philox_row(const PhiloxRow& r, uint32_t q, const PhiloxKeys& K) {
+    uint32_t lo0, hi0, lo1, hi1;
+    mul_wide(0xD2511F53u, q, lo0, hi0);
+    const uint32_t z1 = hi0 ^ r.r1_z;
+    mul_wide(0xCD9E8D57u, z1, lo1, hi1);
+    U4 c{hi1 ^ r.r2_y, lo1, r.r2_hi0 ^ lo0, r.r2_lo0};
+#pragma unroll
+    for (int i = 2; i < 10; ++i) {
+        uint32_t a0, b0, a1, b1;
+        mul_wide(0xD2511F53u, c.x, a0, b0);
+        mul_wide(0xCD9E8D57u, c.z, a1, b1);
+        c = U4{b1 ^ c.y ^ K.k0[i], a1, b0 ^ c.w ^ K.k1[i], a0};
+    }
+    return c;
+}
 __device__ __forceinline__ uint32_t u4_word(const U4& r, uint32_t sel) {
     return sel == 0 ? r.x : sel == 1 ? r.y : sel == 2 ? r.z : r.w;
 }

@@ -490,7 +490,7 @@ dspark_status_t draft_block_impl(int B, int gamma, int V, int H, int r, dspark_d
         gp.U = static_cast<const uint16_t*>(U); gp.W1 = static_cast<const uint16_t*>(W1);
         gp.W2 = static_cast<const uint16_t*>(W2); gp.h = static_cast<const uint16_t*>(h);
         gp.w = static_cast<const uint16_t*>(w); gp.bias = bias; gp.x0 = x0; gp.x = x;
-        gp.cscale = cscale; gp.greedy = greedy; gp.seed = seed;
+        gp.cscale = cscale; gp.greedy = greedy; gp.seed = seed; gp.keys = philox_keys(seed);
         gp.lse_d = lse_d; gp.logp_d = logp_d; gp.c = c; gp.a = a; gp.ws = ws;
         if (g_timing.on) cudaEventRecord(g_timing.ev[0], s);
         const dspark_status_t stg = gemv::launch(gp, gemv::grid_for(V), in_host_memory(U), s);
@@ -512,7 +512,8 @@ dspark_status_t draft_block_impl(int B, int gamma, int V, int H, int r, dspark_d
         p.U = static_cast<const uint16_t*>(U); p.W1 = static_cast<const uint16_t*>(W1);
         p.E = static_cast<const uint16_t*>(E);
         p.W2 = static_cast<const uint16_t*>(W2);
-        p.x0 = x0; p.x = x; p.cscale = cscale; p.greedy = greedy; p.seed = seed; p.P = P; p.ws = ws;
+        p.x0 = x0; p.x = x; p.cscale = cscale; p.greedy = greedy; p.seed = seed; p.keys = philox_keys(seed);
+        p.P = P; p.ws = ws;
     } else {
         nchunk = simt_chunks(V);
     }
@@ -599,7 +600,8 @@ dspark_status_t debug_tc_logits(int B, int V, int r, const void* U, const void* 
     p.B = B; p.gamma = 1; p.V = V; p.r = r; p.k = 1; p.k_last = 1;
     p.U = static_cast<const uint16_t*>(U); p.W1 = static_cast<const uint16_t*>(W1);
     p.W2 = static_cast<const uint16_t*>(W2);
-    p.x0 = prev; p.x = nullptr; p.cscale = 1.f; p.greedy = 1; p.seed = 0; p.P = P; p.ws = ws; p.debug_z = z;
+    p.x0 = prev; p.x = nullptr; p.cscale = 1.f; p.greedy = 1; p.seed = 0; p.keys = philox_keys(0);
+    p.P = P; p.ws = ws; p.debug_z = z;
     return eng::launch_tc<eng::kDraft>(map, p, nM * P, s, false);
 }
 

@@ -180,8 +180,8 @@ __device__ __forceinline__ unsigned long long f2fma(unsigned long long a, unsign
 // ascending order and a key must be strictly larger to win: ties keep the
 // lowest index.  `pr` holds the row's Philox constants; word v & 3 of block
 // v >> 2 keys index v.
-__device__ __forceinline__ void draw32(const float* s, float c, int v0, const PhiloxRow& pr, Best& best, float& M,
-                                       float& S) {
+__device__ __forceinline__ void draw32(const float* s, float c, int v0, const PhiloxRow& pr, const PhiloxKeys& K,
+                                       Best& best, float& M, float& S) {
     float m8[8];
 #pragma unroll
     for (int w = 0; w < 8; ++w) m8[w] = fmaxf(fmaxf(s[w], s[w + 8]), fmaxf(s[w + 16], s[w + 24]));
@@ -206,7 +206,7 @@ __device__ __forceinline__ void draw32(const float* s, float c, int v0, const Ph
         uint32_t wv[16];
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) {
-            const U4 pw = philox_row(pr, q0 + 4 * hh + qq);
+            const U4 pw = philox_row(pr, q0 + 4 * hh + qq, K);
             wv[4 * qq] = pw.x;
             wv[4 * qq + 1] = pw.y;
             wv[4 * qq + 2] = pw.z;
@@ -408,6 +408,7 @@ struct TcParams {
     float cscale;                    // log2e / T (1 for greedy)
     int greedy;
     uint64_t seed;
+    PhiloxKeys keys;                 // the round keys of `seed`
     int P;                           // CTAs per M-tile
     Ws ws;
     float* debug_z;                  // kDraft: write y to [B][V] instead of reducing
@@ -802,7 +803,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                                 for (int w = 0; w < 32; ++w)
                                     if (y[w] > best.key) { best.key = y[w]; best.idx = v0 + w; }
                             } else {
-                                draw32(y, p.cscale, v0, prow, best, M, S);
+                                draw32(y, p.cscale, v0, prow, p.keys, best, M, S);
                             }
                         } else {
                             // residual q = max(0, p_t - p_d), p_d = 2^(y - ld2), p_t = 2^(t c - lt2);
@@ -810,7 +811,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                             const uint32_t qbase = static_cast<uint32_t>(v0) >> 2;
 #pragma unroll
                             for (int qq = 0; qq < 8; ++qq) {
-                                const U4 pw = philox_row(prow, qbase + qq);
+                                const U4 pw = philox_row(prow, qbase + qq, p.keys);
                                 const uint32_t wv[4] = {pw.x, pw.y, pw.z, pw.w};
 #pragma unroll
                                 for (int jj = 0; jj < 4; ++jj) {

@@ -73,6 +73,7 @@ struct Params {
     float cscale;
     int greedy;
     uint64_t seed;
+    PhiloxKeys keys;                // the round keys of `seed`
     float* lse_d;
     float* logp_d;
     float* c;
@@ -309,7 +310,7 @@ draft_gemv(const __grid_constant__ CUtensorMap tmW2, Params p) {
                             const float s4s = fast_exp2(y[0] - m4) + fast_exp2(y[1] - m4) + fast_exp2(y[2] - m4) +
                                               fast_exp2(y[3] - m4);
                             lse_merge(M[q], S[q], m4, s4s);
-                            const U4 pw = philox_row(pr[q], static_cast<uint32_t>(v0) >> 2);
+                            const U4 pw = philox_row(pr[q], static_cast<uint32_t>(v0) >> 2, p.keys);
                             const uint32_t wd[4] = {pw.x, pw.y, pw.z, pw.w};
 #pragma unroll
                             for (int e = 0; e < 4; ++e)

@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(256, kRowsCtasPerSm)
 verify_rows(int gamma, int V, const void* __restrict__ t, const int32_t* __restrict__ x,
             const float* __restrict__ lse_d, const float* __restrict__ logp_d, const int32_t* __restrict__ ell,
             float cscale, int greedy, uint64_t seed, int32_t* __restrict__ n_accept, int32_t* __restrict__ next_token,
-            VerifyWs ws) {
+            VerifyWs ws, const PhiloxKeys keys) {
     __shared__ float rk[8], rm[8], rs[8];
     __shared__ int ri[8];
     __shared__ int s_last;
@@ -395,7 +395,7 @@ verify_rows(int gamma, int V, const void* __restrict__ t, const int32_t* __restr
                         uint32_t cmask = 0u;
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
-                            const U4 pw = philox_row(pr, (static_cast<uint32_t>(v) >> 2) + h);
+                            const U4 pw = philox_row(pr, (static_cast<uint32_t>(v) >> 2) + h, keys);
                             wv[4 * h] = pw.x; wv[4 * h + 1] = pw.y; wv[4 * h + 2] = pw.z; wv[4 * h + 3] = pw.w;
                         }
 #pragma unroll
@@ -604,10 +604,10 @@ static dspark_status_t verify_impl(int B, int gamma, int V, int r, dspark_dtype_
     if (stt != DSPARK_OK) return stt;
     if (bf)
         verify_rows<true><<<rgrid, 256, 0, s>>>(gamma, V, t_logits, x, lse_d, logp_d, ell, cscale, greedy, seed,
-                                                n_accept, next_token, ws);
+                                                n_accept, next_token, ws, philox_keys(seed));
     else
         verify_rows<false><<<rgrid, 256, 0, s>>>(gamma, V, t_logits, x, lse_d, logp_d, ell, cscale, greedy, seed,
-                                                 n_accept, next_token, ws);
+                                                 n_accept, next_token, ws, philox_keys(seed));
     if ((stt = launch_status()) != DSPARK_OK || greedy) return stt;
 
     eng::FinishArgs f{};
@@ -628,7 +628,7 @@ static dspark_status_t verify_impl(int B, int gamma, int V, int r, dspark_dtype_
         p.E = static_cast<const uint16_t*>(E);
         p.W2 = static_cast<const uint16_t*>(W2); p.k_last = 1;
         p.x0 = x0; p.x = const_cast<int32_t*>(x); p.cscale = cscale; p.greedy = 0;   // read only here
-        p.seed = seed; p.P = P;
+        p.seed = seed; p.keys = philox_keys(seed); p.P = P;
         p.ws = eng::Ws{ws.status, ws.res_word, nullptr, nullptr, ws.gbar};
         p.krow = ws.krow; p.T = static_cast<const uint16_t*>(t_logits); p.lt2 = ws.lt2; p.ld2 = ws.ld2;
         p.rej_list = ws.rej_list; p.rej_count = ws.rej_count;
