@@ -135,16 +135,15 @@ __device__ __forceinline__ void best_take(Best& b, float key, int idx, float y) 
     if (key > b.key || (key == b.key && idx < b.idx)) { b.key = key; b.idx = idx; b.y = y; }
 }
 
-// s = 1 - u for u = ((w >> 9) + 1/2) 2^-23: exact in float32, and a lower bound
-// of E = -ln u (since -ln(1 - s) >= s).
-__device__ __forceinline__ float one_minus_u(uint32_t w) {
-    return __uint_as_float(((~w) >> 9) | 0x3F800000u) - 0.999999940395355225f;
-}
-// f = s + (1 - 2^-24) = 1 + m' 2^-23 in [1, 2), exact: comparing f < X + (1 - 2^-24) tests
-// s < X without forming s (the rounding of the sum is covered by the caller's slack).
-__device__ __forceinline__ float one_minus_u_shifted(uint32_t w) {
-    return __uint_as_float(((~w) >> 9) | 0x3F800000u);
-}
+// The draws' candidate test: s = 1 - u for u = ((w >> 9) + 1/2) 2^-23 is a lower
+// bound of E = -ln u (since -ln(1 - s) >= s), so a token whose s already exceeds the
+// bound on E that could beat the running best cannot win.
+// f = 1 + m 2^-23 for m = w >> 9 (one funnel shift puts the exponent bits above m).
+// Then s = 1 - u = 2 - f - 2^-24 exactly, so s < X  <=>  f > 2 - 2^-24 - X; callers test
+// f > fma(X, -1, kTopU): kTopU = 2 - 2^-22 sits 3 2^-24 below 2 - 2^-24, more than the
+// fma's rounding (at most 2^-24 at these magnitudes), so no candidate is dropped.
+constexpr float kTopU = 1.99999976158142089844f;   // 2 - 2^-22
+__device__ __forceinline__ float one_plus_m(uint32_t w) { return __uint_as_float(__funnelshift_r(w, 0x7Fu, 9)); }
 
 // Two float32 lanes in one 64-bit register (Blackwell f32x2 arithmetic); each lane
 // of an f32x2 operation is rounded once, exactly as its float32 counterpart.
@@ -191,9 +190,8 @@ __device__ __forceinline__ void draw32(const float* s, float c, int v0, const Ph
     const float mb = mraw * c;                            // the sub-block's max of y
     const float mref = live ? mb : 0.f;
     constexpr float kSlack = 1.0009765625f;               // 1 + 2^-10
-    // s_v < e_v R  <=>  f_v < e_v R + (1 - 2^-24); 2^-23 more covers the rounding of that sum
-    constexpr float kShift = 0.999999940395355225f + 1.1920928955078125e-07f;
-    const float R = live ? fast_exp2(mb - best.key) * kSlack : 0.f;   // +inf while nothing is drawn yet
+    // s_v < e_v R  <=>  f_v > 2 - 2^-24 - e_v R (f_v = one_plus_m(w_v)), tested against kTopU
+    const float nR = live ? -(fast_exp2(mb - best.key) * kSlack) : 0.f;   // -inf while nothing is drawn yet
     const unsigned long long c2 = f2pack(c, c), nm2 = f2pack(-mref, -mref);
     unsigned long long sum2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};   // two chains of partial sums
     const uint32_t q0 = static_cast<uint32_t>(v0) >> 2;
@@ -219,8 +217,8 @@ __device__ __forceinline__ void draw32(const float* s, float c, int v0, const Ph
             f2unpack(f2fma(f2pack(s[16 * hh + i], s[16 * hh + i + 1]), c2, nm2), a0, a1);
             const float e0 = fast_exp2(a0), e1 = fast_exp2(a1);
             sum2[(i >> 1) & 1] = f2add(sum2[(i >> 1) & 1], f2pack(e0, e1));
-            if (one_minus_u_shifted(wv[i]) < fmaf(e0, R, kShift)) cm[(i >> 1) & 3] |= 1u << i;   // 0 * inf = NaN: false
-            if (one_minus_u_shifted(wv[i + 1]) < fmaf(e1, R, kShift)) cm[(i >> 1) & 3] |= 2u << i;
+            if (one_plus_m(wv[i]) > fmaf(e0, nR, kTopU)) cm[(i >> 1) & 3] |= 1u << i;   // 0 * -inf = NaN: false
+            if (one_plus_m(wv[i + 1]) > fmaf(e1, nR, kTopU)) cm[(i >> 1) & 3] |= 2u << i;
         }
         const uint32_t cmask = (cm[0] | cm[1]) | (cm[2] | cm[3]);
         if (__any_sync(0xffffffffu, cmask != 0u)) {

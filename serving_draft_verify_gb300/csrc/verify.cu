@@ -400,7 +400,8 @@ verify_rows(int gamma, int V, const void* __restrict__ t, const int32_t* __restr
                         }
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            if (eng::one_minus_u(wv[i]) < fast_exp2(y[u][i] * cscale - best) * kSlack) cmask |= 1u << i;
+                            if (eng::one_plus_m(wv[i]) > fmaf(fast_exp2(y[u][i] * cscale - best), -kSlack, eng::kTopU))
+                                cmask |= 1u << i;
                         if (__any_sync(0xffffffffu, cmask != 0u)) {
 #pragma unroll
                             for (int i = 0; i < 8; ++i) {
