@@ -145,6 +145,14 @@ __device__ __forceinline__ void best_take(Best& b, float key, int idx, float y) 
 constexpr float kTopU = 1.99999976158142089844f;   // 2 - 2^-22
 __device__ __forceinline__ float one_plus_m(uint32_t w) { return __uint_as_float(__funnelshift_r(w, 0x7Fu, 9)); }
 
+// lo += float(low bf16 of w), hi += float(high bf16 of w): the bf16 -> float32 widening
+// is exact, so each result is the float32 sum rounded once, as with an explicit widening.
+__device__ __forceinline__ void add_bf16_pair(uint32_t w, float& lo, float& hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tadd.f32.bf16 %0, l, %0;\n\tadd.f32.bf16 %1, h, %1;\n\t}"
+        : "+f"(lo), "+f"(hi)
+        : "r"(w));
+}
+
 // Two float32 lanes in one 64-bit register (Blackwell f32x2 arithmetic); each lane
 // of an f32x2 operation is rounded once, exactly as its float32 counterpart.
 __device__ __forceinline__ unsigned long long f2pack(float lo, float hi) {
@@ -776,11 +784,10 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kBN + off;
                         tc::tmem_ld32(taddr, y);
                         tc::tmem_ld_wait();
-                        // raw logits z = acc + U (two tokens per f32x2 add); the draw scales by cscale
+                        // raw logits z = acc + U (each bf16 U added to its float32 accumulator by one
+                        // mixed-precision add); the draw scales by cscale
 #pragma unroll
-                        for (int w = 0; w < 16; ++w)
-                            f2unpack(f2add(f2pack(y[2 * w], y[2 * w + 1]), f2pack(bf16lo(un[w]), bf16hi(un[w]))),
-                                     y[2 * w], y[2 * w + 1]);
+                        for (int w = 0; w < 16; ++w) add_bf16_pair(un[w], y[2 * w], y[2 * w + 1]);
                         // this sub-block's U words are consumed: fetch the next one's, in flight
                         // while this sub-block is reduced
                         if (kMode == kDraft && vn >= 0) load16(urow, vn, un);
