@@ -145,6 +145,13 @@ __device__ __forceinline__ void best_take(Best& b, float key, int idx, float y) 
 constexpr float kTopU = 1.99999976158142089844f;   // 2 - 2^-22
 __device__ __forceinline__ float one_plus_m(uint32_t w) { return __uint_as_float(__funnelshift_r(w, 0x7Fu, 9)); }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // lo += float(low bf16 of w), hi += float(high bf16 of w): the bf16 -> float32 widening
 // is exact, so each result is the float32 sum rounded once, as with an explicit widening.
 __device__ __forceinline__ void add_bf16_pair(uint32_t w, float& lo, float& hi) {
@@ -189,11 +196,13 @@ __device__ __forceinline__ unsigned long long f2fma(unsigned long long a, unsign
 // v >> 2 keys index v.
 __device__ __forceinline__ void draw32(const float* s, float c, int v0, const PhiloxRow& pr, const PhiloxKeys& K,
                                        Best& best, float& M, float& S) {
-    float m8[8];
+    // the sub-block's max by three-input maxima (max is exact: any grouping gives the same value)
+    float m3[11];
 #pragma unroll
-    for (int w = 0; w < 8; ++w) m8[w] = fmaxf(fmaxf(s[w], s[w + 8]), fmaxf(s[w + 16], s[w + 24]));
-    const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+    for (int w = 0; w < 10; ++w) m3[w] = fmax3(s[w], s[w + 10], s[w + 20]);
+    m3[10] = fmaxf(s[30], s[31]);
+    const float mraw = fmax3(fmax3(m3[0], m3[1], m3[2]), fmax3(m3[3], m3[4], m3[5]),
+                             fmax3(fmax3(m3[6], m3[7], m3[8]), m3[9], m3[10]));
     const bool live = mraw > -INFINITY;                   // no finite logit: no mass, no candidate
     const float mb = mraw * c;                            // the sub-block's max of y
     const float mref = live ? mb : 0.f;
