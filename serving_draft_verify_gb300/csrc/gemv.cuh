@@ -305,7 +305,7 @@ draft_gemv(const __grid_constant__ CUtensorMap tmW2, Params p) {
 #pragma unroll
                         for (int e = 0; e < 4; ++e) best_take(best[q], y[e], v0 + e, y[e]);
                     } else {
-                        const float m4 = fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3]));
+                        const float m4 = fmaxf(eng::fmax3(y[0], y[1], y[2]), y[3]);
                         if (m4 > -INFINITY) {
                             const float s4s = fast_exp2(y[0] - m4) + fast_exp2(y[1] - m4) + fast_exp2(y[2] - m4) +
                                               fast_exp2(y[3] - m4);

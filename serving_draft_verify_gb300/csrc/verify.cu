@@ -416,9 +416,8 @@ verify_rows(int gamma, int V, const void* __restrict__ t, const int32_t* __restr
                     // online (max, sum) of 2^(y c) per lane: a new maximum rescales the sum
 #pragma unroll
                     for (int u = 0; u < kU; ++u) {
-                        float m = y[u][0];
-#pragma unroll
-                        for (int i = 1; i < 8; ++i) m = fmaxf(m, y[u][i]);
+                        const float m = eng::fmax3(eng::fmax3(y[u][0], y[u][1], y[u][2]),
+                                                   eng::fmax3(y[u][3], y[u][4], y[u][5]), fmaxf(y[u][6], y[u][7]));
                         if (!(m > -INFINITY)) continue;
                         const float mc = m * cscale;
                         if (mc > M) {
