@@ -239,24 +239,24 @@ __device__ __forceinline__ void draw32(const float* s, float c, int v0, const Ph
         }
         const uint32_t cmask = (cm[0] | cm[1]) | (cm[2] | cm[3]);
         if (__any_sync(0xffffffffu, cmask != 0u)) {
+            // each lane walks its own candidates of each group of four, lowest first (the
+            // warp runs as many steps as its busiest lane, not one per bit position)
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {
-                if ((cmask >> (4 * qq)) & 0xFu) {
-                    const int g = 16 * hh + 4 * qq;
-#pragma unroll 1
-                    for (int j = 0; j < 4; ++j) {
-                        const float sj = j == 0 ? s[g] : j == 1 ? s[g + 1] : j == 2 ? s[g + 2] : s[g + 3];
-                        const uint32_t wj = j == 0 ? wv[4 * qq] : j == 1 ? wv[4 * qq + 1]
-                                                       : j == 2 ? wv[4 * qq + 2] : wv[4 * qq + 3];
-                        if ((cmask >> (4 * qq + j)) & 1u) {
-                            const float yj = sj * c;
-                            const float key = yj - fast_log2(exp_draw(wj));
-                            if (key > best.key) {
-                                best.key = key;
-                                best.idx = v0 + g + j;
-                                best.y = yj;
-                            }
-                        }
+                uint32_t bits = (cmask >> (4 * qq)) & 0xFu;
+                const int g = 16 * hh + 4 * qq;
+                while (bits != 0u) {
+                    const int j = __ffs(bits) - 1;
+                    bits &= bits - 1u;
+                    const float sj = j == 0 ? s[g] : j == 1 ? s[g + 1] : j == 2 ? s[g + 2] : s[g + 3];
+                    const uint32_t wj = j == 0 ? wv[4 * qq] : j == 1 ? wv[4 * qq + 1]
+                                                   : j == 2 ? wv[4 * qq + 2] : wv[4 * qq + 3];
+                    const float yj = sj * c;
+                    const float key = yj - fast_log2(exp_draw(wj));
+                    if (key > best.key) {
+                        best.key = key;
+                        best.idx = v0 + g + j;
+                        best.y = yj;
                     }
                 }
             }
