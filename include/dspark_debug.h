@@ -47,7 +47,7 @@ dspark_status_t dspark_debug_force_phase_launches(int enable);
 /* Test hook: which path dspark_draft_block takes for bf16 weights with the
  * Markov head (r % 64 == 0, r <= 256).  mode 0 (default): by batch size -- the
  * small-batch GEMV path (W2 streamed once per position for all requests,
- * warp-level MMAs) for B <= 9, where it measured faster, and the tcgen05
+ * warp-level MMAs) for B <= 8, where it measured faster, and the tcgen05
  * engine above; 1: always the tcgen05 engine; 2: the GEMV path wherever it
  * applies (B <= 16), the calls it cannot take returning
  * DSPARK_ERR_UNSUPPORTED.  Both paths draw the same tokens from the same

@@ -403,10 +403,19 @@ verify_rows(int gamma, int V, const void* __restrict__ t, const int32_t* __restr
                             if (eng::one_plus_m(wv[i]) > fmaf(fast_exp2(y[u][i] * cscale - best), -kSlack, eng::kTopU))
                                 cmask |= 1u << i;
                         if (__any_sync(0xffffffffu, cmask != 0u)) {
+                            // each lane walks its own candidates of each group of four, lowest first
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                if ((cmask >> i) & 1u) {
-                                    const float key = y[u][i] * cscale - fast_log2(exp_draw(wv[i]));
+                            for (int q4 = 0; q4 < 2; ++q4) {
+                                uint32_t bits = (cmask >> (4 * q4)) & 0xFu;
+                                while (bits != 0u) {
+                                    const int j = __ffs(bits) - 1;
+                                    bits &= bits - 1u;
+                                    const int i = 4 * q4 + j;
+                                    const float yi = j == 0 ? y[u][4 * q4] : j == 1 ? y[u][4 * q4 + 1]
+                                                   : j == 2 ? y[u][4 * q4 + 2] : y[u][4 * q4 + 3];
+                                    const uint32_t wi = j == 0 ? wv[4 * q4] : j == 1 ? wv[4 * q4 + 1]
+                                                      : j == 2 ? wv[4 * q4 + 2] : wv[4 * q4 + 3];
+                                    const float key = yi * cscale - fast_log2(exp_draw(wi));
                                     if (key > best) { best = key; best_i = v + i; }
                                 }
                             }
