@@ -394,6 +394,26 @@ constexpr int kStages = 8;            // W2 slab ring
 constexpr int kEpiWG = 3;             // epilogue warpgroups
 constexpr int kTmemBufs = 4;          // TMEM accumulators of kBN columns (all 512), used in rotation
 constexpr int kTcThreads = 128 * (1 + kEpiWG);
+// Registers a thread: 128 at launch (512 threads, the whole register file), then
+// warpgroup 0 drops to kCtlRegs and the three epilogue warpgroups rise to kEpiRegs
+// (per scheduler: one warp of the first and three of the others, 56 + 3 x 152 = 4 x 128).
+constexpr uint32_t kLaunchRegs = 65536 / kTcThreads;
+constexpr uint32_t kCtlRegs = 56;
+constexpr uint32_t kEpiRegs = 152;
+static_assert(kCtlRegs + kEpiWG * kEpiRegs <= (1 + kEpiWG) * kLaunchRegs, "register split over the launch's total");
+template <int R>
+struct RoleTag {
+    static constexpr int value = R;
+};
+// setmaxnreg: the warpgroup's registers a thread (every warp of the warpgroup executes it)
+template <uint32_t N>
+__device__ __forceinline__ void reg_alloc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void reg_dealloc() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 constexpr int kPairs = (kTcThreads / 32 - 2) / 2;   // warp pairs of the residual launch's final step
 constexpr int kSlabBytes = kBN * kBK * 2;     // 16 KB
 constexpr int kASlabBytes = kBM * kBK * 2;    // 16 KB
@@ -584,26 +604,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
     tc::fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 0) {
-        // ---------------------------------------------------- TMA producer
-        // streams W2 for every position without waiting for the prologues
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_last();
-            int stage = 0;
-            uint32_t phase = 0;
-            bool failed = false;
-            for (int k = k0; k <= k1 && !failed; ++k)
-                for (int t = t_lo; t < t_hi && !failed; ++t)
-                    for (int s = 0; s < nslab; ++s) {
-                        if (!mbar_wait(&empty[stage], phase ^ 1u)) { failed = true; break; }
-                        mbar_arrive_expect_tx(&full[stage], kSlabBytes);
-                        tc::tma_load_2d(sB + stage * kSlabBytes, &tmW2, s * kBK, t * kBN, &full[stage], pol);
-                        if (++stage == kStages) { stage = 0; phase ^= 1u; }
-                    }
-            if (failed) set_status(st, DSPARK_ERR_TIMEOUT, 10);
-        }
-        __syncwarp();
-    } else {
+    {
         constexpr int kPro = kTcThreads - 32;             // warps 1.. : prologue, MMA, epilogue
         const int ptid = tid - 32;
         auto pro_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(kPro) : "memory"); };
@@ -635,302 +636,340 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
         uint32_t mma_phase = 0;
         bool failed = false;
 
-        for (int k = k0; k <= k1; ++k) {
-            const int base = (k - k0) * ntiles;           // running index of this position's first tile
-            // ---------------------------------------------- prologue: x_{k-1}
-            if (kMode == kDraft && multi && k > k0) {
-                wait_all();                               // every CTA published position k-1
-                for (int rr = ptid; rr < nrows; rr += kPro) {
-                    const int b = req(rr);
-                    const int tok = (*s_fail == 0) ? winner(b, k - 1) : 0;
-                    s_prev[rr] = tok;
-                    if (pc == 0) p.x[b * p.gamma + k - 2] = tok;
-                }
-            } else {
-                for (int rr = ptid; rr < nrows; rr += kPro) {
-                    const int b = req(rr);
-                    const int kb = row_k(b, k);
-                    s_prev[rr] = (kb > 0) ? prev_token(p.x0, p.x, b, p.gamma, kb, p.V, st) : -1;
-                }
-            }
-            pro_sync();
-            failed = failed || (*s_fail != 0);
-
-            // A operand: rows W1[x_{k_b-1}] of this M-tile, K-major, 128-byte swizzle
-            {
-                // one warp per A row, one lane per 16-byte chunk (r / 8 <= 32 chunks)
-                const int cpr = p.r / 8;
-                for (int row = ptid >> 5; row < kBM; row += kPro / 32) {
-                    const int rr = row & (rpc - 1);       // rpc is 32, 64 or 128
-                    const int prev = (rr < nrows) ? s_prev[rr] : -1;
-                    if (lane < cpr) {
-                        const int slab = lane >> 3, c = lane & 7;
-                        uint8_t* dst = sA + slab * kASlabBytes + (row >> 3) * 1024 + (row & 7) * 128 + ((c ^ (row & 7)) << 4);
-                        if (prev >= 0) {
-                            const uint16_t* src = p.E ? p.E + (static_cast<size_t>(req(rr)) * p.gamma + (row_k(req(rr), k) - 1)) * p.r
-                                                      : p.W1 + static_cast<size_t>(prev) * p.r;
-                            cp_async16(dst, src + lane * 8);
-                        }
-                        else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        // The position loop, compiled once per register budget: warps 1-3 (kRole 0: the
+        // prologue share and the MMA issuer) and the epilogue warpgroups (kRole 1: the
+        // prologue share, the draws and the publish) meet at the same barriers.
+        auto positions = [&](auto role) {
+            constexpr int kRole = decltype(role)::value;
+            for (int k = k0; k <= k1; ++k) {
+                const int base = (k - k0) * ntiles;           // running index of this position's first tile
+                // ---------------------------------------------- prologue: x_{k-1}
+                if (kMode == kDraft && multi && k > k0) {
+                    wait_all();                               // every CTA published position k-1
+                    for (int rr = ptid; rr < nrows; rr += kPro) {
+                        const int b = req(rr);
+                        const int tok = (*s_fail == 0) ? winner(b, k - 1) : 0;
+                        s_prev[rr] = tok;
+                        if (pc == 0) p.x[b * p.gamma + k - 2] = tok;
+                    }
+                } else {
+                    for (int rr = ptid; rr < nrows; rr += kPro) {
+                        const int b = req(rr);
+                        const int kb = row_k(b, k);
+                        s_prev[rr] = (kb > 0) ? prev_token(p.x0, p.x, b, p.gamma, kb, p.V, st) : -1;
                     }
                 }
-                cp_async_wait_all();
-                fence_proxy_async_smem();
-                tc::fence_before_sync();
                 pro_sync();
-                tc::fence_after_sync();
-            }
+                failed = failed || (*s_fail != 0);
 
-            if (warp == 1) {
-                // -------------------------------------------------- MMA issuer
-                if (lane == 0) {
-                    constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN);
-                    const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
-                    for (int i = 0; i < ntiles && !failed; ++i) {
-                        // the position's tile i, the launch's tile gi, goes to accumulator
-                        // gi mod kTmemBufs and is reduced by warpgroup i mod kEpiWG (the same
-                        // warpgroup whichever launch runs the position, so that every path
-                        // sums in the same order)
-                        const int gi = base + i;
-                        const int buf = gi % kTmemBufs;
-                        const uint32_t par = static_cast<uint32_t>(gi / kTmemBufs) & 1u;
-                        if (!mbar_wait(&tempty[buf], par ^ 1u)) { failed = true; break; }
-                        tc::fence_after_sync();
-                        const uint32_t d = tmem_base + static_cast<uint32_t>(buf * kBN);
-                        for (int s = 0; s < nslab; ++s) {
-                            if (!mbar_wait(&full[mma_stage], mma_phase)) { failed = true; break; }
-                            tc::fence_after_sync();
-#pragma unroll
-                            for (int kk = 0; kk < kBK / 16; ++kk) {
-                                const uint64_t ad = tc::smem_desc_sw128(a0 + s * kASlabBytes + kk * 32);
-                                const uint64_t bd = tc::smem_desc_sw128(b0 + mma_stage * kSlabBytes + kk * 32);
-                                tc::mma_bf16(d, ad, bd, idesc, (s | kk) != 0);
+                // A operand: rows W1[x_{k_b-1}] of this M-tile, K-major, 128-byte swizzle
+                {
+                    // one warp per A row, one lane per 16-byte chunk (r / 8 <= 32 chunks)
+                    const int cpr = p.r / 8;
+                    for (int row = ptid >> 5; row < kBM; row += kPro / 32) {
+                        const int rr = row & (rpc - 1);       // rpc is 32, 64 or 128
+                        const int prev = (rr < nrows) ? s_prev[rr] : -1;
+                        if (lane < cpr) {
+                            const int slab = lane >> 3, c = lane & 7;
+                            uint8_t* dst = sA + slab * kASlabBytes + (row >> 3) * 1024 + (row & 7) * 128 + ((c ^ (row & 7)) << 4);
+                            if (prev >= 0) {
+                                const uint16_t* src = p.E ? p.E + (static_cast<size_t>(req(rr)) * p.gamma + (row_k(req(rr), k) - 1)) * p.r
+                                                          : p.W1 + static_cast<size_t>(prev) * p.r;
+                                cp_async16(dst, src + lane * 8);
                             }
-                            tc::commit(&empty[mma_stage]);
-                            if (++mma_stage == kStages) { mma_stage = 0; mma_phase ^= 1u; }
+                            else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
                         }
-                        tc::commit(&tfull[buf]);
                     }
-                    if (failed) set_status(st, DSPARK_ERR_TIMEOUT, 11);
-                }
-                __syncwarp();
-            } else if (warp >= 4) {
-                // ---------------------------------------------------- epilogue
-                const int eg = (warp - 4) >> 2;           // warpgroup 0..kEpiWG-1
-                const int q = warp & 3;                   // TMEM lane quarter
-                const int lrow = q * 32 + lane;           // TMEM lane = A row
-                const int copy = lrow / rpc;              // which copy of the request rows
-                const int rr = lrow % rpc;                // request row within the M-tile
-                const int b = (rr < nrows) ? req(rr) : 0;
-                const int kb = (rr < nrows) ? row_k(b, k) : 0;
-                const bool valid = rr < nrows && kb > 0;
-                const bool warp_live = ((q * 32) % rpc) < nrows;
-                // U rows with the normal policy for the draft (a thread reads the two halves of
-                // each 128-byte line one sub-block apart), evict-first for the residual
-                const uint64_t pol = (kMode == kDraft) ? policy_evict_normal() : policy_evict_first();
-                const uint16_t* urow = p.U + (static_cast<size_t>(valid ? b : 0) * p.gamma + (valid ? kb - 1 : 0)) * p.V;
-                float ld2 = 0.f, lt2 = 0.f;
-                const uint16_t* trow = nullptr;
-                if constexpr (kMode == kResidual) {
-                    if (valid) {
-                        ld2 = p.ld2[b];
-                        lt2 = p.lt2[b];
-                        trow = p.T + (static_cast<size_t>(b) * (p.gamma + 1) + (kb - 1)) * p.V;
-                    }
-                }
-                const PhiloxRow prow =
-                    philox_row_setup(p.seed, static_cast<uint32_t>(kb), static_cast<uint32_t>(b),
-                                     (kMode == kDraft) ? kStreamDraftToken : kStreamVerifyToken);
-                Best best{-INFINITY, 0x7FFFFFFF, 0.f};
-                float M = -INFINITY, S = 0.f;
-                float qb = 0.f, Eq = 1.f;                 // kResidual: the running winner's q and E
-                const int i0 = eg;                        // this WG's tiles: eg, eg + kEpiWG, ...
-
-                // The thread's sub-blocks of 32 tokens: four per tile (two or one per tile and
-                // copy when each request is held twice or four times).  One compact loop body
-                // serves them all; the U words of the next sub-block (this tile's next, or the
-                // next tile's first) are loaded one sub-block ahead, so the load has a
-                // sub-block's work to land.
-                const int nsub = kBN / 32 / R;            // this copy's share of a tile: kBN / R tokens
-                const int soff = copy * (kBN / R);        // token offset of the first sub-block in a tile
-                auto load16 = [&](const uint16_t* src, int v0, uint32_t* dst) {
-#pragma unroll
-                    for (int g8 = 0; g8 < 4; ++g8) {
-                        if (valid && v0 + g8 * 8 < p.V) ld_u32x4(src + v0 + g8 * 8, dst + g8 * 4, pol);
-                        else { dst[g8 * 4] = dst[g8 * 4 + 1] = dst[g8 * 4 + 2] = dst[g8 * 4 + 3] = 0u; }
-                    }
-                };
-                uint32_t un[16];                          // U words of the next sub-block (kDraft)
-                if (kMode == kDraft && i0 < ntiles) load16(urow, (t_lo + i0) * kBN + soff, un);
-                for (int i = i0; i < ntiles; i += kEpiWG) {
-                    const int t = t_lo + i;
-                    const int buf = (base + i) % kTmemBufs;
-                    const uint32_t par = static_cast<uint32_t>((base + i) / kTmemBufs) & 1u;
-                    bool bad = false;
-                    if (!failed) bad = !mbar_wait(&tfull[buf], par);
-                    // warp-uniform: the draw's warp votes need every lane on the same path
-                    bad = __any_sync(0xffffffffu, bad);
-                    if (bad) { failed = true; set_status(st, DSPARK_ERR_TIMEOUT, 12); }
+                    cp_async_wait_all();
+                    fence_proxy_async_smem();
+                    tc::fence_before_sync();
+                    pro_sync();
                     tc::fence_after_sync();
-                    const bool have_next = (i + kEpiWG < ntiles);
-                    const int tnext = t + kEpiWG;
-#pragma unroll 1
-                    for (int j = 0; j < nsub; ++j) {
-                        const int off = soff + 32 * j;
-                        const int v0 = t * kBN + off;
-                        // the next sub-block's U (this tile's next, or the next tile's first)
-                        const int vn = (j + 1 < nsub) ? v0 + 32 : (have_next ? tnext * kBN + soff : -1);
-                        if (!warp_live || failed || v0 >= p.V) {  // warp-uniform
-                            if (kMode == kDraft && vn >= 0) load16(urow, vn, un);
-                            continue;
+                }
+
+                if (kRole == 0 && warp == 1) {
+                    // -------------------------------------------------- MMA issuer
+                    if (lane == 0) {
+                        constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN);
+                        const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+                        for (int i = 0; i < ntiles && !failed; ++i) {
+                            // the position's tile i, the launch's tile gi, goes to accumulator
+                            // gi mod kTmemBufs and is reduced by warpgroup i mod kEpiWG (the same
+                            // warpgroup whichever launch runs the position, so that every path
+                            // sums in the same order)
+                            const int gi = base + i;
+                            const int buf = gi % kTmemBufs;
+                            const uint32_t par = static_cast<uint32_t>(gi / kTmemBufs) & 1u;
+                            if (!mbar_wait(&tempty[buf], par ^ 1u)) { failed = true; break; }
+                            tc::fence_after_sync();
+                            const uint32_t d = tmem_base + static_cast<uint32_t>(buf * kBN);
+                            for (int s = 0; s < nslab; ++s) {
+                                if (!mbar_wait(&full[mma_stage], mma_phase)) { failed = true; break; }
+                                tc::fence_after_sync();
+    #pragma unroll
+                                for (int kk = 0; kk < kBK / 16; ++kk) {
+                                    const uint64_t ad = tc::smem_desc_sw128(a0 + s * kASlabBytes + kk * 32);
+                                    const uint64_t bd = tc::smem_desc_sw128(b0 + mma_stage * kSlabBytes + kk * 32);
+                                    tc::mma_bf16(d, ad, bd, idesc, (s | kk) != 0);
+                                }
+                                tc::commit(&empty[mma_stage]);
+                                if (++mma_stage == kStages) { mma_stage = 0; mma_phase ^= 1u; }
+                            }
+                            tc::commit(&tfull[buf]);
                         }
-                        uint32_t tt[16];
-                        if constexpr (kMode == kResidual) {
-                            load16(urow, v0, un);
-                            load16(trow, v0, tt);
+                        if (failed) set_status(st, DSPARK_ERR_TIMEOUT, 11);
+                    }
+                    __syncwarp();
+                } else if (kRole == 1) {
+                    // ---------------------------------------------------- epilogue
+                    const int eg = (warp - 4) >> 2;           // warpgroup 0..kEpiWG-1
+                    const int q = warp & 3;                   // TMEM lane quarter
+                    const int lrow = q * 32 + lane;           // TMEM lane = A row
+                    const int copy = lrow / rpc;              // which copy of the request rows
+                    const int rr = lrow % rpc;                // request row within the M-tile
+                    const int b = (rr < nrows) ? req(rr) : 0;
+                    const int kb = (rr < nrows) ? row_k(b, k) : 0;
+                    const bool valid = rr < nrows && kb > 0;
+                    const bool warp_live = ((q * 32) % rpc) < nrows;
+                    // U rows with the normal policy for the draft (a thread reads the two halves of
+                    // each 128-byte line one sub-block apart), evict-first for the residual
+                    const uint64_t pol = (kMode == kDraft) ? policy_evict_normal() : policy_evict_first();
+                    const uint16_t* urow = p.U + (static_cast<size_t>(valid ? b : 0) * p.gamma + (valid ? kb - 1 : 0)) * p.V;
+                    [[maybe_unused]] float ld2 = 0.f, lt2 = 0.f;   // kResidual
+                    [[maybe_unused]] const uint16_t* trow = nullptr;
+                    if constexpr (kMode == kResidual) {
+                        if (valid) {
+                            ld2 = p.ld2[b];
+                            lt2 = p.lt2[b];
+                            trow = p.T + (static_cast<size_t>(b) * (p.gamma + 1) + (kb - 1)) * p.V;
                         }
-                        float y[32];
-                        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kBN + off;
-                        tc::tmem_ld32(taddr, y);
-                        tc::tmem_ld_wait();
-                        // raw logits z = acc + U (each bf16 U added to its float32 accumulator by one
-                        // mixed-precision add); the draw scales by cscale
-#pragma unroll
-                        for (int w = 0; w < 16; ++w) add_bf16_pair(un[w], y[2 * w], y[2 * w + 1]);
-                        // this sub-block's U words are consumed: fetch the next one's, in flight
-                        // while this sub-block is reduced
-                        if (kMode == kDraft && vn >= 0) load16(urow, vn, un);
-                        if (v0 + 32 > p.V) {
-#pragma unroll
-                            for (int w = 0; w < 32; ++w)
-                                if (v0 + w >= p.V) y[w] = -INFINITY;
+                    }
+                    const PhiloxRow prow =
+                        philox_row_setup(p.seed, static_cast<uint32_t>(kb), static_cast<uint32_t>(b),
+                                         (kMode == kDraft) ? kStreamDraftToken : kStreamVerifyToken);
+                    Best best{-INFINITY, 0x7FFFFFFF, 0.f};
+                    float M = -INFINITY, S = 0.f;
+                    float qb = 0.f, Eq = 1.f;                 // kResidual: the running winner's q and E
+                    const int i0 = eg;                        // this WG's tiles: eg, eg + kEpiWG, ...
+
+                    // The thread's sub-blocks of 32 tokens: four per tile (two or one per tile and
+                    // copy when each request is held twice or four times).  One compact loop body
+                    // serves them all; the U words of the next sub-block (this tile's next, or the
+                    // next tile's first) are loaded one sub-block ahead, so the load has a
+                    // sub-block's work to land.
+                    const int nsub = kBN / 32 / R;            // this copy's share of a tile: kBN / R tokens
+                    const int soff = copy * (kBN / R);        // token offset of the first sub-block in a tile
+                    auto load16 = [&](const uint16_t* src, int v0, uint32_t* dst) {
+    #pragma unroll
+                        for (int g8 = 0; g8 < 4; ++g8) {
+                            if (valid && v0 + g8 * 8 < p.V) ld_u32x4(src + v0 + g8 * 8, dst + g8 * 4, pol);
+                            else { dst[g8 * 4] = dst[g8 * 4 + 1] = dst[g8 * 4 + 2] = dst[g8 * 4 + 3] = 0u; }
                         }
-                        if constexpr (kMode == kDraft) {
-                            if (p.debug_z != nullptr) {
-                                if (valid)                // copies own disjoint halves
-                                    for (int w = 0; w < 32; ++w)
-                                        if (v0 + w < p.V) p.debug_z[static_cast<size_t>(b) * p.V + v0 + w] = y[w] * p.cscale;
+                    };
+                    uint32_t un[16];                          // U words of the next sub-block (kDraft)
+                    if (kMode == kDraft && i0 < ntiles) load16(urow, (t_lo + i0) * kBN + soff, un);
+                    for (int i = i0; i < ntiles; i += kEpiWG) {
+                        const int t = t_lo + i;
+                        const int buf = (base + i) % kTmemBufs;
+                        const uint32_t par = static_cast<uint32_t>((base + i) / kTmemBufs) & 1u;
+                        bool bad = false;
+                        if (!failed) bad = !mbar_wait(&tfull[buf], par);
+                        // warp-uniform: the draw's warp votes need every lane on the same path
+                        bad = __any_sync(0xffffffffu, bad);
+                        if (bad) { failed = true; set_status(st, DSPARK_ERR_TIMEOUT, 12); }
+                        tc::fence_after_sync();
+                        const bool have_next = (i + kEpiWG < ntiles);
+                        const int tnext = t + kEpiWG;
+    #pragma unroll 1
+                        for (int j = 0; j < nsub; ++j) {
+                            const int off = soff + 32 * j;
+                            const int v0 = t * kBN + off;
+                            // the next sub-block's U (this tile's next, or the next tile's first)
+                            const int vn = (j + 1 < nsub) ? v0 + 32 : (have_next ? tnext * kBN + soff : -1);
+                            if (!warp_live || failed || v0 >= p.V) {  // warp-uniform
+                                if (kMode == kDraft && vn >= 0) load16(urow, vn, un);
                                 continue;
                             }
-                            if (p.greedy) {                // cscale = 1
-#pragma unroll
-                                for (int w = 0; w < 32; ++w)
-                                    if (y[w] > best.key) { best.key = y[w]; best.idx = v0 + w; }
-                            } else {
-                                draw32(y, p.cscale, v0, prow, p.keys, best, M, S);
+                            [[maybe_unused]] uint32_t tt[16];   // kResidual: t words
+                            if constexpr (kMode == kResidual) {
+                                load16(urow, v0, un);
+                                load16(trow, v0, tt);
                             }
-                        } else {
-                            // residual q = max(0, p_t - p_d), p_d = 2^(y - ld2), p_t = 2^(t c - lt2);
-                            // the winner maximises q_v / E_v over the thread's tokens
-                            const uint32_t qbase = static_cast<uint32_t>(v0) >> 2;
-#pragma unroll
-                            for (int qq = 0; qq < 8; ++qq) {
-                                const U4 pw = philox_row(prow, qbase + qq, p.keys);
-                                const uint32_t wv[4] = {pw.x, pw.y, pw.z, pw.w};
-#pragma unroll
-                                for (int jj = 0; jj < 4; ++jj) {
-                                    const int w = 4 * qq + jj;
-                                    const float tv = (w & 1) ? bf16hi(tt[w >> 1]) : bf16lo(tt[w >> 1]);
-                                    const float pd = fast_exp2(fmaf(y[w], p.cscale, -ld2));
-                                    const float ptv = fast_exp2(tv * p.cscale - lt2);
-                                    const float qv = (v0 + w < p.V) ? fmaxf(ptv - pd, 0.f) : 0.f;
-                                    const float E = exp_draw(wv[jj]);
-                                    if (qv * Eq > qb * E) { qb = qv; Eq = E; best.idx = v0 + w; }
+                            float y[32];
+                            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kBN + off;
+                            tc::tmem_ld32(taddr, y);
+                            tc::tmem_ld_wait();
+                            // raw logits z = acc + U (each bf16 U added to its float32 accumulator by one
+                            // mixed-precision add); the draw scales by cscale
+    #pragma unroll
+                            for (int w = 0; w < 16; ++w) add_bf16_pair(un[w], y[2 * w], y[2 * w + 1]);
+                            // this sub-block's U words are consumed: fetch the next one's, in flight
+                            // while this sub-block is reduced
+                            if (kMode == kDraft && vn >= 0) load16(urow, vn, un);
+                            if (v0 + 32 > p.V) {
+    #pragma unroll
+                                for (int w = 0; w < 32; ++w)
+                                    if (v0 + w >= p.V) y[w] = -INFINITY;
+                            }
+                            if constexpr (kMode == kDraft) {
+                                if (p.debug_z != nullptr) {
+                                    if (valid)                // copies own disjoint halves
+                                        for (int w = 0; w < 32; ++w)
+                                            if (v0 + w < p.V) p.debug_z[static_cast<size_t>(b) * p.V + v0 + w] = y[w] * p.cscale;
+                                    continue;
+                                }
+                                if (p.greedy) {                // cscale = 1
+    #pragma unroll
+                                    for (int w = 0; w < 32; ++w)
+                                        if (y[w] > best.key) { best.key = y[w]; best.idx = v0 + w; }
+                                } else {
+                                    draw32(y, p.cscale, v0, prow, p.keys, best, M, S);
+                                }
+                            } else {
+                                // residual q = max(0, p_t - p_d), p_d = 2^(y - ld2), p_t = 2^(t c - lt2);
+                                // the winner maximises q_v / E_v over the thread's tokens
+                                const uint32_t qbase = static_cast<uint32_t>(v0) >> 2;
+    #pragma unroll
+                                for (int qq = 0; qq < 8; ++qq) {
+                                    const U4 pw = philox_row(prow, qbase + qq, p.keys);
+                                    const uint32_t wv[4] = {pw.x, pw.y, pw.z, pw.w};
+    #pragma unroll
+                                    for (int jj = 0; jj < 4; ++jj) {
+                                        const int w = 4 * qq + jj;
+                                        const float tv = (w & 1) ? bf16hi(tt[w >> 1]) : bf16lo(tt[w >> 1]);
+                                        const float pd = fast_exp2(fmaf(y[w], p.cscale, -ld2));
+                                        const float ptv = fast_exp2(tv * p.cscale - lt2);
+                                        const float qv = (v0 + w < p.V) ? fmaxf(ptv - pd, 0.f) : 0.f;
+                                        const float E = exp_draw(wv[jj]);
+                                        if (qv * Eq > qb * E) { qb = qv; Eq = E; best.idx = v0 + w; }
+                                    }
                                 }
                             }
                         }
+                        tc::fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&tempty[buf]);
                     }
-                    tc::fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&tempty[buf]);
-                }
-                if (kMode == kResidual && qb > 0.f) best.key = fast_log2(qb) - fast_log2(Eq);
-                // the next position's first U tile of this lane does not depend on x_k:
-                // bring it into L2 while the grid hands over
-                if (kMode == kDraft && k < k1 && valid && warp_live) {
-                    const int inext = eg;                 // its first tile of the next position
-                    if (inext < ntiles) {
-                        const uint16_t* unx = p.U + (static_cast<size_t>(b) * p.gamma + k) * p.V;
-                        for (int off = soff; off < soff + 32 * nsub; off += 64) {
-                            const int v0 = (t_lo + inext) * kBN + off;
-                            if (v0 < p.V) prefetch_l2(unx + v0);
+                    if (kMode == kResidual && qb > 0.f) best.key = fast_log2(qb) - fast_log2(Eq);
+                    // the next position's first U tile of this lane does not depend on x_k:
+                    // bring it into L2 while the grid hands over
+                    if (kMode == kDraft && k < k1 && valid && warp_live) {
+                        const int inext = eg;                 // its first tile of the next position
+                        if (inext < ntiles) {
+                            const uint16_t* unx = p.U + (static_cast<size_t>(b) * p.gamma + k) * p.V;
+                            for (int off = soff; off < soff + 32 * nsub; off += 64) {
+                                const int v0 = (t_lo + inext) * kBN + off;
+                                if (v0 < p.V) prefetch_l2(unx + v0);
+                            }
                         }
                     }
+                    rowres[eg * kBM + lrow] = RowRes{best, M, S};
                 }
-                rowres[eg * kBM + lrow] = RowRes{best, M, S};
-            }
-            pro_sync();
+                pro_sync();
 
-            // --------------------------------------- publish this position
-            if (warp >= 4 && warp < 8 && p.debug_z == nullptr) {
-                const int rr = (warp - 4) * 32 + lane;
-                const int b = (rr < nrows) ? req(rr) : 0;
-                if (rr < nrows && row_k(b, k) > 0) {
-                    Best b0{-INFINITY, 0x7FFFFFFF, 0.f};
-                    float m = -INFINITY, s = 0.f;
-                    for (int e = 0; e < kEpiWG; ++e)
-                        for (int c = 0; c < R; ++c) {
-                            const RowRes r1 = rowres[e * kBM + c * rpc + rr];
-                            best_take(b0, r1.best.key, r1.best.idx, r1.best.y);
-                            lse_merge(m, s, r1.m, r1.s);
+                // --------------------------------------- publish this position
+                if (kRole == 1 && warp < 8 && p.debug_z == nullptr) {
+                    const int rr = (warp - 4) * 32 + lane;
+                    const int b = (rr < nrows) ? req(rr) : 0;
+                    if (rr < nrows && row_k(b, k) > 0) {
+                        Best b0{-INFINITY, 0x7FFFFFFF, 0.f};
+                        float m = -INFINITY, s = 0.f;
+                        for (int e = 0; e < kEpiWG; ++e)
+                            for (int c = 0; c < R; ++c) {
+                                const RowRes r1 = rowres[e * kBM + c * rpc + rr];
+                                best_take(b0, r1.best.key, r1.best.idx, r1.best.y);
+                                lse_merge(m, s, r1.m, r1.s);
+                            }
+                        const size_t slot = static_cast<size_t>(k - 1) * p.B + b;
+                        if (kMode == kDraft && !p.greedy) {
+                            p.ws.part[slot * kMaxChunks + pc] = make_float2(m, s);
+                            p.ws.ybest[slot * kMaxChunks + pc] = b0.y;
                         }
-                    const size_t slot = static_cast<size_t>(k - 1) * p.B + b;
-                    if (kMode == kDraft && !p.greedy) {
-                        p.ws.part[slot * kMaxChunks + pc] = make_float2(m, s);
-                        p.ws.ybest[slot * kMaxChunks + pc] = b0.y;
+                        if (b0.key > -INFINITY) atomicMax(&p.ws.words[slot], pack_key(b0.key, static_cast<uint32_t>(b0.idx)));
+                        // the next A row is one of the CTAs' best tokens; bring ours into L2
+                        if (kMode == kDraft && k < k1 && b0.idx >= 0 && b0.idx < p.V)
+                            for (int off = 0; off < p.r * 2; off += 128)
+                                prefetch_l2(reinterpret_cast<const uint8_t*>(p.W1) + static_cast<size_t>(b0.idx) * p.r * 2 + off);
                     }
-                    if (b0.key > -INFINITY) atomicMax(&p.ws.words[slot], pack_key(b0.key, static_cast<uint32_t>(b0.idx)));
-                    // the next A row is one of the CTAs' best tokens; bring ours into L2
-                    if (kMode == kDraft && k < k1 && b0.idx >= 0 && b0.idx < p.V)
-                        for (int off = 0; off < p.r * 2; off += 128)
-                            prefetch_l2(reinterpret_cast<const uint8_t*>(p.W1) + static_cast<size_t>(b0.idx) * p.r * 2 + off);
+                }
+                if (kMode == kDraft && multi && k < k1) arrive();
+                else pro_sync();                              // rowres is rewritten by the next position
+            }
+
+        };
+        if (warp < 4) {
+            // warpgroup 0 (producer, MMA issuer, two helpers) hands registers to the epilogue
+            reg_dealloc<kCtlRegs>();
+            if (warp == 0) {
+                // ---------------------------------------------------- TMA producer
+                // streams W2 for every position without waiting for the prologues
+                if (lane == 0) {
+                    const uint64_t pol = policy_evict_last();
+                    int stage = 0;
+                    uint32_t phase = 0;
+                    bool failed = false;
+                    for (int k = k0; k <= k1 && !failed; ++k)
+                        for (int t = t_lo; t < t_hi && !failed; ++t)
+                            for (int s = 0; s < nslab; ++s) {
+                                if (!mbar_wait(&empty[stage], phase ^ 1u)) { failed = true; break; }
+                                mbar_arrive_expect_tx(&full[stage], kSlabBytes);
+                                tc::tma_load_2d(sB + stage * kSlabBytes, &tmW2, s * kBK, t * kBN, &full[stage], pol);
+                                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                            }
+                    if (failed) set_status(st, DSPARK_ERR_TIMEOUT, 10);
+                }
+                __syncwarp();
+            } else {
+                positions(RoleTag<0>{});
+            }
+            reg_alloc<kLaunchRegs>();
+        } else {
+            reg_alloc<kEpiRegs>();
+            positions(RoleTag<1>{});
+            reg_dealloc<kLaunchRegs>();
+        }
+        if (warp != 0) {
+            if (kMode == kResidual && p.fuse_tail) {
+                // ------------------------------------------------ final tokens
+                arrive();
+                wait_all();                                   // every CTA published its residual winners
+                if (warp >= 2 && *s_fail == 0) {
+                    const int pair = (warp - 2) >> 1;
+                    for (int b = blockIdx.x + pair * gridDim.x; b < p.B; b += kPairs * gridDim.x)
+                        finish_pair<true>(p.fin, b, p.gamma, p.V, p.cscale, p.seed, st, 2 + pair, xch + 2 * pair,
+                                          xchi + 2 * pair);
                 }
             }
-            if (kMode == kDraft && multi && k < k1) arrive();
-            else pro_sync();                              // rowres is rewritten by the next position
-        }
-
-        if (kMode == kResidual && p.fuse_tail) {
-            // ------------------------------------------------ final tokens
-            arrive();
-            wait_all();                                   // every CTA published its residual winners
-            if (warp >= 2 && *s_fail == 0) {
-                const int pair = (warp - 2) >> 1;
-                for (int b = blockIdx.x + pair * gridDim.x; b < p.B; b += kPairs * gridDim.x)
-                    finish_pair<true>(p.fin, b, p.gamma, p.V, p.cscale, p.seed, st, 2 + pair, xch + 2 * pair,
-                                      xchi + 2 * pair);
-            }
-        }
-        if (kMode == kDraft && p.fuse_tail && p.debug_z == nullptr) {
-            // ------------------------------------------ x_gamma and finalize
-            const int cta = static_cast<int>(blockIdx.x), ncta = static_cast<int>(gridDim.x);
-            const int nown = (cta < p.B) ? (p.B - 1 - cta) / ncta + 1 : 0;
-            arrive();
-            wait_all();                                   // every CTA published the last position
-            for (int j = ptid; j < nown; j += kPro) {
-                const int b = cta + j * ncta;
-                p.x[b * p.gamma + k1 - 1] = (*s_fail == 0) ? winner(b, k1) : 0;
-            }
-            pro_sync();
-            // one warp per (owned request, position)
-            for (int item = warp - 1; item < nown * p.gamma; item += kPro / 32) {
-                const int b = cta + (item / p.gamma) * ncta, k = item % p.gamma + 1;
-                finalize_position<true>(b, k, p.B, p.gamma, p.V, p.H, p.r, p.h, p.W1, p.w, p.bias, p.x0, p.x,
-                                        p.greedy, P, kBN, NT, p.ws.part, p.ws.ybest, p.lse_d, p.logp_d, p.c, st);
-            }
-            pro_sync();
-            for (int j = ptid; j < nown; j += kPro) {     // survival a_k = prod c_1..c_k, in k order
-                const int b = cta + j * ncta;
-                float surv = 1.f;
-                for (int kk = 0; kk < p.gamma; ++kk) {
-                    const size_t o = static_cast<size_t>(b) * p.gamma + kk;
-                    surv = surv * p.c[o];
-                    p.a[o] = surv;
+            if (kMode == kDraft && p.fuse_tail && p.debug_z == nullptr) {
+                // ------------------------------------------ x_gamma and finalize
+                const int cta = static_cast<int>(blockIdx.x), ncta = static_cast<int>(gridDim.x);
+                const int nown = (cta < p.B) ? (p.B - 1 - cta) / ncta + 1 : 0;
+                arrive();
+                wait_all();                                   // every CTA published the last position
+                for (int j = ptid; j < nown; j += kPro) {
+                    const int b = cta + j * ncta;
+                    p.x[b * p.gamma + k1 - 1] = (*s_fail == 0) ? winner(b, k1) : 0;
+                }
+                pro_sync();
+                // one warp per (owned request, position)
+                for (int item = warp - 1; item < nown * p.gamma; item += kPro / 32) {
+                    const int b = cta + (item / p.gamma) * ncta, k = item % p.gamma + 1;
+                    finalize_position<true>(b, k, p.B, p.gamma, p.V, p.H, p.r, p.h, p.W1, p.w, p.bias, p.x0, p.x,
+                                            p.greedy, P, kBN, NT, p.ws.part, p.ws.ybest, p.lse_d, p.logp_d, p.c, st);
+                }
+                pro_sync();
+                for (int j = ptid; j < nown; j += kPro) {     // survival a_k = prod c_1..c_k, in k order
+                    const int b = cta + j * ncta;
+                    float surv = 1.f;
+                    for (int kk = 0; kk < p.gamma; ++kk) {
+                        const size_t o = static_cast<size_t>(b) * p.gamma + kk;
+                        surv = surv * p.c[o];
+                        p.a[o] = surv;
+                    }
                 }
             }
         }
     }
-
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 1) {
@@ -977,6 +1016,12 @@ template <int kMode>
 dspark_status_t launch_tc(const CUtensorMap& map, const TcParams& p, int grid, cudaStream_t s, bool cooperative) {
     static OncePerDevice once;
     if (once.run(current_device(), [] {
+            // the kernel's register split (setmaxnreg) assumes kLaunchRegs a thread at launch:
+            // never launch a build that allocated another count
+            cudaFuncAttributes fa{};
+            cudaError_t e = cudaFuncGetAttributes(&fa, bias_engine_tc<kMode>);
+            if (e != cudaSuccess) return e;
+            if (fa.numRegs != static_cast<int>(kLaunchRegs)) return cudaErrorInvalidDeviceFunction;
             return cudaFuncSetAttribute(bias_engine_tc<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(kTcSmem));
         }) != cudaSuccess)

@@ -145,32 +145,45 @@ __device__ __forceinline__ float group_max(const uint4 v) {
     }
 }
 
-// (m, s) += the group's elements, s a sum of 2^((x - m) log2e): a larger group
-// max first rescales s (rare once m has settled).  For bf16 the exponent is one
-// fused x log2e - (m log2e): every term carries the rounding error r of m log2e
-// (|r| <= ulp(m log2e) / 2, a relative 1e-5 at |m| = 100, inside the bf16 bound).
-// For float32, whose bound is tighter, x - m is formed first, so the maximum's
-// term is exactly 1.
+// (m, s) += the group's elements, s a sum of 2^((x - m) log2e).  m is a running
+// reference, not the running max: the group is summed against the current m, and
+// only when that sum leaves [0, 2^32] (an element at least 22 above m, or no m
+// yet: inf or NaN) is m moved to the group's max, s rescaled and the group summed
+// again -- so the max of a group is taken for a thread's first groups of a row and
+// rarely after.  Terms up to 2^32 change no relative precision of the float sums.
+// For bf16 the exponent is one fused x log2e - (m log2e): every term carries the
+// rounding error r of m log2e (|r| <= ulp(m log2e) / 2, a relative 1e-5 at
+// |m| = 100, inside the bf16 bound).  For float32, whose bound is tighter, x - m is
+// formed first.
 template <bool kBF16>
 __device__ __forceinline__ void group_lse(const uint4 v, float& m, float& s) {
     constexpr int EPG = TVTraits<kBF16>::kEPG;
-    const float gm = group_max<kBF16>(v);
-    if (!(gm > -INFINITY)) return;                        // no mass in this group
-    if (gm > m) {
-        s = (s > 0.f) ? s * fast_exp2((m - gm) * kLog2e) : 0.f;
-        m = gm;
-    }
     float a[EPG];
     unpack<kBF16>(v, a);
-    const unsigned long long L2E = pk(kLog2e, kLog2e);
-    const unsigned long long nm = kBF16 ? pk(-m * kLog2e, -m * kLog2e) : pk(-m, -m);
-    unsigned long long acc = pk(0.f, 0.f);
+    // the group's sum of 2^((x - mm) log2e)
+    auto terms = [&](float mm) -> float {
+        const unsigned long long L2E = pk(kLog2e, kLog2e);
+        const unsigned long long nm = kBF16 ? pk(-mm * kLog2e, -mm * kLog2e) : pk(-mm, -mm);
+        unsigned long long acc = pk(0.f, 0.f);
 #pragma unroll
-    for (int e = 0; e < EPG; e += 2) {
-        const float2 y = kBF16 ? upk(fma2(pk(a[e], a[e + 1]), L2E, nm)) : upk(mul2(add2(pk(a[e], a[e + 1]), nm), L2E));
-        acc = add2(acc, pk(fast_exp2(y.x), fast_exp2(y.y)));
+        for (int e = 0; e < EPG; e += 2) {
+            const float2 y = kBF16 ? upk(fma2(pk(a[e], a[e + 1]), L2E, nm)) : upk(mul2(add2(pk(a[e], a[e + 1]), nm), L2E));
+            acc = add2(acc, pk(fast_exp2(y.x), fast_exp2(y.y)));
+        }
+        return upk(acc).x + upk(acc).y;
+    };
+    float g = terms(m);
+    if (!(g <= 0x1p32f)) {
+        // rare: an element far above m, or no m yet (inf or NaN): rebase on the group's max
+        const float gm = group_max<kBF16>(v);
+        if (!(gm > -INFINITY)) return;                    // no mass in this group
+        if (gm > m) {
+            s = (s > 0.f) ? s * fast_exp2((m - gm) * kLog2e) : 0.f;
+            m = gm;
+        }
+        g = terms(m);
     }
-    s += upk(acc).x + upk(acc).y;
+    s += g;
 }
 
 // Block-wide merge of every thread's (m, s) pair for d and t: all threads get (L_d, L_t)
