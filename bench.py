@@ -86,6 +86,32 @@ def recorded_engine_traffic():
     return d.get("dram_bytes_per_launch") if d.get("source_hash") == engine_source_hash() else None
 
 
+def recorded_engine_issue():
+    """Warp instructions per logit of the draft launch (an ncu count on a small case of
+    the same kernel), while the engine's sources still hash to the captured version."""
+    p = os.path.join(ROOT, "profiles", "draft_engine_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    iss = d.get("issue")
+    if not iss or iss.get("source_hash") != engine_source_hash():
+        return None
+    return iss["warp_instructions"] / iss["logits"]
+
+
+def issue_roof(logits, launch_us, sm_mhz, n_sm):
+    """The issue roof of the draft launch: its warp instructions at one instruction a
+    cycle on every scheduler (4 per SM) at the sampled SM clock, against the launch time."""
+    wipl = recorded_engine_issue()
+    if wipl is None or not sm_mhz or not launch_us:
+        return None
+    ideal_us = logits * wipl / (n_sm * 4 * sm_mhz)
+    return {"warp_instructions_per_logit": round(wipl, 4), "sm_mhz": sm_mhz, "sms": n_sm,
+            "ideal_us": round(ideal_us, 1), "frac": round(ideal_us / launch_us, 4),
+            "source": "ncu instruction count of the same kernel on B = 1024, gamma = 2"}
+
+
 def smi_index(local):
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").strip()
     if vis:
@@ -389,6 +415,8 @@ def run_gpu(args):
     ms_per_step = total_ms / args.steps
     roofline = dict(head["roofline"])
     roofline["traffic"] = args.phase_traffic if args.phase_traffic is not None else recorded_engine_traffic()
+    roofline["issue"] = issue_roof(B * G * V, roofline["avg_launch_us"], (clk or {}).get("sm_mhz"),
+                                   torch.cuda.get_device_properties(dev).multi_processor_count)
 
     # end to end: every step's per-call inputs (U, h, x0, the SPS table and the target
     # logits t) are in pinned host memory and go to the C-ABI calls as host buffers: the

@@ -441,8 +441,8 @@ int g_draft_path = 0;
 // Up to this many requests the bf16 Markov-head draft runs on the small-batch
 // GEMV path.  Measured on the Qwen3 shape (V 151936, r 256, gamma 7, T 0.7):
 //   B            1     4     8     9    12    16
-//   GEMV path  118   132   149   171   187   206 us
-//   tcgen05    153   156   159   160   162   164 us
+//   GEMV path  118   131   147   168   184   206 us
+//   tcgen05    151   153   155   155   156   159 us
 constexpr int kGemvMaxBatch = 8;
 
 dspark_status_t launch_winner(int B, int gamma, int V, int k, int32_t* x, DraftWs ws, cudaStream_t s) {

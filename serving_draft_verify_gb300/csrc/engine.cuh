@@ -706,7 +706,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                             for (int s = 0; s < nslab; ++s) {
                                 if (!mbar_wait(&full[mma_stage], mma_phase)) { failed = true; break; }
                                 tc::fence_after_sync();
-    #pragma unroll
+#pragma unroll
                                 for (int kk = 0; kk < kBK / 16; ++kk) {
                                     const uint64_t ad = tc::smem_desc_sw128(a0 + s * kASlabBytes + kk * 32);
                                     const uint64_t bd = tc::smem_desc_sw128(b0 + mma_stage * kSlabBytes + kk * 32);
@@ -760,7 +760,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                     const int nsub = kBN / 32 / R;            // this copy's share of a tile: kBN / R tokens
                     const int soff = copy * (kBN / R);        // token offset of the first sub-block in a tile
                     auto load16 = [&](const uint16_t* src, int v0, uint32_t* dst) {
-    #pragma unroll
+#pragma unroll
                         for (int g8 = 0; g8 < 4; ++g8) {
                             if (valid && v0 + g8 * 8 < p.V) ld_u32x4(src + v0 + g8 * 8, dst + g8 * 4, pol);
                             else { dst[g8 * 4] = dst[g8 * 4 + 1] = dst[g8 * 4 + 2] = dst[g8 * 4 + 3] = 0u; }
@@ -780,7 +780,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                         tc::fence_after_sync();
                         const bool have_next = (i + kEpiWG < ntiles);
                         const int tnext = t + kEpiWG;
-    #pragma unroll 1
+#pragma unroll 1
                         for (int j = 0; j < nsub; ++j) {
                             const int off = soff + 32 * j;
                             const int v0 = t * kBN + off;
@@ -801,13 +801,13 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                             tc::tmem_ld_wait();
                             // raw logits z = acc + U (each bf16 U added to its float32 accumulator by one
                             // mixed-precision add); the draw scales by cscale
-    #pragma unroll
+#pragma unroll
                             for (int w = 0; w < 16; ++w) add_bf16_pair(un[w], y[2 * w], y[2 * w + 1]);
                             // this sub-block's U words are consumed: fetch the next one's, in flight
                             // while this sub-block is reduced
                             if (kMode == kDraft && vn >= 0) load16(urow, vn, un);
                             if (v0 + 32 > p.V) {
-    #pragma unroll
+#pragma unroll
                                 for (int w = 0; w < 32; ++w)
                                     if (v0 + w >= p.V) y[w] = -INFINITY;
                             }
@@ -819,7 +819,7 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                                     continue;
                                 }
                                 if (p.greedy) {                // cscale = 1
-    #pragma unroll
+#pragma unroll
                                     for (int w = 0; w < 32; ++w)
                                         if (y[w] > best.key) { best.key = y[w]; best.idx = v0 + w; }
                                 } else {
@@ -829,11 +829,11 @@ bias_engine_tc(const __grid_constant__ CUtensorMap tmW2, const TcParams p) {
                                 // residual q = max(0, p_t - p_d), p_d = 2^(y - ld2), p_t = 2^(t c - lt2);
                                 // the winner maximises q_v / E_v over the thread's tokens
                                 const uint32_t qbase = static_cast<uint32_t>(v0) >> 2;
-    #pragma unroll
+#pragma unroll
                                 for (int qq = 0; qq < 8; ++qq) {
                                     const U4 pw = philox_row(prow, qbase + qq, p.keys);
                                     const uint32_t wv[4] = {pw.x, pw.y, pw.z, pw.w};
-    #pragma unroll
+#pragma unroll
                                     for (int jj = 0; jj < 4; ++jj) {
                                         const int w = 4 * qq + jj;
                                         const float tv = (w & 1) ? bf16hi(tt[w >> 1]) : bf16lo(tt[w >> 1]);
