@@ -77,13 +77,16 @@ def engine_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_engine_traffic():
+def recorded_engine_traffic(l2_resident=False):
+    """DRAM bytes of one draft launch (ncu), with or without W2 held in L2, while the
+    engine's sources still hash to the captured version."""
     p = os.path.join(ROOT, "profiles", "draft_engine_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    return d.get("dram_bytes_per_launch") if d.get("source_hash") == engine_source_hash() else None
+    key = "dram_bytes_per_launch_l2_resident" if l2_resident else "dram_bytes_per_launch"
+    return d.get(key) if d.get("source_hash") == engine_source_hash() else None
 
 
 def recorded_engine_issue():
@@ -110,6 +113,18 @@ def issue_roof(logits, launch_us, sm_mhz, n_sm):
     return {"warp_instructions_per_logit": round(wipl, 4), "sm_mhz": sm_mhz, "sms": n_sm,
             "ideal_us": round(ideal_us, 1), "frac": round(ideal_us / launch_us, 4),
             "source": "ncu instruction count of the same kernel on B = 1024, gamma = 2"}
+
+
+def apply_l2_residency(dsv, args):
+    """--l2-residency: the library keeps W2 (V x r bf16 of the Markov head, the same shape
+    in every serving config here) in L2 for the draft and verify calls; returns the bytes
+    set aside, 0 when off."""
+    from serving_draft_verify_gb300 import workloads as wl
+    if not getattr(args, "l2_residency", False):
+        return 0
+    nbytes = wl.HIGH_CONC.V * wl.HIGH_CONC.r * 2
+    dsv.dspark_set_l2_residency(nbytes)
+    return nbytes
 
 
 def smi_index(local):
@@ -256,6 +271,7 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     dsv.load()
+    l2_keep = apply_l2_residency(dsv, args)
     lib = dsv._binding.load()
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -414,7 +430,8 @@ def run_gpu(args):
     value = rows / (total_ms * 1e-3)
     ms_per_step = total_ms / args.steps
     roofline = dict(head["roofline"])
-    roofline["traffic"] = args.phase_traffic if args.phase_traffic is not None else recorded_engine_traffic()
+    roofline["traffic"] = (args.phase_traffic if args.phase_traffic is not None
+                           else recorded_engine_traffic(l2_resident=bool(l2_keep)))
     roofline["issue"] = issue_roof(B * G * V, roofline["avg_launch_us"], (clk or {}).get("sm_mhz"),
                                    torch.cuda.get_device_properties(dev).multi_processor_count)
 
@@ -481,9 +498,12 @@ def run_gpu(args):
             del sv_
             torch.cuda.empty_cache()
 
-    # accept-rate TV on the training workload (16384 x 151936 bf16 rows)
+    # accept-rate TV on the training workload (16384 x 151936 bf16 rows): its second pass
+    # needs the whole L2, so W2's persisting lines (--l2-residency) are released first
     tv = None
     if not args.skip_tv:
+        if l2_keep:
+            dsv.dspark_set_l2_residency(0)
         d_, t_ = wl.make_tv_inputs(wl.TV_TRAIN, device=dev)
         cst = torch.empty(d_.shape[0], dtype=torch.float32, device=dev)
         ws_t = torch.empty(256, dtype=torch.uint8, device=dev)
@@ -511,6 +531,8 @@ def run_gpu(args):
         torch.cuda.empty_cache()
     # the draft block with the gated and recurrent heads (one launch per position plus a
     # head kernel between positions), on the Qwen3-8B-shaped workload
+    if l2_keep and not args.skip_tv:
+        apply_l2_residency(dsv, args)                     # back on for the draft extras below
     heads_x = None
     if not args.skip_heads:
         heads_x = {}
@@ -566,7 +588,9 @@ def run_gpu(args):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded; shapes of the pages' high-concurrency serving setting)",
-            "config": dict(workload_config(world), cuda_graph=head["cuda_graph"]),
+            "config": dict(workload_config(world), cuda_graph=head["cuda_graph"],
+                           l2_residency=(f"W2 held in L2 by a persisting access-policy window ({l2_keep} B set aside)"
+                                         if l2_keep else "off")),
             "hbm_gbs": head["round_hbm_gbs"], "hbm_frac": head["round_hbm_gbs"] / peak, "roofline": roofline,
             "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clk,
             "extra": {"per_call": head["per_call"], "scheduled_rows": head["scheduled_rows"],
@@ -726,6 +750,7 @@ def run_round_case(args):
 
     dev = torch.device("cuda", 0)
     dsv.load()
+    l2_keep = apply_l2_residency(dsv, args)
     lib = dsv._binding.load()
     B, G = (int(x) for x in args.round_case.split(":"))
     sv = Serving(dsv, lib, wl.scaled(wl.HIGH_CONC, B=B, gamma=G), dev)
@@ -748,6 +773,7 @@ def run_round_case(args):
     assert sv.status_ok()
     ell = sv.outs["ell"].cpu()
     print(json.dumps({"workload": f"round, B={B} gamma={G} V={sv.cfg.V} r={sv.cfg.r} T={sv.T}",
+                      "l2_residency": l2_keep,
                       "draft_us": statistics.median(us[0]), "schedule_us": statistics.median(us[1]),
                       "verify_us": statistics.median(us[2]), "scheduled_rows": int((ell + 1).sum()),
                       "rejected": int((sv.outv["n_accept"].cpu() < ell).sum())}))
@@ -766,6 +792,7 @@ def run_draft_only(args):
 
     dev = torch.device("cuda", 0)
     dsv.load()
+    l2_keep = apply_l2_residency(dsv, args)
     lib = dsv._binding.load()
     B, G = (int(x) for x in args.draft_case.split(":"))
     dsv._binding.set_draft_path(DRAFT_PATHS[args.draft_path])
@@ -788,7 +815,7 @@ def run_draft_only(args):
     cfg = sv.cfg
     nb = draft_launch_bytes(cfg.B, cfg.gamma, cfg.V, cfg.H, cfg.r)
     print(json.dumps({"workload": f"draft block, B={B} gamma={G} V={cfg.V} r={cfg.r} T={T}",
-                      "path": args.draft_path, "median_ms": m,
+                      "path": args.draft_path, "l2_residency": l2_keep, "median_ms": m,
                       "gbs": nb / (m * 1e-3) / 1e9, "logits_per_ms": B * G * cfg.V / m}))
 
 
@@ -816,6 +843,9 @@ def main():
     ap.add_argument("--draft-temperature", type=float, default=None, help="temperature of --draft-case")
     ap.add_argument("--draft-path", default="auto", choices=sorted(DRAFT_PATHS),
                     help="draft path of --draft-case: by batch size, the tcgen05 engine, or the CUDA-core GEMV")
+    ap.add_argument("--l2-residency", action="store_true",
+                    help="keep W2 in L2 with the library's opt-in persisting window (dspark_set_l2_residency) for "
+                         "the draft and verify calls; off by default")
     ap.add_argument("--round-case", default=None,
                     help="B:gamma -- time only the round's three calls on that high-concurrency-shaped case")
     ap.add_argument("--tv-rows", type=int, default=None,

@@ -81,6 +81,24 @@ const char* dspark_status_string(dspark_status_t s);
  * Returns DSPARK_ERR_CUDA if the synchronisation or the copy fails. */
 dspark_status_t dspark_workspace_status(const void* workspace, dspark_stream_t stream);
 
+/* Opt-in L2 residency of the Markov weight W2 (read once per draft position).
+ * bytes > 0: sets the persisting-L2 limit of the calling thread's current
+ * context on the current device to min(bytes, the device's maximum), and from
+ * then on every draft launch (dspark_draft_block, its no-allocation twin,
+ * dspark_decode_rounds) and the residual launch of dspark_verify carry an
+ * access-policy window over W2 that marks its lines persisting, so they stay
+ * in L2 from one position and one call to the next instead of being evicted by
+ * the streamed U and target rows.  bytes = 0: drops the window from later
+ * launches, returns the persisting lines to normal status and puts the
+ * limit back to the value it had before the first enabling call.
+ * This changes a context-wide setting: L2 set aside for
+ * persisting lines is no longer available to other kernels of the process
+ * for their normal lines.  Results are bit-identical either way; only the
+ * DRAM traffic (and at small batches the time) changes.  Host-side only: not
+ * while a stream is being captured.  DSPARK_ERR_CUDA if the limit cannot be
+ * set (e.g. no persisting L2 on the device). */
+dspark_status_t dspark_set_l2_residency(size_t bytes);
+
 /* ------------------------------------------------------------------------ *
  * Draft block.  DeepSpec walkthrough section 3.2 (stage two): for k = 1..gamma
  *   z_k = U_k + B(x_{k-1}),  B(x_{k-1}, v) = sum_j W2[v][j] * W1[x_{k-1}][j]

@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     HEAD_RNN,
     dspark_draft_block,
     dspark_schedule_prefix,
+    dspark_set_l2_residency,
     dspark_verify,
     exported_symbols,
     load,

@@ -26,6 +26,7 @@ _p = ctypes.c_void_p
 _SIGNATURES = {
     "dspark_status_string": (ctypes.c_char_p, [_c_int]),
     "dspark_workspace_status": (_c_int, [_p, _p]),
+    "dspark_set_l2_residency": (_c_int, [_c_size]),
     "dspark_draft_block_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "dspark_draft_block": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _p, _p, _p, _p, _p,
                                     _c_float, _p, _c_float, _c_u64, _p, _p, _p, _p, _p, _p, _c_size, _p]),
@@ -145,6 +146,14 @@ def _nbytes(t):
 def workspace_status(workspace, stream=None):
     """Device status code left at the head of `workspace` (synchronises)."""
     return load().dspark_workspace_status(_ptr(workspace), _stream(stream))
+
+
+def dspark_set_l2_residency(nbytes):
+    """Opt-in: keep W2 (the Markov weight streamed every draft position) in L2 by a
+    persisting access-policy window on the draft and residual launches; sets the
+    current context's persisting-L2 limit to min(nbytes, the device maximum).
+    0 turns it off and restores the previous limit.  Results are unchanged."""
+    _check("dspark_set_l2_residency", load().dspark_set_l2_residency(int(nbytes)))
 
 
 # ----------------------------------------------------------------- calls ---

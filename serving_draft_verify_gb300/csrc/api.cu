@@ -69,3 +69,58 @@ extern "C" dspark_status_t dspark_workspace_status(const void* workspace, dspark
     if (cudaStreamSynchronize(s) != cudaSuccess) return DSPARK_ERR_CUDA;
     return static_cast<dspark_status_t>(code);
 }
+
+namespace dspark {
+std::atomic<size_t> g_l2_resident_bytes{0};
+std::atomic<size_t> g_l2_window_max{0};
+namespace {
+std::mutex g_l2_mu;
+bool g_l2_saved = false;
+size_t g_l2_prev_limit = 0;
+}  // namespace
+}  // namespace dspark
+
+extern "C" dspark_status_t dspark_set_l2_residency(size_t bytes) {
+    using namespace dspark;
+    std::lock_guard<std::mutex> lock(g_l2_mu);
+    clear_stale_error();
+    if (bytes == 0) {
+        g_l2_resident_bytes.store(0);
+        if (g_l2_saved) {
+            // W2's lines back to normal, then the set-aside back to what it was
+            if (cudaCtxResetPersistingL2Cache() != cudaSuccess) {
+                cudaGetLastError();
+                return DSPARK_ERR_CUDA;
+            }
+            if (cudaDeviceSetLimit(cudaLimitPersistingL2CacheSize, g_l2_prev_limit) != cudaSuccess) {
+                cudaGetLastError();
+                return DSPARK_ERR_CUDA;
+            }
+            g_l2_saved = false;
+        }
+        return DSPARK_OK;
+    }
+    const int dev = current_device();
+    int maxp = 0, maxw = 0;
+    if (cudaDeviceGetAttribute(&maxp, cudaDevAttrMaxPersistingL2CacheSize, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&maxw, cudaDevAttrMaxAccessPolicyWindowSize, dev) != cudaSuccess || maxp <= 0 ||
+        maxw <= 0) {
+        cudaGetLastError();
+        return DSPARK_ERR_CUDA;
+    }
+    if (!g_l2_saved) {
+        if (cudaDeviceGetLimit(&g_l2_prev_limit, cudaLimitPersistingL2CacheSize) != cudaSuccess) {
+            cudaGetLastError();
+            return DSPARK_ERR_CUDA;
+        }
+        g_l2_saved = true;
+    }
+    const size_t keep = bytes < static_cast<size_t>(maxp) ? bytes : static_cast<size_t>(maxp);
+    if (cudaDeviceSetLimit(cudaLimitPersistingL2CacheSize, keep) != cudaSuccess) {
+        cudaGetLastError();
+        return DSPARK_ERR_CUDA;
+    }
+    g_l2_window_max.store(static_cast<size_t>(maxw));
+    g_l2_resident_bytes.store(keep);
+    return DSPARK_OK;
+}

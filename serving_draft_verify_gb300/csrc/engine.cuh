@@ -1031,11 +1031,16 @@ dspark_status_t launch_tc(const CUtensorMap& map, const TcParams& p, int grid, c
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = kTcSmem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (cooperative) {
+        attr[na].id = cudaLaunchAttributeCooperative;
+        attr[na].val.cooperative = 1;
+        ++na;
+    }
+    if (l2_window(&attr[na], p.W2, static_cast<size_t>(p.V) * p.r * 2)) ++na;   // W2 kept in L2 (opt-in)
     cfg.attrs = attr;
-    cfg.numAttrs = cooperative ? 1 : 0;
+    cfg.numAttrs = na;
     if (cudaLaunchKernelEx(&cfg, bias_engine_tc<kMode>, map, p) != cudaSuccess) {
         cudaGetLastError();
         return DSPARK_ERR_CUDA;

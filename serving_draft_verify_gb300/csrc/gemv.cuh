@@ -435,11 +435,11 @@ dspark_status_t launch_as(const Params& p, int grid, cudaStream_t s) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 1 + (l2_window(&attr[1], p.W2, static_cast<size_t>(p.V) * p.r * 2) ? 1 : 0);   // opt-in
     if (cudaLaunchKernelEx(&cfg, draft_gemv<kUHost>, map, p) != cudaSuccess) {
         cudaGetLastError();
         return DSPARK_ERR_CUDA;

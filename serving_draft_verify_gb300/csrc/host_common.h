@@ -17,6 +17,28 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// W2's L2 residency (dspark_set_l2_residency): the bytes of persisting L2 the
+// context now sets aside (0: off) and the largest access-policy window.
+extern std::atomic<size_t> g_l2_resident_bytes;
+extern std::atomic<size_t> g_l2_window_max;
+
+// Adds to `attr` an access-policy window that marks the lines of [base, base +
+// bytes) persisting, when residency is on; returns whether it did.  The window
+// covers min(bytes, the largest window) and a fraction hitRatio of it is
+// persisting, so that what persists fits the set-aside.
+inline bool l2_window(cudaLaunchAttribute* attr, const void* base, size_t bytes) {
+    const size_t keep = g_l2_resident_bytes.load(), wmax = g_l2_window_max.load();
+    if (keep == 0 || wmax == 0 || base == nullptr || bytes == 0) return false;
+    const size_t nb = bytes < wmax ? bytes : wmax;
+    attr->id = cudaLaunchAttributeAccessPolicyWindow;
+    attr->val.accessPolicyWindow.base_ptr = const_cast<void*>(base);
+    attr->val.accessPolicyWindow.num_bytes = nb;
+    attr->val.accessPolicyWindow.hitRatio = keep >= nb ? 1.f : static_cast<float>(keep) / static_cast<float>(nb);
+    attr->val.accessPolicyWindow.hitProp = cudaAccessPropertyPersisting;
+    attr->val.accessPolicyWindow.missProp = cudaAccessPropertyStreaming;
+    return true;
+}
+
 // Current device and its SM count (cached per device; calls from several host
 // threads may fill an entry at once, all with the same value).
 inline int current_device() {

@@ -8,7 +8,8 @@ import bench
 
 def _profile(tmp_path, monkeypatch, traffic_hash, issue_hash):
     (tmp_path / "profiles").mkdir()
-    rec = {"dram_bytes_per_launch": 6_500_000_000, "source_hash": traffic_hash,
+    rec = {"dram_bytes_per_launch": 6_500_000_000, "dram_bytes_per_launch_l2_resident": 5_400_000_000,
+           "source_hash": traffic_hash,
            "issue": {"source_hash": issue_hash, "warp_instructions": 250_000_000, "logits": 312_500_000}}
     (tmp_path / "profiles" / "draft_engine_traffic.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
@@ -18,6 +19,7 @@ def _profile(tmp_path, monkeypatch, traffic_hash, issue_hash):
 def test_figures_of_the_current_sources_are_reported(tmp_path, monkeypatch):
     _profile(tmp_path, monkeypatch, "current", "current")
     assert bench.recorded_engine_traffic() == 6_500_000_000
+    assert bench.recorded_engine_traffic(l2_resident=True) == 5_400_000_000
     assert bench.recorded_engine_issue() == 0.8
 
 

@@ -163,3 +163,39 @@ def test_draft_reads_inputs_from_pinned_host_memory(dsv, temperature, B):
     torch.cuda.synchronize()
     for k in a:
         assert torch.equal(a[k], b[k]), k
+
+
+def test_l2_residency_changes_no_result(dsv):
+    """W2 held in L2 by a persisting access-policy window (opt-in): the same outputs,
+    bit for bit, on both draft paths and the residual launch of verification; turning it
+    off again restores the context's previous persisting-L2 limit."""
+    for B in (40, 5):                                     # the tcgen05 engine; the small-batch path
+        cfg = wl.scaled(wl.QWEN3_8B, B=B, V=8192, H=64)
+        inp = wl.make_draft_inputs(cfg)
+        g = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+        run = lambda: dsv.dspark_draft_block(g["U"], g["h"], g["W1"], g["W2"], g["w"], 0.0, g["x0"],  # noqa: E731
+                                             cfg.temperature, cfg.seed)
+        a = run()
+        dsv.dspark_set_l2_residency(g["W2"].numel() * 2)
+        try:
+            b = run()
+            torch.cuda.synchronize()
+        finally:
+            dsv.dspark_set_l2_residency(0)
+        for k in a:
+            assert torch.equal(a[k], b[k]), (B, k)
+    # verification with many rejections (its residual launch reads W2 through the window)
+    from tests.gpu_harness import gpu_draft as draft_run, gpu_verify
+    cfg = wl.scaled(wl.QWEN3_8B, B=64, gamma=5, V=4096, H=32, target_noise=2.0)
+    inp = wl.make_draft_inputs(cfg)
+    d = draft_run(dsv, inp)
+    ell = np.full(cfg.B, cfg.gamma)
+    v0 = gpu_verify(dsv, inp, d, ell)
+    dsv.dspark_set_l2_residency(inp["W2"].numel() * 2)
+    try:
+        v1 = gpu_verify(dsv, inp, d, ell)
+    finally:
+        dsv.dspark_set_l2_residency(0)
+    for k in v0:
+        assert np.array_equal(v0[k], v1[k]), k
+    assert np.mean(v0["n_accept"] < cfg.gamma) > 0.3
