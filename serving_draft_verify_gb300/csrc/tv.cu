@@ -128,7 +128,9 @@ constexpr int kMaxLossCtas = 1024;
 // Loads: every thread copies its own 16-byte groups into its own slots of a ring
 // in shared memory with cp.async (no block barrier guards a slot: only the thread
 // that copied it reads it), kTv2Stages - 1 groups of d and of t ahead of the one
-// it is summing: 96 KB in flight per SM.
+// it is summing: 96 KB in flight per SM.  A pass's first groups are issued before
+// the block merge that precedes it, so they land while the CTA waits there; a
+// row's c* is summed across the block inside the next row's merge.
 constexpr int kTv2Threads = 1024;
 constexpr int kTv2Stages = 4;
 constexpr size_t kTv2Smem = static_cast<size_t>(kTv2Stages) * 2 * kTv2Threads * 16;
@@ -188,7 +190,8 @@ __device__ __forceinline__ void group_lse(const uint4 v, float& m, float& s) {
 
 // Block-wide merge of every thread's (m, s) pair for d and t: all threads get (L_d, L_t)
 // in natural units.
-__device__ __forceinline__ float2 block_lse2(float md, float sd, float mt, float st, float4* red, float2* fin) {
+__device__ __forceinline__ float2 block_lse2(float md, float sd, float mt, float st, float4* red, float2* fin,
+                                             const float* prev = nullptr, float* prev_out = nullptr) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     warp_lse(md, sd);
     warp_lse(mt, st);
@@ -198,10 +201,14 @@ __device__ __forceinline__ float2 block_lse2(float md, float sd, float mt, float
         float4 r = (lane < kTv2Threads / 32) ? red[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
         warp_lse(r.x, r.y);
         warp_lse(r.z, r.w);
+        // the previous row's per-warp partial sums, left in `prev` before this barrier
+        float pv = 0.f;
+        if (prev_out != nullptr) pv = warp_sum((lane < kTv2Threads / 32) ? prev[lane] : 0.f);
         if (lane == 0) {
             const float Ld = (r.y > 0.f) ? r.x + fast_log2(r.y) * kLn2 : -INFINITY;
             const float Lt = (r.w > 0.f) ? r.z + fast_log2(r.w) * kLn2 : -INFINITY;
             *fin = make_float2(Ld, Lt);
+            if (prev_out != nullptr) *prev_out = pv;
         }
     }
     __syncthreads();
@@ -222,9 +229,25 @@ __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0
 // and t go through its ring, copied kTv2Stages - 1 groups ahead of the one that
 // body(vd, vt, g) sums (g: the group's index in the row).  Each issue commits one cp.async group, empty past the last,
 // so that "group i has landed" is always wait_group(S - 2) after i + S - 1 commits.
+// Issues the first kTv2Stages - 1 groups of a pass into the ring (tv2_pass with
+// `primed` skips them): lets the next pass's loads fly while the block merges.
+__device__ __forceinline__ void tv2_prime(const uint4* gd, const uint4* gt, int nmine, uint4* ring, uint64_t pol) {
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int i = 0; i < kTv2Stages - 1; ++i) {
+        if (i < nmine) {
+            const int g = tid + i * kTv2Threads;
+            uint4* slot = ring + static_cast<size_t>(i % kTv2Stages) * 2 * kTv2Threads + tid;
+            cp16_hint(slot, gd + g, pol);
+            cp16_hint(slot + kTv2Threads, gt + g, pol);
+        }
+        cp_commit();
+    }
+}
+
 template <class F>
 __device__ __forceinline__ void tv2_pass(const uint4* gd, const uint4* gt, int nmine, uint4* ring, uint64_t pol,
-                                         F&& body) {
+                                         F&& body, bool primed = false) {
     const int tid = threadIdx.x;
     auto issue = [&](int i) {
         if (i < nmine) {
@@ -235,8 +258,10 @@ __device__ __forceinline__ void tv2_pass(const uint4* gd, const uint4* gt, int n
         }
         cp_commit();
     };
+    if (!primed) {
 #pragma unroll
-    for (int i = 0; i < kTv2Stages - 1; ++i) issue(i);
+        for (int i = 0; i < kTv2Stages - 1; ++i) issue(i);
+    }
     for (int i = 0; i < nmine; ++i) {
         cp_wait<kTv2Stages - 2>();                        // group i has landed
         const uint4* slot = ring + static_cast<size_t>(i % kTv2Stages) * 2 * kTv2Threads + tid;
@@ -262,6 +287,7 @@ tv_two_pass(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float*
     const int ngroups = V / EPG;
     const int nmine = (ngroups > tid) ? (ngroups - tid + kTv2Threads - 1) / kTv2Threads : 0;
     const uint64_t keep = policy_evict_last(), drop = policy_evict_first();
+    int64_t prev_row = -1;                                // its per-warp partials wait in red2
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
         const uint4* gd = reinterpret_cast<const uint4*>(d + static_cast<size_t>(row) * V * ESZ);
         const uint4* gt = reinterpret_cast<const uint4*>(t + static_cast<size_t>(row) * V * ESZ);
@@ -273,10 +299,14 @@ tv_two_pass(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float*
         });
         if (!(md > -INFINITY)) { md = 0.f; sd = 0.f; }
         if (!(mt > -INFINITY)) { mt = 0.f; st = 0.f; }
-        const float2 L = block_lse2(md, sd, mt, st, red, &fin);
+        // pass 2's first loads fly while the block merges this row's logsumexps (which
+        // also finishes the previous row's c*)
+        tv2_prime(gd, gt, nmine, ring, drop);
+        const float2 L = block_lse2(md, sd, mt, st, red, &fin, red2, prev_row >= 0 ? c_star + prev_row : nullptr);
         // pass 2: sum of 2^(min(d - L_d, t - L_t) log2e), from L2 (for bf16 the
         // exponents are the fused d log2e - L_d log2e and t log2e - L_t log2e)
         unsigned long long acc = pk(0.f, 0.f);
+        if (!(L.x > -INFINITY && L.y > -INFINITY)) cp_wait<0>();   // no mass: the primed loads are dropped
         if (L.x > -INFINITY && L.y > -INFINITY) {
             const unsigned long long L2E = pk(kLog2e, kLog2e);
             const float sc = kBF16 ? kLog2e : 1.f;
@@ -298,18 +328,20 @@ tv_two_pass(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float*
                         acc = add2(acc, pk(fast_exp2(z.x), fast_exp2(z.y)));
                     }
                 }
-            });
+            }, /*primed=*/true);
         }
         float part = upk(acc).x + upk(acc).y;
         part = warp_sum(part);
-        if (lane == 0) red2[warp] = part;
+        if (lane == 0) red2[warp] = part;                 // read after the next row's first barrier
+        prev_row = row;
+        // red and fin are rewritten by the next row after the first barrier in block_lse2
+    }
+    if (prev_row >= 0) {
         __syncthreads();
         if (warp == 0) {
-            float v = (lane < kTv2Threads / 32) ? red2[lane] : 0.f;
-            v = warp_sum(v);
-            if (lane == 0) c_star[row] = v;
+            const float v = warp_sum((lane < kTv2Threads / 32) ? red2[lane] : 0.f);
+            if (lane == 0) c_star[prev_row] = v;
         }
-        // red, fin and red2 are rewritten by the next row after a barrier in block_lse2
     }
 }
 
@@ -388,10 +420,12 @@ loss_three_pass(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, in
         });
         if (!(md > -INFINITY)) { md = 0.f; sd = 0.f; }
         if (!(mt > -INFINITY)) { mt = 0.f; st = 0.f; }
+        tv2_prime(gd, gt, nmine, ring, keep);             // pass 2's first loads fly during the merge
         const float4 P = block_lse2_parts(md, sd, mt, st, red, &fin);
         const float Ld = P.x + P.y, Lt = P.z + P.w;       // natural-log logsumexp
         const float dL = (P.x - P.z) + (P.y - P.w);       // L_d - L_t from the parts
         const bool mass = Ld > -INFINITY && Lt > -INFINITY;
+        if (!mass) cp_wait<0>();                          // no mass: the primed loads are dropped
         // 2: c*, P_lt, P_eq, from L2
         // exponents: for bf16 the fused x log2e - L log2e, for float32 (x - L) log2e
         const float sc = kBF16 ? kLog2e : 1.f;
@@ -415,7 +449,9 @@ loss_three_pass(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, in
                 plt += (r0 < dL ? e0 : 0.f) + (r1 < dL ? e1 : 0.f);
                 peq += (r0 == dL ? e0 : 0.f) + (r1 == dL ? e1 : 0.f);
             }
-        });
+        }, /*primed=*/mass);
+        const bool grad3 = la.grad != nullptr && mass;
+        if (grad3) tv2_prime(gd, gt, nmine, ring, drop);   // pass 3's first loads fly during the merge
         {
             const float p = warp_sum(upk(pc).x + upk(pc).y), q1 = warp_sum(plt), q2 = warp_sum(peq);
             if (lane == 0) red_c[warp] = make_float4(p, q1, q2, 0.f);
@@ -465,7 +501,7 @@ loss_three_pass(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, in
                 asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(grow + g * 16),
                              "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w), "l"(drop)
                              : "memory");
-            });
+            }, /*primed=*/grad3);
         }
         if (tid == 0) {
             const float sv = la.s[row];
