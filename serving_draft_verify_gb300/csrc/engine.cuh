@@ -10,16 +10,18 @@
 //              greedy: the running argmax of z;
 //   kResidual  the Gumbel-max draw from the residual max(0, p_t - p_d)
 //              (section 8.2): the token maximising q_v / E_v, stream 2.
-// Inside a 32-token sub-block the draw is an exponential race: with
-// e_v = 2^(y_v - m) (already formed for the sum) the winner maximises e_v / E_v,
-// compared by cross-multiplication, so one logarithm per token (inside E_v) is
-// all the draw adds; the sub-block's winner enters the thread's running best
-// as the key y_v - log2 E_v.
+// Inside a 32-token sub-block the draw is an exponential race with an exact
+// filter: with e_v = 2^(y_v - m) (already formed for the sum) and R = 2^(m - best)
+// for the thread's running best key, token v can win only if E_v < e_v R, and
+// since E_v >= s_v = 1 - u_v (exact from the word) a token with s_v >= e_v R is
+// skipped; only the rare others take E_v and the exact key y_v - log2 E_v, each
+// lane walking its own candidate bits in ascending order.
 // Each CTA publishes its best token per row with a 64-bit atomicMax of
 // (key, ~token) and, for kDraft, its (max, sum) partial and the y of its best
 // token (for log p_d of the token that wins overall).
 //
-// Layout of one CTA (512 threads, one CTA per SM):
+// Layout of one CTA (512 threads, one CTA per SM; 128 registers a thread at
+// launch, then 56 for warpgroup 0 and 152 for the epilogue warpgroups):
 //   warp 0      TMA producer: W2 tiles [128 tokens x 64 K] into a slab ring
 //               (128-byte swizzle, L2 evict-last so W2 stays resident);
 //   warp 1      TMEM allocator and MMA issuer: tcgen05.mma kind::f16,
@@ -30,7 +32,7 @@
 //               overlaps the epilogues of the others.
 // The A operand (rows W1[x_{k_b-1}], or the rows E[b][k_b] of a gated or
 // recurrent head, gathered into shared memory with the same swizzle) is built
-// by warps 1-11 at the start of every position.
+// by warps 1-15 at the start of every position.
 //
 // Draft launches may cover positions k .. k_last (a cooperative launch, all
 // CTAs resident, TMEM and barriers set up once, the producer streaming W2
