@@ -10,7 +10,7 @@
 // dL/dd).  A CTA's row of the Qwen3 vocabulary is 607,744 bytes of bf16, 92 MB
 // for one row per SM: it stays in the L2 between the passes.  Every thread
 // streams its own 16-byte groups through its own slots of a cp.async ring in
-// shared memory, three groups ahead.
+// shared memory, five groups ahead.
 #include "common.cuh"
 #include "host_common.h"
 
@@ -128,11 +128,11 @@ constexpr int kMaxLossCtas = 1024;
 // Loads: every thread copies its own 16-byte groups into its own slots of a ring
 // in shared memory with cp.async (no block barrier guards a slot: only the thread
 // that copied it reads it), kTv2Stages - 1 groups of d and of t ahead of the one
-// it is summing: 96 KB in flight per SM.  A pass's first groups are issued before
+// it is summing: 160 KB in flight per SM.  A pass's first groups are issued before
 // the block merge that precedes it, so they land while the CTA waits there; a
 // row's c* is summed across the block inside the next row's merge.
 constexpr int kTv2Threads = 1024;
-constexpr int kTv2Stages = 4;
+constexpr int kTv2Stages = 6;
 constexpr size_t kTv2Smem = static_cast<size_t>(kTv2Stages) * 2 * kTv2Threads * 16;
 
 // The group's max (raw units), -inf if it has no finite element.
