@@ -11,6 +11,8 @@
 // for one row per SM: it stays in the L2 between the passes.  Every thread
 // streams its own 16-byte groups through its own slots of a cp.async ring in
 // shared memory, five groups ahead.
+#include <type_traits>
+
 #include "common.cuh"
 #include "host_common.h"
 
@@ -134,6 +136,11 @@ constexpr int kMaxLossCtas = 1024;
 constexpr int kTv2Threads = 1024;
 constexpr int kTv2Stages = 6;
 constexpr size_t kTv2Smem = static_cast<size_t>(kTv2Stages) * 2 * kTv2Threads * 16;
+// The loss keeps a sign byte per 16-byte group of d beside the ring for rows of up to
+// this many groups per thread (V = 270,336 for bf16): 33 KB more shared memory,
+// 227 KB per CTA in all with the kernel's static arrays.
+constexpr int kLossMaxBitGroups = 33;
+constexpr size_t kLossSmemMax = kTv2Smem + static_cast<size_t>(kLossMaxBitGroups) * kTv2Threads;
 
 // The group's max (raw units), -inf if it has no finite element.
 template <bool kBF16>
@@ -226,12 +233,16 @@ template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // One pass over a row: a thread's groups i = 0 .. nmine - 1 (group tid + i T) of d
-// and t go through its ring, copied kTv2Stages - 1 groups ahead of the one that
-// body(vd, vt, g) sums (g: the group's index in the row).  Each issue commits one cp.async group, empty past the last,
-// so that "group i has landed" is always wait_group(S - 2) after i + S - 1 commits.
+// and t (of d alone with kT = false; vt is then vd) go through its ring, copied
+// kTv2Stages - 1 groups ahead of the one that body(vd, vt, g) sums (g: the group's
+// index in the row), d with L2 policy pol and t with polt.  Each issue commits one
+// cp.async group, empty past the last, so that "group i has landed" is always
+// wait_group(S - 2) after i + S - 1 commits.
 // Issues the first kTv2Stages - 1 groups of a pass into the ring (tv2_pass with
 // `primed` skips them): lets the next pass's loads fly while the block merges.
-__device__ __forceinline__ void tv2_prime(const uint4* gd, const uint4* gt, int nmine, uint4* ring, uint64_t pol) {
+template <bool kT = true>
+__device__ __forceinline__ void tv2_prime(const uint4* gd, const uint4* gt, int nmine, uint4* ring, uint64_t pol,
+                                          uint64_t polt) {
     const int tid = threadIdx.x;
 #pragma unroll
     for (int i = 0; i < kTv2Stages - 1; ++i) {
@@ -239,34 +250,37 @@ __device__ __forceinline__ void tv2_prime(const uint4* gd, const uint4* gt, int 
             const int g = tid + i * kTv2Threads;
             uint4* slot = ring + static_cast<size_t>(i % kTv2Stages) * 2 * kTv2Threads + tid;
             cp16_hint(slot, gd + g, pol);
-            cp16_hint(slot + kTv2Threads, gt + g, pol);
+            if (kT) cp16_hint(slot + kTv2Threads, gt + g, polt);
         }
         cp_commit();
     }
 }
 
-template <class F>
+template <bool kT = true, class F>
 __device__ __forceinline__ void tv2_pass(const uint4* gd, const uint4* gt, int nmine, uint4* ring, uint64_t pol,
-                                         F&& body, bool primed = false) {
+                                         uint64_t polt, F&& body, bool primed = false) {
     const int tid = threadIdx.x;
-    auto issue = [&](int i) {
+    auto issue = [&](int i, int slot) {
         if (i < nmine) {
             const int g = tid + i * kTv2Threads;
-            uint4* slot = ring + static_cast<size_t>(i % kTv2Stages) * 2 * kTv2Threads + tid;
-            cp16_hint(slot, gd + g, pol);
-            cp16_hint(slot + kTv2Threads, gt + g, pol);
+            uint4* dst = ring + static_cast<size_t>(slot) * 2 * kTv2Threads + tid;
+            cp16_hint(dst, gd + g, pol);
+            if (kT) cp16_hint(dst + kTv2Threads, gt + g, polt);
         }
         cp_commit();
     };
     if (!primed) {
 #pragma unroll
-        for (int i = 0; i < kTv2Stages - 1; ++i) issue(i);
+        for (int i = 0; i < kTv2Stages - 1; ++i) issue(i, i);
     }
+    int rd = 0, wr = kTv2Stages - 1;
     for (int i = 0; i < nmine; ++i) {
-        cp_wait<kTv2Stages - 2>();                        // group i has landed
-        const uint4* slot = ring + static_cast<size_t>(i % kTv2Stages) * 2 * kTv2Threads + tid;
-        const uint4 vd = slot[0], vt = slot[kTv2Threads];
-        issue(i + kTv2Stages - 1);                        // refills the slot read one group ago
+        cp_wait<kTv2Stages - 2>();
+        const uint4* slot = ring + static_cast<size_t>(rd) * 2 * kTv2Threads + tid;
+        const uint4 vd = slot[0], vt = kT ? slot[kTv2Threads] : vd;
+        issue(i + kTv2Stages - 1, wr);
+        wr = rd;
+        rd = rd == kTv2Stages - 1 ? 0 : rd + 1;
         body(vd, vt, tid + i * kTv2Threads);
     }
     cp_wait<0>();
@@ -293,7 +307,7 @@ tv_two_pass(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float*
         const uint4* gt = reinterpret_cast<const uint4*>(t + static_cast<size_t>(row) * V * ESZ);
         // pass 1: (max, sum) of d and t, from HBM
         float md = -INFINITY, sd = 0.f, mt = -INFINITY, st = 0.f;
-        tv2_pass(gd, gt, nmine, ring, keep, [&](const uint4 vd, const uint4 vt, int) {
+        tv2_pass(gd, gt, nmine, ring, keep, keep, [&](const uint4 vd, const uint4 vt, int) {
             group_lse<kBF16>(vd, md, sd);
             group_lse<kBF16>(vt, mt, st);
         });
@@ -301,7 +315,7 @@ tv_two_pass(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float*
         if (!(mt > -INFINITY)) { mt = 0.f; st = 0.f; }
         // pass 2's first loads fly while the block merges this row's logsumexps (which
         // also finishes the previous row's c*)
-        tv2_prime(gd, gt, nmine, ring, drop);
+        tv2_prime(gd, gt, nmine, ring, drop, drop);
         const float2 L = block_lse2(md, sd, mt, st, red, &fin, red2, prev_row >= 0 ? c_star + prev_row : nullptr);
         // pass 2: sum of 2^(min(d - L_d, t - L_t) log2e), from L2 (for bf16 the
         // exponents are the fused d log2e - L_d log2e and t log2e - L_t log2e)
@@ -311,7 +325,7 @@ tv_two_pass(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, float*
             const unsigned long long L2E = pk(kLog2e, kLog2e);
             const float sc = kBF16 ? kLog2e : 1.f;
             const unsigned long long nLd = pk(-L.x * sc, -L.x * sc), nLt = pk(-L.y * sc, -L.y * sc);
-            tv2_pass(gd, gt, nmine, ring, drop, [&](const uint4 vd, const uint4 vt, int) {
+            tv2_pass(gd, gt, nmine, ring, drop, drop, [&](const uint4 vd, const uint4 vt, int) {
                 float a[EPG], b[EPG];
                 unpack<kBF16>(vd, a);
                 unpack<kBF16>(vt, b);
@@ -371,12 +385,20 @@ __device__ __forceinline__ float4 block_lse2_parts(float md, float sd, float mt,
 // turn, each row in three passes through the per-thread cp.async ring:
 //   1. from HBM (evict-last): each tensor's (max, sum) -> L_d, L_t, and
 //      L_d - L_t from their parts (it keeps the precision of a small number);
-//   2. from L2 (evict-last again, pass 3 reads the row once more): the terms
-//      2^(min(d - L_d, t - L_t) log2e), their sum c* and the p_d mass where
-//      d - t < L_d - L_t (P_lt) and where they tie (P_eq), the terms being p_d
-//      there; sum_u p_d(u) sgn_u = 1 - 2 P_lt - P_eq;
+//   2. from L2 (d evict-last again, pass 3 reads it once more; t evict-first when
+//      pass 3 does not need it): the terms 2^(min(d - L_d, t - L_t) log2e), their
+//      sum c* and the p_d mass where d - t < L_d - L_t (P_lt), the terms being
+//      p_d there, and whether any element ties (d - t = L_d - L_t);
+//      sum_u p_d(u) sgn_u = 1 - 2 P_lt - P_eq, with P_eq the p_d mass of the ties;
 //   3. from L2 (evict-first), only with a gradient: dL/dd written with 16-byte
 //      evict-first stores.
+// A row without ties (all real logits but a set of measure zero) has P_eq = 0
+// and sgn_v = +-1 from the one comparison d_v - t_v < L_d - L_t, which pass 2
+// leaves as a bit per element in shared memory (a byte per group, nbits groups
+// per thread; 19 KB for V = 151936 in bf16): pass 3 then streams d alone.  Where
+// the bytes do not fit (nbits = 0) pass 3 streams t again and compares.  A row
+// with a tie (d = t, for one) runs pass 2 once more with the sign's three cases,
+// summing P_lt and P_eq, and pass 3 with all three.
 // sgn_v compares d_v - t_v (exact for bf16 inputs) with L_d - L_t formed from
 // the two logsumexps' parts, so a sign is wrong only where |ln(p_d / p_t)| is
 // within float32 rounding of the row's logsumexps; for bf16 the exponents are the
@@ -386,15 +408,16 @@ __device__ __forceinline__ float4 block_lse2_parts(float md, float sd, float mt,
 template <bool kBF16>
 __global__ void __launch_bounds__(kTv2Threads, 1)
 loss_three_pass(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, int64_t rows, int V,
-                StatusBlock* status, LossArgs la) {
+                StatusBlock* status, LossArgs la, int nbits) {
     using Tr = TVTraits<kBF16>;
     constexpr int EPG = Tr::kEPG, ESZ = Tr::kESZ;
     extern __shared__ __align__(16) uint8_t tv2_smem[];
     uint4* ring = reinterpret_cast<uint4*>(tv2_smem);
+    uint8_t* sbits = tv2_smem + kTv2Smem;               // [nbits][kTv2Threads] sign bytes, 0 if nbits = 0
     __shared__ float4 red[kTv2Threads / 32];
     __shared__ float4 fin;
     __shared__ float4 red_c[kTv2Threads / 32];
-    __shared__ float3 fin_c;
+    __shared__ float4 fin_c;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ngroups = V / EPG;
     const int nmine = (ngroups > tid) ? (ngroups - tid + kTv2Threads - 1) / kTv2Threads : 0;
@@ -414,13 +437,13 @@ loss_three_pass(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, in
         }
         // 1: (max, sum) of d and t, from HBM
         float md = -INFINITY, sd = 0.f, mt = -INFINITY, st = 0.f;
-        tv2_pass(gd, gt, nmine, ring, keep, [&](const uint4 vd, const uint4 vt, int) {
+        tv2_pass(gd, gt, nmine, ring, keep, keep, [&](const uint4 vd, const uint4 vt, int) {
             group_lse<kBF16>(vd, md, sd);
             group_lse<kBF16>(vt, mt, st);
         });
         if (!(md > -INFINITY)) { md = 0.f; sd = 0.f; }
         if (!(mt > -INFINITY)) { mt = 0.f; st = 0.f; }
-        tv2_prime(gd, gt, nmine, ring, keep);             // pass 2's first loads fly during the merge
+        tv2_prime(gd, gt, nmine, ring, keep, keep);             // pass 2's first loads fly during the merge
         const float4 P = block_lse2_parts(md, sd, mt, st, red, &fin);
         const float Ld = P.x + P.y, Lt = P.z + P.w;       // natural-log logsumexp
         const float dL = (P.x - P.z) + (P.y - P.w);       // L_d - L_t from the parts
@@ -435,35 +458,79 @@ loss_three_pass(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, in
             return kBF16 ? upk(fma2(pk(a0, a1), L2E, nL)) : upk(mul2(add2(pk(a0, a1), nL), L2E));
         };
         unsigned long long pc = pk(0.f, 0.f);
-        float plt = 0.f, peq = 0.f;
-        tv2_pass(gd, gt, mass ? nmine : 0, ring, keep, [&](const uint4 vd, const uint4 vt, int) {
+        float plt0 = 0.f, plt1 = 0.f;
+        bool tie = false;                                 // some d_v - t_v == L_d - L_t in this thread's groups
+        const bool bits = nbits > 0 && la.grad != nullptr;   // pass 3 takes the signs from sbits
+        tv2_pass(gd, gt, mass ? nmine : 0, ring, keep, bits ? drop : keep, [&](const uint4 vd, const uint4 vt, int g) {
             float a[EPG], b[EPG];
             unpack<kBF16>(vd, a);
             unpack<kBF16>(vt, b);
+            uint32_t m = 0;                               // bit e: d_e - t_e < L_d - L_t
 #pragma unroll
             for (int e = 0; e < EPG; e += 2) {
                 const float2 x = expo(a[e], a[e + 1], nLd), y = expo(b[e], b[e + 1], nLt);
-                const float e0 = fast_exp2(fminf(x.x, y.x)), e1 = fast_exp2(fminf(x.y, y.y));
-                pc = add2(pc, pk(e0, e1));
+                // min(p_d, p_t) is p_d exactly where d - t < L_d - L_t: the comparison that
+                // decides the sign picks the smaller exponent too
                 const float r0 = a[e] - b[e], r1 = a[e + 1] - b[e + 1];
-                plt += (r0 < dL ? e0 : 0.f) + (r1 < dL ? e1 : 0.f);
-                peq += (r0 == dL ? e0 : 0.f) + (r1 == dL ? e1 : 0.f);
+                const bool l0 = r0 < dL, l1 = r1 < dL;
+                const float e0 = fast_exp2(l0 ? x.x : y.x), e1 = fast_exp2(l1 ? x.y : y.y);
+                pc = add2(pc, pk(e0, e1));
+                if (l0) { plt0 += e0; m |= 1u << e; }
+                if (l1) { plt1 += e1; m |= 2u << e; }
+                tie |= (r0 == dL) | (r1 == dL);
             }
+            if (bits) sbits[g] = static_cast<uint8_t>(m);   // g = tid + i T: slot i of this thread
         }, /*primed=*/mass);
         const bool grad3 = la.grad != nullptr && mass;
-        if (grad3) tv2_prime(gd, gt, nmine, ring, drop);   // pass 3's first loads fly during the merge
+        if (grad3) {                                      // pass 3's first loads fly during the merge
+            if (bits) tv2_prime<false>(gd, gt, nmine, ring, drop, drop);
+            else tv2_prime(gd, gt, nmine, ring, drop, drop);
+        }
         {
-            const float p = warp_sum(upk(pc).x + upk(pc).y), q1 = warp_sum(plt), q2 = warp_sum(peq);
-            if (lane == 0) red_c[warp] = make_float4(p, q1, q2, 0.f);
+            const float p = warp_sum(upk(pc).x + upk(pc).y), q1 = warp_sum(plt0 + plt1);
+            const bool tw = __any_sync(0xffffffffu, tie);
+            if (lane == 0) red_c[warp] = make_float4(p, q1, 0.f, tw ? 1.f : 0.f);
             __syncthreads();
             if (warp == 0) {
                 const float4 r = (lane < kTv2Threads / 32) ? red_c[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-                const float c0 = warp_sum(r.x), c1 = warp_sum(r.y), c2 = warp_sum(r.z);
-                if (lane == 0) fin_c = make_float3(c0, c1, c2);
+                const float c0 = warp_sum(r.x), c1 = warp_sum(r.y), c3 = warp_sum(r.w);
+                if (lane == 0) fin_c = make_float4(c0, c1, 0.f, c3);
             }
             __syncthreads();
         }
-        const float3 C = fin_c;                           // (c*, P_lt, P_eq)
+        float4 C = fin_c;                                 // (c*, P_lt, P_eq, ties): P_eq = 0 without ties
+        const bool tie_row = C.w > 0.f;                   // block-uniform
+        if (tie_row && la.grad != nullptr) {
+            // rare: some d_v - t_v equals L_d - L_t exactly, where sgn_v = 0.  Pass 2
+            // again, from L2, with P_lt and P_eq summed per element as in the sign's
+            // three-way definition.
+            cp_wait<0>();                                 // the primed loads have landed: the ring is free
+            float plt = 0.f, peq = 0.f;
+            tv2_pass(gd, gt, nmine, ring, keep, keep, [&](const uint4 vd, const uint4 vt, int) {
+                float a[EPG], b[EPG];
+                unpack<kBF16>(vd, a);
+                unpack<kBF16>(vt, b);
+#pragma unroll
+                for (int e = 0; e < EPG; e += 2) {
+                    const float2 x = expo(a[e], a[e + 1], nLd), y = expo(b[e], b[e + 1], nLt);
+                    const float e0 = fast_exp2(fminf(x.x, y.x)), e1 = fast_exp2(fminf(x.y, y.y));
+                    const float r0 = a[e] - b[e], r1 = a[e + 1] - b[e + 1];
+                    plt += (r0 < dL ? e0 : 0.f) + (r1 < dL ? e1 : 0.f);
+                    peq += (r0 == dL ? e0 : 0.f) + (r1 == dL ? e1 : 0.f);
+                }
+            });
+            const float q1 = warp_sum(plt), q2 = warp_sum(peq);
+            if (lane == 0) red_c[warp] = make_float4(0.f, q1, q2, 0.f);
+            __syncthreads();
+            if (warp == 0) {
+                const float4 r = (lane < kTv2Threads / 32) ? red_c[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float c1 = warp_sum(r.y), c2 = warp_sum(r.z);
+                if (lane == 0) fin_c = make_float4(C.x, c1, c2, C.w);
+            }
+            __syncthreads();
+            C = fin_c;
+            tv2_prime(gd, gt, nmine, ring, drop, drop);
+        }
         const float sbar = 1.f - 2.f * C.y - C.z;         // sum_u p_d(u) sign(p_d(u) - p_t(u))
         const float om = la.omega[row];
         // 3: dL/dd, from L2, written once
@@ -473,35 +540,54 @@ loss_three_pass(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, in
             const float c0 = ka - kl * sbar, cp = c0 + kl, cm = c0 - kl;
             const int tg = tgt >= 0 ? tgt / EPG : -1;     // the target's group
             uint8_t* grow = static_cast<uint8_t*>(la.grad) + static_cast<size_t>(row) * V * ESZ;
-            tv2_pass(gd, gt, mass ? nmine : 0, ring, drop, [&](const uint4 vd, const uint4 vt, int g) {
-                float a[EPG], b[EPG], gv[EPG];
-                unpack<kBF16>(vd, a);
-                unpack<kBF16>(vt, b);
+            // kMode 0: the sign's three cases; 1 (no tie in the row): two; 2 (no tie, signs
+            // kept by pass 2): two, read from sbits, d alone streamed
+            auto grad_pass = [&](auto mode) {
+                constexpr int kMode = decltype(mode)::value;
+                tv2_pass<kMode != 2>(gd, gt, mass ? nmine : 0, ring, drop, drop, [&](const uint4 vd, const uint4 vt, int g) {
+                    float a[EPG], b[EPG], gv[EPG];
+                    unpack<kBF16>(vd, a);
+                    uint32_t m = 0;
+                    if constexpr (kMode == 2) m = sbits[g];
+                    else unpack<kBF16>(vt, b);
 #pragma unroll
-                for (int e = 0; e < EPG; e += 2) {
-                    const float2 z = expo(a[e], a[e + 1], nLd);
-                    const float p0 = fast_exp2(z.x), p1 = fast_exp2(z.y);
-                    const float r0 = a[e] - b[e], r1 = a[e + 1] - b[e + 1];
-                    gv[e] = p0 * (r0 > dL ? cp : (r0 < dL ? cm : c0));
-                    gv[e + 1] = p1 * (r1 > dL ? cp : (r1 < dL ? cm : c0));
-                }
-                if (g == tg) {
+                    for (int e = 0; e < EPG; e += 2) {
+                        const float2 z = expo(a[e], a[e + 1], nLd);
+                        const float p0 = fast_exp2(z.x), p1 = fast_exp2(z.y);
+                        if constexpr (kMode == 0) {
+                            const float r0 = a[e] - b[e], r1 = a[e + 1] - b[e + 1];
+                            gv[e] = p0 * (r0 > dL ? cp : (r0 < dL ? cm : c0));
+                            gv[e + 1] = p1 * (r1 > dL ? cp : (r1 < dL ? cm : c0));
+                        } else if constexpr (kMode == 1) {
+                            const float r0 = a[e] - b[e], r1 = a[e + 1] - b[e + 1];
+                            gv[e] = p0 * (r0 < dL ? cm : cp);
+                            gv[e + 1] = p1 * (r1 < dL ? cm : cp);
+                        } else {
+                            gv[e] = p0 * ((m >> e) & 1u ? cm : cp);
+                            gv[e + 1] = p1 * ((m >> (e + 1)) & 1u ? cm : cp);
+                        }
+                    }
+                    if (g == tg) {
 #pragma unroll
-                    for (int e = 0; e < EPG; ++e)
-                        if (g * EPG + e == tgt) gv[e] -= ka;
-                }
-                uint4 o;
-                if constexpr (kBF16) {
-                    o.x = pack_bf16(gv[0], gv[1]); o.y = pack_bf16(gv[2], gv[3]);
-                    o.z = pack_bf16(gv[4], gv[5]); o.w = pack_bf16(gv[6], gv[7]);
-                } else {
-                    o = make_uint4(__float_as_uint(gv[0]), __float_as_uint(gv[1]), __float_as_uint(gv[2]),
-                                   __float_as_uint(gv[3]));
-                }
-                asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(grow + g * 16),
-                             "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w), "l"(drop)
-                             : "memory");
-            }, /*primed=*/grad3);
+                        for (int e = 0; e < EPG; ++e)
+                            if (g * EPG + e == tgt) gv[e] -= ka;
+                    }
+                    uint4 o;
+                    if constexpr (kBF16) {
+                        o.x = pack_bf16(gv[0], gv[1]); o.y = pack_bf16(gv[2], gv[3]);
+                        o.z = pack_bf16(gv[4], gv[5]); o.w = pack_bf16(gv[6], gv[7]);
+                    } else {
+                        o = make_uint4(__float_as_uint(gv[0]), __float_as_uint(gv[1]), __float_as_uint(gv[2]),
+                                       __float_as_uint(gv[3]));
+                    }
+                    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(grow + g * 16),
+                                 "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w), "l"(drop)
+                                 : "memory");
+                }, /*primed=*/grad3);
+            };
+            if (tie_row) grad_pass(std::integral_constant<int, 0>{});
+            else if (bits) grad_pass(std::integral_constant<int, 2>{});
+            else grad_pass(std::integral_constant<int, 1>{});
         }
         if (tid == 0) {
             const float sv = la.s[row];
@@ -534,14 +620,19 @@ dspark_status_t launch_loss_three_pass(int64_t rows, int V, const void* d, const
     static OncePerDevice once;
     if (once.run(dev, [] {
             return cudaFuncSetAttribute(loss_three_pass<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(kTv2Smem));
+                                        static_cast<int>(kLossSmemMax));
         }) != cudaSuccess)
         return DSPARK_ERR_CUDA;
     int sms = sm_count(dev);
     if (sms > kMaxLossCtas) sms = kMaxLossCtas;
     const int64_t grid = rows < sms ? rows : sms;
-    loss_three_pass<kBF16><<<static_cast<unsigned>(grid), kTv2Threads, kTv2Smem, stream>>>(
-        static_cast<const uint8_t*>(d), static_cast<const uint8_t*>(t), rows, V, status, la);
+    // a sign byte per group for every thread's groups, when they fit beside the ring
+    const int ngroups = V / TVTraits<kBF16>::kEPG;
+    const int per_thread = (ngroups + kTv2Threads - 1) / kTv2Threads;
+    const int nbits = (la.grad != nullptr && per_thread <= kLossMaxBitGroups) ? per_thread : 0;
+    const size_t smem = kTv2Smem + static_cast<size_t>(nbits) * kTv2Threads;
+    loss_three_pass<kBF16><<<static_cast<unsigned>(grid), kTv2Threads, smem, stream>>>(
+        static_cast<const uint8_t*>(d), static_cast<const uint8_t*>(t), rows, V, status, la, nbits);
     return launch_status();
 }
 
