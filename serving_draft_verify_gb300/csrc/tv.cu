@@ -140,6 +140,9 @@ constexpr size_t kTv2Smem = static_cast<size_t>(kTv2Stages) * 2 * kTv2Threads * 
 // this many groups per thread (V = 270,336 for bf16): 33 KB more shared memory,
 // 227 KB per CTA in all with the kernel's static arrays.
 constexpr int kLossMaxBitGroups = 33;
+// The loss's passes run their group loop unrolled three times (0.6 % faster than
+// once; the accept rate's two passes are faster rolled).
+constexpr int kLossUnroll = 3;
 constexpr size_t kLossSmemMax = kTv2Smem + static_cast<size_t>(kLossMaxBitGroups) * kTv2Threads;
 
 // The group's max (raw units), -inf if it has no finite element.
@@ -256,7 +259,7 @@ __device__ __forceinline__ void tv2_prime(const uint4* gd, const uint4* gt, int 
     }
 }
 
-template <bool kT = true, class F>
+template <bool kT = true, int kUnroll = 1, class F>
 __device__ __forceinline__ void tv2_pass(const uint4* gd, const uint4* gt, int nmine, uint4* ring, uint64_t pol,
                                          uint64_t polt, F&& body, bool primed = false) {
     const int tid = threadIdx.x;
@@ -274,6 +277,7 @@ __device__ __forceinline__ void tv2_pass(const uint4* gd, const uint4* gt, int n
         for (int i = 0; i < kTv2Stages - 1; ++i) issue(i, i);
     }
     int rd = 0, wr = kTv2Stages - 1;
+#pragma unroll kUnroll
     for (int i = 0; i < nmine; ++i) {
         cp_wait<kTv2Stages - 2>();
         const uint4* slot = ring + static_cast<size_t>(rd) * 2 * kTv2Threads + tid;
@@ -437,7 +441,7 @@ loss_three_pass(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, in
         }
         // 1: (max, sum) of d and t, from HBM
         float md = -INFINITY, sd = 0.f, mt = -INFINITY, st = 0.f;
-        tv2_pass(gd, gt, nmine, ring, keep, keep, [&](const uint4 vd, const uint4 vt, int) {
+        tv2_pass<true, kLossUnroll>(gd, gt, nmine, ring, keep, keep, [&](const uint4 vd, const uint4 vt, int) {
             group_lse<kBF16>(vd, md, sd);
             group_lse<kBF16>(vt, mt, st);
         });
@@ -461,7 +465,7 @@ loss_three_pass(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, in
         float plt0 = 0.f, plt1 = 0.f;
         bool tie = false;                                 // some d_v - t_v == L_d - L_t in this thread's groups
         const bool bits = nbits > 0 && la.grad != nullptr;   // pass 3 takes the signs from sbits
-        tv2_pass(gd, gt, mass ? nmine : 0, ring, keep, bits ? drop : keep, [&](const uint4 vd, const uint4 vt, int g) {
+        tv2_pass<true, kLossUnroll>(gd, gt, mass ? nmine : 0, ring, keep, bits ? drop : keep, [&](const uint4 vd, const uint4 vt, int g) {
             float a[EPG], b[EPG];
             unpack<kBF16>(vd, a);
             unpack<kBF16>(vt, b);
@@ -506,7 +510,7 @@ loss_three_pass(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, in
             // three-way definition.
             cp_wait<0>();                                 // the primed loads have landed: the ring is free
             float plt = 0.f, peq = 0.f;
-            tv2_pass(gd, gt, nmine, ring, keep, keep, [&](const uint4 vd, const uint4 vt, int) {
+            tv2_pass<true, kLossUnroll>(gd, gt, nmine, ring, keep, keep, [&](const uint4 vd, const uint4 vt, int) {
                 float a[EPG], b[EPG];
                 unpack<kBF16>(vd, a);
                 unpack<kBF16>(vt, b);
@@ -544,7 +548,7 @@ loss_three_pass(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, in
             // kept by pass 2): two, read from sbits, d alone streamed
             auto grad_pass = [&](auto mode) {
                 constexpr int kMode = decltype(mode)::value;
-                tv2_pass<kMode != 2>(gd, gt, mass ? nmine : 0, ring, drop, drop, [&](const uint4 vd, const uint4 vt, int g) {
+                tv2_pass<kMode != 2, kLossUnroll>(gd, gt, mass ? nmine : 0, ring, drop, drop, [&](const uint4 vd, const uint4 vt, int g) {
                     float a[EPG], b[EPG], gv[EPG];
                     unpack<kBF16>(vd, a);
                     uint32_t m = 0;
