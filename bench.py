@@ -436,10 +436,11 @@ def run_gpu(args):
                                    torch.cuda.get_device_properties(dev).multi_processor_count)
 
     # end to end: every step's per-call inputs (U, h, x0, the SPS table and the target
-    # logits t) are in pinned host memory and go to the C-ABI calls as host buffers: the
-    # kernels read them over the host link inside the timed region, each byte they need
-    # once (t only in its scheduled rows; the weights W1, W2, w stay resident on the
-    # device).  Each step's results (x, n_accept, next_token) are copied back to pinned
+    # logits t) are in pinned host memory and go to the C-ABI calls as host buffers, all
+    # inside the timed region: the draft call copies U and h to the device in one
+    # copy-engine transfer each, and the kernels read the rest over the host link, each
+    # byte they need once (t only in its scheduled rows; the weights W1, W2, w stay
+    # resident on the device).  Each step's results (x, n_accept, next_token) are copied back to pinned
     # host memory.  Two host input sets alternate between steps; every step streams more
     # than 5 GB, so nothing of a step's inputs is still in L2 for the next.
     e2e = None
@@ -473,7 +474,9 @@ def run_gpu(args):
         assert sv.status_ok()
         e2e = {"value": e_rows / (e_ms * 1e-3), "unit": "rows/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-               "inputs": "pinned host buffers passed to the C-ABI calls; the kernels read them over the host link",
+               "inputs": "pinned host buffers passed to the C-ABI calls; the draft call copies U and h to the device"
+                         " (one copy-engine transfer each), the kernels read x0, the SPS table and t's scheduled rows"
+                         " over the host link",
                "l2": "no flush: every step reads more than 5 GB of host inputs"}
         del host_sets
     parity = None if args.no_cpu_baseline or world > 1 else parity_sample(sv, args.parity_requests)

@@ -115,7 +115,13 @@ dspark_status_t dspark_set_l2_residency(size_t bytes);
  *   Outputs [B][gamma]: x (int32 tokens), lse_d = logsumexp(z_k / T),
  *   logp_d = z_k[x_k] / T - lse_d, c, a (float32).
  *   U, h and x0 may also point to pinned (page-locked, registered) host
- *   memory: the kernels then read them over the host link, each byte once.
+ *   memory.  U and h are then copied to the device first, each in one
+ *   copy-engine transfer on `stream` (the host link's full rate), into memory
+ *   from a pool private to the library; the pool keeps what it allocated (up
+ *   to the largest B * gamma * (V + H) elements staged) until the process
+ *   exits.  While `stream` is being captured into a graph, or if that memory
+ *   cannot be had, the kernels read U and h over the host link instead, each
+ *   byte once; they always read x0 that way.
  *   Unregistered host memory returns DSPARK_ERR_INVALID_ARGUMENT.
  * Requires 1 <= B <= 65535, 1 <= gamma <= DSPARK_MAX_GAMMA, r % 8 == 0 and
  * r <= 256.  bf16 inputs with r % 64 == 0 run the bias on tensor cores.
@@ -147,6 +153,8 @@ dspark_status_t dspark_draft_block(int B, int gamma, int V, int H, int r, dspark
  *   - All calls share the one array: calls that overlap on the GPU (other
  *     streams, other host threads) race and corrupt each other's results.
  *     Each call clears what must start at zero.
+ *   - U, h and x0 in pinned host memory are read by the kernels over the host
+ *     link (no staging copy to the device, which would allocate).
  *   - The first call on a device looks up the array's device address with
  *     cudaGetSymbolAddress (with that device current); make that first call
  *     before any stream capture.

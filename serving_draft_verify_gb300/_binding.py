@@ -359,12 +359,12 @@ def dspark_draft_block_noalloc(U, h, W1, W2, w, bias, x0, temperature, seed, out
     B, G, V = U.shape
     H = h.shape[-1]
     r = W1.shape[-1]
-    _need(U, (B, G, V), name="U")
-    _need(h, (B, G, H), U.dtype, name="h")
+    _need(U, (B, G, V), name="U", host_ok=True)
+    _need(h, (B, G, H), U.dtype, name="h", host_ok=True)
     _need(W1, (V, r), U.dtype, name="W1")
     _need(W2, (V, r), U.dtype, name="W2")
     _need(w, (H + r,), U.dtype, name="w")
-    _need(x0, (B,), torch.int32, name="x0")
+    _need(x0, (B,), torch.int32, name="x0", host_ok=True)
     _need(out["x"], (B, G), torch.int32, name="x")
     for k in ("lse_d", "logp_d", "c", "a"):
         _need(out[k], (B, G), torch.float32, name=k)

@@ -71,6 +71,62 @@ extern "C" dspark_status_t dspark_workspace_status(const void* workspace, dspark
 }
 
 namespace dspark {
+namespace {
+std::mutex g_stage_mu;
+cudaMemPool_t g_stage_pool[64] = {};
+
+// The library's own pool on device `dev` (created on first use), which keeps its
+// memory between calls rather than returning it at every synchronisation.
+cudaMemPool_t stage_pool(int dev) {
+    if (dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_stage_mu);
+    if (g_stage_pool[dev] != nullptr) return g_stage_pool[dev];
+    cudaMemPoolProps pp{};
+    pp.allocType = cudaMemAllocationTypePinned;
+    pp.location.type = cudaMemLocationTypeDevice;
+    pp.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &pp) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    uint64_t keep = ~static_cast<uint64_t>(0);
+    if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+        cudaGetLastError();
+        cudaMemPoolDestroy(pool);
+        return nullptr;
+    }
+    g_stage_pool[dev] = pool;
+    return pool;
+}
+}  // namespace
+
+void* stage_to_device(const void* host, size_t bytes, cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (cs != cudaStreamCaptureStatusNone || bytes == 0) return nullptr;
+    cudaMemPool_t pool = stage_pool(current_device());
+    if (pool == nullptr) return nullptr;
+    void* d = nullptr;
+    if (cudaMallocFromPoolAsync(&d, bytes, pool, s) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (cudaMemcpyAsync(d, host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFreeAsync(d, s);
+        return nullptr;
+    }
+    return d;
+}
+
+void stage_release(void* p, cudaStream_t s) {
+    if (p != nullptr) cudaFreeAsync(p, s);
+}
+
 std::atomic<size_t> g_l2_resident_bytes{0};
 std::atomic<size_t> g_l2_window_max{0};
 namespace {

@@ -617,12 +617,11 @@ extern "C" size_t dspark_draft_block_workspace_size(int B, int gamma, int V, int
     return draft_ws_layout(B, gamma, &ob, &ow, &op, &oy);
 }
 
-extern "C" dspark_status_t dspark_draft_block(int B, int gamma, int V, int H, int r, dspark_dtype_t dt,
-                                              const void* U, const void* h, const void* W1, const void* W2,
-                                              const void* w, float bias, const int32_t* x0, float temperature,
-                                              uint64_t seed, int32_t* x, float* lse_d, float* logp_d, float* c,
-                                              float* a, void* workspace, size_t workspace_bytes,
-                                              dspark_stream_t stream) {
+dspark_status_t dspark::draft_block_entry(int B, int gamma, int V, int H, int r, dspark_dtype_t dt, const void* U,
+                                          const void* h, const void* W1, const void* W2, const void* w, float bias,
+                                          const int32_t* x0, float temperature, uint64_t seed, int32_t* x,
+                                          float* lse_d, float* logp_d, float* c, float* a, void* workspace,
+                                          size_t workspace_bytes, dspark_stream_t stream, bool stage) {
     if (B <= 0 || B > 65535 || gamma <= 0 || gamma > DSPARK_MAX_GAMMA || V <= 0 || H < 0 || r <= 0 || r > 256)
         return DSPARK_ERR_INVALID_ARGUMENT;
     if (dt != DSPARK_F32 && dt != DSPARK_BF16) return DSPARK_ERR_INVALID_ARGUMENT;
@@ -634,16 +633,39 @@ extern "C" dspark_status_t dspark_draft_block(int B, int gamma, int V, int H, in
     if (workspace == nullptr || !aligned256(workspace)) return DSPARK_ERR_INVALID_ARGUMENT;
     if (workspace_bytes < dspark_draft_block_workspace_size(B, gamma, V, r)) return DSPARK_ERR_WORKSPACE_TOO_SMALL;
     clear_stale_error();
-    // the per-call inputs U, h and x0 may be in registered host memory: the kernels read
-    // them through the mapping's device address, each byte once, over the host link
+    // the per-call inputs U, h and x0 may be in registered host memory.  U and h are
+    // copied to the device first, each in one copy-engine transfer (the host link's
+    // full rate); where that is not possible (stream capture) and for x0, the kernels
+    // read them through the mapping's device address, each byte once, over the link
+    const void* U_in = U;
+    const void* h_in = h;
     if (!device_view(U, &U) || (H > 0 && !device_view(h, &h))) return DSPARK_ERR_INVALID_ARGUMENT;
     {
         const void* v = x0;
         if (!device_view(v, &v)) return DSPARK_ERR_INVALID_ARGUMENT;
         x0 = static_cast<const int32_t*>(v);
     }
-    return draft_block_impl(B, gamma, V, H, r, dt, U, h, W1, W2, w, bias, x0, temperature, seed, x, lse_d, logp_d,
-                            c, a, workspace, reinterpret_cast<cudaStream_t>(stream), nullptr);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t esz = dt == DSPARK_BF16 ? 2 : 4;
+    void* sU = stage && in_host_memory(U_in)
+                   ? stage_to_device(U_in, static_cast<size_t>(B) * gamma * V * esz, s) : nullptr;
+    void* sh = stage && H > 0 && in_host_memory(h_in)
+                   ? stage_to_device(h_in, static_cast<size_t>(B) * gamma * H * esz, s) : nullptr;
+    const dspark_status_t st = draft_block_impl(B, gamma, V, H, r, dt, sU ? sU : U, sh ? sh : h, W1, W2, w, bias,
+                                                x0, temperature, seed, x, lse_d, logp_d, c, a, workspace, s, nullptr);
+    stage_release(sU, s);
+    stage_release(sh, s);
+    return st;
+}
+
+extern "C" dspark_status_t dspark_draft_block(int B, int gamma, int V, int H, int r, dspark_dtype_t dt,
+                                              const void* U, const void* h, const void* W1, const void* W2,
+                                              const void* w, float bias, const int32_t* x0, float temperature,
+                                              uint64_t seed, int32_t* x, float* lse_d, float* logp_d, float* c,
+                                              float* a, void* workspace, size_t workspace_bytes,
+                                              dspark_stream_t stream) {
+    return draft_block_entry(B, gamma, V, H, r, dt, U, h, W1, W2, w, bias, x0, temperature, seed, x, lse_d, logp_d,
+                             c, a, workspace, workspace_bytes, stream, /*stage=*/true);
 }
 
 // Workspace of dspark_draft_block_ex: dspark_draft_block's, then (gated, RNN) the

@@ -57,7 +57,9 @@ extern "C" dspark_status_t dspark_draft_block_noalloc(int B, int gamma, int V, i
     if (dev >= kMaxDevices) return DSPARK_ERR_UNSUPPORTED;
     void* scratch = scratch_address(dev);
     if (scratch == nullptr) return DSPARK_ERR_CUDA;
-    // dspark_draft_block clears the status block and the per-position words itself
-    return dspark_draft_block(B, gamma, V, H, r, dt, U, h, W1, W2, w, bias, x0, temperature, seed, x, lse_d, logp_d,
-                              c, a, scratch, kNoAllocScratchBytes, stream);
+    // dspark_draft_block's path clears the status block and the per-position words
+    // itself; inputs in host memory are read over the link (no staging copy, which
+    // would allocate)
+    return dspark::draft_block_entry(B, gamma, V, H, r, dt, U, h, W1, W2, w, bias, x0, temperature, seed, x, lse_d,
+                                     logp_d, c, a, scratch, kNoAllocScratchBytes, stream, /*stage=*/false);
 }

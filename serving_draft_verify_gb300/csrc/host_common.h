@@ -103,6 +103,27 @@ inline bool in_host_memory(const void* p) {
     return pa.type == cudaMemoryTypeHost;
 }
 
+// Device memory holding a copy of `bytes` of page-locked host memory at `host`,
+// written by one copy-engine transfer on `s` (the host link's full rate; a
+// kernel's own scattered reads of a mapping reach less).  The memory comes,
+// stream-ordered, from a pool private to the library that keeps what it has
+// allocated between calls, until the process exits.  nullptr where that is not
+// possible -- `s` is being captured into a graph, or the allocation fails --
+// and the caller's kernels then read the mapping themselves.
+void* stage_to_device(const void* host, size_t bytes, cudaStream_t s);
+// Returns a stage_to_device buffer to the pool once the work queued on `s` so far
+// is done.
+void stage_release(void* p, cudaStream_t s);
+
+// dspark_draft_block with `stage` choosing whether U and h in host memory are first
+// copied to the device (stage_to_device) or read over the link by the kernels; the
+// no-allocation entry point passes false.
+dspark_status_t draft_block_entry(int B, int gamma, int V, int H, int r, dspark_dtype_t dt, const void* U,
+                                  const void* h, const void* W1, const void* W2, const void* w, float bias,
+                                  const int32_t* x0, float temperature, uint64_t seed, int32_t* x, float* lse_d,
+                                  float* logp_d, float* c, float* a, void* workspace, size_t workspace_bytes,
+                                  dspark_stream_t stream, bool stage);
+
 // Once-per-device flag for one-time kernel attribute setup.
 struct OncePerDevice {
     std::mutex mu;

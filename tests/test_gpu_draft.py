@@ -151,8 +151,10 @@ def test_draft_one_launch_equals_per_position(dsv, key, changes, temperature):
 @pytest.mark.parametrize("B", [40, 5])                   # the tcgen05 engine; the small-batch path
 @pytest.mark.parametrize("temperature", [None, 0.0])
 def test_draft_reads_inputs_from_pinned_host_memory(dsv, temperature, B):
-    """U, h and x0 in pinned host memory (read by the kernels over the host link): the
-    same outputs, bit for bit, as from device memory."""
+    """U, h and x0 in pinned host memory: the same outputs, bit for bit, as from device
+    memory -- with U and h copied to the device by the call (dspark_draft_block), and
+    with every input read by the kernels over the host link (the no-allocation entry
+    point, which does not stage)."""
     cfg = wl.scaled(wl.QWEN3_8B, B=B, V=8192, H=64)
     inp = wl.make_draft_inputs(cfg)
     T = cfg.temperature if temperature is None else temperature
@@ -160,9 +162,13 @@ def test_draft_reads_inputs_from_pinned_host_memory(dsv, temperature, B):
     a = dsv.dspark_draft_block(g["U"], g["h"], g["W1"], g["W2"], g["w"], 0.0, g["x0"], T, cfg.seed)
     host = {k: inp[k].clone().pin_memory() for k in ("U", "h", "x0")}
     b = dsv.dspark_draft_block(host["U"], host["h"], g["W1"], g["W2"], g["w"], 0.0, host["x0"], T, cfg.seed)
+    out = {k: torch.empty_like(a[k]) for k in ("x", "lse_d", "logp_d", "c", "a")}
+    c = dsv._binding.dspark_draft_block_noalloc(host["U"], host["h"], g["W1"], g["W2"], g["w"], 0.0, host["x0"], T,
+                                               cfg.seed, out=out)
     torch.cuda.synchronize()
     for k in a:
         assert torch.equal(a[k], b[k]), k
+        assert torch.equal(a[k], c[k]), k
 
 
 def test_l2_residency_changes_no_result(dsv):
