@@ -115,12 +115,14 @@ def issue_roof(logits, launch_us, sm_mhz, n_sm):
             "source": "ncu instruction count of the same kernel on B = 1024, gamma = 2"}
 
 
-def apply_l2_residency(dsv, args):
-    """--l2-residency: the library keeps W2 (V x r bf16 of the Markov head, the same shape
-    in every serving config here) in L2 for the draft and verify calls; returns the bytes
-    set aside, 0 when off."""
+def apply_l2_residency(dsv, args, default=False):
+    """--l2-residency on|off|auto: the library keeps W2 (V x r bf16 of the Markov head, the
+    same shape in every serving config here) in L2 for the draft and verify calls; `auto`
+    takes `default` (on for the headline run, off for the one-kernel modes).  Returns the
+    bytes set aside, 0 when off."""
     from serving_draft_verify_gb300 import workloads as wl
-    if not getattr(args, "l2_residency", False):
+    mode = getattr(args, "l2_residency", "auto")
+    if not (mode == "on" or (mode == "auto" and default)):
         return 0
     nbytes = wl.HIGH_CONC.V * wl.HIGH_CONC.r * 2
     dsv.dspark_set_l2_residency(nbytes)
@@ -271,7 +273,7 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     dsv.load()
-    l2_keep = apply_l2_residency(dsv, args)
+    l2_keep = apply_l2_residency(dsv, args, default=True)
     lib = dsv._binding.load()
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -502,7 +504,7 @@ def run_gpu(args):
             torch.cuda.empty_cache()
 
     # accept-rate TV on the training workload (16384 x 151936 bf16 rows): its second pass
-    # needs the whole L2, so W2's persisting lines (--l2-residency) are released first
+    # needs the whole L2, so W2's persisting lines (the residency) are released first
     tv = None
     if not args.skip_tv:
         if l2_keep:
@@ -535,7 +537,7 @@ def run_gpu(args):
     # the draft block with the gated and recurrent heads (one launch per position plus a
     # head kernel between positions), on the Qwen3-8B-shaped workload
     if l2_keep and not args.skip_tv:
-        apply_l2_residency(dsv, args)                     # back on for the draft extras below
+        apply_l2_residency(dsv, args, default=True)     # back on for the draft extras below
     heads_x = None
     if not args.skip_heads:
         heads_x = {}
@@ -846,9 +848,10 @@ def main():
     ap.add_argument("--draft-temperature", type=float, default=None, help="temperature of --draft-case")
     ap.add_argument("--draft-path", default="auto", choices=sorted(DRAFT_PATHS),
                     help="draft path of --draft-case: by batch size, the tcgen05 engine, or the CUDA-core GEMV")
-    ap.add_argument("--l2-residency", action="store_true",
+    ap.add_argument("--l2-residency", nargs="?", const="on", default="auto", choices=["auto", "on", "off"],
                     help="keep W2 in L2 with the library's opt-in persisting window (dspark_set_l2_residency) for "
-                         "the draft and verify calls; off by default")
+                         "the draft and verify calls: on for the headline run and off for --draft-case and "
+                         "--round-case unless given (the flag alone means on)")
     ap.add_argument("--round-case", default=None,
                     help="B:gamma -- time only the round's three calls on that high-concurrency-shaped case")
     ap.add_argument("--tv-rows", type=int, default=None,
