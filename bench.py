@@ -824,7 +824,7 @@ def run_draft_only(args):
                       "gbs": nb / (m * 1e-3) / 1e9, "logits_per_ms": B * G * cfg.V / m}))
 
 
-def main():
+def arg_parser():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
@@ -856,7 +856,11 @@ def main():
                     help="B:gamma -- time only the round's three calls on that high-concurrency-shaped case")
     ap.add_argument("--tv-rows", type=int, default=None,
                     help="time only the TV and training-loss kernels on this many training rows")
-    args = ap.parse_args()
+    return ap
+
+
+def main():
+    args = arg_parser().parse_args()
     if args.warmup < 3 and args.impl == "native":
         args.warmup = 3
     if args.tv_rows is not None:
