@@ -465,7 +465,8 @@ loss_three_pass(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, in
         float plt0 = 0.f, plt1 = 0.f;
         bool tie = false;                                 // some d_v - t_v == L_d - L_t in this thread's groups
         const bool bits = nbits > 0 && la.grad != nullptr;   // pass 3 takes the signs from sbits
-        tv2_pass<true, kLossUnroll>(gd, gt, mass ? nmine : 0, ring, keep, bits ? drop : keep, [&](const uint4 vd, const uint4 vt, int g) {
+        const uint64_t tpol = bits ? drop : keep;
+        tv2_pass<true, kLossUnroll>(gd, gt, mass ? nmine : 0, ring, keep, tpol, [&](const uint4 vd, const uint4 vt, int g) {
             float a[EPG], b[EPG];
             unpack<kBF16>(vd, a);
             unpack<kBF16>(vt, b);
@@ -548,7 +549,8 @@ loss_three_pass(const uint8_t* __restrict__ d, const uint8_t* __restrict__ t, in
             // kept by pass 2): two, read from sbits, d alone streamed
             auto grad_pass = [&](auto mode) {
                 constexpr int kMode = decltype(mode)::value;
-                tv2_pass<kMode != 2, kLossUnroll>(gd, gt, mass ? nmine : 0, ring, drop, drop, [&](const uint4 vd, const uint4 vt, int g) {
+                const int n3 = mass ? nmine : 0;
+                tv2_pass<kMode != 2, kLossUnroll>(gd, gt, n3, ring, drop, drop, [&](const uint4 vd, const uint4 vt, int g) {
                     float a[EPG], b[EPG], gv[EPG];
                     unpack<kBF16>(vd, a);
                     uint32_t m = 0;
