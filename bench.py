@@ -472,10 +472,13 @@ def run_gpu(args):
 
         e2e_steps = max(3, min(args.steps, args.e2e_steps))
         e2e_run(min(args.warmup, 3))
+        staged0 = dsv._binding.staged_bytes()
         e_ms, e_rows = aggregate(e2e_run(e2e_steps), B * G * e2e_steps, world, dev)
+        staged = (dsv._binding.staged_bytes() - staged0) // e2e_steps
         assert sv.status_ok()
         e2e = {"value": e_rows / (e_ms * 1e-3), "unit": "rows/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "staged_bytes_per_step": staged,
                "inputs": "pinned host buffers passed to the C-ABI calls; the draft call copies U and h to the device"
                          " (one copy-engine transfer each), the kernels read x0, the SPS table and t's scheduled rows"
                          " over the host link",

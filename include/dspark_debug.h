@@ -79,6 +79,12 @@ dspark_status_t dspark_debug_exp_draws(const uint32_t* words, float* E, int64_t 
 dspark_status_t dspark_debug_philox_rows(uint64_t seed, uint32_t k, uint32_t b, uint32_t stream, uint32_t q0,
                                          int64_t n, uint32_t* out, dspark_stream_t stream_);
 
+/* Measurement hook: the bytes of host inputs the library has copied to the
+ * device with a copy-engine transfer so far in this process (dspark_draft_block
+ * stages U and h in pinned host memory that way, outside stream capture);
+ * inputs the kernels read over the host link are not counted. */
+uint64_t dspark_debug_staged_bytes(void);
+
 #ifdef __cplusplus
 }
 #endif

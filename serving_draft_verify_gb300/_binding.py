@@ -56,6 +56,7 @@ _SIGNATURES = {
     "dspark_debug_phase_times": (_c_int, [_p, _c_int]),
     "dspark_debug_force_phase_launches": (_c_int, [_c_int]),
     "dspark_debug_set_draft_path": (_c_int, [_c_int]),
+    "dspark_debug_staged_bytes": (ctypes.c_uint64, []),
     "dspark_debug_bounded_wait": (_c_int, [_p, _c_size, ctypes.c_uint64, _p]),
     "dspark_debug_exp_draws": (_c_int, [_p, _p, _c_i64, _p]),
     "dspark_debug_philox_rows": (_c_int, [_c_u64, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
@@ -447,6 +448,12 @@ def dspark_debug_draft_logits(U_k, W1, W2, prev, z=None, workspace=None, stream=
 def phase_timing(enable):
     """Measurement hook: record CUDA events around every draft phase launch."""
     _check("dspark_debug_enable_phase_timing", load().dspark_debug_enable_phase_timing(1 if enable else 0))
+
+
+def staged_bytes():
+    """Measurement hook: bytes of host inputs the library has staged to the device by
+    copy engine so far in this process."""
+    return int(load().dspark_debug_staged_bytes())
 
 
 def force_phase_launches(enable):

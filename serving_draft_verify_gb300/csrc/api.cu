@@ -101,6 +101,8 @@ cudaMemPool_t stage_pool(int dev) {
 }
 }  // namespace
 
+std::atomic<uint64_t> g_staged_bytes{0};
+
 void* stage_to_device(const void* host, size_t bytes, cudaStream_t s) {
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
@@ -120,6 +122,7 @@ void* stage_to_device(const void* host, size_t bytes, cudaStream_t s) {
         cudaFreeAsync(d, s);
         return nullptr;
     }
+    g_staged_bytes.fetch_add(bytes);
     return d;
 }
 
@@ -180,3 +183,5 @@ extern "C" dspark_status_t dspark_set_l2_residency(size_t bytes) {
     g_l2_resident_bytes.store(keep);
     return DSPARK_OK;
 }
+
+extern "C" uint64_t dspark_debug_staged_bytes(void) { return dspark::g_staged_bytes.load(); }

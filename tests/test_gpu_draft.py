@@ -161,11 +161,16 @@ def test_draft_reads_inputs_from_pinned_host_memory(dsv, temperature, B):
     g = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
     a = dsv.dspark_draft_block(g["U"], g["h"], g["W1"], g["W2"], g["w"], 0.0, g["x0"], T, cfg.seed)
     host = {k: inp[k].clone().pin_memory() for k in ("U", "h", "x0")}
+    staged0 = dsv._binding.staged_bytes()
     b = dsv.dspark_draft_block(host["U"], host["h"], g["W1"], g["W2"], g["w"], 0.0, host["x0"], T, cfg.seed)
+    staged1 = dsv._binding.staged_bytes()
     out = {k: torch.empty_like(a[k]) for k in ("x", "lse_d", "logp_d", "c", "a")}
     c = dsv._binding.dspark_draft_block_noalloc(host["U"], host["h"], g["W1"], g["W2"], g["w"], 0.0, host["x0"], T,
                                                cfg.seed, out=out)
     torch.cuda.synchronize()
+    # U and h went by copy engine in the first call, nothing in the no-allocation one
+    assert staged1 - staged0 == (host["U"].numel() + host["h"].numel()) * 2
+    assert dsv._binding.staged_bytes() == staged1
     for k in a:
         assert torch.equal(a[k], b[k]), k
         assert torch.equal(a[k], c[k]), k
